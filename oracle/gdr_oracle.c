@@ -1,0 +1,163 @@
+/*
+ * fp64 CPU oracle for the linear-attention memory S_t (d_v x d_k) under the
+ * gated delta rule and its special cases.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file defines what the GPU library must
+ * compute; it is never part of the product path.  Only tests/, the smoke
+ * check in __graft_entry__.py and the cpu_baseline leg of bench.py may load
+ * it.  It shares no code, header or constant with the CUDA library.
+ *
+ * What it computes (the plain sequential definition, one token at a time):
+ *
+ *   mode 0  LINEAR       S_t = S_{t-1} + v_t k_t^T
+ *           "Scrivere meglio nella memoria: gate e delta rule", opening
+ *           equation (linear-attention accumulation) and the summary table.
+ *   mode 1  DECAY        S_t = alpha_t S_{t-1} + v_t k_t^T
+ *           same page, section "Dimenticare: i gate", scalar-decay equation
+ *           (RetNet with a fixed gamma, Mamba-2 with a data-dependent alpha).
+ *   mode 2  DELTA        S_t = S_{t-1} + beta_t (v_t - S_{t-1} k_t) k_t^T
+ *           same page, section "Correggere: la delta rule", Widrow-Hoff form.
+ *   mode 3  GATED_DELTA  S_t = S_{t-1} [alpha_t (I - beta_t k_t k_t^T)]
+ *                              + beta_t v_t k_t^T
+ *           same page, section "Unire oblio e correzione: Gated DeltaNet".
+ *
+ * and the read-out o_t = S_t q_t with the state AFTER the update of token t
+ * (opening section of the same page: "o_t = S_t q_t", S_t being the memory
+ * after the first t tokens).
+ *
+ * The GATED_DELTA product S[alpha(I - beta k k^T)] is evaluated as
+ *   alpha S - alpha beta (S k) k^T
+ * i.e. the matrix S (k k^T) is formed as the outer product (S k) k^T, which
+ * is the same matrix by associativity; nothing else is rearranged.
+ *
+ * Layouts (row-major, contiguous, all double):
+ *   q, k   [B][H][T][dk]     v, o  [B][H][T][dv]
+ *   alpha, beta  [B][H][T]   (ignored, and may be NULL, where the mode has
+ *                             no such parameter: LINEAR ignores both, DECAY
+ *                             ignores beta, DELTA ignores alpha)
+ *   S0, ST [B][H][dv][dk]    rows are value channels, columns key channels
+ *                             (o = S q); S0 == NULL means S_0 = 0.
+ *
+ * Every (b, h) pair is an independent sequence; OpenMP runs them in
+ * parallel.  Within a sequence the loop over t is strictly sequential.
+ */
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { OR_LINEAR = 0, OR_DECAY = 1, OR_DELTA = 2, OR_GATED_DELTA = 3 };
+
+/* One sequence: T tokens of the chosen recurrence.  Scratch w has dv slots. */
+static void run_sequence(int mode, int T, int dk, int dv,
+                         const double *q, const double *k, const double *v,
+                         const double *alpha, const double *beta,
+                         double *S, double *o, double *w)
+{
+    for (int t = 0; t < T; ++t) {
+        const double *kt = k + (size_t)t * dk;
+        const double *qt = q + (size_t)t * dk;
+        const double *vt = v + (size_t)t * dv;
+        const double a = (mode == OR_DECAY || mode == OR_GATED_DELTA) ? alpha[t] : 1.0;
+        const double b = (mode == OR_DELTA || mode == OR_GATED_DELTA) ? beta[t] : 1.0;
+
+        /* w = S_{t-1} k_t : what the memory currently returns for k_t */
+        for (int r = 0; r < dv; ++r) {
+            double acc = 0.0;
+            for (int c = 0; c < dk; ++c) acc += S[(size_t)r * dk + c] * kt[c];
+            w[r] = acc;
+        }
+
+        for (int r = 0; r < dv; ++r) {
+            double *row = S + (size_t)r * dk;
+            for (int c = 0; c < dk; ++c) {
+                switch (mode) {
+                case OR_LINEAR:       /* S + v k^T */
+                    row[c] = row[c] + vt[r] * kt[c];
+                    break;
+                case OR_DECAY:        /* alpha S + v k^T */
+                    row[c] = a * row[c] + vt[r] * kt[c];
+                    break;
+                case OR_DELTA:        /* S + beta (v - S k) k^T */
+                    row[c] = row[c] + b * (vt[r] - w[r]) * kt[c];
+                    break;
+                default:              /* alpha S - alpha beta (S k) k^T + beta v k^T */
+                    row[c] = a * row[c] - a * b * w[r] * kt[c] + b * vt[r] * kt[c];
+                    break;
+                }
+            }
+        }
+
+        /* o_t = S_t q_t, with the state that already holds token t */
+        double *ot = o + (size_t)t * dv;
+        for (int r = 0; r < dv; ++r) {
+            double acc = 0.0;
+            for (int c = 0; c < dk; ++c) acc += S[(size_t)r * dk + c] * qt[c];
+            ot[r] = acc;
+        }
+    }
+}
+
+/*
+ * Returns 0 on success, 1 on a bad argument (unknown mode, non-positive
+ * size, NULL where the mode needs a pointer), 2 if scratch allocation fails.
+ * ST may alias S0.
+ */
+int gdr_oracle_recurrent(int mode, int B, int H, int T, int dk, int dv,
+                         const double *q, const double *k, const double *v,
+                         const double *alpha, const double *beta,
+                         const double *S0, double *o, double *ST,
+                         int num_threads)
+{
+    if (mode < OR_LINEAR || mode > OR_GATED_DELTA) return 1;
+    if (B <= 0 || H <= 0 || T < 0 || dk <= 0 || dv <= 0) return 1;
+    if (!q || !k || !v || !o || !ST) return 1;
+    if ((mode == OR_DECAY || mode == OR_GATED_DELTA) && !alpha) return 1;
+    if ((mode == OR_DELTA || mode == OR_GATED_DELTA) && !beta) return 1;
+
+    const int BH = B * H;
+    const size_t sz = (size_t)dv * dk;
+    int failed = 0;
+
+#ifdef _OPENMP
+    if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads) reduction(| : failed)
+#endif
+    for (int bh = 0; bh < BH; ++bh) {
+        double *S = (double *)malloc(sz * sizeof(double));
+        double *w = (double *)malloc((size_t)dv * sizeof(double));
+        if (!S || !w) {
+            free(S);
+            free(w);
+            failed |= 1;
+            continue;
+        }
+        if (S0) memcpy(S, S0 + (size_t)bh * sz, sz * sizeof(double));
+        else memset(S, 0, sz * sizeof(double));
+
+        run_sequence(mode, T, dk, dv,
+                     q + (size_t)bh * T * dk, k + (size_t)bh * T * dk,
+                     v + (size_t)bh * T * dv,
+                     alpha ? alpha + (size_t)bh * T : NULL,
+                     beta ? beta + (size_t)bh * T : NULL,
+                     S, o + (size_t)bh * T * dv, w);
+
+        memcpy(ST + (size_t)bh * sz, S, sz * sizeof(double));
+        free(S);
+        free(w);
+    }
+    (void)num_threads;
+    return failed ? 2 : 0;
+}
+
+/* Number of threads an OpenMP region would use (1 without OpenMP). */
+int gdr_oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
