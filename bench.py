@@ -1,0 +1,440 @@
+"""Benchmark of the gated delta rule forward on GB300.
+
+One step = one chunked prefill of the whole workload through the C ABI
+(lr_fwd_chunked): every row of the hot path (staging, log-decay, masked
+scores, delta couplings, UT/WY pseudo-values, output, state carry).  The
+default workload is the long gated-delta prefill: B=2, H=16, T=16384,
+dk=dv=128, bf16 q/k/v/o, fp32 state, chunk 64.  Its inputs (545 MB) are larger
+than L2, so no flush is needed between steps.  A second measurement, reported
+under "decode", times 1000 consecutive decode steps (lr_step) over 512
+sequences x 32 heads.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
+of the workload (independent sequences, no data exchange): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+DEFAULT_WORKLOAD = "gdn_prefill_bf16"
+DECODE_WORKLOAD = "gdn_decode_bf16"
+METRIC = "chunked fwd tokens/s"
+UNIT = "tokens/s"
+
+
+# --------------------------------------------------------------- work counts
+
+def head_token_bytes(w):
+    """Algorithmic bytes per head-token: q, k, v, o once each, alpha and beta
+    where the mode reads them."""
+    es = 2 if w.dtype == "bf16" else 4
+    b = es * (2 * w.dk + 2 * w.dv)
+    if w.mode in (workloads.DECAY, workloads.GATED_DELTA):
+        b += 4
+    if w.mode in (workloads.DELTA, workloads.GATED_DELTA):
+        b += 4
+    return b
+
+
+def chunk_bytes(w):
+    """Algorithmic bytes of one chunked call: per head-token bytes plus S0 read
+    (when given) and S_T written once."""
+    heads = w.B * w.H
+    state = heads * w.dv * w.dk * 4
+    return heads * w.T * head_token_bytes(w) + state * (2 if w.s0_std > 0 else 1)
+
+
+def chunk_flops(w):
+    """Chunk-form tensor flops (dense C x C tiles counted in full, UT inverse
+    excluded): 2C(3dk+2dv)+6dk*dv per head-token with delta,
+    2C(dk+dv)+4dk*dv without."""
+    C = w.chunk
+    if w.mode in (workloads.DELTA, workloads.GATED_DELTA):
+        per = 2 * C * (3 * w.dk + 2 * w.dv) + 6 * w.dk * w.dv
+    else:
+        per = 2 * C * (w.dk + w.dv) + 4 * w.dk * w.dv
+    return w.B * w.H * w.T * per
+
+
+def decode_step_bytes(w):
+    """State read + written once, plus q, k, v, o and alpha, beta."""
+    nh = w.B * w.H
+    es = 2 if w.dtype == "bf16" else 4
+    return nh * (2 * w.dv * w.dk * 4 + es * (2 * w.dk + 2 * w.dv) + 8)
+
+
+# ------------------------------------------------------------------- helpers
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples, kept for a [t0, t1] wall window."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(f"/tmp/lr_clocks_{os.getpid()}.csv", "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.out.name) as f:
+            for r in csv.reader(io.StringIO(f.read())):
+                if len(r) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(r[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    frac = float("0." + r[0].strip().split(".")[1]) if "." in r[0] else 0.0
+                    rows.append((ts + frac, [x.strip() for x in r]))
+                except ValueError:
+                    continue
+        os.unlink(self.out.name)
+        inside = [x for t, x in rows if t0 - 0.15 <= t <= t1 + 0.15] or [x for _, x in rows]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(x[2]) for x in inside if x[2].replace(".", "").isdigit()]
+        mx = [float(x[3]) for x in inside if x[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for x in inside for i in range(4) if x[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside),
+                "power_w_max": max((float(x[4]) for x in inside
+                                    if x[4].replace(".", "").isdigit()), default=None)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist, rank, ws, local
+    return None, 0, 1, 0
+
+
+def barrier(dist, device):
+    if dist is not None:
+        dist.barrier(device_ids=[device.index] if device.type == "cuda" else None)
+
+
+def max_over_ranks(dist, x, device):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ oracle timing
+
+def time_oracle(w, budget_s=15.0, max_heads=None):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload:
+    whole sequences of the first n heads, n sized for about ``budget_s`` of
+    CPU work.  Returns (tokens/s scaled to the workload, info)."""
+    import oracle
+    x = workloads.draw(w.gen, 1, w.H, w.T, w.dk, w.dv, w.seed, w.torch_dtype, w.s0_std)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+    def run(nh, threads):
+        sl = lambda t: None if t is None else t[:, :nh].contiguous()
+        t0 = time.perf_counter()
+        oracle.recurrent(w.mode, sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["alpha"]), sl(x["beta"]),
+                         sl(x["S0"]), threads=threads)
+        return time.perf_counter() - t0
+
+    one = run(1, 1)                                    # one head, one thread
+    n = max(1, min(w.H if max_heads is None else max_heads, int(budget_s / max(one, 1e-6))))
+    threads = min(n, cores)
+    wall = run(n, threads)
+    head_tokens_per_s = n * w.T / wall
+    tokens_per_s = head_tokens_per_s / w.H             # a token carries H heads
+    info = {"value": tokens_per_s, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {w.B * w.H} (batch, head) sequences, all T={w.T} tokens each, "
+                      f"fp64 C recurrence; {n * w.T} head-tokens in {wall:.2f} s wall "
+                      f"({one:.2f} s for one sequence on one core)"}
+    return tokens_per_s, info
+
+
+# ------------------------------------------------------------------- arms
+
+def run_ours(args, dist, rank, world, local):
+    import gated_delta_rule_fwd_gb300 as lr
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.WORKLOADS[args.workload]
+    peaks = load_peaks()
+
+    x = workloads.draw_workload(w)
+    xd = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.torch_dtype, device=dev)
+    st = torch.empty((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        lr.lr_fwd_chunked(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], xd["S0"],
+                          mode=w.mode, chunk=w.chunk, o=o, S_T=st, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    barrier(dist, dev)
+    clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(dist, ms, dev)
+    ms_per_step = ms_max / args.steps
+
+    tokens = w.B * w.T * world
+    value = tokens * args.steps / (ms_max / 1e3)
+    kernel_s = ms / args.steps / 1e3                   # one launch per step
+    nbytes, nflops = chunk_bytes(w), chunk_flops(w)
+    achieved_gbs = nbytes / kernel_s / 1e9
+    achieved_tf = nflops / kernel_s / 1e12
+
+    # end to end through the public API: pinned host inputs -> device, call,
+    # outputs -> pinned host, every step
+    hx = {n: (t.pin_memory() if t is not None else None) for n, t in x.items()}
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hs = torch.empty(st.shape, dtype=st.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for n, t in hx.items()
+              if t is not None and not (n == "alpha" and w.mode in (workloads.LINEAR, workloads.DELTA))
+              and not (n == "beta" and w.mode in (workloads.LINEAR, workloads.DECAY)))
+    d2h = ho.numel() * ho.element_size() + hs.numel() * hs.element_size()
+
+    def e2e_step():
+        d = {n: (t.to(dev, non_blocking=True) if t is not None else None) for n, t in hx.items()}
+        oo, ss = lr.lr_fwd_chunked(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["S0"],
+                                   mode=w.mode, chunk=w.chunk, stream=stream)
+        ho.copy_(oo, non_blocking=True)
+        hs.copy_(ss, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
+    e2e_value = tokens * e2e_steps / (e_ms / 1e3)
+    del hx, ho, hs
+
+    decode = None if args.no_decode else run_decode(lr, dev, dist, peaks, args)
+
+    out = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            _, cpu = time_oracle(w, budget_s=args.cpu_budget)
+        out = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic (seeded; shapes and distributions of the workload)",
+            "config": {"workload": w.name, "mode": "gated_delta" if w.mode == 3 else w.mode,
+                       "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
+                       "state": "fp32", "global_batch": w.B * world, "seq_len": w.T,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs 545 MB > 129 MB L2, no flush between steps"},
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
+                         "traffic": args.traffic, "peak_source": peaks["source"] + " burst copy",
+                         "algorithmic_bytes_per_launch": nbytes},
+            "tensor": {"achieved_tflops": achieved_tf, "peak_tflops": peaks["bf16_tflops"],
+                       "frac_of_bf16_peak": achieved_tf / peaks["bf16_tflops"],
+                       "flops_per_launch": nflops, "count": "chunk-form MMA flops"},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": args.steps,
+            "clocks": clocks.summary(wall0, wall1),
+            "cpu_baseline": cpu,
+        }
+        if decode is not None:
+            out["decode"] = decode
+    return out
+
+
+def run_decode(lr, dev, dist, peaks, args):
+    """1000 consecutive decode steps (fresh inputs per step, drawn beforehand
+    on the device), timed as a whole after 10 warm-up steps on a scratch
+    copy of the state."""
+    w = workloads.WORKLOADS[DECODE_WORKLOAD]
+    g = torch.Generator(dev)
+    S = workloads.draw_decode_state(w, dev, g)
+    steps = w.steps
+    inputs = [workloads.draw_decode_step(w, s, dev, g) for s in range(steps)]
+    o = torch.empty((w.B, w.H, w.dv), dtype=w.torch_dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    scratch = S.clone()
+    for s in range(10):
+        i = inputs[s]
+        lr.lr_step(i["q"], i["k"], i["v"], i["alpha"], i["beta"], scratch, mode=w.mode, o=o,
+                   stream=stream)
+    del scratch
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in inputs:
+        lr.lr_step(i["q"], i["k"], i["v"], i["alpha"], i["beta"], S, mode=w.mode, o=o,
+                   stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
+    per = ms / steps / 1e3
+    gbs = decode_step_bytes(w) / per / 1e9
+    return {"workload": w.name, "metric": "decode step state GB/s", "value": gbs, "unit": "GB/s",
+            "frac_hbm": gbs / peaks["hbm_gbs"], "peak_gbs": peaks["hbm_gbs"],
+            "us_per_step": per * 1e6, "steps": steps, "tokens_per_s": w.B / per,
+            "bytes_per_step": decode_step_bytes(w), "gpu_launches": steps,
+            "N": w.B, "H": w.H, "dk": w.dk, "dv": w.dv}
+
+
+def run_reference(args, rank):
+    """The oracle on the host cores, as the reference arm: each step is the
+    fp64 recurrence over a bounded sample of the workload."""
+    if rank != 0:
+        return None
+    w = workloads.WORKLOADS[args.workload]
+    import oracle
+    x = workloads.draw(w.gen, 1, w.H, w.T, w.dk, w.dv, w.seed, w.torch_dtype, w.s0_std)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    nh = min(w.H, cores)
+    T = min(w.T, args.ref_tokens)
+    def sl(name, t):
+        if t is None:
+            return None
+        if name == "S0":
+            return t[:, :nh].contiguous()
+        return t[:, :nh, :T].contiguous()
+
+    xs = {n: sl(n, t) for n, t in x.items()}
+
+    def step():
+        oracle.recurrent(w.mode, xs["q"], xs["k"], xs["v"], xs["alpha"], xs["beta"], xs["S0"],
+                         threads=nh)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = nh * T * args.steps / dt / w.H
+    sample = (f"{nh} of {w.B * w.H} (batch, head) sequences x first {T} of {w.T} tokens per step, "
+              f"fp64 C recurrence, {nh} threads")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; shapes and distributions of the workload)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
+                       "chunk": w.chunk},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nh, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=[k for k in workloads.WORKLOADS if k != DECODE_WORKLOAD])
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of single-core oracle work in the cpu_baseline sample")
+    ap.add_argument("--ref-tokens", type=int, default=2048,
+                    help="tokens per sequence in each reference-arm step")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch from an ncu capture of the current kernel")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+
+    dist, rank, world, local = dist_setup()
+    if args.impl == "reference":
+        out = run_reference(args, rank)
+    else:
+        out = run_ours(args, dist, rank, world, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

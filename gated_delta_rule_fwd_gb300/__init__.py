@@ -1,0 +1,179 @@
+"""Gated delta rule forward on GB300 (sm_103a): Python binding of liblr.
+
+The library's C ABI is declared in ``include/lr.h``; this module only
+marshals arguments (tensor pointers, sizes, the current CUDA stream) into it.
+Every step of the computation runs in the library's CUDA kernels.  PyTorch is
+used for device memory and streams.  There is no fallback: if ``liblr.so`` is
+missing or cannot be loaded, every call raises.
+
+    lr_fwd_chunked(q, k, v, alpha, beta, S0, mode=...) -> (o, S_T)
+        chunkwise prefill over whole sequences (q, k: [B,H,T,dk], v: [B,H,T,dv])
+    lr_step(q, k, v, alpha, beta, S, mode=...) -> o
+        one decode step for N sequences, S: [N,H,dv,dk] updated in place
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+LINEAR, DECAY, DELTA, GATED_DELTA = 0, 1, 2, 3
+MODES = {"linear": LINEAR, "decay": DECAY, "delta": DELTA, "gated_delta": GATED_DELTA}
+F32, BF16 = 0, 1
+SYMBOLS = ("lr_fwd_chunked", "lr_step", "lr_status_string", "lr_abi_version")
+STATUS = {0: "LR_OK", 1: "LR_ERR_NULL", 2: "LR_ERR_SHAPE", 3: "LR_ERR_DTYPE", 4: "LR_ERR_ALIGN",
+          5: "LR_ERR_MODE", 6: "LR_ERR_UNSUPPORTED", 7: "LR_ERR_CUDA", 8: "LR_ERR_ALIAS"}
+_USES_ALPHA = {LINEAR: False, DECAY: True, DELTA: False, GATED_DELTA: True}
+_USES_BETA = {LINEAR: False, DECAY: False, DELTA: True, GATED_DELTA: True}
+
+
+class LrError(RuntimeError):
+    """A non-OK lr_status returned by the library."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded liblr.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built; build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "or `python -m gated_delta_rule_fwd_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, fp, i = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int
+        L.lr_fwd_chunked.restype = i
+        L.lr_fwd_chunked.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp] + [i] * 6 + [i, i, vp]
+        L.lr_step.restype = i
+        L.lr_step.argtypes = [vp, vp, vp, fp, fp, fp, vp] + [i] * 4 + [i, i, vp]
+        L.lr_status_string.restype = ctypes.c_char_p
+        L.lr_status_string.argtypes = [i]
+        L.lr_abi_version.restype = i
+        L.lr_abi_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().lr_status_string(int(status)).decode()
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"q, k, v must be float32 or bfloat16, got {t.dtype}")
+
+
+def _check(t, name, shape, dtype, device):
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def lr_fwd_chunked(q, k, v, alpha=None, beta=None, S0=None, *, mode=GATED_DELTA, chunk=64,
+                   o=None, S_T=None, stream=None):
+    """Chunkwise forward (see ``lr_fwd_chunked`` in include/lr.h).
+
+    q, k: [B,H,T,dk]; v: [B,H,T,dv] (float32 or bfloat16, same dtype);
+    alpha, beta: [B,H,T] float32 where the mode uses them; S0: [B,H,dv,dk]
+    float32 or None.  ``o`` and ``S_T`` may be given to write into (``S_T``
+    may be ``S0``).  Returns (o, S_T).
+    """
+    import torch
+    mode = MODES.get(mode, mode)
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _check(q, "q", (B, H, T, dk), q.dtype, dev)
+    _check(k, "k", (B, H, T, dk), q.dtype, dev)
+    _check(v, "v", (B, H, T, dv), q.dtype, dev)
+    if _USES_ALPHA[mode]:
+        _check(alpha, "alpha", (B, H, T), torch.float32, dev)
+    else:
+        alpha = None
+    if _USES_BETA[mode]:
+        _check(beta, "beta", (B, H, T), torch.float32, dev)
+    else:
+        beta = None
+    if S0 is not None:
+        _check(S0, "S0", (B, H, dv, dk), torch.float32, dev)
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=q.dtype, device=dev)
+    else:
+        _check(o, "o", (B, H, T, dv), q.dtype, dev)
+    if S_T is None:
+        S_T = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+    else:
+        _check(S_T, "S_T", (B, H, dv, dk), torch.float32, dev)
+    st = lib().lr_fwd_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
+                              _ptr(o), _ptr(S_T), B, H, T, dk, dv, int(chunk), dt, int(mode),
+                              _stream_handle(stream, dev))
+    if st != 0:
+        raise LrError(st, "lr_fwd_chunked")
+    return o, S_T
+
+
+def lr_step(q, k, v, alpha, beta, S, *, mode=GATED_DELTA, o=None, stream=None):
+    """One decode step (see ``lr_step`` in include/lr.h); S is updated in place.
+
+    q, k: [N,H,dk]; v: [N,H,dv]; alpha, beta: [N,H] float32 where the mode
+    uses them; S: [N,H,dv,dk] float32.  Returns o: [N,H,dv].
+    """
+    import torch
+    mode = MODES.get(mode, mode)
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _check(q, "q", (N, H, dk), q.dtype, dev)
+    _check(k, "k", (N, H, dk), q.dtype, dev)
+    _check(v, "v", (N, H, dv), q.dtype, dev)
+    if _USES_ALPHA[mode]:
+        _check(alpha, "alpha", (N, H), torch.float32, dev)
+    else:
+        alpha = None
+    if _USES_BETA[mode]:
+        _check(beta, "beta", (N, H), torch.float32, dev)
+    else:
+        beta = None
+    _check(S, "S", (N, H, dv, dk), torch.float32, dev)
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=q.dtype, device=dev)
+    else:
+        _check(o, "o", (N, H, dv), q.dtype, dev)
+    st = lib().lr_step(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S), _ptr(o),
+                       N, H, dk, dv, dt, int(mode), _stream_handle(stream, dev))
+    if st != 0:
+        raise LrError(st, "lr_step")
+    return o

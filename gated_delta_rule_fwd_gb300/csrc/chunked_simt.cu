@@ -1,0 +1,275 @@
+// Chunked forward on CUDA cores, all arithmetic in fp32 (no tensor cores, so
+// fp32 inputs keep fp32 accuracy).
+//
+// The chunkwise form (page "Le architetture lineari: RetNet, RWKV, xLSTM",
+// section "RetNet: la retention e le sue tre forme"): blocks of C = 64 tokens
+// computed together, the end-of-block state carried to the next block.
+// Inside a block, with G_r = sum_{i<=r} ln alpha_i (log-space gate products,
+// which depend on the input alone -- page "Scrivere meglio nella memoria: gate
+// e delta rule", section "Correggere: la delta rule") and g_r = exp(G_r):
+//
+//   delta rows, pseudo-values of the WY representation (same section):
+//     u_r = beta_r (v_r - g_r S k_r - sum_{i<r} e^{G_r - G_i} (k_i.k_r) u_i)
+//     i.e. (I + A) U = diag(beta) (V - diag(g) K S^T),
+//          A_ri = beta_r e^{G_r - G_i} k_i.k_r  (i < r);
+//   other rows: u_r = v_r;
+//   output    O = diag(g) Q S^T + (Q K^T (.) M) U,  M_ri = e^{G_r - G_i}, i <= r;
+//   carry     S <- g_C S + U^T diag(e^{G_C - G_i}) K.
+//
+// Grid: one CTA per (value-channel slice of 32 rows, head, batch); rows of S
+// evolve independently given k, alpha and beta, so slices never exchange
+// data.  The loop over blocks is sequential inside the CTA.  The triangular
+// system is solved by forward substitution, one warp per 4 columns with 8
+// lanes splitting each inner sum.  A final block shorter than C is padded
+// with k = q = v = 0, alpha = 1, beta = 0, which leaves state and outputs of
+// the real tokens unchanged; padded outputs are not stored.
+#include "lr_internal.cuh"
+
+namespace lr {
+namespace {
+
+constexpr int C = 64;     // tokens per block
+constexpr int DVS = 32;   // value channels per CTA
+constexpr int NT = 256;   // threads per CTA
+
+template <int DK>
+struct SimtSmem {
+    static constexpr int KP = DK + 1;       // padded key row (bank-conflict-free column walks)
+    static constexpr int UP = DVS + 1;      // padded pseudo-value row
+    static constexpr int PP = C + 1;        // padded score row
+    static constexpr int kK = 0;
+    static constexpr int kQ = kK + C * KP;
+    static constexpr int kS = kQ + C * KP;
+    static constexpr int kV = kS + DVS * KP;
+    static constexpr int kU = kV + C * DVS;
+    static constexpr int kP = kU + C * UP;
+    static constexpr int kA = kP + C * PP;
+    static constexpr int kG = kA + C * PP;
+    static constexpr int kB = kG + C;
+    static constexpr int kW = kB + C;
+    static constexpr int floats = kW + C;
+    static constexpr int bytes = floats * 4;
+};
+
+template <int DK, typename Tin, bool ALPHA, bool DELTA>
+__global__ void __launch_bounds__(NT)
+chunk_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
+                  const Tin *__restrict__ v, const float *__restrict__ alpha,
+                  const float *__restrict__ beta, const float *__restrict__ S0,
+                  Tin *__restrict__ o, float *__restrict__ ST, int H, int T, int dv) {
+    using L = SimtSmem<DK>;
+    constexpr int KP = L::KP, UP = L::UP, PP = L::PP;
+    extern __shared__ float sm[];
+    float *Ks = sm + L::kK;
+    float *Qs = sm + L::kQ;
+    float *Ss = sm + L::kS;
+    float *Vs = sm + L::kV;
+    float *Us = sm + L::kU;
+    float *Ps = sm + L::kP;
+    float *As = sm + L::kA;
+    float *Gs = sm + L::kG;
+    float *Bs = sm + L::kB;
+    float *Ws = sm + L::kW;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int c0 = blockIdx.x * DVS;
+    const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
+
+    for (int idx = tid; idx < DVS * DK; idx += NT) {
+        const int c = idx / DK, j = idx % DK;
+        Ss[c * KP + j] = S0 ? S0[(bh * dv + c0 + c) * DK + j] : 0.f;
+    }
+
+    for (int t0 = 0; t0 < T; t0 += C) {
+        const int n = min(C, T - t0);
+        __syncthreads();  // the previous block is done with every buffer
+
+        // ---- stage the block (fp32 in shared memory)
+        for (int idx = tid; idx < C * DK; idx += NT) {
+            const int r = idx / DK, j = idx % DK;
+            const bool ok = r < n;
+            const size_t g = (bh * T + t0 + r) * DK + j;
+            Ks[r * KP + j] = ok ? to_f(k[g]) : 0.f;
+            Qs[r * KP + j] = ok ? to_f(q[g]) : 0.f;
+        }
+        for (int idx = tid; idx < C * DVS; idx += NT) {
+            const int r = idx / DVS, c = idx % DVS;
+            Vs[r * DVS + c] = r < n ? to_f(v[(bh * T + t0 + r) * dv + c0 + c]) : 0.f;
+        }
+        if (tid < C) {
+            const bool ok = tid < n;
+            Gs[tid] = (ALPHA && ok) ? logf(alpha[bh * T + t0 + tid]) : 0.f;
+            Bs[tid] = (DELTA && ok) ? beta[bh * T + t0 + tid] : 0.f;
+        }
+        __syncthreads();
+
+        // ---- cumulative log decay: inclusive scan of 64 values by warp 0
+        if (ALPHA && warp == 0) {
+            const float x0 = Gs[2 * lane], x1 = Gs[2 * lane + 1];
+            const float pair = x0 + x1;
+            float incl = pair;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += y;
+            }
+            const float excl = incl - pair;
+            Gs[2 * lane] = excl + x0;
+            Gs[2 * lane + 1] = excl + pair;
+        }
+        __syncthreads();
+        if (tid < C) Ws[tid] = ALPHA ? expf(Gs[C - 1] - Gs[tid]) : 1.f;
+
+        // ---- decay-masked scores P and delta couplings A
+        for (int idx = tid; idx < C * C; idx += NT) {
+            const int r = idx / C, i = idx % C;
+            float p = 0.f, a = 0.f;
+            if (i <= r) {
+                float dq = 0.f, dk = 0.f;
+#pragma unroll 8
+                for (int j = 0; j < DK; ++j) {
+                    const float kij = Ks[i * KP + j];
+                    dq += Qs[r * KP + j] * kij;
+                    if (DELTA) dk += Ks[r * KP + j] * kij;
+                }
+                const float dec = ALPHA ? expf(Gs[r] - Gs[i]) : 1.f;
+                p = dq * dec;
+                if (DELTA && i < r) a = Bs[r] * dk * dec;
+            }
+            Ps[r * PP + i] = p;
+            if (DELTA) As[r * PP + i] = a;
+        }
+
+        // ---- right-hand side of the pseudo-value system (delta rows)
+        if (DELTA) {
+            for (int idx = tid; idx < C * DVS; idx += NT) {
+                const int r = idx / DVS, c = idx % DVS;
+                float sk = 0.f;
+#pragma unroll 8
+                for (int j = 0; j < DK; ++j) sk += Ss[c * KP + j] * Ks[r * KP + j];
+                const float g = ALPHA ? expf(Gs[r]) : 1.f;
+                Us[r * UP + c] = Bs[r] * (Vs[r * DVS + c] - g * sk);
+            }
+        } else {
+            for (int idx = tid; idx < C * DVS; idx += NT) {
+                const int r = idx / DVS, c = idx % DVS;
+                Us[r * UP + c] = Vs[r * DVS + c];
+            }
+        }
+        __syncthreads();
+
+        // ---- forward substitution (I + A) U = rhs, in place in Us
+        if (DELTA) {
+            const int c = warp * 4 + (lane >> 3);
+            const int sub = lane & 7;
+            for (int r = 1; r < C; ++r) {
+                float part = 0.f;
+                for (int i = sub; i < r; i += 8) part += As[r * PP + i] * Us[i * UP + c];
+                part += __shfl_xor_sync(0xffffffffu, part, 1);
+                part += __shfl_xor_sync(0xffffffffu, part, 2);
+                part += __shfl_xor_sync(0xffffffffu, part, 4);
+                if (sub == 0) Us[r * UP + c] -= part;
+                __syncwarp();
+            }
+        }
+        __syncthreads();
+
+        // ---- output O = diag(g) Q S^T + P U  (S still the block's initial state)
+        for (int idx = tid; idx < C * DVS; idx += NT) {
+            const int r = idx / DVS, c = idx % DVS;
+            if (r >= n) continue;
+            float qs = 0.f;
+#pragma unroll 8
+            for (int j = 0; j < DK; ++j) qs += Qs[r * KP + j] * Ss[c * KP + j];
+            float pu = 0.f;
+            for (int i = 0; i <= r; ++i) pu += Ps[r * PP + i] * Us[i * UP + c];
+            const float g = ALPHA ? expf(Gs[r]) : 1.f;
+            o[(bh * T + t0 + r) * dv + c0 + c] = from_f<Tin>(g * qs + pu);
+        }
+        __syncthreads();
+
+        // ---- carry S <- g_C S + U^T diag(e^{G_C - G_i}) K
+        const float gC = ALPHA ? expf(Gs[C - 1]) : 1.f;
+        for (int idx = tid; idx < DVS * DK; idx += NT) {
+            const int c = idx / DK, j = idx % DK;
+            float acc = 0.f;
+#pragma unroll 8
+            for (int i = 0; i < C; ++i) acc += Us[i * UP + c] * Ws[i] * Ks[i * KP + j];
+            Ss[c * KP + j] = gC * Ss[c * KP + j] + acc;
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < DVS * DK; idx += NT) {
+        const int c = idx / DK, j = idx % DK;
+        ST[(bh * dv + c0 + c) * DK + j] = Ss[c * KP + j];
+    }
+}
+
+template <int DK, typename Tin, bool ALPHA, bool DELTA>
+cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *alpha,
+                         const float *beta, const float *S0, void *o, float *S_T, int B, int H,
+                         int T, int dv, cudaStream_t stream, int slot) {
+    auto fn = chunk_simt_kernel<DK, Tin, ALPHA, DELTA>;
+    const int bytes = SimtSmem<DK>::bytes;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(fn), bytes, slot);
+    if (e != cudaSuccess) return e;
+    dim3 grid(dv / DVS, H, B);
+    fn<<<grid, NT, bytes, stream>>>(static_cast<const Tin *>(q), static_cast<const Tin *>(k),
+                                    static_cast<const Tin *>(v), alpha, beta, S0,
+                                    static_cast<Tin *>(o), S_T, H, T, dv);
+    return cudaGetLastError();
+}
+
+template <int DK, typename Tin>
+cudaError_t launch_mode(const void *q, const void *k, const void *v, const float *alpha,
+                        const float *beta, const float *S0, void *o, float *S_T, int B, int H,
+                        int T, int dv, lr_mode mode, cudaStream_t stream, int slot) {
+    switch (mode) {
+    case LR_MODE_LINEAR:
+        return launch_typed<DK, Tin, false, false>(q, k, v, alpha, beta, S0, o, S_T, B, H, T,
+                                                   dv, stream, slot + 0);
+    case LR_MODE_DECAY:
+        return launch_typed<DK, Tin, true, false>(q, k, v, alpha, beta, S0, o, S_T, B, H, T,
+                                                  dv, stream, slot + 1);
+    case LR_MODE_DELTA:
+        return launch_typed<DK, Tin, false, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T,
+                                                  dv, stream, slot + 2);
+    default:
+        return launch_typed<DK, Tin, true, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv,
+                                                 stream, slot + 3);
+    }
+}
+
+template <typename Tin>
+cudaError_t launch_dk(const void *q, const void *k, const void *v, const float *alpha,
+                      const float *beta, const float *S0, void *o, float *S_T, int B, int H,
+                      int T, int dk, int dv, lr_mode mode, cudaStream_t stream, int slot) {
+    switch (dk) {
+    case 32:
+        return launch_mode<32, Tin>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, stream,
+                                    slot + 0);
+    case 64:
+        return launch_mode<64, Tin>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, stream,
+                                    slot + 4);
+    default:
+        return launch_mode<128, Tin>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode,
+                                     stream, slot + 8);
+    }
+}
+
+}  // namespace
+
+// Attribute slots 0..23 belong to this file.
+cudaError_t launch_chunked_simt(const void *q, const void *k, const void *v, const float *alpha,
+                                const float *beta, const float *S0, void *o, float *S_T, int B,
+                                int H, int T, int dk, int dv, lr_dtype dt, lr_mode mode,
+                                cudaStream_t stream) {
+    if (dt == LR_DT_F32)
+        return launch_dk<float>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, mode, stream,
+                                0);
+    return launch_dk<__nv_bfloat16>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, mode,
+                                    stream, 12);
+}
+
+}  // namespace lr

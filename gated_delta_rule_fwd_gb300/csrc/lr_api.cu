@@ -1,0 +1,168 @@
+// Host side of the C ABI declared in include/lr.h: argument validation,
+// dispatch to the kernels, status mapping.  Validation happens before any
+// launch, so an error status means nothing was enqueued.
+#include <atomic>
+
+#include "lr_internal.cuh"
+
+namespace lr {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSlots = 64;
+std::atomic<int> g_smem_bytes[kMaxDevices][kMaxSlots];
+
+bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }
+
+bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Span {
+    uintptr_t lo = 0, hi = 0;  // [lo, hi)
+};
+Span span(const void *p, size_t bytes) {
+    Span s;
+    if (p && bytes) {
+        s.lo = reinterpret_cast<uintptr_t>(p);
+        s.hi = s.lo + bytes;
+    }
+    return s;
+}
+bool overlap(Span a, Span b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
+
+bool uses_alpha(lr_mode m) { return m == LR_MODE_DECAY || m == LR_MODE_GATED_DELTA; }
+bool uses_beta(lr_mode m) { return m == LR_MODE_DELTA || m == LR_MODE_GATED_DELTA; }
+
+// Element counts fit comfortably in 64 bits and in what one device can hold.
+bool count_ok(long long a, long long b, long long c, long long d) {
+    const long long lim = 1ll << 40;
+    long long x = a;
+    for (long long f : {b, c, d}) {
+        if (f <= 0) return f == 0;
+        if (x > lim / f) return false;
+        x *= f;
+    }
+    return true;
+}
+
+__global__ void copy_state_kernel(const float *__restrict__ src, float *__restrict__ dst,
+                                  size_t n) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = src ? src[i] : 0.f;
+}
+
+}  // namespace
+
+cudaError_t ensure_smem_attr(const void *fn, int bytes, int slot) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= kMaxSlots)
+        return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (g_smem_bytes[dev][slot].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) g_smem_bytes[dev][slot].store(bytes, std::memory_order_release);
+    return e;
+}
+
+}  // namespace lr
+
+using namespace lr;
+
+extern "C" {
+
+int lr_abi_version(void) { return 1; }
+
+const char *lr_status_string(lr_status s) {
+    switch (s) {
+    case LR_OK: return "ok";
+    case LR_ERR_NULL: return "a required pointer is NULL";
+    case LR_ERR_SHAPE: return "invalid size (negative, zero where not allowed, or too large)";
+    case LR_ERR_DTYPE: return "unknown element type";
+    case LR_ERR_ALIGN: return "a base pointer is not 16-byte aligned";
+    case LR_ERR_MODE: return "unknown mode";
+    case LR_ERR_UNSUPPORTED: return "unsupported size: dk and dv must be 32, 64 or 128 and chunk 64";
+    case LR_ERR_CUDA: return "CUDA runtime error at launch";
+    case LR_ERR_ALIAS: return "an output overlaps an input";
+    }
+    return "unknown status";
+}
+
+lr_status lr_fwd_chunked(const void *q, const void *k, const void *v, const float *alpha,
+                         const float *beta, const float *S0, void *o, float *S_T, int B, int H,
+                         int T, int dk, int dv, int chunk, lr_dtype dt, lr_mode mode,
+                         cudaStream_t stream) {
+    if (mode < LR_MODE_LINEAR || mode > LR_MODE_GATED_DELTA) return LR_ERR_MODE;
+    if (dt != LR_DT_F32 && dt != LR_DT_BF16) return LR_ERR_DTYPE;
+    if (B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1 || chunk < 1) return LR_ERR_SHAPE;
+    if (!count_ok(B, H, T, dk > dv ? dk : dv) || !count_ok(B, H, dv, dk)) return LR_ERR_SHAPE;
+    if (!supported_dim(dk) || !supported_dim(dv) || chunk != 64) return LR_ERR_UNSUPPORTED;
+    if (!S_T) return LR_ERR_NULL;
+    if (T > 0 && (!q || !k || !v || !o)) return LR_ERR_NULL;
+    if (T > 0 && uses_alpha(mode) && !alpha) return LR_ERR_NULL;
+    if (T > 0 && uses_beta(mode) && !beta) return LR_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) ||
+        !aligned16(beta) || !aligned16(S0) || !aligned16(o) || !aligned16(S_T))
+        return LR_ERR_ALIGN;
+
+    const size_t es = dt == LR_DT_F32 ? 4 : 2;
+    const size_t bht = (size_t)B * H * T;
+    const size_t state_bytes = (size_t)B * H * dv * dk * 4;
+    const Span sq = span(q, bht * dk * es), sk = span(k, bht * dk * es),
+               sv = span(v, bht * dv * es);
+    const Span sa = span(uses_alpha(mode) ? alpha : nullptr, bht * 4);
+    const Span sb = span(uses_beta(mode) ? beta : nullptr, bht * 4);
+    const Span s0 = span(S0, state_bytes), so = span(o, bht * dv * es),
+               st = span(S_T, state_bytes);
+    for (Span in : {sq, sk, sv, sa, sb, s0, st})
+        if (overlap(so, in)) return LR_ERR_ALIAS;
+    for (Span in : {sq, sk, sv, sa, sb})
+        if (overlap(st, in)) return LR_ERR_ALIAS;
+    if (S0 && S0 != S_T && overlap(s0, st)) return LR_ERR_ALIAS;
+
+    cudaError_t e;
+    if (T == 0) {
+        if (S0 == S_T) return LR_OK;
+        const size_t n = (size_t)B * H * dv * dk;
+        copy_state_kernel<<<(unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0,
+                            stream>>>(S0, S_T, n);
+        e = cudaGetLastError();
+    } else {
+        e = launch_chunked_simt(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, dt, mode,
+                                stream);
+    }
+    return e == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+}
+
+lr_status lr_step(const void *q, const void *k, const void *v, const float *alpha,
+                  const float *beta, float *S, void *o, int N, int H, int dk, int dv,
+                  lr_dtype dt, lr_mode mode, cudaStream_t stream) {
+    if (mode < LR_MODE_LINEAR || mode > LR_MODE_GATED_DELTA) return LR_ERR_MODE;
+    if (dt != LR_DT_F32 && dt != LR_DT_BF16) return LR_ERR_DTYPE;
+    if (N < 1 || H < 1 || dk < 1 || dv < 1) return LR_ERR_SHAPE;
+    if (!count_ok(N, H, dv, dk) || (long long)N * H > 0x7fffffffll) return LR_ERR_SHAPE;
+    if (!supported_dim(dk) || !supported_dim(dv)) return LR_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !S || !o) return LR_ERR_NULL;
+    if (uses_alpha(mode) && !alpha) return LR_ERR_NULL;
+    if (uses_beta(mode) && !beta) return LR_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) ||
+        !aligned16(beta) || !aligned16(S) || !aligned16(o))
+        return LR_ERR_ALIGN;
+
+    const size_t es = dt == LR_DT_F32 ? 4 : 2;
+    const size_t nh = (size_t)N * H;
+    const Span sq = span(q, nh * dk * es), sk = span(k, nh * dk * es), sv = span(v, nh * dv * es);
+    const Span sa = span(uses_alpha(mode) ? alpha : nullptr, nh * 4);
+    const Span sb = span(uses_beta(mode) ? beta : nullptr, nh * 4);
+    const Span ss = span(S, nh * dv * dk * 4), so = span(o, nh * dv * es);
+    for (Span in : {sq, sk, sv, sa, sb, ss})
+        if (overlap(so, in)) return LR_ERR_ALIAS;
+    for (Span in : {sq, sk, sv, sa, sb})
+        if (overlap(ss, in)) return LR_ERR_ALIAS;
+
+    const cudaError_t e = launch_step(q, k, v, alpha, beta, S, o, N, H, dk, dv, dt, mode, stream);
+    return e == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+}
+
+}  // extern "C"

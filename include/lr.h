@@ -1,0 +1,149 @@
+/*
+ * lr.h -- C ABI of the GB300 (sm_103a) library for the fixed-size
+ * linear-attention memory S_t (d_v x d_k) under the gated delta rule.
+ *
+ * The operation (page "Scrivere meglio nella memoria: gate e delta rule",
+ * section "Unire oblio e correzione: Gated DeltaNet", and the summary table of
+ * the same page):
+ *
+ *     S_t = S_{t-1} [ alpha_t (I - beta_t k_t k_t^T) ] + beta_t v_t k_t^T
+ *     o_t = S_t q_t                     (read-out after the write of token t)
+ *
+ * and its special cases, selected by lr_mode.  S has value channels as rows
+ * and key channels as columns, so o = S q (same page, gates section, on the
+ * side from which a transition multiplies).
+ *
+ * Conventions shared by every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates no memory and keeps no state between calls other than
+ *     per-device kernel attributes set once.
+ *   - Tensors are contiguous and row-major with the shapes given below; base
+ *     pointers must be 16-byte aligned (else LR_ERR_ALIGN).
+ *   - alpha, beta and the state are always fp32; q, k, v and o have the
+ *     element type given by lr_dtype.
+ *   - Arguments are validated on the host, before any launch; a call that
+ *     returns an error status launched nothing and wrote nothing.
+ *   - Work is enqueued on `stream`; the call returns without synchronising.
+ *     Faults inside a kernel surface at the caller's next synchronisation
+ *     (LR_ERR_CUDA is returned only for launch failures reported at once).
+ *   - Values are not validated.  The documented domain is alpha in (0, 1],
+ *     beta in [0, 1]; NaN and Inf propagate.
+ *   - No exceptions cross the ABI.  Calls on different streams are
+ *     independent; calls that write the same buffers race.
+ */
+#ifndef LR_H_
+#define LR_H_
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LR_OK = 0,
+    LR_ERR_NULL = 1,        /* a required pointer is NULL                         */
+    LR_ERR_SHAPE = 2,       /* a size is negative, zero where it must not be, or
+                               the element count overflows                          */
+    LR_ERR_DTYPE = 3,       /* unknown lr_dtype                                    */
+    LR_ERR_ALIGN = 4,       /* a base pointer is not 16-byte aligned               */
+    LR_ERR_MODE = 5,        /* unknown lr_mode                                     */
+    LR_ERR_UNSUPPORTED = 6, /* valid but not implemented: d_k or d_v outside
+                               {32, 64, 128}, or chunk != 64                       */
+    LR_ERR_CUDA = 7,        /* the CUDA runtime reported an error at launch        */
+    LR_ERR_ALIAS = 8        /* an output overlaps an input it must not overlap     */
+} lr_status;
+
+/* Which row of the family (summary table of the first page). */
+typedef enum {
+    /* S_t = S_{t-1} + v_t k_t^T  (plain accumulation, opening section).
+       alpha and beta are ignored and may be NULL. */
+    LR_MODE_LINEAR = 0,
+    /* S_t = alpha_t S_{t-1} + v_t k_t^T  (scalar gate: RetNet with a fixed
+       per-head gamma broadcast by the caller, or a Mamba-2-style data-dependent
+       alpha; section "Dimenticare: i gate").  beta is ignored, may be NULL. */
+    LR_MODE_DECAY = 1,
+    /* S_t = S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T  (delta rule,
+       section "Correggere: la delta rule").  alpha is ignored, may be NULL. */
+    LR_MODE_DELTA = 2,
+    /* S_t = S_{t-1} [alpha_t (I - beta_t k_t k_t^T)] + beta_t v_t k_t^T
+       (Gated DeltaNet).  Both alpha and beta are required. */
+    LR_MODE_GATED_DELTA = 3
+} lr_mode;
+
+/* Element type of q, k, v and o. */
+typedef enum {
+    LR_DT_F32 = 0,  /* fp32 in and out; computed in fp32 on CUDA cores          */
+    LR_DT_BF16 = 1  /* bf16 in and out; bf16 tensor-core products with fp32
+                       accumulation, fp32 state                               */
+} lr_dtype;
+
+/*
+ * Chunkwise forward over whole sequences (prefill).
+ *
+ * Computes, for every (b, h), the recurrence over t = 0..T-1 from S0 and
+ * returns every read-out and the final state.  The sequence is processed in
+ * blocks of `chunk` tokens: inside a block all tokens are computed together
+ * (decay-masked scores and, for the delta rows, the pseudo-value triangular
+ * system of the WY representation -- first page, section "Correggere: la
+ * delta rule"); only the end-of-block state passes from one block to the next
+ * (page "Le architetture lineari: RetNet, RWKV, xLSTM", section "RetNet: la
+ * retention e le sue tre forme", chunkwise form).  The result equals the
+ * sequential recurrence up to rounding.  A final block shorter than `chunk`
+ * is handled.
+ *
+ *   q      [B, H, T, dk]   dtype dt
+ *   k      [B, H, T, dk]   dtype dt
+ *   v      [B, H, T, dv]   dtype dt
+ *   alpha  [B, H, T]       fp32; required for DECAY and GATED_DELTA
+ *   beta   [B, H, T]       fp32; required for DELTA and GATED_DELTA
+ *   S0     [B, H, dv, dk]  fp32 initial state, or NULL for zeros
+ *   o      [B, H, T, dv]   dtype dt, written; must not overlap any input
+ *   S_T    [B, H, dv, dk]  fp32 final state, written; may be the same pointer
+ *                          as S0 (in-place update), must not overlap anything
+ *                          else
+ *   B, H >= 1; T >= 0 (T == 0 copies S0, or zeros, to S_T);
+ *   dk, dv in {32, 64, 128}; chunk == 64.
+ *
+ * q, k, v and o may be NULL when T == 0.
+ */
+lr_status lr_fwd_chunked(const void *q, const void *k, const void *v,
+                         const float *alpha, const float *beta,
+                         const float *S0, void *o, float *S_T,
+                         int B, int H, int T, int dk, int dv, int chunk,
+                         lr_dtype dt, lr_mode mode, cudaStream_t stream);
+
+/*
+ * One recurrent step for N independent sequences (decode).  Per (n, h) and
+ * per value channel r independently, with s = S[r, :] (page "Le architetture
+ * lineari", recurrent form, O(d^2) per token and fixed memory):
+ *
+ *     a   = alpha (1 for LINEAR and DELTA)
+ *     u_r = beta (v_r - a s.k)   for DELTA / GATED_DELTA,   v_r otherwise
+ *     S[r, :] <- a s + u_r k
+ *     o_r     =  a (s.q) + u_r (k.q)        ( = S_new[r, :] . q )
+ *
+ *   q, k   [N, H, dk]       dtype dt
+ *   v      [N, H, dv]       dtype dt
+ *   alpha  [N, H]           fp32 (required for DECAY, GATED_DELTA)
+ *   beta   [N, H]           fp32 (required for DELTA, GATED_DELTA)
+ *   S      [N, H, dv, dk]   fp32, read and updated IN PLACE
+ *   o      [N, H, dv]       dtype dt, written; must not overlap S or inputs
+ *   N, H >= 1; dk, dv in {32, 64, 128}.
+ */
+lr_status lr_step(const void *q, const void *k, const void *v,
+                  const float *alpha, const float *beta, float *S, void *o,
+                  int N, int H, int dk, int dv, lr_dtype dt, lr_mode mode,
+                  cudaStream_t stream);
+
+/* Static English text for a status code (never NULL). */
+const char *lr_status_string(lr_status s);
+
+/* ABI version of this header: 1. */
+int lr_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LR_H_ */

@@ -1,0 +1,119 @@
+"""CPU-side checks of liblr: it builds, loads, exports every symbol the header
+declares, and rejects invalid arguments before any launch.
+
+Calls that pass deliberately invalid arguments run in a child process with no
+GPU visible, so that even a validation bug could not launch a kernel on fake
+pointers.
+"""
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lr.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_delta_rule_fwd_gb300.build import build
+    build()
+    import gated_delta_rule_fwd_gb300 as lr
+    return lr.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lr_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    assert set(_declared_functions()) == {"lr_fwd_chunked", "lr_step", "lr_status_string",
+                                          "lr_abi_version"}
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s+(\w+)", out))
+    for name in _declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings_and_version(lib):
+    import gated_delta_rule_fwd_gb300 as lr
+    assert lib.lr_abi_version() == 1
+    for code in range(9):
+        s = lr.status_string(code)
+        assert s and s != "unknown status"
+    assert lr.status_string(99) == "unknown status"
+
+
+def test_python_binding_matches_header_names():
+    import gated_delta_rule_fwd_gb300 as lr
+    assert callable(lr.lr_fwd_chunked) and callable(lr.lr_step)
+    assert tuple(sorted(lr.SYMBOLS)) == tuple(_declared_functions())
+
+
+_VALIDATION_CHILD = r"""
+import ctypes, sys
+sys.path.insert(0, sys.argv[1])
+import gated_delta_rule_fwd_gb300 as lr
+L = lr.lib()
+P = lambda a: ctypes.c_void_p(a)
+A = [0x10000000 + i * 0x10000000 for i in range(8)]   # distinct, aligned, never dereferenced
+q, k, v, al, be, s0, o, st = (P(a) for a in A)
+S = None
+def chunk(**kw):
+    args = dict(q=q, k=k, v=v, al=al, be=be, s0=s0, o=o, st=st, B=1, H=1, T=8, dk=32, dv=32,
+                chunk=64, dt=0, mode=3)
+    args.update(kw)
+    a = args
+    return L.lr_fwd_chunked(a['q'], a['k'], a['v'], a['al'], a['be'], a['s0'], a['o'], a['st'],
+                            a['B'], a['H'], a['T'], a['dk'], a['dv'], a['chunk'], a['dt'],
+                            a['mode'], None)
+def step(**kw):
+    args = dict(q=q, k=k, v=v, al=al, be=be, s=s0, o=o, N=1, H=1, dk=32, dv=32, dt=1, mode=3)
+    args.update(kw)
+    a = args
+    return L.lr_step(a['q'], a['k'], a['v'], a['al'], a['be'], a['s'], a['o'], a['N'], a['H'],
+                     a['dk'], a['dv'], a['dt'], a['mode'], None)
+cases = [
+    ("mode", chunk(mode=4), 5), ("mode-neg", chunk(mode=-1), 5), ("dtype", chunk(dt=2), 3),
+    ("B0", chunk(B=0), 2), ("Hneg", chunk(H=-1), 2), ("Tneg", chunk(T=-1), 2),
+    ("huge", chunk(B=1 << 20, H=1 << 10, T=1 << 20), 2),
+    ("dk48", chunk(dk=48), 6), ("dv256", chunk(dv=256), 6), ("chunk32", chunk(chunk=32), 6),
+    ("nullq", chunk(q=None), 1), ("nullo", chunk(o=None), 1), ("nullST", chunk(st=None), 1),
+    ("nullalpha", chunk(al=None), 1), ("nullbeta", chunk(be=None), 1),
+    ("decay-nullbeta-ok-but-nullalpha", chunk(mode=1, be=None, al=None), 1),
+    ("misaligned", chunk(k=P(A[1] + 8)), 4),
+    ("alias-o-q", chunk(o=q), 8), ("alias-st-k", chunk(st=k), 8),
+    ("alias-st-partial-s0", chunk(st=P(A[5] + 16)), 8),
+    ("step-mode", step(mode=9), 5), ("step-dtype", step(dt=3), 3), ("step-N0", step(N=0), 2),
+    ("step-dk16", step(dk=16), 6), ("step-nullS", step(s=None), 1),
+    ("step-nullalpha", step(al=None), 1), ("step-misaligned", step(v=P(A[2] + 4)), 4),
+    ("step-alias-o-S", step(o=s0), 8),
+]
+bad = [(n, got, want) for n, got, want in cases if got != want]
+print("BAD", bad)
+sys.exit(1 if bad else 0)
+"""
+
+
+def test_invalid_arguments_rejected_before_launch(lib):
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", _VALIDATION_CHILD, ROOT], env=env,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    import gated_delta_rule_fwd_gb300 as lr
+    monkeypatch.setattr(lr, "_lib", None)
+    monkeypatch.setattr(lr, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        lr.lib()

@@ -1,0 +1,211 @@
+"""Parity of the CUDA library (through its C ABI) with the fp64 oracle.
+
+Metric: max|gpu - oracle| / max|oracle| over a whole tensor, separately for
+the outputs o and the final state.  Bars: 1e-4 for fp32 inputs, 2e-2 for
+bf16 inputs (bf16 tensor-core products with fp32 accumulation).
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_fwd_gb300 as lr
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+MODES = [lr.LINEAR, lr.DECAY, lr.DELTA, lr.GATED_DELTA]
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from gated_delta_rule_fwd_gb300.build import build
+    build()
+    return torch.device("cuda:0")
+
+
+def rel_err(gpu, ref):
+    g = gpu.detach().float().cpu().double().numpy() if hasattr(gpu, "detach") else np.asarray(gpu)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
+    return float(np.max(np.abs(g - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+def to_dev(x, dev):
+    return {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+
+
+def run_chunked(x, mode, dev, **kw):
+    d = to_dev(x, dev)
+    o, st = lr.lr_fwd_chunked(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["S0"], mode=mode, **kw)
+    torch.cuda.synchronize()
+    return o, st
+
+
+def ref_chunked(x, mode):
+    return oracle.recurrent(mode, x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["S0"])
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("mode", MODES, ids=["linear", "decay", "delta", "gated_delta"])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 64), (128, 128)])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
+def test_chunked_small(dev, dtype, mode, dk, dv, T):
+    seed = 1000 + 7 * T + dk + 3 * dv + 11 * mode
+    x = workloads.draw("uniform", 2, 3, T, dk, dv, seed=seed, dtype=dtype,
+                       s0_std=0.1 if (T + mode) % 2 else 0.0)
+    o, st = run_chunked(x, mode, dev)
+    o_ref, s_ref = ref_chunked(x, mode)
+    assert rel_err(o, o_ref) <= TOL[dtype]
+    assert rel_err(st, s_ref) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_chunked_gdn_inputs_several_tiles(dev, dtype):
+    x = workloads.draw("gdn", 2, 4, 64 * 5 + 17, 128, 128, seed=77, dtype=dtype, s0_std=0.1)
+    o, st = run_chunked(x, lr.GATED_DELTA, dev)
+    o_ref, s_ref = ref_chunked(x, lr.GATED_DELTA)
+    assert rel_err(o, o_ref) <= TOL[dtype]
+    assert rel_err(st, s_ref) <= TOL[dtype]
+
+
+def test_chunked_state_in_place(dev):
+    x = workloads.draw("gdn", 1, 2, 130, 64, 64, seed=5, dtype=torch.bfloat16, s0_std=0.1)
+    d = to_dev(x, dev)
+    S = d["S0"].clone()
+    o, st = lr.lr_fwd_chunked(d["q"], d["k"], d["v"], d["alpha"], d["beta"], S, S_T=S,
+                              mode=lr.GATED_DELTA)
+    torch.cuda.synchronize()
+    assert st.data_ptr() == S.data_ptr()
+    o_ref, s_ref = ref_chunked(x, lr.GATED_DELTA)
+    assert rel_err(o, o_ref) <= 2e-2 and rel_err(S, s_ref) <= 2e-2
+
+
+def test_chunked_empty_sequence(dev):
+    x = workloads.draw("gdn", 2, 2, 0, 32, 64, seed=6, dtype=torch.bfloat16, s0_std=0.1)
+    o, st = run_chunked(x, lr.GATED_DELTA, dev)
+    assert o.shape == (2, 2, 0, 64)
+    assert torch.equal(st.cpu(), x["S0"])
+    x["S0"] = None
+    o, st = run_chunked(x, lr.GATED_DELTA, dev)
+    assert torch.count_nonzero(st) == 0
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_chunked_resume_equals_one_call(dev, dtype):
+    """The state is the checkpoint: two calls over halves, the first's S_T fed as
+    the second's S0, give the one-call result (only the end-of-block state
+    crosses a block boundary)."""
+    T = 300
+    x = workloads.draw("gdn", 1, 3, T, 128, 128, seed=8, dtype=dtype, s0_std=0.1)
+    d = to_dev(x, dev)
+    o_full, s_full = lr.lr_fwd_chunked(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["S0"])
+    cut = 150   # not a multiple of the block size
+    sl = lambda t, a, b: t[:, :, a:b].contiguous()
+    o1, s1 = lr.lr_fwd_chunked(sl(d["q"], 0, cut), sl(d["k"], 0, cut), sl(d["v"], 0, cut),
+                               sl(d["alpha"], 0, cut), sl(d["beta"], 0, cut), d["S0"])
+    o2, s2 = lr.lr_fwd_chunked(sl(d["q"], cut, T), sl(d["k"], cut, T), sl(d["v"], cut, T),
+                               sl(d["alpha"], cut, T), sl(d["beta"], cut, T), s1)
+    torch.cuda.synchronize()
+    _, s_ref = ref_chunked(x, lr.GATED_DELTA)
+    assert rel_err(torch.cat([o1, o2], dim=2), o_full.float().cpu().numpy()) <= TOL[dtype]
+    assert rel_err(s2, s_ref) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("name", ["gdn_fp32_small", "retnet_bf16", "mamba2_gate_bf16",
+                                  "gdn_prefill_bf16"])
+def test_workload_full_size(dev, name):
+    """Every output and the whole final state at the workload's full size, in
+    the launch configuration the benchmark times."""
+    w = workloads.WORKLOADS[name]
+    x = workloads.draw_workload(w)
+    o, st = run_chunked(x, w.mode, dev, chunk=w.chunk)
+    o_ref, s_ref = ref_chunked(x, w.mode)
+    tol = TOL[w.torch_dtype]
+    eo, es = rel_err(o, o_ref), rel_err(st, s_ref)
+    print(f"{name}: rel err o={eo:.3e} S_T={es:.3e}")
+    assert eo <= tol and es <= tol
+
+
+# ------------------------------------------------------------------ decode
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("mode", MODES, ids=["linear", "decay", "delta", "gated_delta"])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 64), (128, 128)])
+def test_step_small(dev, dtype, mode, dk, dv):
+    N, H, T = 5, 3, 4
+    x = workloads.draw("uniform", N, H, T, dk, dv, seed=31 + dk + dv + mode, dtype=dtype,
+                       s0_std=0.1)
+    S = x["S0"].to(dev)
+    outs = []
+    for t in range(T):
+        c = lambda n: x[n][:, :, t].contiguous().to(dev)
+        outs.append(lr.lr_step(c("q"), c("k"), c("v"), c("alpha"), c("beta"), S, mode=mode))
+    torch.cuda.synchronize()
+    o_ref, s_ref = ref_chunked(x, mode)
+    assert rel_err(torch.stack(outs, 2), o_ref) <= TOL[dtype]
+    assert rel_err(S, s_ref) <= TOL[dtype]
+
+
+def test_decode_workload_sampled_heads(dev):
+    """1000 consecutive steps over 512 x 32 states.  All heads are checked
+    after step 1; 64 sampled (sequence, head) pairs are checked at every one
+    of the 1000 steps (heads are independent, so the sample is exact)."""
+    w = workloads.WORKLOADS["gdn_decode_bf16"]
+    g = torch.Generator(dev)
+    S = workloads.draw_decode_state(w, dev, g)
+    rng = np.random.default_rng(2024)
+    pick = rng.choice(w.B * w.H, size=64, replace=False)
+    pn = torch.tensor(pick // w.H, device=dev)
+    ph = torch.tensor(pick % w.H, device=dev)
+    S0_pick = S[pn, ph].cpu()
+    S_all0 = S.cpu()
+    seq = {n: [] for n in ("q", "k", "v", "alpha", "beta", "o")}
+    for step in range(w.steps):
+        inp = workloads.draw_decode_step(w, step, dev, g)
+        o = lr.lr_step(inp["q"], inp["k"], inp["v"], inp["alpha"], inp["beta"], S, mode=w.mode)
+        if step == 0:
+            torch.cuda.synchronize()
+            c = {n: t.cpu().unsqueeze(2) for n, t in inp.items()}
+            o_ref, s_ref = oracle.recurrent(w.mode, c["q"], c["k"], c["v"], c["alpha"], c["beta"],
+                                            S_all0)
+            assert rel_err(o, o_ref[:, :, 0]) <= 2e-2
+            assert rel_err(S, s_ref) <= 2e-2
+            del S_all0, c, o_ref, s_ref
+        for n in ("q", "k", "v", "alpha", "beta"):
+            seq[n].append(inp[n][pn, ph].cpu())
+        seq["o"].append(o[pn, ph].cpu())
+    torch.cuda.synchronize()
+    st = lambda n: torch.stack(seq[n], dim=1).unsqueeze(1)   # [64,1,steps,...]
+    o_ref, s_ref = oracle.recurrent(w.mode, st("q"), st("k"), st("v"), st("alpha"), st("beta"),
+                                    S0_pick.unsqueeze(1))
+    eo = rel_err(st("o"), o_ref)
+    es = rel_err(S[pn, ph].unsqueeze(1), s_ref)
+    print(f"decode 1000 steps, 64 sampled heads: rel err o={eo:.3e} S={es:.3e}")
+    assert eo <= 2e-2 and es <= 2e-2
+
+
+# ------------------------------------------------------------ validation
+
+def test_binding_rejects_bad_tensors(dev):
+    x = to_dev(workloads.draw("gdn", 1, 2, 10, 64, 64, seed=3, dtype=torch.bfloat16), dev)
+    with pytest.raises(ValueError):
+        lr.lr_fwd_chunked(x["q"], x["k"], x["v"][..., :32], x["alpha"], x["beta"])
+    with pytest.raises(TypeError):
+        lr.lr_fwd_chunked(x["q"], x["k"].float(), x["v"], x["alpha"], x["beta"])
+    with pytest.raises(ValueError):
+        lr.lr_fwd_chunked(x["q"].transpose(2, 3).contiguous().transpose(2, 3), x["k"], x["v"],
+                          x["alpha"], x["beta"])
+    q48 = torch.zeros(1, 2, 10, 48, device=dev, dtype=torch.bfloat16)
+    with pytest.raises(lr.LrError) as e:
+        lr.lr_fwd_chunked(q48, q48.clone(), x["v"], x["alpha"], x["beta"])
+    assert e.value.status == 6
+    with pytest.raises(lr.LrError) as e:
+        lr.lr_fwd_chunked(x["q"], x["k"], x["v"], x["alpha"], x["beta"], chunk=32)
+    assert e.value.status == 6
+    with pytest.raises(lr.LrError) as e:
+        lr.lr_fwd_chunked(x["q"], x["k"], x["v"], x["alpha"], x["beta"], o=x["v"])
+    assert e.value.status == 8

@@ -1,0 +1,158 @@
+"""Seeded synthetic inputs for the gated delta rule family.
+
+This module only draws and shapes random inputs; it holds none of the
+method's arithmetic.  Tests, the smoke check and the benchmark use it to give
+the CUDA library and the fp64 oracle the same inputs.
+
+The feature maps applied here belong to the model layer around the memory,
+not to the memory itself (page "Scrivere meglio nella memoria: gate e delta
+rule", opening section: the feature map is absorbed in the projections that
+produce q and k -- DeltaNet puts a SiLU followed by an L2 normalisation
+there -- and beta comes from a sigmoid):
+
+* ``gdn`` inputs: q, k = L2norm(SiLU(N(0,1))) per token; v ~ N(0,1);
+  beta = sigmoid(N(0,1)); alpha = sigmoid(N(3,1)); S0 = 0 or N(0, 0.1^2).
+* ``retnet``: q, k, v ~ N(0,1)/sqrt(dk); alpha = gamma_h = 1 - 2^(-5-h) for
+  head h = 0..H-1, the same at every token.
+* ``mamba2``: q, k ~ N(0,1)/sqrt(dk); v ~ N(0,1);
+  alpha = exp(-0.1 softplus(N(0,1))).
+
+Draw order with one ``torch.Generator('cpu')``: q, k, v, beta, alpha, S0.
+Values are drawn in fp32 and, for bf16 workloads, rounded to bf16 once; the
+oracle consumes the rounded values.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+LINEAR, DECAY, DELTA, GATED_DELTA = 0, 1, 2, 3
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    mode: int
+    dtype: str          # "f32" or "bf16": element type of q, k, v, o
+    B: int
+    H: int
+    T: int
+    dk: int
+    dv: int
+    chunk: int
+    seed: int
+    gen: str            # "gdn", "retnet" or "mamba2"
+    s0_std: float       # 0 -> S0 = None (zeros)
+    steps: int = 0      # decode workloads: number of consecutive steps (T unused)
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    def describe(self):
+        return dataclasses.asdict(self)
+
+
+# The five workloads: (1) gated delta fp32 small; (2) RetNet retention;
+# (3) Mamba-2-style scalar gate; (4) gated delta long prefill; (5) gated delta
+# decode, 1000 consecutive steps over 512 sequences x 32 heads.
+WORKLOADS = {
+    "gdn_fp32_small": Workload("gdn_fp32_small", GATED_DELTA, "f32", 1, 2, 256, 32, 32, 64, 0,
+                               "gdn", 0.0),
+    "retnet_bf16": Workload("retnet_bf16", DECAY, "bf16", 4, 8, 2048, 128, 128, 64, 2,
+                            "retnet", 0.0),
+    "mamba2_gate_bf16": Workload("mamba2_gate_bf16", DECAY, "bf16", 8, 16, 4096, 128, 128, 64, 3,
+                                 "mamba2", 0.0),
+    "gdn_prefill_bf16": Workload("gdn_prefill_bf16", GATED_DELTA, "bf16", 2, 16, 16384, 128, 128,
+                                 64, 4, "gdn", 0.1),
+    "gdn_decode_bf16": Workload("gdn_decode_bf16", GATED_DELTA, "bf16", 512, 32, 1, 128, 128, 64,
+                                5, "gdn", 0.1, steps=1000),
+}
+
+
+def _silu_l2(x):
+    x = x * torch.sigmoid(x)
+    return x / torch.clamp(torch.linalg.vector_norm(x, dim=-1, keepdim=True), min=1e-12)
+
+
+def retnet_gamma(H: int) -> torch.Tensor:
+    """Per-head fixed decay 1 - 2^(-5-h), h = 0..H-1 (multi-scale retention)."""
+    return 1.0 - torch.pow(2.0, -5.0 - torch.arange(H, dtype=torch.float64)).float()
+
+
+def draw(gen: str, B, H, T, dk, dv, seed, dtype=torch.float32, s0_std=0.0, device="cpu"):
+    """Draw one input set.  Returns dict q, k, v, alpha, beta, S0 (S0 may be None).
+
+    Shapes: q, k [B,H,T,dk]; v [B,H,T,dv]; alpha, beta [B,H,T] fp32;
+    S0 [B,H,dv,dk] fp32.  q, k, v are rounded once to ``dtype``.  Drawn on
+    the CPU generator and then moved to ``device``.
+    """
+    g = torch.Generator("cpu")
+    g.manual_seed(int(seed))
+    shp_k, shp_v, shp_t = (B, H, T, dk), (B, H, T, dv), (B, H, T)
+    if gen == "gdn":
+        q = _silu_l2(torch.randn(shp_k, generator=g))
+        k = _silu_l2(torch.randn(shp_k, generator=g))
+        v = torch.randn(shp_v, generator=g)
+        beta = torch.sigmoid(torch.randn(shp_t, generator=g))
+        alpha = torch.sigmoid(3.0 + torch.randn(shp_t, generator=g))
+    elif gen == "retnet":
+        s = 1.0 / math.sqrt(dk)
+        q = torch.randn(shp_k, generator=g) * s
+        k = torch.randn(shp_k, generator=g) * s
+        v = torch.randn(shp_v, generator=g) * s
+        beta = torch.zeros(shp_t)
+        alpha = retnet_gamma(H).view(1, H, 1).expand(B, H, T).contiguous()
+    elif gen == "mamba2":
+        s = 1.0 / math.sqrt(dk)
+        q = torch.randn(shp_k, generator=g) * s
+        k = torch.randn(shp_k, generator=g) * s
+        v = torch.randn(shp_v, generator=g)
+        beta = torch.zeros(shp_t)
+        alpha = torch.exp(-0.1 * torch.nn.functional.softplus(torch.randn(shp_t, generator=g)))
+    elif gen == "uniform":
+        # generic small-case inputs: keys of norm <= 1, gates in (0.5, 1)
+        q = torch.randn(shp_k, generator=g) / math.sqrt(dk)
+        k = _silu_l2(torch.randn(shp_k, generator=g))
+        v = torch.randn(shp_v, generator=g)
+        beta = torch.rand(shp_t, generator=g)
+        alpha = 0.5 + 0.5 * torch.rand(shp_t, generator=g)
+    else:
+        raise ValueError(gen)
+    S0 = torch.randn((B, H, dv, dk), generator=g) * s0_std if s0_std > 0 else None
+    out = dict(q=q.to(dtype), k=k.to(dtype), v=v.to(dtype), alpha=alpha.float().contiguous(),
+               beta=beta.float().contiguous(), S0=S0)
+    if device != "cpu":
+        out = {n: (t.to(device) if t is not None else None) for n, t in out.items()}
+    return out
+
+
+def draw_workload(w: Workload, device="cpu"):
+    return draw(w.gen, w.B, w.H, w.T, w.dk, w.dv, w.seed, w.torch_dtype, w.s0_std, device)
+
+
+def draw_decode_step(w: Workload, step: int, device, generator=None):
+    """Inputs of decode step ``step`` for workload ``w`` (fresh per step), drawn
+    on ``device`` with a generator seeded from (seed, step).
+
+    Returns q, k [N,H,dk]; v [N,H,dv] in the workload dtype; alpha, beta [N,H].
+    """
+    g = generator if generator is not None else torch.Generator(device)
+    g.manual_seed(int(w.seed) * 1000003 + int(step))
+    N, H, dk, dv = w.B, w.H, w.dk, w.dv
+    q = _silu_l2(torch.randn((N, H, dk), generator=g, device=device))
+    k = _silu_l2(torch.randn((N, H, dk), generator=g, device=device))
+    v = torch.randn((N, H, dv), generator=g, device=device)
+    beta = torch.sigmoid(torch.randn((N, H), generator=g, device=device))
+    alpha = torch.sigmoid(3.0 + torch.randn((N, H), generator=g, device=device))
+    dt = w.torch_dtype
+    return dict(q=q.to(dt), k=k.to(dt), v=v.to(dt), alpha=alpha.float(), beta=beta.float())
+
+
+def draw_decode_state(w: Workload, device, generator=None):
+    """Initial decode state S ~ N(0, s0_std^2), [N,H,dv,dk] fp32, on ``device``."""
+    g = generator if generator is not None else torch.Generator(device)
+    g.manual_seed(int(w.seed) * 1000003 - 1)
+    return torch.randn((w.B, w.H, w.dv, w.dk), generator=g, device=device) * w.s0_std
