@@ -21,9 +21,10 @@ from .build import LIB_PATH
 LINEAR, DECAY, DELTA, GATED_DELTA = 0, 1, 2, 3
 MODES = {"linear": LINEAR, "decay": DECAY, "delta": DELTA, "gated_delta": GATED_DELTA}
 F32, BF16 = 0, 1
-SYMBOLS = ("lr_fwd_chunked", "lr_step", "lr_status_string", "lr_abi_version")
+SYMBOLS = ("lr_fwd_chunked", "lr_step", "lr_device_status", "lr_status_string", "lr_abi_version")
 STATUS = {0: "LR_OK", 1: "LR_ERR_NULL", 2: "LR_ERR_SHAPE", 3: "LR_ERR_DTYPE", 4: "LR_ERR_ALIGN",
-          5: "LR_ERR_MODE", 6: "LR_ERR_UNSUPPORTED", 7: "LR_ERR_CUDA", 8: "LR_ERR_ALIAS"}
+          5: "LR_ERR_MODE", 6: "LR_ERR_UNSUPPORTED", 7: "LR_ERR_CUDA", 8: "LR_ERR_ALIAS",
+          9: "LR_ERR_TIMEOUT"}
 _USES_ALPHA = {LINEAR: False, DECAY: True, DELTA: False, GATED_DELTA: True}
 _USES_BETA = {LINEAR: False, DECAY: False, DELTA: True, GATED_DELTA: True}
 
@@ -58,12 +59,20 @@ def lib() -> ctypes.CDLL:
         L.lr_status_string.argtypes = [i]
         L.lr_abi_version.restype = i
         L.lr_abi_version.argtypes = []
+        L.lr_device_status.restype = i
+        L.lr_device_status.argtypes = []
         _lib = L
     return _lib
 
 
 def status_string(status: int) -> str:
     return lib().lr_status_string(int(status)).decode()
+
+
+def device_status() -> int:
+    """lr_device_status(): synchronises the current device and returns (and
+    clears) the library's bounded-wait error word as a status code."""
+    return int(lib().lr_device_status())
 
 
 def _dtype_code(t):

@@ -85,6 +85,7 @@ const char *lr_status_string(lr_status s) {
     case LR_ERR_UNSUPPORTED: return "unsupported size: dk and dv must be 32, 64 or 128 and chunk 64";
     case LR_ERR_CUDA: return "CUDA runtime error at launch";
     case LR_ERR_ALIAS: return "an output overlaps an input";
+    case LR_ERR_TIMEOUT: return "a kernel gave up a bounded wait; its outputs are incomplete";
     }
     return "unknown status";
 }
@@ -129,10 +130,19 @@ lr_status lr_fwd_chunked(const void *q, const void *k, const void *v, const floa
                             stream>>>(S0, S_T, n);
         e = cudaGetLastError();
     } else {
-        e = launch_chunked_simt(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, dt, mode,
-                                stream);
+        e = dt == LR_DT_BF16
+                ? launch_chunked_tc(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, mode, stream)
+                : launch_chunked_simt(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, dt, mode,
+                                      stream);
     }
     return e == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+}
+
+lr_status lr_device_status(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return LR_ERR_CUDA;
+    const int e = read_and_clear_tc_error();
+    if (e < 0) return LR_ERR_CUDA;
+    return e ? LR_ERR_TIMEOUT : LR_OK;
 }
 
 lr_status lr_step(const void *q, const void *k, const void *v, const float *alpha,

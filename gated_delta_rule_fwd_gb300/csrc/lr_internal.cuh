@@ -68,6 +68,10 @@ cudaError_t launch_chunked_tc(const void *q, const void *k, const void *v, const
                               const float *beta, const float *S0, void *o, float *S_T, int B,
                               int H, int T, int dk, int dv, lr_mode mode, cudaStream_t stream);
 
+// Returns and clears the tensor-core kernel's bounded-wait error word
+// (1 if set, 0 if clear, -1 if the device could not be read).
+int read_and_clear_tc_error();
+
 // Set the dynamic shared-memory limit of `fn` once per device.
 cudaError_t ensure_smem_attr(const void *fn, int bytes, int slot);
 

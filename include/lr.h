@@ -51,7 +51,8 @@ typedef enum {
     LR_ERR_UNSUPPORTED = 6, /* valid but not implemented: d_k or d_v outside
                                {32, 64, 128}, or chunk != 64                       */
     LR_ERR_CUDA = 7,        /* the CUDA runtime reported an error at launch        */
-    LR_ERR_ALIAS = 8        /* an output overlaps an input it must not overlap     */
+    LR_ERR_ALIAS = 8,       /* an output overlaps an input it must not overlap     */
+    LR_ERR_TIMEOUT = 9      /* a kernel gave up a bounded wait (see lr_device_status) */
 } lr_status;
 
 /* Which row of the family (summary table of the first page). */
@@ -135,6 +136,16 @@ lr_status lr_step(const void *q, const void *k, const void *v,
                   const float *alpha, const float *beta, float *S, void *o,
                   int N, int H, int dk, int dv, lr_dtype dt, lr_mode mode,
                   cudaStream_t stream);
+
+/*
+ * Reports, then clears, the error word that kernels of this library set on
+ * the current device when a bounded wait inside them gave up (a tensor-core
+ * completion signal that never arrived); such a kernel stops early and its
+ * outputs are incomplete.  Synchronises the current device first.
+ * Returns LR_OK, LR_ERR_TIMEOUT, or LR_ERR_CUDA if the device cannot be
+ * queried.
+ */
+lr_status lr_device_status(void);
 
 /* Static English text for a status code (never NULL). */
 const char *lr_status_string(lr_status s);

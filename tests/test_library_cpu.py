@@ -31,8 +31,8 @@ def _declared_functions():
 
 
 def test_header_declares_expected_entry_points():
-    assert set(_declared_functions()) == {"lr_fwd_chunked", "lr_step", "lr_status_string",
-                                          "lr_abi_version"}
+    assert set(_declared_functions()) == {"lr_fwd_chunked", "lr_step", "lr_device_status",
+                                          "lr_status_string", "lr_abi_version"}
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings_and_version(lib):
     import gated_delta_rule_fwd_gb300 as lr
     assert lib.lr_abi_version() == 1
-    for code in range(9):
+    for code in range(10):
         s = lr.status_string(code)
         assert s and s != "unknown status"
     assert lr.status_string(99) == "unknown status"

@@ -23,7 +23,9 @@ def dev():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     from gated_delta_rule_fwd_gb300.build import build
     build()
-    return torch.device("cuda:0")
+    yield torch.device("cuda:0")
+    # no kernel of the module gave up a bounded wait
+    assert lr.device_status() == 0
 
 
 def rel_err(gpu, ref):
