@@ -21,10 +21,11 @@ from .build import LIB_PATH
 LINEAR, DECAY, DELTA, GATED_DELTA = 0, 1, 2, 3
 MODES = {"linear": LINEAR, "decay": DECAY, "delta": DELTA, "gated_delta": GATED_DELTA}
 F32, BF16 = 0, 1
-SYMBOLS = ("lr_fwd_chunked", "lr_step", "lr_device_status", "lr_status_string", "lr_abi_version")
+SYMBOLS = ("lr_fwd_chunked", "lr_fwd_chunked_workspace_size", "lr_step", "lr_device_status",
+           "lr_status_string", "lr_abi_version")
 STATUS = {0: "LR_OK", 1: "LR_ERR_NULL", 2: "LR_ERR_SHAPE", 3: "LR_ERR_DTYPE", 4: "LR_ERR_ALIGN",
           5: "LR_ERR_MODE", 6: "LR_ERR_UNSUPPORTED", 7: "LR_ERR_CUDA", 8: "LR_ERR_ALIAS",
-          9: "LR_ERR_TIMEOUT"}
+          9: "LR_ERR_TIMEOUT", 10: "LR_ERR_WORKSPACE"}
 _USES_ALPHA = {LINEAR: False, DECAY: True, DELTA: False, GATED_DELTA: True}
 _USES_BETA = {LINEAR: False, DECAY: False, DELTA: True, GATED_DELTA: True}
 
@@ -52,7 +53,10 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(LIB_PATH)
         vp, fp, i = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int
         L.lr_fwd_chunked.restype = i
-        L.lr_fwd_chunked.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp] + [i] * 6 + [i, i, vp]
+        L.lr_fwd_chunked.argtypes = ([vp, vp, vp, fp, fp, fp, vp, fp] + [i] * 6 +
+                                     [i, i, vp, ctypes.c_size_t, vp])
+        L.lr_fwd_chunked_workspace_size.restype = ctypes.c_size_t
+        L.lr_fwd_chunked_workspace_size.argtypes = [i] * 8
         L.lr_step.restype = i
         L.lr_step.argtypes = [vp, vp, vp, fp, fp, fp, vp] + [i] * 4 + [i, i, vp]
         L.lr_status_string.restype = ctypes.c_char_p
@@ -105,14 +109,24 @@ def _stream_handle(stream, device):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def workspace_size(B, H, T, dk, dv, dtype, mode=GATED_DELTA, chunk=64) -> int:
+    """lr_fwd_chunked_workspace_size for these sizes (dtype: torch dtype)."""
+    import torch
+    dt = F32 if dtype == torch.float32 else BF16
+    return int(lib().lr_fwd_chunked_workspace_size(B, H, T, dk, dv, int(chunk), dt,
+                                                   int(MODES.get(mode, mode))))
+
+
 def lr_fwd_chunked(q, k, v, alpha=None, beta=None, S0=None, *, mode=GATED_DELTA, chunk=64,
-                   o=None, S_T=None, stream=None):
+                   o=None, S_T=None, workspace=None, stream=None):
     """Chunkwise forward (see ``lr_fwd_chunked`` in include/lr.h).
 
     q, k: [B,H,T,dk]; v: [B,H,T,dv] (float32 or bfloat16, same dtype);
     alpha, beta: [B,H,T] float32 where the mode uses them; S0: [B,H,dv,dk]
     float32 or None.  ``o`` and ``S_T`` may be given to write into (``S_T``
-    may be ``S0``).  Returns (o, S_T).
+    may be ``S0``).  ``workspace`` is a uint8 CUDA tensor of at least
+    ``workspace_size(...)`` bytes; when None one is allocated through the
+    PyTorch caching allocator.  Returns (o, S_T).
     """
     import torch
     mode = MODES.get(mode, mode)
@@ -143,9 +157,13 @@ def lr_fwd_chunked(q, k, v, alpha=None, beta=None, S0=None, *, mode=GATED_DELTA,
         S_T = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
     else:
         _check(S_T, "S_T", (B, H, dv, dk), torch.float32, dev)
+    need = int(lib().lr_fwd_chunked_workspace_size(B, H, T, dk, dv, int(chunk), dt, int(mode)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().lr_fwd_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
                               _ptr(o), _ptr(S_T), B, H, T, dk, dv, int(chunk), dt, int(mode),
-                              _stream_handle(stream, dev))
+                              _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
     if st != 0:
         raise LrError(st, "lr_fwd_chunked")
     return o, S_T

@@ -8,34 +8,41 @@
 // steps at once -- page "Scrivere meglio nella memoria: gate e delta rule",
 // section "Correggere: la delta rule"), g_r = e^{G_r}, kd_i = e^{G_C - G_i}:
 //
-//   P   = (Q K^T) (.) M,            M_ri = e^{G_r - G_i} for i <= r     (scores)
-//   A   = strict_lower(diag(beta) (K K^T) (.) M)                       (delta couplings)
-//   T   = (I + A)^-1                (unit lower triangular; the WY / UT step)
-//   W   = T diag(beta g) K,         Ut = T diag(beta) V
-//   U   = Ut - W S^T                pseudo-values (u_r of the WY representation)
-//   O   = diag(g) Q S^T + P U
-//   S  <- g_C S + U^T diag(kd) K
-// and without the delta term U = V (T unused).  The derivation: the gated
-// recurrence unrolled inside a block gives u_r = beta_r (v_r - g_r S k_r -
+//   P  = (Q K^T) (.) M,          M_ri = e^{G_r - G_i} for i <= r        (scores)
+//   A  = strict_lower(diag(beta) (K K^T) (.) M)                        (delta couplings)
+//   T  = (I + A)^-1              unit lower triangular (the WY / UT step)
+//   W  = T diag(beta g) K,       Ut = T diag(beta) V
+//   U  = Ut - W S^T              pseudo-values u_r of the WY representation
+//   O  = diag(g) Q S^T + P U
+//   S <- g_C S + U^T diag(kd) K
+// and without the delta term U = V.  The derivation: the gated recurrence
+// unrolled inside a block gives u_r = beta_r (v_r - g_r S k_r -
 // sum_{i<r} e^{G_r - G_i} (k_i.k_r) u_i), a unit-lower-triangular system.
 //
-// Work split.  One CTA of 128 threads per (32 value channels, head, batch);
-// rows of S evolve independently, so value-channel slices never exchange
-// data.  Every product runs on the tensor cores as an M = 128 tcgen05.mma
-// with both operands in shared memory (K-major, 128-byte swizzle) and the
-// fp32 accumulator in TMEM.  Two 64-row operands are stacked to fill M:
-//   E1  [Q; K] K^T           -> [Q K^T ; K K^T]            (TMEM R1, 64 cols)
-//   E3  [T; P] (beta g K)^T  -> [W ; -]                    (R2, dk cols)
-//       [T; P] (beta V)^T    -> [Ut ; P beta V]            (R3, 32 cols)
-//   S1  [-W; g Q] S^T   +=   -> [U ; P beta V + g Q S^T]   (R3)
-//   S3  (kd K)^T U      =    -> Delta S^T                  (R4, 32 cols)
-//       [T; P] (U - beta V)^T += -> rows 64..127 = O        (R3)
+// Two launches:
+//  * prep: one CTA per (block, head, batch), all blocks in parallel.  Computes
+//    what does not depend on the state: G, the scores P, the UT inverse T
+//    (blocked forward substitution in fp32 on the CUDA cores) and -W, and
+//    writes -W, T and P to the workspace as bf16 tiles already in the
+//    shared-memory operand layout, plus the per-token gate vectors.
+//  * scan: one CTA per (32 value channels, head, batch); rows of S evolve
+//    independently given k, alpha and beta, so slices never exchange data.
+//    The loop over blocks is sequential; the next block's tiles are fetched
+//    and its operand tiles built while the current block's products run.
+//
+// Every product runs as an M = 128 tcgen05.mma with K-major 128-byte-swizzled
+// shared-memory operands and an fp32 accumulator in tensor memory; 64-row
+// operands are stacked to fill M:
+//   prep  E1  [Q; K] K^T            -> [Q K^T ; K K^T]
+//         E3  [T; 0] (beta g K)^T   -> [W ; 0]
+//   scan  G1  [T; 0] (beta V)^T     -> [Ut ; 0]           (R3)
+//             [-W; g Q] S^T        +=  [U ; g Q S^T]     (R3)
+//         G2  (kd K)^T U           ->  Delta S^T          (R4)
+//             [0; P] U             +=  rows 64..127 = O   (R3)
 // The fp32 master copy of the state slice lives in registers (thread j owns
-// column j); a bf16 copy in shared memory feeds S1.  T is formed in fp32 on
-// the CUDA cores by blocked forward substitution (16 x 16 diagonal blocks).
-// Inputs of the next block are prefetched with cp.async while the current
-// block computes; a final short block is zero-filled (alpha treated as 1,
-// beta as 0), which leaves the real tokens' results unchanged.
+// column j); a bf16 copy in shared memory feeds the next block.  A final
+// short block is zero-filled (alpha treated as 1, beta as 0), which leaves
+// the real tokens' results unchanged.
 #include "lr_internal.cuh"
 #include "tc_common.cuh"
 
@@ -46,39 +53,23 @@ using bf16 = __nv_bfloat16;
 using namespace tc;
 
 constexpr int C = 64;      // tokens per block
-constexpr int DVS = 32;    // value channels per CTA
-constexpr int NT = 128;    // threads per CTA (one warpgroup)
+constexpr int DVS = 32;    // value channels per scan CTA
+constexpr int NT = 128;    // threads per CTA
 constexpr int AP = C + 1;  // padded fp32 row of A and T
+constexpr int XP = 49;     // padded fp32 row of the solve scratch
 
 __device__ int g_tc_error = 0;  // set to 1 when a bounded wait gives up
 
+// Workspace record of one (head, block), written by prep and read by scan.
 template <int DK>
-struct TcLayout {
-    static constexpr int KB = (DK + 63) / 64;           // 64-wide K blocks of a dk-long row
-    static constexpr int QK = 0;                         // 2 x [128 rows][DK]   (Q rows, K rows)
-    static constexpr int QK_BYTES = 128 * 128 * KB;
-    static constexpr int WQ = QK + 2 * QK_BYTES;         // [128][DK]: -W rows, g*Q rows
-    static constexpr int TP = WQ + QK_BYTES;             // [128][64]: T rows, P rows
-    static constexpr int KBT = TP + 16384;               // [DK][64]:  (beta g K)^T
-    static constexpr int KBT_BYTES = (DK < 8 ? 8 : DK) * 128;
-    static constexpr int KTT = KBT + ((KBT_BYTES + 1023) / 1024) * 1024;  // [128][64]: (kd K)^T
-    static constexpr int VBT = KTT + 16384;              // [32][64]:  (beta V)^T (V^T w/o delta)
-    static constexpr int UB = VBT + 4096;                // [32][64]:  U^T
-    static constexpr int XB = UB + 4096;                 // [32][64]:  (U - beta V)^T
-    static constexpr int SB = XB + 4096;                 // [32][DK]:  bf16 state slice
-    static constexpr int VRAW = SB + 32 * 128 * KB;      // 2 x [64][32] bf16 raw V slice
-    static constexpr int AB = VRAW + 2 * 4096;           // 2 x {alpha[64], beta[64]} fp32
-    static constexpr int AMAT = AB + 2 * 512;            // fp32 [64][65]
-    static constexpr int TMAT = AMAT + C * AP * 4;       // fp32 [64][65]
-    static constexpr int XTMP = TMAT + C * AP * 4;       // fp32 [16][49]
-    static constexpr int VEC = XTMP + 16 * 49 * 4;      // fp32 G, g, kd, bg, b   [5][64]
-    static constexpr int BAR = VEC + 5 * 64 * 4;         // mbarrier + TMEM base
-    static constexpr int BYTES = BAR + 64;
-    static constexpr int ALLOC = BYTES + 1024;           // slack for 1024-byte alignment
+struct Rec {
+    static constexpr int KB = (DK + 63) / 64;
+    static constexpr int WT = 0;                 // -W: KB blocks of [64 rows][128 B]
+    static constexpr int TT = WT + KB * 8192;    // T:  [64][64] bf16 tile
+    static constexpr int PT = TT + 8192;         // P:  [64][64] bf16 tile
+    static constexpr int VEC = PT + 8192;        // G, g, kd, beta: 4 x 64 fp32
+    static constexpr int BYTES = VEC + 1024;
 };
-
-// TMEM columns
-constexpr uint32_t kR1 = 0, kR2 = 64, kR3 = 192, kR4 = 224, kTmemCols = 256;
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
@@ -98,6 +89,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
     return lo | (hi << 16);
 }
+__device__ __forceinline__ uint4 pack8(const float *x) {
+    uint4 r;
+    r.x = pack_bf16(x[0], x[1]);
+    r.y = pack_bf16(x[2], x[3]);
+    r.z = pack_bf16(x[4], x[5]);
+    r.w = pack_bf16(x[6], x[7]);
+    return r;
+}
 __device__ __forceinline__ float bf16_at(const uint8_t *tile, uint32_t off) {
     return __bfloat162float(*reinterpret_cast<const bf16 *>(tile + off));
 }
@@ -105,78 +104,444 @@ __device__ __forceinline__ void st_bf16(uint8_t *tile, uint32_t off, float x) {
     *reinterpret_cast<bf16 *>(tile + off) = __float2bfloat16_rn(x);
 }
 
-// Stage block `t0` of (bh, slice) into buffer `buf` with cp.async (zero-filled
-// past the end of the sequence).
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) &
+                                       ~static_cast<uintptr_t>(1023));
+}
+
+// ===================================================================== prep
+
 template <int DK>
-__device__ __forceinline__ void prefetch_block(uint8_t *sm, int buf, const bf16 *q, const bf16 *k,
-                                               const bf16 *v, const float *alpha,
-                                               const float *beta, size_t bh, int T, int t0,
-                                               int dv, int c0, int tid) {
-    using L = TcLayout<DK>;
-    uint8_t *qk = sm + L::QK + buf * L::QK_BYTES;
-    constexpr int CPR = DK / 8;  // 16-byte chunks per row
-    for (int idx = tid; idx < 2 * C * CPR; idx += NT) {
-        const int which = idx / (C * CPR);  // 0: q, 1: k
-        const int rem = idx % (C * CPR);
-        const int r = rem / CPR, ch = rem % CPR;
-        const bool ok = t0 + r < T;
-        const bf16 *src = (which ? k : q) + ((bh * T + (ok ? t0 + r : 0)) * DK + ch * 8);
-        cp_async16(smem_u32(qk + sw128_offset(which * 64 + r, ch * 8, 128)), src, ok);
+struct PrepLayout {
+    static constexpr int KB = (DK + 63) / 64;
+    static constexpr int QK = 0;                            // [128 rows][DK]: Q rows, K rows
+    static constexpr int TZ = QK + 128 * 128 * KB;          // [128][64]: T rows, zero rows
+    static constexpr int KBT = TZ + 16384;                  // [DK][64]: (beta g K)^T
+    static constexpr int AM = KBT + ((DK * 128 + 1023) / 1024) * 1024;  // fp32 [64][AP]
+    static constexpr int TM = AM + C * AP * 4;              // fp32 [64][AP]
+    static constexpr int XT = TM + C * AP * 4;              // fp32 [16][XP]
+    static constexpr int VEC = XT + 16 * XP * 4;            // G, ginv, g, kd, bg, b
+    static constexpr int BAR = VEC + 6 * 64 * 4;
+    static constexpr int BYTES = BAR + 64;
+    static constexpr int ALLOC = BYTES + 1024;
+};
+
+// One block row of the blocked UT inverse: with the rows of T above it done,
+//   X = A[rows b, cols < 16b] T[< 16b, < 16b];   T[rows b, cols < 16b] = -T_bb X.
+// 128 threads: thread = (row rr of the block, column group cg), columns cg + 8k.
+template <int BR>
+__device__ __forceinline__ void ut_block_row(const float *Am, float *Tm, float *Xt, int tid) {
+    constexpr int NC = 2 * BR;  // columns per thread (16*BR columns / 8 groups)
+    const int rr = tid & 15, cg = tid >> 4;
+    const int row = 16 * BR + rr;
+    float acc[NC];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) acc[k] = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < 16 * BR; ++i) {
+        const float a = Am[row * AP + i];
+#pragma unroll
+        for (int k = 0; k < NC; ++k) acc[k] += a * Tm[i * AP + cg + 8 * k];
     }
-    uint8_t *vr = sm + L::VRAW + buf * 4096;
-    for (int idx = tid; idx < C * (DVS / 8); idx += NT) {
-        const int r = idx / (DVS / 8), ch = idx % (DVS / 8);
-        const bool ok = t0 + r < T;
-        const bf16 *src = v + ((bh * T + (ok ? t0 + r : 0)) * dv + c0 + ch * 8);
-        cp_async16(smem_u32(vr + (r * DVS + ch * 8) * 2), src, ok);
+#pragma unroll
+    for (int k = 0; k < NC; ++k) Xt[rr * XP + cg + 8 * k] = acc[k];
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < NC; ++k) acc[k] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float t = Tm[row * AP + 16 * BR + i];
+#pragma unroll
+        for (int k = 0; k < NC; ++k) acc[k] += t * Xt[i * XP + cg + 8 * k];
     }
-    float *ab = reinterpret_cast<float *>(sm + L::AB + buf * 512);
-    if (tid < C) {
-        const bool ok = t0 + tid < T;
-        const size_t gi = bh * T + (ok ? t0 + tid : 0);
-        if (alpha) cp_async4(smem_u32(ab + tid), alpha + gi, ok);
-        if (beta) cp_async4(smem_u32(ab + 64 + tid), beta + gi, ok);
+#pragma unroll
+    for (int k = 0; k < NC; ++k) Tm[row * AP + cg + 8 * k] = -acc[k];
+    __syncthreads();
+}
+
+// T = (I + A)^-1 for a strictly lower A (64 x 64, fp32 in shared memory).
+// Tm must hold zeros in the blocks above the block diagonal on entry; on exit
+// it holds T's lower triangle with zeros above the diagonal.
+__device__ __forceinline__ void ut_inverse(const float *Am, float *Tm, float *Xt, int tid) {
+    if (tid < 64) {
+        const int b = tid >> 4, c = tid & 15;
+        const float *Ab = Am + (16 * b) * AP + 16 * b;
+        float x[16];
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+            float s0 = (rr == c) ? 1.f : 0.f, s1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < rr; ++i) {
+                if (i & 1) s1 -= Ab[rr * AP + i] * x[i];
+                else s0 -= Ab[rr * AP + i] * x[i];
+            }
+            x[rr] = s0 + s1;
+        }
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) Tm[(16 * b + rr) * AP + 16 * b + c] = x[rr];
     }
-    cp_async_commit();
+    __syncthreads();
+    ut_block_row<1>(Am, Tm, Xt, tid);
+    ut_block_row<2>(Am, Tm, Xt, tid);
+    ut_block_row<3>(Am, Tm, Xt, tid);
 }
 
 template <int DK, bool ALPHA, bool DELTA>
-__global__ void __launch_bounds__(NT, 1)
-chunk_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
-                const bf16 *__restrict__ v, const float *__restrict__ alpha,
-                const float *__restrict__ beta, const float *__restrict__ S0,
-                bf16 *__restrict__ o, float *__restrict__ ST, int H, int T, int dv) {
-    using L = TcLayout<DK>;
+__global__ void __launch_bounds__(NT)
+chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
+                  const float *__restrict__ alpha, const float *__restrict__ beta,
+                  uint8_t *__restrict__ ws, int H, int T, int nblk) {
+    using L = PrepLayout<DK>;
+    using R = Rec<DK>;
     extern __shared__ uint8_t sm_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
-                                              ~static_cast<uintptr_t>(1023));
+    uint8_t *sm = align1024(sm_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c0 = blockIdx.x * DVS;
+    const int blk = blockIdx.x;
     const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
+    const int t0 = blk * C;
+    const int n = min(C, T - t0);
+    uint8_t *rec = ws + (bh * nblk + blk) * (size_t)R::BYTES;
 
-    uint8_t *WQ = sm + L::WQ, *TP = sm + L::TP, *KBT = sm + L::KBT, *KTT = sm + L::KTT;
-    uint8_t *VBT = sm + L::VBT, *UB = sm + L::UB, *XB = sm + L::XB, *SB = sm + L::SB;
-    float *Am = reinterpret_cast<float *>(sm + L::AMAT);
-    float *Tm = reinterpret_cast<float *>(sm + L::TMAT);
-    float *Xt = reinterpret_cast<float *>(sm + L::XTMP);
+    uint8_t *QK = sm + L::QK, *TZ = sm + L::TZ, *KBT = sm + L::KBT;
+    float *Am = reinterpret_cast<float *>(sm + L::AM);
+    float *Tm = reinterpret_cast<float *>(sm + L::TM);
+    float *Xt = reinterpret_cast<float *>(sm + L::XT);
     float *Gv = reinterpret_cast<float *>(sm + L::VEC);
-    float *gv = Gv + 64, *kdv = Gv + 128, *bgv = Gv + 192, *bv = Gv + 256;
+    float *giv = Gv + 64, *gv = Gv + 128, *kdv = Gv + 192, *bgv = Gv + 256, *bv = Gv + 320;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8);
 
-    // ---- one-time set-up: zero the operand tiles whose padding must read as 0
-    for (int i = tid; i < (L::VRAW - L::WQ) / 16; i += NT)
-        reinterpret_cast<uint4 *>(sm + L::WQ)[i] = make_uint4(0, 0, 0, 0);
+    // ---- stage Q, K (zero-filled past the end) and the gates
+    constexpr int CPR = DK / 8;
+    for (int idx = tid; idx < 2 * C * CPR; idx += NT) {
+        const int which = idx / (C * CPR);
+        const int rem = idx % (C * CPR);
+        const int r = rem / CPR, ch = rem % CPR;
+        const bool ok = r < n;
+        const bf16 *src = (which ? k : q) + ((bh * T + (ok ? t0 + r : 0)) * DK + ch * 8);
+        cp_async16(smem_u32(QK + sw128_offset(which * 64 + r, ch * 8, 128)), src, ok);
+    }
+    cp_async_commit();
+    if (DELTA) {
+        // zero rows 64..127 of [T; 0] and the upper blocks of Tm
+        for (int i = tid; i < 8192 / 16; i += NT)
+            reinterpret_cast<uint4 *>(TZ + 8192)[i] = make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < C * AP; i += NT) Tm[i] = 0.f;
+    }
+    float la = 0.f, b = 0.f;
+    if (tid < C && tid < n) {
+        if (ALPHA) la = __logf(alpha[bh * T + t0 + tid]);
+        if (DELTA) b = beta[bh * T + t0 + tid];
+    }
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_alloc(tmem_slot, 256);
         tmem_relinquish();
     }
+    // inclusive scan of ln alpha over the block (warps 0 and 1 hold the 64 values)
+    if (warp < 2) {
+        float incl = la;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += y;
+        }
+        Gv[tid] = incl;  // warp 1 adds warp 0's total below
+    }
+    __syncthreads();
+    const float Gfull = tid < C ? Gv[tid] + (tid >= 32 ? Gv[31] : 0.f) : 0.f;
+    __syncthreads();
+    if (tid < C) Gv[tid] = Gfull;
+    __syncthreads();
+    // exp(G_r - G_i) = g_r * ginv_i when exp(-G_63) is finite in fp32
+    const bool factor = !ALPHA || Gv[C - 1] > -80.f;
+    if (tid < C) {
+        const float G = Gv[tid];
+        const float g = ALPHA ? __expf(G) : 1.f;
+        gv[tid] = g;
+        giv[tid] = ALPHA ? __expf(-G) : 1.f;
+        kdv[tid] = ALPHA ? __expf(Gv[C - 1] - G) : 1.f;
+        bgv[tid] = b * g;
+        bv[tid] = b;
+        float *vec = reinterpret_cast<float *>(rec + R::VEC);
+        vec[tid] = G;
+        vec[64 + tid] = g;
+        vec[128 + tid] = ALPHA ? __expf(Gv[C - 1] - G) : 1.f;
+        vec[192 + tid] = b;
+    }
+    cp_async_wait_all();
+    __syncthreads();
 
-    __syncthreads();  // zeroing done before any tile is written
+    // ---- (beta g K)^T for W: thread j builds row j
+    if (DELTA && tid < DK) {
+        const int j = tid;
+#pragma unroll
+        for (int i8 = 0; i8 < C / 8; ++i8) {
+            float w8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                w8[e] = bgv[i8 * 8 + e] * bf16_at(QK, sw128_offset(64 + i8 * 8 + e, j, 128));
+            *reinterpret_cast<uint4 *>(KBT + sw128_offset(j, i8 * 8, DK)) = pack8(w8);
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    bool ok = true;
+
+    // ---- E1: [Q; K] K^T -> TMEM cols [0, 64)
+    if (tid == 0) {
+        const uint32_t id = idesc_bf16_f32(128, 64);
+#pragma unroll
+        for (int ks = 0; ks < DK / 16; ++ks)
+            mma_bf16(tmem, tile_desc(smem_u32(QK), 128, 0, ks), tile_desc(smem_u32(QK), 128, 64, ks),
+                     id, ks > 0);
+        mma_commit(bar);
+    }
+    ok = __syncthreads_and(mbar_wait(bar, 0) ? 1 : 0) != 0;
+    tc_fence_after();
+
+    // ---- E2: P rows (bf16 tile to the workspace), A rows (fp32)
+    if (ok) {
+        const int r = 32 * (warp & 1) + lane;
+        const bool is_q = warp < 2;
+        const float Gr = Gv[r], gr = gv[r];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float a[32];
+            tmem_ld32(tmem + lane_base + 32 * half, a);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int i = half * 32 + e;
+                const float dec = !ALPHA ? 1.f : (factor ? gr * giv[i] : __expf(Gr - Gv[i]));
+                a[e] = (i <= r && (is_q || i < r)) ? a[e] * dec : 0.f;
+            }
+            if (is_q) {
+#pragma unroll
+                for (int i8 = 0; i8 < 4; ++i8)
+                    *reinterpret_cast<uint4 *>(rec + R::PT +
+                                               sw128_offset(r, half * 32 + i8 * 8, 64)) =
+                        pack8(a + i8 * 8);
+            } else if (DELTA) {
+                const float br = bv[r];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) Am[r * AP + half * 32 + e] = br * a[e];
+            }
+        }
+    }
+    __syncthreads();
+
+    if (DELTA && ok) {
+        ut_inverse(Am, Tm, Xt, tid);
+        // T (bf16) -> rows 0..63 of [T; 0] and to the workspace
+        for (int idx = tid; idx < C * 8; idx += NT) {
+            const int r = idx >> 3, i8 = idx & 7;
+            float t[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t[e] = Tm[r * AP + i8 * 8 + e];
+            const uint4 w4 = pack8(t);
+            const uint32_t off = sw128_offset(r, i8 * 8, 64);
+            *reinterpret_cast<uint4 *>(TZ + off) = w4;
+            *reinterpret_cast<uint4 *>(rec + R::TT + off) = w4;
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // ---- E3: [T; 0] (beta g K)^T -> TMEM cols [64, 64 + DK)
+        if (tid == 0) {
+            const uint32_t id = idesc_bf16_f32(128, DK);
+#pragma unroll
+            for (int ks = 0; ks < C / 16; ++ks)
+                mma_bf16(tmem + 64, tile_desc(smem_u32(TZ), 128, 0, ks),
+                         tile_desc(smem_u32(KBT), DK, 0, ks), id, ks > 0);
+            mma_commit(bar);
+        }
+        ok = __syncthreads_and(mbar_wait(bar, 1) ? 1 : 0) != 0;
+        tc_fence_after();
+
+        // ---- -W rows -> workspace
+        if (ok && warp < 2) {
+            const int r = 32 * warp + lane;
+#pragma unroll
+            for (int cb = 0; cb < DK / 32; ++cb) {
+                float w[32];
+                tmem_ld32(tmem + lane_base + 64 + 32 * cb, w);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) w[e] = -w[e];
+#pragma unroll
+                for (int i8 = 0; i8 < 4; ++i8)
+                    *reinterpret_cast<uint4 *>(rec + R::WT +
+                                               sw128_offset(r, cb * 32 + i8 * 8, 64)) =
+                        pack8(w + i8 * 8);
+            }
+        }
+    }
+    if (!ok && lane == 0) atomicExch(&g_tc_error, 1);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ===================================================================== scan
+
+template <int DK>
+struct ScanLayout {
+    static constexpr int KB = (DK + 63) / 64;
+    static constexpr int WQ_BYTES = 128 * 128 * KB;          // [128][DK]: -W rows, g Q rows
+    static constexpr int WQ = 0;                              // x2
+    static constexpr int TZP = WQ + 2 * WQ_BYTES;             // x2 [192][64]: T, 0, P rows
+    static constexpr int KR_BYTES = 64 * 128 * KB;            // raw K block [64][DK]
+    static constexpr int KR = TZP + 2 * 24576;                // x2
+    static constexpr int KTT = KR + 2 * KR_BYTES;             // x2 [128][64]: (kd K)^T
+    static constexpr int VBT = KTT + 2 * 16384;               // x2 [32][64]: (beta V)^T or V^T
+    static constexpr int VR = VBT + 2 * 4096;                 // x2 raw V slice [64][32]
+    static constexpr int VEC = VR + 2 * 4096;                 // x2 G, g, kd, beta
+    static constexpr int UB = VEC + 2 * 1024;                 // [32][64]: U^T
+    static constexpr int SB = UB + 4096;                      // [32][DK]: bf16 state slice
+    static constexpr int BAR = SB + 32 * 128 * KB;
+    static constexpr int BYTES = BAR + 64;
+    static constexpr int ALLOC = BYTES + 1024;
+};
+
+// TMEM columns of the scan kernel
+constexpr uint32_t kR3 = 0, kR4 = 32, kScanCols = 64;
+
+// Fetch block `blk` of (bh, slice) into buffer `buf` (one cp.async group).
+template <int DK, bool DELTA>
+__device__ __forceinline__ void scan_fetch(uint8_t *sm, int buf, const bf16 *q, const bf16 *k,
+                                           const bf16 *v, const uint8_t *rec, size_t bh, int T,
+                                           int blk, int dv, int c0, int tid) {
+    using L = ScanLayout<DK>;
+    using R = Rec<DK>;
+    const int t0 = blk * C;
+    constexpr int CPR = DK / 8;
+    uint8_t *wq = sm + L::WQ + buf * L::WQ_BYTES;
+    uint8_t *kr = sm + L::KR + buf * L::KR_BYTES;
+    for (int idx = tid; idx < 2 * C * CPR; idx += NT) {
+        const int which = idx / (C * CPR);
+        const int rem = idx % (C * CPR);
+        const int r = rem / CPR, ch = rem % CPR;
+        const bool ok = t0 + r < T;
+        const bf16 *src = (which ? k : q) + ((bh * T + (ok ? t0 + r : 0)) * DK + ch * 8);
+        const uint32_t dst = which ? smem_u32(kr + sw128_offset(r, ch * 8, 64))
+                                   : smem_u32(wq + sw128_offset(64 + r, ch * 8, 128));
+        cp_async16(dst, src, ok);
+    }
+    uint8_t *vr = sm + L::VR + buf * 4096;
+    for (int idx = tid; idx < C * (DVS / 8); idx += NT) {
+        const int r = idx / (DVS / 8), ch = idx % (DVS / 8);
+        const bool ok = t0 + r < T;
+        cp_async16(smem_u32(vr + (r * DVS + ch * 8) * 2),
+                   v + ((bh * T + (ok ? t0 + r : 0)) * dv + c0 + ch * 8), ok);
+    }
+    if (DELTA) {
+        // -W rows -> rows 0..63 of each 64-wide K block of WQ; T -> rows 0..63 of TZP
+        for (int idx = tid; idx < R::KB * 512; idx += NT) {
+            const int kb = idx >> 9, c16 = idx & 511;
+            cp_async16(smem_u32(wq + kb * 16384 + c16 * 16), rec + R::WT + kb * 8192 + c16 * 16, true);
+        }
+        for (int idx = tid; idx < 512; idx += NT)
+            cp_async16(smem_u32(sm + L::TZP + buf * 24576 + idx * 16), rec + R::TT + idx * 16, true);
+    }
+    for (int idx = tid; idx < 512; idx += NT)
+        cp_async16(smem_u32(sm + L::TZP + buf * 24576 + 16384 + idx * 16), rec + R::PT + idx * 16,
+                   true);
+    for (int idx = tid; idx < 64; idx += NT)
+        cp_async16(smem_u32(sm + L::VEC + buf * 1024 + idx * 16), rec + R::VEC + idx * 16, true);
+    cp_async_commit();
+}
+
+// Operand tiles of block `buf` that need only its fetched inputs:
+// g Q in place, (kd K)^T, (beta V)^T (delta) or V^T.
+template <int DK, bool DELTA>
+__device__ __forceinline__ void scan_tiles(uint8_t *sm, int buf, int tid) {
+    using L = ScanLayout<DK>;
+    uint8_t *wq = sm + L::WQ + buf * L::WQ_BYTES;
+    const uint8_t *kr = sm + L::KR + buf * L::KR_BYTES;
+    uint8_t *ktt = sm + L::KTT + buf * 16384;
+    uint8_t *vbt = sm + L::VBT + buf * 4096;
+    const bf16 *vr = reinterpret_cast<const bf16 *>(sm + L::VR + buf * 4096);
+    const float *vec = reinterpret_cast<const float *>(sm + L::VEC + buf * 1024);
+    const float *gv = vec + 64, *kdv = vec + 128, *bv = vec + 192;
+    for (int idx = tid; idx < C * (DK / 8); idx += NT) {
+        const int r = idx / (DK / 8), ch = idx % (DK / 8);
+        uint4 *p = reinterpret_cast<uint4 *>(wq + sw128_offset(64 + r, ch * 8, 128));
+        const uint4 raw = *p;
+        const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
+        const float g = gv[r];
+        float x[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) x[t] = g * __bfloat162float(e[t]);
+        *p = pack8(x);
+    }
+    if (tid < DK) {
+        const int j = tid;
+#pragma unroll
+        for (int i8 = 0; i8 < C / 8; ++i8) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                x[e] = kdv[i8 * 8 + e] * bf16_at(kr, sw128_offset(i8 * 8 + e, j, 64));
+            *reinterpret_cast<uint4 *>(ktt + sw128_offset(j, i8 * 8, 128)) = pack8(x);
+        }
+    }
+    {
+        const int c = tid & 31, part = tid >> 5;  // 4 parts of 16 tokens
+#pragma unroll
+        for (int i8 = 0; i8 < 2; ++i8) {
+            const int i0 = part * 16 + i8 * 8;
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float vv = __bfloat162float(vr[(i0 + e) * DVS + c]);
+                x[e] = DELTA ? bv[i0 + e] * vv : vv;
+            }
+            *reinterpret_cast<uint4 *>(vbt + sw128_offset(c, i0, 32)) = pack8(x);
+        }
+    }
+}
+
+template <int DK, bool ALPHA, bool DELTA>
+__global__ void __launch_bounds__(NT, 1)
+chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
+                  const bf16 *__restrict__ v, const uint8_t *__restrict__ ws,
+                  const float *__restrict__ S0, bf16 *__restrict__ o, float *__restrict__ ST,
+                  int H, int T, int dv, int nblk) {
+    using L = ScanLayout<DK>;
+    using R = Rec<DK>;
+    extern __shared__ uint8_t sm_raw[];
+    uint8_t *sm = align1024(sm_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c0 = blockIdx.x * DVS;
+    const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
+    const uint8_t *recs = ws + bh * nblk * (size_t)R::BYTES;
+
+    uint8_t *UB = sm + L::UB, *SB = sm + L::SB;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8);
+
+    // zero everything once: the padding rows of the stacked operands must read 0
+    for (int i = tid; i < L::BAR / 16; i += NT)
+        reinterpret_cast<uint4 *>(sm)[i] = make_uint4(0, 0, 0, 0);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kScanCols);
+        tmem_relinquish();
+    }
+    __syncthreads();
 
     // fp32 master copy of the state slice: thread j owns S[c0 + c][j], c < 32
     float Sr[DVS];
@@ -188,8 +553,13 @@ chunk_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         for (int c = 0; c < DVS; ++c) st_bf16(SB, sw128_offset(c, tid, 32), Sr[c]);
     }
 
-    if (T > 0) prefetch_block<DK>(sm, 0, q, k, v, alpha, beta, bh, T, 0, dv, c0, tid);
-
+    scan_fetch<DK, DELTA>(sm, 0, q, k, v, recs, bh, T, 0, dv, c0, tid);
+    if (nblk > 1)
+        scan_fetch<DK, DELTA>(sm, 1, q, k, v, recs + R::BYTES, bh, T, 1, dv, c0, tid);
+    if (nblk > 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else cp_async_wait_all();
+    __syncthreads();
+    scan_tiles<DK, DELTA>(sm, 0, tid);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -199,8 +569,6 @@ chunk_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     uint32_t phase = 0;
     bool ok = true;
 
-    // Every thread waits; the give-up decision is made block-wide so that all
-    // threads leave the loop together.
     auto mma_wait = [&]() {
         const bool mine = mbar_wait(bar, phase & 1);
         ++phase;
@@ -208,316 +576,86 @@ chunk_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         tc_fence_after();
     };
 
-    const int nblocks = (T + C - 1) / C;
-    for (int blk = 0; blk < nblocks && ok; ++blk) {
+    const uint32_t id32 = idesc_bf16_f32(128, DVS);
+    for (int blk = 0; blk < nblk && ok; ++blk) {
+        const int buf = blk & 1;
         const int t0 = blk * C;
         const int n = min(C, T - t0);
-        const int buf = blk & 1;
-        uint8_t *QK = sm + L::QK + buf * L::QK_BYTES;
-        const bf16 *Vraw = reinterpret_cast<const bf16 *>(sm + L::VRAW + buf * 4096);
-        const float *ab = reinterpret_cast<const float *>(sm + L::AB + buf * 512);
+        const uint32_t wq = smem_u32(sm + L::WQ + buf * L::WQ_BYTES);
+        const uint32_t tzp = smem_u32(sm + L::TZP + buf * 24576);
+        const uint32_t ktt = smem_u32(sm + L::KTT + buf * 16384);
+        const uint32_t vbt = smem_u32(sm + L::VBT + buf * 4096);
+        const float *vec = reinterpret_cast<const float *>(sm + L::VEC + buf * 1024);
 
-        cp_async_wait_all();
-        __syncthreads();
-        if (blk + 1 < nblocks)
-            prefetch_block<DK>(sm, buf ^ 1, q, k, v, alpha, beta, bh, T, t0 + C, dv, c0, tid);
-
-        // ---- gate products in log space: G = cumsum(ln alpha) over the block
-        if (warp == 0) {
-            float x0 = 0.f, x1 = 0.f;
-            if (ALPHA) {
-                x0 = (2 * lane < n) ? logf(ab[2 * lane]) : 0.f;
-                x1 = (2 * lane + 1 < n) ? logf(ab[2 * lane + 1]) : 0.f;
-            }
-            const float pair = x0 + x1;
-            float incl = pair;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, incl, d);
-                if (lane >= d) incl += y;
-            }
-            const float e = incl - pair;
-            Gv[2 * lane] = e + x0;
-            Gv[2 * lane + 1] = e + pair;
-        }
-        __syncthreads();
-        if (tid < C) {
-            const float G = Gv[tid];
-            const float b = (DELTA && tid < n) ? ab[64 + tid] : 0.f;
-            const float g = ALPHA ? expf(G) : 1.f;
-            gv[tid] = g;
-            kdv[tid] = ALPHA ? expf(Gv[C - 1] - G) : 1.f;
-            bgv[tid] = b * g;
-            bv[tid] = b;
-        }
-        __syncthreads();
-
-        // ---- operand tiles that need no MMA result
-        // g * Q -> rows 64..127 of WQ (same swizzle phase as the Q rows of QK)
-        for (int idx = tid; idx < C * (DK / 8); idx += NT) {
-            const int r = idx / (DK / 8), ch = idx % (DK / 8);
-            const uint4 raw = *reinterpret_cast<const uint4 *>(QK + sw128_offset(r, ch * 8, 128));
-            const float g = gv[r];
-            const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
-            uint4 outv;
-            outv.x = pack_bf16(g * __bfloat162float(e[0]), g * __bfloat162float(e[1]));
-            outv.y = pack_bf16(g * __bfloat162float(e[2]), g * __bfloat162float(e[3]));
-            outv.z = pack_bf16(g * __bfloat162float(e[4]), g * __bfloat162float(e[5]));
-            outv.w = pack_bf16(g * __bfloat162float(e[6]), g * __bfloat162float(e[7]));
-            *reinterpret_cast<uint4 *>(WQ + sw128_offset(64 + r, ch * 8, 128)) = outv;
-        }
-        // (kd K)^T and, with delta, (beta g K)^T: thread j builds row j
-        if (tid < DK) {
-            const int j = tid;
-#pragma unroll
-            for (int i8 = 0; i8 < C / 8; ++i8) {
-                float kv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    kv[e] = bf16_at(QK, sw128_offset(64 + i8 * 8 + e, j, 128));
-                uint4 a;
-                a.x = pack_bf16(kdv[i8 * 8 + 0] * kv[0], kdv[i8 * 8 + 1] * kv[1]);
-                a.y = pack_bf16(kdv[i8 * 8 + 2] * kv[2], kdv[i8 * 8 + 3] * kv[3]);
-                a.z = pack_bf16(kdv[i8 * 8 + 4] * kv[4], kdv[i8 * 8 + 5] * kv[5]);
-                a.w = pack_bf16(kdv[i8 * 8 + 6] * kv[6], kdv[i8 * 8 + 7] * kv[7]);
-                *reinterpret_cast<uint4 *>(KTT + sw128_offset(j, i8 * 8, 128)) = a;
-                if (DELTA) {
-                    uint4 b;
-                    b.x = pack_bf16(bgv[i8 * 8 + 0] * kv[0], bgv[i8 * 8 + 1] * kv[1]);
-                    b.y = pack_bf16(bgv[i8 * 8 + 2] * kv[2], bgv[i8 * 8 + 3] * kv[3]);
-                    b.z = pack_bf16(bgv[i8 * 8 + 4] * kv[4], bgv[i8 * 8 + 5] * kv[5]);
-                    b.w = pack_bf16(bgv[i8 * 8 + 6] * kv[6], bgv[i8 * 8 + 7] * kv[7]);
-                    *reinterpret_cast<uint4 *>(KBT + sw128_offset(j, i8 * 8, DK < 8 ? 8 : DK)) = b;
-                }
-            }
-        }
-        // (beta V)^T with delta, V^T without: row c of a [32][64] tile
-        {
-            const int c = tid & 31, part = tid >> 5;  // 4 parts of 16 tokens
-#pragma unroll
-            for (int i8 = 0; i8 < 2; ++i8) {
-                const int i0 = part * 16 + i8 * 8;
-                float vv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float x = __bfloat162float(Vraw[(i0 + e) * DVS + c]);
-                    vv[e] = DELTA ? bv[i0 + e] * x : x;
-                }
-                uint4 a;
-                a.x = pack_bf16(vv[0], vv[1]);
-                a.y = pack_bf16(vv[2], vv[3]);
-                a.z = pack_bf16(vv[4], vv[5]);
-                a.w = pack_bf16(vv[6], vv[7]);
-                *reinterpret_cast<uint4 *>((DELTA ? VBT : XB) + sw128_offset(c, i0, 32)) = a;
-                if (!DELTA) *reinterpret_cast<uint4 *>(UB + sw128_offset(c, i0, 32)) = a;
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-
-        // ---- E1: [Q; K] K^T -> R1
+        // ---- G1: R3 = [T; 0] (beta V)^T + [-W; gQ] S^T   (without delta: [0; gQ] S^T,
+        //      and the state update and the P V part of the output go with it)
         if (tid == 0) {
-            const uint32_t id = idesc_bf16_f32(128, 64);
+            if (DELTA) {
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks)
+                    mma_bf16(tmem + kR3, tile_desc(tzp, 192, 0, ks), tile_desc(vbt, 32, 0, ks), id32,
+                             ks > 0);
+            }
 #pragma unroll
             for (int ks = 0; ks < DK / 16; ++ks)
-                mma_bf16(tmem + kR1, tile_desc(smem_u32(QK), 128, 0, ks),
-                         tile_desc(smem_u32(QK), 128, 64, ks), id, ks > 0);
-            mma_commit(bar);
-        }
-        mma_wait();
-        if (!ok) break;
-
-        // ---- E2: decay-masked scores P (bf16, rows 64..127 of TP) and couplings A (fp32)
-        {
-            const int r = 32 * (warp & 1) + lane;  // token of this row
-            const bool is_q = warp < 2;
-            float a[32];
-            const float Gr = Gv[r];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                tmem_ld32(tmem + lane_base + kR1 + 32 * half, a);
-                tmem_ld_wait();
-                if (is_q) {
-#pragma unroll
-                    for (int i8 = 0; i8 < 4; ++i8) {
-                        float p[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int i = half * 32 + i8 * 8 + e;
-                            p[e] = (i <= r) ? a[i8 * 8 + e] * (ALPHA ? expf(Gr - Gv[i]) : 1.f) : 0.f;
-                        }
-                        uint4 w4;
-                        w4.x = pack_bf16(p[0], p[1]);
-                        w4.y = pack_bf16(p[2], p[3]);
-                        w4.z = pack_bf16(p[4], p[5]);
-                        w4.w = pack_bf16(p[6], p[7]);
-                        *reinterpret_cast<uint4 *>(TP + sw128_offset(64 + r, half * 32 + i8 * 8, 128)) = w4;
-                    }
-                } else if (DELTA) {
-                    const float br = bv[r];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int i = half * 32 + e;
-                        Am[r * AP + i] = (i < r) ? br * a[e] * (ALPHA ? expf(Gr - Gv[i]) : 1.f) : 0.f;
-                    }
-                }
-            }
-        }
-        tc_fence_before();
-        __syncthreads();
-
-        if (DELTA) {
-            // ---- T = (I + A)^-1: diagonal 16x16 blocks by forward substitution
-            if (tid < 64) {
-                const int b = tid >> 4, c = tid & 15;
-                float x[16];
-#pragma unroll
-                for (int rr = 0; rr < 16; ++rr) {
-                    float s = (rr == c) ? 1.f : 0.f;
-#pragma unroll
-                    for (int i = 0; i < rr; ++i) s -= Am[(16 * b + rr) * AP + 16 * b + i] * x[i];
-                    x[rr] = s;
-                }
-#pragma unroll
-                for (int rr = 0; rr < 16; ++rr) Tm[(16 * b + rr) * AP + 16 * b + c] = x[rr];
-            }
-            __syncthreads();
-            // off-diagonal blocks, one block row at a time:
-            //   X = A[rows b, cols < 16b] T[< 16b, < 16b];  T[rows b, < 16b] = -T_bb X
-            for (int b = 1; b < 4; ++b) {
-                const int ncol = 16 * b;
-                for (int idx = tid; idx < 16 * ncol; idx += NT) {
-                    const int rr = idx / ncol, col = idx % ncol;
-                    float s = 0.f;
-                    for (int i = col; i < ncol; ++i) s += Am[(16 * b + rr) * AP + i] * Tm[i * AP + col];
-                    Xt[rr * 49 + col] = s;
-                }
-                __syncthreads();
-                for (int idx = tid; idx < 16 * ncol; idx += NT) {
-                    const int rr = idx / ncol, col = idx % ncol;
-                    float s = 0.f;
-                    for (int i = 0; i <= rr; ++i) s += Tm[(16 * b + rr) * AP + 16 * b + i] * Xt[i * 49 + col];
-                    Tm[(16 * b + rr) * AP + col] = -s;
-                }
-                __syncthreads();
-            }
-            // T (lower triangle, bf16) -> rows 0..63 of TP
-            for (int idx = tid; idx < C * 8; idx += NT) {
-                const int r = idx >> 3, i8 = idx & 7;
-                float t[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int i = i8 * 8 + e;
-                    t[e] = (i <= r) ? Tm[r * AP + i] : 0.f;
-                }
-                uint4 w4;
-                w4.x = pack_bf16(t[0], t[1]);
-                w4.y = pack_bf16(t[2], t[3]);
-                w4.z = pack_bf16(t[4], t[5]);
-                w4.w = pack_bf16(t[6], t[7]);
-                *reinterpret_cast<uint4 *>(TP + sw128_offset(r, i8 * 8, 128)) = w4;
-            }
-            fence_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
-
-            // ---- E3: [T; P] (beta g K)^T -> R2 (rows 0..63 = W);  [T; P] (beta V)^T -> R3
-            if (tid == 0) {
-                const uint32_t idw = idesc_bf16_f32(128, DK);
-                const uint32_t idu = idesc_bf16_f32(128, DVS);
+                mma_bf16(tmem + kR3, tile_desc(wq, 128, 0, ks), tile_desc(smem_u32(SB), 32, 0, ks),
+                         id32, (DELTA || ks > 0) ? 1u : 0u);
+            if (!DELTA) {
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks) {
-                    const uint64_t ad = tile_desc(smem_u32(TP), 128, 0, ks);
-                    mma_bf16(tmem + kR2, ad, tile_desc(smem_u32(KBT), DK < 8 ? 8 : DK, 0, ks), idw, ks > 0);
-                    mma_bf16(tmem + kR3, ad, tile_desc(smem_u32(VBT), 32, 0, ks), idu, ks > 0);
-                }
-                mma_commit(bar);
-            }
-            mma_wait();
-            if (!ok) break;
-
-            // ---- E4: -W -> rows 0..63 of WQ
-            if (warp < 2) {
-                const int r = 32 * warp + lane;
-#pragma unroll
-                for (int cb = 0; cb < (DK + 31) / 32; ++cb) {
-                    float w[32];
-                    tmem_ld32(tmem + lane_base + kR2 + 32 * cb, w);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i8 = 0; i8 < 4; ++i8) {
-                        uint4 w4;
-                        w4.x = pack_bf16(-w[i8 * 8 + 0], -w[i8 * 8 + 1]);
-                        w4.y = pack_bf16(-w[i8 * 8 + 2], -w[i8 * 8 + 3]);
-                        w4.z = pack_bf16(-w[i8 * 8 + 4], -w[i8 * 8 + 5]);
-                        w4.w = pack_bf16(-w[i8 * 8 + 6], -w[i8 * 8 + 7]);
-                        *reinterpret_cast<uint4 *>(WQ + sw128_offset(r, cb * 32 + i8 * 8, 128)) = w4;
-                    }
+                    mma_bf16(tmem + kR4, tile_desc(ktt, 128, 0, ks), tile_desc(vbt, 32, 0, ks), id32,
+                             ks > 0);
+                    mma_bf16(tmem + kR3, tile_desc(tzp, 192, 64, ks), tile_desc(vbt, 32, 0, ks),
+                             id32, 1u);
                 }
             }
-            fence_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
-        }
-
-        // ---- S1: [-W; g Q] S^T (+)= R3
-        if (tid == 0) {
-            const uint32_t id = idesc_bf16_f32(128, DVS);
-#pragma unroll
-            for (int ks = 0; ks < DK / 16; ++ks)
-                mma_bf16(tmem + kR3, tile_desc(smem_u32(WQ), 128, 0, ks),
-                         tile_desc(smem_u32(SB), 32, 0, ks), id, DELTA ? 1u : (ks > 0 ? 1u : 0u));
             mma_commit(bar);
+        }
+        // meanwhile: the next block's operand tiles
+        if (blk + 1 < nblk) {
+            cp_async_wait_all();
+            __syncthreads();
+            scan_tiles<DK, DELTA>(sm, buf ^ 1, tid);
+            fence_async_smem();
         }
         mma_wait();
         if (!ok) break;
 
         if (DELTA) {
-            // ---- S2: U^T and (U - beta V)^T from rows 0..63 of R3
+            // ---- U^T from rows 0..63 of R3
             if (warp < 2) {
                 const int i = 32 * warp + lane;
                 float u[32];
                 tmem_ld32(tmem + lane_base + kR3, u);
                 tmem_ld_wait();
-                const float b = bv[i];
 #pragma unroll
-                for (int c = 0; c < DVS; ++c) {
-                    st_bf16(UB, sw128_offset(c, i, 32), u[c]);
-                    const float x = __bfloat162float(Vraw[i * DVS + c]);
-                    st_bf16(XB, sw128_offset(c, i, 32), u[c] - b * x);
-                }
+                for (int c = 0; c < DVS; ++c) st_bf16(UB, sw128_offset(c, i, 32), u[c]);
             }
             fence_async_smem();
             tc_fence_before();
             __syncthreads();
             tc_fence_after();
-        }
-
-        // ---- S3: (kd K)^T U -> R4;  [T; P] (U - beta V)^T += R3
-        if (tid == 0) {
-            const uint32_t id = idesc_bf16_f32(128, DVS);
+            // ---- G2: R4 = (kd K)^T U;  R3 += [0; P] U
+            if (tid == 0) {
 #pragma unroll
-            for (int ks = 0; ks < C / 16; ++ks) {
-                mma_bf16(tmem + kR4, tile_desc(smem_u32(KTT), 128, 0, ks),
-                         tile_desc(smem_u32(UB), 32, 0, ks), id, ks > 0);
-                mma_bf16(tmem + kR3, tile_desc(smem_u32(TP), 128, 0, ks),
-                         tile_desc(smem_u32(XB), 32, 0, ks), id, 1u);
+                for (int ks = 0; ks < C / 16; ++ks) {
+                    mma_bf16(tmem + kR4, tile_desc(ktt, 128, 0, ks), tile_desc(smem_u32(UB), 32, 0, ks),
+                             id32, ks > 0);
+                    mma_bf16(tmem + kR3, tile_desc(tzp, 192, 64, ks),
+                             tile_desc(smem_u32(UB), 32, 0, ks), id32, 1u);
+                }
+                mma_commit(bar);
             }
-            mma_commit(bar);
+            mma_wait();
+            if (!ok) break;
         }
-        mma_wait();
-        if (!ok) break;
 
-        // ---- S4: S <- g_C S + Delta S (registers, bf16 copy to SB); O out
+        // ---- state S <- g_C S + Delta S (registers; bf16 copy to SB); O out
         {
             float d[32];
             tmem_ld32(tmem + lane_base + kR4, d);
             tmem_ld_wait();
-            const float gC = gv[C - 1];
+            const float gC = vec[64 + C - 1];
             if (tid < DK) {
 #pragma unroll
                 for (int c = 0; c < DVS; ++c) {
@@ -533,14 +671,7 @@ chunk_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                 if (r < n) {
                     uint4 *dst = reinterpret_cast<uint4 *>(o + (bh * T + t0 + r) * dv + c0);
 #pragma unroll
-                    for (int i8 = 0; i8 < 4; ++i8) {
-                        uint4 w4;
-                        w4.x = pack_bf16(ov[i8 * 8 + 0], ov[i8 * 8 + 1]);
-                        w4.y = pack_bf16(ov[i8 * 8 + 2], ov[i8 * 8 + 3]);
-                        w4.z = pack_bf16(ov[i8 * 8 + 4], ov[i8 * 8 + 5]);
-                        w4.w = pack_bf16(ov[i8 * 8 + 6], ov[i8 * 8 + 7]);
-                        dst[i8] = w4;
-                    }
+                    for (int i8 = 0; i8 < 4; ++i8) dst[i8] = pack8(ov + i8 * 8);
                 }
             }
         }
@@ -548,11 +679,12 @@ chunk_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        if (blk + 2 < nblk)
+            scan_fetch<DK, DELTA>(sm, buf, q, k, v, recs + (size_t)(blk + 2) * R::BYTES, bh, T,
+                                  blk + 2, dv, c0, tid);
     }
 
-    if (!ok) {
-        if (lane == 0) atomicExch(&g_tc_error, 1);
-    }
+    if (!ok && lane == 0) atomicExch(&g_tc_error, 1);
     cp_async_wait_all();
     if (ok && tid < DK) {
 #pragma unroll
@@ -560,58 +692,75 @@ chunk_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 0) tmem_dealloc(tmem, kScanCols);
 }
+
+// ================================================================== launch
 
 template <int DK, bool ALPHA, bool DELTA>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *alpha,
                          const float *beta, const float *S0, void *o, float *S_T, int B, int H,
-                         int T, int dv, cudaStream_t stream, int slot) {
-    auto fn = chunk_tc_kernel<DK, ALPHA, DELTA>;
-    const int bytes = TcLayout<DK>::ALLOC;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(fn), bytes, slot);
+                         int T, int dv, void *ws, cudaStream_t stream, int slot) {
+    const int nblk = (T + C - 1) / C;
+    auto prep = chunk_prep_kernel<DK, ALPHA, DELTA>;
+    auto scan = chunk_scan_kernel<DK, ALPHA, DELTA>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(prep), PrepLayout<DK>::ALLOC,
+                                     slot);
     if (e != cudaSuccess) return e;
-    dim3 grid(dv / DVS, H, B);
-    fn<<<grid, NT, bytes, stream>>>(static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
-                                    static_cast<const bf16 *>(v), ALPHA ? alpha : nullptr,
-                                    DELTA ? beta : nullptr, S0, static_cast<bf16 *>(o), S_T, H,
-                                    T, dv);
+    e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC, slot + 12);
+    if (e != cudaSuccess) return e;
+    prep<<<dim3(nblk, H, B), NT, PrepLayout<DK>::ALLOC, stream>>>(
+        static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), ALPHA ? alpha : nullptr,
+        DELTA ? beta : nullptr, static_cast<uint8_t *>(ws), H, T, nblk);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    scan<<<dim3(dv / DVS, H, B), NT, ScanLayout<DK>::ALLOC, stream>>>(
+        static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), static_cast<const bf16 *>(v),
+        static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk);
     return cudaGetLastError();
 }
 
 template <int DK>
 cudaError_t launch_mode(const void *q, const void *k, const void *v, const float *alpha,
                         const float *beta, const float *S0, void *o, float *S_T, int B, int H,
-                        int T, int dv, lr_mode mode, cudaStream_t stream, int slot) {
+                        int T, int dv, lr_mode mode, void *ws, cudaStream_t stream, int slot) {
     switch (mode) {
     case LR_MODE_LINEAR:
-        return launch_typed<DK, false, false>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv,
+        return launch_typed<DK, false, false>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, ws,
                                               stream, slot + 0);
     case LR_MODE_DECAY:
-        return launch_typed<DK, true, false>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv,
+        return launch_typed<DK, true, false>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, ws,
                                              stream, slot + 1);
     case LR_MODE_DELTA:
-        return launch_typed<DK, false, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv,
+        return launch_typed<DK, false, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, ws,
                                              stream, slot + 2);
     default:
-        return launch_typed<DK, true, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv,
+        return launch_typed<DK, true, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, ws,
                                             stream, slot + 3);
     }
 }
 
 }  // namespace
 
-// Attribute slots 32..43 belong to this file.
+size_t chunked_tc_workspace_bytes(int B, int H, int T, int dk) {
+    const size_t nblk = (size_t)((T + C - 1) / C);
+    const size_t rec = dk == 32 ? Rec<32>::BYTES : dk == 64 ? Rec<64>::BYTES : Rec<128>::BYTES;
+    return (size_t)B * H * nblk * rec;
+}
+
+// Attribute slots 32..55 belong to this file.
 cudaError_t launch_chunked_tc(const void *q, const void *k, const void *v, const float *alpha,
                               const float *beta, const float *S0, void *o, float *S_T, int B,
-                              int H, int T, int dk, int dv, lr_mode mode, cudaStream_t stream) {
+                              int H, int T, int dk, int dv, lr_mode mode, void *ws,
+                              cudaStream_t stream) {
     switch (dk) {
     case 32:
-        return launch_mode<32>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, stream, 32);
+        return launch_mode<32>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, ws, stream, 32);
     case 64:
-        return launch_mode<64>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, stream, 36);
+        return launch_mode<64>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, ws, stream, 36);
     default:
-        return launch_mode<128>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, stream, 40);
+        return launch_mode<128>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, ws, stream,
+                                40);
     }
 }
 

@@ -86,25 +86,43 @@ const char *lr_status_string(lr_status s) {
     case LR_ERR_CUDA: return "CUDA runtime error at launch";
     case LR_ERR_ALIAS: return "an output overlaps an input";
     case LR_ERR_TIMEOUT: return "a kernel gave up a bounded wait; its outputs are incomplete";
+    case LR_ERR_WORKSPACE: return "workspace is NULL or smaller than lr_fwd_chunked_workspace_size";
     }
     return "unknown status";
 }
 
-lr_status lr_fwd_chunked(const void *q, const void *k, const void *v, const float *alpha,
-                         const float *beta, const float *S0, void *o, float *S_T, int B, int H,
-                         int T, int dk, int dv, int chunk, lr_dtype dt, lr_mode mode,
-                         cudaStream_t stream) {
+static lr_status check_chunked_shape(int B, int H, int T, int dk, int dv, int chunk, lr_dtype dt,
+                                     lr_mode mode) {
     if (mode < LR_MODE_LINEAR || mode > LR_MODE_GATED_DELTA) return LR_ERR_MODE;
     if (dt != LR_DT_F32 && dt != LR_DT_BF16) return LR_ERR_DTYPE;
     if (B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1 || chunk < 1) return LR_ERR_SHAPE;
     if (!count_ok(B, H, T, dk > dv ? dk : dv) || !count_ok(B, H, dv, dk)) return LR_ERR_SHAPE;
     if (!supported_dim(dk) || !supported_dim(dv) || chunk != 64) return LR_ERR_UNSUPPORTED;
+    return LR_OK;
+}
+
+size_t lr_fwd_chunked_workspace_size(int B, int H, int T, int dk, int dv, int chunk, lr_dtype dt,
+                                     lr_mode mode) {
+    if (check_chunked_shape(B, H, T, dk, dv, chunk, dt, mode) != LR_OK) return 0;
+    if (dt != LR_DT_BF16 || T == 0) return 0;
+    return chunked_tc_workspace_bytes(B, H, T, dk);
+}
+
+lr_status lr_fwd_chunked(const void *q, const void *k, const void *v, const float *alpha,
+                         const float *beta, const float *S0, void *o, float *S_T, int B, int H,
+                         int T, int dk, int dv, int chunk, lr_dtype dt, lr_mode mode,
+                         void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    const lr_status shape = check_chunked_shape(B, H, T, dk, dv, chunk, dt, mode);
+    if (shape != LR_OK) return shape;
     if (!S_T) return LR_ERR_NULL;
     if (T > 0 && (!q || !k || !v || !o)) return LR_ERR_NULL;
     if (T > 0 && uses_alpha(mode) && !alpha) return LR_ERR_NULL;
     if (T > 0 && uses_beta(mode) && !beta) return LR_ERR_NULL;
+    const size_t need = lr_fwd_chunked_workspace_size(B, H, T, dk, dv, chunk, dt, mode);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return LR_ERR_WORKSPACE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) ||
-        !aligned16(beta) || !aligned16(S0) || !aligned16(o) || !aligned16(S_T))
+        !aligned16(beta) || !aligned16(S0) || !aligned16(o) || !aligned16(S_T) ||
+        (need > 0 && !aligned16(workspace)))
         return LR_ERR_ALIGN;
 
     const size_t es = dt == LR_DT_F32 ? 4 : 2;
@@ -121,6 +139,9 @@ lr_status lr_fwd_chunked(const void *q, const void *k, const void *v, const floa
     for (Span in : {sq, sk, sv, sa, sb})
         if (overlap(st, in)) return LR_ERR_ALIAS;
     if (S0 && S0 != S_T && overlap(s0, st)) return LR_ERR_ALIAS;
+    const Span sw = span(need > 0 ? workspace : nullptr, need);
+    for (Span other : {sq, sk, sv, sa, sb, s0, so, st})
+        if (overlap(sw, other)) return LR_ERR_ALIAS;
 
     cudaError_t e;
     if (T == 0) {
@@ -131,7 +152,8 @@ lr_status lr_fwd_chunked(const void *q, const void *k, const void *v, const floa
         e = cudaGetLastError();
     } else {
         e = dt == LR_DT_BF16
-                ? launch_chunked_tc(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, mode, stream)
+                ? launch_chunked_tc(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, mode,
+                                    workspace, stream)
                 : launch_chunked_simt(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, dt, mode,
                                       stream);
     }

@@ -66,7 +66,10 @@ cudaError_t launch_chunked_simt(const void *q, const void *k, const void *v, con
 // Chunked forward on the tensor cores, bf16 (chunked_tc.cu).
 cudaError_t launch_chunked_tc(const void *q, const void *k, const void *v, const float *alpha,
                               const float *beta, const float *S0, void *o, float *S_T, int B,
-                              int H, int T, int dk, int dv, lr_mode mode, cudaStream_t stream);
+                              int H, int T, int dk, int dv, lr_mode mode, void *ws,
+                              cudaStream_t stream);
+// Workspace bytes the tensor-core path needs.
+size_t chunked_tc_workspace_bytes(int B, int H, int T, int dk);
 
 // Returns and clears the tensor-core kernel's bounded-wait error word
 // (1 if set, 0 if clear, -1 if the device could not be read).

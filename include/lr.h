@@ -34,6 +34,7 @@
 #ifndef LR_H_
 #define LR_H_
 
+#include <stddef.h>
 #include <cuda_runtime_api.h>
 
 #ifdef __cplusplus
@@ -52,7 +53,8 @@ typedef enum {
                                {32, 64, 128}, or chunk != 64                       */
     LR_ERR_CUDA = 7,        /* the CUDA runtime reported an error at launch        */
     LR_ERR_ALIAS = 8,       /* an output overlaps an input it must not overlap     */
-    LR_ERR_TIMEOUT = 9      /* a kernel gave up a bounded wait (see lr_device_status) */
+    LR_ERR_TIMEOUT = 9,     /* a kernel gave up a bounded wait (see lr_device_status) */
+    LR_ERR_WORKSPACE = 10   /* workspace NULL or smaller than lr_fwd_chunked_workspace_size */
 } lr_status;
 
 /* Which row of the family (summary table of the first page). */
@@ -105,6 +107,18 @@ typedef enum {
  *                          else
  *   B, H >= 1; T >= 0 (T == 0 copies S0, or zeros, to S_T);
  *   dk, dv in {32, 64, 128}; chunk == 64.
+ *   workspace       device scratch of at least
+ *                   lr_fwd_chunked_workspace_size(...) bytes, 16-byte aligned,
+ *                   owned by the caller and not overlapping any argument; its
+ *                   contents on entry do not matter and are undefined on exit.
+ *                   May be NULL when that size is 0.
+ *   workspace_bytes its size in bytes.
+ *
+ * The bf16 path runs two kernels on `stream`: a per-block pass over all
+ * blocks in parallel (gate products, decay-masked scores, the UT inverse of
+ * the delta rows and W = T diag(beta g) K), stored in the workspace, then the
+ * sequential pass over blocks that carries the state.  The fp32 path needs no
+ * workspace.  Calls that share a workspace must be ordered on one stream.
  *
  * q, k, v and o may be NULL when T == 0.
  */
@@ -112,7 +126,18 @@ lr_status lr_fwd_chunked(const void *q, const void *k, const void *v,
                          const float *alpha, const float *beta,
                          const float *S0, void *o, float *S_T,
                          int B, int H, int T, int dk, int dv, int chunk,
-                         lr_dtype dt, lr_mode mode, cudaStream_t stream);
+                         lr_dtype dt, lr_mode mode,
+                         void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/*
+ * Bytes of workspace lr_fwd_chunked needs for these arguments: 0 for the fp32
+ * path and for T == 0; for bf16, about 33 KB per (batch, head, 64-token
+ * block) at dk = 128.  Returns 0 as well for arguments lr_fwd_chunked would
+ * reject.
+ */
+size_t lr_fwd_chunked_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
+                                     lr_dtype dt, lr_mode mode);
 
 /*
  * One recurrent step for N independent sequences (decode).  Per (n, h) and

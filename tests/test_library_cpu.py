@@ -31,8 +31,9 @@ def _declared_functions():
 
 
 def test_header_declares_expected_entry_points():
-    assert set(_declared_functions()) == {"lr_fwd_chunked", "lr_step", "lr_device_status",
-                                          "lr_status_string", "lr_abi_version"}
+    assert set(_declared_functions()) == {"lr_fwd_chunked", "lr_fwd_chunked_workspace_size",
+                                          "lr_step", "lr_device_status", "lr_status_string",
+                                          "lr_abi_version"}
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -47,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings_and_version(lib):
     import gated_delta_rule_fwd_gb300 as lr
     assert lib.lr_abi_version() == 1
-    for code in range(10):
+    for code in range(11):
         s = lr.status_string(code)
         assert s and s != "unknown status"
     assert lr.status_string(99) == "unknown status"
@@ -65,17 +66,18 @@ sys.path.insert(0, sys.argv[1])
 import gated_delta_rule_fwd_gb300 as lr
 L = lr.lib()
 P = lambda a: ctypes.c_void_p(a)
-A = [0x10000000 + i * 0x10000000 for i in range(8)]   # distinct, aligned, never dereferenced
-q, k, v, al, be, s0, o, st = (P(a) for a in A)
+A = [0x10000000 + i * 0x10000000 for i in range(9)]   # distinct, aligned, never dereferenced
+q, k, v, al, be, s0, o, st, ws = (P(a) for a in A)
 S = None
 def chunk(**kw):
     args = dict(q=q, k=k, v=v, al=al, be=be, s0=s0, o=o, st=st, B=1, H=1, T=8, dk=32, dv=32,
-                chunk=64, dt=0, mode=3)
+                chunk=64, dt=0, mode=3, ws=ws, wsb=1 << 24)
     args.update(kw)
     a = args
     return L.lr_fwd_chunked(a['q'], a['k'], a['v'], a['al'], a['be'], a['s0'], a['o'], a['st'],
                             a['B'], a['H'], a['T'], a['dk'], a['dv'], a['chunk'], a['dt'],
-                            a['mode'], None)
+                            a['mode'], a['ws'], a['wsb'], None)
+need = L.lr_fwd_chunked_workspace_size(1, 1, 8, 32, 32, 64, 1, 3)
 def step(**kw):
     args = dict(q=q, k=k, v=v, al=al, be=be, s=s0, o=o, N=1, H=1, dk=32, dv=32, dt=1, mode=3)
     args.update(kw)
@@ -93,6 +95,12 @@ cases = [
     ("misaligned", chunk(k=P(A[1] + 8)), 4),
     ("alias-o-q", chunk(o=q), 8), ("alias-st-k", chunk(st=k), 8),
     ("alias-st-partial-s0", chunk(st=P(A[5] + 16)), 8),
+    ("ws-null", chunk(dt=1, ws=None), 10), ("ws-small", chunk(dt=1, wsb=need - 16), 10),
+    ("ws-misaligned", chunk(dt=1, ws=P(A[8] + 8)), 4), ("ws-alias-o", chunk(dt=1, ws=o), 8),
+    ("ws-size-f32", L.lr_fwd_chunked_workspace_size(1, 1, 8, 32, 32, 64, 0, 3), 0),
+    ("ws-size-T0", L.lr_fwd_chunked_workspace_size(1, 1, 0, 32, 32, 64, 1, 3), 0),
+    ("ws-size-bad", L.lr_fwd_chunked_workspace_size(1, 1, 8, 48, 32, 64, 1, 3), 0),
+    ("ws-size-bf16-positive", int(need > 0), 1),
     ("step-mode", step(mode=9), 5), ("step-dtype", step(dt=3), 3), ("step-N0", step(N=0), 2),
     ("step-dk16", step(dk=16), 6), ("step-nullS", step(s=None), 1),
     ("step-nullalpha", step(al=None), 1), ("step-misaligned", step(v=P(A[2] + 4)), 4),

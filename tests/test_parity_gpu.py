@@ -211,3 +211,23 @@ def test_binding_rejects_bad_tensors(dev):
     with pytest.raises(lr.LrError) as e:
         lr.lr_fwd_chunked(x["q"], x["k"], x["v"], x["alpha"], x["beta"], o=x["v"])
     assert e.value.status == 8
+    need = lr.workspace_size(1, 2, 10, 64, 64, torch.bfloat16)
+    assert need > 0 and lr.workspace_size(1, 2, 10, 64, 64, torch.float32) == 0
+    small = torch.empty(need - 16, dtype=torch.uint8, device=dev)
+    with pytest.raises(lr.LrError) as e:
+        lr.lr_fwd_chunked(x["q"], x["k"], x["v"], x["alpha"], x["beta"], workspace=small)
+    assert e.value.status == 10
+
+
+def test_workspace_reuse_across_calls(dev):
+    """One workspace serves successive calls of different sizes on a stream."""
+    ws = torch.empty(lr.workspace_size(2, 2, 300, 128, 128, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+    for T, seed in ((300, 1), (77, 2), (300, 3)):
+        x = workloads.draw("gdn", 2, 2, T, 128, 128, seed=seed, dtype=torch.bfloat16, s0_std=0.1)
+        d = to_dev(x, dev)
+        o, st = lr.lr_fwd_chunked(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["S0"],
+                                  workspace=ws)
+        torch.cuda.synchronize()
+        o_ref, s_ref = ref_chunked(x, lr.GATED_DELTA)
+        assert rel_err(o, o_ref) <= 2e-2 and rel_err(st, s_ref) <= 2e-2
