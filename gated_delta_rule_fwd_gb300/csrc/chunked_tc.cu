@@ -35,14 +35,21 @@
 // operands are stacked to fill M:
 //   prep  E1  [Q; K] K^T            -> [Q K^T ; K K^T]
 //         E3  [T; 0] (beta g K)^T   -> [W ; 0]
-//   scan  G1  [T; 0] (beta V)^T     -> [Ut ; 0]           (R3)
-//             [-W; g Q] S^T        +=  [U ; g Q S^T]     (R3)
-//         G2  (kd K)^T U           ->  Delta S^T          (R4)
-//             [0; P] U             +=  rows 64..127 = O   (R3)
+//   scan      [T diag(beta); 0] V  -> [Ut ; 0]
+//             [-W; Q] S^T          -> [-W S^T ; Q S^T]    (two K halves)
+//             K^T (kd U)           -> Delta S^T           (K read MN-major)
+//             [0; P] U             -> rows 64..127 = P U
+//   with U = Ut - W S^T and O = diag(g) Q S^T + P U formed in the epilogues.
 // The fp32 master copy of the state slice lives in registers (thread j owns
 // column j); a bf16 copy in shared memory feeds the next block.  A final
 // short block is zero-filled (alpha treated as 1, beta as 0), which leaves
 // the real tokens' results unchanged.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "lr_internal.cuh"
 #include "tc_common.cuh"
 
@@ -115,12 +122,11 @@ template <int DK>
 struct PrepLayout {
     static constexpr int KB = (DK + 63) / 64;
     static constexpr int QK = 0;                            // [128 rows][DK]: Q rows, K rows
-    static constexpr int TZ = QK + 128 * 128 * KB;          // [128][64]: T rows, zero rows
-    static constexpr int KBT = TZ + 16384;                  // [DK][64]: (beta g K)^T
-    static constexpr int AM = KBT + ((DK * 128 + 1023) / 1024) * 1024;  // fp32 [64][AP]
+    static constexpr int TZ = QK + 128 * 128 * KB;          // [128][64]: T diag(beta) rows, 0 rows
+    static constexpr int AM = TZ + 16384;                   // fp32 [64][AP]
     static constexpr int TM = AM + C * AP * 4;              // fp32 [64][AP]
     static constexpr int XT = TM + C * AP * 4;              // fp32 [16][XP]
-    static constexpr int VEC = XT + 16 * XP * 4;            // G, ginv, g, kd, bg, b
+    static constexpr int VEC = XT + 16 * XP * 4;            // G, ginv, g, kd, -, b
     static constexpr int BAR = VEC + 6 * 64 * 4;
     static constexpr int BYTES = BAR + 64;
     static constexpr int ALLOC = BYTES + 1024;
@@ -202,12 +208,12 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     const int n = min(C, T - t0);
     uint8_t *rec = ws + (bh * nblk + blk) * (size_t)R::BYTES;
 
-    uint8_t *QK = sm + L::QK, *TZ = sm + L::TZ, *KBT = sm + L::KBT;
+    uint8_t *QK = sm + L::QK, *TZ = sm + L::TZ;
     float *Am = reinterpret_cast<float *>(sm + L::AM);
     float *Tm = reinterpret_cast<float *>(sm + L::TM);
     float *Xt = reinterpret_cast<float *>(sm + L::XT);
     float *Gv = reinterpret_cast<float *>(sm + L::VEC);
-    float *giv = Gv + 64, *gv = Gv + 128, *kdv = Gv + 192, *bgv = Gv + 256, *bv = Gv + 320;
+    float *giv = Gv + 64, *gv = Gv + 128, *bv = Gv + 320;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8);
 
@@ -223,7 +229,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     }
     cp_async_commit();
     if (DELTA) {
-        // zero rows 64..127 of [T; 0] and the upper blocks of Tm
+        // zero rows 64..127 of [T diag(beta); 0] and the upper blocks of Tm
         for (int i = tid; i < 8192 / 16; i += NT)
             reinterpret_cast<uint4 *>(TZ + 8192)[i] = make_uint4(0, 0, 0, 0);
         for (int i = tid; i < C * AP; i += NT) Tm[i] = 0.f;
@@ -263,8 +269,6 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         const float g = ALPHA ? __expf(G) : 1.f;
         gv[tid] = g;
         giv[tid] = ALPHA ? __expf(-G) : 1.f;
-        kdv[tid] = ALPHA ? __expf(Gv[C - 1] - G) : 1.f;
-        bgv[tid] = b * g;
         bv[tid] = b;
         float *vec = reinterpret_cast<float *>(rec + R::VEC);
         vec[tid] = G;
@@ -273,20 +277,6 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         vec[192 + tid] = b;
     }
     cp_async_wait_all();
-    __syncthreads();
-
-    // ---- (beta g K)^T for W: thread j builds row j
-    if (DELTA && tid < DK) {
-        const int j = tid;
-#pragma unroll
-        for (int i8 = 0; i8 < C / 8; ++i8) {
-            float w8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                w8[e] = bgv[i8 * 8 + e] * bf16_at(QK, sw128_offset(64 + i8 * 8 + e, j, 128));
-            *reinterpret_cast<uint4 *>(KBT + sw128_offset(j, i8 * 8, DK)) = pack8(w8);
-        }
-    }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -307,7 +297,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     ok = __syncthreads_and(mbar_wait(bar, 0) ? 1 : 0) != 0;
     tc_fence_after();
 
-    // ---- E2: P rows (bf16 tile to the workspace), A rows (fp32)
+    // ---- E2: P rows (bf16 tile to the workspace), A rows (fp32); then g K in place
     if (ok) {
         const int r = 32 * (warp & 1) + lane;
         const bool is_q = warp < 2;
@@ -335,17 +325,30 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                 for (int e = 0; e < 32; ++e) Am[r * AP + half * 32 + e] = br * a[e];
             }
         }
+        if (DELTA) {
+            // K rows of QK scaled by g (B operand of W, read MN-major)
+            for (int idx = tid; idx < C * (DK / 8); idx += NT) {
+                const int r2 = idx / (DK / 8), ch = idx % (DK / 8);
+                uint4 *p = reinterpret_cast<uint4 *>(QK + sw128_offset(64 + r2, ch * 8, 128));
+                const uint4 raw = *p;
+                const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
+                float x[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) x[t] = gv[r2] * __bfloat162float(e[t]);
+                *p = pack8(x);
+            }
+        }
     }
     __syncthreads();
 
     if (DELTA && ok) {
         ut_inverse(Am, Tm, Xt, tid);
-        // T (bf16) -> rows 0..63 of [T; 0] and to the workspace
+        // T diag(beta) (bf16) -> rows 0..63 of [T diag(beta); 0] and to the workspace
         for (int idx = tid; idx < C * 8; idx += NT) {
             const int r = idx >> 3, i8 = idx & 7;
             float t[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) t[e] = Tm[r * AP + i8 * 8 + e];
+            for (int e = 0; e < 8; ++e) t[e] = Tm[r * AP + i8 * 8 + e] * bv[i8 * 8 + e];
             const uint4 w4 = pack8(t);
             const uint32_t off = sw128_offset(r, i8 * 8, 64);
             *reinterpret_cast<uint4 *>(TZ + off) = w4;
@@ -356,13 +359,13 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         __syncthreads();
         tc_fence_after();
 
-        // ---- E3: [T; 0] (beta g K)^T -> TMEM cols [64, 64 + DK)
+        // ---- E3: [T diag(beta); 0] (g K) -> TMEM cols [64, 64 + DK) = [W; 0]
         if (tid == 0) {
-            const uint32_t id = idesc_bf16_f32(128, DK);
+            const uint32_t id = idesc_bf16_f32_mn(128, DK, false, true);
 #pragma unroll
             for (int ks = 0; ks < C / 16; ++ks)
                 mma_bf16(tmem + 64, tile_desc(smem_u32(TZ), 128, 0, ks),
-                         tile_desc(smem_u32(KBT), DK, 0, ks), id, ks > 0);
+                         desc_mnmajor_sw128(smem_u32(QK) + 8192 + ks * 2048, 16384), id, ks > 0);
             mma_commit(bar);
         }
         ok = __syncthreads_and(mbar_wait(bar, 1) ? 1 : 0) != 0;
@@ -397,126 +400,153 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
 template <int DK>
 struct ScanLayout {
     static constexpr int KB = (DK + 63) / 64;
-    static constexpr int WQ_BYTES = 128 * 128 * KB;          // [128][DK]: -W rows, g Q rows
+    static constexpr int WQ_BYTES = 128 * 128 * KB;          // [128][DK] K-major: -W rows, g Q rows
     static constexpr int WQ = 0;                              // x2
-    static constexpr int TZP = WQ + 2 * WQ_BYTES;             // x2 [192][64]: T, 0, P rows
-    static constexpr int KR_BYTES = 64 * 128 * KB;            // raw K block [64][DK]
-    static constexpr int KR = TZP + 2 * 24576;                // x2
-    static constexpr int KTT = KR + 2 * KR_BYTES;             // x2 [128][64]: (kd K)^T
-    static constexpr int VBT = KTT + 2 * 16384;               // x2 [32][64]: (beta V)^T or V^T
-    static constexpr int VR = VBT + 2 * 4096;                 // x2 raw V slice [64][32]
-    static constexpr int VEC = VR + 2 * 4096;                 // x2 G, g, kd, beta
-    static constexpr int UB = VEC + 2 * 1024;                 // [32][64]: U^T
-    static constexpr int SB = UB + 4096;                      // [32][DK]: bf16 state slice
-    static constexpr int BAR = SB + 32 * 128 * KB;
-    static constexpr int BYTES = BAR + 64;
+    static constexpr int TZP = WQ + 2 * WQ_BYTES;             // x2 [192][64] K-major: T diag(beta), 0, P
+    static constexpr int KR = TZP + 2 * 24576;                // x2 [64 tokens][128] MN-major: kd K
+    static constexpr int VR = KR + 2 * 16384;                 // x2 [64 tokens][32] MN-major: V slice
+    static constexpr int VK = VR + 2 * 8192;                  // x2 [64 tokens][32] MN-major: kd V (no delta)
+    static constexpr int VEC = VK + 2 * 8192;                 // x2 G, g, kd, beta
+    static constexpr int UB = VEC + 2 * 1024;                 // [64 tokens][32] MN-major: U (or V)
+    static constexpr int UBK = UB + 8192;                     // [64 tokens][32] MN-major: kd U (or kd V)
+    static constexpr int SB = UBK + 8192;                     // [DK][32] MN-major: bf16 state slice^T
+    static constexpr int BAR = SB + 128 * 128;
+    static constexpr int BYTES = BAR + 256;
     static constexpr int ALLOC = BYTES + 1024;
 };
 
-// TMEM columns of the scan kernel
-constexpr uint32_t kR3 = 0, kR4 = 32, kScanCols = 64;
+// TMEM columns of the scan kernel (fp32 accumulators, 32 columns each)
+constexpr uint32_t kS1a = 0, kS1b = 32, kDSa = 64, kDSb = 96, kUt = 128, kPU = 160;
+constexpr uint32_t kScanCols = 256;
 
-// Fetch block `blk` of (bh, slice) into buffer `buf` (one cp.async group).
+// Fetch block `blk` of (bh, slice) into buffer `buf`: workspace tiles by bulk
+// copy and, for dk >= 64, the q and k rows by tiled TMA (128-byte swizzle,
+// zero fill past the end of the sequence), all completing on full[buf]; v
+// rows (and q, k rows for dk = 32) by cp.async (one group).
 template <int DK, bool DELTA>
 __device__ __forceinline__ void scan_fetch(uint8_t *sm, int buf, const bf16 *q, const bf16 *k,
-                                           const bf16 *v, const uint8_t *rec, size_t bh, int T,
+                                           const bf16 *v, const void *tmq, const void *tmk,
+                                           const uint8_t *rec, uint64_t *full, size_t bh, int T,
                                            int blk, int dv, int c0, int tid) {
     using L = ScanLayout<DK>;
     using R = Rec<DK>;
+    constexpr bool kTma = DK >= 64;
     const int t0 = blk * C;
-    constexpr int CPR = DK / 8;
     uint8_t *wq = sm + L::WQ + buf * L::WQ_BYTES;
-    uint8_t *kr = sm + L::KR + buf * L::KR_BYTES;
+    uint8_t *tzp = sm + L::TZP + buf * 24576;
+    uint8_t *kr = sm + L::KR + buf * 16384;
+    if (tid == 0) {
+        const uint32_t bytes = (DELTA ? (uint32_t)R::KB * 8192u + 8192u : 0u) + 8192u + 1024u +
+                               (kTma ? 2u * (uint32_t)R::KB * 8192u : 0u);
+        mbar_expect_tx(full, bytes);
+        if (DELTA) {
+#pragma unroll
+            for (int kb = 0; kb < R::KB; ++kb)
+                bulk_g2s(wq + kb * 16384, rec + R::WT + kb * 8192, 8192, full);
+            bulk_g2s(tzp, rec + R::TT, 8192, full);
+        }
+        bulk_g2s(tzp + 16384, rec + R::PT, 8192, full);
+        bulk_g2s(sm + L::VEC + buf * 1024, rec + R::VEC, 1024, full);
+        if (kTma) {
+#pragma unroll
+            for (int kb = 0; kb < R::KB; ++kb) {
+                tma_load_3d(wq + kb * 16384 + 8192, tmq, kb * 64, t0, (int)bh, full);
+                tma_load_3d(kr + kb * 8192, tmk, kb * 64, t0, (int)bh, full);
+            }
+        }
+    }
+    if (!kTma) {
+        constexpr int CPR = DK / 8;
+        for (int idx = tid; idx < 2 * C * CPR; idx += NT) {
+            const int which = idx / (C * CPR);
+            const int rem = idx % (C * CPR);
+            const int r = rem / CPR, ch = rem % CPR;
+            const bool ok = t0 + r < T;
+            const bf16 *src = (which ? k : q) + ((bh * T + (ok ? t0 + r : 0)) * DK + ch * 8);
+            const uint32_t dst = which ? smem_u32(kr + sw128_offset(r, ch * 8, 64))
+                                       : smem_u32(wq + sw128_offset(64 + r, ch * 8, 128));
+            cp_async16(dst, src, ok);
+        }
+    }
+    uint8_t *vr = sm + L::VR + buf * 8192;
+    for (int idx = tid; idx < C * (DVS / 8); idx += NT) {
+        const int r = idx / (DVS / 8), ch = idx % (DVS / 8);
+        const bool ok = t0 + r < T;
+        cp_async16(smem_u32(vr + sw128_offset(r, ch * 8, 64)),
+                   v + ((bh * T + (ok ? t0 + r : 0)) * dv + c0 + ch * 8), ok);
+    }
+    cp_async_commit();
+}
+
+// L2 prefetch of everything block `blk` will fetch (one thread).
+template <int DK>
+__device__ __forceinline__ void scan_prefetch_l2(const bf16 *q, const bf16 *k, const bf16 *v,
+                                                 const uint8_t *rec, size_t bh, int T, int blk,
+                                                 int dv) {
+    const int t0 = blk * C;
+    const int n = min(C, T - t0);
+    prefetch_l2(rec, Rec<DK>::BYTES);
+    prefetch_l2(q + (bh * T + t0) * DK, (uint32_t)n * DK * 2);
+    prefetch_l2(k + (bh * T + t0) * DK, (uint32_t)n * DK * 2);
+    prefetch_l2(v + (bh * T + t0) * dv, (uint32_t)n * dv * 2);
+}
+
+// g Q rows and kd K rows of buffer `buf`, scaled in place.
+template <int DK>
+__device__ __forceinline__ void scan_scale(uint8_t *sm, int buf, int tid) {
+    using L = ScanLayout<DK>;
+    uint8_t *wq = sm + L::WQ + buf * L::WQ_BYTES;
+    uint8_t *kr = sm + L::KR + buf * 16384;
+    const float *vec = reinterpret_cast<const float *>(sm + L::VEC + buf * 1024);
+    constexpr int CPR = DK / 8;
     for (int idx = tid; idx < 2 * C * CPR; idx += NT) {
         const int which = idx / (C * CPR);
         const int rem = idx % (C * CPR);
         const int r = rem / CPR, ch = rem % CPR;
-        const bool ok = t0 + r < T;
-        const bf16 *src = (which ? k : q) + ((bh * T + (ok ? t0 + r : 0)) * DK + ch * 8);
-        const uint32_t dst = which ? smem_u32(kr + sw128_offset(r, ch * 8, 64))
-                                   : smem_u32(wq + sw128_offset(64 + r, ch * 8, 128));
-        cp_async16(dst, src, ok);
-    }
-    uint8_t *vr = sm + L::VR + buf * 4096;
-    for (int idx = tid; idx < C * (DVS / 8); idx += NT) {
-        const int r = idx / (DVS / 8), ch = idx % (DVS / 8);
-        const bool ok = t0 + r < T;
-        cp_async16(smem_u32(vr + (r * DVS + ch * 8) * 2),
-                   v + ((bh * T + (ok ? t0 + r : 0)) * dv + c0 + ch * 8), ok);
-    }
-    if (DELTA) {
-        // -W rows -> rows 0..63 of each 64-wide K block of WQ; T -> rows 0..63 of TZP
-        for (int idx = tid; idx < R::KB * 512; idx += NT) {
-            const int kb = idx >> 9, c16 = idx & 511;
-            cp_async16(smem_u32(wq + kb * 16384 + c16 * 16), rec + R::WT + kb * 8192 + c16 * 16, true);
-        }
-        for (int idx = tid; idx < 512; idx += NT)
-            cp_async16(smem_u32(sm + L::TZP + buf * 24576 + idx * 16), rec + R::TT + idx * 16, true);
-    }
-    for (int idx = tid; idx < 512; idx += NT)
-        cp_async16(smem_u32(sm + L::TZP + buf * 24576 + 16384 + idx * 16), rec + R::PT + idx * 16,
-                   true);
-    for (int idx = tid; idx < 64; idx += NT)
-        cp_async16(smem_u32(sm + L::VEC + buf * 1024 + idx * 16), rec + R::VEC + idx * 16, true);
-    cp_async_commit();
-}
-
-// Operand tiles of block `buf` that need only its fetched inputs:
-// g Q in place, (kd K)^T, (beta V)^T (delta) or V^T.
-template <int DK, bool DELTA>
-__device__ __forceinline__ void scan_tiles(uint8_t *sm, int buf, int tid) {
-    using L = ScanLayout<DK>;
-    uint8_t *wq = sm + L::WQ + buf * L::WQ_BYTES;
-    const uint8_t *kr = sm + L::KR + buf * L::KR_BYTES;
-    uint8_t *ktt = sm + L::KTT + buf * 16384;
-    uint8_t *vbt = sm + L::VBT + buf * 4096;
-    const bf16 *vr = reinterpret_cast<const bf16 *>(sm + L::VR + buf * 4096);
-    const float *vec = reinterpret_cast<const float *>(sm + L::VEC + buf * 1024);
-    const float *gv = vec + 64, *kdv = vec + 128, *bv = vec + 192;
-    for (int idx = tid; idx < C * (DK / 8); idx += NT) {
-        const int r = idx / (DK / 8), ch = idx % (DK / 8);
-        uint4 *p = reinterpret_cast<uint4 *>(wq + sw128_offset(64 + r, ch * 8, 128));
+        uint4 *p = reinterpret_cast<uint4 *>(which ? kr + sw128_offset(r, ch * 8, 64)
+                                                   : wq + sw128_offset(64 + r, ch * 8, 128));
+        const float f = vec[(which ? 128 : 64) + r];
         const uint4 raw = *p;
         const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
-        const float g = gv[r];
         float x[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) x[t] = g * __bfloat162float(e[t]);
+        for (int t = 0; t < 8; ++t) x[t] = f * __bfloat162float(e[t]);
         *p = pack8(x);
-    }
-    if (tid < DK) {
-        const int j = tid;
-#pragma unroll
-        for (int i8 = 0; i8 < C / 8; ++i8) {
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                x[e] = kdv[i8 * 8 + e] * bf16_at(kr, sw128_offset(i8 * 8 + e, j, 64));
-            *reinterpret_cast<uint4 *>(ktt + sw128_offset(j, i8 * 8, 128)) = pack8(x);
-        }
-    }
-    {
-        const int c = tid & 31, part = tid >> 5;  // 4 parts of 16 tokens
-#pragma unroll
-        for (int i8 = 0; i8 < 2; ++i8) {
-            const int i0 = part * 16 + i8 * 8;
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float vv = __bfloat162float(vr[(i0 + e) * DVS + c]);
-                x[e] = DELTA ? bv[i0 + e] * vv : vv;
-            }
-            *reinterpret_cast<uint4 *>(vbt + sw128_offset(c, i0, 32)) = pack8(x);
-        }
     }
 }
 
+// Scan kernel roles (256 threads):
+//   warp 0, lane 0  issues every tensor-core product of the block loop
+//   warps 1..3      producers: fetch a block into a free buffer (TMA / bulk /
+//                   cp.async), wait for it, scale the q and k rows in place
+//   warps 4..7      epilogue (TMEM lanes 0..127): U rows, the state update and
+//                   its bf16 copy, the output rows
+// Hand-offs are mbarriers; every wait is bounded.  TMEM accumulators are kept
+// per block parity so that the output of block b can still be read while
+// block b+1 runs.
+constexpr int kScanThreads = 256;
+constexpr int kProducers = 96;
+
+struct ScanBars {
+    uint64_t ready[2];  // producers -> MMA: buffer filled and scaled      (96 arrivals)
+    uint64_t full[2];   // loads landed                                   (1 + tx bytes)
+    uint64_t empty[2];  // MMA done with the buffer + epilogue read its gates (1 + 128)
+    uint64_t tfree[2];  // output rows of the block with this parity read       (64)
+    uint64_t g1;        // S1 (and Ut) products done                      (commit)
+    uint64_t u;         // U rows written                                 (64)
+    uint64_t ds;        // Delta S products done                          (commit)
+    uint64_t pu;        // P U products done                              (commit)
+    uint64_t s;         // bf16 state copy written                        (128)
+    uint32_t tmem;
+};
+
 template <int DK, bool ALPHA, bool DELTA>
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(kScanThreads, 1)
 chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                   const bf16 *__restrict__ v, const uint8_t *__restrict__ ws,
                   const float *__restrict__ S0, bf16 *__restrict__ o, float *__restrict__ ST,
-                  int H, int T, int dv, int nblk) {
+                  int H, int T, int dv, int nblk, const __grid_constant__ CUtensorMap tmq,
+                  const __grid_constant__ CUtensorMap tmk) {
     using L = ScanLayout<DK>;
     using R = Rec<DK>;
     extern __shared__ uint8_t sm_raw[];
@@ -525,177 +555,350 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     const int c0 = blockIdx.x * DVS;
     const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
     const uint8_t *recs = ws + bh * nblk * (size_t)R::BYTES;
-
     uint8_t *UB = sm + L::UB, *SB = sm + L::SB;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8);
+    ScanBars *bars = reinterpret_cast<ScanBars *>(sm + L::BAR);
 
-    // zero everything once: the padding rows of the stacked operands must read 0
-    for (int i = tid; i < L::BAR / 16; i += NT)
+    // zero everything once: padding rows and columns of the operands must read 0
+    for (int i = tid; i < L::BAR / 16; i += kScanThreads)
         reinterpret_cast<uint4 *>(sm)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
-        mbar_init(bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->ready[b], kProducers);
+            mbar_init(&bars->full[b], 1);
+            mbar_init(&bars->empty[b], 1 + 128);
+            mbar_init(&bars->tfree[b], 64);
+        }
+        mbar_init(&bars->g1, 1);
+        mbar_init(&bars->u, 64);
+        mbar_init(&bars->ds, 1);
+        mbar_init(&bars->pu, 1);
+        mbar_init(&bars->s, 128);
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, kScanCols);
+        tmem_alloc(&bars->tmem, 512);
         tmem_relinquish();
     }
-    __syncthreads();
-
-    // fp32 master copy of the state slice: thread j owns S[c0 + c][j], c < 32
-    float Sr[DVS];
-#pragma unroll
-    for (int c = 0; c < DVS; ++c)
-        Sr[c] = (S0 && tid < DK) ? S0[(bh * dv + c0 + c) * DK + tid] : 0.f;
-    if (tid < DK) {
-#pragma unroll
-        for (int c = 0; c < DVS; ++c) st_bf16(SB, sw128_offset(c, tid, 32), Sr[c]);
-    }
-
-    scan_fetch<DK, DELTA>(sm, 0, q, k, v, recs, bh, T, 0, dv, c0, tid);
-    if (nblk > 1)
-        scan_fetch<DK, DELTA>(sm, 1, q, k, v, recs + R::BYTES, bh, T, 1, dv, c0, tid);
-    if (nblk > 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
-    else cp_async_wait_all();
-    __syncthreads();
-    scan_tiles<DK, DELTA>(sm, 0, tid);
-    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-    uint32_t phase = 0;
+    const uint32_t tmem = bars->tmem;
     bool ok = true;
 
-    auto mma_wait = [&]() {
-        const bool mine = mbar_wait(bar, phase & 1);
-        ++phase;
-        ok = __syncthreads_and(mine ? 1 : 0) != 0;
-        tc_fence_after();
-    };
-
-    const uint32_t id32 = idesc_bf16_f32(128, DVS);
-    for (int blk = 0; blk < nblk && ok; ++blk) {
-        const int buf = blk & 1;
-        const int t0 = blk * C;
-        const int n = min(C, T - t0);
-        const uint32_t wq = smem_u32(sm + L::WQ + buf * L::WQ_BYTES);
-        const uint32_t tzp = smem_u32(sm + L::TZP + buf * 24576);
-        const uint32_t ktt = smem_u32(sm + L::KTT + buf * 16384);
-        const uint32_t vbt = smem_u32(sm + L::VBT + buf * 4096);
-        const float *vec = reinterpret_cast<const float *>(sm + L::VEC + buf * 1024);
-
-        // ---- G1: R3 = [T; 0] (beta V)^T + [-W; gQ] S^T   (without delta: [0; gQ] S^T,
-        //      and the state update and the P V part of the output go with it)
-        if (tid == 0) {
-            if (DELTA) {
+    if (warp == 0) {
+        // =========================================================== MMA issue
+        if (lane == 0) {
+            const uint32_t id_kn = idesc_bf16_f32_mn(128, DVS, false, true);
+            const uint32_t id_nn = idesc_bf16_f32_mn(128, DVS, true, true);
+            const uint64_t d_sb = tile_desc_mn(smem_u32(SB), DK, 0);
+            const uint64_t d_ub = tile_desc_mn(smem_u32(UB), 64, 0);
+            const uint64_t d_ubk = tile_desc_mn(smem_u32(sm + L::UBK), 64, 0);
+            constexpr int KS = DK / 16, KH = (KS + 1) / 2;
+            auto descs = [&](int buf, uint64_t &d_wq, uint64_t &d_tz, uint64_t &d_zp, uint64_t &d_kr,
+                             uint64_t &d_vr) {
+                d_wq = tile_desc(smem_u32(sm + L::WQ + buf * L::WQ_BYTES), 128, 0, 0);
+                d_tz = tile_desc(smem_u32(sm + L::TZP + buf * 24576), 192, 0, 0);
+                d_zp = tile_desc(smem_u32(sm + L::TZP + buf * 24576), 192, 64, 0);
+                d_kr = tile_desc_mn(smem_u32(sm + L::KR + buf * 16384), 64, 0);
+                d_vr = tile_desc_mn(smem_u32(sm + L::VR + buf * 8192), 64, 0);
+            };
+            auto issue_ut = [&](int blk) {  // Ut = T diag(beta) V  (delta only)
+                uint64_t d_wq, d_tz, d_zp, d_kr, d_vr;
+                descs(blk & 1, d_wq, d_tz, d_zp, d_kr, d_vr);
+                const uint32_t col = (blk & 1) * 192 + 64;
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks)
-                    mma_bf16(tmem + kR3, tile_desc(tzp, 192, 0, ks), tile_desc(vbt, 32, 0, ks), id32,
+                    mma_bf16(tmem + col, kdesc_step(d_tz, 192, ks), mndesc_step(d_vr, ks), id_kn,
                              ks > 0);
+            };
+            if (DELTA && nblk > 0) {
+                ok = mbar_wait(&bars->ready[0], 0);
+                if (ok) issue_ut(0);
             }
+            for (int blk = 0; blk < nblk && ok; ++blk) {
+                const int buf = blk & 1, p = blk & 1;
+                const uint32_t base = p * 192;
+                uint64_t d_wq, d_tz, d_zp, d_kr, d_vr;
+                descs(buf, d_wq, d_tz, d_zp, d_kr, d_vr);
+                const uint64_t d_vk = tile_desc_mn(smem_u32(sm + L::VK + buf * 8192), 64, 0);
+                // Each barrier below is waited on by its consumers before it can
+                // complete again: the outputs of the previous block must be read
+                // (which also frees this parity's accumulators), and the state
+                // copy for this block written, before this block's products.
+                if (!DELTA) ok = ok && mbar_wait(&bars->ready[buf], (blk >> 1) & 1);
+                if (blk >= 1) ok = ok && mbar_wait(&bars->tfree[p ^ 1], ((blk - 1) >> 1) & 1);
+                ok = ok && mbar_wait(&bars->s, blk & 1);
+                if (!ok) break;
+                tc_fence_after();
+                // S1 = [-W; gQ] S^T in two K halves
 #pragma unroll
-            for (int ks = 0; ks < DK / 16; ++ks)
-                mma_bf16(tmem + kR3, tile_desc(wq, 128, 0, ks), tile_desc(smem_u32(SB), 32, 0, ks),
-                         id32, (DELTA || ks > 0) ? 1u : 0u);
-            if (!DELTA) {
+                for (int ks = 0; ks < KS; ++ks)
+                    mma_bf16(tmem + base + (ks < KH ? 0 : 32), kdesc_step(d_wq, 128, ks),
+                             mndesc_step(d_sb, ks), id_kn, (ks == 0 || ks == KH) ? 0u : 1u);
+                if (!DELTA) {
+                    // Delta S = K^T (kd V); its commit also covers S1, which reads the
+                    // bf16 state copy the epilogue overwrites once Delta S is done
 #pragma unroll
-                for (int ks = 0; ks < C / 16; ++ks) {
-                    mma_bf16(tmem + kR4, tile_desc(ktt, 128, 0, ks), tile_desc(vbt, 32, 0, ks), id32,
-                             ks > 0);
-                    mma_bf16(tmem + kR3, tile_desc(tzp, 192, 64, ks), tile_desc(vbt, 32, 0, ks),
-                             id32, 1u);
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_bf16(tmem + base + (ks < 2 ? 128 : 160), mndesc_step(d_kr, ks),
+                                 mndesc_step(d_vk, ks), id_nn, (ks & 1) ? 1u : 0u);
+                    mma_commit(&bars->ds);
+                }
+                if (DELTA) {
+                    mma_commit(&bars->g1);
+                    ok = mbar_wait(&bars->u, blk & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_bf16(tmem + base + (ks < 2 ? 128 : 160), mndesc_step(d_kr, ks),
+                                 mndesc_step(d_ubk, ks), id_nn, (ks & 1) ? 1u : 0u);
+                    mma_commit(&bars->ds);
+                }
+                const uint64_t d_x = DELTA ? d_ub : d_vr;  // U, or V without delta
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks)
+                    mma_bf16(tmem + base + 96, kdesc_step(d_zp, 192, ks), mndesc_step(d_x, ks),
+                             id_kn, ks > 0);
+                mma_commit(&bars->pu);
+                mma_commit(&bars->empty[buf]);
+                if (DELTA && blk + 1 < nblk) {
+                    ok = mbar_wait(&bars->ready[buf ^ 1], ((blk + 1) >> 1) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_ut(blk + 1);
                 }
             }
-            mma_commit(bar);
         }
-        // meanwhile: the next block's operand tiles
-        if (blk + 1 < nblk) {
-            cp_async_wait_all();
-            __syncthreads();
-            scan_tiles<DK, DELTA>(sm, buf ^ 1, tid);
-            fence_async_smem();
-        }
-        mma_wait();
-        if (!ok) break;
-
-        if (DELTA) {
-            // ---- U^T from rows 0..63 of R3
-            if (warp < 2) {
-                const int i = 32 * warp + lane;
-                float u[32];
-                tmem_ld32(tmem + lane_base + kR3, u);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < DVS; ++c) st_bf16(UB, sw128_offset(c, i, 32), u[c]);
-            }
-            fence_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
-            // ---- G2: R4 = (kd K)^T U;  R3 += [0; P] U
-            if (tid == 0) {
-#pragma unroll
-                for (int ks = 0; ks < C / 16; ++ks) {
-                    mma_bf16(tmem + kR4, tile_desc(ktt, 128, 0, ks), tile_desc(smem_u32(UB), 32, 0, ks),
-                             id32, ks > 0);
-                    mma_bf16(tmem + kR3, tile_desc(tzp, 192, 64, ks),
-                             tile_desc(smem_u32(UB), 32, 0, ks), id32, 1u);
-                }
-                mma_commit(bar);
-            }
-            mma_wait();
+    } else if (warp < 4) {
+        // ========================================================== producers
+        const int pt = tid - 32;
+        for (int blk = 0; blk < nblk && ok; ++blk) {
+            const int buf = blk & 1;
+            if (blk >= 2) ok = mbar_wait(&bars->empty[buf], ((blk >> 1) - 1) & 1);
             if (!ok) break;
-        }
-
-        // ---- state S <- g_C S + Delta S (registers; bf16 copy to SB); O out
-        {
-            float d[32];
-            tmem_ld32(tmem + lane_base + kR4, d);
-            tmem_ld_wait();
-            const float gC = vec[64 + C - 1];
-            if (tid < DK) {
+            const int t0 = blk * C;
+            const uint8_t *rec = recs + (size_t)blk * R::BYTES;
+            uint8_t *wq = sm + L::WQ + buf * L::WQ_BYTES;
+            uint8_t *tzp = sm + L::TZP + buf * 24576;
+            uint8_t *kr = sm + L::KR + buf * 16384;
+            uint8_t *vr = sm + L::VR + buf * 8192;
+            constexpr bool kTma = DK >= 64;
+            if (pt == 0) {
+                if (blk + 2 < nblk) scan_prefetch_l2<DK>(q, k, v, rec + 2 * R::BYTES, bh, T, blk + 2, dv);
+                const uint32_t bytes = (DELTA ? (uint32_t)R::KB * 8192u + 8192u : 0u) + 8192u +
+                                       1024u + (kTma ? 2u * (uint32_t)R::KB * 8192u : 0u);
+                mbar_expect_tx(&bars->full[buf], bytes);
+                if (DELTA) {
 #pragma unroll
-                for (int c = 0; c < DVS; ++c) {
-                    Sr[c] = gC * Sr[c] + d[c];
-                    st_bf16(SB, sw128_offset(c, tid, 32), Sr[c]);
+                    for (int kb = 0; kb < R::KB; ++kb)
+                        bulk_g2s(wq + kb * 16384, rec + R::WT + kb * 8192, 8192, &bars->full[buf]);
+                    bulk_g2s(tzp, rec + R::TT, 8192, &bars->full[buf]);
+                }
+                bulk_g2s(tzp + 16384, rec + R::PT, 8192, &bars->full[buf]);
+                bulk_g2s(sm + L::VEC + buf * 1024, rec + R::VEC, 1024, &bars->full[buf]);
+                if (kTma) {
+#pragma unroll
+                    for (int kb = 0; kb < R::KB; ++kb) {
+                        tma_load_3d(wq + kb * 16384 + 8192, &tmq, kb * 64, t0, (int)bh,
+                                    &bars->full[buf]);
+                        tma_load_3d(kr + kb * 8192, &tmk, kb * 64, t0, (int)bh, &bars->full[buf]);
+                    }
                 }
             }
-            if (warp >= 2) {
-                const int r = 32 * (warp - 2) + lane;
-                float ov[32];
-                tmem_ld32(tmem + lane_base + kR3, ov);
+            if (!kTma) {
+                constexpr int CPR = DK / 8;
+                for (int idx = pt; idx < 2 * C * CPR; idx += kProducers) {
+                    const int which = idx / (C * CPR);
+                    const int rem = idx % (C * CPR);
+                    const int r = rem / CPR, ch = rem % CPR;
+                    const bool okr = t0 + r < T;
+                    const bf16 *src = (which ? k : q) + ((bh * T + (okr ? t0 + r : 0)) * DK + ch * 8);
+                    const uint32_t dst = which ? smem_u32(kr + sw128_offset(r, ch * 8, 64))
+                                               : smem_u32(wq + sw128_offset(64 + r, ch * 8, 128));
+                    cp_async16(dst, src, okr);
+                }
+            }
+            for (int idx = pt; idx < C * (DVS / 8); idx += kProducers) {
+                const int r = idx / (DVS / 8), ch = idx % (DVS / 8);
+                const bool okr = t0 + r < T;
+                cp_async16(smem_u32(vr + sw128_offset(r, ch * 8, 64)),
+                           v + ((bh * T + (okr ? t0 + r : 0)) * dv + c0 + ch * 8), okr);
+            }
+            cp_async_commit();
+            cp_async_wait_all();
+            ok = mbar_wait(&bars->full[buf], (blk >> 1) & 1);
+            if (!ok) break;
+            if (!DELTA) {
+                // kd V (B operand of Delta S = K^T diag(kd) V); g and kd are folded
+                // into the epilogues everywhere else
+                const float *vec = reinterpret_cast<const float *>(sm + L::VEC + buf * 1024);
+                uint8_t *vk = sm + L::VK + buf * 8192;
+                for (int idx = pt; idx < C * (DVS / 8); idx += kProducers) {
+                    const int r = idx / (DVS / 8), ch = idx % (DVS / 8);
+                    const uint32_t off = sw128_offset(r, ch * 8, 64);
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(vr + off);
+                    const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
+                    const float f = vec[128 + r];
+                    float x[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) x[t] = f * __bfloat162float(e[t]);
+                    *reinterpret_cast<uint4 *>(vk + off) = pack8(x);
+                }
+            }
+            fence_async_smem();
+            mbar_arrive(&bars->ready[buf]);
+        }
+    } else {
+        // =========================================================== epilogue
+        const int j = tid - 128;  // TMEM lane; key channel of the state column
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        float Sr[DVS];
+#pragma unroll
+        for (int c = 0; c < DVS; ++c) Sr[c] = (S0 && j < DK) ? S0[(bh * dv + c0 + c) * DK + j] : 0.f;
+        if (j < DK) {
+#pragma unroll
+            for (int c8 = 0; c8 < DVS / 8; ++c8)
+                *reinterpret_cast<uint4 *>(SB + sw128_offset(j, c8 * 8, DK)) = pack8(Sr + c8 * 8);
+        }
+        fence_async_smem();
+        mbar_arrive(&bars->s);
+        for (int blk = 0; blk < nblk && ok; ++blk) {
+            const int buf = blk & 1, p = blk & 1;
+            const uint32_t base = p * 192;
+            const int t0 = blk * C;
+            const int n = min(C, T - t0);
+            // gates of this block, read before the buffer is released: g_C for
+            // the state, g_r of this thread's output row, kd_i of its U row
+            const float *vec = reinterpret_cast<const float *>(sm + L::VEC + buf * 1024);
+            float gC, gr = 0.f, kdi = 0.f;
+            if (DELTA) {
+                ok = mbar_wait(&bars->g1, blk & 1);
+                if (!ok) break;
+                tc_fence_after();
+                gC = vec[64 + C - 1];
+                if (warp >= 6) gr = vec[64 + j - 64];
+                else kdi = vec[128 + j];
+                mbar_arrive(&bars->empty[buf]);
+                if (warp < 6) {  // U rows = tokens 0..63
+                    float u[32], x[32];
+                    tmem_ld32(tmem + lane_base + base + 64, u);
+                    tmem_ld32(tmem + lane_base + base + 0, x);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) u[c] += x[c];
+                    tmem_ld32(tmem + lane_base + base + 32, x);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) u[c] += x[c];
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8)
+                        *reinterpret_cast<uint4 *>(UB + sw128_offset(j, c8 * 8, 64)) =
+                            pack8(u + c8 * 8);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) u[c] *= kdi;
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8)
+                        *reinterpret_cast<uint4 *>(sm + L::UBK + sw128_offset(j, c8 * 8, 64)) =
+                            pack8(u + c8 * 8);
+                    fence_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(&bars->u);
+                }
+            }
+            ok = mbar_wait(&bars->ds, blk & 1);
+            if (!ok) break;
+            tc_fence_after();
+            if (!DELTA) {
+                gC = vec[64 + C - 1];
+                if (warp >= 6) gr = vec[64 + j - 64];
+                mbar_arrive(&bars->empty[buf]);
+            }
+            {
+                float d[32], e[32];
+                tmem_ld32(tmem + lane_base + base + 128, d);
+                tmem_ld32(tmem + lane_base + base + 160, e);
                 tmem_ld_wait();
+                if (j < DK) {
+#pragma unroll
+                    for (int c = 0; c < DVS; ++c) Sr[c] = gC * Sr[c] + d[c] + e[c];
+#pragma unroll
+                    for (int c8 = 0; c8 < DVS / 8; ++c8)
+                        *reinterpret_cast<uint4 *>(SB + sw128_offset(j, c8 * 8, DK)) =
+                            pack8(Sr + c8 * 8);
+                }
+                fence_async_smem();
+                tc_fence_before();
+                mbar_arrive(&bars->s);
+            }
+            if (warp >= 6) {  // output rows = tokens 0..63
+                ok = mbar_wait(&bars->pu, blk & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const int r = j - 64;
+                float d[32], e[32];
+                tmem_ld32(tmem + lane_base + base + 0, d);
+                tmem_ld32(tmem + lane_base + base + 32, e);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) d[c] = gr * (d[c] + e[c]);  // g_r Q S^T
+                tmem_ld32(tmem + lane_base + base + 96, e);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) d[c] += e[c];              // + P U
+                tc_fence_before();
+                mbar_arrive(&bars->tfree[p]);
                 if (r < n) {
                     uint4 *dst = reinterpret_cast<uint4 *>(o + (bh * T + t0 + r) * dv + c0);
 #pragma unroll
-                    for (int i8 = 0; i8 < 4; ++i8) dst[i8] = pack8(ov + i8 * 8);
+                    for (int i8 = 0; i8 < 4; ++i8) dst[i8] = pack8(d + i8 * 8);
                 }
             }
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (blk + 2 < nblk)
-            scan_fetch<DK, DELTA>(sm, buf, q, k, v, recs + (size_t)(blk + 2) * R::BYTES, bh, T,
-                                  blk + 2, dv, c0, tid);
+        if (ok && j < DK) {
+#pragma unroll
+            for (int c = 0; c < DVS; ++c) ST[(bh * dv + c0 + c) * DK + j] = Sr[c];
+        }
     }
 
-    if (!ok && lane == 0) atomicExch(&g_tc_error, 1);
+    if (!ok) atomicExch(&g_tc_error, 1);
     cp_async_wait_all();
-    if (ok && tid < DK) {
-#pragma unroll
-        for (int c = 0; c < DVS; ++c) ST[(bh * dv + c0 + c) * DK + tid] = Sr[c];
-    }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kScanCols);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // ================================================================== launch
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [B*H][T][d] bf16 tensor, boxes of 64 rows x 64 columns, 128-byte swizzle,
+// zero fill outside.
+cudaError_t make_rows_map(CUtensorMap *m, const void *base, int d, int T, int BH) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * (cuuint64_t)T};
+    const cuuint32_t box[3] = {64, 64, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 template <int DK, bool ALPHA, bool DELTA>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *alpha,
@@ -714,9 +917,19 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
         DELTA ? beta : nullptr, static_cast<uint8_t *>(ws), H, T, nblk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    scan<<<dim3(dv / DVS, H, B), NT, ScanLayout<DK>::ALLOC, stream>>>(
+    CUtensorMap tmq, tmk;
+    memset(&tmq, 0, sizeof(tmq));
+    memset(&tmk, 0, sizeof(tmk));
+    if (DK >= 64) {
+        e = make_rows_map(&tmq, q, DK, T, B * H);
+        if (e != cudaSuccess) return e;
+        e = make_rows_map(&tmk, k, DK, T, B * H);
+        if (e != cudaSuccess) return e;
+    }
+    scan<<<dim3(dv / DVS, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
         static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), static_cast<const bf16 *>(v),
-        static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk);
+        static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, tmq,
+        tmk);
     return cudaGetLastError();
 }
 

@@ -23,6 +23,10 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+// Plain arrive (count 1) on `bar`.
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 // Wait until the phase with the given parity has completed.  Returns false
 // if the bounded spin ran out.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
@@ -108,6 +112,21 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr, uint32_t s
     return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand with the 128-byte
+// swizzle: the stored tile's rows are the K index (each 128-byte row holds 64
+// consecutive M/N elements, 16-byte chunk c of row r at chunk position
+// c ^ (r & 7)), 8-row K groups every 1024 bytes, 64-wide M/N blocks every
+// `lbo` bytes.  `saddr` points at the first K row of the slice.
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo & 0x3FFFFu) >> 4) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D,
 // shape M x N.  Bits: [4,6) D format (1 = f32), [7,10) A format (1 = bf16),
 // [10,13) B format (1 = bf16), 15/16 A/B major (0 = K), [17,23) N>>3,
@@ -115,6 +134,11 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr, uint32_t s
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
+}
+
+// The same with A and/or B MN-major (bits 15 and 16).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int M, int N, bool a_mn, bool b_mn) {
+    return idesc_bf16_f32(M, N) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one instruction (K = 16 for bf16).
@@ -148,6 +172,54 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int k, int ro
     const int kin = k & 63;
     const int chunk = (kin >> 3) ^ (row & 7);
     return (uint32_t)(kb * rows * 128 + row * 128 + chunk * 16 + (kin & 7) * 2);
+}
+
+// The same descriptors advanced by K slice `ks` from slice 0 (the start
+// address field moves; nothing else changes).
+__device__ __forceinline__ uint64_t kdesc_step(uint64_t d0, int rows, int ks) {
+    return d0 + (uint64_t)(((uint32_t)(ks >> 2) * (uint32_t)rows * 128u + (uint32_t)(ks & 3) * 32u) >> 4);
+}
+__device__ __forceinline__ uint64_t mndesc_step(uint64_t d0, int ks) {
+    return d0 + (uint64_t)((uint32_t)ks * 128u);
+}
+
+// Descriptor of K slice `ks` of an MN-major tile laid out by
+// sw128_offset(k, mn, krows) (rows = K index, 64-wide M/N blocks every
+// krows * 128 bytes).
+__device__ __forceinline__ uint64_t tile_desc_mn(uint32_t tile_saddr, int krows, int ks) {
+    return desc_mnmajor_sw128(tile_saddr + (uint32_t)ks * 2048u, (uint32_t)krows * 128u);
+}
+
+// ------------------------------------------------------------- bulk copies
+// Expect `bytes` more transaction bytes on `bar` and arrive once.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+// Global -> shared bulk copy (16-byte aligned, size a multiple of 16),
+// completion counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Tiled TMA load of a 3-D box (coordinates x innermost) into shared memory,
+// completion counted on `bar`.  `map` is a __grid_constant__ CUtensorMap.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *map, int x, int y, int z,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+// Hint: bring [p, p + bytes) into L2 (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Descriptor of the 16-wide K slice `ks` (K elements [16*ks, 16*ks+16)) of a
