@@ -21,11 +21,12 @@ from .build import LIB_PATH
 LINEAR, DECAY, DELTA, GATED_DELTA = 0, 1, 2, 3
 MODES = {"linear": LINEAR, "decay": DECAY, "delta": DELTA, "gated_delta": GATED_DELTA}
 F32, BF16 = 0, 1
-SYMBOLS = ("lr_fwd_chunked", "lr_fwd_chunked_workspace_size", "lr_step", "lr_device_status",
-           "lr_status_string", "lr_abi_version")
+SYMBOLS = ("lr_fwd_chunked", "lr_fwd_chunked_workspace_size", "lr_fwd_chunked_noalloc", "lr_step",
+           "lr_device_status", "lr_status_string", "lr_abi_version")
+STATIC_WORKSPACE_BYTES = 64 << 20   # LR_STATIC_WORKSPACE_BYTES
 STATUS = {0: "LR_OK", 1: "LR_ERR_NULL", 2: "LR_ERR_SHAPE", 3: "LR_ERR_DTYPE", 4: "LR_ERR_ALIGN",
           5: "LR_ERR_MODE", 6: "LR_ERR_UNSUPPORTED", 7: "LR_ERR_CUDA", 8: "LR_ERR_ALIAS",
-          9: "LR_ERR_TIMEOUT", 10: "LR_ERR_WORKSPACE"}
+          9: "LR_ERR_TIMEOUT", 10: "LR_ERR_WORKSPACE", 11: "LR_ERR_TOO_LARGE"}
 _USES_ALPHA = {LINEAR: False, DECAY: True, DELTA: False, GATED_DELTA: True}
 _USES_BETA = {LINEAR: False, DECAY: False, DELTA: True, GATED_DELTA: True}
 
@@ -55,6 +56,8 @@ def lib() -> ctypes.CDLL:
         L.lr_fwd_chunked.restype = i
         L.lr_fwd_chunked.argtypes = ([vp, vp, vp, fp, fp, fp, vp, fp] + [i] * 6 +
                                      [i, i, vp, ctypes.c_size_t, vp])
+        L.lr_fwd_chunked_noalloc.restype = i
+        L.lr_fwd_chunked_noalloc.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp] + [i] * 6 + [i, i, vp]
         L.lr_fwd_chunked_workspace_size.restype = ctypes.c_size_t
         L.lr_fwd_chunked_workspace_size.argtypes = [i] * 8
         L.lr_step.restype = i
@@ -166,6 +169,47 @@ def lr_fwd_chunked(q, k, v, alpha=None, beta=None, S0=None, *, mode=GATED_DELTA,
                               _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
     if st != 0:
         raise LrError(st, "lr_fwd_chunked")
+    return o, S_T
+
+
+def lr_fwd_chunked_noalloc(q, k, v, alpha=None, beta=None, S0=None, *, mode=GATED_DELTA,
+                           chunk=64, o=None, S_T=None, stream=None):
+    """Chunkwise forward through ``lr_fwd_chunked_noalloc`` (include/lr.h):
+    the same result as :func:`lr_fwd_chunked`, with the scratch taken from
+    the library's fixed static device array instead of a workspace, for
+    callers that cannot allocate device memory.  Raises LrError with
+    LR_ERR_TOO_LARGE when the problem needs more than STATIC_WORKSPACE_BYTES
+    of scratch.  Outputs ``o`` and ``S_T`` are allocated here only when not
+    given.  Returns (o, S_T).
+    """
+    import torch
+    mode = MODES.get(mode, mode)
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _check(q, "q", (B, H, T, dk), q.dtype, dev)
+    _check(k, "k", (B, H, T, dk), q.dtype, dev)
+    _check(v, "v", (B, H, T, dv), q.dtype, dev)
+    alpha = alpha if _USES_ALPHA[mode] else None
+    beta = beta if _USES_BETA[mode] else None
+    if alpha is not None:
+        _check(alpha, "alpha", (B, H, T), torch.float32, dev)
+    if beta is not None:
+        _check(beta, "beta", (B, H, T), torch.float32, dev)
+    if S0 is not None:
+        _check(S0, "S0", (B, H, dv, dk), torch.float32, dev)
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=q.dtype, device=dev)
+    if S_T is None:
+        S_T = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+    st = lib().lr_fwd_chunked_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                                      _ptr(S0), _ptr(o), _ptr(S_T), B, H, T, dk, dv, int(chunk),
+                                      dt, int(mode), _stream_handle(stream, dev))
+    if st != 0:
+        raise LrError(st, "lr_fwd_chunked_noalloc")
     return o, S_T
 
 

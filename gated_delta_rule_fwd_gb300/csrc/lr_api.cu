@@ -87,6 +87,7 @@ const char *lr_status_string(lr_status s) {
     case LR_ERR_ALIAS: return "an output overlaps an input";
     case LR_ERR_TIMEOUT: return "a kernel gave up a bounded wait; its outputs are incomplete";
     case LR_ERR_WORKSPACE: return "workspace is NULL or smaller than lr_fwd_chunked_workspace_size";
+    case LR_ERR_TOO_LARGE: return "problem needs more scratch than the static workspace holds (LR_STATIC_WORKSPACE_BYTES)";
     }
     return "unknown status";
 }

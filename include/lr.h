@@ -15,8 +15,9 @@
  *
  * Conventions shared by every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
- *     allocates no memory and keeps no state between calls other than
- *     per-device kernel attributes set once.
+ *     allocates no memory at run time and keeps no state between calls other
+ *     than per-device kernel attributes set once and the fixed scratch array
+ *     used by lr_fwd_chunked_noalloc (part of the loaded module).
  *   - Tensors are contiguous and row-major with the shapes given below; base
  *     pointers must be 16-byte aligned (else LR_ERR_ALIGN).
  *   - alpha, beta and the state are always fp32; q, k, v and o have the
@@ -54,7 +55,9 @@ typedef enum {
     LR_ERR_CUDA = 7,        /* the CUDA runtime reported an error at launch        */
     LR_ERR_ALIAS = 8,       /* an output overlaps an input it must not overlap     */
     LR_ERR_TIMEOUT = 9,     /* a kernel gave up a bounded wait (see lr_device_status) */
-    LR_ERR_WORKSPACE = 10   /* workspace NULL or smaller than lr_fwd_chunked_workspace_size */
+    LR_ERR_WORKSPACE = 10,  /* workspace NULL or smaller than lr_fwd_chunked_workspace_size */
+    LR_ERR_TOO_LARGE = 11   /* lr_fwd_chunked_noalloc: the problem needs more scratch
+                               than LR_STATIC_WORKSPACE_BYTES */
 } lr_status;
 
 /* Which row of the family (summary table of the first page). */
@@ -171,6 +174,38 @@ lr_status lr_step(const void *q, const void *k, const void *v,
  * queried.
  */
 lr_status lr_device_status(void);
+
+/*
+ * Chunked forward without any allocation by the caller.  No counterpart on
+ * the pages: this is a deployment variant of lr_fwd_chunked.
+ *
+ * For callers that cannot allocate device memory -- code inside a host
+ * framework that owns all device memory and gives its plug-ins no allocator,
+ * or code on a path where cudaMalloc must not run because it can synchronise
+ * the device or fail at an unpredictable time.  Same arguments and result as
+ * lr_fwd_chunked, without the workspace: the scratch comes from a fixed
+ * array of LR_STATIC_WORKSPACE_BYTES in the library's own device memory,
+ * which every GPU that loads the library holds until the process exits.
+ *
+ *   - Returns LR_ERR_TOO_LARGE, launching nothing, when
+ *     lr_fwd_chunked_workspace_size(...) exceeds LR_STATIC_WORKSPACE_BYTES
+ *     (at dk = 128 about 33 KB per (batch, head, 64-token block), so roughly
+ *     B * H * ceil(T / 64) <= 2000).
+ *   - The first call on a device looks up the array's device address (with
+ *     cudaGetSymbolAddress, that device current); make that first call before
+ *     any stream capture.
+ *   - Every call uses the same array: calls that may run at the same time on
+ *     the GPU (other streams, other host threads) race and must be ordered by
+ *     the caller.  No clearing is needed between calls.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define LR_STATIC_WORKSPACE_BYTES (64u << 20)
+
+lr_status lr_fwd_chunked_noalloc(const void *q, const void *k, const void *v,
+                                 const float *alpha, const float *beta,
+                                 const float *S0, void *o, float *S_T,
+                                 int B, int H, int T, int dk, int dv, int chunk,
+                                 lr_dtype dt, lr_mode mode, cudaStream_t stream);
 
 /* Static English text for a status code (never NULL). */
 const char *lr_status_string(lr_status s);

@@ -32,8 +32,8 @@ def _declared_functions():
 
 def test_header_declares_expected_entry_points():
     assert set(_declared_functions()) == {"lr_fwd_chunked", "lr_fwd_chunked_workspace_size",
-                                          "lr_step", "lr_device_status", "lr_status_string",
-                                          "lr_abi_version"}
+                                          "lr_fwd_chunked_noalloc", "lr_step", "lr_device_status",
+                                          "lr_status_string", "lr_abi_version"}
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings_and_version(lib):
     import gated_delta_rule_fwd_gb300 as lr
     assert lib.lr_abi_version() == 1
-    for code in range(11):
+    for code in range(12):
         s = lr.status_string(code)
         assert s and s != "unknown status"
     assert lr.status_string(99) == "unknown status"
