@@ -111,7 +111,7 @@ class ClockSampler:
             self.out = open(f"/tmp/lr_clocks_{os.getpid()}.csv", "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -140,7 +140,7 @@ class ClockSampler:
                 except ValueError:
                     continue
         os.unlink(self.out.name)
-        inside = [x for t, x in rows if t0 - 0.15 <= t <= t1 + 0.15] or [x for _, x in rows]
+        inside = [x for t, x in rows if t0 - 0.05 <= t <= t1 + 0.05] or [x for _, x in rows]
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         sm = [float(x[2]) for x in inside if x[2].replace(".", "").isdigit()]
@@ -334,12 +334,12 @@ def run_decode(lr, dev, dist, peaks, args):
     w = workloads.WORKLOADS[DECODE_WORKLOAD]
     g = torch.Generator(dev)
     S = workloads.draw_decode_state(w, dev, g)
-    steps = w.steps
+    steps = w.steps if args.decode_steps is None else max(1, args.decode_steps)
     inputs = [workloads.draw_decode_step(w, s, dev, g) for s in range(steps)]
     o = torch.empty((w.B, w.H, w.dv), dtype=w.torch_dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
     scratch = S.clone()
-    for s in range(10):
+    for s in range(min(10, steps)):
         i = inputs[s]
         lr.lr_step(i["q"], i["k"], i["v"], i["alpha"], i["beta"], scratch, mode=w.mode, o=o,
                    stream=stream)
@@ -410,12 +410,14 @@ def run_reference(args, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=[k for k in workloads.WORKLOADS if k != DECODE_WORKLOAD])
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--decode-steps", type=int, default=None,
+                    help="decode steps to time (default: the workload's 1000)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of single-core oracle work in the cpu_baseline sample")
