@@ -122,15 +122,20 @@ template <int DK>
 struct PrepLayout {
     static constexpr int KB = (DK + 63) / 64;
     static constexpr int QK = 0;                            // [128 rows][DK]: Q rows, K rows
-    static constexpr int TZ = QK + 128 * 128 * KB;          // [128][64]: T diag(beta) rows, 0 rows
-    static constexpr int AM = TZ + 16384;                   // fp32 [64][AP]
+    static constexpr int TB = QK + 128 * 128 * KB;          // [64][64] bf16: T diag(beta)
+    static constexpr int XT = TB;                           // fp32 [16][XP] solve scratch, inside TB
+    static constexpr int AM = TB + 8192;                    // fp32 [64][AP]
     static constexpr int TM = AM + C * AP * 4;              // fp32 [64][AP]
-    static constexpr int XT = TM + C * AP * 4;              // fp32 [16][XP]
-    static constexpr int VEC = XT + 16 * XP * 4;            // G, ginv, g, kd, -, b
-    static constexpr int BAR = VEC + 6 * 64 * 4;
+    static constexpr int VEC = TM + C * AP * 4;             // G, ginv, g, beta
+    static constexpr int BAR = VEC + 4 * 64 * 4;
     static constexpr int BYTES = BAR + 64;
     static constexpr int ALLOC = BYTES + 1024;
 };
+static_assert(16 * XP * 4 <= 8192, "solve scratch must fit inside the T tile");
+
+// Element (r, c) of a 64 x 64 fp32 matrix in shared memory, rows padded to 65
+// floats so that a warp touching one column of 32 rows hits 32 banks.
+__device__ __forceinline__ int sw64(int r, int c) { return r * AP + c; }
 
 // One block row of the blocked UT inverse: with the rows of T above it done,
 //   X = A[rows b, cols < 16b] T[< 16b, < 16b];   T[rows b, cols < 16b] = -T_bb X.
@@ -145,9 +150,9 @@ __device__ __forceinline__ void ut_block_row(const float *Am, float *Tm, float *
     for (int k = 0; k < NC; ++k) acc[k] = 0.f;
 #pragma unroll 4
     for (int i = 0; i < 16 * BR; ++i) {
-        const float a = Am[row * AP + i];
+        const float a = Am[sw64(row, i)];
 #pragma unroll
-        for (int k = 0; k < NC; ++k) acc[k] += a * Tm[i * AP + cg + 8 * k];
+        for (int k = 0; k < NC; ++k) acc[k] += a * Tm[sw64(i, cg + 8 * k)];
     }
 #pragma unroll
     for (int k = 0; k < NC; ++k) Xt[rr * XP + cg + 8 * k] = acc[k];
@@ -156,12 +161,12 @@ __device__ __forceinline__ void ut_block_row(const float *Am, float *Tm, float *
     for (int k = 0; k < NC; ++k) acc[k] = 0.f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const float t = Tm[row * AP + 16 * BR + i];
+        const float t = Tm[sw64(row, 16 * BR + i)];
 #pragma unroll
         for (int k = 0; k < NC; ++k) acc[k] += t * Xt[i * XP + cg + 8 * k];
     }
 #pragma unroll
-    for (int k = 0; k < NC; ++k) Tm[row * AP + cg + 8 * k] = -acc[k];
+    for (int k = 0; k < NC; ++k) Tm[sw64(row, cg + 8 * k)] = -acc[k];
     __syncthreads();
 }
 
@@ -171,20 +176,20 @@ __device__ __forceinline__ void ut_block_row(const float *Am, float *Tm, float *
 __device__ __forceinline__ void ut_inverse(const float *Am, float *Tm, float *Xt, int tid) {
     if (tid < 64) {
         const int b = tid >> 4, c = tid & 15;
-        const float *Ab = Am + (16 * b) * AP + 16 * b;
         float x[16];
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
             float s0 = (rr == c) ? 1.f : 0.f, s1 = 0.f;
 #pragma unroll
             for (int i = 0; i < rr; ++i) {
-                if (i & 1) s1 -= Ab[rr * AP + i] * x[i];
-                else s0 -= Ab[rr * AP + i] * x[i];
+                const float a = Am[sw64(16 * b + rr, 16 * b + i)];
+                if (i & 1) s1 -= a * x[i];
+                else s0 -= a * x[i];
             }
             x[rr] = s0 + s1;
         }
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) Tm[(16 * b + rr) * AP + 16 * b + c] = x[rr];
+        for (int rr = 0; rr < 16; ++rr) Tm[sw64(16 * b + rr, 16 * b + c)] = x[rr];
     }
     __syncthreads();
     ut_block_row<1>(Am, Tm, Xt, tid);
@@ -208,12 +213,12 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     const int n = min(C, T - t0);
     uint8_t *rec = ws + (bh * nblk + blk) * (size_t)R::BYTES;
 
-    uint8_t *QK = sm + L::QK, *TZ = sm + L::TZ;
+    uint8_t *QK = sm + L::QK, *TB = sm + L::TB;
     float *Am = reinterpret_cast<float *>(sm + L::AM);
     float *Tm = reinterpret_cast<float *>(sm + L::TM);
     float *Xt = reinterpret_cast<float *>(sm + L::XT);
     float *Gv = reinterpret_cast<float *>(sm + L::VEC);
-    float *giv = Gv + 64, *gv = Gv + 128, *bv = Gv + 320;
+    float *giv = Gv + 64, *gv = Gv + 128, *bv = Gv + 192;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8);
 
@@ -228,12 +233,8 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         cp_async16(smem_u32(QK + sw128_offset(which * 64 + r, ch * 8, 128)), src, ok);
     }
     cp_async_commit();
-    if (DELTA) {
-        // zero rows 64..127 of [T diag(beta); 0] and the upper blocks of Tm
-        for (int i = tid; i < 8192 / 16; i += NT)
-            reinterpret_cast<uint4 *>(TZ + 8192)[i] = make_uint4(0, 0, 0, 0);
+    if (DELTA)  // zero the blocks above the diagonal of T, which the solve never writes
         for (int i = tid; i < C * AP; i += NT) Tm[i] = 0.f;
-    }
     float la = 0.f, b = 0.f;
     if (tid < C && tid < n) {
         if (ALPHA) la = __logf(alpha[bh * T + t0 + tid]);
@@ -244,7 +245,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, 256);
+        tmem_alloc(tmem_slot, 128);
         tmem_relinquish();
     }
     // inclusive scan of ln alpha over the block (warps 0 and 1 hold the 64 values)
@@ -322,7 +323,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
             } else if (DELTA) {
                 const float br = bv[r];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) Am[r * AP + half * 32 + e] = br * a[e];
+                for (int e = 0; e < 32; ++e) Am[sw64(r, half * 32 + e)] = br * a[e];
             }
         }
         if (DELTA) {
@@ -339,19 +340,20 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
             }
         }
     }
+    tc_fence_before();  // the score columns are reused by W below
     __syncthreads();
 
     if (DELTA && ok) {
         ut_inverse(Am, Tm, Xt, tid);
-        // T diag(beta) (bf16) -> rows 0..63 of [T diag(beta); 0] and to the workspace
+        // T diag(beta) (bf16) -> the T tile (over the solve scratch) and to the workspace
         for (int idx = tid; idx < C * 8; idx += NT) {
             const int r = idx >> 3, i8 = idx & 7;
             float t[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) t[e] = Tm[r * AP + i8 * 8 + e] * bv[i8 * 8 + e];
+            for (int e = 0; e < 8; ++e) t[e] = Tm[sw64(r, i8 * 8 + e)] * bv[i8 * 8 + e];
             const uint4 w4 = pack8(t);
             const uint32_t off = sw128_offset(r, i8 * 8, 64);
-            *reinterpret_cast<uint4 *>(TZ + off) = w4;
+            *reinterpret_cast<uint4 *>(TB + off) = w4;
             *reinterpret_cast<uint4 *>(rec + R::TT + off) = w4;
         }
         fence_async_smem();
@@ -359,12 +361,13 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         __syncthreads();
         tc_fence_after();
 
-        // ---- E3: [T diag(beta); 0] (g K) -> TMEM cols [64, 64 + DK) = [W; 0]
+        // ---- E3: T diag(beta) (g K) -> W, M = 64 (TMEM cols [0, DK): rows 16w..16w+15
+        //      in lanes 32w..32w+15 of warp w)
         if (tid == 0) {
-            const uint32_t id = idesc_bf16_f32_mn(128, DK, false, true);
+            const uint32_t id = idesc_bf16_f32_mn(64, DK, false, true);
 #pragma unroll
             for (int ks = 0; ks < C / 16; ++ks)
-                mma_bf16(tmem + 64, tile_desc(smem_u32(TZ), 128, 0, ks),
+                mma_bf16(tmem, tile_desc(smem_u32(TB), 64, 0, ks),
                          desc_mnmajor_sw128(smem_u32(QK) + 8192 + ks * 2048, 16384), id, ks > 0);
             mma_commit(bar);
         }
@@ -372,27 +375,29 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         tc_fence_after();
 
         // ---- -W rows -> workspace
-        if (ok && warp < 2) {
-            const int r = 32 * warp + lane;
+        if (ok) {
+            const int r = 16 * warp + lane;
 #pragma unroll
             for (int cb = 0; cb < DK / 32; ++cb) {
                 float w[32];
-                tmem_ld32(tmem + lane_base + 64 + 32 * cb, w);
+                tmem_ld32(tmem + lane_base + 32 * cb, w);
                 tmem_ld_wait();
+                if (lane < 16) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) w[e] = -w[e];
+                    for (int e = 0; e < 32; ++e) w[e] = -w[e];
 #pragma unroll
-                for (int i8 = 0; i8 < 4; ++i8)
-                    *reinterpret_cast<uint4 *>(rec + R::WT +
-                                               sw128_offset(r, cb * 32 + i8 * 8, 64)) =
-                        pack8(w + i8 * 8);
+                    for (int i8 = 0; i8 < 4; ++i8)
+                        *reinterpret_cast<uint4 *>(rec + R::WT +
+                                                   sw128_offset(r, cb * 32 + i8 * 8, 64)) =
+                            pack8(w + i8 * 8);
+                }
             }
         }
     }
     if (!ok && lane == 0) atomicExch(&g_tc_error, 1);
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 // ===================================================================== scan
@@ -516,27 +521,32 @@ __device__ __forceinline__ void scan_scale(uint8_t *sm, int buf, int tid) {
 }
 
 // Scan kernel roles (256 threads):
-//   warp 0, lane 0  issues every tensor-core product of the block loop
-//   warps 1..3      producers: fetch a block into a free buffer (TMA / bulk /
-//                   cp.async), wait for it, scale the q and k rows in place
+//   warp 0, lane 0  issues the products on the state chain: S1 = [-W; Q] S^T
+//                   and Delta S (and, without delta, Delta S from K^T (kd V))
+//   warp 1, lane 0  issues the products off the chain: P U (P V) and the next
+//                   block's Ut = T diag(beta) V
+//   warps 2, 3      producers: fetch a block into a free buffer (TMA / bulk /
+//                   cp.async) and wait for it to land
 //   warps 4..7      epilogue (TMEM lanes 0..127): U rows, the state update and
 //                   its bf16 copy, the output rows
 // Hand-offs are mbarriers; every wait is bounded.  TMEM accumulators are kept
 // per block parity so that the output of block b can still be read while
-// block b+1 runs.
+// block b+1 runs.  Every barrier is waited on by all of its consumers before
+// it can complete again (so a parity wait is never ambiguous).
 constexpr int kScanThreads = 256;
-constexpr int kProducers = 96;
+constexpr int kProducers = 64;
 
 struct ScanBars {
-    uint64_t ready[2];  // producers -> MMA: buffer filled and scaled      (96 arrivals)
-    uint64_t full[2];   // loads landed                                   (1 + tx bytes)
-    uint64_t empty[2];  // MMA done with the buffer + epilogue read its gates (1 + 128)
-    uint64_t tfree[2];  // output rows of the block with this parity read       (64)
-    uint64_t g1;        // S1 (and Ut) products done                      (commit)
-    uint64_t u;         // U rows written                                 (64)
-    uint64_t ds;        // Delta S products done                          (commit)
-    uint64_t pu;        // P U products done                              (commit)
-    uint64_t s;         // bf16 state copy written                        (128)
+    uint64_t ready[2];  // buffer filled                                   (64 producers)
+    uint64_t full[2];   // loads landed                                    (1 + tx bytes)
+    uint64_t empty[2];  // both issuers done with the buffer + epilogue read its gates (2 + 128)
+    uint64_t tfree[2];  // output rows of the block with this parity read  (64)
+    uint64_t g1;        // S1 products done                                (commit)
+    uint64_t ut;        // Ut products done                                (commit)
+    uint64_t u;         // U rows written                                  (64)
+    uint64_t ds;        // Delta S products done                           (commit)
+    uint64_t pu[2];     // P U products of the block with this parity done (commit)
+    uint64_t s;         // bf16 state copy written                         (128)
     uint32_t tmem;
 };
 
@@ -565,13 +575,15 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars->ready[b], kProducers);
             mbar_init(&bars->full[b], 1);
-            mbar_init(&bars->empty[b], 1 + 128);
+            mbar_init(&bars->empty[b], 2 + 128);
             mbar_init(&bars->tfree[b], 64);
         }
         mbar_init(&bars->g1, 1);
+        mbar_init(&bars->ut, 1);
         mbar_init(&bars->u, 64);
         mbar_init(&bars->ds, 1);
-        mbar_init(&bars->pu, 1);
+        mbar_init(&bars->pu[0], 1);
+        mbar_init(&bars->pu[1], 1);
         mbar_init(&bars->s, 128);
         fence_mbar_init();
     }
@@ -585,82 +597,93 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     const uint32_t tmem = bars->tmem;
     bool ok = true;
 
+    const uint32_t id_kn = idesc_bf16_f32_mn(128, DVS, false, true);
+    const uint32_t id_nn = idesc_bf16_f32_mn(128, DVS, true, true);
+    auto wq_desc = [&](int buf) { return tile_desc(smem_u32(sm + L::WQ + buf * L::WQ_BYTES), 128, 0, 0); };
+    auto tz_desc = [&](int buf) { return tile_desc(smem_u32(sm + L::TZP + buf * 24576), 192, 0, 0); };
+    auto zp_desc = [&](int buf) { return tile_desc(smem_u32(sm + L::TZP + buf * 24576), 192, 64, 0); };
+    auto kr_desc = [&](int buf) { return tile_desc_mn(smem_u32(sm + L::KR + buf * 16384), 64, 0); };
+    auto vr_desc = [&](int buf) { return tile_desc_mn(smem_u32(sm + L::VR + buf * 8192), 64, 0); };
+    auto vk_desc = [&](int buf) { return tile_desc_mn(smem_u32(sm + L::VK + buf * 8192), 64, 0); };
+
     if (warp == 0) {
-        // =========================================================== MMA issue
+        // ================================================ chain products
         if (lane == 0) {
-            const uint32_t id_kn = idesc_bf16_f32_mn(128, DVS, false, true);
-            const uint32_t id_nn = idesc_bf16_f32_mn(128, DVS, true, true);
             const uint64_t d_sb = tile_desc_mn(smem_u32(SB), DK, 0);
-            const uint64_t d_ub = tile_desc_mn(smem_u32(UB), 64, 0);
             const uint64_t d_ubk = tile_desc_mn(smem_u32(sm + L::UBK), 64, 0);
             constexpr int KS = DK / 16, KH = (KS + 1) / 2;
-            auto descs = [&](int buf, uint64_t &d_wq, uint64_t &d_tz, uint64_t &d_zp, uint64_t &d_kr,
-                             uint64_t &d_vr) {
-                d_wq = tile_desc(smem_u32(sm + L::WQ + buf * L::WQ_BYTES), 128, 0, 0);
-                d_tz = tile_desc(smem_u32(sm + L::TZP + buf * 24576), 192, 0, 0);
-                d_zp = tile_desc(smem_u32(sm + L::TZP + buf * 24576), 192, 64, 0);
-                d_kr = tile_desc_mn(smem_u32(sm + L::KR + buf * 16384), 64, 0);
-                d_vr = tile_desc_mn(smem_u32(sm + L::VR + buf * 8192), 64, 0);
-            };
-            auto issue_ut = [&](int blk) {  // Ut = T diag(beta) V  (delta only)
-                uint64_t d_wq, d_tz, d_zp, d_kr, d_vr;
-                descs(blk & 1, d_wq, d_tz, d_zp, d_kr, d_vr);
-                const uint32_t col = (blk & 1) * 192 + 64;
-#pragma unroll
-                for (int ks = 0; ks < C / 16; ++ks)
-                    mma_bf16(tmem + col, kdesc_step(d_tz, 192, ks), mndesc_step(d_vr, ks), id_kn,
-                             ks > 0);
-            };
-            if (DELTA && nblk > 0) {
-                ok = mbar_wait(&bars->ready[0], 0);
-                if (ok) issue_ut(0);
-            }
             for (int blk = 0; blk < nblk && ok; ++blk) {
-                const int buf = blk & 1, p = blk & 1;
-                const uint32_t base = p * 192;
-                uint64_t d_wq, d_tz, d_zp, d_kr, d_vr;
-                descs(buf, d_wq, d_tz, d_zp, d_kr, d_vr);
-                const uint64_t d_vk = tile_desc_mn(smem_u32(sm + L::VK + buf * 8192), 64, 0);
-                // Each barrier below is waited on by its consumers before it can
-                // complete again: the outputs of the previous block must be read
-                // (which also frees this parity's accumulators), and the state
-                // copy for this block written, before this block's products.
-                if (!DELTA) ok = ok && mbar_wait(&bars->ready[buf], (blk >> 1) & 1);
-                if (blk >= 1) ok = ok && mbar_wait(&bars->tfree[p ^ 1], ((blk - 1) >> 1) & 1);
+                const int buf = blk & 1;
+                const uint32_t base = (blk & 1) * 192;
+                const uint64_t d_wq = wq_desc(buf), d_kr = kr_desc(buf), d_vk = vk_desc(buf);
+                ok = mbar_wait(&bars->ready[buf], (blk >> 1) & 1);
+                // accumulators of this parity free: outputs of block blk-2 read
+                if (blk >= 2) ok = ok && mbar_wait(&bars->tfree[blk & 1], ((blk >> 1) - 1) & 1);
                 ok = ok && mbar_wait(&bars->s, blk & 1);
                 if (!ok) break;
                 tc_fence_after();
-                // S1 = [-W; gQ] S^T in two K halves
+                // S1 = [-W; Q] S^T in two K halves
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks)
                     mma_bf16(tmem + base + (ks < KH ? 0 : 32), kdesc_step(d_wq, 128, ks),
                              mndesc_step(d_sb, ks), id_kn, (ks == 0 || ks == KH) ? 0u : 1u);
-                if (!DELTA) {
-                    // Delta S = K^T (kd V); its commit also covers S1, which reads the
-                    // bf16 state copy the epilogue overwrites once Delta S is done
-#pragma unroll
-                    for (int ks = 0; ks < C / 16; ++ks)
-                        mma_bf16(tmem + base + (ks < 2 ? 128 : 160), mndesc_step(d_kr, ks),
-                                 mndesc_step(d_vk, ks), id_nn, (ks & 1) ? 1u : 0u);
-                    mma_commit(&bars->ds);
-                }
                 if (DELTA) {
                     mma_commit(&bars->g1);
                     ok = mbar_wait(&bars->u, blk & 1);
                     if (!ok) break;
                     tc_fence_after();
-#pragma unroll
-                    for (int ks = 0; ks < C / 16; ++ks)
-                        mma_bf16(tmem + base + (ks < 2 ? 128 : 160), mndesc_step(d_kr, ks),
-                                 mndesc_step(d_ubk, ks), id_nn, (ks & 1) ? 1u : 0u);
-                    mma_commit(&bars->ds);
                 }
-                const uint64_t d_x = DELTA ? d_ub : d_vr;  // U, or V without delta
+                // Delta S^T = K^T (kd U), or K^T (kd V) without delta; the commit also
+                // covers S1, which reads the bf16 state copy the epilogue rewrites
+                // once Delta S is done
+                const uint64_t d_b = DELTA ? d_ubk : d_vk;
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks)
+                    mma_bf16(tmem + base + (ks < 2 ? 128 : 160), mndesc_step(d_kr, ks),
+                             mndesc_step(d_b, ks), id_nn, (ks & 1) ? 1u : 0u);
+                mma_commit(&bars->ds);
+                mma_commit(&bars->empty[buf]);
+            }
+        }
+    } else if (warp == 1) {
+        // ============================================ off-chain products
+        if (lane == 0) {
+            const uint64_t d_ub = tile_desc_mn(smem_u32(UB), 64, 0);
+            auto issue_ut = [&](int blk) {  // Ut = T diag(beta) V  (delta only)
+                const int buf = blk & 1;
+                const uint64_t d_tz = tz_desc(buf), d_vr = vr_desc(buf);
+                const uint32_t col = (blk & 1) * 192 + 64;
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks)
+                    mma_bf16(tmem + col, kdesc_step(d_tz, 192, ks), mndesc_step(d_vr, ks), id_kn,
+                             ks > 0);
+                mma_commit(&bars->ut);
+            };
+            if (DELTA && nblk > 0) {
+                ok = mbar_wait(&bars->ready[0], 0);
+                if (ok) {
+                    tc_fence_after();
+                    issue_ut(0);
+                }
+            }
+            for (int blk = 0; blk < nblk && ok; ++blk) {
+                const int buf = blk & 1;
+                const uint32_t base = (blk & 1) * 192;
+                const uint64_t d_zp = zp_desc(buf);
+                if (DELTA) {
+                    ok = mbar_wait(&bars->u, blk & 1);
+                } else {
+                    ok = mbar_wait(&bars->ready[buf], (blk >> 1) & 1);
+                    if (blk >= 2) ok = ok && mbar_wait(&bars->tfree[blk & 1], ((blk >> 1) - 1) & 1);
+                }
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t d_x = DELTA ? d_ub : vr_desc(buf);  // U, or V without delta
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks)
                     mma_bf16(tmem + base + 96, kdesc_step(d_zp, 192, ks), mndesc_step(d_x, ks),
                              id_kn, ks > 0);
-                mma_commit(&bars->pu);
+                mma_commit(&bars->pu[blk & 1]);
                 mma_commit(&bars->empty[buf]);
                 if (DELTA && blk + 1 < nblk) {
                     ok = mbar_wait(&bars->ready[buf ^ 1], ((blk + 1) >> 1) & 1);
@@ -672,7 +695,7 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         }
     } else if (warp < 4) {
         // ========================================================== producers
-        const int pt = tid - 32;
+        const int pt = tid - 64;
         for (int blk = 0; blk < nblk && ok; ++blk) {
             const int buf = blk & 1;
             if (blk >= 2) ok = mbar_wait(&bars->empty[buf], ((blk >> 1) - 1) & 1);
@@ -774,6 +797,7 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
             float gC, gr = 0.f, kdi = 0.f;
             if (DELTA) {
                 ok = mbar_wait(&bars->g1, blk & 1);
+                if (warp < 6) ok = ok && mbar_wait(&bars->ut, blk & 1);  // only the U rows need Ut
                 if (!ok) break;
                 tc_fence_after();
                 gC = vec[64 + C - 1];
@@ -832,7 +856,7 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                 mbar_arrive(&bars->s);
             }
             if (warp >= 6) {  // output rows = tokens 0..63
-                ok = mbar_wait(&bars->pu, blk & 1);
+                ok = mbar_wait(&bars->pu[p], (blk >> 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
                 const int r = j - 64;
