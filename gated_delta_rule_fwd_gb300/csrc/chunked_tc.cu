@@ -137,42 +137,72 @@ static_assert(16 * XP * 4 <= 8192, "solve scratch must fit inside the T tile");
 // floats so that a warp touching one column of 32 rows hits 32 banks.
 __device__ __forceinline__ int sw64(int r, int c) { return r * AP + c; }
 
-// One block row of the blocked UT inverse: with the rows of T above it done,
-//   X = A[rows b, cols < 16b] T[< 16b, < 16b];   T[rows b, cols < 16b] = -T_bb X.
-// 128 threads: thread = (row rr of the block, column group cg), columns cg + 8k.
+// D (16x8, fp32) += A (16x8, tf32) B (8x8, tf32): the warp-level tensor-core
+// product, fragments as in the PTX m16n8k8 layout (g = lane/4, t = lane%4):
+// a = {A[g][t], A[g+8][t], A[g][t+4], A[g+8][t+4]}, b = {B[t][g], B[t+4][g]},
+// d = {D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1]}.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One block row BR of the blocked UT inverse (rows 16BR..16BR+15), with the
+// rows above it done:
+//   X = A[rows, cols < 16BR] T[< 16BR, < 16BR];   T[rows, cols < 16BR] = -T_bb X
+// on the tensor cores (m16n8k8, tf32 in, fp32 accumulate).  Warp w takes the
+// 8-column tiles nt = w, w+4, ...; K steps that only meet the zero blocks of T
+// above its block diagonal are skipped, so those blocks are never read.
 template <int BR>
 __device__ __forceinline__ void ut_block_row(const float *Am, float *Tm, float *Xt, int tid) {
-    constexpr int NC = 2 * BR;  // columns per thread (16*BR columns / 8 groups)
-    const int rr = tid & 15, cg = tid >> 4;
-    const int row = 16 * BR + rr;
-    float acc[NC];
-#pragma unroll
-    for (int k = 0; k < NC; ++k) acc[k] = 0.f;
-#pragma unroll 4
-    for (int i = 0; i < 16 * BR; ++i) {
-        const float a = Am[sw64(row, i)];
-#pragma unroll
-        for (int k = 0; k < NC; ++k) acc[k] += a * Tm[sw64(i, cg + 8 * k)];
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int r0 = 16 * BR;
+    for (int nt = warp; nt < 2 * BR; nt += 4) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int kk = 2 * (nt >> 1); kk < 2 * BR; ++kk) {
+            const uint32_t a[4] = {to_tf32(Am[(r0 + g) * AP + 8 * kk + t]),
+                                   to_tf32(Am[(r0 + g + 8) * AP + 8 * kk + t]),
+                                   to_tf32(Am[(r0 + g) * AP + 8 * kk + t + 4]),
+                                   to_tf32(Am[(r0 + g + 8) * AP + 8 * kk + t + 4])};
+            mma_tf32(d, a, to_tf32(Tm[(8 * kk + t) * AP + 8 * nt + g]),
+                     to_tf32(Tm[(8 * kk + t + 4) * AP + 8 * nt + g]));
+        }
+        Xt[g * XP + 8 * nt + 2 * t] = d[0];
+        Xt[g * XP + 8 * nt + 2 * t + 1] = d[1];
+        Xt[(g + 8) * XP + 8 * nt + 2 * t] = d[2];
+        Xt[(g + 8) * XP + 8 * nt + 2 * t + 1] = d[3];
     }
-#pragma unroll
-    for (int k = 0; k < NC; ++k) Xt[rr * XP + cg + 8 * k] = acc[k];
     __syncthreads();
+    for (int nt = warp; nt < 2 * BR; nt += 4) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int k = 0; k < NC; ++k) acc[k] = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const float t = Tm[sw64(row, 16 * BR + i)];
-#pragma unroll
-        for (int k = 0; k < NC; ++k) acc[k] += t * Xt[i * XP + cg + 8 * k];
+        for (int kk = 0; kk < 2; ++kk) {
+            const uint32_t a[4] = {to_tf32(Tm[(r0 + g) * AP + r0 + 8 * kk + t]),
+                                   to_tf32(Tm[(r0 + g + 8) * AP + r0 + 8 * kk + t]),
+                                   to_tf32(Tm[(r0 + g) * AP + r0 + 8 * kk + t + 4]),
+                                   to_tf32(Tm[(r0 + g + 8) * AP + r0 + 8 * kk + t + 4])};
+            mma_tf32(d, a, to_tf32(Xt[(8 * kk + t) * XP + 8 * nt + g]),
+                     to_tf32(Xt[(8 * kk + t + 4) * XP + 8 * nt + g]));
+        }
+        Tm[(r0 + g) * AP + 8 * nt + 2 * t] = -d[0];
+        Tm[(r0 + g) * AP + 8 * nt + 2 * t + 1] = -d[1];
+        Tm[(r0 + g + 8) * AP + 8 * nt + 2 * t] = -d[2];
+        Tm[(r0 + g + 8) * AP + 8 * nt + 2 * t + 1] = -d[3];
     }
-#pragma unroll
-    for (int k = 0; k < NC; ++k) Tm[sw64(row, cg + 8 * k)] = -acc[k];
     __syncthreads();
 }
 
-// T = (I + A)^-1 for a strictly lower A (64 x 64, fp32 in shared memory).
-// Tm must hold zeros in the blocks above the block diagonal on entry; on exit
-// it holds T's lower triangle with zeros above the diagonal.
+// T = (I + A)^-1 for a strictly lower A (64 x 64, fp32 in shared memory).  On
+// exit Tm holds T's lower triangle (diagonal blocks include their zero upper
+// triangles); the blocks above the block diagonal are never written or read.
 __device__ __forceinline__ void ut_inverse(const float *Am, float *Tm, float *Xt, int tid) {
     if (tid < 64) {
         const int b = tid >> 4, c = tid & 15;
@@ -201,7 +231,8 @@ template <int DK, bool ALPHA, bool DELTA>
 __global__ void __launch_bounds__(NT)
 chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                   const float *__restrict__ alpha, const float *__restrict__ beta,
-                  uint8_t *__restrict__ ws, int H, int T, int nblk) {
+                  uint8_t *__restrict__ ws, int H, int T, int nblk,
+                  const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk) {
     using L = PrepLayout<DK>;
     using R = Rec<DK>;
     extern __shared__ uint8_t sm_raw[];
@@ -220,21 +251,35 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     float *Gv = reinterpret_cast<float *>(sm + L::VEC);
     float *giv = Gv + 64, *gv = Gv + 128, *bv = Gv + 192;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 32);
 
-    // ---- stage Q, K (zero-filled past the end) and the gates
-    constexpr int CPR = DK / 8;
-    for (int idx = tid; idx < 2 * C * CPR; idx += NT) {
-        const int which = idx / (C * CPR);
-        const int rem = idx % (C * CPR);
-        const int r = rem / CPR, ch = rem % CPR;
-        const bool ok = r < n;
-        const bf16 *src = (which ? k : q) + ((bh * T + (ok ? t0 + r : 0)) * DK + ch * 8);
-        cp_async16(smem_u32(QK + sw128_offset(which * 64 + r, ch * 8, 128)), src, ok);
+    // ---- stage Q, K (zero-filled past the end: tiled TMA for dk >= 64, cp.async
+    //      otherwise) and the gates
+    uint64_t *lbar = bar + 2;
+    constexpr bool kTma = DK >= 64;
+    if (kTma) {
+        if (tid == 0) {
+            mbar_init(lbar, 1);
+            fence_mbar_init();
+            mbar_expect_tx(lbar, 2u * (uint32_t)L::KB * 8192u);
+#pragma unroll
+            for (int kb = 0; kb < L::KB; ++kb) {
+                tma_load_3d(QK + kb * 16384, &tmq, kb * 64, t0, (int)bh, lbar);
+                tma_load_3d(QK + kb * 16384 + 8192, &tmk, kb * 64, t0, (int)bh, lbar);
+            }
+        }
+    } else {
+        constexpr int CPR = DK / 8;
+        for (int idx = tid; idx < 2 * C * CPR; idx += NT) {
+            const int which = idx / (C * CPR);
+            const int rem = idx % (C * CPR);
+            const int r = rem / CPR, ch = rem % CPR;
+            const bool okr = r < n;
+            const bf16 *src = (which ? k : q) + ((bh * T + (okr ? t0 + r : 0)) * DK + ch * 8);
+            cp_async16(smem_u32(QK + sw128_offset(which * 64 + r, ch * 8, 128)), src, okr);
+        }
+        cp_async_commit();
     }
-    cp_async_commit();
-    if (DELTA)  // zero the blocks above the diagonal of T, which the solve never writes
-        for (int i = tid; i < C * AP; i += NT) Tm[i] = 0.f;
     float la = 0.f, b = 0.f;
     if (tid < C && tid < n) {
         if (ALPHA) la = __logf(alpha[bh * T + t0 + tid]);
@@ -277,14 +322,15 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         vec[128 + tid] = ALPHA ? __expf(Gv[C - 1] - G) : 1.f;
         vec[192 + tid] = b;
     }
-    cp_async_wait_all();
+    bool ok = true;
+    if (kTma) ok = mbar_wait(lbar, 0);
+    else cp_async_wait_all();
     fence_async_smem();
     tc_fence_before();
-    __syncthreads();
+    ok = __syncthreads_and(ok ? 1 : 0) != 0;
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-    bool ok = true;
 
     // ---- E1: [Q; K] K^T -> TMEM cols [0, 64)
     if (tid == 0) {
@@ -295,10 +341,10 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                      id, ks > 0);
         mma_commit(bar);
     }
-    ok = __syncthreads_and(mbar_wait(bar, 0) ? 1 : 0) != 0;
+    ok = __syncthreads_and((ok && mbar_wait(bar, 0)) ? 1 : 0) != 0;
     tc_fence_after();
 
-    // ---- E2: P rows (bf16 tile to the workspace), A rows (fp32); then g K in place
+    // ---- E2: P rows (bf16 tile to the workspace), A rows (fp32)
     if (ok) {
         const int r = 32 * (warp & 1) + lane;
         const bool is_q = warp < 2;
@@ -326,43 +372,34 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                 for (int e = 0; e < 32; ++e) Am[sw64(r, half * 32 + e)] = br * a[e];
             }
         }
-        if (DELTA) {
-            // K rows of QK scaled by g (B operand of W, read MN-major)
-            for (int idx = tid; idx < C * (DK / 8); idx += NT) {
-                const int r2 = idx / (DK / 8), ch = idx % (DK / 8);
-                uint4 *p = reinterpret_cast<uint4 *>(QK + sw128_offset(64 + r2, ch * 8, 128));
-                const uint4 raw = *p;
-                const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
-                float x[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) x[t] = gv[r2] * __bfloat162float(e[t]);
-                *p = pack8(x);
-            }
-        }
     }
     tc_fence_before();  // the score columns are reused by W below
     __syncthreads();
 
     if (DELTA && ok) {
         ut_inverse(Am, Tm, Xt, tid);
-        // T diag(beta) (bf16) -> the T tile (over the solve scratch) and to the workspace
+        // T diag(beta) (bf16) -> workspace; T diag(beta g) -> the T tile (over the
+        // solve scratch), the A operand of W = T diag(beta g) K
         for (int idx = tid; idx < C * 8; idx += NT) {
             const int r = idx >> 3, i8 = idx & 7;
-            float t[8];
+            float t[8], tg[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) t[e] = Tm[sw64(r, i8 * 8 + e)] * bv[i8 * 8 + e];
-            const uint4 w4 = pack8(t);
+            for (int e = 0; e < 8; ++e) {
+                const int i = i8 * 8 + e;
+                t[e] = i <= r ? Tm[sw64(r, i)] * bv[i] : 0.f;
+                tg[e] = t[e] * gv[i];
+            }
             const uint32_t off = sw128_offset(r, i8 * 8, 64);
-            *reinterpret_cast<uint4 *>(TB + off) = w4;
-            *reinterpret_cast<uint4 *>(rec + R::TT + off) = w4;
+            *reinterpret_cast<uint4 *>(rec + R::TT + off) = pack8(t);
+            *reinterpret_cast<uint4 *>(TB + off) = pack8(tg);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
 
-        // ---- E3: T diag(beta) (g K) -> W, M = 64 (TMEM cols [0, DK): rows 16w..16w+15
-        //      in lanes 32w..32w+15 of warp w)
+        // ---- E3: T diag(beta g) K -> W, M = 64 (TMEM cols [0, DK): rows 16w..16w+15
+        //      in lanes 32w..32w+15 of warp w); K read MN-major from the K rows
         if (tid == 0) {
             const uint32_t id = idesc_bf16_f32_mn(64, DK, false, true);
 #pragma unroll
@@ -936,11 +973,6 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
     if (e != cudaSuccess) return e;
     e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC, slot + 12);
     if (e != cudaSuccess) return e;
-    prep<<<dim3(nblk, H, B), NT, PrepLayout<DK>::ALLOC, stream>>>(
-        static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), ALPHA ? alpha : nullptr,
-        DELTA ? beta : nullptr, static_cast<uint8_t *>(ws), H, T, nblk);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     CUtensorMap tmq, tmk;
     memset(&tmq, 0, sizeof(tmq));
     memset(&tmk, 0, sizeof(tmk));
@@ -950,6 +982,11 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
         e = make_rows_map(&tmk, k, DK, T, B * H);
         if (e != cudaSuccess) return e;
     }
+    prep<<<dim3(nblk, H, B), NT, PrepLayout<DK>::ALLOC, stream>>>(
+        static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), ALPHA ? alpha : nullptr,
+        DELTA ? beta : nullptr, static_cast<uint8_t *>(ws), H, T, nblk, tmq, tmk);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     scan<<<dim3(dv / DVS, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
         static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), static_cast<const bf16 *>(v),
         static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, tmq,
