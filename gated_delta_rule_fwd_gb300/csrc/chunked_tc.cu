@@ -573,17 +573,24 @@ __device__ __forceinline__ void scan_scale(uint8_t *sm, int buf, int tid) {
 constexpr int kScanThreads = 256;
 constexpr int kProducers = 64;
 
+// Arrive once per warp on `bar`: every lane has finished its part (and its own
+// fences) before lane 0 arrives.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 struct ScanBars {
-    uint64_t ready[2];  // buffer filled                                   (64 producers)
+    uint64_t ready[2];  // buffer filled                                   (2 producer warps)
     uint64_t full[2];   // loads landed                                    (1 + tx bytes)
-    uint64_t empty[2];  // both issuers done with the buffer + epilogue read its gates (2 + 128)
-    uint64_t tfree[2];  // output rows of the block with this parity read  (64)
+    uint64_t empty[2];  // both issuers done with the buffer + epilogue read its gates (2 + 4 warps)
+    uint64_t tfree[2];  // output rows of the block with this parity read  (2 warps)
     uint64_t g1;        // S1 products done                                (commit)
     uint64_t ut;        // Ut products done                                (commit)
-    uint64_t u;         // U rows written                                  (64)
+    uint64_t u;         // U rows written                                  (2 warps)
     uint64_t ds;        // Delta S products done                           (commit)
     uint64_t pu[2];     // P U products of the block with this parity done (commit)
-    uint64_t s;         // bf16 state copy written                         (128)
+    uint64_t s;         // bf16 state copy written                         (4 warps)
     uint32_t tmem;
 };
 
@@ -610,18 +617,18 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         reinterpret_cast<uint4 *>(sm)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&bars->ready[b], kProducers);
+            mbar_init(&bars->ready[b], kProducers / 32);
             mbar_init(&bars->full[b], 1);
-            mbar_init(&bars->empty[b], 2 + 128);
-            mbar_init(&bars->tfree[b], 64);
+            mbar_init(&bars->empty[b], 2 + 4);
+            mbar_init(&bars->tfree[b], 2);
         }
         mbar_init(&bars->g1, 1);
         mbar_init(&bars->ut, 1);
-        mbar_init(&bars->u, 64);
+        mbar_init(&bars->u, 2);
         mbar_init(&bars->ds, 1);
         mbar_init(&bars->pu[0], 1);
         mbar_init(&bars->pu[1], 1);
-        mbar_init(&bars->s, 128);
+        mbar_init(&bars->s, 4);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -736,6 +743,7 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         for (int blk = 0; blk < nblk && ok; ++blk) {
             const int buf = blk & 1;
             if (blk >= 2) ok = mbar_wait(&bars->empty[buf], ((blk >> 1) - 1) & 1);
+            ok = __all_sync(0xffffffffu, ok);  // warp-uniform, for the warp-level arrives
             if (!ok) break;
             const int t0 = blk * C;
             const uint8_t *rec = recs + (size_t)blk * R::BYTES;
@@ -787,7 +795,7 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
             }
             cp_async_commit();
             cp_async_wait_all();
-            ok = mbar_wait(&bars->full[buf], (blk >> 1) & 1);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->full[buf], (blk >> 1) & 1));
             if (!ok) break;
             if (!DELTA) {
                 // kd V (B operand of Delta S = K^T diag(kd) V); g and kd are folded
@@ -807,7 +815,7 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                 }
             }
             fence_async_smem();
-            mbar_arrive(&bars->ready[buf]);
+            warp_arrive(&bars->ready[buf]);
         }
     } else {
         // =========================================================== epilogue
@@ -822,7 +830,7 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                 *reinterpret_cast<uint4 *>(SB + sw128_offset(j, c8 * 8, DK)) = pack8(Sr + c8 * 8);
         }
         fence_async_smem();
-        mbar_arrive(&bars->s);
+        warp_arrive(&bars->s);
         for (int blk = 0; blk < nblk && ok; ++blk) {
             const int buf = blk & 1, p = blk & 1;
             const uint32_t base = p * 192;
@@ -835,12 +843,13 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
             if (DELTA) {
                 ok = mbar_wait(&bars->g1, blk & 1);
                 if (warp < 6) ok = ok && mbar_wait(&bars->ut, blk & 1);  // only the U rows need Ut
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
                 gC = vec[64 + C - 1];
                 if (warp >= 6) gr = vec[64 + j - 64];
                 else kdi = vec[128 + j];
-                mbar_arrive(&bars->empty[buf]);
+                warp_arrive(&bars->empty[buf]);
                 if (warp < 6) {  // U rows = tokens 0..63
                     float u[32], x[32];
                     tmem_ld32(tmem + lane_base + base + 64, u);
@@ -864,16 +873,16 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                             pack8(u + c8 * 8);
                     fence_async_smem();
                     tc_fence_before();
-                    mbar_arrive(&bars->u);
+                    warp_arrive(&bars->u);
                 }
             }
-            ok = mbar_wait(&bars->ds, blk & 1);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->ds, blk & 1));
             if (!ok) break;
             tc_fence_after();
             if (!DELTA) {
                 gC = vec[64 + C - 1];
                 if (warp >= 6) gr = vec[64 + j - 64];
-                mbar_arrive(&bars->empty[buf]);
+                warp_arrive(&bars->empty[buf]);
             }
             {
                 float d[32], e[32];
@@ -890,10 +899,10 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                 }
                 fence_async_smem();
                 tc_fence_before();
-                mbar_arrive(&bars->s);
+                warp_arrive(&bars->s);
             }
             if (warp >= 6) {  // output rows = tokens 0..63
-                ok = mbar_wait(&bars->pu[p], (blk >> 1) & 1);
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars->pu[p], (blk >> 1) & 1));
                 if (!ok) break;
                 tc_fence_after();
                 const int r = j - 64;
@@ -908,7 +917,7 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
 #pragma unroll
                 for (int c = 0; c < 32; ++c) d[c] += e[c];              // + P U
                 tc_fence_before();
-                mbar_arrive(&bars->tfree[p]);
+                warp_arrive(&bars->tfree[p]);
                 if (r < n) {
                     uint4 *dst = reinterpret_cast<uint4 *>(o + (bh * T + t0 + r) * dv + c0);
 #pragma unroll
