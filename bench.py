@@ -39,6 +39,35 @@ METRIC = "chunked fwd tokens/s"
 UNIT = "tokens/s"
 
 
+# DRAM traffic per lr_fwd_chunked call (prep + scan launches) from one ncu
+# capture of each kernel (dram__bytes_read.sum + dram__bytes_write.sum), tied
+# to the kernel source it was taken on: reported only while that source is
+# unchanged (profiles/chunk_prep_gdn_prefill_b2h16t16384.md and
+# profiles/chunk_scan_gdn_prefill_b2h16t16384.md).
+TRAFFIC_SOURCES = ("gated_delta_rule_fwd_gb300/csrc/chunked_tc.cu",
+                   "gated_delta_rule_fwd_gb300/csrc/tc_common.cuh")
+TRAFFIC = {
+    "gdn_prefill_bf16": {"bytes": 272.721408e6 + 224.870656e6 + 681.656320e6 + 121.073408e6,
+                         "sha256": "c12dc0985642e7979a9637abd29e6ebc84a6ce228c796e818a1e4e80675edd3b"},
+}
+
+
+def kernel_source_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(w):
+    t = TRAFFIC.get(w.name)
+    if t is None or t["sha256"] != kernel_source_sha256():
+        return None
+    return t["bytes"]
+
+
 # --------------------------------------------------------------- work counts
 
 def head_token_bytes(w):
@@ -311,14 +340,15 @@ def run_ours(args, dist, rank, world, local):
                        "l2": "inputs 545 MB > 129 MB L2, no flush between steps"},
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
-                         "traffic": args.traffic, "peak_source": peaks["source"] + " burst copy",
+                         "traffic": args.traffic if args.traffic is not None else measured_traffic(w), "peak_source": peaks["source"] + " burst copy",
                          "algorithmic_bytes_per_launch": nbytes},
             "tensor": {"achieved_tflops": achieved_tf, "peak_tflops": peaks["bf16_tflops"],
                        "frac_of_bf16_peak": achieved_tf / peaks["bf16_tflops"],
                        "flops_per_launch": nflops, "count": "chunk-form MMA flops"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-            "gpu_launches": args.steps,
+            # lr_fwd_chunked launches chunk_prep + chunk_scan for bf16, one kernel for fp32
+            "gpu_launches": args.steps * (2 if w.dtype == "bf16" else 1),
             "clocks": clocks.summary(wall0, wall1),
             "cpu_baseline": cpu,
         }
