@@ -3,51 +3,62 @@
 //
 // Chunkwise form (page "Le architetture lineari: RetNet, RWKV, xLSTM",
 // section "RetNet: la retention e le sue tre forme"): blocks of C = 64
-// tokens, only the end-of-block state handed to the next block.  Inside a
-// block, with G_r = sum_{i<=r} ln alpha_i (gate products, computable for all
+// tokens, only the end-of-block state handed to the next block.  Inside block
+// j, with G_r = sum_{i<=r} ln alpha_i (gate products, computable for all
 // steps at once -- page "Scrivere meglio nella memoria: gate e delta rule",
-// section "Correggere: la delta rule"), g_r = e^{G_r}, kd_i = e^{G_C - G_i}:
+// section "Correggere: la delta rule"), g_r = e^{G_r}, kd_i = e^{G_C - G_i},
+// g_C = e^{G_C} and S_j the state when the block starts:
 //
-//   P  = (Q K^T) (.) M,          M_ri = e^{G_r - G_i} for i <= r        (scores)
-//   A  = strict_lower(diag(beta) (K K^T) (.) M)                        (delta couplings)
-//   T  = (I + A)^-1              unit lower triangular (the WY / UT step)
-//   W  = T diag(beta g) K,       Ut = T diag(beta) V
-//   U  = Ut - W S^T              pseudo-values u_r of the WY representation
-//   O  = diag(g) Q S^T + P U
-//   S <- g_C S + U^T diag(kd) K
+//   P_j = (Q K^T) (.) M,        M_ri = e^{G_r - G_i} for i <= r        (scores)
+//   A_j = strict_lower(diag(beta) (K K^T) (.) M)                       (delta couplings)
+//   T_j = (I + A_j)^-1          unit lower triangular (the WY / UT step)
+//   W_j = T_j diag(beta g) K,   Ut_j = T_j diag(beta) V
+//   U_j = Ut_j - W_j S_j^T      pseudo-values u_r of the WY representation
+//   O_j = diag(g) Q S_j^T + P_j U_j
+//   S_{j+1} = g_C S_j + U_j^T diag(kd) K
 // and without the delta term U = V.  The derivation: the gated recurrence
 // unrolled inside a block gives u_r = beta_r (v_r - g_r S k_r -
 // sum_{i<r} e^{G_r - G_i} (k_i.k_r) u_i), a unit-lower-triangular system.
 //
+// Look-ahead form used by the scan.  Substituting the state update into the
+// next block's U gives
+//   U_{j+1} = Ut_{j+1} - g_C W_{j+1} S_j^T - Z_j U_j,
+//   Z_j = W_{j+1} K_j^T diag(kd_j)          (64 x 64, independent of the state)
+// so one accumulator D_{j+1} (M = 128 rows) collects
+//   rows  0..63:  [T diag(beta)]_{j+1} V_{j+1} + (-g_C W_{j+1}) S_j^T + (-Z_j) U_j  = U_{j+1}
+//   rows 64..127:                                   Q_j S_j^T  +  P_j U_j         (O_j before g)
+// from three products whose A operands stack a row block of block j+1 on a
+// row block of block j.  The loop-carried chain is then U_j -> one K = 64
+// product -> U_{j+1}; the state update S_{j+1} = g_C S_j + K_j^T (kd U_j)
+// runs beside it and is needed one block later.
+//
 // Two launches:
 //  * prep: one CTA per (block, head, batch), all blocks in parallel.  Computes
-//    what does not depend on the state: G, the scores P, the UT inverse T
-//    (blocked forward substitution in fp32 on the CUDA cores) and -W, and
-//    writes -W, T and P to the workspace as bf16 tiles already in the
-//    shared-memory operand layout, plus the per-token gate vectors.
+//    what does not depend on the state: the gates, the scores P, the UT
+//    inverse T (fp32; 16 x 16 diagonal blocks on the CUDA cores, the block
+//    rows on warp-level tf32 MMAs), W and Z, and writes the workspace record
+//    of "stage" j: -g_C' W_j, T_j diag(beta), -Z_{j-1}, P_{j-1} and the gate
+//    vectors, as bf16 tiles already in the shared-memory operand layout
+//    (primes: the previous block).  Stage j's P row block is written by the
+//    CTA of block j-1; there is one more stage than blocks.
 //  * scan: one CTA per (32 value channels, head, batch); rows of S evolve
 //    independently given k, alpha and beta, so slices never exchange data.
-//    The loop over blocks is sequential; the next block's tiles are fetched
-//    and its operand tiles built while the current block's products run.
+//    It walks the stages in order with warp-specialised roles (below).
 //
-// Every product runs as an M = 128 tcgen05.mma with K-major 128-byte-swizzled
-// shared-memory operands and an fp32 accumulator in tensor memory; 64-row
-// operands are stacked to fill M:
-//   prep  E1  [Q; K] K^T            -> [Q K^T ; K K^T]
-//         E3  [T; 0] (beta g K)^T   -> [W ; 0]
-//   scan      [T diag(beta); 0] V  -> [Ut ; 0]
-//             [-W; Q] S^T          -> [-W S^T ; Q S^T]    (two K halves)
-//             K^T (kd U)           -> Delta S^T           (K read MN-major)
-//             [0; P] U             -> rows 64..127 = P U
-//   with U = Ut - W S^T and O = diag(g) Q S^T + P U formed in the epilogues.
-// The fp32 master copy of the state slice lives in registers (thread j owns
-// column j); a bf16 copy in shared memory feeds the next block.  A final
-// short block is zero-filled (alpha treated as 1, beta as 0), which leaves
-// the real tokens' results unchanged.
+// Every product runs as an M = 128 tcgen05.mma with 128-byte-swizzled
+// shared-memory operands and an fp32 accumulator in tensor memory:
+//   prep  E1  [Q; K] K^T              -> [Q K^T ; K K^T]
+//         E3  T diag(beta g) K        -> W           (M = 64, K read MN-major)
+//         E4  W K'^T                  -> Z'          (M = 64)
+//   scan  a   [T diag(beta); *] V     -> Ut rows
+//         b   [-g_C' W; Q'] S'^T      -> U and O' parts
+//         c   [-Z'; P'] U'            -> U and O' parts
+//         ds  K'^T (kd' U')           -> Delta S'^T  (K read MN-major)
+// A final short block is zero-filled (alpha treated as 1, beta as 0), which
+// leaves the real tokens' results unchanged.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include <cstring>
 #include <mutex>
 
 #include "lr_internal.cuh"
@@ -61,35 +72,24 @@ using namespace tc;
 
 constexpr int C = 64;      // tokens per block
 constexpr int DVS = 32;    // value channels per scan CTA
-constexpr int NT = 128;    // threads per CTA
+constexpr int NT = 128;    // threads per prep CTA
 constexpr int AP = C + 1;  // padded fp32 row of A and T
 constexpr int XP = 49;     // padded fp32 row of the solve scratch
 
 __device__ int g_tc_error = 0;  // set to 1 when a bounded wait gives up
 
-// Workspace record of one (head, block), written by prep and read by scan.
+// Workspace record of stage j of one head (stages 0..nblk), written by the
+// prep CTAs of blocks j and j-1 and read by the scan.
 template <int DK>
 struct Rec {
     static constexpr int KB = (DK + 63) / 64;
-    static constexpr int WT = 0;                 // -W: KB blocks of [64 rows][128 B]
-    static constexpr int TT = WT + KB * 8192;    // T:  [64][64] bf16 tile
-    static constexpr int PT = TT + 8192;         // P:  [64][64] bf16 tile
-    static constexpr int VEC = PT + 8192;        // G, g, kd, beta: 4 x 64 fp32
+    static constexpr int WT = 0;                // -g_C' W_j: KB blocks of [64 rows][128 B]
+    static constexpr int TZP = WT + KB * 8192;  // [192 rows][64] bf16: T_j diag(beta), -Z_{j-1}, P_{j-1}
+    static constexpr int VEC = TZP + 24576;     // fp32: g' [64], kd' [64], kd [64], g_C'
     static constexpr int BYTES = VEC + 1024;
 };
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, bool valid) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
-                 "r"(valid ? 4 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// offsets (in floats) inside the gate vector of a record
+constexpr int kVgPrev = 0, kVkdPrev = 64, kVkd = 128, kVgCPrev = 192;
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
@@ -104,12 +104,6 @@ __device__ __forceinline__ uint4 pack8(const float *x) {
     r.w = pack_bf16(x[6], x[7]);
     return r;
 }
-__device__ __forceinline__ float bf16_at(const uint8_t *tile, uint32_t off) {
-    return __bfloat162float(*reinterpret_cast<const bf16 *>(tile + off));
-}
-__device__ __forceinline__ void st_bf16(uint8_t *tile, uint32_t off, float x) {
-    *reinterpret_cast<bf16 *>(tile + off) = __float2bfloat16_rn(x);
-}
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) &
@@ -121,17 +115,18 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 template <int DK>
 struct PrepLayout {
     static constexpr int KB = (DK + 63) / 64;
-    static constexpr int QK = 0;                            // [128 rows][DK]: Q rows, K rows
-    static constexpr int TB = QK + 128 * 128 * KB;          // [64][64] bf16: T diag(beta)
+    static constexpr int QK = 0;                            // [128 rows][DK]: Q rows (later K'), K rows
+    static constexpr int TB = QK + 128 * 128 * KB;          // [64][64] bf16: T diag(beta g)
     static constexpr int XT = TB;                           // fp32 [16][XP] solve scratch, inside TB
-    static constexpr int AM = TB + 8192;                    // fp32 [64][AP]
+    static constexpr int AM = TB + 8192;                    // fp32 [64][AP]; later bf16 W [64][DK]
     static constexpr int TM = AM + C * AP * 4;              // fp32 [64][AP]
-    static constexpr int VEC = TM + C * AP * 4;             // G, ginv, g, beta
-    static constexpr int BAR = VEC + 4 * 64 * 4;
+    static constexpr int VEC = TM + C * AP * 4;             // G (later kd'), ginv, g, beta
+    static constexpr int BAR = VEC + 4 * 64 * 4;            // 3 barriers, TMEM slot, g_C'
     static constexpr int BYTES = BAR + 64;
     static constexpr int ALLOC = BYTES + 1024;
 };
 static_assert(16 * XP * 4 <= 8192, "solve scratch must fit inside the T tile");
+static_assert(128 * 64 * 2 <= C * AP * 4, "the W tile must fit over the A matrix");
 
 // Element (r, c) of a 64 x 64 fp32 matrix in shared memory, rows padded to 65
 // floats so that a warp touching one column of 32 rows hits 32 banks.
@@ -227,6 +222,9 @@ __device__ __forceinline__ void ut_inverse(const float *Am, float *Tm, float *Xt
     ut_block_row<3>(Am, Tm, Xt, tid);
 }
 
+// Prep of block j = blockIdx.x.  Writes to record j: -g_C' W_j, T_j diag(beta),
+// -Z_{j-1} and the gate vectors; to record j+1: P_j (and, for the last block,
+// record j+1's gate vectors).
 template <int DK, bool ALPHA, bool DELTA>
 __global__ void __launch_bounds__(NT)
 chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
@@ -242,90 +240,92 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
     const int t0 = blk * C;
     const int n = min(C, T - t0);
-    uint8_t *rec = ws + (bh * nblk + blk) * (size_t)R::BYTES;
+    uint8_t *rec = ws + (bh * (nblk + 1) + blk) * (size_t)R::BYTES;
+    uint8_t *rec_next = rec + R::BYTES;
+    float *vec = reinterpret_cast<float *>(rec + R::VEC);
+    float *vec_next = reinterpret_cast<float *>(rec_next + R::VEC);
 
-    uint8_t *QK = sm + L::QK, *TB = sm + L::TB;
+    uint8_t *QK = sm + L::QK, *TB = sm + L::TB, *WB = sm + L::AM;
     float *Am = reinterpret_cast<float *>(sm + L::AM);
     float *Tm = reinterpret_cast<float *>(sm + L::TM);
     float *Xt = reinterpret_cast<float *>(sm + L::XT);
     float *Gv = reinterpret_cast<float *>(sm + L::VEC);
     float *giv = Gv + 64, *gv = Gv + 128, *bv = Gv + 192;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
+    float *kdv = Gv;  // kd of the previous block, once G is no longer needed
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);  // MMA, q/k tiles, previous k tile
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 32);
+    float *gcp_slot = reinterpret_cast<float *>(sm + L::BAR + 48);
+    const bool zprev = DELTA && blk > 0;  // Z_{j-1} exists
 
-    // ---- stage Q, K (zero-filled past the end: tiled TMA for dk >= 64, cp.async
-    //      otherwise) and the gates
-    uint64_t *lbar = bar + 2;
-    constexpr bool kTma = DK >= 64;
-    if (kTma) {
-        if (tid == 0) {
-            mbar_init(lbar, 1);
-            fence_mbar_init();
-            mbar_expect_tx(lbar, 2u * (uint32_t)L::KB * 8192u);
-#pragma unroll
-            for (int kb = 0; kb < L::KB; ++kb) {
-                tma_load_3d(QK + kb * 16384, &tmq, kb * 64, t0, (int)bh, lbar);
-                tma_load_3d(QK + kb * 16384 + 8192, &tmk, kb * 64, t0, (int)bh, lbar);
-            }
-        }
-    } else {
-        constexpr int CPR = DK / 8;
-        for (int idx = tid; idx < 2 * C * CPR; idx += NT) {
-            const int which = idx / (C * CPR);
-            const int rem = idx % (C * CPR);
-            const int r = rem / CPR, ch = rem % CPR;
-            const bool okr = r < n;
-            const bf16 *src = (which ? k : q) + ((bh * T + (okr ? t0 + r : 0)) * DK + ch * 8);
-            cp_async16(smem_u32(QK + sw128_offset(which * 64 + r, ch * 8, 128)), src, okr);
-        }
-        cp_async_commit();
-    }
-    float la = 0.f, b = 0.f;
-    if (tid < C && tid < n) {
-        if (ALPHA) la = __logf(alpha[bh * T + t0 + tid]);
-        if (DELTA) b = beta[bh * T + t0 + tid];
-    }
+    // ---- stage Q, K by tiled TMA (zero-filled past the end of the sequence
+    //      and, for d_k = 32, in the outer half of the 64-column box)
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_init(&bar[2], 1);
         fence_mbar_init();
+        mbar_expect_tx(&bar[1], 2u * (uint32_t)L::KB * 8192u);
+#pragma unroll
+        for (int kb = 0; kb < L::KB; ++kb) {
+            tma_load_3d(QK + kb * 16384, &tmq, kb * 64, t0, (int)bh, &bar[1]);
+            tma_load_3d(QK + kb * 16384 + 8192, &tmk, kb * 64, t0, (int)bh, &bar[1]);
+        }
+    }
+    // ---- gates: warps 0-1 hold this block's tokens, warps 2-3 the previous
+    //      block's (all ones for block 0)
+    const int tok = tid & 63;
+    float la = 0.f, b = 0.f;
+    if (tid < C) {
+        if (tok < n) {
+            if (ALPHA) la = __logf(alpha[bh * T + t0 + tok]);
+            if (DELTA) b = beta[bh * T + t0 + tok];
+        }
+    } else if (ALPHA && blk > 0) {
+        la = __logf(alpha[bh * T + t0 - C + tok]);
     }
     if (warp == 0) {
         tmem_alloc(tmem_slot, 128);
         tmem_relinquish();
     }
-    // inclusive scan of ln alpha over the block (warps 0 and 1 hold the 64 values)
-    if (warp < 2) {
-        float incl = la;
+    float incl = la;  // inclusive scan within the warp
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= d) incl += y;
-        }
-        Gv[tid] = incl;  // warp 1 adds warp 0's total below
+    for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
     }
+    Am[tid] = incl;  // scratch (A is written only after E1)
     __syncthreads();
-    const float Gfull = tid < C ? Gv[tid] + (tid >= 32 ? Gv[31] : 0.f) : 0.f;
-    __syncthreads();
-    if (tid < C) Gv[tid] = Gfull;
-    __syncthreads();
+    const int pb = tid & 64;
+    const float G = incl + ((tid & 32) ? Am[pb + 31] : 0.f);
+    const float Glast = Am[pb + 31] + Am[pb + 63];
     // exp(G_r - G_i) = g_r * ginv_i when exp(-G_63) is finite in fp32
-    const bool factor = !ALPHA || Gv[C - 1] > -80.f;
+    const bool factor = !ALPHA || Am[31] + Am[63] > -80.f;
+    float kdp = 1.f;
     if (tid < C) {
-        const float G = Gv[tid];
         const float g = ALPHA ? __expf(G) : 1.f;
-        gv[tid] = g;
-        giv[tid] = ALPHA ? __expf(-G) : 1.f;
-        bv[tid] = b;
-        float *vec = reinterpret_cast<float *>(rec + R::VEC);
-        vec[tid] = G;
-        vec[64 + tid] = g;
-        vec[128 + tid] = ALPHA ? __expf(Gv[C - 1] - G) : 1.f;
-        vec[192 + tid] = b;
+        const float kd = ALPHA ? __expf(Glast - G) : 1.f;
+        Gv[tok] = G;
+        gv[tok] = g;
+        giv[tok] = ALPHA ? __expf(-G) : 1.f;
+        bv[tok] = b;
+        vec[kVkd + tok] = kd;
+        if (blk == nblk - 1) {  // the stage after the last block reads this block as its previous one
+            vec_next[kVgPrev + tok] = g;
+            vec_next[kVkdPrev + tok] = kd;
+            if (tok == C - 1) vec_next[kVgCPrev] = ALPHA ? __expf(Glast) : 1.f;
+        }
+    } else {
+        const float g = ALPHA ? __expf(G) : 1.f;
+        kdp = ALPHA ? __expf(Glast - G) : 1.f;
+        vec[kVgPrev + tok] = g;
+        vec[kVkdPrev + tok] = kdp;
+        if (tok == C - 1) {
+            const float gc = ALPHA ? __expf(Glast) : 1.f;
+            vec[kVgCPrev] = gc;
+            *gcp_slot = gc;
+        }
     }
-    bool ok = true;
-    if (kTma) ok = mbar_wait(lbar, 0);
-    else cp_async_wait_all();
-    fence_async_smem();
+    bool ok = mbar_wait(&bar[1], 0);
     tc_fence_before();
     ok = __syncthreads_and(ok ? 1 : 0) != 0;
     tc_fence_after();
@@ -333,18 +333,26 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
 
     // ---- E1: [Q; K] K^T -> TMEM cols [0, 64)
-    if (tid == 0) {
+    if (tid == 0 && ok) {
         const uint32_t id = idesc_bf16_f32(128, 64);
 #pragma unroll
         for (int ks = 0; ks < DK / 16; ++ks)
             mma_bf16(tmem, tile_desc(smem_u32(QK), 128, 0, ks), tile_desc(smem_u32(QK), 128, 64, ks),
                      id, ks > 0);
-        mma_commit(bar);
+        mma_commit(&bar[0]);
     }
-    ok = __syncthreads_and((ok && mbar_wait(bar, 0)) ? 1 : 0) != 0;
+    ok = __syncthreads_and((ok && mbar_wait(&bar[0], 0)) ? 1 : 0) != 0;
     tc_fence_after();
 
-    // ---- E2: P rows (bf16 tile to the workspace), A rows (fp32)
+    // ---- the Q rows are free: fetch the previous block's K rows there (for Z)
+    if (zprev && ok && tid == 0) {
+        mbar_expect_tx(&bar[2], (uint32_t)L::KB * 8192u);
+#pragma unroll
+        for (int kb = 0; kb < L::KB; ++kb)
+            tma_load_3d(QK + kb * 16384, &tmk, kb * 64, t0 - C, (int)bh, &bar[2]);
+    }
+
+    // ---- E2: P rows (bf16 tile to the next stage's record), A rows (fp32)
     if (ok) {
         const int r = 32 * (warp & 1) + lane;
         const bool is_q = warp < 2;
@@ -363,8 +371,8 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
             if (is_q) {
 #pragma unroll
                 for (int i8 = 0; i8 < 4; ++i8)
-                    *reinterpret_cast<uint4 *>(rec + R::PT +
-                                               sw128_offset(r, half * 32 + i8 * 8, 64)) =
+                    *reinterpret_cast<uint4 *>(rec_next + R::TZP +
+                                               sw128_offset(128 + r, half * 32 + i8 * 8, 192)) =
                         pack8(a + i8 * 8);
             } else if (DELTA) {
                 const float br = bv[r];
@@ -377,8 +385,9 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     __syncthreads();
 
     if (DELTA && ok) {
+        if (tid >= C) kdv[tok] = kdp;  // G is dead; read after the syncs below
         ut_inverse(Am, Tm, Xt, tid);
-        // T diag(beta) (bf16) -> workspace; T diag(beta g) -> the T tile (over the
+        // T diag(beta) (bf16) -> record; T diag(beta g) -> the T tile (over the
         // solve scratch), the A operand of W = T diag(beta g) K
         for (int idx = tid; idx < C * 8; idx += NT) {
             const int r = idx >> 3, i8 = idx & 7;
@@ -389,9 +398,8 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                 t[e] = i <= r ? Tm[sw64(r, i)] * bv[i] : 0.f;
                 tg[e] = t[e] * gv[i];
             }
-            const uint32_t off = sw128_offset(r, i8 * 8, 64);
-            *reinterpret_cast<uint4 *>(rec + R::TT + off) = pack8(t);
-            *reinterpret_cast<uint4 *>(TB + off) = pack8(tg);
+            *reinterpret_cast<uint4 *>(rec + R::TZP + sw128_offset(r, i8 * 8, 192)) = pack8(t);
+            *reinterpret_cast<uint4 *>(TB + sw128_offset(r, i8 * 8, 64)) = pack8(tg);
         }
         fence_async_smem();
         tc_fence_before();
@@ -406,13 +414,15 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
             for (int ks = 0; ks < C / 16; ++ks)
                 mma_bf16(tmem, tile_desc(smem_u32(TB), 64, 0, ks),
                          desc_mnmajor_sw128(smem_u32(QK) + 8192 + ks * 2048, 16384), id, ks > 0);
-            mma_commit(bar);
+            mma_commit(&bar[0]);
         }
-        ok = __syncthreads_and(mbar_wait(bar, 1) ? 1 : 0) != 0;
+        ok = __syncthreads_and(mbar_wait(&bar[0], 1) ? 1 : 0) != 0;
         tc_fence_after();
 
-        // ---- -W rows -> workspace
+        // ---- -g_C' W rows -> record; W rows (bf16) -> the W tile over A, the
+        //      A operand of Z
         if (ok) {
+            const float gcp = *gcp_slot;
             const int r = 16 * warp + lane;
 #pragma unroll
             for (int cb = 0; cb < DK / 32; ++cb) {
@@ -421,12 +431,54 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                 tmem_ld_wait();
                 if (lane < 16) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) w[e] = -w[e];
+                    for (int i8 = 0; i8 < 4; ++i8)
+                        *reinterpret_cast<uint4 *>(WB + sw128_offset(r, cb * 32 + i8 * 8, 64)) =
+                            pack8(w + i8 * 8);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) w[e] *= -gcp;
 #pragma unroll
                     for (int i8 = 0; i8 < 4; ++i8)
                         *reinterpret_cast<uint4 *>(rec + R::WT +
                                                    sw128_offset(r, cb * 32 + i8 * 8, 64)) =
                             pack8(w + i8 * 8);
+                }
+            }
+        }
+
+        // ---- E4: Z' = W K'^T (M = 64, N = 64 previous tokens, K = DK) -> TMEM
+        //      cols [0, 64); record rows 64..127 of the TZP tile get -Z' diag(kd')
+        if (zprev) {
+            ok = mbar_wait(&bar[2], 0) && ok;
+            fence_async_smem();
+            tc_fence_before();
+            ok = __syncthreads_and(ok ? 1 : 0) != 0;
+            tc_fence_after();
+            if (tid == 0 && ok) {
+                const uint32_t id = idesc_bf16_f32(64, 64);
+#pragma unroll
+                for (int ks = 0; ks < DK / 16; ++ks)
+                    mma_bf16(tmem, tile_desc(smem_u32(WB), 64, 0, ks),
+                             tile_desc(smem_u32(QK), 128, 0, ks), id, ks > 0);
+                mma_commit(&bar[0]);
+            }
+            ok = __syncthreads_and((ok && mbar_wait(&bar[0], 0)) ? 1 : 0) != 0;
+            tc_fence_after();
+            if (ok) {
+                const int r = 16 * warp + lane;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float z[32];
+                    tmem_ld32(tmem + lane_base + 32 * half, z);
+                    tmem_ld_wait();
+                    if (lane < 16) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) z[e] = -z[e] * kdv[half * 32 + e];
+#pragma unroll
+                        for (int i8 = 0; i8 < 4; ++i8)
+                            *reinterpret_cast<uint4 *>(
+                                rec + R::TZP + sw128_offset(64 + r, half * 32 + i8 * 8, 192)) =
+                                pack8(z + i8 * 8);
+                    }
                 }
             }
         }
@@ -442,136 +494,73 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
 template <int DK>
 struct ScanLayout {
     static constexpr int KB = (DK + 63) / 64;
-    static constexpr int WQ_BYTES = 128 * 128 * KB;          // [128][DK] K-major: -W rows, g Q rows
-    static constexpr int WQ = 0;                              // x2
-    static constexpr int TZP = WQ + 2 * WQ_BYTES;             // x2 [192][64] K-major: T diag(beta), 0, P
-    static constexpr int KR = TZP + 2 * 24576;                // x2 [64 tokens][128] MN-major: kd K
-    static constexpr int VR = KR + 2 * 16384;                 // x2 [64 tokens][32] MN-major: V slice
-    static constexpr int VK = VR + 2 * 8192;                  // x2 [64 tokens][32] MN-major: kd V (no delta)
-    static constexpr int VEC = VK + 2 * 8192;                 // x2 G, g, kd, beta
-    static constexpr int UB = VEC + 2 * 1024;                 // [64 tokens][32] MN-major: U (or V)
-    static constexpr int UBK = UB + 8192;                     // [64 tokens][32] MN-major: kd U (or kd V)
-    static constexpr int SB = UBK + 8192;                     // [DK][32] MN-major: bf16 state slice^T
-    static constexpr int BAR = SB + 128 * 128;
+    static constexpr int AW_BYTES = 128 * 128 * KB;  // [128][DK] K-major: -g_C' W rows, Q' rows
+    static constexpr int AW = 0;                      // x2
+    static constexpr int TZP = AW + 2 * AW_BYTES;     // x2 [192][64] K-major: T diag(beta), -Z', P'
+    static constexpr int KR = TZP + 2 * 24576;        // x2 [64 tokens][128] MN-major: K'
+    static constexpr int VR = KR + 2 * 16384;         // x2 [64 tokens][64] MN-major: v box (this CTA: 32 channels)
+    static constexpr int VEC = VR + 2 * 8192;         // x2 gate vectors of the stage
+    static constexpr int UB = VEC + 2 * 1024;         // [64 tokens][64] MN-major: U
+    static constexpr int UBK = UB + 8192;             // x2 [64 tokens][64] MN-major: kd U (kd' V')
+    static constexpr int SB_BYTES = 128 * DK;         // [DK][64] MN-major: bf16 S^T slice (32 used)
+    static constexpr int SB = UBK + 2 * 8192;         // x2
+    static constexpr int BAR = SB + 2 * SB_BYTES;
     static constexpr int BYTES = BAR + 256;
     static constexpr int ALLOC = BYTES + 1024;
 };
 
-// TMEM columns of the scan kernel (fp32 accumulators, 32 columns each)
-constexpr uint32_t kS1a = 0, kS1b = 32, kDSa = 64, kDSb = 96, kUt = 128, kPU = 160;
+// TMEM columns of the scan kernel: per stage parity p, at p * kParCols, four
+// fp32 accumulators of 32 columns (M = 128 lanes).
+constexpr uint32_t kDa = 0, kDb = 32, kDc = 64, kDS = 96, kParCols = 128;
 constexpr uint32_t kScanCols = 256;
 
-// Fetch block `blk` of (bh, slice) into buffer `buf`: workspace tiles by bulk
-// copy and, for dk >= 64, the q and k rows by tiled TMA (128-byte swizzle,
-// zero fill past the end of the sequence), all completing on full[buf]; v
-// rows (and q, k rows for dk = 32) by cp.async (one group).
+// L2 prefetch of what stage `st` will fetch (one thread).
 template <int DK, bool DELTA>
-__device__ __forceinline__ void scan_fetch(uint8_t *sm, int buf, const bf16 *q, const bf16 *k,
-                                           const bf16 *v, const void *tmq, const void *tmk,
-                                           const uint8_t *rec, uint64_t *full, size_t bh, int T,
-                                           int blk, int dv, int c0, int tid) {
-    using L = ScanLayout<DK>;
-    using R = Rec<DK>;
-    constexpr bool kTma = DK >= 64;
-    const int t0 = blk * C;
-    uint8_t *wq = sm + L::WQ + buf * L::WQ_BYTES;
-    uint8_t *tzp = sm + L::TZP + buf * 24576;
-    uint8_t *kr = sm + L::KR + buf * 16384;
-    if (tid == 0) {
-        const uint32_t bytes = (DELTA ? (uint32_t)R::KB * 8192u + 8192u : 0u) + 8192u + 1024u +
-                               (kTma ? 2u * (uint32_t)R::KB * 8192u : 0u);
-        mbar_expect_tx(full, bytes);
-        if (DELTA) {
-#pragma unroll
-            for (int kb = 0; kb < R::KB; ++kb)
-                bulk_g2s(wq + kb * 16384, rec + R::WT + kb * 8192, 8192, full);
-            bulk_g2s(tzp, rec + R::TT, 8192, full);
-        }
-        bulk_g2s(tzp + 16384, rec + R::PT, 8192, full);
-        bulk_g2s(sm + L::VEC + buf * 1024, rec + R::VEC, 1024, full);
-        if (kTma) {
-#pragma unroll
-            for (int kb = 0; kb < R::KB; ++kb) {
-                tma_load_3d(wq + kb * 16384 + 8192, tmq, kb * 64, t0, (int)bh, full);
-                tma_load_3d(kr + kb * 8192, tmk, kb * 64, t0, (int)bh, full);
-            }
-        }
-    }
-    if (!kTma) {
-        constexpr int CPR = DK / 8;
-        for (int idx = tid; idx < 2 * C * CPR; idx += NT) {
-            const int which = idx / (C * CPR);
-            const int rem = idx % (C * CPR);
-            const int r = rem / CPR, ch = rem % CPR;
-            const bool ok = t0 + r < T;
-            const bf16 *src = (which ? k : q) + ((bh * T + (ok ? t0 + r : 0)) * DK + ch * 8);
-            const uint32_t dst = which ? smem_u32(kr + sw128_offset(r, ch * 8, 64))
-                                       : smem_u32(wq + sw128_offset(64 + r, ch * 8, 128));
-            cp_async16(dst, src, ok);
-        }
-    }
-    uint8_t *vr = sm + L::VR + buf * 8192;
-    for (int idx = tid; idx < C * (DVS / 8); idx += NT) {
-        const int r = idx / (DVS / 8), ch = idx % (DVS / 8);
-        const bool ok = t0 + r < T;
-        cp_async16(smem_u32(vr + sw128_offset(r, ch * 8, 64)),
-                   v + ((bh * T + (ok ? t0 + r : 0)) * dv + c0 + ch * 8), ok);
-    }
-    cp_async_commit();
-}
-
-// L2 prefetch of everything block `blk` will fetch (one thread).
-template <int DK>
 __device__ __forceinline__ void scan_prefetch_l2(const bf16 *q, const bf16 *k, const bf16 *v,
-                                                 const uint8_t *rec, size_t bh, int T, int blk,
-                                                 int dv) {
-    const int t0 = blk * C;
-    const int n = min(C, T - t0);
+                                                 const uint8_t *rec, size_t bh, int T, int st,
+                                                 int nblk, int dv) {
     prefetch_l2(rec, Rec<DK>::BYTES);
-    prefetch_l2(q + (bh * T + t0) * DK, (uint32_t)n * DK * 2);
-    prefetch_l2(k + (bh * T + t0) * DK, (uint32_t)n * DK * 2);
-    prefetch_l2(v + (bh * T + t0) * dv, (uint32_t)n * dv * 2);
-}
-
-// g Q rows and kd K rows of buffer `buf`, scaled in place.
-template <int DK>
-__device__ __forceinline__ void scan_scale(uint8_t *sm, int buf, int tid) {
-    using L = ScanLayout<DK>;
-    uint8_t *wq = sm + L::WQ + buf * L::WQ_BYTES;
-    uint8_t *kr = sm + L::KR + buf * 16384;
-    const float *vec = reinterpret_cast<const float *>(sm + L::VEC + buf * 1024);
-    constexpr int CPR = DK / 8;
-    for (int idx = tid; idx < 2 * C * CPR; idx += NT) {
-        const int which = idx / (C * CPR);
-        const int rem = idx % (C * CPR);
-        const int r = rem / CPR, ch = rem % CPR;
-        uint4 *p = reinterpret_cast<uint4 *>(which ? kr + sw128_offset(r, ch * 8, 64)
-                                                   : wq + sw128_offset(64 + r, ch * 8, 128));
-        const float f = vec[(which ? 128 : 64) + r];
-        const uint4 raw = *p;
-        const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
-        float x[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) x[t] = f * __bfloat162float(e[t]);
-        *p = pack8(x);
+    const int pb = st - 1;
+    if (pb >= 0 && pb < nblk) {
+        const int t0 = pb * C, n = min(C, T - t0);
+        prefetch_l2(q + (bh * T + t0) * DK, (uint32_t)n * DK * 2);
+        prefetch_l2(k + (bh * T + t0) * DK, (uint32_t)n * DK * 2);
+    }
+    const int vb = DELTA ? st : st - 1;
+    if (vb >= 0 && vb < nblk) {
+        const int t0 = vb * C, n = min(C, T - t0);
+        prefetch_l2(v + (bh * T + t0) * dv, (uint32_t)n * dv * 2);
     }
 }
 
-// Scan kernel roles (256 threads):
-//   warp 0, lane 0  issues the products on the state chain: S1 = [-W; Q] S^T
-//                   and Delta S (and, without delta, Delta S from K^T (kd V))
-//   warp 1, lane 0  issues the products off the chain: P U (P V) and the next
-//                   block's Ut = T diag(beta) V
-//   warps 2, 3      producers: fetch a block into a free buffer (TMA / bulk /
-//                   cp.async) and wait for it to land
-//   warps 4..7      epilogue (TMEM lanes 0..127): U rows, the state update and
-//                   its bf16 copy, the output rows
-// Hand-offs are mbarriers; every wait is bounded.  TMEM accumulators are kept
-// per block parity so that the output of block b can still be read while
-// block b+1 runs.  Every barrier is waited on by all of its consumers before
-// it can complete again (so a parity wait is never ambiguous).
-constexpr int kScanThreads = 256;
-constexpr int kProducers = 64;
+// Scan kernel roles (384 threads), stage j = 0..nblk (parity p = j & 1):
+//   warp 0, lane 0   issues b_j = [-g_C' W_j; Q_{j-1}] S_{j-1}^T and
+//                    c_j = [-Z_{j-1}; P_{j-1}] U_{j-1}   (P_{j-1} V_{j-1} without delta)
+//   warp 1, lane 0   issues a_j = [T_j diag(beta); *] V_j and
+//                    ds = K_{j-1}^T (kd U_{j-1})          (K^T (kd V) without delta)
+//   warp 2, lane 0   loads the early group of stage j into buffer p: what a_j
+//                    and b_j read (-g_C' W_j, T_j diag(beta), Q_{j-1}, V_j)
+//   warp 3           lane 0 loads the late group: what c_j, ds and the
+//                    epilogues read (-Z_{j-1}, P_{j-1}, K_{j-1}, the gates;
+//                    V_{j-1} without delta); without delta the warp then forms
+//                    kd' V' for ds
+//   warps 4, 5, 8, 9 U rows (TMEM lanes 0..63): U_j = Da + Db + Dc -> bf16 U,
+//                    kd U
+//   warps 6, 7, 10, 11  output rows (lanes 64..127): O_{j-1} = g' Db + Dc
+//   warps 12..19     state (lanes 0..127 = key channels): S_j = g_C' S_{j-1} + ds,
+//                    fp32 in registers, bf16 copy for b_{j+1}
+// Each epilogue role is split over two warps per TMEM lane quarter, one per
+// half of the 32 value channels, to keep the per-warp instruction chains short.
+// All loads are TMA or bulk copies completing on the group's `full` barrier,
+// which the consumers wait on directly.  The early group is released as soon
+// as a_j and b_j are done, so the next fill of that half of the buffer starts
+// about half a stage earlier than the late one.
+// The state before the first block plays S_{-1} (with g_C = 1 and U_{-1} = 0).
+// Hand-offs are mbarriers, every wait bounded.  Each barrier is waited on by
+// all of its consumers before it can complete again: barriers that complete
+// once per stage and could run ahead are kept per parity, and every consumer
+// arrives on a group's `empty` barrier only after its waits of that stage.
+constexpr int kScanThreads = 640;
 
 // Arrive once per warp on `bar`: every lane has finished its part (and its own
 // fences) before lane 0 arrives.
@@ -581,58 +570,66 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
 }
 
 struct ScanBars {
-    uint64_t ready[2];  // buffer filled                                   (2 producer warps)
-    uint64_t full[2];   // loads landed                                    (1 + tx bytes)
-    uint64_t empty[2];  // both issuers done with the buffer + epilogue read its gates (2 + 4 warps)
-    uint64_t tfree[2];  // output rows of the block with this parity read  (2 warps)
-    uint64_t g1;        // S1 products done                                (commit)
-    uint64_t ut;        // Ut products done                                (commit)
-    uint64_t u;         // U rows written                                  (2 warps)
-    uint64_t ds;        // Delta S products done                           (commit)
-    uint64_t pu[2];     // P U products of the block with this parity done (commit)
-    uint64_t s;         // bf16 state copy written                         (4 warps)
+    uint64_t fullE[2];   // early group landed                           (1 + tx bytes)
+    uint64_t emptyE[2];  // early group read                             (2 commits)
+    uint64_t fullL[2];   // late group landed                            (1 + tx bytes)
+    uint64_t emptyL[2];  // late group read                              (2 commits + 16 warps)
+    uint64_t vkr[2];     // kd' V' written (no delta)                    (1 warp)
+    uint64_t dA[2];      // b and c products of the stage done           (commit)
+    uint64_t dB[2];      // a product of the stage done                  (commit)
+    uint64_t dsf[2];     // ds product of the stage done                 (commit)
+    uint64_t tfree[2];   // output rows of the stage read                (4 warps)
+    uint64_t uk[2];      // kd U rows of this parity written             (4 warps)
+    uint64_t s[2];       // bf16 state copy of this parity written       (8 warps)
+    uint64_t u;          // U rows written                               (4 warps)
+    uint64_t fin[2];     // every product an issuer issued has completed (commit)
     uint32_t tmem;
 };
+constexpr uint32_t kEmptyLCount = 2 + 4 + 4 + 8;  // both issuers' commits, U, output and state warps
 
 template <int DK, bool ALPHA, bool DELTA>
 __global__ void __launch_bounds__(kScanThreads, 1)
-chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
-                  const bf16 *__restrict__ v, const uint8_t *__restrict__ ws,
-                  const float *__restrict__ S0, bf16 *__restrict__ o, float *__restrict__ ST,
-                  int H, int T, int dv, int nblk, const __grid_constant__ CUtensorMap tmq,
-                  const __grid_constant__ CUtensorMap tmk) {
+chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
+                  bf16 *__restrict__ o, float *__restrict__ ST, int H, int T, int dv, int nblk,
+                  const bf16 *__restrict__ q, const bf16 *__restrict__ k,
+                  const bf16 *__restrict__ v, const __grid_constant__ CUtensorMap tmq,
+                  const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
     using L = ScanLayout<DK>;
     using R = Rec<DK>;
     extern __shared__ uint8_t sm_raw[];
     uint8_t *sm = align1024(sm_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c0 = blockIdx.x * DVS;
+    const int vx = c0 & ~63;                           // TMA box column of the v slice
+    const uint32_t voff = (uint32_t)(c0 & 63) * 2u;    // byte offset of the slice in a box row
     const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
-    const uint8_t *recs = ws + bh * nblk * (size_t)R::BYTES;
-    uint8_t *UB = sm + L::UB, *SB = sm + L::SB;
+    const uint8_t *recs = ws + bh * (nblk + 1) * (size_t)R::BYTES;
     ScanBars *bars = reinterpret_cast<ScanBars *>(sm + L::BAR);
+    auto vec_of = [&](int p) { return reinterpret_cast<const float *>(sm + L::VEC + p * 1024); };
 
     // zero everything once: padding rows and columns of the operands must read 0
     for (int i = tid; i < L::BAR / 16; i += kScanThreads)
         reinterpret_cast<uint4 *>(sm)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&bars->ready[b], kProducers / 32);
-            mbar_init(&bars->full[b], 1);
-            mbar_init(&bars->empty[b], 2 + 4);
-            mbar_init(&bars->tfree[b], 2);
+            mbar_init(&bars->fullE[b], 1);
+            mbar_init(&bars->emptyE[b], 2);
+            mbar_init(&bars->fullL[b], 1);
+            mbar_init(&bars->emptyL[b], kEmptyLCount);
+            mbar_init(&bars->vkr[b], 1);
+            mbar_init(&bars->dA[b], 1);
+            mbar_init(&bars->dB[b], 1);
+            mbar_init(&bars->dsf[b], 1);
+            mbar_init(&bars->tfree[b], 4);
+            mbar_init(&bars->uk[b], 4);
+            mbar_init(&bars->s[b], 8);
+            mbar_init(&bars->fin[b], 1);
         }
-        mbar_init(&bars->g1, 1);
-        mbar_init(&bars->ut, 1);
-        mbar_init(&bars->u, 2);
-        mbar_init(&bars->ds, 1);
-        mbar_init(&bars->pu[0], 1);
-        mbar_init(&bars->pu[1], 1);
-        mbar_init(&bars->s, 4);
+        mbar_init(&bars->u, 4);
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(&bars->tmem, 512);
+        tmem_alloc(&bars->tmem, kScanCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -643,299 +640,331 @@ chunk_scan_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
 
     const uint32_t id_kn = idesc_bf16_f32_mn(128, DVS, false, true);
     const uint32_t id_nn = idesc_bf16_f32_mn(128, DVS, true, true);
-    auto wq_desc = [&](int buf) { return tile_desc(smem_u32(sm + L::WQ + buf * L::WQ_BYTES), 128, 0, 0); };
-    auto tz_desc = [&](int buf) { return tile_desc(smem_u32(sm + L::TZP + buf * 24576), 192, 0, 0); };
-    auto zp_desc = [&](int buf) { return tile_desc(smem_u32(sm + L::TZP + buf * 24576), 192, 64, 0); };
-    auto kr_desc = [&](int buf) { return tile_desc_mn(smem_u32(sm + L::KR + buf * 16384), 64, 0); };
-    auto vr_desc = [&](int buf) { return tile_desc_mn(smem_u32(sm + L::VR + buf * 8192), 64, 0); };
-    auto vk_desc = [&](int buf) { return tile_desc_mn(smem_u32(sm + L::VK + buf * 8192), 64, 0); };
+    auto aw_desc = [&](int p) { return tile_desc(smem_u32(sm + L::AW + p * L::AW_BYTES), 128, 0, 0); };
+    auto tz_desc = [&](int p) { return tile_desc(smem_u32(sm + L::TZP + p * 24576), 192, 0, 0); };
+    auto zp_desc = [&](int p) { return tile_desc(smem_u32(sm + L::TZP + p * 24576), 192, 64, 0); };
+    auto kr_desc = [&](int p) { return tile_desc_mn(smem_u32(sm + L::KR + p * 16384), 64, 0); };
+    // the v box holds 64 channels; this CTA's 32 start `voff` bytes into each row
+    auto vr_desc = [&](int p) { return tile_desc_mn(smem_u32(sm + L::VR + p * 8192) + voff, 64, 0); };
+    auto ubk_desc = [&](int i) { return tile_desc_mn(smem_u32(sm + L::UBK + i * 8192), 64, 0); };
+    auto sb_desc = [&](int i) { return tile_desc_mn(smem_u32(sm + L::SB + i * L::SB_BYTES), DK, 0); };
 
     if (warp == 0) {
-        // ================================================ chain products
+        // ======================================= b and c products (issuer A)
         if (lane == 0) {
-            const uint64_t d_sb = tile_desc_mn(smem_u32(SB), DK, 0);
-            const uint64_t d_ubk = tile_desc_mn(smem_u32(sm + L::UBK), 64, 0);
-            constexpr int KS = DK / 16, KH = (KS + 1) / 2;
-            for (int blk = 0; blk < nblk && ok; ++blk) {
-                const int buf = blk & 1;
-                const uint32_t base = (blk & 1) * 192;
-                const uint64_t d_wq = wq_desc(buf), d_kr = kr_desc(buf), d_vk = vk_desc(buf);
-                ok = mbar_wait(&bars->ready[buf], (blk >> 1) & 1);
-                // accumulators of this parity free: outputs of block blk-2 read
-                if (blk >= 2) ok = ok && mbar_wait(&bars->tfree[blk & 1], ((blk >> 1) - 1) & 1);
-                ok = ok && mbar_wait(&bars->s, blk & 1);
+            const uint64_t d_ub = tile_desc_mn(smem_u32(sm + L::UB), 64, 0);
+            for (int j = 0; j <= nblk && ok; ++j) {
+                const int p = j & 1;
+                const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
+                ok = mbar_wait(&bars->fullE[p], ph);
+                // output rows of stage j-2 (same accumulators) read
+                if (ok && j >= 2) ok = mbar_wait(&bars->tfree[p], ph ^ 1);
+                // S_{j-1} in state copy p
+                if (ok) ok = mbar_wait(&bars->s[p], ph);
                 if (!ok) break;
                 tc_fence_after();
-                // S1 = [-W; Q] S^T in two K halves
+                const uint64_t d_aw = aw_desc(p), d_sb = sb_desc(p);
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks)
-                    mma_bf16(tmem + base + (ks < KH ? 0 : 32), kdesc_step(d_wq, 128, ks),
-                             mndesc_step(d_sb, ks), id_kn, (ks == 0 || ks == KH) ? 0u : 1u);
-                if (DELTA) {
-                    mma_commit(&bars->g1);
-                    ok = mbar_wait(&bars->u, blk & 1);
+                for (int ks = 0; ks < DK / 16; ++ks)
+                    mma_bf16(tmem + base + kDb, kdesc_step(d_aw, 128, ks), mndesc_step(d_sb, ks),
+                             id_kn, ks > 0);
+                mma_commit(&bars->emptyE[p]);
+                if (j >= 1) {
+                    ok = mbar_wait(&bars->fullL[p], ph);
+                    if (ok && DELTA) ok = mbar_wait(&bars->u, (j - 1) & 1);  // U_{j-1}
                     if (!ok) break;
                     tc_fence_after();
-                }
-                // Delta S^T = K^T (kd U), or K^T (kd V) without delta; the commit also
-                // covers S1, which reads the bf16 state copy the epilogue rewrites
-                // once Delta S is done
-                const uint64_t d_b = DELTA ? d_ubk : d_vk;
+                    const uint64_t d_zp = zp_desc(p), d_x = DELTA ? d_ub : vr_desc(p);
 #pragma unroll
-                for (int ks = 0; ks < C / 16; ++ks)
-                    mma_bf16(tmem + base + (ks < 2 ? 128 : 160), mndesc_step(d_kr, ks),
-                             mndesc_step(d_b, ks), id_nn, (ks & 1) ? 1u : 0u);
-                mma_commit(&bars->ds);
-                mma_commit(&bars->empty[buf]);
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_bf16(tmem + base + kDc, kdesc_step(d_zp, 192, ks), mndesc_step(d_x, ks),
+                                 id_kn, ks > 0);
+                }
+                mma_commit(&bars->dA[p]);
+                mma_commit(&bars->emptyL[p]);
             }
+            mma_commit(&bars->fin[0]);
+            if (!mbar_wait(&bars->fin[0], 0)) ok = false;
         }
     } else if (warp == 1) {
-        // ============================================ off-chain products
+        // ====================================== a and ds products (issuer B)
         if (lane == 0) {
-            const uint64_t d_ub = tile_desc_mn(smem_u32(UB), 64, 0);
-            auto issue_ut = [&](int blk) {  // Ut = T diag(beta) V  (delta only)
-                const int buf = blk & 1;
-                const uint64_t d_tz = tz_desc(buf), d_vr = vr_desc(buf);
-                const uint32_t col = (blk & 1) * 192 + 64;
-#pragma unroll
-                for (int ks = 0; ks < C / 16; ++ks)
-                    mma_bf16(tmem + col, kdesc_step(d_tz, 192, ks), mndesc_step(d_vr, ks), id_kn,
-                             ks > 0);
-                mma_commit(&bars->ut);
-            };
-            if (DELTA && nblk > 0) {
-                ok = mbar_wait(&bars->ready[0], 0);
-                if (ok) {
-                    tc_fence_after();
-                    issue_ut(0);
-                }
-            }
-            for (int blk = 0; blk < nblk && ok; ++blk) {
-                const int buf = blk & 1;
-                const uint32_t base = (blk & 1) * 192;
-                const uint64_t d_zp = zp_desc(buf);
-                if (DELTA) {
-                    ok = mbar_wait(&bars->u, blk & 1);
-                } else {
-                    ok = mbar_wait(&bars->ready[buf], (blk >> 1) & 1);
-                    if (blk >= 2) ok = ok && mbar_wait(&bars->tfree[blk & 1], ((blk >> 1) - 1) & 1);
-                }
+            for (int j = 0; j <= nblk && ok; ++j) {
+                const int p = j & 1;
+                const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
+                ok = mbar_wait(&bars->fullE[p], ph);
                 if (!ok) break;
                 tc_fence_after();
-                const uint64_t d_x = DELTA ? d_ub : vr_desc(buf);  // U, or V without delta
+                if (DELTA && j < nblk) {
+                    const uint64_t d_tz = tz_desc(p), d_vr = vr_desc(p);
 #pragma unroll
-                for (int ks = 0; ks < C / 16; ++ks)
-                    mma_bf16(tmem + base + 96, kdesc_step(d_zp, 192, ks), mndesc_step(d_x, ks),
-                             id_kn, ks > 0);
-                mma_commit(&bars->pu[blk & 1]);
-                mma_commit(&bars->empty[buf]);
-                if (DELTA && blk + 1 < nblk) {
-                    ok = mbar_wait(&bars->ready[buf ^ 1], ((blk + 1) >> 1) & 1);
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_bf16(tmem + base + kDa, kdesc_step(d_tz, 192, ks), mndesc_step(d_vr, ks),
+                                 id_kn, ks > 0);
+                }
+                mma_commit(&bars->dB[p]);
+                mma_commit(&bars->emptyE[p]);
+                if (j >= 1) {
+                    ok = mbar_wait(&bars->fullL[p], ph);
+                    if (ok) ok = DELTA ? mbar_wait(&bars->uk[(j - 1) & 1], ((j - 1) >> 1) & 1)  // kd U_{j-1}
+                                       : mbar_wait(&bars->vkr[p], ph);                          // kd' V'
                     if (!ok) break;
                     tc_fence_after();
-                    issue_ut(blk + 1);
+                    const uint64_t d_kr = kr_desc(p), d_y = ubk_desc(DELTA ? (j - 1) & 1 : p);
+#pragma unroll
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_bf16(tmem + base + kDS, mndesc_step(d_kr, ks), mndesc_step(d_y, ks),
+                                 id_nn, ks > 0);
                 }
+                mma_commit(&bars->dsf[p]);
+                mma_commit(&bars->emptyL[p]);
             }
+            mma_commit(&bars->fin[1]);
+            if (!mbar_wait(&bars->fin[1], 0)) ok = false;
         }
-    } else if (warp < 4) {
-        // ========================================================== producers
-        const int pt = tid - 64;
-        for (int blk = 0; blk < nblk && ok; ++blk) {
-            const int buf = blk & 1;
-            if (blk >= 2) ok = mbar_wait(&bars->empty[buf], ((blk >> 1) - 1) & 1);
-            ok = __all_sync(0xffffffffu, ok);  // warp-uniform, for the warp-level arrives
-            if (!ok) break;
-            const int t0 = blk * C;
-            const uint8_t *rec = recs + (size_t)blk * R::BYTES;
-            uint8_t *wq = sm + L::WQ + buf * L::WQ_BYTES;
-            uint8_t *tzp = sm + L::TZP + buf * 24576;
-            uint8_t *kr = sm + L::KR + buf * 16384;
-            uint8_t *vr = sm + L::VR + buf * 8192;
-            constexpr bool kTma = DK >= 64;
-            if (pt == 0) {
-                if (blk + 2 < nblk) scan_prefetch_l2<DK>(q, k, v, rec + 2 * R::BYTES, bh, T, blk + 2, dv);
-                const uint32_t bytes = (DELTA ? (uint32_t)R::KB * 8192u + 8192u : 0u) + 8192u +
-                                       1024u + (kTma ? 2u * (uint32_t)R::KB * 8192u : 0u);
-                mbar_expect_tx(&bars->full[buf], bytes);
-                if (DELTA) {
+    } else if (warp == 2) {
+        // ============================================ early-group loads
+        if (lane == 0) {
+            int issued = -1;
+            for (int j = 0; j <= nblk && ok; ++j) {
+                const int p = j & 1;
+                if (j >= 2) ok = mbar_wait(&bars->emptyE[p], ((j >> 1) - 1) & 1);
+                if (!ok) break;
+                const uint8_t *rec = recs + (size_t)j * R::BYTES;
+                uint8_t *aw = sm + L::AW + p * L::AW_BYTES;
+                if (j + 2 <= nblk)
+                    scan_prefetch_l2<DK, DELTA>(q, k, v, rec + 2 * (size_t)R::BYTES, bh, T, j + 2,
+                                                nblk, dv);
+                const bool cur = DELTA && j < nblk, prev = j >= 1;
+                const uint32_t bytes = (cur ? (uint32_t)R::KB * 8192u + 8192u + 8192u : 0u) +
+                                       (prev ? (uint32_t)R::KB * 8192u : 0u);
+                mbar_expect_tx(&bars->fullE[p], bytes);
+                if (cur) {
 #pragma unroll
                     for (int kb = 0; kb < R::KB; ++kb)
-                        bulk_g2s(wq + kb * 16384, rec + R::WT + kb * 8192, 8192, &bars->full[buf]);
-                    bulk_g2s(tzp, rec + R::TT, 8192, &bars->full[buf]);
+                        bulk_g2s(aw + kb * 16384, rec + R::WT + kb * 8192, 8192, &bars->fullE[p]);
+                    bulk_g2s(sm + L::TZP + p * 24576, rec + R::TZP, 8192, &bars->fullE[p]);
+                    tma_load_3d(sm + L::VR + p * 8192, &tmv, vx, j * C, (int)bh, &bars->fullE[p]);
                 }
-                bulk_g2s(tzp + 16384, rec + R::PT, 8192, &bars->full[buf]);
-                bulk_g2s(sm + L::VEC + buf * 1024, rec + R::VEC, 1024, &bars->full[buf]);
-                if (kTma) {
+                if (prev) {
 #pragma unroll
-                    for (int kb = 0; kb < R::KB; ++kb) {
-                        tma_load_3d(wq + kb * 16384 + 8192, &tmq, kb * 64, t0, (int)bh,
-                                    &bars->full[buf]);
-                        tma_load_3d(kr + kb * 8192, &tmk, kb * 64, t0, (int)bh, &bars->full[buf]);
+                    for (int kb = 0; kb < R::KB; ++kb)
+                        tma_load_3d(aw + kb * 16384 + 8192, &tmq, kb * 64, (j - 1) * C, (int)bh,
+                                    &bars->fullE[p]);
+                }
+                issued = j;
+            }
+            // never leave with copies into shared memory in flight
+            for (int j = issued > 0 ? issued - 1 : 0; j <= issued; ++j)
+                if (!mbar_wait(&bars->fullE[j & 1], (j >> 1) & 1)) ok = false;
+        }
+    } else if (warp == 3) {
+        // ============================================= late-group loads
+        int issued = -1;
+        for (int j = 0; j <= nblk && ok; ++j) {
+            const int p = j & 1;
+            const bool prev = j >= 1;
+            if (lane == 0) {
+                if (j >= 2) ok = mbar_wait(&bars->emptyL[p], ((j >> 1) - 1) & 1);
+                if (ok) {
+                    const uint8_t *rec = recs + (size_t)j * R::BYTES;
+                    uint32_t bytes = 1024u;
+                    if (prev) bytes += (DELTA ? 16384u : 8192u) + (uint32_t)R::KB * 8192u +
+                                       (DELTA ? 0u : 8192u);
+                    mbar_expect_tx(&bars->fullL[p], bytes);
+                    bulk_g2s(sm + L::VEC + p * 1024, rec + R::VEC, 1024, &bars->fullL[p]);
+                    if (prev) {
+                        if (DELTA)
+                            bulk_g2s(sm + L::TZP + p * 24576 + 8192, rec + R::TZP + 8192, 16384,
+                                     &bars->fullL[p]);
+                        else
+                            bulk_g2s(sm + L::TZP + p * 24576 + 16384, rec + R::TZP + 16384, 8192,
+                                     &bars->fullL[p]);
+#pragma unroll
+                        for (int kb = 0; kb < R::KB; ++kb)
+                            tma_load_3d(sm + L::KR + p * 16384 + kb * 8192, &tmk, kb * 64,
+                                        (j - 1) * C, (int)bh, &bars->fullL[p]);
+                        if (!DELTA)
+                            tma_load_3d(sm + L::VR + p * 8192, &tmv, vx, (j - 1) * C, (int)bh,
+                                        &bars->fullL[p]);
                     }
+                    issued = j;
                 }
             }
-            if (!kTma) {
-                constexpr int CPR = DK / 8;
-                for (int idx = pt; idx < 2 * C * CPR; idx += kProducers) {
-                    const int which = idx / (C * CPR);
-                    const int rem = idx % (C * CPR);
-                    const int r = rem / CPR, ch = rem % CPR;
-                    const bool okr = t0 + r < T;
-                    const bf16 *src = (which ? k : q) + ((bh * T + (okr ? t0 + r : 0)) * DK + ch * 8);
-                    const uint32_t dst = which ? smem_u32(kr + sw128_offset(r, ch * 8, 64))
-                                               : smem_u32(wq + sw128_offset(64 + r, ch * 8, 128));
-                    cp_async16(dst, src, okr);
-                }
-            }
-            for (int idx = pt; idx < C * (DVS / 8); idx += kProducers) {
-                const int r = idx / (DVS / 8), ch = idx % (DVS / 8);
-                const bool okr = t0 + r < T;
-                cp_async16(smem_u32(vr + sw128_offset(r, ch * 8, 64)),
-                           v + ((bh * T + (okr ? t0 + r : 0)) * dv + c0 + ch * 8), okr);
-            }
-            cp_async_commit();
-            cp_async_wait_all();
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->full[buf], (blk >> 1) & 1));
+            ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            if (!DELTA) {
-                // kd V (B operand of Delta S = K^T diag(kd) V); g and kd are folded
-                // into the epilogues everywhere else
-                const float *vec = reinterpret_cast<const float *>(sm + L::VEC + buf * 1024);
-                uint8_t *vk = sm + L::VK + buf * 8192;
-                for (int idx = pt; idx < C * (DVS / 8); idx += kProducers) {
+            if (!DELTA && !prev) warp_arrive(&bars->vkr[p]);  // one completion per stage keeps the parities aligned
+            if (!DELTA && prev) {
+                // kd' V' (B operand of Delta S = K'^T diag(kd') V')
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars->fullL[p], (j >> 1) & 1));
+                if (!ok) break;
+                const float *vec = vec_of(p);
+                const uint8_t *vr = sm + L::VR + p * 8192;
+                uint8_t *vk = sm + L::UBK + p * 8192;
+                for (int idx = lane; idx < C * (DVS / 8); idx += 32) {
                     const int r = idx / (DVS / 8), ch = idx % (DVS / 8);
-                    const uint32_t off = sw128_offset(r, ch * 8, 64);
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(vr + off);
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(
+                        vr + sw128_offset(r, (c0 & 63) + ch * 8, 64));
                     const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
-                    const float f = vec[128 + r];
+                    const float f = vec[kVkdPrev + r];
                     float x[8];
 #pragma unroll
                     for (int t = 0; t < 8; ++t) x[t] = f * __bfloat162float(e[t]);
-                    *reinterpret_cast<uint4 *>(vk + off) = pack8(x);
+                    *reinterpret_cast<uint4 *>(vk + sw128_offset(r, ch * 8, 64)) = pack8(x);
                 }
+                fence_async_smem();
+                warp_arrive(&bars->vkr[p]);
             }
-            fence_async_smem();
-            warp_arrive(&bars->ready[buf]);
         }
-    } else {
-        // =========================================================== epilogue
-        const int j = tid - 128;  // TMEM lane; key channel of the state column
-        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        float Sr[DVS];
-#pragma unroll
-        for (int c = 0; c < DVS; ++c) Sr[c] = (S0 && j < DK) ? S0[(bh * dv + c0 + c) * DK + j] : 0.f;
-        if (j < DK) {
-#pragma unroll
-            for (int c8 = 0; c8 < DVS / 8; ++c8)
-                *reinterpret_cast<uint4 *>(SB + sw128_offset(j, c8 * 8, DK)) = pack8(Sr + c8 * 8);
-        }
-        fence_async_smem();
-        warp_arrive(&bars->s);
-        for (int blk = 0; blk < nblk && ok; ++blk) {
-            const int buf = blk & 1, p = blk & 1;
-            const uint32_t base = p * 192;
-            const int t0 = blk * C;
-            const int n = min(C, T - t0);
-            // gates of this block, read before the buffer is released: g_C for
-            // the state, g_r of this thread's output row, kd_i of its U row
-            const float *vec = reinterpret_cast<const float *>(sm + L::VEC + buf * 1024);
-            float gC, gr = 0.f, kdi = 0.f;
-            if (DELTA) {
-                ok = mbar_wait(&bars->g1, blk & 1);
-                if (warp < 6) ok = ok && mbar_wait(&bars->ut, blk & 1);  // only the U rows need Ut
+        // never leave with copies into shared memory in flight
+        if (lane == 0)
+            for (int j = issued > 0 ? issued - 1 : 0; j <= issued; ++j)
+                if (!mbar_wait(&bars->fullL[j & 1], (j >> 1) & 1)) ok = false;
+    } else if (warp < 12 && (warp & 3) < 2) {
+        // ============================================ U rows (TMEM lanes 0..63)
+        const int r = 32 * (warp & 3) + lane;
+        const int ch = 16 * ((warp - 4) >> 2);  // first value channel of this warp's half
+        const uint32_t lb = ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)ch;
+        for (int j = 0; j <= nblk && ok; ++j) {
+            const int p = j & 1;
+            const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
+            ok = mbar_wait(&bars->fullL[p], ph);
+            if (DELTA && j < nblk) {
+                ok = ok && mbar_wait(&bars->dA[p], ph);
+                ok = ok && mbar_wait(&bars->dB[p], ph);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                gC = vec[64 + C - 1];
-                if (warp >= 6) gr = vec[64 + j - 64];
-                else kdi = vec[128 + j];
-                warp_arrive(&bars->empty[buf]);
-                if (warp < 6) {  // U rows = tokens 0..63
-                    float u[32], x[32];
-                    tmem_ld32(tmem + lane_base + base + 64, u);
-                    tmem_ld32(tmem + lane_base + base + 0, x);
+                const float kdr = vec_of(p)[kVkd + r];
+                float x[16], y[16], z[16];
+                tmem_ld16(tmem + lb + base + kDa, x);
+                tmem_ld16(tmem + lb + base + kDb, y);
+                if (j > 0) {
+                    tmem_ld16(tmem + lb + base + kDc, z);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) u[c] += x[c];
-                    tmem_ld32(tmem + lane_base + base + 32, x);
+                    for (int c = 0; c < 16; ++c) x[c] += y[c] + z[c];
+                } else {
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) u[c] += x[c];
-#pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8)
-                        *reinterpret_cast<uint4 *>(UB + sw128_offset(j, c8 * 8, 64)) =
-                            pack8(u + c8 * 8);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) u[c] *= kdi;
-#pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8)
-                        *reinterpret_cast<uint4 *>(sm + L::UBK + sw128_offset(j, c8 * 8, 64)) =
-                            pack8(u + c8 * 8);
-                    fence_async_smem();
-                    tc_fence_before();
-                    warp_arrive(&bars->u);
+                    for (int c = 0; c < 16; ++c) x[c] += y[c];
                 }
-            }
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->ds, blk & 1));
-            if (!ok) break;
-            tc_fence_after();
-            if (!DELTA) {
-                gC = vec[64 + C - 1];
-                if (warp >= 6) gr = vec[64 + j - 64];
-                warp_arrive(&bars->empty[buf]);
-            }
-            {
-                float d[32], e[32];
-                tmem_ld32(tmem + lane_base + base + 128, d);
-                tmem_ld32(tmem + lane_base + base + 160, e);
-                tmem_ld_wait();
-                if (j < DK) {
 #pragma unroll
-                    for (int c = 0; c < DVS; ++c) Sr[c] = gC * Sr[c] + d[c] + e[c];
-#pragma unroll
-                    for (int c8 = 0; c8 < DVS / 8; ++c8)
-                        *reinterpret_cast<uint4 *>(SB + sw128_offset(j, c8 * 8, DK)) =
-                            pack8(Sr + c8 * 8);
-                }
+                for (int c8 = 0; c8 < 2; ++c8)
+                    *reinterpret_cast<uint4 *>(sm + L::UB + sw128_offset(r, ch + c8 * 8, 64)) =
+                        pack8(x + c8 * 8);
                 fence_async_smem();
                 tc_fence_before();
-                warp_arrive(&bars->s);
-            }
-            if (warp >= 6) {  // output rows = tokens 0..63
-                ok = __all_sync(0xffffffffu, mbar_wait(&bars->pu[p], (blk >> 1) & 1));
+                warp_arrive(&bars->u);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) x[c] *= kdr;
+#pragma unroll
+                for (int c8 = 0; c8 < 2; ++c8)
+                    *reinterpret_cast<uint4 *>(sm + L::UBK + p * 8192 +
+                                               sw128_offset(r, ch + c8 * 8, 64)) = pack8(x + c8 * 8);
+                fence_async_smem();
+                warp_arrive(&bars->uk[p]);
+            } else {
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
+            }
+            warp_arrive(&bars->emptyL[p]);
+        }
+    } else if (warp < 12) {
+        // ===================================== output rows (TMEM lanes 64..127)
+        const int r = 32 * (warp & 3) + lane - 64;
+        const int ch = 16 * ((warp - 4) >> 2);
+        const uint32_t lb = ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)ch;
+        for (int j = 0; j <= nblk && ok; ++j) {
+            const int p = j & 1;
+            const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
+            ok = mbar_wait(&bars->fullL[p], ph);
+            if (j >= 1) ok = ok && mbar_wait(&bars->dA[p], ph);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            if (j >= 1) {
                 tc_fence_after();
-                const int r = j - 64;
-                float d[32], e[32];
-                tmem_ld32(tmem + lane_base + base + 0, d);
-                tmem_ld32(tmem + lane_base + base + 32, e);
+                const float gr = vec_of(p)[kVgPrev + r];
+                float x[16], y[16];
+                tmem_ld16(tmem + lb + base + kDb, x);
+                tmem_ld16(tmem + lb + base + kDc, y);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 32; ++c) d[c] = gr * (d[c] + e[c]);  // g_r Q S^T
-                tmem_ld32(tmem + lane_base + base + 96, e);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) d[c] += e[c];              // + P U
+                for (int c = 0; c < 16; ++c) x[c] = gr * x[c] + y[c];  // g' Q' S'^T + P' U'
                 tc_fence_before();
                 warp_arrive(&bars->tfree[p]);
-                if (r < n) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(o + (bh * T + t0 + r) * dv + c0);
+                warp_arrive(&bars->emptyL[p]);
+                const int t = (j - 1) * C + r;
+                if (t < T) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(o + (bh * T + t) * dv + c0 + ch);
 #pragma unroll
-                    for (int i8 = 0; i8 < 4; ++i8) dst[i8] = pack8(d + i8 * 8);
+                    for (int i8 = 0; i8 < 2; ++i8) dst[i8] = pack8(x + i8 * 8);
                 }
+            } else {
+                warp_arrive(&bars->tfree[p]);
+                warp_arrive(&bars->emptyL[p]);
             }
         }
-        if (ok && j < DK) {
+    } else {
+        // ========================== state (TMEM lanes 0..127 = key channels)
+        constexpr int SC = DVS / 2;  // value channels per warp
+        const int kc = 32 * (warp & 3) + lane;
+        const int ch = SC * ((warp - 12) >> 2);
+        const uint32_t lb = ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)ch;
+        float Sr[SC];
 #pragma unroll
-            for (int c = 0; c < DVS; ++c) ST[(bh * dv + c0 + c) * DK + j] = Sr[c];
+        for (int c = 0; c < SC; ++c)
+            Sr[c] = (S0 && kc < DK) ? S0[(bh * dv + c0 + ch + c) * DK + kc] : 0.f;
+        auto write_sb = [&](int i) {
+            if (kc < DK) {
+#pragma unroll
+                for (int c8 = 0; c8 < SC / 8; ++c8)
+                    *reinterpret_cast<uint4 *>(sm + L::SB + i * L::SB_BYTES +
+                                               sw128_offset(kc, ch + c8 * 8, DK)) = pack8(Sr + c8 * 8);
+            }
+        };
+        // S_{-1} = S_0 in copy 0 (read by b_0), S_0 in copy 1 (read by b_1)
+        write_sb(0);
+        write_sb(1);
+        fence_async_smem();
+        warp_arrive(&bars->s[0]);
+        warp_arrive(&bars->s[1]);
+        for (int j = 0; j <= nblk && ok; ++j) {
+            const int p = j & 1;
+            const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
+            ok = mbar_wait(&bars->fullL[p], ph);
+            ok = ok && mbar_wait(&bars->dsf[p], ph);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            if (j >= 1) {
+                tc_fence_after();
+                const float gC = vec_of(p)[kVgCPrev];
+                float d[SC];
+                tmem_ld16(tmem + lb + base + kDS, d);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < SC; ++c) Sr[c] = gC * Sr[c] + d[c];
+                tc_fence_before();
+                warp_arrive(&bars->emptyL[p]);
+                if (j < nblk) {  // S_j -> copy (j+1)&1, read by b_{j+1}
+                    write_sb((j + 1) & 1);
+                    fence_async_smem();
+                    warp_arrive(&bars->s[(j + 1) & 1]);
+                }
+            } else {
+                warp_arrive(&bars->emptyL[p]);
+            }
+        }
+        if (ok && kc < DK) {
+#pragma unroll
+            for (int c = 0; c < SC; ++c) ST[(bh * dv + c0 + ch + c) * DK + kc] = Sr[c];
         }
     }
 
     if (!ok) atomicExch(&g_tc_error, 1);
-    cp_async_wait_all();
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == 0) tmem_dealloc(tmem, kScanCols);
 }
 
 // ================================================================== launch
@@ -955,7 +984,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // [B*H][T][d] bf16 tensor, boxes of 64 rows x 64 columns, 128-byte swizzle,
-// zero fill outside.
+// zero fill outside (also the columns of a box wider than d).
 cudaError_t make_rows_map(CUtensorMap *m, const void *base, int d, int T, int BH) {
     auto enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
@@ -982,24 +1011,24 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
     if (e != cudaSuccess) return e;
     e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC, slot + 12);
     if (e != cudaSuccess) return e;
-    CUtensorMap tmq, tmk;
-    memset(&tmq, 0, sizeof(tmq));
-    memset(&tmk, 0, sizeof(tmk));
-    if (DK >= 64) {
-        e = make_rows_map(&tmq, q, DK, T, B * H);
-        if (e != cudaSuccess) return e;
-        e = make_rows_map(&tmk, k, DK, T, B * H);
-        if (e != cudaSuccess) return e;
-    }
+    // q, k and v as [B*H][T][d] with 64 x 64 boxes (for d = 32 the box is
+    // wider than a row; its outer half reads zeros)
+    CUtensorMap tmq, tmk, tmv;
+    e = make_rows_map(&tmq, q, DK, T, B * H);
+    if (e != cudaSuccess) return e;
+    e = make_rows_map(&tmk, k, DK, T, B * H);
+    if (e != cudaSuccess) return e;
+    e = make_rows_map(&tmv, v, dv, T, B * H);
+    if (e != cudaSuccess) return e;
     prep<<<dim3(nblk, H, B), NT, PrepLayout<DK>::ALLOC, stream>>>(
         static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), ALPHA ? alpha : nullptr,
         DELTA ? beta : nullptr, static_cast<uint8_t *>(ws), H, T, nblk, tmq, tmk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     scan<<<dim3(dv / DVS, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
+        static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk,
         static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), static_cast<const bf16 *>(v),
-        static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, tmq,
-        tmk);
+        tmq, tmk, tmv);
     return cudaGetLastError();
 }
 
@@ -1025,10 +1054,11 @@ cudaError_t launch_mode(const void *q, const void *k, const void *v, const float
 
 }  // namespace
 
+// One record per stage: a head of nblk blocks has nblk + 1 stages.
 size_t chunked_tc_workspace_bytes(int B, int H, int T, int dk) {
     const size_t nblk = (size_t)((T + C - 1) / C);
     const size_t rec = dk == 32 ? Rec<32>::BYTES : dk == 64 ? Rec<64>::BYTES : Rec<128>::BYTES;
-    return (size_t)B * H * nblk * rec;
+    return (size_t)B * H * (nblk + 1) * rec;
 }
 
 // Attribute slots 32..55 belong to this file.

@@ -119,7 +119,8 @@ typedef enum {
  *
  * The bf16 path runs two kernels on `stream`: a per-block pass over all
  * blocks in parallel (gate products, decay-masked scores, the UT inverse of
- * the delta rows and W = T diag(beta g) K), stored in the workspace, then the
+ * the delta rows, W = T diag(beta g) K and the block-to-block coupling
+ * W K'^T of consecutive blocks), stored in the workspace, then the
  * sequential pass over blocks that carries the state.  The fp32 path needs no
  * workspace.  Calls that share a workspace must be ordered on one stream.
  *
@@ -135,8 +136,8 @@ lr_status lr_fwd_chunked(const void *q, const void *k, const void *v,
 
 /*
  * Bytes of workspace lr_fwd_chunked needs for these arguments: 0 for the fp32
- * path and for T == 0; for bf16, about 33 KB per (batch, head, 64-token
- * block) at dk = 128.  Returns 0 as well for arguments lr_fwd_chunked would
+ * path and for T == 0; for bf16, 41 KB per (batch, head) for every 64-token
+ * block plus one more, at dk = 128 (33 KB at dk = 32 or 64).  Returns 0 as well for arguments lr_fwd_chunked would
  * reject.
  */
 size_t lr_fwd_chunked_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
@@ -189,8 +190,8 @@ lr_status lr_device_status(void);
  *
  *   - Returns LR_ERR_TOO_LARGE, launching nothing, when
  *     lr_fwd_chunked_workspace_size(...) exceeds LR_STATIC_WORKSPACE_BYTES
- *     (at dk = 128 about 33 KB per (batch, head, 64-token block), so roughly
- *     B * H * ceil(T / 64) <= 2000).
+ *     (at dk = 128, 41 KB per (batch, head) for every 64-token block plus
+ *     one, so B * H * (ceil(T / 64) + 1) <= 1598).
  *   - The first call on a device looks up the array's device address (with
  *     cudaGetSymbolAddress, that device current); make that first call before
  *     any stream capture.
