@@ -35,11 +35,11 @@
 // Two launches:
 //  * prep: one CTA per (block, head, batch), all blocks in parallel.  Computes
 //    what does not depend on the state: the gates, the scores P, the UT
-//    inverse T (fp32; 16 x 16 diagonal blocks on the CUDA cores, the block
-//    rows on warp-level tf32 MMAs), W and Z, and writes the workspace record
-//    of "stage" j: -g_C' W_j, T_j diag(beta), -Z_{j-1}, P_{j-1} and the gate
-//    vectors, as bf16 tiles already in the shared-memory operand layout
-//    (primes: the previous block).  Stage j's P row block is written by the
+//    inverse T (fp32, in place; 16 x 16 diagonal blocks on the CUDA cores,
+//    the block rows on warp-level tf32 MMAs), W and Z, and writes the
+//    workspace record of "stage" j: W_j, T_j diag(beta), -Z_{j-1}, P_{j-1}
+//    and the gate vectors, as bf16 tiles already in the shared-memory operand
+//    layout (primes: the previous block).  Stage j's P row block is written by the
 //    CTA of block j-1; there is one more stage than blocks.
 //  * scan: one CTA per (32 value channels, head, batch); rows of S evolve
 //    independently given k, alpha and beta, so slices never exchange data.
@@ -51,7 +51,7 @@
 //         E3  T diag(beta g) K        -> W           (M = 64, K read MN-major)
 //         E4  W K'^T                  -> Z'          (M = 64)
 //   scan  a   [T diag(beta); *] V     -> Ut rows
-//         b   [-g_C' W; Q'] S'^T      -> U and O' parts
+//         b   [W; Q'] S'^T            -> U (times -g_C') and O' parts
 //         c   [-Z'; P'] U'            -> U and O' parts
 //         ds  K'^T (kd' U')           -> Delta S'^T  (K read MN-major)
 // A final short block is zero-filled (alpha treated as 1, beta as 0), which
@@ -83,7 +83,7 @@ __device__ int g_tc_error = 0;  // set to 1 when a bounded wait gives up
 template <int DK>
 struct Rec {
     static constexpr int KB = (DK + 63) / 64;
-    static constexpr int WT = 0;                // -g_C' W_j: KB blocks of [64 rows][128 B]
+    static constexpr int WT = 0;                // W_j: KB blocks of [64 rows][128 B]
     static constexpr int TZP = WT + KB * 8192;  // [192 rows][64] bf16: T_j diag(beta), -Z_{j-1}, P_{j-1}
     static constexpr int VEC = TZP + 24576;     // fp32: g' [64], kd' [64], kd [64], g_C'
     static constexpr int BYTES = VEC + 1024;
@@ -112,21 +112,27 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 
 // ===================================================================== prep
 
+// Shared memory of a prep CTA, with the regions reused as the block goes:
+//   QK  [128 rows][DK] K-major: Q rows 0..63 and K rows 64..127 (E1); then
+//       the Q rows host the T diag(beta g) tile and the solve scratch, and
+//       after E3 the K rows are refilled with the previous block's K rows (E4)
+//   AT  fp32 [64][AP]: A, inverted in place into T; then bf16 W [64][DK]
+// 50 KB at d_k = 128: four CTAs per SM.
 template <int DK>
 struct PrepLayout {
     static constexpr int KB = (DK + 63) / 64;
-    static constexpr int QK = 0;                            // [128 rows][DK]: Q rows (later K'), K rows
-    static constexpr int TB = QK + 128 * 128 * KB;          // [64][64] bf16: T diag(beta g)
+    static constexpr int QK = 0;
+    static constexpr int TB = QK;                           // [64][64] bf16, in the Q rows of block 0
     static constexpr int XT = TB;                           // fp32 [16][XP] solve scratch, inside TB
-    static constexpr int AM = TB + 8192;                    // fp32 [64][AP]; later bf16 W [64][DK]
-    static constexpr int TM = AM + C * AP * 4;              // fp32 [64][AP]
-    static constexpr int VEC = TM + C * AP * 4;             // G (later kd'), ginv, g, beta
-    static constexpr int BAR = VEC + 4 * 64 * 4;            // 3 barriers, TMEM slot, g_C'
+    static constexpr int AT = QK + 128 * 128 * KB;
+    static constexpr int VEC = AT + C * AP * 4;             // G (later kd'), ginv, g, beta
+    static constexpr int BAR = VEC + 4 * 64 * 4;            // 3 barriers, TMEM slot
     static constexpr int BYTES = BAR + 64;
     static constexpr int ALLOC = BYTES + 1024;
 };
 static_assert(16 * XP * 4 <= 8192, "solve scratch must fit inside the T tile");
 static_assert(128 * 64 * 2 <= C * AP * 4, "the W tile must fit over the A matrix");
+static_assert(PrepLayout<128>::AT % 1024 == 0, "the W tile must be 1024-byte aligned");
 
 // Element (r, c) of a 64 x 64 fp32 matrix in shared memory, rows padded to 65
 // floats so that a warp touching one column of 32 rows hits 32 banks.
@@ -153,11 +159,14 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
 // One block row BR of the blocked UT inverse (rows 16BR..16BR+15), with the
 // rows above it done:
 //   X = A[rows, cols < 16BR] T[< 16BR, < 16BR];   T[rows, cols < 16BR] = -T_bb X
+// in place: T[rows, cols < 16BR] overwrites A there once X is formed.
 // on the tensor cores (m16n8k8, tf32 in, fp32 accumulate).  Warp w takes the
 // 8-column tiles nt = w, w+4, ...; K steps that only meet the zero blocks of T
 // above its block diagonal are skipped, so those blocks are never read.
 template <int BR>
-__device__ __forceinline__ void ut_block_row(const float *Am, float *Tm, float *Xt, int tid) {
+__device__ __forceinline__ void ut_block_row(float *AT, float *Xt, int tid) {
+    const float *Am = AT;  // row block BR still holds A left of its diagonal block
+    float *Tm = AT;        // rows above it and its diagonal block already hold T
     const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const int r0 = 16 * BR;
     for (int nt = warp; nt < 2 * BR; nt += 4) {
@@ -195,34 +204,38 @@ __device__ __forceinline__ void ut_block_row(const float *Am, float *Tm, float *
     __syncthreads();
 }
 
-// T = (I + A)^-1 for a strictly lower A (64 x 64, fp32 in shared memory).  On
-// exit Tm holds T's lower triangle (diagonal blocks include their zero upper
-// triangles); the blocks above the block diagonal are never written or read.
-__device__ __forceinline__ void ut_inverse(const float *Am, float *Tm, float *Xt, int tid) {
+// T = (I + A)^-1 for a strictly lower A (64 x 64, fp32 in shared memory),
+// computed in place.  On exit AT holds T's lower triangle (diagonal blocks
+// include their zero upper triangles); the blocks above the block diagonal
+// keep A's zeros and are never read.
+__device__ __forceinline__ void ut_inverse(float *AT, float *Xt, int tid) {
+    float x[16];
+    const int b = tid >> 4, c = tid & 15;
     if (tid < 64) {
-        const int b = tid >> 4, c = tid & 15;
-        float x[16];
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
             float s0 = (rr == c) ? 1.f : 0.f, s1 = 0.f;
 #pragma unroll
             for (int i = 0; i < rr; ++i) {
-                const float a = Am[sw64(16 * b + rr, 16 * b + i)];
+                const float a = AT[sw64(16 * b + rr, 16 * b + i)];
                 if (i & 1) s1 -= a * x[i];
                 else s0 -= a * x[i];
             }
             x[rr] = s0 + s1;
         }
+    }
+    __syncthreads();  // every diagonal block of A read before T replaces it
+    if (tid < 64) {
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) Tm[sw64(16 * b + rr, 16 * b + c)] = x[rr];
+        for (int rr = 0; rr < 16; ++rr) AT[sw64(16 * b + rr, 16 * b + c)] = x[rr];
     }
     __syncthreads();
-    ut_block_row<1>(Am, Tm, Xt, tid);
-    ut_block_row<2>(Am, Tm, Xt, tid);
-    ut_block_row<3>(Am, Tm, Xt, tid);
+    ut_block_row<1>(AT, Xt, tid);
+    ut_block_row<2>(AT, Xt, tid);
+    ut_block_row<3>(AT, Xt, tid);
 }
 
-// Prep of block j = blockIdx.x.  Writes to record j: -g_C' W_j, T_j diag(beta),
+// Prep of block j = blockIdx.x.  Writes to record j: W_j, T_j diag(beta),
 // -Z_{j-1} and the gate vectors; to record j+1: P_j (and, for the last block,
 // record j+1's gate vectors).
 template <int DK, bool ALPHA, bool DELTA>
@@ -245,16 +258,14 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     float *vec = reinterpret_cast<float *>(rec + R::VEC);
     float *vec_next = reinterpret_cast<float *>(rec_next + R::VEC);
 
-    uint8_t *QK = sm + L::QK, *TB = sm + L::TB, *WB = sm + L::AM;
-    float *Am = reinterpret_cast<float *>(sm + L::AM);
-    float *Tm = reinterpret_cast<float *>(sm + L::TM);
+    uint8_t *QK = sm + L::QK, *TB = sm + L::TB, *WB = sm + L::AT;
+    float *Am = reinterpret_cast<float *>(sm + L::AT);  // A, then T in place
     float *Xt = reinterpret_cast<float *>(sm + L::XT);
     float *Gv = reinterpret_cast<float *>(sm + L::VEC);
     float *giv = Gv + 64, *gv = Gv + 128, *bv = Gv + 192;
     float *kdv = Gv;  // kd of the previous block, once G is no longer needed
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);  // MMA, q/k tiles, previous k tile
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 32);
-    float *gcp_slot = reinterpret_cast<float *>(sm + L::BAR + 48);
     const bool zprev = DELTA && blk > 0;  // Z_{j-1} exists
 
     // ---- stage Q, K by tiled TMA (zero-filled past the end of the sequence
@@ -322,7 +333,6 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         if (tok == C - 1) {
             const float gc = ALPHA ? __expf(Glast) : 1.f;
             vec[kVgCPrev] = gc;
-            *gcp_slot = gc;
         }
     }
     bool ok = mbar_wait(&bar[1], 0);
@@ -343,14 +353,6 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     }
     ok = __syncthreads_and((ok && mbar_wait(&bar[0], 0)) ? 1 : 0) != 0;
     tc_fence_after();
-
-    // ---- the Q rows are free: fetch the previous block's K rows there (for Z)
-    if (zprev && ok && tid == 0) {
-        mbar_expect_tx(&bar[2], (uint32_t)L::KB * 8192u);
-#pragma unroll
-        for (int kb = 0; kb < L::KB; ++kb)
-            tma_load_3d(QK + kb * 16384, &tmk, kb * 64, t0 - C, (int)bh, &bar[2]);
-    }
 
     // ---- E2: P rows (bf16 tile to the next stage's record), A rows (fp32)
     if (ok) {
@@ -386,7 +388,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
 
     if (DELTA && ok) {
         if (tid >= C) kdv[tok] = kdp;  // G is dead; read after the syncs below
-        ut_inverse(Am, Tm, Xt, tid);
+        ut_inverse(Am, Xt, tid);
         // T diag(beta) (bf16) -> record; T diag(beta g) -> the T tile (over the
         // solve scratch), the A operand of W = T diag(beta g) K
         for (int idx = tid; idx < C * 8; idx += NT) {
@@ -395,7 +397,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int i = i8 * 8 + e;
-                t[e] = i <= r ? Tm[sw64(r, i)] * bv[i] : 0.f;
+                t[e] = i <= r ? Am[sw64(r, i)] * bv[i] : 0.f;
                 tg[e] = t[e] * gv[i];
             }
             *reinterpret_cast<uint4 *>(rec + R::TZP + sw128_offset(r, i8 * 8, 192)) = pack8(t);
@@ -419,10 +421,17 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         ok = __syncthreads_and(mbar_wait(&bar[0], 1) ? 1 : 0) != 0;
         tc_fence_after();
 
-        // ---- -g_C' W rows -> record; W rows (bf16) -> the W tile over A, the
-        //      A operand of Z
+        // ---- the K rows are free: fetch the previous block's K rows there (for Z)
+        if (zprev && ok && tid == 0) {
+            mbar_expect_tx(&bar[2], (uint32_t)L::KB * 8192u);
+#pragma unroll
+            for (int kb = 0; kb < L::KB; ++kb)
+                tma_load_3d(QK + kb * 16384 + 8192, &tmk, kb * 64, t0 - C, (int)bh, &bar[2]);
+        }
+
+        // ---- W rows (bf16) -> the W tile over T: the A operand of Z and, by one
+        //      bulk copy, the record's W tile (same layout)
         if (ok) {
-            const float gcp = *gcp_slot;
             const int r = 16 * warp + lane;
 #pragma unroll
             for (int cb = 0; cb < DK / 32; ++cb) {
@@ -434,31 +443,29 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                     for (int i8 = 0; i8 < 4; ++i8)
                         *reinterpret_cast<uint4 *>(WB + sw128_offset(r, cb * 32 + i8 * 8, 64)) =
                             pack8(w + i8 * 8);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) w[e] *= -gcp;
-#pragma unroll
-                    for (int i8 = 0; i8 < 4; ++i8)
-                        *reinterpret_cast<uint4 *>(rec + R::WT +
-                                                   sw128_offset(r, cb * 32 + i8 * 8, 64)) =
-                            pack8(w + i8 * 8);
                 }
             }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        ok = __syncthreads_and(ok ? 1 : 0) != 0;
+        tc_fence_after();
+        if (tid == 0 && ok) {
+            bulk_s2g(rec + R::WT, WB, (uint32_t)R::KB * 8192u);
+            bulk_commit();
         }
 
         // ---- E4: Z' = W K'^T (M = 64, N = 64 previous tokens, K = DK) -> TMEM
         //      cols [0, 64); record rows 64..127 of the TZP tile get -Z' diag(kd')
         if (zprev) {
             ok = mbar_wait(&bar[2], 0) && ok;
-            fence_async_smem();
-            tc_fence_before();
             ok = __syncthreads_and(ok ? 1 : 0) != 0;
-            tc_fence_after();
             if (tid == 0 && ok) {
                 const uint32_t id = idesc_bf16_f32(64, 64);
 #pragma unroll
                 for (int ks = 0; ks < DK / 16; ++ks)
                     mma_bf16(tmem, tile_desc(smem_u32(WB), 64, 0, ks),
-                             tile_desc(smem_u32(QK), 128, 0, ks), id, ks > 0);
+                             tile_desc(smem_u32(QK), 128, 64, ks), id, ks > 0);
                 mma_commit(&bar[0]);
             }
             ok = __syncthreads_and((ok && mbar_wait(&bar[0], 0)) ? 1 : 0) != 0;
@@ -484,6 +491,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         }
     }
     if (!ok && lane == 0) atomicExch(&g_tc_error, 1);
+    if (tid == 0) bulk_wait_all();  // the W tile copy has read shared memory and landed
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 128);
@@ -494,7 +502,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
 template <int DK>
 struct ScanLayout {
     static constexpr int KB = (DK + 63) / 64;
-    static constexpr int AW_BYTES = 128 * 128 * KB;  // [128][DK] K-major: -g_C' W rows, Q' rows
+    static constexpr int AW_BYTES = 128 * 128 * KB;  // [128][DK] K-major: W rows, Q' rows
     static constexpr int AW = 0;                      // x2
     static constexpr int TZP = AW + 2 * AW_BYTES;     // x2 [192][64] K-major: T diag(beta), -Z', P'
     static constexpr int KR = TZP + 2 * 24576;        // x2 [64 tokens][128] MN-major: K'
@@ -534,12 +542,12 @@ __device__ __forceinline__ void scan_prefetch_l2(const bf16 *q, const bf16 *k, c
 }
 
 // Scan kernel roles (384 threads), stage j = 0..nblk (parity p = j & 1):
-//   warp 0, lane 0   issues b_j = [-g_C' W_j; Q_{j-1}] S_{j-1}^T and
+//   warp 0, lane 0   issues b_j = [W_j; Q_{j-1}] S_{j-1}^T (the U rows take -g_C') and
 //                    c_j = [-Z_{j-1}; P_{j-1}] U_{j-1}   (P_{j-1} V_{j-1} without delta)
 //   warp 1, lane 0   issues a_j = [T_j diag(beta); *] V_j and
 //                    ds = K_{j-1}^T (kd U_{j-1})          (K^T (kd V) without delta)
 //   warp 2, lane 0   loads the early group of stage j into buffer p: what a_j
-//                    and b_j read (-g_C' W_j, T_j diag(beta), Q_{j-1}, V_j)
+//                    and b_j read (W_j, T_j diag(beta), Q_{j-1}, V_j)
 //   warp 3           lane 0 loads the late group: what c_j, ds and the
 //                    epilogues read (-Z_{j-1}, P_{j-1}, K_{j-1}, the gates;
 //                    V_{j-1} without delta); without delta the warp then forms
@@ -836,6 +844,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                 if (!ok) break;
                 tc_fence_after();
                 const float kdr = vec_of(p)[kVkd + r];
+                const float gn = -vec_of(p)[kVgCPrev];  // b's W rows carry -g_C'
                 float x[16], y[16], z[16];
                 tmem_ld16(tmem + lb + base + kDa, x);
                 tmem_ld16(tmem + lb + base + kDb, y);
@@ -843,11 +852,11 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                     tmem_ld16(tmem + lb + base + kDc, z);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) x[c] += y[c] + z[c];
+                    for (int c = 0; c < 16; ++c) x[c] += gn * y[c] + z[c];
                 } else {
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) x[c] += y[c];
+                    for (int c = 0; c < 16; ++c) x[c] += gn * y[c];
                 }
 #pragma unroll
                 for (int c8 = 0; c8 < 2; ++c8)

@@ -221,6 +221,17 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Shared -> global bulk copy (both 16-byte aligned, size a multiple of 16),
+// tracked by the issuing thread's bulk-async group; commit and wait below.
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed shared -> global bulk copy of this thread is done.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Tiled TMA load of a 3-D box (coordinates x innermost) into shared memory,
 // completion counted on `bar`.  `map` is a __grid_constant__ CUtensorMap.
 __device__ __forceinline__ void tma_load_3d(void *dst, const void *map, int x, int y, int z,
