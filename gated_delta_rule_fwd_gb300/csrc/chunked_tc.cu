@@ -858,21 +858,21 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
 #pragma unroll
                     for (int c = 0; c < 16; ++c) x[c] += gn * y[c];
                 }
+                // kd U (for ds, on the state chain) and U (for c, on the U chain)
+                float xk[16];
 #pragma unroll
-                for (int c8 = 0; c8 < 2; ++c8)
+                for (int c = 0; c < 16; ++c) xk[c] = x[c] * kdr;
+#pragma unroll
+                for (int c8 = 0; c8 < 2; ++c8) {
+                    *reinterpret_cast<uint4 *>(sm + L::UBK + p * 8192 +
+                                               sw128_offset(r, ch + c8 * 8, 64)) = pack8(xk + c8 * 8);
                     *reinterpret_cast<uint4 *>(sm + L::UB + sw128_offset(r, ch + c8 * 8, 64)) =
                         pack8(x + c8 * 8);
+                }
                 fence_async_smem();
                 tc_fence_before();
-                warp_arrive(&bars->u);
-#pragma unroll
-                for (int c = 0; c < 16; ++c) x[c] *= kdr;
-#pragma unroll
-                for (int c8 = 0; c8 < 2; ++c8)
-                    *reinterpret_cast<uint4 *>(sm + L::UBK + p * 8192 +
-                                               sw128_offset(r, ch + c8 * 8, 64)) = pack8(x + c8 * 8);
-                fence_async_smem();
                 warp_arrive(&bars->uk[p]);
+                warp_arrive(&bars->u);
             } else {
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
@@ -954,12 +954,12 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
 #pragma unroll
                 for (int c = 0; c < SC; ++c) Sr[c] = gC * Sr[c] + d[c];
                 tc_fence_before();
-                warp_arrive(&bars->emptyL[p]);
                 if (j < nblk) {  // S_j -> copy (j+1)&1, read by b_{j+1}
                     write_sb((j + 1) & 1);
                     fence_async_smem();
                     warp_arrive(&bars->s[(j + 1) & 1]);
                 }
+                warp_arrive(&bars->emptyL[p]);
             } else {
                 warp_arrive(&bars->emptyL[p]);
             }
