@@ -548,12 +548,10 @@ __device__ __forceinline__ void scan_prefetch_l2(const bf16 *q, const bf16 *k, c
 //                    ds = K_{j-1}^T (kd U_{j-1})          (K^T (kd V) without delta)
 //   warp 2, lane 0   loads the early group of stage j into buffer p: what a_j
 //                    and b_j read (W_j, T_j diag(beta), Q_{j-1}, V_j)
-//   warp 3           lane 0 loads the late group: what c_j, ds and the
-//                    epilogues read (-Z_{j-1}, P_{j-1}, K_{j-1}, the gates;
-//                    V_{j-1} without delta); without delta the warp then forms
-//                    kd' V' for ds
+//   warp 3, lane 0   loads the late group: what c_j, ds and the epilogues read
+//                    (-Z_{j-1}, P_{j-1}, K_{j-1}, the gates; V_{j-1} without delta)
 //   warps 4, 5, 8, 9 U rows (TMEM lanes 0..63): U_j = Da + Db + Dc -> bf16 U,
-//                    kd U
+//                    kd U; without delta they form kd' V' for ds instead
 //   warps 6, 7, 10, 11  output rows (lanes 64..127): O_{j-1} = g' Db + Dc
 //   warps 12..19     state (lanes 0..127 = key channels): S_j = g_C' S_{j-1} + ds,
 //                    fp32 in registers, bf16 copy for b_{j+1}
@@ -582,7 +580,7 @@ struct ScanBars {
     uint64_t emptyE[2];  // early group read                             (2 commits)
     uint64_t fullL[2];   // late group landed                            (1 + tx bytes)
     uint64_t emptyL[2];  // late group read                              (2 commits + 16 warps)
-    uint64_t vkr[2];     // kd' V' written (no delta)                    (1 warp)
+    uint64_t vkr[2];     // kd' V' written (no delta)                    (4 warps)
     uint64_t dA[2];      // b and c products of the stage done           (commit)
     uint64_t dB[2];      // a product of the stage done                  (commit)
     uint64_t dsf[2];     // ds product of the stage done                 (commit)
@@ -624,7 +622,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             mbar_init(&bars->emptyE[b], 2);
             mbar_init(&bars->fullL[b], 1);
             mbar_init(&bars->emptyL[b], kEmptyLCount);
-            mbar_init(&bars->vkr[b], 1);
+            mbar_init(&bars->vkr[b], 4);
             mbar_init(&bars->dA[b], 1);
             mbar_init(&bars->dB[b], 1);
             mbar_init(&bars->dsf[b], 1);
@@ -801,28 +799,6 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            if (!DELTA && !prev) warp_arrive(&bars->vkr[p]);  // one completion per stage keeps the parities aligned
-            if (!DELTA && prev) {
-                // kd' V' (B operand of Delta S = K'^T diag(kd') V')
-                ok = __all_sync(0xffffffffu, mbar_wait(&bars->fullL[p], (j >> 1) & 1));
-                if (!ok) break;
-                const float *vec = vec_of(p);
-                const uint8_t *vr = sm + L::VR + p * 8192;
-                uint8_t *vk = sm + L::UBK + p * 8192;
-                for (int idx = lane; idx < C * (DVS / 8); idx += 32) {
-                    const int r = idx / (DVS / 8), ch = idx % (DVS / 8);
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(
-                        vr + sw128_offset(r, (c0 & 63) + ch * 8, 64));
-                    const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
-                    const float f = vec[kVkdPrev + r];
-                    float x[8];
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) x[t] = f * __bfloat162float(e[t]);
-                    *reinterpret_cast<uint4 *>(vk + sw128_offset(r, ch * 8, 64)) = pack8(x);
-                }
-                fence_async_smem();
-                warp_arrive(&bars->vkr[p]);
-            }
         }
         // never leave with copies into shared memory in flight
         if (lane == 0)
@@ -876,6 +852,28 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             } else {
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
+                if (!DELTA && j >= 1) {
+                    // kd' V' (B operand of Delta S = K'^T diag(kd') V'): this warp's
+                    // 16 token rows
+                    const float *vec = vec_of(p);
+                    const uint8_t *vr = sm + L::VR + p * 8192;
+                    uint8_t *vk = sm + L::UBK + p * 8192;
+                    const int rw = 16 * (((warp & 3) << 1) | ((warp - 4) >> 2));
+                    for (int idx = lane; idx < 16 * (DVS / 8); idx += 32) {
+                        const int rr = rw + idx / (DVS / 8), c8 = idx % (DVS / 8);
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(
+                            vr + sw128_offset(rr, (c0 & 63) + c8 * 8, 64));
+                        const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
+                        const float f = vec[kVkdPrev + rr];
+                        float xv[8];
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) xv[t] = f * __bfloat162float(e[t]);
+                        *reinterpret_cast<uint4 *>(vk + sw128_offset(rr, c8 * 8, 64)) = pack8(xv);
+                    }
+                    fence_async_smem();
+                }
+                // one completion per stage (also the first) keeps the parities aligned
+                if (!DELTA) warp_arrive(&bars->vkr[p]);
             }
             warp_arrive(&bars->emptyL[p]);
         }
