@@ -47,8 +47,8 @@ UNIT = "tokens/s"
 TRAFFIC_SOURCES = ("gated_delta_rule_fwd_gb300/csrc/chunked_tc.cu",
                    "gated_delta_rule_fwd_gb300/csrc/tc_common.cuh")
 TRAFFIC = {
-    "gdn_prefill_bf16": {"bytes": 272.721408e6 + 224.870656e6 + 681.656320e6 + 121.073408e6,
-                         "sha256": "c12dc0985642e7979a9637abd29e6ebc84a6ce228c796e818a1e4e80675edd3b"},
+    "gdn_prefill_bf16": {"bytes": 272.972544e6 + 290.167552e6 + 749.619712e6 + 122.302208e6,
+                         "sha256": "f830be6297d03eb31cc33167cf5a52c8651053093b7c0cfeb651e3779c4e1dbe"},
 }
 
 
