@@ -267,6 +267,18 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);  // MMA, q/k tiles, previous k tile
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 32);
     const bool zprev = DELTA && blk > 0;  // Z_{j-1} exists
+    // gate inputs first, so their global-load latency overlaps the staging:
+    // threads 0-63 this block's tokens, 64-127 the previous block's
+    const int tok = tid & 63;
+    float araw = 1.f, b = 0.f;
+    if (tid < C) {
+        if (tok < n) {
+            if (ALPHA) araw = alpha[bh * T + t0 + tok];
+            if (DELTA) b = beta[bh * T + t0 + tok];
+        }
+    } else if (ALPHA && blk > 0) {
+        araw = alpha[bh * T + t0 - C + tok];
+    }
 
     // ---- stage Q, K by tiled TMA (zero-filled past the end of the sequence
     //      and, for d_k = 32, in the outer half of the 64-column box)
@@ -284,16 +296,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     }
     // ---- gates: warps 0-1 hold this block's tokens, warps 2-3 the previous
     //      block's (all ones for block 0)
-    const int tok = tid & 63;
-    float la = 0.f, b = 0.f;
-    if (tid < C) {
-        if (tok < n) {
-            if (ALPHA) la = __logf(alpha[bh * T + t0 + tok]);
-            if (DELTA) b = beta[bh * T + t0 + tok];
-        }
-    } else if (ALPHA && blk > 0) {
-        la = __logf(alpha[bh * T + t0 - C + tok]);
-    }
+    const float la = ALPHA ? __logf(araw) : 0.f;
     if (warp == 0) {
         tmem_alloc(tmem_slot, 128);
         tmem_relinquish();
@@ -364,10 +367,19 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
             float a[32];
             tmem_ld32(tmem + lane_base + 32 * half, a);
             tmem_ld_wait();
+            float gi[32];  // 1 / g of the key tokens of this half
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+                const float4 v4 = reinterpret_cast<const float4 *>(giv + half * 32)[e4];
+                gi[4 * e4] = v4.x;
+                gi[4 * e4 + 1] = v4.y;
+                gi[4 * e4 + 2] = v4.z;
+                gi[4 * e4 + 3] = v4.w;
+            }
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
                 const int i = half * 32 + e;
-                const float dec = !ALPHA ? 1.f : (factor ? gr * giv[i] : __expf(Gr - Gv[i]));
+                const float dec = !ALPHA ? 1.f : (factor ? gr * gi[e] : __expf(Gr - Gv[i]));
                 a[e] = (i <= r && (is_q || i < r)) ? a[e] * dec : 0.f;
             }
             if (is_q) {
@@ -479,7 +491,13 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                     tmem_ld_wait();
                     if (lane < 16) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) z[e] = -z[e] * kdv[half * 32 + e];
+                        for (int e4 = 0; e4 < 8; ++e4) {  // -Z' diag(kd')
+                            const float4 v4 = reinterpret_cast<const float4 *>(kdv + half * 32)[e4];
+                            z[4 * e4] *= -v4.x;
+                            z[4 * e4 + 1] *= -v4.y;
+                            z[4 * e4 + 2] *= -v4.z;
+                            z[4 * e4 + 3] *= -v4.w;
+                        }
 #pragma unroll
                         for (int i8 = 0; i8 < 4; ++i8)
                             *reinterpret_cast<uint4 *>(
@@ -738,7 +756,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                 if (!ok) break;
                 const uint8_t *rec = recs + (size_t)j * R::BYTES;
                 uint8_t *aw = sm + L::AW + p * L::AW_BYTES;
-                if (j + 2 <= nblk)
+                if (j + 2 <= nblk && blockIdx.x == 0)  // one CTA of the head suffices
                     scan_prefetch_l2<DK, DELTA>(q, k, v, rec + 2 * (size_t)R::BYTES, bh, T, j + 2,
                                                 nblk, dv);
                 const bool cur = DELTA && j < nblk, prev = j >= 1;
@@ -812,15 +830,19 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
         for (int j = 0; j <= nblk && ok; ++j) {
             const int p = j & 1;
             const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
-            ok = mbar_wait(&bars->fullL[p], ph);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->fullL[p], ph));
+            if (!ok) break;
+            // with delta only the gates are read from the late group: take them
+            // and release it now
+            const float kdr = DELTA ? vec_of(p)[kVkd + r] : 0.f;
+            const float gn = DELTA ? -vec_of(p)[kVgCPrev] : 0.f;  // b's W rows carry -g_C'
+            if (DELTA) warp_arrive(&bars->emptyL[p]);
             if (DELTA && j < nblk) {
-                ok = ok && mbar_wait(&bars->dA[p], ph);
+                ok = mbar_wait(&bars->dA[p], ph);
                 ok = ok && mbar_wait(&bars->dB[p], ph);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                const float kdr = vec_of(p)[kVkd + r];
-                const float gn = -vec_of(p)[kVgCPrev];  // b's W rows carry -g_C'
                 float x[16], y[16], z[16];
                 tmem_ld16(tmem + lb + base + kDa, x);
                 tmem_ld16(tmem + lb + base + kDb, y);
@@ -875,7 +897,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                 // one completion per stage (also the first) keeps the parities aligned
                 if (!DELTA) warp_arrive(&bars->vkr[p]);
             }
-            warp_arrive(&bars->emptyL[p]);
+            if (!DELTA) warp_arrive(&bars->emptyL[p]);
         }
     } else if (warp < 12) {
         // ===================================== output rows (TMEM lanes 64..127)
@@ -885,13 +907,14 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
         for (int j = 0; j <= nblk && ok; ++j) {
             const int p = j & 1;
             const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
-            ok = mbar_wait(&bars->fullL[p], ph);
-            if (j >= 1) ok = ok && mbar_wait(&bars->dA[p], ph);
-            ok = __all_sync(0xffffffffu, ok);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->fullL[p], ph));
+            if (!ok) break;
+            const float gr = vec_of(p)[kVgPrev + r];  // the only late-group value read here
+            warp_arrive(&bars->emptyL[p]);
+            if (j >= 1) ok = __all_sync(0xffffffffu, mbar_wait(&bars->dA[p], ph));
             if (!ok) break;
             if (j >= 1) {
                 tc_fence_after();
-                const float gr = vec_of(p)[kVgPrev + r];
                 float x[16], y[16];
                 tmem_ld16(tmem + lb + base + kDb, x);
                 tmem_ld16(tmem + lb + base + kDc, y);
@@ -900,7 +923,6 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                 for (int c = 0; c < 16; ++c) x[c] = gr * x[c] + y[c];  // g' Q' S'^T + P' U'
                 tc_fence_before();
                 warp_arrive(&bars->tfree[p]);
-                warp_arrive(&bars->emptyL[p]);
                 const int t = (j - 1) * C + r;
                 if (t < T) {
                     uint4 *dst = reinterpret_cast<uint4 *>(o + (bh * T + t) * dv + c0 + ch);
@@ -909,7 +931,6 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                 }
             } else {
                 warp_arrive(&bars->tfree[p]);
-                warp_arrive(&bars->emptyL[p]);
             }
         }
     } else {
@@ -939,13 +960,14 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
         for (int j = 0; j <= nblk && ok; ++j) {
             const int p = j & 1;
             const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
-            ok = mbar_wait(&bars->fullL[p], ph);
-            ok = ok && mbar_wait(&bars->dsf[p], ph);
-            ok = __all_sync(0xffffffffu, ok);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->fullL[p], ph));
+            if (!ok) break;
+            const float gC = vec_of(p)[kVgCPrev];  // the only late-group value read here
+            warp_arrive(&bars->emptyL[p]);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->dsf[p], ph));
             if (!ok) break;
             if (j >= 1) {
                 tc_fence_after();
-                const float gC = vec_of(p)[kVgCPrev];
                 float d[SC];
                 tmem_ld16(tmem + lb + base + kDS, d);
                 tmem_ld_wait();
@@ -957,9 +979,6 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                     fence_async_smem();
                     warp_arrive(&bars->s[(j + 1) & 1]);
                 }
-                warp_arrive(&bars->emptyL[p]);
-            } else {
-                warp_arrive(&bars->emptyL[p]);
             }
         }
         if (ok && kc < DK) {
