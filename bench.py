@@ -47,8 +47,8 @@ UNIT = "tokens/s"
 TRAFFIC_SOURCES = ("gated_delta_rule_fwd_gb300/csrc/chunked_tc.cu",
                    "gated_delta_rule_fwd_gb300/csrc/tc_common.cuh")
 TRAFFIC = {
-    "gdn_prefill_bf16": {"bytes": 272.972544e6 + 290.167552e6 + 749.619712e6 + 122.302208e6,
-                         "sha256": "f830be6297d03eb31cc33167cf5a52c8651053093b7c0cfeb651e3779c4e1dbe"},
+    "gdn_prefill_bf16": {"bytes": 273.014528e6 + 290.017792e6 + 749.657344e6 + 122.396672e6,
+                         "sha256": "7421293ca7219fb9f02715822e2252ef70d7ddbcc6785674c738536d5a602f03"},
 }
 
 
