@@ -36,11 +36,12 @@
 //  * prep: one CTA per (block, head, batch), all blocks in parallel.  Computes
 //    what does not depend on the state: the gates, the scores P, the UT
 //    inverse T (fp32, in place; 16 x 16 diagonal blocks on the CUDA cores,
-//    the block rows on warp-level tf32 MMAs), W and Z, and writes the
-//    workspace record of "stage" j: W_j, T_j diag(beta), -Z_{j-1}, P_{j-1}
-//    and the gate vectors, as bf16 tiles already in the shared-memory operand
-//    layout (primes: the previous block).  Stage j's P row block is written by the
-//    CTA of block j-1; there is one more stage than blocks.
+//    then 32 x 32 and 64 x 64 block inversion on warp-level tf32 MMAs), W and
+//    Z, and writes the workspace record of "stage" j: W_j, T_j diag(beta),
+//    -Z_{j-1}, P_{j-1} and the gate vectors, as bf16 tiles already in the
+//    shared-memory operand layout (primes: the previous block).  Stage j's P
+//    row block is written by the CTA of block j-1; there is one more stage
+//    than blocks.
 //  * scan: one CTA per (32 value channels, head, batch); rows of S evolve
 //    independently given k, alpha and beta, so slices never exchange data.
 //    It walks the stages in order with warp-specialised roles (below).
@@ -73,8 +74,8 @@ using namespace tc;
 constexpr int C = 64;      // tokens per block
 constexpr int DVS = 32;    // value channels per scan CTA
 constexpr int NT = 128;    // threads per prep CTA
-constexpr int AP = C + 1;  // padded fp32 row of A and T
-constexpr int XP = 49;     // padded fp32 row of the solve scratch
+constexpr int AP = C + 4;  // fp32 row of A and T: 16-byte rows, 8-row groups on distinct banks
+constexpr int XS = 40;     // fp32 row of the solve scratch
 
 __device__ int g_tc_error = 0;  // set to 1 when a bounded wait gives up
 
@@ -123,19 +124,19 @@ struct PrepLayout {
     static constexpr int KB = (DK + 63) / 64;
     static constexpr int QK = 0;
     static constexpr int TB = QK;                           // [64][64] bf16, in the Q rows of block 0
-    static constexpr int XT = TB;                           // fp32 [16][XP] solve scratch, inside TB
+    static constexpr int XT = TB;                           // fp32 [32][XS] solve scratch, inside TB
     static constexpr int AT = QK + 128 * 128 * KB;
     static constexpr int VEC = AT + C * AP * 4;             // G (later kd'), ginv, g, beta
     static constexpr int BAR = VEC + 4 * 64 * 4;            // 3 barriers, TMEM slot
     static constexpr int BYTES = BAR + 64;
     static constexpr int ALLOC = BYTES + 1024;
 };
-static_assert(16 * XP * 4 <= 8192, "solve scratch must fit inside the T tile");
+static_assert(32 * XS * 4 <= 8192, "solve scratch must fit inside the T tile");
 static_assert(128 * 64 * 2 <= C * AP * 4, "the W tile must fit over the A matrix");
 static_assert(PrepLayout<128>::AT % 1024 == 0, "the W tile must be 1024-byte aligned");
 
-// Element (r, c) of a 64 x 64 fp32 matrix in shared memory, rows padded to 65
-// floats so that a warp touching one column of 32 rows hits 32 banks.
+// Element (r, c) of a 64 x 64 fp32 matrix in shared memory, rows padded to
+// AP floats.
 __device__ __forceinline__ int sw64(int r, int c) { return r * AP + c; }
 
 // D (16x8, fp32) += A (16x8, tf32) B (8x8, tf32): the warp-level tensor-core
@@ -155,60 +156,32 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-
-// One block row BR of the blocked UT inverse (rows 16BR..16BR+15), with the
-// rows above it done:
-//   X = A[rows, cols < 16BR] T[< 16BR, < 16BR];   T[rows, cols < 16BR] = -T_bb X
-// in place: T[rows, cols < 16BR] overwrites A there once X is formed.
-// on the tensor cores (m16n8k8, tf32 in, fp32 accumulate).  Warp w takes the
-// 8-column tiles nt = w, w+4, ...; K steps that only meet the zero blocks of T
-// above its block diagonal are skipped, so those blocks are never read.
-template <int BR>
-__device__ __forceinline__ void ut_block_row(float *AT, float *Xt, int tid) {
-    const float *Am = AT;  // row block BR still holds A left of its diagonal block
-    float *Tm = AT;        // rows above it and its diagonal block already hold T
-    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-    const int r0 = 16 * BR;
-    for (int nt = warp; nt < 2 * BR; nt += 4) {
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int kk = 2 * (nt >> 1); kk < 2 * BR; ++kk) {
-            const uint32_t a[4] = {to_tf32(Am[(r0 + g) * AP + 8 * kk + t]),
-                                   to_tf32(Am[(r0 + g + 8) * AP + 8 * kk + t]),
-                                   to_tf32(Am[(r0 + g) * AP + 8 * kk + t + 4]),
-                                   to_tf32(Am[(r0 + g + 8) * AP + 8 * kk + t + 4])};
-            mma_tf32(d, a, to_tf32(Tm[(8 * kk + t) * AP + 8 * nt + g]),
-                     to_tf32(Tm[(8 * kk + t + 4) * AP + 8 * nt + g]));
-        }
-        Xt[g * XP + 8 * nt + 2 * t] = d[0];
-        Xt[g * XP + 8 * nt + 2 * t + 1] = d[1];
-        Xt[(g + 8) * XP + 8 * nt + 2 * t] = d[2];
-        Xt[(g + 8) * XP + 8 * nt + 2 * t + 1] = d[3];
-    }
-    __syncthreads();
-    for (int nt = warp; nt < 2 * BR; nt += 4) {
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
+// A fragment of the rows r0..r0+15, columns c0..c0+7 (c0 % 4 == 0) of a fp32
+// matrix with row stride AP, rounded to tf32.  ldmatrix.x4 on 32-bit data:
+// each 8 x 8 b16 matrix is 8 rows x 4 floats, and thread (g, t) receives
+// element (g, t) of each of the four 8 x 4 quarters.
+__device__ __forceinline__ void lda_tf32(uint32_t (&a)[4], const float *m, int r0, int c0,
+                                         int lane) {
+    const int q = lane >> 3, rr = lane & 7;
+    const float *p = m + (r0 + rr + 8 * (q & 1)) * AP + c0 + 4 * (q >> 1);
+    uint32_t v[4];
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "r"(smem_u32(p)));
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-            const uint32_t a[4] = {to_tf32(Tm[(r0 + g) * AP + r0 + 8 * kk + t]),
-                                   to_tf32(Tm[(r0 + g + 8) * AP + r0 + 8 * kk + t]),
-                                   to_tf32(Tm[(r0 + g) * AP + r0 + 8 * kk + t + 4]),
-                                   to_tf32(Tm[(r0 + g + 8) * AP + r0 + 8 * kk + t + 4])};
-            mma_tf32(d, a, to_tf32(Xt[(8 * kk + t) * XP + 8 * nt + g]),
-                     to_tf32(Xt[(8 * kk + t + 4) * XP + 8 * nt + g]));
-        }
-        Tm[(r0 + g) * AP + 8 * nt + 2 * t] = -d[0];
-        Tm[(r0 + g) * AP + 8 * nt + 2 * t + 1] = -d[1];
-        Tm[(r0 + g + 8) * AP + 8 * nt + 2 * t] = -d[2];
-        Tm[(r0 + g + 8) * AP + 8 * nt + 2 * t + 1] = -d[3];
-    }
-    __syncthreads();
+    for (int i = 0; i < 4; ++i) a[i] = to_tf32(__uint_as_float(v[i]));
 }
 
 // T = (I + A)^-1 for a strictly lower A (64 x 64, fp32 in shared memory),
-// computed in place.  On exit AT holds T's lower triangle (diagonal blocks
-// include their zero upper triangles); the blocks above the block diagonal
-// keep A's zeros and are never read.
+// computed in place by block inversion: with A = [A11 0; A21 A22],
+//   T = [T11 0; -T22 A21 T11  T22],
+// applied to the 16 x 16 diagonal blocks (CUDA cores, fp32), then to the two
+// 32 x 32 diagonal blocks, then to the whole (tf32 warp-level MMAs with fp32
+// accumulation).  On exit AT holds T's lower triangle; the blocks above the
+// block diagonal keep A's zeros.  Xt is a 32 x XS fp32 scratch.
 __device__ __forceinline__ void ut_inverse(float *AT, float *Xt, int tid) {
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    // ---- 16 x 16 diagonal blocks: thread (b, c) solves column c of block b
     float x[16];
     const int b = tid >> 4, c = tid & 15;
     if (tid < 64) {
@@ -230,9 +203,76 @@ __device__ __forceinline__ void ut_inverse(float *AT, float *Xt, int tid) {
         for (int rr = 0; rr < 16; ++rr) AT[sw64(16 * b + rr, 16 * b + c)] = x[rr];
     }
     __syncthreads();
-    ut_block_row<1>(AT, Xt, tid);
-    ut_block_row<2>(AT, Xt, tid);
-    ut_block_row<3>(AT, Xt, tid);
+    // ---- 32 x 32 diagonal blocks: T[R, C] = -T[R, R] A[R, C] T[C, C] for the
+    //      16-row blocks (R, C) = (1, 0) and (3, 2); warp w: pair w/2, column tile w%2
+    {
+        const int pr = warp >> 1, nt = warp & 1;
+        const int R = 32 * pr + 16, Cc = 32 * pr;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int kk = nt; kk < 2; ++kk) {  // rows of T[C, C] above 8 nt are zero in this tile
+            uint32_t a[4];
+            lda_tf32(a, AT, R, Cc + 8 * kk, lane);
+            mma_tf32(d, a, to_tf32(AT[sw64(Cc + 8 * kk + t, Cc + 8 * nt + g)]),
+                     to_tf32(AT[sw64(Cc + 8 * kk + t + 4, Cc + 8 * nt + g)]));
+        }
+        float *xw = Xt + (16 * pr) * XS + 8 * nt;  // this warp's 16 x 8 tile of X
+        xw[g * XS + 2 * t] = d[0];
+        xw[g * XS + 2 * t + 1] = d[1];
+        xw[(g + 8) * XS + 2 * t] = d[2];
+        xw[(g + 8) * XS + 2 * t + 1] = d[3];
+        __syncwarp();
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            uint32_t a[4];
+            lda_tf32(a, AT, R, R + 8 * kk, lane);
+            mma_tf32(e, a, to_tf32(xw[(8 * kk + t) * XS + g]),
+                     to_tf32(xw[(8 * kk + t + 4) * XS + g]));
+        }
+        __syncthreads();  // both column tiles have read A[R, C]
+        AT[sw64(R + g, Cc + 8 * nt + 2 * t)] = -e[0];
+        AT[sw64(R + g, Cc + 8 * nt + 2 * t + 1)] = -e[1];
+        AT[sw64(R + g + 8, Cc + 8 * nt + 2 * t)] = -e[2];
+        AT[sw64(R + g + 8, Cc + 8 * nt + 2 * t + 1)] = -e[3];
+    }
+    __syncthreads();
+    // ---- whole matrix: X = A21 T11 (32 x 32) to the scratch; warp w takes the
+    //      tiles (w%2, w/2) and (1 - w%2, 3 - w/2), five k steps in all
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int mt = h ? 1 - (warp & 1) : (warp & 1);
+        const int nt = h ? 3 - (warp >> 1) : (warp >> 1);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int kk = nt; kk < 4; ++kk) {  // rows of T11 above 8 nt are zero in this tile
+            uint32_t a[4];
+            lda_tf32(a, AT, 32 + 16 * mt, 8 * kk, lane);
+            mma_tf32(d, a, to_tf32(AT[sw64(8 * kk + t, 8 * nt + g)]),
+                     to_tf32(AT[sw64(8 * kk + t + 4, 8 * nt + g)]));
+        }
+        float *xw = Xt + (16 * mt) * XS + 8 * nt;
+        xw[g * XS + 2 * t] = d[0];
+        xw[g * XS + 2 * t + 1] = d[1];
+        xw[(g + 8) * XS + 2 * t] = d[2];
+        xw[(g + 8) * XS + 2 * t + 1] = d[3];
+    }
+    __syncthreads();  // X complete, A21 no longer read
+    //      T21 = -T22 X: warp w takes column tile w, both row tiles
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+        const int nt = warp;
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int kk = 0; kk < 2 * mt + 2; ++kk) {  // T22 row tile mt is zero right of 16 (mt + 1)
+            uint32_t a[4];
+            lda_tf32(a, AT, 32 + 16 * mt, 32 + 8 * kk, lane);
+            mma_tf32(e, a, to_tf32(Xt[(8 * kk + t) * XS + 8 * nt + g]),
+                     to_tf32(Xt[(8 * kk + t + 4) * XS + 8 * nt + g]));
+        }
+        AT[sw64(32 + 16 * mt + g, 8 * nt + 2 * t)] = -e[0];
+        AT[sw64(32 + 16 * mt + g, 8 * nt + 2 * t + 1)] = -e[1];
+        AT[sw64(32 + 16 * mt + g + 8, 8 * nt + 2 * t)] = -e[2];
+        AT[sw64(32 + 16 * mt + g + 8, 8 * nt + 2 * t + 1)] = -e[3];
+    }
+    __syncthreads();
 }
 
 // Prep of block j = blockIdx.x.  Writes to record j: W_j, T_j diag(beta),
@@ -390,8 +430,11 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                         pack8(a + i8 * 8);
             } else if (DELTA) {
                 const float br = bv[r];
+                float4 *row = reinterpret_cast<float4 *>(Am + sw64(r, half * 32));
 #pragma unroll
-                for (int e = 0; e < 32; ++e) Am[sw64(r, half * 32 + e)] = br * a[e];
+                for (int e4 = 0; e4 < 8; ++e4)
+                    row[e4] = make_float4(br * a[4 * e4], br * a[4 * e4 + 1], br * a[4 * e4 + 2],
+                                          br * a[4 * e4 + 3]);
             }
         }
     }
@@ -405,12 +448,20 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         // solve scratch), the A operand of W = T diag(beta g) K
         for (int idx = tid; idx < C * 8; idx += NT) {
             const int r = idx >> 3, i8 = idx & 7;
-            float t[8], tg[8];
+            float t[8], tg[8], tv[8], bb[8], gg[8];
+            *reinterpret_cast<float4 *>(tv) =
+                *reinterpret_cast<const float4 *>(Am + sw64(r, i8 * 8));
+            *reinterpret_cast<float4 *>(tv + 4) =
+                *reinterpret_cast<const float4 *>(Am + sw64(r, i8 * 8 + 4));
+            *reinterpret_cast<float4 *>(bb) = reinterpret_cast<const float4 *>(bv)[2 * i8];
+            *reinterpret_cast<float4 *>(bb + 4) = reinterpret_cast<const float4 *>(bv)[2 * i8 + 1];
+            *reinterpret_cast<float4 *>(gg) = reinterpret_cast<const float4 *>(gv)[2 * i8];
+            *reinterpret_cast<float4 *>(gg + 4) = reinterpret_cast<const float4 *>(gv)[2 * i8 + 1];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int i = i8 * 8 + e;
-                t[e] = i <= r ? Am[sw64(r, i)] * bv[i] : 0.f;
-                tg[e] = t[e] * gv[i];
+                t[e] = i <= r ? tv[e] * bb[e] : 0.f;
+                tg[e] = t[e] * gg[e];
             }
             *reinterpret_cast<uint4 *>(rec + R::TZP + sw128_offset(r, i8 * 8, 192)) = pack8(t);
             *reinterpret_cast<uint4 *>(TB + sw128_offset(r, i8 * 8, 64)) = pack8(tg);
