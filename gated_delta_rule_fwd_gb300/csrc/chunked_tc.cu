@@ -615,10 +615,11 @@ __device__ __forceinline__ void scan_prefetch_l2(const bf16 *q, const bf16 *k, c
 //                    c_j = [-Z_{j-1}; P_{j-1}] U_{j-1}   (P_{j-1} V_{j-1} without delta)
 //   warp 1, lane 0   issues a_j = [T_j diag(beta); *] V_j and
 //                    ds = K_{j-1}^T (kd U_{j-1})          (K^T (kd V) without delta)
-//   warp 2, lane 0   loads the early group of stage j into buffer p: what a_j
-//                    and b_j read (W_j, T_j diag(beta), Q_{j-1}, V_j)
-//   warp 3, lane 0   loads the late group: what c_j, ds and the epilogues read
-//                    (-Z_{j-1}, P_{j-1}, K_{j-1}, the gates; V_{j-1} without delta)
+//   warp 2, lane 0   loads the early group of stage j into buffer p: what b_j
+//                    reads (W_j, Q_{j-1})
+//   warp 3, lane 0   loads the late group: what a_j, c_j, ds and the epilogues
+//                    read (T_j diag(beta), -Z_{j-1}, P_{j-1}, K_{j-1}, the gates,
+//                    V_j; V_{j-1} without delta)
 //   warps 4, 5, 8, 9 U rows (TMEM lanes 0..63): U_j = Da + Db + Dc -> bf16 U,
 //                    kd U; without delta they form kd' V' for ds instead
 //   warps 6, 7, 10, 11  output rows (lanes 64..127): O_{j-1} = g' Db + Dc
@@ -628,8 +629,9 @@ __device__ __forceinline__ void scan_prefetch_l2(const bf16 *q, const bf16 *k, c
 // half of the 32 value channels, to keep the per-warp instruction chains short.
 // All loads are TMA or bulk copies completing on the group's `full` barrier,
 // which the consumers wait on directly.  The early group is released as soon
-// as a_j and b_j are done, so the next fill of that half of the buffer starts
-// about half a stage earlier than the late one.
+// as b_j is done, so the next fill of that part of the buffer starts about
+// half a stage earlier than the late one; it is kept small (32 KB at
+// d_k = 128) because b_j sits on the state chain.
 // The state before the first block plays S_{-1} (with g_C = 1 and U_{-1} = 0).
 // Hand-offs are mbarriers, every wait bounded.  Each barrier is waited on by
 // all of its consumers before it can complete again: barriers that complete
@@ -646,7 +648,7 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
 
 struct ScanBars {
     uint64_t fullE[2];   // early group landed                           (1 + tx bytes)
-    uint64_t emptyE[2];  // early group read                             (2 commits)
+    uint64_t emptyE[2];  // early group read                             (1 commit)
     uint64_t fullL[2];   // late group landed                            (1 + tx bytes)
     uint64_t emptyL[2];  // late group read                              (2 commits + 16 warps)
     uint64_t vkr[2];     // kd' V' written (no delta)                    (4 warps)
@@ -688,7 +690,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars->fullE[b], 1);
-            mbar_init(&bars->emptyE[b], 2);
+            mbar_init(&bars->emptyE[b], 1);
             mbar_init(&bars->fullL[b], 1);
             mbar_init(&bars->emptyL[b], kEmptyLCount);
             mbar_init(&bars->vkr[b], 4);
@@ -767,7 +769,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             for (int j = 0; j <= nblk && ok; ++j) {
                 const int p = j & 1;
                 const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
-                ok = mbar_wait(&bars->fullE[p], ph);
+                ok = mbar_wait(&bars->fullL[p], ph);
                 if (!ok) break;
                 tc_fence_after();
                 if (DELTA && j < nblk) {
@@ -778,9 +780,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                                  id_kn, ks > 0);
                 }
                 mma_commit(&bars->dB[p]);
-                mma_commit(&bars->emptyE[p]);
                 if (j >= 1) {
-                    ok = mbar_wait(&bars->fullL[p], ph);
                     if (ok) ok = DELTA ? mbar_wait(&bars->uk[(j - 1) & 1], ((j - 1) >> 1) & 1)  // kd U_{j-1}
                                        : mbar_wait(&bars->vkr[p], ph);                          // kd' V'
                     if (!ok) break;
@@ -811,15 +811,13 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                     scan_prefetch_l2<DK, DELTA>(q, k, v, rec + 2 * (size_t)R::BYTES, bh, T, j + 2,
                                                 nblk, dv);
                 const bool cur = DELTA && j < nblk, prev = j >= 1;
-                const uint32_t bytes = (cur ? (uint32_t)R::KB * 8192u + 8192u + 8192u : 0u) +
+                const uint32_t bytes = (cur ? (uint32_t)R::KB * 8192u : 0u) +
                                        (prev ? (uint32_t)R::KB * 8192u : 0u);
                 mbar_expect_tx(&bars->fullE[p], bytes);
                 if (cur) {
 #pragma unroll
                     for (int kb = 0; kb < R::KB; ++kb)
                         bulk_g2s(aw + kb * 16384, rec + R::WT + kb * 8192, 8192, &bars->fullE[p]);
-                    bulk_g2s(sm + L::TZP + p * 24576, rec + R::TZP, 8192, &bars->fullE[p]);
-                    tma_load_3d(sm + L::VR + p * 8192, &tmv, vx, j * C, (int)bh, &bars->fullE[p]);
                 }
                 if (prev) {
 #pragma unroll
@@ -843,16 +841,18 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                 if (j >= 2) ok = mbar_wait(&bars->emptyL[p], ((j >> 1) - 1) & 1);
                 if (ok) {
                     const uint8_t *rec = recs + (size_t)j * R::BYTES;
-                    uint32_t bytes = 1024u;
-                    if (prev) bytes += (DELTA ? 16384u : 8192u) + (uint32_t)R::KB * 8192u +
+                    const bool cur = DELTA && j < nblk;
+                    uint32_t bytes = 1024u + (DELTA ? 24576u : 0u) + (cur ? 8192u : 0u);
+                    if (prev) bytes += (DELTA ? 0u : 8192u) + (uint32_t)R::KB * 8192u +
                                        (DELTA ? 0u : 8192u);
                     mbar_expect_tx(&bars->fullL[p], bytes);
                     bulk_g2s(sm + L::VEC + p * 1024, rec + R::VEC, 1024, &bars->fullL[p]);
+                    if (DELTA)
+                        bulk_g2s(sm + L::TZP + p * 24576, rec + R::TZP, 24576, &bars->fullL[p]);
+                    if (cur)
+                        tma_load_3d(sm + L::VR + p * 8192, &tmv, vx, j * C, (int)bh, &bars->fullL[p]);
                     if (prev) {
-                        if (DELTA)
-                            bulk_g2s(sm + L::TZP + p * 24576 + 8192, rec + R::TZP + 8192, 16384,
-                                     &bars->fullL[p]);
-                        else
+                        if (!DELTA)
                             bulk_g2s(sm + L::TZP + p * 24576 + 16384, rec + R::TZP + 16384, 8192,
                                      &bars->fullL[p]);
 #pragma unroll
