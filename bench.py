@@ -47,8 +47,8 @@ UNIT = "tokens/s"
 TRAFFIC_SOURCES = ("gated_delta_rule_fwd_gb300/csrc/chunked_tc.cu",
                    "gated_delta_rule_fwd_gb300/csrc/tc_common.cuh")
 TRAFFIC = {
-    "gdn_prefill_bf16": {"bytes": 273.014528e6 + 290.017792e6 + 749.657344e6 + 122.396672e6,
-                         "sha256": "7421293ca7219fb9f02715822e2252ef70d7ddbcc6785674c738536d5a602f03"},
+    "gdn_prefill_bf16": {"bytes": 273.051392e6 + 289.682176e6 + 750.554880e6 + 122.247424e6,
+                         "sha256": "e65ceac0d2c9e7883d6d7fee5878f597d4f70855c1939e9b04df9a81e17770c3"},
 }
 
 
