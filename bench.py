@@ -102,6 +102,11 @@ def chunk_flops(w):
     return w.B * w.H * w.T * per
 
 
+def recurrent_flops(w):
+    """Recurrent-form count: three d_k x d_v products per head-token."""
+    return w.B * w.H * w.T * 6 * w.dk * w.dv
+
+
 def decode_step_bytes(w):
     """State read + written once, plus q, k, v, o and alpha, beta."""
     nh = w.B * w.H
@@ -374,7 +379,9 @@ def run_ours(args, dist, rank, world, local):
                          "algorithmic_bytes_per_launch": nbytes},
             "tensor": {"achieved_tflops": achieved_tf, "peak_tflops": peaks["bf16_tflops"],
                        "frac_of_bf16_peak": achieved_tf / peaks["bf16_tflops"],
-                       "flops_per_launch": nflops, "count": "chunk-form MMA flops"},
+                       "flops_per_launch": nflops, "count": "chunk-form MMA flops",
+                       "recurrent_flops_per_launch": recurrent_flops(w),
+                       "achieved_tflops_recurrent_count": recurrent_flops(w) / kernel_s / 1e12},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                     "pipelined": "uploads, calls and downloads on three streams, two buffer sets"},
