@@ -10,6 +10,10 @@ missing or cannot be loaded, every call raises.
         chunkwise prefill over whole sequences (q, k: [B,H,T,dk], v: [B,H,T,dv])
     lr_step(q, k, v, alpha, beta, S, mode=...) -> o
         one decode step for N sequences, S: [N,H,dv,dk] updated in place
+    lr_fwd_chunked_fused / lr_step_fused(..., flags=..., ...)
+        the same with the maps around the recurrence (SiLU + L2 of q and k,
+        sigmoid beta, sigmoid or softplus alpha, output RMSNorm) applied inside
+        the kernels; flags are the FUSE_* constants
 """
 from __future__ import annotations
 
@@ -22,13 +26,26 @@ LINEAR, DECAY, DELTA, GATED_DELTA = 0, 1, 2, 3
 MODES = {"linear": LINEAR, "decay": DECAY, "delta": DELTA, "gated_delta": GATED_DELTA}
 F32, BF16 = 0, 1
 SYMBOLS = ("lr_fwd_chunked", "lr_fwd_chunked_workspace_size", "lr_fwd_chunked_noalloc", "lr_step",
+           "lr_fwd_chunked_fused", "lr_fwd_chunked_fused_workspace_size", "lr_step_fused",
            "lr_device_status", "lr_status_string", "lr_abi_version")
+# lr_fuse flags (include/lr.h)
+FUSE_QK_SILU_L2 = 0x1
+FUSE_BETA_SIGMOID = 0x2
+FUSE_ALPHA_SIGMOID = 0x4
+FUSE_ALPHA_SOFTPLUS = 0x8
+FUSE_O_RMSNORM = 0x10
 STATIC_WORKSPACE_BYTES = 64 << 20   # LR_STATIC_WORKSPACE_BYTES
 STATUS = {0: "LR_OK", 1: "LR_ERR_NULL", 2: "LR_ERR_SHAPE", 3: "LR_ERR_DTYPE", 4: "LR_ERR_ALIGN",
           5: "LR_ERR_MODE", 6: "LR_ERR_UNSUPPORTED", 7: "LR_ERR_CUDA", 8: "LR_ERR_ALIAS",
-          9: "LR_ERR_TIMEOUT", 10: "LR_ERR_WORKSPACE", 11: "LR_ERR_TOO_LARGE"}
+          9: "LR_ERR_TIMEOUT", 10: "LR_ERR_WORKSPACE", 11: "LR_ERR_TOO_LARGE", 12: "LR_ERR_FUSE"}
 _USES_ALPHA = {LINEAR: False, DECAY: True, DELTA: False, GATED_DELTA: True}
 _USES_BETA = {LINEAR: False, DECAY: False, DELTA: True, GATED_DELTA: True}
+
+
+class Fuse(ctypes.Structure):
+    """lr_fuse (include/lr.h)."""
+    _fields_ = [("flags", ctypes.c_uint), ("alpha_scale", ctypes.c_void_p),
+                ("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float)]
 
 
 class LrError(RuntimeError):
@@ -62,6 +79,14 @@ def lib() -> ctypes.CDLL:
         L.lr_fwd_chunked_workspace_size.argtypes = [i] * 8
         L.lr_step.restype = i
         L.lr_step.argtypes = [vp, vp, vp, fp, fp, fp, vp] + [i] * 4 + [i, i, vp]
+        fz = ctypes.POINTER(Fuse)
+        L.lr_fwd_chunked_fused.restype = i
+        L.lr_fwd_chunked_fused.argtypes = ([vp, vp, vp, fp, fp, fp, vp, fp] + [i] * 6 +
+                                           [i, i, fz, vp, ctypes.c_size_t, vp])
+        L.lr_fwd_chunked_fused_workspace_size.restype = ctypes.c_size_t
+        L.lr_fwd_chunked_fused_workspace_size.argtypes = [i] * 8 + [ctypes.c_uint]
+        L.lr_step_fused.restype = i
+        L.lr_step_fused.argtypes = [vp, vp, vp, fp, fp, fp, vp] + [i] * 4 + [i, i, fz, vp]
         L.lr_status_string.restype = ctypes.c_char_p
         L.lr_status_string.argtypes = [i]
         L.lr_abi_version.restype = i
@@ -247,4 +272,111 @@ def lr_step(q, k, v, alpha, beta, S, *, mode=GATED_DELTA, o=None, stream=None):
                        N, H, dk, dv, dt, int(mode), _stream_handle(stream, dev))
     if st != 0:
         raise LrError(st, "lr_step")
+    return o
+
+
+def _fuse(flags, alpha_scale, norm_weight, norm_eps, H, dv, dev):
+    import torch
+    if alpha_scale is not None:
+        _check(alpha_scale, "alpha_scale", (H,), torch.float32, dev)
+    if norm_weight is not None:
+        _check(norm_weight, "norm_weight", (dv,), torch.float32, dev)
+    return Fuse(int(flags), None if alpha_scale is None else alpha_scale.data_ptr(),
+                None if norm_weight is None else norm_weight.data_ptr(), float(norm_eps))
+
+
+def fused_workspace_size(B, H, T, dk, dv, dtype, mode=GATED_DELTA, flags=0, chunk=64) -> int:
+    """lr_fwd_chunked_fused_workspace_size for these sizes and flags."""
+    import torch
+    dt = F32 if dtype == torch.float32 else BF16
+    return int(lib().lr_fwd_chunked_fused_workspace_size(B, H, T, dk, dv, int(chunk), dt,
+                                                         int(MODES.get(mode, mode)), int(flags)))
+
+
+def lr_fwd_chunked_fused(q, k, v, alpha=None, beta=None, S0=None, *, mode=GATED_DELTA, flags=0,
+                         alpha_scale=None, norm_weight=None, norm_eps=1e-6, chunk=64, o=None,
+                         S_T=None, workspace=None, stream=None):
+    """Chunkwise forward with the maps around the recurrence
+    (``lr_fwd_chunked_fused`` in include/lr.h).
+
+    As :func:`lr_fwd_chunked`, with q, k, alpha and beta holding the
+    pre-activation values of the maps that ``flags`` selects (FUSE_*);
+    ``alpha_scale``: [H] float32 (the c_h of FUSE_ALPHA_SOFTPLUS);
+    ``norm_weight``: [dv] float32 or None (FUSE_O_RMSNORM).  Returns (o, S_T).
+    """
+    import torch
+    mode = MODES.get(mode, mode)
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _check(q, "q", (B, H, T, dk), q.dtype, dev)
+    _check(k, "k", (B, H, T, dk), q.dtype, dev)
+    _check(v, "v", (B, H, T, dv), q.dtype, dev)
+    alpha = alpha if _USES_ALPHA[mode] else None
+    beta = beta if _USES_BETA[mode] else None
+    if alpha is not None:
+        _check(alpha, "alpha", (B, H, T), torch.float32, dev)
+    if beta is not None:
+        _check(beta, "beta", (B, H, T), torch.float32, dev)
+    if S0 is not None:
+        _check(S0, "S0", (B, H, dv, dk), torch.float32, dev)
+    fz = _fuse(flags, alpha_scale, norm_weight, norm_eps, H, dv, dev)
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=q.dtype, device=dev)
+    else:
+        _check(o, "o", (B, H, T, dv), q.dtype, dev)
+    if S_T is None:
+        S_T = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+    else:
+        _check(S_T, "S_T", (B, H, dv, dk), torch.float32, dev)
+    need = int(lib().lr_fwd_chunked_fused_workspace_size(B, H, T, dk, dv, int(chunk), dt,
+                                                         int(mode), int(flags)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().lr_fwd_chunked_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                                    _ptr(S0), _ptr(o), _ptr(S_T), B, H, T, dk, dv, int(chunk),
+                                    dt, int(mode), ctypes.byref(fz), _ptr(workspace), ws_bytes,
+                                    _stream_handle(stream, dev))
+    if st != 0:
+        raise LrError(st, "lr_fwd_chunked_fused")
+    return o, S_T
+
+
+def lr_step_fused(q, k, v, alpha, beta, S, *, mode=GATED_DELTA, flags=0, alpha_scale=None,
+                  norm_weight=None, norm_eps=1e-6, o=None, stream=None):
+    """One decode step with the maps around the recurrence
+    (``lr_step_fused`` in include/lr.h); S is updated in place.  Arguments as
+    :func:`lr_step` plus those of :func:`lr_fwd_chunked_fused`.  Returns o."""
+    import torch
+    mode = MODES.get(mode, mode)
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _check(q, "q", (N, H, dk), q.dtype, dev)
+    _check(k, "k", (N, H, dk), q.dtype, dev)
+    _check(v, "v", (N, H, dv), q.dtype, dev)
+    alpha = alpha if _USES_ALPHA[mode] else None
+    beta = beta if _USES_BETA[mode] else None
+    if alpha is not None:
+        _check(alpha, "alpha", (N, H), torch.float32, dev)
+    if beta is not None:
+        _check(beta, "beta", (N, H), torch.float32, dev)
+    _check(S, "S", (N, H, dv, dk), torch.float32, dev)
+    fz = _fuse(flags, alpha_scale, norm_weight, norm_eps, H, dv, dev)
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=q.dtype, device=dev)
+    else:
+        _check(o, "o", (N, H, dv), q.dtype, dev)
+    st = lib().lr_step_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S), _ptr(o),
+                             N, H, dk, dv, dt, int(mode), ctypes.byref(fz),
+                             _stream_handle(stream, dev))
+    if st != 0:
+        raise LrError(st, "lr_step_fused")
     return o

@@ -23,6 +23,12 @@
 // lanes splitting each inner sum.  A final block shorter than C is padded
 // with k = q = v = 0, alpha = 1, beta = 0, which leaves state and outputs of
 // the real tokens unchanged; padded outputs are not stored.
+//
+// The lr_fuse maps act on what a block stages: the gates as they are read
+// (ln alpha formed directly from the pre-activation), and SiLU + L2 of the q
+// and k rows in shared memory (fp32, one warp per row).  The output RMSNorm
+// needs all d_v channels of a token, which are spread over the CTAs of a
+// head; it runs as a separate pass (norm.cu).
 #include "lr_internal.cuh"
 
 namespace lr {
@@ -56,7 +62,8 @@ __global__ void __launch_bounds__(NT)
 chunk_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                   const Tin *__restrict__ v, const float *__restrict__ alpha,
                   const float *__restrict__ beta, const float *__restrict__ S0,
-                  Tin *__restrict__ o, float *__restrict__ ST, int H, int T, int dv) {
+                  Tin *__restrict__ o, float *__restrict__ ST, int H, int T, int dv,
+                  const Fuse fz) {
     using L = SimtSmem<DK>;
     constexpr int KP = L::KP, UP = L::UP, PP = L::PP;
     extern __shared__ float sm[];
@@ -75,6 +82,9 @@ chunk_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     const int lane = tid & 31, warp = tid >> 5;
     const int c0 = blockIdx.x * DVS;
     const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
+    const unsigned fl = fz.flags;
+    const bool amap = (fl & (LR_FUSE_ALPHA_SIGMOID | LR_FUSE_ALPHA_SOFTPLUS)) != 0;
+    const float ac = (ALPHA && (fl & LR_FUSE_ALPHA_SOFTPLUS)) ? fz.ascale[blockIdx.y] : 0.f;
 
     for (int idx = tid; idx < DVS * DK; idx += NT) {
         const int c = idx / DK, j = idx % DK;
@@ -99,10 +109,35 @@ chunk_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         }
         if (tid < C) {
             const bool ok = tid < n;
-            Gs[tid] = (ALPHA && ok) ? logf(alpha[bh * T + t0 + tid]) : 0.f;
-            Bs[tid] = (DELTA && ok) ? beta[bh * T + t0 + tid] : 0.f;
+            float la = 0.f, b = 0.f;
+            if (ALPHA && ok) {
+                const float a = alpha[bh * T + t0 + tid];
+                la = amap ? log_gate(fl, a, ac) : logf(a);
+            }
+            if (DELTA && ok) b = write_strength(fl, beta[bh * T + t0 + tid]);
+            Gs[tid] = la;
+            Bs[tid] = b;
         }
         __syncthreads();
+
+        // ---- SiLU + L2 of the q and k rows (padded rows stay zero)
+        if (fl & LR_FUSE_QK_SILU_L2) {
+            for (int rr = warp; rr < 2 * C; rr += NT / 32) {
+                float *row = rr < C ? Qs + rr * KP : Ks + (rr - C) * KP;
+                float x[DK / 32];
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < DK / 32; ++e) {
+                    x[e] = silu_f(row[lane + 32 * e]);
+                    ss += x[e] * x[e];
+                }
+#pragma unroll
+                for (int d = 16; d >= 1; d >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, d);
+                const float inv = inv_l2(ss);
+#pragma unroll
+                for (int e = 0; e < DK / 32; ++e) row[lane + 32 * e] = x[e] * inv;
+            }
+        }
 
         // ---- cumulative log decay: inclusive scan of 64 values by warp 0
         if (ALPHA && warp == 0) {
@@ -209,7 +244,7 @@ chunk_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 template <int DK, typename Tin, bool ALPHA, bool DELTA>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *alpha,
                          const float *beta, const float *S0, void *o, float *S_T, int B, int H,
-                         int T, int dv, cudaStream_t stream, int slot) {
+                         int T, int dv, const Fuse &fz, cudaStream_t stream, int slot) {
     auto fn = chunk_simt_kernel<DK, Tin, ALPHA, DELTA>;
     const int bytes = SimtSmem<DK>::bytes;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(fn), bytes, slot);
@@ -217,44 +252,46 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
     dim3 grid(dv / DVS, H, B);
     fn<<<grid, NT, bytes, stream>>>(static_cast<const Tin *>(q), static_cast<const Tin *>(k),
                                     static_cast<const Tin *>(v), alpha, beta, S0,
-                                    static_cast<Tin *>(o), S_T, H, T, dv);
+                                    static_cast<Tin *>(o), S_T, H, T, dv, fz);
     return cudaGetLastError();
 }
 
 template <int DK, typename Tin>
 cudaError_t launch_mode(const void *q, const void *k, const void *v, const float *alpha,
                         const float *beta, const float *S0, void *o, float *S_T, int B, int H,
-                        int T, int dv, lr_mode mode, cudaStream_t stream, int slot) {
+                        int T, int dv, lr_mode mode, const Fuse &fz, cudaStream_t stream,
+                        int slot) {
     switch (mode) {
     case LR_MODE_LINEAR:
         return launch_typed<DK, Tin, false, false>(q, k, v, alpha, beta, S0, o, S_T, B, H, T,
-                                                   dv, stream, slot + 0);
+                                                   dv, fz, stream, slot + 0);
     case LR_MODE_DECAY:
         return launch_typed<DK, Tin, true, false>(q, k, v, alpha, beta, S0, o, S_T, B, H, T,
-                                                  dv, stream, slot + 1);
+                                                  dv, fz, stream, slot + 1);
     case LR_MODE_DELTA:
         return launch_typed<DK, Tin, false, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T,
-                                                  dv, stream, slot + 2);
+                                                  dv, fz, stream, slot + 2);
     default:
         return launch_typed<DK, Tin, true, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv,
-                                                 stream, slot + 3);
+                                                 fz, stream, slot + 3);
     }
 }
 
 template <typename Tin>
 cudaError_t launch_dk(const void *q, const void *k, const void *v, const float *alpha,
                       const float *beta, const float *S0, void *o, float *S_T, int B, int H,
-                      int T, int dk, int dv, lr_mode mode, cudaStream_t stream, int slot) {
+                      int T, int dk, int dv, lr_mode mode, const Fuse &fz, cudaStream_t stream,
+                      int slot) {
     switch (dk) {
     case 32:
-        return launch_mode<32, Tin>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, stream,
-                                    slot + 0);
+        return launch_mode<32, Tin>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, fz,
+                                    stream, slot + 0);
     case 64:
-        return launch_mode<64, Tin>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, stream,
-                                    slot + 4);
+        return launch_mode<64, Tin>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, fz,
+                                    stream, slot + 4);
     default:
         return launch_mode<128, Tin>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode,
-                                     stream, slot + 8);
+                                     fz, stream, slot + 8);
     }
 }
 
@@ -264,11 +301,11 @@ cudaError_t launch_dk(const void *q, const void *k, const void *v, const float *
 cudaError_t launch_chunked_simt(const void *q, const void *k, const void *v, const float *alpha,
                                 const float *beta, const float *S0, void *o, float *S_T, int B,
                                 int H, int T, int dk, int dv, lr_dtype dt, lr_mode mode,
-                                cudaStream_t stream) {
+                                const Fuse &fz, cudaStream_t stream) {
     if (dt == LR_DT_F32)
-        return launch_dk<float>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, mode, stream,
-                                0);
-    return launch_dk<__nv_bfloat16>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, mode,
+        return launch_dk<float>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, mode, fz,
+                                stream, 0);
+    return launch_dk<__nv_bfloat16>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, mode, fz,
                                     stream, 12);
 }
 

@@ -57,6 +57,14 @@
 //         ds  K'^T (kd' U')           -> Delta S'^T  (K read MN-major)
 // A final short block is zero-filled (alpha treated as 1, beta as 0), which
 // leaves the real tokens' results unchanged.
+//
+// The lr_fuse maps live in prep (page "Scrivere meglio nella memoria: gate e
+// delta rule"): the gates are mapped as they are read, and with SiLU + L2 of
+// q and k each thread normalises one row of the staged [Q; K] tile in place
+// (fp32 sum of squares, one rounding to bf16) before E1; the CTA writes its
+// normalised rows to the workspace by TMA stores, and the scan reads q and k
+// from there.  The previous block's k rows, staged again for E4, are
+// normalised again the same way, so they match the stored copy bit for bit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -275,15 +283,57 @@ __device__ __forceinline__ void ut_inverse(float *AT, float *Xt, int tid) {
     __syncthreads();
 }
 
+// SiLU, then L2 normalisation, of row `row` of a bf16 K-major 128-byte
+// swizzled tile of `rows` rows (sw128_offset layout), in place.  Two passes
+// over the row (sum of squares, then scale) so that nothing but 8 values is
+// held at a time; zero rows stay zero.
+template <int DK>
+__device__ __forceinline__ void silu_l2_row(uint8_t *tile, int row, int rows) {
+    constexpr int KB = (DK + 63) / 64, CH = DK < 64 ? DK / 8 : 8;  // 16-byte chunks per block
+    uint8_t *base = tile + row * 128;
+    float ss = 0.f;
+#pragma unroll 1
+    for (int kb = 0; kb < KB; ++kb) {
+#pragma unroll 2
+        for (int c = 0; c < CH; ++c) {
+            const uint4 raw = *reinterpret_cast<const uint4 *>(base + kb * rows * 128 +
+                                                               ((c ^ (row & 7)) << 4));
+            const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float x = silu_f(__bfloat162float(e[i]));
+                ss += x * x;
+            }
+        }
+    }
+    const float inv = inv_l2(ss);
+#pragma unroll 1
+    for (int kb = 0; kb < KB; ++kb) {
+#pragma unroll 2
+        for (int c = 0; c < CH; ++c) {
+            uint4 *p = reinterpret_cast<uint4 *>(base + kb * rows * 128 + ((c ^ (row & 7)) << 4));
+            const uint4 raw = *p;
+            const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
+            float x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = silu_f(__bfloat162float(e[i])) * inv;
+            *p = pack8(x);
+        }
+    }
+}
+
 // Prep of block j = blockIdx.x.  Writes to record j: W_j, T_j diag(beta),
 // -Z_{j-1} and the gate vectors; to record j+1: P_j (and, for the last block,
-// record j+1's gate vectors).
+// record j+1's gate vectors).  With SiLU + L2 of q and k, also the block's
+// normalised q and k rows, through the maps tmqn and tmkn.
 template <int DK, bool ALPHA, bool DELTA>
 __global__ void __launch_bounds__(NT)
 chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                   const float *__restrict__ alpha, const float *__restrict__ beta,
                   uint8_t *__restrict__ ws, int H, int T, int nblk,
-                  const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk) {
+                  const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                  const Fuse fz, const __grid_constant__ CUtensorMap tmqn,
+                  const __grid_constant__ CUtensorMap tmkn) {
     using L = PrepLayout<DK>;
     using R = Rec<DK>;
     extern __shared__ uint8_t sm_raw[];
@@ -310,11 +360,13 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     // gate inputs first, so their global-load latency overlaps the staging:
     // threads 0-63 this block's tokens, 64-127 the previous block's
     const int tok = tid & 63;
+    const unsigned fl = fz.flags;
+    const bool qk = (fl & LR_FUSE_QK_SILU_L2) != 0;
     float araw = 1.f, b = 0.f;
     if (tid < C) {
         if (tok < n) {
             if (ALPHA) araw = alpha[bh * T + t0 + tok];
-            if (DELTA) b = beta[bh * T + t0 + tok];
+            if (DELTA) b = write_strength(fl, beta[bh * T + t0 + tok]);
         }
     } else if (ALPHA && blk > 0) {
         araw = alpha[bh * T + t0 - C + tok];
@@ -336,7 +388,10 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     }
     // ---- gates: warps 0-1 hold this block's tokens, warps 2-3 the previous
     //      block's (all ones for block 0)
-    const float la = ALPHA ? __logf(araw) : 0.f;
+    const bool has_a = ALPHA && (tid < C ? tok < n : blk > 0);
+    const float la = has_a ? log_gate(fl, araw,
+                                      (fl & LR_FUSE_ALPHA_SOFTPLUS) ? fz.ascale[blockIdx.y] : 0.f)
+                           : 0.f;
     if (warp == 0) {
         tmem_alloc(tmem_slot, 128);
         tmem_relinquish();
@@ -379,6 +434,10 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         }
     }
     bool ok = mbar_wait(&bar[1], 0);
+    if (qk && ok) {  // thread t: row t of [Q; K]
+        silu_l2_row<DK>(QK, tid, 128);
+        fence_async_smem();
+    }
     tc_fence_before();
     ok = __syncthreads_and(ok ? 1 : 0) != 0;
     tc_fence_after();
@@ -393,6 +452,14 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
             mma_bf16(tmem, tile_desc(smem_u32(QK), 128, 0, ks), tile_desc(smem_u32(QK), 128, 64, ks),
                      id, ks > 0);
         mma_commit(&bar[0]);
+        if (qk) {  // the normalised rows -> workspace (rows past T are not written)
+#pragma unroll
+            for (int kb = 0; kb < L::KB; ++kb) {
+                tma_store_3d(&tmqn, QK + kb * 16384, kb * 64, t0, (int)bh);
+                tma_store_3d(&tmkn, QK + kb * 16384 + 8192, kb * 64, t0, (int)bh);
+            }
+            bulk_commit();
+        }
     }
     ok = __syncthreads_and((ok && mbar_wait(&bar[0], 0)) ? 1 : 0) != 0;
     tc_fence_after();
@@ -438,6 +505,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
             }
         }
     }
+    if (qk && tid == 0) bulk_wait_read();  // the stores have read the [Q; K] tile (reused below)
     tc_fence_before();  // the score columns are reused by W below
     __syncthreads();
 
@@ -522,6 +590,10 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         //      cols [0, 64); record rows 64..127 of the TZP tile get -Z' diag(kd')
         if (zprev) {
             ok = mbar_wait(&bar[2], 0) && ok;
+            if (qk && ok && tid < C) {
+                silu_l2_row<DK>(QK, C + tid, 128);
+                fence_async_smem();
+            }
             ok = __syncthreads_and(ok ? 1 : 0) != 0;
             if (tid == 0 && ok) {
                 const uint32_t id = idesc_bf16_f32(64, 64);
@@ -1076,10 +1148,19 @@ cudaError_t make_rows_map(CUtensorMap *m, const void *base, int d, int T, int BH
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// One record per stage: a head of nblk blocks has nblk + 1 stages.  With
+// SiLU + L2 of q and k, the normalised q and k ([B, H, T, dk] bf16 each)
+// follow the records.
+size_t records_bytes(int B, int H, int T, int dk) {
+    const size_t nblk = (size_t)((T + C - 1) / C);
+    const size_t rec = dk == 32 ? Rec<32>::BYTES : dk == 64 ? Rec<64>::BYTES : Rec<128>::BYTES;
+    return (size_t)B * H * (nblk + 1) * rec;
+}
+
 template <int DK, bool ALPHA, bool DELTA>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *alpha,
                          const float *beta, const float *S0, void *o, float *S_T, int B, int H,
-                         int T, int dv, void *ws, cudaStream_t stream, int slot) {
+                         int T, int dv, const Fuse &fz, void *ws, cudaStream_t stream, int slot) {
     const int nblk = (T + C - 1) / C;
     auto prep = chunk_prep_kernel<DK, ALPHA, DELTA>;
     auto scan = chunk_scan_kernel<DK, ALPHA, DELTA>;
@@ -1097,60 +1178,74 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
     if (e != cudaSuccess) return e;
     e = make_rows_map(&tmv, v, dv, T, B * H);
     if (e != cudaSuccess) return e;
+    // normalised q and k in the workspace (the scan reads them instead)
+    const bool qk = (fz.flags & LR_FUSE_QK_SILU_L2) != 0;
+    const bf16 *qs = static_cast<const bf16 *>(q), *ks = static_cast<const bf16 *>(k);
+    CUtensorMap tmqn = tmq, tmkn = tmk;
+    if (qk) {
+        bf16 *qn = reinterpret_cast<bf16 *>(static_cast<uint8_t *>(ws) + records_bytes(B, H, T, DK));
+        bf16 *kn = qn + (size_t)B * H * T * DK;
+        e = make_rows_map(&tmqn, qn, DK, T, B * H);
+        if (e != cudaSuccess) return e;
+        e = make_rows_map(&tmkn, kn, DK, T, B * H);
+        if (e != cudaSuccess) return e;
+        qs = qn;
+        ks = kn;
+    }
     prep<<<dim3(nblk, H, B), NT, PrepLayout<DK>::ALLOC, stream>>>(
         static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), ALPHA ? alpha : nullptr,
-        DELTA ? beta : nullptr, static_cast<uint8_t *>(ws), H, T, nblk, tmq, tmk);
+        DELTA ? beta : nullptr, static_cast<uint8_t *>(ws), H, T, nblk, tmq, tmk, fz, tmqn, tmkn);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     scan<<<dim3(dv / DVS, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
-        static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk,
-        static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), static_cast<const bf16 *>(v),
-        tmq, tmk, tmv);
+        static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qs, ks,
+        static_cast<const bf16 *>(v), qk ? tmqn : tmq, qk ? tmkn : tmk, tmv);
     return cudaGetLastError();
 }
 
 template <int DK>
 cudaError_t launch_mode(const void *q, const void *k, const void *v, const float *alpha,
                         const float *beta, const float *S0, void *o, float *S_T, int B, int H,
-                        int T, int dv, lr_mode mode, void *ws, cudaStream_t stream, int slot) {
+                        int T, int dv, lr_mode mode, const Fuse &fz, void *ws,
+                        cudaStream_t stream, int slot) {
     switch (mode) {
     case LR_MODE_LINEAR:
-        return launch_typed<DK, false, false>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, ws,
-                                              stream, slot + 0);
+        return launch_typed<DK, false, false>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, fz,
+                                              ws, stream, slot + 0);
     case LR_MODE_DECAY:
-        return launch_typed<DK, true, false>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, ws,
-                                             stream, slot + 1);
+        return launch_typed<DK, true, false>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, fz,
+                                             ws, stream, slot + 1);
     case LR_MODE_DELTA:
-        return launch_typed<DK, false, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, ws,
-                                             stream, slot + 2);
+        return launch_typed<DK, false, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, fz,
+                                             ws, stream, slot + 2);
     default:
-        return launch_typed<DK, true, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, ws,
-                                            stream, slot + 3);
+        return launch_typed<DK, true, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, fz,
+                                            ws, stream, slot + 3);
     }
 }
 
 }  // namespace
 
-// One record per stage: a head of nblk blocks has nblk + 1 stages.
-size_t chunked_tc_workspace_bytes(int B, int H, int T, int dk) {
-    const size_t nblk = (size_t)((T + C - 1) / C);
-    const size_t rec = dk == 32 ? Rec<32>::BYTES : dk == 64 ? Rec<64>::BYTES : Rec<128>::BYTES;
-    return (size_t)B * H * (nblk + 1) * rec;
+size_t chunked_tc_workspace_bytes(int B, int H, int T, int dk, unsigned flags) {
+    const size_t qk = (flags & LR_FUSE_QK_SILU_L2) ? 2 * (size_t)B * H * T * dk * 2 : 0;
+    return records_bytes(B, H, T, dk) + qk;
 }
 
 // Attribute slots 32..55 belong to this file.
 cudaError_t launch_chunked_tc(const void *q, const void *k, const void *v, const float *alpha,
                               const float *beta, const float *S0, void *o, float *S_T, int B,
-                              int H, int T, int dk, int dv, lr_mode mode, void *ws,
-                              cudaStream_t stream) {
+                              int H, int T, int dk, int dv, lr_mode mode, const Fuse &fz,
+                              void *ws, cudaStream_t stream) {
     switch (dk) {
     case 32:
-        return launch_mode<32>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, ws, stream, 32);
+        return launch_mode<32>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, fz, ws, stream,
+                               32);
     case 64:
-        return launch_mode<64>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, ws, stream, 36);
+        return launch_mode<64>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, fz, ws, stream,
+                               36);
     default:
-        return launch_mode<128>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, ws, stream,
-                                40);
+        return launch_mode<128>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, fz, ws,
+                                stream, 40);
     }
 }
 

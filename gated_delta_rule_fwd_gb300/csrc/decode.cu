@@ -15,6 +15,12 @@
 // warp covers 4 rows per pass, the CTA 16 rows.  Each thread keeps UNROLL
 // rows of loads in flight.  Row dot products reduce over the 8 lanes with
 // three xor shuffles.
+//
+// With the lr_fuse maps (page "Scrivere meglio nella memoria: gate e delta
+// rule"): q and k are SiLU'd and L2-normalised in registers (the 8 lanes of a
+// row hold a whole vector, so the norm is one more 8-lane sum), the gates are
+// mapped on load, and with the output RMSNorm the d_v outputs of the head are
+// kept in shared memory, normalised together and stored once.
 #include "lr_internal.cuh"
 
 namespace lr {
@@ -38,11 +44,23 @@ __device__ __forceinline__ float sum8(float x) {
     return x;
 }
 
+__device__ __forceinline__ float4 silu4(float4 x) {
+    return make_float4(silu_f(x.x), silu_f(x.y), silu_f(x.z), silu_f(x.w));
+}
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+    return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+}
+__device__ __forceinline__ float4 scale4(float4 a, float s) {
+    return make_float4(a.x * s, a.y * s, a.z * s, a.w * s);
+}
+
 template <int DK, typename Tin, bool ALPHA, bool DELTA, int UNROLL>
 __global__ void __launch_bounds__(kStepThreads)
 step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
             const float *__restrict__ alpha, const float *__restrict__ beta,
-            float *__restrict__ S, Tin *__restrict__ o, int dv) {
+            float *__restrict__ S, Tin *__restrict__ o, int H, int dv, const Fuse fz) {
+    __shared__ float o_sh[128];  // the head's outputs, with the output RMSNorm
+    __shared__ float inv_sh;
     constexpr int NV = DK / (4 * kLanesPerRow);  // float4 per lane per row
     static_assert(NV >= 1 && NV * 4 * kLanesPerRow == DK, "DK must be 32, 64 or 128");
 
@@ -58,18 +76,39 @@ step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__r
     float *Sh = S + (size_t)head * dv * DK;
     Tin *oh = o + (size_t)head * dv;
 
+    const unsigned fl = fz.flags;
     float4 kr[NV], qr[NV];
-    float kq = 0.f;
 #pragma unroll
     for (int m = 0; m < NV; ++m) {
         const int col = 4 * (kLanesPerRow * m + sub);
         kr[m] = load4(kh + col);
         qr[m] = load4(qh + col);
-        kq += kr[m].x * qr[m].x + kr[m].y * qr[m].y + kr[m].z * qr[m].z + kr[m].w * qr[m].w;
     }
+    if (fl & LR_FUSE_QK_SILU_L2) {
+        float kk = 0.f, qq = 0.f;
+#pragma unroll
+        for (int m = 0; m < NV; ++m) {
+            kr[m] = silu4(kr[m]);
+            qr[m] = silu4(qr[m]);
+            kk += dot4(kr[m], kr[m]);
+            qq += dot4(qr[m], qr[m]);
+        }
+        const float ik = inv_l2(sum8(kk)), iq = inv_l2(sum8(qq));
+#pragma unroll
+        for (int m = 0; m < NV; ++m) {
+            kr[m] = scale4(kr[m], ik);
+            qr[m] = scale4(qr[m], iq);
+        }
+    }
+    float kq = 0.f;
+#pragma unroll
+    for (int m = 0; m < NV; ++m) kq += dot4(kr[m], qr[m]);
     kq = sum8(kq);
-    const float a = ALPHA ? alpha[head] : 1.f;
-    const float b = DELTA ? beta[head] : 1.f;
+    const float a = ALPHA ? gate(fl, alpha[head],
+                                 (fl & LR_FUSE_ALPHA_SOFTPLUS) ? fz.ascale[head % H] : 0.f)
+                          : 1.f;
+    const float b = DELTA ? write_strength(fl, beta[head]) : 1.f;
+    const bool norm = (fl & LR_FUSE_O_RMSNORM) != 0;
 
     const int passes = dv / kRowsPerPass;
     for (int p0 = 0; p0 < passes; p0 += UNROLL) {
@@ -105,46 +144,63 @@ step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__r
                 t.w = a * s[u][m].w + ur * kr[m].w;
                 st_stream(Sh + (size_t)r * DK + 4 * (kLanesPerRow * m + sub), t);
             }
-            if (sub == 0) oh[r] = from_f<Tin>(a * sq + ur * kq);
+            if (sub == 0) {
+                const float orow = a * sq + ur * kq;
+                if (norm) o_sh[r] = orow;
+                else oh[r] = from_f<Tin>(orow);
+            }
         }
+    }
+    if (norm) {
+        __syncthreads();
+        if (warp == 0) {
+            float ss = 0.f;
+            for (int r = lane; r < dv; r += 32) ss += o_sh[r] * o_sh[r];
+#pragma unroll
+            for (int d = 16; d >= 1; d >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, d);
+            if (lane == 0) inv_sh = rsqrtf(ss / (float)dv + fz.norm_eps);
+        }
+        __syncthreads();
+        const int r = threadIdx.x;
+        if (r < dv) oh[r] = from_f<Tin>(o_sh[r] * inv_sh * (fz.norm_w ? fz.norm_w[r] : 1.f));
     }
 }
 
 template <int DK, typename Tin, bool ALPHA, bool DELTA>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *alpha,
-                         const float *beta, float *S, void *o, int NH, int dv,
-                         cudaStream_t stream) {
+                         const float *beta, float *S, void *o, int NH, int H, int dv,
+                         const Fuse &fz, cudaStream_t stream) {
     // dv in {32, 64, 128}: 2, 4 or 8 passes of 16 rows; UNROLL 2 divides all.
     step_kernel<DK, Tin, ALPHA, DELTA, 2><<<NH, kStepThreads, 0, stream>>>(
         static_cast<const Tin *>(q), static_cast<const Tin *>(k), static_cast<const Tin *>(v),
-        alpha, beta, S, static_cast<Tin *>(o), dv);
+        alpha, beta, S, static_cast<Tin *>(o), H, dv, fz);
     return cudaGetLastError();
 }
 
 template <int DK, typename Tin>
 cudaError_t launch_mode(const void *q, const void *k, const void *v, const float *alpha,
-                        const float *beta, float *S, void *o, int NH, int dv, lr_mode mode,
-                        cudaStream_t stream) {
+                        const float *beta, float *S, void *o, int NH, int H, int dv,
+                        lr_mode mode, const Fuse &fz, cudaStream_t stream) {
     switch (mode) {
     case LR_MODE_LINEAR:
-        return launch_typed<DK, Tin, false, false>(q, k, v, alpha, beta, S, o, NH, dv, stream);
+        return launch_typed<DK, Tin, false, false>(q, k, v, alpha, beta, S, o, NH, H, dv, fz, stream);
     case LR_MODE_DECAY:
-        return launch_typed<DK, Tin, true, false>(q, k, v, alpha, beta, S, o, NH, dv, stream);
+        return launch_typed<DK, Tin, true, false>(q, k, v, alpha, beta, S, o, NH, H, dv, fz, stream);
     case LR_MODE_DELTA:
-        return launch_typed<DK, Tin, false, true>(q, k, v, alpha, beta, S, o, NH, dv, stream);
+        return launch_typed<DK, Tin, false, true>(q, k, v, alpha, beta, S, o, NH, H, dv, fz, stream);
     default:
-        return launch_typed<DK, Tin, true, true>(q, k, v, alpha, beta, S, o, NH, dv, stream);
+        return launch_typed<DK, Tin, true, true>(q, k, v, alpha, beta, S, o, NH, H, dv, fz, stream);
     }
 }
 
 template <typename Tin>
 cudaError_t launch_dk(const void *q, const void *k, const void *v, const float *alpha,
-                      const float *beta, float *S, void *o, int NH, int dk, int dv,
-                      lr_mode mode, cudaStream_t stream) {
+                      const float *beta, float *S, void *o, int NH, int H, int dk, int dv,
+                      lr_mode mode, const Fuse &fz, cudaStream_t stream) {
     switch (dk) {
-    case 32: return launch_mode<32, Tin>(q, k, v, alpha, beta, S, o, NH, dv, mode, stream);
-    case 64: return launch_mode<64, Tin>(q, k, v, alpha, beta, S, o, NH, dv, mode, stream);
-    default: return launch_mode<128, Tin>(q, k, v, alpha, beta, S, o, NH, dv, mode, stream);
+    case 32: return launch_mode<32, Tin>(q, k, v, alpha, beta, S, o, NH, H, dv, mode, fz, stream);
+    case 64: return launch_mode<64, Tin>(q, k, v, alpha, beta, S, o, NH, H, dv, mode, fz, stream);
+    default: return launch_mode<128, Tin>(q, k, v, alpha, beta, S, o, NH, H, dv, mode, fz, stream);
     }
 }
 
@@ -152,11 +208,11 @@ cudaError_t launch_dk(const void *q, const void *k, const void *v, const float *
 
 cudaError_t launch_step(const void *q, const void *k, const void *v, const float *alpha,
                         const float *beta, float *S, void *o, int N, int H, int dk, int dv,
-                        lr_dtype dt, lr_mode mode, cudaStream_t stream) {
+                        lr_dtype dt, lr_mode mode, const Fuse &fz, cudaStream_t stream) {
     const int NH = N * H;
     if (dt == LR_DT_F32)
-        return launch_dk<float>(q, k, v, alpha, beta, S, o, NH, dk, dv, mode, stream);
-    return launch_dk<__nv_bfloat16>(q, k, v, alpha, beta, S, o, NH, dk, dv, mode, stream);
+        return launch_dk<float>(q, k, v, alpha, beta, S, o, NH, H, dk, dv, mode, fz, stream);
+    return launch_dk<__nv_bfloat16>(q, k, v, alpha, beta, S, o, NH, H, dk, dv, mode, fz, stream);
 }
 
 }  // namespace lr

@@ -33,6 +33,28 @@ bool overlap(Span a, Span b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi 
 bool uses_alpha(lr_mode m) { return m == LR_MODE_DECAY || m == LR_MODE_GATED_DELTA; }
 bool uses_beta(lr_mode m) { return m == LR_MODE_DELTA || m == LR_MODE_GATED_DELTA; }
 
+constexpr unsigned kFuseAll = LR_FUSE_QK_SILU_L2 | LR_FUSE_BETA_SIGMOID | LR_FUSE_ALPHA_SIGMOID |
+                              LR_FUSE_ALPHA_SOFTPLUS | LR_FUSE_O_RMSNORM;
+
+// The kernels' view of lr_fuse: flags validated, the gate maps dropped where
+// the mode has no such gate.
+lr_status to_fuse(const lr_fuse *f, lr_mode mode, Fuse *out) {
+    *out = Fuse{};
+    if (!f) return LR_OK;
+    unsigned fl = f->flags;
+    if (fl & ~kFuseAll) return LR_ERR_FUSE;
+    if ((fl & LR_FUSE_ALPHA_SIGMOID) && (fl & LR_FUSE_ALPHA_SOFTPLUS)) return LR_ERR_FUSE;
+    if ((fl & LR_FUSE_O_RMSNORM) && !(f->norm_eps >= 0.f && f->norm_eps <= 3.4e38f))
+        return LR_ERR_FUSE;
+    if (!uses_alpha(mode)) fl &= ~(LR_FUSE_ALPHA_SIGMOID | LR_FUSE_ALPHA_SOFTPLUS);
+    if (!uses_beta(mode)) fl &= ~LR_FUSE_BETA_SIGMOID;
+    out->flags = fl;
+    out->ascale = (fl & LR_FUSE_ALPHA_SOFTPLUS) ? f->alpha_scale : nullptr;
+    out->norm_w = (fl & LR_FUSE_O_RMSNORM) ? f->norm_weight : nullptr;
+    out->norm_eps = f->norm_eps;
+    return LR_OK;
+}
+
 // Element counts fit comfortably in 64 bits and in what one device can hold.
 bool count_ok(long long a, long long b, long long c, long long d) {
     const long long lim = 1ll << 40;
@@ -72,7 +94,7 @@ using namespace lr;
 
 extern "C" {
 
-int lr_abi_version(void) { return 1; }
+int lr_abi_version(void) { return 2; }
 
 const char *lr_status_string(lr_status s) {
     switch (s) {
@@ -88,6 +110,7 @@ const char *lr_status_string(lr_status s) {
     case LR_ERR_TIMEOUT: return "a kernel gave up a bounded wait; its outputs are incomplete";
     case LR_ERR_WORKSPACE: return "workspace is NULL or smaller than lr_fwd_chunked_workspace_size";
     case LR_ERR_TOO_LARGE: return "problem needs more scratch than the static workspace holds (LR_STATIC_WORKSPACE_BYTES)";
+    case LR_ERR_FUSE: return "invalid lr_fuse: unknown flag, both alpha maps, or a negative or non-finite norm_eps";
     }
     return "unknown status";
 }
@@ -102,28 +125,41 @@ static lr_status check_chunked_shape(int B, int H, int T, int dk, int dv, int ch
     return LR_OK;
 }
 
-size_t lr_fwd_chunked_workspace_size(int B, int H, int T, int dk, int dv, int chunk, lr_dtype dt,
-                                     lr_mode mode) {
+size_t lr_fwd_chunked_fused_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
+                                           lr_dtype dt, lr_mode mode, unsigned flags) {
     if (check_chunked_shape(B, H, T, dk, dv, chunk, dt, mode) != LR_OK) return 0;
+    if ((flags & ~kFuseAll) || ((flags & LR_FUSE_ALPHA_SIGMOID) && (flags & LR_FUSE_ALPHA_SOFTPLUS)))
+        return 0;
     if (dt != LR_DT_BF16 || T == 0) return 0;
-    return chunked_tc_workspace_bytes(B, H, T, dk);
+    return chunked_tc_workspace_bytes(B, H, T, dk, flags);
 }
 
-lr_status lr_fwd_chunked(const void *q, const void *k, const void *v, const float *alpha,
-                         const float *beta, const float *S0, void *o, float *S_T, int B, int H,
-                         int T, int dk, int dv, int chunk, lr_dtype dt, lr_mode mode,
-                         void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+size_t lr_fwd_chunked_workspace_size(int B, int H, int T, int dk, int dv, int chunk, lr_dtype dt,
+                                     lr_mode mode) {
+    return lr_fwd_chunked_fused_workspace_size(B, H, T, dk, dv, chunk, dt, mode, 0u);
+}
+
+lr_status lr_fwd_chunked_fused(const void *q, const void *k, const void *v, const float *alpha,
+                               const float *beta, const float *S0, void *o, float *S_T, int B,
+                               int H, int T, int dk, int dv, int chunk, lr_dtype dt, lr_mode mode,
+                               const lr_fuse *fuse, void *workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
     const lr_status shape = check_chunked_shape(B, H, T, dk, dv, chunk, dt, mode);
     if (shape != LR_OK) return shape;
+    Fuse fz;
+    const lr_status fs = to_fuse(fuse, mode, &fz);
+    if (fs != LR_OK) return fs;
     if (!S_T) return LR_ERR_NULL;
     if (T > 0 && (!q || !k || !v || !o)) return LR_ERR_NULL;
     if (T > 0 && uses_alpha(mode) && !alpha) return LR_ERR_NULL;
     if (T > 0 && uses_beta(mode) && !beta) return LR_ERR_NULL;
-    const size_t need = lr_fwd_chunked_workspace_size(B, H, T, dk, dv, chunk, dt, mode);
+    if (T > 0 && (fz.flags & LR_FUSE_ALPHA_SOFTPLUS) && !fz.ascale) return LR_ERR_NULL;
+    const size_t need =
+        lr_fwd_chunked_fused_workspace_size(B, H, T, dk, dv, chunk, dt, mode, fz.flags);
     if (need > 0 && (!workspace || workspace_bytes < need)) return LR_ERR_WORKSPACE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) ||
         !aligned16(beta) || !aligned16(S0) || !aligned16(o) || !aligned16(S_T) ||
-        (need > 0 && !aligned16(workspace)))
+        (need > 0 && !aligned16(workspace)) || !aligned16(fz.ascale) || !aligned16(fz.norm_w))
         return LR_ERR_ALIGN;
 
     const size_t es = dt == LR_DT_F32 ? 4 : 2;
@@ -143,6 +179,9 @@ lr_status lr_fwd_chunked(const void *q, const void *k, const void *v, const floa
     const Span sw = span(need > 0 ? workspace : nullptr, need);
     for (Span other : {sq, sk, sv, sa, sb, s0, so, st})
         if (overlap(sw, other)) return LR_ERR_ALIAS;
+    const Span sc = span(fz.ascale, (size_t)H * 4), sn = span(fz.norm_w, (size_t)dv * 4);
+    for (Span out : {so, st, sw})
+        if (overlap(out, sc) || overlap(out, sn)) return LR_ERR_ALIAS;
 
     cudaError_t e;
     if (T == 0) {
@@ -153,12 +192,22 @@ lr_status lr_fwd_chunked(const void *q, const void *k, const void *v, const floa
         e = cudaGetLastError();
     } else {
         e = dt == LR_DT_BF16
-                ? launch_chunked_tc(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, mode,
+                ? launch_chunked_tc(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, mode, fz,
                                     workspace, stream)
                 : launch_chunked_simt(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, dt, mode,
-                                      stream);
+                                      fz, stream);
+        if (e == cudaSuccess && (fz.flags & LR_FUSE_O_RMSNORM))
+            e = launch_rmsnorm(o, fz.norm_w, fz.norm_eps, (size_t)B * H * T, dv, dt, stream);
     }
     return e == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+}
+
+lr_status lr_fwd_chunked(const void *q, const void *k, const void *v, const float *alpha,
+                         const float *beta, const float *S0, void *o, float *S_T, int B, int H,
+                         int T, int dk, int dv, int chunk, lr_dtype dt, lr_mode mode,
+                         void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return lr_fwd_chunked_fused(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, chunk, dt, mode,
+                                nullptr, workspace, workspace_bytes, stream);
 }
 
 lr_status lr_device_status(void) {
@@ -168,19 +217,24 @@ lr_status lr_device_status(void) {
     return e ? LR_ERR_TIMEOUT : LR_OK;
 }
 
-lr_status lr_step(const void *q, const void *k, const void *v, const float *alpha,
-                  const float *beta, float *S, void *o, int N, int H, int dk, int dv,
-                  lr_dtype dt, lr_mode mode, cudaStream_t stream) {
+lr_status lr_step_fused(const void *q, const void *k, const void *v, const float *alpha,
+                        const float *beta, float *S, void *o, int N, int H, int dk, int dv,
+                        lr_dtype dt, lr_mode mode, const lr_fuse *fuse, cudaStream_t stream) {
     if (mode < LR_MODE_LINEAR || mode > LR_MODE_GATED_DELTA) return LR_ERR_MODE;
     if (dt != LR_DT_F32 && dt != LR_DT_BF16) return LR_ERR_DTYPE;
     if (N < 1 || H < 1 || dk < 1 || dv < 1) return LR_ERR_SHAPE;
     if (!count_ok(N, H, dv, dk) || (long long)N * H > 0x7fffffffll) return LR_ERR_SHAPE;
     if (!supported_dim(dk) || !supported_dim(dv)) return LR_ERR_UNSUPPORTED;
+    Fuse fz;
+    const lr_status fs = to_fuse(fuse, mode, &fz);
+    if (fs != LR_OK) return fs;
     if (!q || !k || !v || !S || !o) return LR_ERR_NULL;
     if (uses_alpha(mode) && !alpha) return LR_ERR_NULL;
     if (uses_beta(mode) && !beta) return LR_ERR_NULL;
+    if ((fz.flags & LR_FUSE_ALPHA_SOFTPLUS) && !fz.ascale) return LR_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) ||
-        !aligned16(beta) || !aligned16(S) || !aligned16(o))
+        !aligned16(beta) || !aligned16(S) || !aligned16(o) || !aligned16(fz.ascale) ||
+        !aligned16(fz.norm_w))
         return LR_ERR_ALIGN;
 
     const size_t es = dt == LR_DT_F32 ? 4 : 2;
@@ -193,9 +247,19 @@ lr_status lr_step(const void *q, const void *k, const void *v, const float *alph
         if (overlap(so, in)) return LR_ERR_ALIAS;
     for (Span in : {sq, sk, sv, sa, sb})
         if (overlap(ss, in)) return LR_ERR_ALIAS;
+    const Span sc = span(fz.ascale, (size_t)H * 4), sn = span(fz.norm_w, (size_t)dv * 4);
+    for (Span out : {so, ss})
+        if (overlap(out, sc) || overlap(out, sn)) return LR_ERR_ALIAS;
 
-    const cudaError_t e = launch_step(q, k, v, alpha, beta, S, o, N, H, dk, dv, dt, mode, stream);
+    const cudaError_t e =
+        launch_step(q, k, v, alpha, beta, S, o, N, H, dk, dv, dt, mode, fz, stream);
     return e == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+}
+
+lr_status lr_step(const void *q, const void *k, const void *v, const float *alpha,
+                  const float *beta, float *S, void *o, int N, int H, int dk, int dv,
+                  lr_dtype dt, lr_mode mode, cudaStream_t stream) {
+    return lr_step_fused(q, k, v, alpha, beta, S, o, N, H, dk, dv, dt, mode, nullptr, stream);
 }
 
 }  // extern "C"

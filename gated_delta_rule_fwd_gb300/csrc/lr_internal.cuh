@@ -48,6 +48,42 @@ __host__ __device__ constexpr ModeBits mode_bits(int mode) {
                     mode == LR_MODE_DELTA || mode == LR_MODE_GATED_DELTA};
 }
 
+// ------------------------------------------------- maps around the recurrence
+// The lr_fuse options as the kernels receive them (validated on the host).
+struct Fuse {
+    unsigned flags = 0;
+    const float *ascale = nullptr;  // [H], c_h of the softplus gate
+    const float *norm_w = nullptr;  // [dv] or NULL for ones
+    float norm_eps = 0.f;
+};
+
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + __expf(-x)); }
+// ln(1 + e^x) without overflow
+__device__ __forceinline__ float softplus_f(float x) {
+    return fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x)));
+}
+// x sigmoid(x)
+__device__ __forceinline__ float silu_f(float x) { return x / (1.f + __expf(-x)); }
+// 1 / max(sqrt(ss), 1e-12): the scale that L2-normalises a vector with sum of squares ss
+__device__ __forceinline__ float inv_l2(float ss) { return rsqrtf(fmaxf(ss, 1e-24f)); }
+
+// ln alpha from the value read from memory: ln a without a gate map,
+// ln sigmoid(a) = -softplus(-a), or -c softplus(a).
+__device__ __forceinline__ float log_gate(unsigned fl, float a, float c) {
+    if (fl & LR_FUSE_ALPHA_SIGMOID) return -softplus_f(-a);
+    if (fl & LR_FUSE_ALPHA_SOFTPLUS) return -c * softplus_f(a);
+    return __logf(a);
+}
+// alpha itself (decode)
+__device__ __forceinline__ float gate(unsigned fl, float a, float c) {
+    if (fl & LR_FUSE_ALPHA_SIGMOID) return sigmoid_f(a);
+    if (fl & LR_FUSE_ALPHA_SOFTPLUS) return __expf(-c * softplus_f(a));
+    return a;
+}
+__device__ __forceinline__ float write_strength(unsigned fl, float b) {
+    return (fl & LR_FUSE_BETA_SIGMOID) ? sigmoid_f(b) : b;
+}
+
 // ------------------------------------------------------------------ launchers
 // Every launcher assumes arguments already validated by lr_api.cu and returns
 // the cudaError_t of the launch.
@@ -55,21 +91,26 @@ __host__ __device__ constexpr ModeBits mode_bits(int mode) {
 // Decode step (decode.cu).
 cudaError_t launch_step(const void *q, const void *k, const void *v, const float *alpha,
                         const float *beta, float *S, void *o, int N, int H, int dk, int dv,
-                        lr_dtype dt, lr_mode mode, cudaStream_t stream);
+                        lr_dtype dt, lr_mode mode, const Fuse &fz, cudaStream_t stream);
 
 // Chunked forward on CUDA cores in fp32 (chunked_simt.cu).
 cudaError_t launch_chunked_simt(const void *q, const void *k, const void *v, const float *alpha,
                                 const float *beta, const float *S0, void *o, float *S_T, int B,
                                 int H, int T, int dk, int dv, lr_dtype dt, lr_mode mode,
-                                cudaStream_t stream);
+                                const Fuse &fz, cudaStream_t stream);
 
 // Chunked forward on the tensor cores, bf16 (chunked_tc.cu).
 cudaError_t launch_chunked_tc(const void *q, const void *k, const void *v, const float *alpha,
                               const float *beta, const float *S0, void *o, float *S_T, int B,
-                              int H, int T, int dk, int dv, lr_mode mode, void *ws,
-                              cudaStream_t stream);
-// Workspace bytes the tensor-core path needs.
-size_t chunked_tc_workspace_bytes(int B, int H, int T, int dk);
+                              int H, int T, int dk, int dv, lr_mode mode, const Fuse &fz,
+                              void *ws, cudaStream_t stream);
+// Workspace bytes the tensor-core path needs (with the normalised q and k
+// when the flags ask for them).
+size_t chunked_tc_workspace_bytes(int B, int H, int T, int dk, unsigned flags);
+
+// In-place RMSNorm of `rows` rows of dv channels (norm.cu).
+cudaError_t launch_rmsnorm(void *o, const float *w, float eps, size_t rows, int dv, lr_dtype dt,
+                           cudaStream_t stream);
 
 // Returns and clears the tensor-core kernel's bounded-wait error word
 // (1 if set, 0 if clear, -1 if the device could not be read).

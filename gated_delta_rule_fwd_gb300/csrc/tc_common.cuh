@@ -242,6 +242,18 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *map, int x, i
         "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
+// Tiled TMA store of a 3-D box from shared memory (box elements outside the
+// tensor are not written), tracked by the issuing thread's bulk-async group.
+__device__ __forceinline__ void tma_store_3d(const void *map, const void *src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::
+                     "l"(map), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+// Wait until every committed bulk store of this thread has finished reading
+// shared memory (the writes to global memory may still be in flight).
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 // Hint: bring [p, p + bytes) into L2 (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");

@@ -56,8 +56,10 @@ typedef enum {
     LR_ERR_ALIAS = 8,       /* an output overlaps an input it must not overlap     */
     LR_ERR_TIMEOUT = 9,     /* a kernel gave up a bounded wait (see lr_device_status) */
     LR_ERR_WORKSPACE = 10,  /* workspace NULL or smaller than lr_fwd_chunked_workspace_size */
-    LR_ERR_TOO_LARGE = 11   /* lr_fwd_chunked_noalloc: the problem needs more scratch
+    LR_ERR_TOO_LARGE = 11,  /* lr_fwd_chunked_noalloc: the problem needs more scratch
                                than LR_STATIC_WORKSPACE_BYTES */
+    LR_ERR_FUSE = 12        /* lr_fuse: unknown flag bits, both alpha maps at once,
+                               or norm_eps negative or not finite */
 } lr_status;
 
 /* Which row of the family (summary table of the first page). */
@@ -208,10 +210,97 @@ lr_status lr_fwd_chunked_noalloc(const void *q, const void *k, const void *v,
                                  int B, int H, int T, int dk, int dv, int chunk,
                                  lr_dtype dt, lr_mode mode, cudaStream_t stream);
 
+/*
+ * Fused entry points: the maps that sit on either side of the recurrence,
+ * applied inside the library's kernels, so that the caller passes
+ * pre-activation values and receives the normalised read-out (page "Scrivere
+ * meglio nella memoria: gate e delta rule"):
+ *
+ *   LR_FUSE_QK_SILU_L2      q_t <- SiLU(q_t) / max(||SiLU(q_t)||_2, 1e-12), the
+ *                           same for k_t, per token over the d_k channels
+ *                           (opening section: DeltaNet's feature map on keys
+ *                           and queries, which keeps the eigenvalues of
+ *                           I - beta k k^T in [0, 1])
+ *   LR_FUSE_BETA_SIGMOID    beta_t <- sigmoid(beta_t)  (section "Correggere: la
+ *                           delta rule": a write strength between 0 and 1)
+ *   LR_FUSE_ALPHA_SIGMOID   alpha_t <- sigmoid(alpha_t)
+ *   LR_FUSE_ALPHA_SOFTPLUS  alpha_t <- exp(-c_h softplus(alpha_t)), c_h =
+ *                           alpha_scale[h]  (section "Dimenticare: i gate":
+ *                           a decay computed from the input; the page leaves
+ *                           the parametrisation open, these are the two in
+ *                           common use)
+ *   LR_FUSE_O_RMSNORM       o_t <- o_t / sqrt(mean_r o_t[r]^2 + norm_eps) *
+ *                           norm_weight, per token over the d_v channels of a
+ *                           head (same page, the read-out of DeltaNet is
+ *                           stabilised by an RMSNorm)
+ *
+ * The alpha maps apply only in modes that use alpha, the beta map only in
+ * modes that use beta; the other flags apply in every mode.  The state is
+ * never normalised.  Gates are evaluated in fp32; ln alpha is formed directly
+ * (-softplus(-a) or -c softplus(a)), not as the log of a rounded alpha.
+ */
+#define LR_FUSE_QK_SILU_L2 0x1u
+#define LR_FUSE_BETA_SIGMOID 0x2u
+#define LR_FUSE_ALPHA_SIGMOID 0x4u
+#define LR_FUSE_ALPHA_SOFTPLUS 0x8u
+#define LR_FUSE_O_RMSNORM 0x10u
+
+typedef struct {
+    unsigned flags;            /* OR of LR_FUSE_* (0: the plain call)                */
+    const float *alpha_scale;  /* [H] fp32 device, c_h of LR_FUSE_ALPHA_SOFTPLUS;
+                                  required with that flag in modes using alpha     */
+    const float *norm_weight;  /* [d_v] fp32 device, shared by all heads, or NULL
+                                  for ones (LR_FUSE_O_RMSNORM)                      */
+    float norm_eps;            /* >= 0, finite (LR_FUSE_O_RMSNORM)                  */
+} lr_fuse;
+
+/*
+ * lr_fwd_chunked with the maps of `fuse` (NULL or flags 0: exactly
+ * lr_fwd_chunked).  Arguments as for lr_fwd_chunked, except that alpha, beta,
+ * q and k hold the pre-activation values of the maps selected, and the
+ * workspace must hold lr_fwd_chunked_fused_workspace_size(..., flags) bytes.
+ * alpha_scale and norm_weight must be 16-byte aligned and must not overlap o
+ * or S_T.
+ *
+ * bf16: the per-block pass applies the gate maps to the gates it reads, and
+ * SiLU + L2 to the q and k tiles it stages; it writes the normalised q and k
+ * (bf16, [B, H, T, dk] each) to the workspace, where the sequential pass
+ * reads them instead of q and k (2 * B * H * T * dk * 2 more bytes of
+ * workspace).  fp32: the single kernel applies the maps to what it stages.
+ * With LR_FUSE_O_RMSNORM one more kernel normalises o in place (the value
+ * channels of a head are split over several CTAs of the sequential pass, so
+ * a token's full output first exists in memory).
+ */
+lr_status lr_fwd_chunked_fused(const void *q, const void *k, const void *v,
+                               const float *alpha, const float *beta,
+                               const float *S0, void *o, float *S_T,
+                               int B, int H, int T, int dk, int dv, int chunk,
+                               lr_dtype dt, lr_mode mode, const lr_fuse *fuse,
+                               void *workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+
+/* Workspace bytes lr_fwd_chunked_fused needs with these flags (0 for
+ * arguments it would reject). */
+size_t lr_fwd_chunked_fused_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
+                                           lr_dtype dt, lr_mode mode, unsigned flags);
+
+/*
+ * lr_step with the maps of `fuse` (NULL or flags 0: exactly lr_step), all
+ * inside the one decode kernel: q and k normalised in registers (fp32, not
+ * rounded), the gates mapped, and the d_v outputs of a head normalised
+ * together before they are stored.  alpha_scale and norm_weight must be
+ * 16-byte aligned and must not overlap o or S.
+ */
+lr_status lr_step_fused(const void *q, const void *k, const void *v,
+                        const float *alpha, const float *beta, float *S, void *o,
+                        int N, int H, int dk, int dv, lr_dtype dt, lr_mode mode,
+                        const lr_fuse *fuse, cudaStream_t stream);
+
 /* Static English text for a status code (never NULL). */
 const char *lr_status_string(lr_status s);
 
-/* ABI version of this header: 1. */
+/* ABI version of this header: 2 (2 added the fused entry points and
+ * LR_ERR_FUSE; every entry point of 1 is unchanged). */
 int lr_abi_version(void);
 
 #ifdef __cplusplus

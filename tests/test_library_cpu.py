@@ -33,6 +33,8 @@ def _declared_functions():
 def test_header_declares_expected_entry_points():
     assert set(_declared_functions()) == {"lr_fwd_chunked", "lr_fwd_chunked_workspace_size",
                                           "lr_fwd_chunked_noalloc", "lr_step", "lr_device_status",
+                                          "lr_fwd_chunked_fused",
+                                          "lr_fwd_chunked_fused_workspace_size", "lr_step_fused",
                                           "lr_status_string", "lr_abi_version"}
 
 
@@ -47,8 +49,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings_and_version(lib):
     import gated_delta_rule_fwd_gb300 as lr
-    assert lib.lr_abi_version() == 1
-    for code in range(12):
+    assert lib.lr_abi_version() == 2
+    for code in range(13):
         s = lr.status_string(code)
         assert s and s != "unknown status"
     assert lr.status_string(99) == "unknown status"
@@ -57,6 +59,7 @@ def test_status_strings_and_version(lib):
 def test_python_binding_matches_header_names():
     import gated_delta_rule_fwd_gb300 as lr
     assert callable(lr.lr_fwd_chunked) and callable(lr.lr_step)
+    assert callable(lr.lr_fwd_chunked_fused) and callable(lr.lr_step_fused)
     assert tuple(sorted(lr.SYMBOLS)) == tuple(_declared_functions())
 
 
@@ -105,6 +108,49 @@ cases = [
     ("step-dk16", step(dk=16), 6), ("step-nullS", step(s=None), 1),
     ("step-nullalpha", step(al=None), 1), ("step-misaligned", step(v=P(A[2] + 4)), 4),
     ("step-alias-o-S", step(o=s0), 8),
+]
+def fz(flags=0, ascale=A[6] + 0x100000, w=A[6] + 0x200000, eps=1e-6):
+    return ctypes.byref(lr.Fuse(flags, ascale, w, eps))
+def fchunk(flags=0, ascale=A[6] + 0x100000, w=A[6] + 0x200000, eps=1e-6, **kw):
+    args = dict(q=q, k=k, v=v, al=al, be=be, s0=s0, o=P(A[7] + 0x4000000), st=st, B=1, H=1, T=8,
+                dk=32, dv=32, chunk=64, dt=1, mode=3, ws=ws, wsb=1 << 24)
+    args.update(kw)
+    a = args
+    return L.lr_fwd_chunked_fused(a['q'], a['k'], a['v'], a['al'], a['be'], a['s0'], a['o'],
+                                  a['st'], a['B'], a['H'], a['T'], a['dk'], a['dv'], a['chunk'],
+                                  a['dt'], a['mode'], fz(flags, ascale, w, eps), a['ws'], a['wsb'],
+                                  None)
+def fstep(flags=0, ascale=A[6] + 0x100000, w=A[6] + 0x200000, eps=1e-6, **kw):
+    args = dict(q=q, k=k, v=v, al=al, be=be, s=s0, o=o, N=1, H=1, dk=32, dv=32, dt=1, mode=3)
+    args.update(kw)
+    a = args
+    return L.lr_step_fused(a['q'], a['k'], a['v'], a['al'], a['be'], a['s'], a['o'], a['N'],
+                           a['H'], a['dk'], a['dv'], a['dt'], a['mode'], fz(flags, ascale, w, eps),
+                           None)
+ws_plain = L.lr_fwd_chunked_fused_workspace_size(1, 1, 8, 32, 32, 64, 1, 3, 0)
+ws_qk = L.lr_fwd_chunked_fused_workspace_size(1, 1, 8, 32, 32, 64, 1, 3, 1)
+cases += [
+    ("fused-unknown-flag", fchunk(flags=0x40), 12),
+    ("fused-both-alpha-maps", fchunk(flags=0x4 | 0x8), 12),
+    ("fused-negative-eps", fchunk(flags=0x10, eps=-1.0), 12),
+    ("fused-nan-eps", fchunk(flags=0x10, eps=float("nan")), 12),
+    ("fused-softplus-null-scale", fchunk(flags=0x8, ascale=None), 1),
+    ("fused-misaligned-weight", fchunk(flags=0x10, w=A[6] + 0x200004), 4),
+    ("fused-misaligned-scale", fchunk(flags=0x8, ascale=A[6] + 0x100008), 4),
+    ("fused-alias-o-weight", fchunk(flags=0x10, w=A[7] + 0x4000000), 8),
+    ("fused-alias-st-scale", fchunk(flags=0x8, ascale=A[7]), 8),
+    ("fused-ws-small-with-qk", fchunk(flags=0x1, wsb=ws_plain), 10),
+    ("fused-shape-first", fchunk(flags=0x40, dk=48), 6),
+    # a map of a gate the mode does not use is dropped: validation passes, and
+    # with no GPU visible the launch then fails
+    ("fused-softplus-ignored-in-delta", fchunk(flags=0x8, ascale=None, mode=2), 7),
+    ("ws-size-qk", ws_qk - ws_plain, 2 * 8 * 32 * 2),
+    ("ws-size-bad-flags", L.lr_fwd_chunked_fused_workspace_size(1, 1, 8, 32, 32, 64, 1, 3, 0x40), 0),
+    ("ws-size-plain-same", ws_plain, need),
+    ("step-fused-unknown-flag", fstep(flags=0x80), 12),
+    ("step-fused-null-scale", fstep(flags=0x8, ascale=None), 1),
+    ("step-fused-alias-S-weight", fstep(flags=0x10, w=A[5]), 8),
+    ("step-fused-misaligned-weight", fstep(flags=0x10, w=A[6] + 0x200004), 4),
 ]
 bad = [(n, got, want) for n, got, want in cases if got != want]
 print("BAD", bad)

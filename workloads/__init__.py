@@ -129,6 +129,68 @@ def draw(gen: str, B, H, T, dk, dv, seed, dtype=torch.float32, s0_std=0.0, devic
     return out
 
 
+# lr_fuse flags (the library's LR_FUSE_* bits) of the pre-activation inputs
+# of each generator: the gated-delta layer maps q, k, beta and alpha and
+# normalises o; the Mamba-2-style layer maps alpha by the softplus gate.
+FUSE_QK_SILU_L2, FUSE_BETA_SIGMOID, FUSE_ALPHA_SIGMOID, FUSE_ALPHA_SOFTPLUS, FUSE_O_RMSNORM = (
+    0x1, 0x2, 0x4, 0x8, 0x10)
+FUSED_FLAGS = {
+    "gdn": FUSE_QK_SILU_L2 | FUSE_BETA_SIGMOID | FUSE_ALPHA_SIGMOID | FUSE_O_RMSNORM,
+    "mamba2": FUSE_ALPHA_SOFTPLUS | FUSE_O_RMSNORM,
+}
+MAMBA2_ALPHA_SCALE = 0.1
+
+
+def draw_pre(gen: str, B, H, T, dk, dv, seed, dtype=torch.float32, s0_std=0.0, device="cpu"):
+    """Pre-activation inputs for the fused entry points (the same distributions
+    as :func:`draw` before its maps): q, k, v ~ N(0,1) rounded once to
+    ``dtype``; for "gdn" beta ~ N(0,1) and alpha ~ N(3,1) (sigmoid gates), for
+    "mamba2" alpha ~ N(0,1) (softplus gate, alpha_scale 0.1 for every head)
+    and beta = 0; norm_weight ~ U(0.5, 1.5) [dv]; S0 ~ N(0, s0_std^2) or None.
+
+    Returns dict q, k, v, alpha, beta, S0, alpha_scale [H], norm_weight [dv].
+    Draw order: q, k, v, beta, alpha, S0, norm_weight.
+    """
+    g = torch.Generator("cpu")
+    g.manual_seed(int(seed))
+    shp_k, shp_v, shp_t = (B, H, T, dk), (B, H, T, dv), (B, H, T)
+    q = torch.randn(shp_k, generator=g)
+    k = torch.randn(shp_k, generator=g)
+    v = torch.randn(shp_v, generator=g)
+    if gen == "gdn":
+        beta = torch.randn(shp_t, generator=g)
+        alpha = 3.0 + torch.randn(shp_t, generator=g)
+    elif gen == "mamba2":
+        beta = torch.zeros(shp_t)
+        alpha = torch.randn(shp_t, generator=g)
+    else:
+        raise ValueError(gen)
+    S0 = torch.randn((B, H, dv, dk), generator=g) * s0_std if s0_std > 0 else None
+    w = 0.5 + torch.rand((dv,), generator=g)
+    out = dict(q=q.to(dtype), k=k.to(dtype), v=v.to(dtype), alpha=alpha.float().contiguous(),
+               beta=beta.float().contiguous(), S0=S0,
+               alpha_scale=torch.full((H,), MAMBA2_ALPHA_SCALE), norm_weight=w.float())
+    if device != "cpu":
+        out = {n: (t.to(device) if t is not None else None) for n, t in out.items()}
+    return out
+
+
+def draw_decode_step_pre(w: Workload, step: int, device, generator=None):
+    """Pre-activation inputs of decode step ``step`` (the fused decode entry
+    point): q, k, v ~ N(0,1) in the workload dtype; beta ~ N(0,1), alpha ~
+    N(3,1) [N,H]."""
+    g = generator if generator is not None else torch.Generator(device)
+    g.manual_seed(int(w.seed) * 1000003 + int(step))
+    N, H, dk, dv = w.B, w.H, w.dk, w.dv
+    q = torch.randn((N, H, dk), generator=g, device=device)
+    k = torch.randn((N, H, dk), generator=g, device=device)
+    v = torch.randn((N, H, dv), generator=g, device=device)
+    beta = torch.randn((N, H), generator=g, device=device)
+    alpha = 3.0 + torch.randn((N, H), generator=g, device=device)
+    dt = w.torch_dtype
+    return dict(q=q.to(dt), k=k.to(dt), v=v.to(dt), alpha=alpha.float(), beta=beta.float())
+
+
 def draw_workload(w: Workload, device="cpu"):
     return draw(w.gen, w.B, w.H, w.T, w.dk, w.dv, w.seed, w.torch_dtype, w.s0_std, device)
 
