@@ -357,6 +357,12 @@ def run_ours(args, dist, rank, world, local):
     del hx, ho, hs, dx, do_, ds_
 
     decode = None if args.no_decode else run_decode(lr, dev, dist, peaks, args)
+    fused = None
+    if not args.no_fused and w.gen in workloads.FUSED_FLAGS:
+        fused = run_fused(lr, dev, dist, args, w, ms_per_step)
+    fused_decode = None
+    if not args.no_fused and not args.no_decode:
+        fused_decode = run_decode(lr, dev, dist, peaks, args, fused=True)
 
     out = None
     if rank == 0:
@@ -392,39 +398,103 @@ def run_ours(args, dist, rank, world, local):
         }
         if decode is not None:
             out["decode"] = decode
+        if fused is not None:
+            out["fused"] = fused
+        if fused_decode is not None:
+            out["fused_decode"] = fused_decode
     return out
 
 
-def run_decode(lr, dev, dist, peaks, args):
+def run_fused(lr, dev, dist, args, w, plain_ms):
+    """The same workload through lr_fwd_chunked_fused from pre-activation
+    inputs (the maps of the workload's layer in the kernels), timed like the
+    headline, with and without the output RMSNorm pass."""
+    flags_all = workloads.FUSED_FLAGS[w.gen]
+    x = workloads.draw_pre(w.gen, w.B, w.H, w.T, w.dk, w.dv, w.seed, w.torch_dtype, w.s0_std)
+    if w.gen == "mamba2":
+        x["q"] = (x["q"].float() / w.dk ** 0.5).to(w.torch_dtype)
+        x["k"] = (x["k"].float() / w.dk ** 0.5).to(w.torch_dtype)
+    xd = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.torch_dtype, device=dev)
+    st = torch.empty((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, lr.fused_workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.torch_dtype,
+                                                    w.mode, flags_all, w.chunk)),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    steps = max(3, min(args.steps, 50))
+    res = {}
+    for name, flags in (("maps", flags_all & ~workloads.FUSE_O_RMSNORM), ("maps_and_norm", flags_all)):
+        def step():
+            lr.lr_fwd_chunked_fused(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], xd["S0"],
+                                    mode=w.mode, flags=flags, alpha_scale=xd["alpha_scale"],
+                                    norm_weight=xd["norm_weight"], chunk=w.chunk, o=o, S_T=st,
+                                    workspace=ws, stream=stream)
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        barrier(dist, dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        res[name] = max_over_ranks(dist, e0.elapsed_time(e1), dev) / steps
+    world = dist.get_world_size() if dist else 1
+    ms = res["maps_and_norm"]
+    return {"workload": w.name, "entry_point": "lr_fwd_chunked_fused", "flags": flags_all,
+            "maps": "SiLU+L2 q,k; sigmoid beta; sigmoid alpha; output RMSNorm" if w.gen == "gdn"
+                    else "softplus alpha gate (c = 0.1); output RMSNorm",
+            "value": w.B * w.T * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+            "ms_per_step_without_norm": res["maps"], "ms_per_step_plain": plain_ms,
+            "steps": steps,
+            "gpu_launches": steps * ((2 if w.dtype == "bf16" else 1) + 1)}
+
+
+def run_decode(lr, dev, dist, peaks, args, fused=False):
     """1000 consecutive decode steps (fresh inputs per step, drawn beforehand
     on the device), timed as a whole after 10 warm-up steps on a scratch
-    copy of the state."""
+    copy of the state.  With ``fused``: pre-activation inputs through
+    lr_step_fused with the gated-delta layer's maps (200 steps)."""
     w = workloads.WORKLOADS[DECODE_WORKLOAD]
     g = torch.Generator(dev)
     S = workloads.draw_decode_state(w, dev, g)
     steps = w.steps if args.decode_steps is None else max(1, args.decode_steps)
-    inputs = [workloads.draw_decode_step(w, s, dev, g) for s in range(steps)]
+    if fused:
+        steps = min(steps, 200)
+        inputs = [workloads.draw_decode_step_pre(w, s, dev, g) for s in range(steps)]
+        wn = (0.5 + torch.rand((w.dv,), generator=g, device=dev)).float()
+        flags = workloads.FUSED_FLAGS["gdn"]
+    else:
+        inputs = [workloads.draw_decode_step(w, s, dev, g) for s in range(steps)]
     o = torch.empty((w.B, w.H, w.dv), dtype=w.torch_dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def call(i, state):
+        if fused:
+            lr.lr_step_fused(i["q"], i["k"], i["v"], i["alpha"], i["beta"], state, mode=w.mode,
+                             flags=flags, norm_weight=wn, o=o, stream=stream)
+        else:
+            lr.lr_step(i["q"], i["k"], i["v"], i["alpha"], i["beta"], state, mode=w.mode, o=o,
+                       stream=stream)
+
     scratch = S.clone()
     for s in range(min(10, steps)):
-        i = inputs[s]
-        lr.lr_step(i["q"], i["k"], i["v"], i["alpha"], i["beta"], scratch, mode=w.mode, o=o,
-                   stream=stream)
+        call(inputs[s], scratch)
     del scratch
     torch.cuda.synchronize(dev)
     barrier(dist, dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in inputs:
-        lr.lr_step(i["q"], i["k"], i["v"], i["alpha"], i["beta"], S, mode=w.mode, o=o,
-                   stream=stream)
+        call(i, S)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
     per = ms / steps / 1e3
     gbs = decode_step_bytes(w) / per / 1e9
-    return {"workload": w.name, "metric": "decode step state GB/s", "value": gbs, "unit": "GB/s",
+    return {"workload": w.name, "entry_point": "lr_step_fused (all maps)" if fused else "lr_step",
+            "metric": "decode step state GB/s", "value": gbs, "unit": "GB/s",
             "frac_hbm": gbs / peaks["hbm_gbs"], "peak_gbs": peaks["hbm_gbs"],
             "us_per_step": per * 1e6, "steps": steps, "tokens_per_s": w.B / per,
             "bytes_per_step": decode_step_bytes(w), "gpu_launches": steps,
@@ -487,6 +557,8 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=None,
                     help="decode steps to time (default: the workload's 1000)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fused", action="store_true",
+                    help="skip the fused entry points' timings (prefill and decode)")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of single-core oracle work in the cpu_baseline sample")
     ap.add_argument("--ref-tokens", type=int, default=2048,

@@ -59,12 +59,20 @@
 // leaves the real tokens' results unchanged.
 //
 // The lr_fuse maps live in prep (page "Scrivere meglio nella memoria: gate e
-// delta rule"): the gates are mapped as they are read, and with SiLU + L2 of
-// q and k each thread normalises one row of the staged [Q; K] tile in place
-// (fp32 sum of squares, one rounding to bf16) before E1; the CTA writes its
-// normalised rows to the workspace by TMA stores, and the scan reads q and k
-// from there.  The previous block's k rows, staged again for E4, are
-// normalised again the same way, so they match the stored copy bit for bit.
+// delta rule"), in a separate instantiation so the plain path is untouched.
+// The gates are mapped as they are read.  SiLU + L2 of q and k: each thread
+// takes one row of the staged [Q; K] tile through SiLU in place (fp32, one
+// rounding to bf16) and keeps the row's inverse L2 norm in fp32; the norms
+// are never applied to the tiles but folded into the per-row and per-column
+// factors every product is already scaled by:
+//   P_ri  *= 1/|q_r| 1/|k_i|        A_ri *= 1/|k_r| 1/|k_i|      (E2)
+//   W = T diag(beta g / |k|) K~                                     (E3)
+//   -Z' diag(kd' / |k'|)                                           (E4)
+//   record vectors g' / |q'| (output rows) and kd / |k| (the kd U rows)
+// so that every result equals the one with normalised q and k.  The CTA
+// writes its SiLU'd q and k rows to the workspace by TMA stores and the scan
+// reads them there unchanged; the previous block's k rows, staged again for
+// E4, go through the same SiLU, so they match the stored copy bit for bit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -126,7 +134,7 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 //       the Q rows host the T diag(beta g) tile and the solve scratch, and
 //       after E3 the K rows are refilled with the previous block's K rows (E4)
 //   AT  fp32 [64][AP]: A, inverted in place into T; then bf16 W [64][DK]
-// 50 KB at d_k = 128: four CTAs per SM.
+// 51 KB at d_k = 128: four CTAs per SM.
 template <int DK>
 struct PrepLayout {
     static constexpr int KB = (DK + 63) / 64;
@@ -134,8 +142,9 @@ struct PrepLayout {
     static constexpr int TB = QK;                           // [64][64] bf16, in the Q rows of block 0
     static constexpr int XT = TB;                           // fp32 [32][XS] solve scratch, inside TB
     static constexpr int AT = QK + 128 * 128 * KB;
-    static constexpr int VEC = AT + C * AP * 4;             // G (later kd'), ginv, g, beta
-    static constexpr int BAR = VEC + 4 * 64 * 4;            // 3 barriers, TMEM slot
+    static constexpr int VEC = AT + C * AP * 4;             // G (later kd'), ginv, g, beta,
+                                                            // 1/|q|, 1/|k|, 1/|k'| (maps)
+    static constexpr int BAR = VEC + 7 * 64 * 4;            // 3 barriers, TMEM slot
     static constexpr int BYTES = BAR + 64;
     static constexpr int ALLOC = BYTES + 1024;
 };
@@ -283,50 +292,44 @@ __device__ __forceinline__ void ut_inverse(float *AT, float *Xt, int tid) {
     __syncthreads();
 }
 
-// SiLU, then L2 normalisation, of row `row` of a bf16 K-major 128-byte
-// swizzled tile of `rows` rows (sw128_offset layout), in place.  Two passes
-// over the row (sum of squares, then scale) so that nothing but 8 values is
-// held at a time; zero rows stay zero.
+// SiLU of row `row` of a bf16 K-major 128-byte-swizzled tile of `rows` rows
+// (sw128_offset layout), in place (computed in fp32, rounded once); returns
+// 1 / max(|SiLU(row)|, 1e-12) from the fp32 values.  Zero rows stay zero.
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+
 template <int DK>
-__device__ __forceinline__ void silu_l2_row(uint8_t *tile, int row, int rows) {
+__device__ __forceinline__ float silu_row(uint8_t *tile, int row, int rows) {
     constexpr int KB = (DK + 63) / 64, CH = DK < 64 ? DK / 8 : 8;  // 16-byte chunks per block
     uint8_t *base = tile + row * 128;
     float ss = 0.f;
-#pragma unroll 1
-    for (int kb = 0; kb < KB; ++kb) {
-#pragma unroll 2
-        for (int c = 0; c < CH; ++c) {
-            const uint4 raw = *reinterpret_cast<const uint4 *>(base + kb * rows * 128 +
-                                                               ((c ^ (row & 7)) << 4));
-            const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float x = silu_f(__bfloat162float(e[i]));
-                ss += x * x;
-            }
-        }
-    }
-    const float inv = inv_l2(ss);
-#pragma unroll 1
     for (int kb = 0; kb < KB; ++kb) {
-#pragma unroll 2
+#pragma unroll 4
         for (int c = 0; c < CH; ++c) {
             uint4 *p = reinterpret_cast<uint4 *>(base + kb * rows * 128 + ((c ^ (row & 7)) << 4));
             const uint4 raw = *p;
-            const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
             float x[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = silu_f(__bfloat162float(e[i])) * inv;
+            for (int i = 0; i < 4; ++i) {
+                x[2 * i] = silu_fast(__uint_as_float(w[i] << 16));
+                x[2 * i + 1] = silu_fast(__uint_as_float(w[i] & 0xffff0000u));
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss += x[i] * x[i];
             *p = pack8(x);
         }
     }
+    return inv_l2(ss);
 }
 
 // Prep of block j = blockIdx.x.  Writes to record j: W_j, T_j diag(beta),
 // -Z_{j-1} and the gate vectors; to record j+1: P_j (and, for the last block,
-// record j+1's gate vectors).  With SiLU + L2 of q and k, also the block's
-// normalised q and k rows, through the maps tmqn and tmkn.
-template <int DK, bool ALPHA, bool DELTA>
+// record j+1's gate vectors).  MAPS: the lr_fuse maps of `fz`; with SiLU + L2
+// of q and k also the block's SiLU'd q and k rows, through tmqn and tmkn, and
+// (for every block) record j+1's previous-block vectors, which carry the
+// norms.
+template <int DK, bool ALPHA, bool DELTA, bool MAPS>
 __global__ void __launch_bounds__(NT)
 chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                   const float *__restrict__ alpha, const float *__restrict__ beta,
@@ -354,19 +357,21 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     float *Gv = reinterpret_cast<float *>(sm + L::VEC);
     float *giv = Gv + 64, *gv = Gv + 128, *bv = Gv + 192;
     float *kdv = Gv;  // kd of the previous block, once G is no longer needed
+    float *inq = Gv + 256, *ink = Gv + 320, *inkp = Gv + 384;  // inverse norms (maps)
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);  // MMA, q/k tiles, previous k tile
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 32);
     const bool zprev = DELTA && blk > 0;  // Z_{j-1} exists
     // gate inputs first, so their global-load latency overlaps the staging:
     // threads 0-63 this block's tokens, 64-127 the previous block's
     const int tok = tid & 63;
-    const unsigned fl = fz.flags;
-    const bool qk = (fl & LR_FUSE_QK_SILU_L2) != 0;
+    const unsigned fl = MAPS ? fz.flags : 0u;
+    const bool qk = MAPS && (fl & LR_FUSE_QK_SILU_L2) != 0;
     float araw = 1.f, b = 0.f;
     if (tid < C) {
         if (tok < n) {
             if (ALPHA) araw = alpha[bh * T + t0 + tok];
-            if (DELTA) b = write_strength(fl, beta[bh * T + t0 + tok]);
+            if (DELTA) b = beta[bh * T + t0 + tok];
+            if (MAPS && DELTA) b = write_strength(fl, b);
         }
     } else if (ALPHA && blk > 0) {
         araw = alpha[bh * T + t0 - C + tok];
@@ -388,10 +393,12 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     }
     // ---- gates: warps 0-1 hold this block's tokens, warps 2-3 the previous
     //      block's (all ones for block 0)
-    const bool has_a = ALPHA && (tid < C ? tok < n : blk > 0);
-    const float la = has_a ? log_gate(fl, araw,
-                                      (fl & LR_FUSE_ALPHA_SOFTPLUS) ? fz.ascale[blockIdx.y] : 0.f)
-                           : 0.f;
+    float la = ALPHA ? __logf(araw) : 0.f;
+    if (MAPS) {
+        const bool has_a = ALPHA && (tid < C ? tok < n : blk > 0);
+        la = has_a ? log_gate(fl, araw, (fl & LR_FUSE_ALPHA_SOFTPLUS) ? fz.ascale[blockIdx.y] : 0.f)
+                   : 0.f;
+    }
     if (warp == 0) {
         tmem_alloc(tmem_slot, 128);
         tmem_relinquish();
@@ -409,7 +416,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     const float Glast = Am[pb + 31] + Am[pb + 63];
     // exp(G_r - G_i) = g_r * ginv_i when exp(-G_63) is finite in fp32
     const bool factor = !ALPHA || Am[31] + Am[63] > -80.f;
-    float kdp = 1.f;
+    float kdp = 1.f, my_g = 1.f, my_kd = 1.f;
     if (tid < C) {
         const float g = ALPHA ? __expf(G) : 1.f;
         const float kd = ALPHA ? __expf(Glast - G) : 1.f;
@@ -417,30 +424,47 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         gv[tok] = g;
         giv[tok] = ALPHA ? __expf(-G) : 1.f;
         bv[tok] = b;
-        vec[kVkd + tok] = kd;
-        if (blk == nblk - 1) {  // the stage after the last block reads this block as its previous one
-            vec_next[kVgPrev + tok] = g;
-            vec_next[kVkdPrev + tok] = kd;
-            if (tok == C - 1) vec_next[kVgCPrev] = ALPHA ? __expf(Glast) : 1.f;
+        my_g = g;
+        my_kd = kd;
+        if (!MAPS) {
+            vec[kVkd + tok] = kd;
+            if (blk == nblk - 1) {  // the stage after the last block reads this block as its previous one
+                vec_next[kVgPrev + tok] = g;
+                vec_next[kVkdPrev + tok] = kd;
+                if (tok == C - 1) vec_next[kVgCPrev] = ALPHA ? __expf(Glast) : 1.f;
+            }
         }
     } else {
         const float g = ALPHA ? __expf(G) : 1.f;
         kdp = ALPHA ? __expf(Glast - G) : 1.f;
-        vec[kVgPrev + tok] = g;
-        vec[kVkdPrev + tok] = kdp;
-        if (tok == C - 1) {
-            const float gc = ALPHA ? __expf(Glast) : 1.f;
-            vec[kVgCPrev] = gc;
+        // with the maps record j's previous-block vectors come from the CTA of
+        // block j-1 (they carry its norms); stage 0 has no previous block
+        if (!MAPS || blk == 0) {
+            vec[kVgPrev + tok] = g;
+            vec[kVkdPrev + tok] = kdp;
+            if (tok == C - 1) {
+                const float gc = ALPHA ? __expf(Glast) : 1.f;
+                vec[kVgCPrev] = gc;
+            }
         }
     }
     bool ok = mbar_wait(&bar[1], 0);
     if (qk && ok) {  // thread t: row t of [Q; K]
-        silu_l2_row<DK>(QK, tid, 128);
+        const float in = silu_row<DK>(QK, tid, 128);
+        if (tid < C) inq[tid] = in;
+        else ink[tok] = in;
         fence_async_smem();
     }
     tc_fence_before();
     ok = __syncthreads_and(ok ? 1 : 0) != 0;
     tc_fence_after();
+    if (MAPS && tid < C) {  // the vectors that carry this block's norms
+        const float sq = qk ? inq[tok] : 1.f, sk = qk ? ink[tok] : 1.f;
+        vec[kVkd + tok] = my_kd * sk;
+        vec_next[kVgPrev + tok] = my_g * sq;
+        vec_next[kVkdPrev + tok] = my_kd * sk;
+        if (tok == C - 1) vec_next[kVgCPrev] = ALPHA ? __expf(Glast) : 1.f;
+    }
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
 
@@ -452,7 +476,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
             mma_bf16(tmem, tile_desc(smem_u32(QK), 128, 0, ks), tile_desc(smem_u32(QK), 128, 64, ks),
                      id, ks > 0);
         mma_commit(&bar[0]);
-        if (qk) {  // the normalised rows -> workspace (rows past T are not written)
+        if (qk) {  // the SiLU'd rows -> workspace (rows past T are not written)
 #pragma unroll
             for (int kb = 0; kb < L::KB; ++kb) {
                 tma_store_3d(&tmqn, QK + kb * 16384, kb * 64, t0, (int)bh);
@@ -469,6 +493,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         const int r = 32 * (warp & 1) + lane;
         const bool is_q = warp < 2;
         const float Gr = Gv[r], gr = gv[r];
+        const float rs = qk ? (is_q ? inq[r] : ink[r]) : 1.f;  // 1/|q_r| or 1/|k_r|
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             float a[32];
@@ -488,6 +513,16 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                 const int i = half * 32 + e;
                 const float dec = !ALPHA ? 1.f : (factor ? gr * gi[e] : __expf(Gr - Gv[i]));
                 a[e] = (i <= r && (is_q || i < r)) ? a[e] * dec : 0.f;
+            }
+            if (qk) {  // the norms: 1/|q_r| (or 1/|k_r|) times 1/|k_i|
+#pragma unroll
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const float4 v4 = reinterpret_cast<const float4 *>(ink + half * 32)[e4];
+                    a[4 * e4] *= rs * v4.x;
+                    a[4 * e4 + 1] *= rs * v4.y;
+                    a[4 * e4 + 2] *= rs * v4.z;
+                    a[4 * e4 + 3] *= rs * v4.w;
+                }
             }
             if (is_q) {
 #pragma unroll
@@ -525,6 +560,12 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
             *reinterpret_cast<float4 *>(bb + 4) = reinterpret_cast<const float4 *>(bv)[2 * i8 + 1];
             *reinterpret_cast<float4 *>(gg) = reinterpret_cast<const float4 *>(gv)[2 * i8];
             *reinterpret_cast<float4 *>(gg + 4) = reinterpret_cast<const float4 *>(gv)[2 * i8 + 1];
+            if (qk) {  // W = T diag(beta g / |k|) K~
+                const float4 k0 = reinterpret_cast<const float4 *>(ink)[2 * i8];
+                const float4 k1 = reinterpret_cast<const float4 *>(ink)[2 * i8 + 1];
+                gg[0] *= k0.x, gg[1] *= k0.y, gg[2] *= k0.z, gg[3] *= k0.w;
+                gg[4] *= k1.x, gg[5] *= k1.y, gg[6] *= k1.z, gg[7] *= k1.w;
+            }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int i = i8 * 8 + e;
@@ -591,7 +632,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         if (zprev) {
             ok = mbar_wait(&bar[2], 0) && ok;
             if (qk && ok && tid < C) {
-                silu_l2_row<DK>(QK, C + tid, 128);
+                inkp[tid] = silu_row<DK>(QK, C + tid, 128);
                 fence_async_smem();
             }
             ok = __syncthreads_and(ok ? 1 : 0) != 0;
@@ -614,8 +655,12 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                     tmem_ld_wait();
                     if (lane < 16) {
 #pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {  // -Z' diag(kd')
-                            const float4 v4 = reinterpret_cast<const float4 *>(kdv + half * 32)[e4];
+                        for (int e4 = 0; e4 < 8; ++e4) {  // -Z' diag(kd') (/ |k'|)
+                            float4 v4 = reinterpret_cast<const float4 *>(kdv + half * 32)[e4];
+                            if (qk) {
+                                const float4 n4 = reinterpret_cast<const float4 *>(inkp + half * 32)[e4];
+                                v4.x *= n4.x, v4.y *= n4.y, v4.z *= n4.z, v4.w *= n4.w;
+                            }
                             z[4 * e4] *= -v4.x;
                             z[4 * e4 + 1] *= -v4.y;
                             z[4 * e4 + 2] *= -v4.z;
@@ -734,6 +779,7 @@ struct ScanBars {
     uint64_t fin[2];     // every product an issuer issued has completed (commit)
     uint32_t tmem;
 };
+static_assert(sizeof(ScanBars) <= 256, "the barriers must fit their shared-memory slot");
 constexpr uint32_t kEmptyLCount = 2 + 4 + 4 + 8;  // both issuers' commits, U, output and state warps
 
 template <int DK, bool ALPHA, bool DELTA>
@@ -1080,13 +1126,18 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
         fence_async_smem();
         warp_arrive(&bars->s[0]);
         warp_arrive(&bars->s[1]);
+        // Without delta these warps also order two reuses that the U chain
+        // orders with delta: the late group (and with it the Delta S
+        // accumulator of this parity and its dsf barrier) is released only
+        // after Delta S is read, and a bf16 state copy is rewritten only after
+        // b_{j-1}, its last reader, is done (emptyE).
         for (int j = 0; j <= nblk && ok; ++j) {
             const int p = j & 1;
             const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
             ok = __all_sync(0xffffffffu, mbar_wait(&bars->fullL[p], ph));
             if (!ok) break;
             const float gC = vec_of(p)[kVgCPrev];  // the only late-group value read here
-            warp_arrive(&bars->emptyL[p]);
+            if (DELTA) warp_arrive(&bars->emptyL[p]);
             ok = __all_sync(0xffffffffu, mbar_wait(&bars->dsf[p], ph));
             if (!ok) break;
             if (j >= 1) {
@@ -1094,14 +1145,21 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                 float d[SC];
                 tmem_ld16(tmem + lb + base + kDS, d);
                 tmem_ld_wait();
+                tc_fence_before();
+                if (!DELTA) warp_arrive(&bars->emptyL[p]);
 #pragma unroll
                 for (int c = 0; c < SC; ++c) Sr[c] = gC * Sr[c] + d[c];
-                tc_fence_before();
                 if (j < nblk) {  // S_j -> copy (j+1)&1, read by b_{j+1}
+                    if (!DELTA)
+                        ok = __all_sync(0xffffffffu,
+                                        mbar_wait(&bars->emptyE[(j - 1) & 1], ((j - 1) >> 1) & 1));
+                    if (!ok) break;
                     write_sb((j + 1) & 1);
                     fence_async_smem();
                     warp_arrive(&bars->s[(j + 1) & 1]);
                 }
+            } else if (!DELTA) {
+                warp_arrive(&bars->emptyL[p]);
             }
         }
         if (ok && kc < DK) {
@@ -1162,10 +1220,13 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
                          const float *beta, const float *S0, void *o, float *S_T, int B, int H,
                          int T, int dv, const Fuse &fz, void *ws, cudaStream_t stream, int slot) {
     const int nblk = (T + C - 1) / C;
-    auto prep = chunk_prep_kernel<DK, ALPHA, DELTA>;
+    // the maps that prep applies (the output RMSNorm runs after the scan)
+    const bool maps = (fz.flags & ~LR_FUSE_O_RMSNORM) != 0;
+    auto prep = maps ? chunk_prep_kernel<DK, ALPHA, DELTA, true>
+                     : chunk_prep_kernel<DK, ALPHA, DELTA, false>;
     auto scan = chunk_scan_kernel<DK, ALPHA, DELTA>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(prep), PrepLayout<DK>::ALLOC,
-                                     slot);
+                                     slot + (maps ? 24 : 0));
     if (e != cudaSuccess) return e;
     e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC, slot + 12);
     if (e != cudaSuccess) return e;
@@ -1178,7 +1239,7 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
     if (e != cudaSuccess) return e;
     e = make_rows_map(&tmv, v, dv, T, B * H);
     if (e != cudaSuccess) return e;
-    // normalised q and k in the workspace (the scan reads them instead)
+    // SiLU'd q and k in the workspace (the scan reads them instead)
     const bool qk = (fz.flags & LR_FUSE_QK_SILU_L2) != 0;
     const bf16 *qs = static_cast<const bf16 *>(q), *ks = static_cast<const bf16 *>(k);
     CUtensorMap tmqn = tmq, tmkn = tmk;
@@ -1231,7 +1292,7 @@ size_t chunked_tc_workspace_bytes(int B, int H, int T, int dk, unsigned flags) {
     return records_bytes(B, H, T, dk) + qk;
 }
 
-// Attribute slots 32..55 belong to this file.
+// Attribute slots 32..67 belong to this file.
 cudaError_t launch_chunked_tc(const void *q, const void *k, const void *v, const float *alpha,
                               const float *beta, const float *S0, void *o, float *S_T, int B,
                               int H, int T, int dk, int dv, lr_mode mode, const Fuse &fz,

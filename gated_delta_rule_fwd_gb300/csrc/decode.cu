@@ -60,7 +60,7 @@ step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__r
             const float *__restrict__ alpha, const float *__restrict__ beta,
             float *__restrict__ S, Tin *__restrict__ o, int H, int dv, const Fuse fz) {
     __shared__ float o_sh[128];  // the head's outputs, with the output RMSNorm
-    __shared__ float inv_sh;
+    __shared__ float ss_sh[kStepThreads / 32];
     constexpr int NV = DK / (4 * kLanesPerRow);  // float4 per lane per row
     static_assert(NV >= 1 && NV * 4 * kLanesPerRow == DK, "DK must be 32, 64 or 128");
 
@@ -109,6 +109,7 @@ step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__r
                           : 1.f;
     const float b = DELTA ? write_strength(fl, beta[head]) : 1.f;
     const bool norm = (fl & LR_FUSE_O_RMSNORM) != 0;
+    float oss = 0.f;  // sum of squares of the outputs this lane produced
 
     const int passes = dv / kRowsPerPass;
     for (int p0 = 0; p0 < passes; p0 += UNROLL) {
@@ -146,23 +147,26 @@ step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__r
             }
             if (sub == 0) {
                 const float orow = a * sq + ur * kq;
-                if (norm) o_sh[r] = orow;
-                else oh[r] = from_f<Tin>(orow);
+                if (norm) {
+                    o_sh[r] = orow;
+                    oss += orow * orow;
+                } else {
+                    oh[r] = from_f<Tin>(orow);
+                }
             }
         }
     }
-    if (norm) {
-        __syncthreads();
-        if (warp == 0) {
-            float ss = 0.f;
-            for (int r = lane; r < dv; r += 32) ss += o_sh[r] * o_sh[r];
+    if (norm) {  // one barrier: per-warp partial sums, then every thread finishes the sum
 #pragma unroll
-            for (int d = 16; d >= 1; d >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, d);
-            if (lane == 0) inv_sh = rsqrtf(ss / (float)dv + fz.norm_eps);
-        }
+        for (int d = 16; d >= 1; d >>= 1) oss += __shfl_xor_sync(0xffffffffu, oss, d);
+        if (lane == 0) ss_sh[warp] = oss;
         __syncthreads();
+        float ss = 0.f;
+#pragma unroll
+        for (int w = 0; w < kStepThreads / 32; ++w) ss += ss_sh[w];
+        const float inv = rsqrtf(ss / (float)dv + fz.norm_eps);
         const int r = threadIdx.x;
-        if (r < dv) oh[r] = from_f<Tin>(o_sh[r] * inv_sh * (fz.norm_w ? fz.norm_w[r] : 1.f));
+        if (r < dv) oh[r] = from_f<Tin>(o_sh[r] * inv * (fz.norm_w ? fz.norm_w[r] : 1.f));
     }
 }
 
