@@ -47,8 +47,8 @@ UNIT = "tokens/s"
 TRAFFIC_SOURCES = ("gated_delta_rule_fwd_gb300/csrc/chunked_tc.cu",
                    "gated_delta_rule_fwd_gb300/csrc/tc_common.cuh")
 TRAFFIC = {
-    "gdn_prefill_bf16": {"bytes": 273.051392e6 + 289.682176e6 + 750.554880e6 + 122.247424e6,
-                         "sha256": "e65ceac0d2c9e7883d6d7fee5878f597d4f70855c1939e9b04df9a81e17770c3"},
+    "gdn_prefill_bf16": {"bytes": 272.984064e6 + 289.703168e6 + 750.225152e6 + 122.367488e6,
+                         "sha256": "8879ae46b2b38daaabb472546913269b6a7683966ca5b06751cb702eef2acaf0"},
 }
 
 

@@ -292,21 +292,29 @@ __device__ __forceinline__ void ut_inverse(float *AT, float *Xt, int tid) {
     __syncthreads();
 }
 
-// SiLU of row `row` of a bf16 K-major 128-byte-swizzled tile of `rows` rows
-// (sw128_offset layout), in place (computed in fp32, rounded once); returns
-// 1 / max(|SiLU(row)|, 1e-12) from the fp32 values.  Zero rows stay zero.
-__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+// SiLU(x) = x sigmoid(x) = h + h tanh(h), h = x / 2, with the hardware tanh
+// approximation (one special-function operation per element; its relative
+// error, about 2^-11, is below a bf16 rounding of the result).
+__device__ __forceinline__ float silu_fast(float x) {
+    const float h = 0.5f * x;
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+    return fmaf(h, t, h);
+}
 
-template <int DK>
-__device__ __forceinline__ float silu_row(uint8_t *tile, int row, int rows) {
-    constexpr int KB = (DK + 63) / 64, CH = DK < 64 ? DK / 8 : 8;  // 16-byte chunks per block
+// SiLU of columns [c0, c0 + ncol) (multiples of 8) of row `row` of a bf16
+// K-major 128-byte-swizzled tile of `rows` rows (sw128_offset layout), in
+// place (fp32, rounded once to bf16); returns the sum of squares of the fp32
+// values.  Zero entries stay zero.
+template <int NCOL>
+__device__ __forceinline__ float silu_cols(uint8_t *tile, int row, int rows, int c0) {
     uint8_t *base = tile + row * 128;
     float ss = 0.f;
-#pragma unroll
-    for (int kb = 0; kb < KB; ++kb) {
 #pragma unroll 4
-        for (int c = 0; c < CH; ++c) {
-            uint4 *p = reinterpret_cast<uint4 *>(base + kb * rows * 128 + ((c ^ (row & 7)) << 4));
+    for (int c = 0; c < NCOL / 8; ++c) {
+        const int k = c0 + 8 * c, kb = k >> 6, ch = (k & 63) >> 3;
+        {
+            uint4 *p = reinterpret_cast<uint4 *>(base + kb * rows * 128 + ((ch ^ (row & 7)) << 4));
             const uint4 raw = *p;
             const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
             float x[8];
@@ -316,20 +324,20 @@ __device__ __forceinline__ float silu_row(uint8_t *tile, int row, int rows) {
                 x[2 * i + 1] = silu_fast(__uint_as_float(w[i] & 0xffff0000u));
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ss += x[i] * x[i];
+            for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
             *p = pack8(x);
         }
     }
-    return inv_l2(ss);
+    return ss;
 }
 
 // Prep of block j = blockIdx.x.  Writes to record j: W_j, T_j diag(beta),
 // -Z_{j-1} and the gate vectors; to record j+1: P_j (and, for the last block,
-// record j+1's gate vectors).  MAPS: the lr_fuse maps of `fz`; with SiLU + L2
-// of q and k also the block's SiLU'd q and k rows, through tmqn and tmkn, and
-// (for every block) record j+1's previous-block vectors, which carry the
-// norms.
-template <int DK, bool ALPHA, bool DELTA, bool MAPS>
+// record j+1's gate vectors).  MAPS 1: the gate maps of `fz`; MAPS 2: also
+// SiLU + L2 of q and k, with the block's SiLU'd q and k rows written through
+// tmqn and tmkn.  With maps every block also writes record j+1's
+// previous-block vectors (they carry the norms).
+template <int DK, bool ALPHA, bool DELTA, int MAPS>
 __global__ void __launch_bounds__(NT)
 chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                   const float *__restrict__ alpha, const float *__restrict__ beta,
@@ -365,7 +373,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     // threads 0-63 this block's tokens, 64-127 the previous block's
     const int tok = tid & 63;
     const unsigned fl = MAPS ? fz.flags : 0u;
-    const bool qk = MAPS && (fl & LR_FUSE_QK_SILU_L2) != 0;
+    constexpr bool qk = MAPS == 2;
     float araw = 1.f, b = 0.f;
     if (tid < C) {
         if (tok < n) {
@@ -450,7 +458,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     }
     bool ok = mbar_wait(&bar[1], 0);
     if (qk && ok) {  // thread t: row t of [Q; K]
-        const float in = silu_row<DK>(QK, tid, 128);
+        const float in = inv_l2(silu_cols<DK>(QK, tid, 128, 0));
         if (tid < C) inq[tid] = in;
         else ink[tok] = in;
         fence_async_smem();
@@ -631,8 +639,10 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         //      cols [0, 64); record rows 64..127 of the TZP tile get -Z' diag(kd')
         if (zprev) {
             ok = mbar_wait(&bar[2], 0) && ok;
-            if (qk && ok && tid < C) {
-                inkp[tid] = silu_row<DK>(QK, C + tid, 128);
+            if (qk && __all_sync(0xffffffffu, ok)) {  // two threads (adjacent lanes) per row, half the columns each
+                float ss = silu_cols<DK / 2>(QK, C + (tid >> 1), 128, (tid & 1) * (DK / 2));
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (!(tid & 1)) inkp[tid >> 1] = inv_l2(ss);
                 fence_async_smem();
             }
             ok = __syncthreads_and(ok ? 1 : 0) != 0;
@@ -1221,12 +1231,13 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
                          int T, int dv, const Fuse &fz, void *ws, cudaStream_t stream, int slot) {
     const int nblk = (T + C - 1) / C;
     // the maps that prep applies (the output RMSNorm runs after the scan)
-    const bool maps = (fz.flags & ~LR_FUSE_O_RMSNORM) != 0;
-    auto prep = maps ? chunk_prep_kernel<DK, ALPHA, DELTA, true>
-                     : chunk_prep_kernel<DK, ALPHA, DELTA, false>;
+    const int maps = (fz.flags & LR_FUSE_QK_SILU_L2) ? 2 : (fz.flags & ~LR_FUSE_O_RMSNORM) ? 1 : 0;
+    auto prep = maps == 2 ? chunk_prep_kernel<DK, ALPHA, DELTA, 2>
+                : maps == 1 ? chunk_prep_kernel<DK, ALPHA, DELTA, 1>
+                            : chunk_prep_kernel<DK, ALPHA, DELTA, 0>;
     auto scan = chunk_scan_kernel<DK, ALPHA, DELTA>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(prep), PrepLayout<DK>::ALLOC,
-                                     slot + (maps ? 24 : 0));
+                                     slot + 24 * maps);
     if (e != cudaSuccess) return e;
     e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC, slot + 12);
     if (e != cudaSuccess) return e;
@@ -1240,7 +1251,7 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
     e = make_rows_map(&tmv, v, dv, T, B * H);
     if (e != cudaSuccess) return e;
     // SiLU'd q and k in the workspace (the scan reads them instead)
-    const bool qk = (fz.flags & LR_FUSE_QK_SILU_L2) != 0;
+    const bool qk = maps == 2;
     const bf16 *qs = static_cast<const bf16 *>(q), *ks = static_cast<const bf16 *>(k);
     CUtensorMap tmqn = tmq, tmkn = tmk;
     if (qk) {
@@ -1292,7 +1303,7 @@ size_t chunked_tc_workspace_bytes(int B, int H, int T, int dk, unsigned flags) {
     return records_bytes(B, H, T, dk) + qk;
 }
 
-// Attribute slots 32..67 belong to this file.
+// Attribute slots 32..91 belong to this file.
 cudaError_t launch_chunked_tc(const void *q, const void *k, const void *v, const float *alpha,
                               const float *beta, const float *S0, void *o, float *S_T, int B,
                               int H, int T, int dk, int dv, lr_mode mode, const Fuse &fz,

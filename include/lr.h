@@ -263,10 +263,15 @@ typedef struct {
  * or S_T.
  *
  * bf16: the per-block pass applies the gate maps to the gates it reads, and
- * SiLU + L2 to the q and k tiles it stages; it writes the normalised q and k
- * (bf16, [B, H, T, dk] each) to the workspace, where the sequential pass
- * reads them instead of q and k (2 * B * H * T * dk * 2 more bytes of
- * workspace).  fp32: the single kernel applies the maps to what it stages.
+ * SiLU to the q and k tiles it stages (fp32 through the hardware tanh
+ * approximation, relative error about 2^-11, then one rounding to bf16); the
+ * rows' L2 norms are kept in fp32 and folded into the factors the products
+ * are scaled by, so the result is that of the normalised vectors.  It writes
+ * SiLU(q) and SiLU(k) (bf16, [B, H, T, dk] each) to the workspace, where the
+ * sequential pass reads them instead of q and k (2 * B * H * T * dk * 2 more
+ * bytes of workspace).  fp32: the single kernel applies the maps to what it
+ * stages, in fp32.  Rows whose sum of squares overflows fp32 (entries beyond
+ * about 1e19) normalise to zero.
  * With LR_FUSE_O_RMSNORM one more kernel normalises o in place (the value
  * channels of a head are split over several CTAs of the sequential pass, so
  * a token's full output first exists in memory).
