@@ -18,7 +18,10 @@ Three forms of the same result, each written from the pages:
   inside each block, the recurrent hand-off of the end-of-block state between
   blocks (second page, same section, chunkwise form).
 
-Mode numbers: 0 LINEAR, 1 DECAY, 2 DELTA, 3 GATED_DELTA.
+Mode numbers: 0 LINEAR, 1 DECAY, 2 DELTA, 3 GATED_DELTA, 4 DIAG_DECAY (the
+diagonal gate of GLA, first page, section "Dimenticare: i gate": alpha has one
+value per key channel, [B,H,T,dk]; :mod:`oracle.diag` holds its parallel and
+chunkwise forms).
 """
 from __future__ import annotations
 
@@ -28,10 +31,11 @@ import subprocess
 
 import numpy as np
 
-LINEAR, DECAY, DELTA, GATED_DELTA = 0, 1, 2, 3
-MODE_NAMES = {LINEAR: "linear", DECAY: "decay", DELTA: "delta", GATED_DELTA: "gated_delta"}
-USES_ALPHA = {LINEAR: False, DECAY: True, DELTA: False, GATED_DELTA: True}
-USES_BETA = {LINEAR: False, DECAY: False, DELTA: True, GATED_DELTA: True}
+LINEAR, DECAY, DELTA, GATED_DELTA, DIAG_DECAY = 0, 1, 2, 3, 4
+MODE_NAMES = {LINEAR: "linear", DECAY: "decay", DELTA: "delta", GATED_DELTA: "gated_delta",
+              DIAG_DECAY: "diag_decay"}
+USES_ALPHA = {LINEAR: False, DECAY: True, DELTA: False, GATED_DELTA: True, DIAG_DECAY: True}
+USES_BETA = {LINEAR: False, DECAY: False, DELTA: True, GATED_DELTA: True, DIAG_DECAY: False}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gdr_oracle.c")
@@ -84,8 +88,9 @@ def recurrent(mode, q, k, v, alpha=None, beta=None, S0=None, threads: int = 0):
     """Sequential definition of the recurrence, fp64.
 
     q, k: [B,H,T,dk]; v: [B,H,T,dv]; alpha, beta: [B,H,T] (only where the mode
-    uses them); S0: [B,H,dv,dk] or None for zeros.  Inputs of any float dtype
-    are widened exactly to float64.  Returns (o [B,H,T,dv], S_T [B,H,dv,dk]).
+    uses them; alpha is [B,H,T,dk] for DIAG_DECAY); S0: [B,H,dv,dk] or None
+    for zeros.  Inputs of any float dtype are widened exactly to float64.
+    Returns (o [B,H,T,dv], S_T [B,H,dv,dk]).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, T, dk = q.shape
@@ -93,9 +98,10 @@ def recurrent(mode, q, k, v, alpha=None, beta=None, S0=None, threads: int = 0):
     assert k.shape == (B, H, T, dk) and v.shape == (B, H, T, dv)
     a = _f64(alpha) if USES_ALPHA[mode] else None
     b = _f64(beta) if USES_BETA[mode] else None
-    for x in (a, b):
-        if x is not None:
-            assert x.shape == (B, H, T)
+    if a is not None:
+        assert a.shape == ((B, H, T, dk) if mode == DIAG_DECAY else (B, H, T))
+    if b is not None:
+        assert b.shape == (B, H, T)
     s0 = _f64(S0)
     if s0 is not None:
         assert s0.shape == (B, H, dv, dk)

@@ -20,6 +20,11 @@
  *   mode 3  GATED_DELTA  S_t = S_{t-1} [alpha_t (I - beta_t k_t k_t^T)]
  *                              + beta_t v_t k_t^T
  *           same page, section "Unire oblio e correzione: Gated DeltaNet".
+ *   mode 4  DIAG_DECAY   S_t = S_{t-1} Diag(alpha_t) + v_t k_t^T,
+ *                        alpha_t in (0,1)^dk, one gate per key channel
+ *           same page, section "Dimenticare: i gate", the GLA equation:
+ *           the diagonal multiplies from the right, so column c of S (key
+ *           channel c) decays by alpha_t[c].
  *
  * and the read-out o_t = S_t q_t with the state AFTER the update of token t
  * (opening section of the same page: "o_t = S_t q_t", S_t being the memory
@@ -34,7 +39,8 @@
  *   q, k   [B][H][T][dk]     v, o  [B][H][T][dv]
  *   alpha, beta  [B][H][T]   (ignored, and may be NULL, where the mode has
  *                             no such parameter: LINEAR ignores both, DECAY
- *                             ignores beta, DELTA ignores alpha)
+ *                             and DIAG_DECAY ignore beta, DELTA ignores alpha)
+ *   alpha for DIAG_DECAY     [B][H][T][dk]
  *   S0, ST [B][H][dv][dk]    rows are value channels, columns key channels
  *                             (o = S q); S0 == NULL means S_0 = 0.
  *
@@ -48,7 +54,7 @@
 #include <omp.h>
 #endif
 
-enum { OR_LINEAR = 0, OR_DECAY = 1, OR_DELTA = 2, OR_GATED_DELTA = 3 };
+enum { OR_LINEAR = 0, OR_DECAY = 1, OR_DELTA = 2, OR_GATED_DELTA = 3, OR_DIAG_DECAY = 4 };
 
 /* One sequence: T tokens of the chosen recurrence.  Scratch w has dv slots. */
 static void run_sequence(int mode, int T, int dk, int dv,
@@ -61,6 +67,7 @@ static void run_sequence(int mode, int T, int dk, int dv,
         const double *qt = q + (size_t)t * dk;
         const double *vt = v + (size_t)t * dv;
         const double a = (mode == OR_DECAY || mode == OR_GATED_DELTA) ? alpha[t] : 1.0;
+        const double *at = mode == OR_DIAG_DECAY ? alpha + (size_t)t * dk : NULL;
         const double b = (mode == OR_DELTA || mode == OR_GATED_DELTA) ? beta[t] : 1.0;
 
         /* w = S_{t-1} k_t : what the memory currently returns for k_t */
@@ -82,6 +89,9 @@ static void run_sequence(int mode, int T, int dk, int dv,
                     break;
                 case OR_DELTA:        /* S + beta (v - S k) k^T */
                     row[c] = row[c] + b * (vt[r] - w[r]) * kt[c];
+                    break;
+                case OR_DIAG_DECAY:   /* S Diag(alpha) + v k^T: column c scaled by alpha[c] */
+                    row[c] = row[c] * at[c] + vt[r] * kt[c];
                     break;
                 default:              /* alpha S - alpha beta (S k) k^T + beta v k^T */
                     row[c] = a * row[c] - a * b * w[r] * kt[c] + b * vt[r] * kt[c];
@@ -111,10 +121,10 @@ int gdr_oracle_recurrent(int mode, int B, int H, int T, int dk, int dv,
                          const double *S0, double *o, double *ST,
                          int num_threads)
 {
-    if (mode < OR_LINEAR || mode > OR_GATED_DELTA) return 1;
+    if (mode < OR_LINEAR || mode > OR_DIAG_DECAY) return 1;
     if (B <= 0 || H <= 0 || T < 0 || dk <= 0 || dv <= 0) return 1;
     if (!q || !k || !v || !o || !ST) return 1;
-    if ((mode == OR_DECAY || mode == OR_GATED_DELTA) && !alpha) return 1;
+    if ((mode == OR_DECAY || mode == OR_GATED_DELTA || mode == OR_DIAG_DECAY) && !alpha) return 1;
     if ((mode == OR_DELTA || mode == OR_GATED_DELTA) && !beta) return 1;
 
     const int BH = B * H;
@@ -140,7 +150,7 @@ int gdr_oracle_recurrent(int mode, int B, int H, int T, int dk, int dv,
         run_sequence(mode, T, dk, dv,
                      q + (size_t)bh * T * dk, k + (size_t)bh * T * dk,
                      v + (size_t)bh * T * dv,
-                     alpha ? alpha + (size_t)bh * T : NULL,
+                     alpha ? alpha + (size_t)bh * T * (mode == OR_DIAG_DECAY ? dk : 1) : NULL,
                      beta ? beta + (size_t)bh * T : NULL,
                      S, o + (size_t)bh * T * dv, w);
 
