@@ -15,7 +15,10 @@ rule"):
   section);
 * the scalar decay alpha_t is produced from the input in Mamba-2 (section
   "Dimenticare: i gate"); the page leaves its parametrisation open, so the two
-  used by the workloads are provided: sigmoid(a) and exp(-c softplus(a)).
+  used by the workloads are provided: sigmoid(a) and exp(-c softplus(a));
+* the diagonal gate of GLA (same section) is a sigmoid raised to 1/tau with
+  tau = 16 (a temperature that pushes the gates towards 1): sigmoid(a)^c,
+  c = 1/tau, applied per key channel.
 
 Each map takes the pre-activation values (after the projection, which is not
 part of this library) and returns the values the recurrence consumes.
@@ -32,6 +35,7 @@ BETA_SIGMOID = 2
 ALPHA_SIGMOID = 4
 ALPHA_SOFTPLUS = 8
 O_RMSNORM = 16
+ALPHA_SIGMOID_POW = 32
 
 L2_EPS = 1e-12   # x / max(||x||, eps): the pages give no epsilon
 RMS_EPS = 1e-6   # o / sqrt(mean(o^2) + eps): the pages give no epsilon
@@ -68,14 +72,25 @@ def silu_l2(x):
     return l2_normalise(silu(x))
 
 
+def _per_head(c, ndim):
+    c = np.asarray(c, dtype=np.float64)
+    if c.ndim == 1:
+        c = c.reshape((1, -1) + (1,) * (ndim - 2))
+    return c
+
+
+def sigmoid_pow_gate(a, c):
+    """alpha = sigmoid(a)^c (GLA: c = 1/tau).  `a` is [B, H, T(, dk)] or
+    [N, H(, dk)]; `c` a scalar or one value per head [H]."""
+    a = np.asarray(a, dtype=np.float64)
+    return np.exp(-_per_head(c, a.ndim) * softplus(-a))
+
+
 def softplus_gate(a, c):
     """alpha = exp(-c softplus(a)), in (0, 1) for c > 0.  `a` is [B, H, T]
     (prefill) or [N, H] (decode); `c` a scalar or one value per head [H]."""
     a = np.asarray(a, dtype=np.float64)
-    c = np.asarray(c, dtype=np.float64)
-    if c.ndim == 1:
-        c = c.reshape((1, -1) + (1,) * (a.ndim - 2))
-    return np.exp(-c * softplus(a))
+    return np.exp(-_per_head(c, a.ndim) * softplus(a))
 
 
 def rmsnorm(o, weight=None, eps=RMS_EPS):
@@ -102,6 +117,8 @@ def apply_prologue(flags, q, k, alpha, beta, alpha_scale=1.0):
             alpha = sigmoid(alpha)
         elif flags & ALPHA_SOFTPLUS:
             alpha = softplus_gate(alpha, alpha_scale)
+        elif flags & ALPHA_SIGMOID_POW:
+            alpha = sigmoid_pow_gate(alpha, alpha_scale)
     if beta is not None:
         beta = np.asarray(beta, dtype=np.float64)
         if flags & BETA_SIGMOID:

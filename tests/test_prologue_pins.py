@@ -56,6 +56,14 @@ def pin_softplus_gate():
     # one value of c per head: [B, H, T] gates, c of shape [H]
     g = P.softplus_gate(np.zeros((1, 3, 2)), np.array([1.0, 2.0, 3.0]))
     ok &= np.allclose(g[0, :, 0], [0.5, 0.25, 0.125], rtol=0, atol=1e-15)
+    # GLA's gate sigmoid(a)^(1/tau): at a = 0 it is 2^(-1/tau); at a = ln 3 it is (3/4)^(1/tau);
+    # per key channel ([B, H, T, dk]) with c per head
+    tau = 16.0
+    ok &= abs(P.sigmoid_pow_gate(0.0, 1 / tau) - 2.0 ** (-1 / tau)) < 1e-15
+    ok &= abs(P.sigmoid_pow_gate(math.log(3.0), 1 / tau) - 0.75 ** (1 / tau)) < 1e-15
+    gd = P.sigmoid_pow_gate(np.zeros((1, 2, 3, 4)), np.array([1.0, 0.5]))
+    ok &= np.allclose(gd[0, 0], 0.5, rtol=0, atol=1e-15) and np.allclose(gd[0, 1], 0.5 ** 0.5, rtol=0,
+                                                                            atol=1e-15)
     return bool(ok)
 
 
@@ -186,6 +194,9 @@ MISTAKES = {
     "rms_sum": ("rmsnorm", lambda o, weight=None, eps=P.RMS_EPS: (
         np.asarray(o, float) / np.sqrt(np.sum(np.asarray(o, float) ** 2, axis=-1, keepdims=True) + eps)
         * (1.0 if weight is None else np.asarray(weight, float)))),
+    # GLA gate with the power applied outside the wrong way
+    "pow_inverse": ("sigmoid_pow_gate", lambda a, c: P.sigmoid(a) ** (1.0 / np.asarray(c, float))
+                    if np.ndim(c) == 0 else P.sigmoid(a)),
     # softplus gate with the sign of c flipped
     "gate_sign": ("softplus_gate", lambda a, c: np.exp(np.asarray(c, float).reshape(
         (1, -1) + (1,) * (np.ndim(a) - 2)) * P.softplus(a) if np.ndim(c) == 1 else c * P.softplus(a))),
