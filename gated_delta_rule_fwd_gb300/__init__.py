@@ -22,8 +22,9 @@ import os
 
 from .build import LIB_PATH
 
-LINEAR, DECAY, DELTA, GATED_DELTA = 0, 1, 2, 3
-MODES = {"linear": LINEAR, "decay": DECAY, "delta": DELTA, "gated_delta": GATED_DELTA}
+LINEAR, DECAY, DELTA, GATED_DELTA, DIAG_DECAY = 0, 1, 2, 3, 4
+MODES = {"linear": LINEAR, "decay": DECAY, "delta": DELTA, "gated_delta": GATED_DELTA,
+         "diag_decay": DIAG_DECAY}
 F32, BF16 = 0, 1
 SYMBOLS = ("lr_fwd_chunked", "lr_fwd_chunked_workspace_size", "lr_fwd_chunked_noalloc", "lr_step",
            "lr_fwd_chunked_fused", "lr_fwd_chunked_fused_workspace_size", "lr_step_fused",
@@ -34,12 +35,18 @@ FUSE_BETA_SIGMOID = 0x2
 FUSE_ALPHA_SIGMOID = 0x4
 FUSE_ALPHA_SOFTPLUS = 0x8
 FUSE_O_RMSNORM = 0x10
+FUSE_ALPHA_SIGMOID_POW = 0x20
 STATIC_WORKSPACE_BYTES = 64 << 20   # LR_STATIC_WORKSPACE_BYTES
 STATUS = {0: "LR_OK", 1: "LR_ERR_NULL", 2: "LR_ERR_SHAPE", 3: "LR_ERR_DTYPE", 4: "LR_ERR_ALIGN",
           5: "LR_ERR_MODE", 6: "LR_ERR_UNSUPPORTED", 7: "LR_ERR_CUDA", 8: "LR_ERR_ALIAS",
           9: "LR_ERR_TIMEOUT", 10: "LR_ERR_WORKSPACE", 11: "LR_ERR_TOO_LARGE", 12: "LR_ERR_FUSE"}
-_USES_ALPHA = {LINEAR: False, DECAY: True, DELTA: False, GATED_DELTA: True}
-_USES_BETA = {LINEAR: False, DECAY: False, DELTA: True, GATED_DELTA: True}
+_USES_ALPHA = {LINEAR: False, DECAY: True, DELTA: False, GATED_DELTA: True, DIAG_DECAY: True}
+_USES_BETA = {LINEAR: False, DECAY: False, DELTA: True, GATED_DELTA: True, DIAG_DECAY: False}
+
+
+def _alpha_shape(mode, lead, dk):
+    """alpha has one value per token, or one per key channel for DIAG_DECAY."""
+    return tuple(lead) + ((dk,) if mode == DIAG_DECAY else ())
 
 
 class Fuse(ctypes.Structure):
@@ -150,7 +157,8 @@ def lr_fwd_chunked(q, k, v, alpha=None, beta=None, S0=None, *, mode=GATED_DELTA,
     """Chunkwise forward (see ``lr_fwd_chunked`` in include/lr.h).
 
     q, k: [B,H,T,dk]; v: [B,H,T,dv] (float32 or bfloat16, same dtype);
-    alpha, beta: [B,H,T] float32 where the mode uses them; S0: [B,H,dv,dk]
+    alpha, beta: [B,H,T] float32 where the mode uses them (alpha [B,H,T,dk]
+    for DIAG_DECAY); S0: [B,H,dv,dk]
     float32 or None.  ``o`` and ``S_T`` may be given to write into (``S_T``
     may be ``S0``).  ``workspace`` is a uint8 CUDA tensor of at least
     ``workspace_size(...)`` bytes; when None one is allocated through the
@@ -168,7 +176,7 @@ def lr_fwd_chunked(q, k, v, alpha=None, beta=None, S0=None, *, mode=GATED_DELTA,
     _check(k, "k", (B, H, T, dk), q.dtype, dev)
     _check(v, "v", (B, H, T, dv), q.dtype, dev)
     if _USES_ALPHA[mode]:
-        _check(alpha, "alpha", (B, H, T), torch.float32, dev)
+        _check(alpha, "alpha", _alpha_shape(mode, (B, H, T), dk), torch.float32, dev)
     else:
         alpha = None
     if _USES_BETA[mode]:
@@ -221,7 +229,7 @@ def lr_fwd_chunked_noalloc(q, k, v, alpha=None, beta=None, S0=None, *, mode=GATE
     alpha = alpha if _USES_ALPHA[mode] else None
     beta = beta if _USES_BETA[mode] else None
     if alpha is not None:
-        _check(alpha, "alpha", (B, H, T), torch.float32, dev)
+        _check(alpha, "alpha", _alpha_shape(mode, (B, H, T), dk), torch.float32, dev)
     if beta is not None:
         _check(beta, "beta", (B, H, T), torch.float32, dev)
     if S0 is not None:
@@ -242,7 +250,7 @@ def lr_step(q, k, v, alpha, beta, S, *, mode=GATED_DELTA, o=None, stream=None):
     """One decode step (see ``lr_step`` in include/lr.h); S is updated in place.
 
     q, k: [N,H,dk]; v: [N,H,dv]; alpha, beta: [N,H] float32 where the mode
-    uses them; S: [N,H,dv,dk] float32.  Returns o: [N,H,dv].
+    uses them (alpha [N,H,dk] for DIAG_DECAY); S: [N,H,dv,dk] float32.  Returns o: [N,H,dv].
     """
     import torch
     mode = MODES.get(mode, mode)
@@ -256,7 +264,7 @@ def lr_step(q, k, v, alpha, beta, S, *, mode=GATED_DELTA, o=None, stream=None):
     _check(k, "k", (N, H, dk), q.dtype, dev)
     _check(v, "v", (N, H, dv), q.dtype, dev)
     if _USES_ALPHA[mode]:
-        _check(alpha, "alpha", (N, H), torch.float32, dev)
+        _check(alpha, "alpha", _alpha_shape(mode, (N, H), dk), torch.float32, dev)
     else:
         alpha = None
     if _USES_BETA[mode]:
@@ -318,7 +326,7 @@ def lr_fwd_chunked_fused(q, k, v, alpha=None, beta=None, S0=None, *, mode=GATED_
     alpha = alpha if _USES_ALPHA[mode] else None
     beta = beta if _USES_BETA[mode] else None
     if alpha is not None:
-        _check(alpha, "alpha", (B, H, T), torch.float32, dev)
+        _check(alpha, "alpha", _alpha_shape(mode, (B, H, T), dk), torch.float32, dev)
     if beta is not None:
         _check(beta, "beta", (B, H, T), torch.float32, dev)
     if S0 is not None:
@@ -365,7 +373,7 @@ def lr_step_fused(q, k, v, alpha, beta, S, *, mode=GATED_DELTA, flags=0, alpha_s
     alpha = alpha if _USES_ALPHA[mode] else None
     beta = beta if _USES_BETA[mode] else None
     if alpha is not None:
-        _check(alpha, "alpha", (N, H), torch.float32, dev)
+        _check(alpha, "alpha", _alpha_shape(mode, (N, H), dk), torch.float32, dev)
     if beta is not None:
         _check(beta, "beta", (N, H), torch.float32, dev)
     _check(S, "S", (N, H, dv, dk), torch.float32, dev)

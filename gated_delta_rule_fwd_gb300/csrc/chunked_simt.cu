@@ -83,8 +83,8 @@ chunk_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     const int c0 = blockIdx.x * DVS;
     const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
     const unsigned fl = fz.flags;
-    const bool amap = (fl & (LR_FUSE_ALPHA_SIGMOID | LR_FUSE_ALPHA_SOFTPLUS)) != 0;
-    const float ac = (ALPHA && (fl & LR_FUSE_ALPHA_SOFTPLUS)) ? fz.ascale[blockIdx.y] : 0.f;
+    const bool amap = (fl & kAlphaMaps) != 0;
+    const float ac = (ALPHA && (fl & kScaledAlphaMaps)) ? fz.ascale[blockIdx.y] : 0.f;
 
     for (int idx = tid; idx < DVS * DK; idx += NT) {
         const int c = idx / DK, j = idx % DK;
@@ -241,6 +241,186 @@ chunk_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     }
 }
 
+// ---------------------------------------------------------- diagonal gate
+// The GLA row (page "Scrivere meglio nella memoria: gate e delta rule",
+// section "Dimenticare: i gate"): S_t = S_{t-1} Diag(alpha_t) + v_t k_t^T with
+// one gate per key channel.  Inside a block, G_r[c] = sum_{i<=r} ln alpha_i[c]
+// (per channel), and
+//   O   = (Q * e^G) S^T + P V,       P_ri = sum_c q_r[c] k_i[c] e^{G_r[c] - G_i[c]}, i <= r
+//   S  <- S Diag(e^{G_last}) + V^T (K * e^{G_last - G}).
+// The scores use a second level of 16-token blocks (the summary of the same
+// page: GLA needs it for numerical stability): for the key sub-block J,
+//   P[:, J] = (Q * e^{G - G_e}) (K_J * e^{G_e - G_J})^T,  G_e = G at the last token of J,
+// where the key factor is <= 1 and the query factor is <= 1 for rows after J
+// and at most e^80 (clamped) for rows inside J.
+template <int DK>
+struct DiagSmem {
+    static constexpr int KP = DK + 1, PP = C + 1;
+    static constexpr int kK = 0;                // K, then K * e^{G_last - G}
+    static constexpr int kQ = kK + C * KP;      // Q, then Q * e^G
+    static constexpr int kS = kQ + C * KP;      // state slice [DVS][KP]
+    static constexpr int kV = kS + DVS * KP;    // V slice [C][DVS]
+    static constexpr int kP = kV + C * DVS;     // P [C][PP]
+    static constexpr int kG = kP + C * PP;      // G [C][KP]
+    static constexpr int kQh = kG + C * KP;     // query factors of one key sub-block
+    static constexpr int kKh = kQh + C * KP;    // K * e^{G_e - G}
+    static constexpr int floats = kKh + C * KP;
+    static constexpr int bytes = floats * 4;
+};
+constexpr int kSub = 16;
+
+template <int DK, typename Tin>
+__global__ void __launch_bounds__(NT)
+chunk_simt_diag_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
+                       const Tin *__restrict__ v, const float *__restrict__ alpha,
+                       const float *__restrict__ S0, Tin *__restrict__ o, float *__restrict__ ST,
+                       int H, int T, int dv, const Fuse fz) {
+    using L = DiagSmem<DK>;
+    constexpr int KP = L::KP, PP = L::PP;
+    extern __shared__ float sm[];
+    float *Ks = sm + L::kK, *Qs = sm + L::kQ, *Ss = sm + L::kS, *Vs = sm + L::kV;
+    float *Ps = sm + L::kP, *Gs = sm + L::kG, *Qh = sm + L::kQh, *Kh = sm + L::kKh;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c0 = blockIdx.x * DVS;
+    const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
+    const unsigned fl = fz.flags;
+    const float ac = (fl & kScaledAlphaMaps) ? fz.ascale[blockIdx.y] : 0.f;
+
+    for (int idx = tid; idx < DVS * DK; idx += NT) {
+        const int c = idx / DK, j = idx % DK;
+        Ss[c * KP + j] = S0 ? S0[(bh * dv + c0 + c) * DK + j] : 0.f;
+    }
+
+    for (int t0 = 0; t0 < T; t0 += C) {
+        const int n = min(C, T - t0);
+        __syncthreads();  // the previous block is done with every buffer
+
+        // ---- stage the block: q, k, v, ln alpha (zero past the end)
+        for (int idx = tid; idx < C * DK; idx += NT) {
+            const int r = idx / DK, j = idx % DK;
+            const bool ok = r < n;
+            const size_t g = (bh * T + t0 + r) * DK + j;
+            Ks[r * KP + j] = ok ? to_f(k[g]) : 0.f;
+            Qs[r * KP + j] = ok ? to_f(q[g]) : 0.f;
+            float la = 0.f;
+            if (ok) {
+                const float a = alpha[g];
+                la = (fl & kAlphaMaps) ? log_gate(fl, a, ac) : logf(a);
+            }
+            Gs[r * KP + j] = la;
+        }
+        for (int idx = tid; idx < C * DVS; idx += NT) {
+            const int r = idx / DVS, c = idx % DVS;
+            Vs[r * DVS + c] = r < n ? to_f(v[(bh * T + t0 + r) * dv + c0 + c]) : 0.f;
+        }
+        __syncthreads();
+
+        // ---- cumulative log gates per channel; SiLU + L2 of the q and k rows
+        if (tid < DK) {
+            float acc = 0.f;
+            for (int r = 0; r < C; ++r) {
+                acc += Gs[r * KP + tid];
+                Gs[r * KP + tid] = acc;
+            }
+        } else if (fl & LR_FUSE_QK_SILU_L2) {
+            // the warps past the first DK threads normalise the rows meanwhile
+            for (int rr = warp - DK / 32; rr < 2 * C; rr += NT / 32 - DK / 32) {
+                float *row = rr < C ? Qs + rr * KP : Ks + (rr - C) * KP;
+                float x[DK / 32];
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < DK / 32; ++e) {
+                    x[e] = silu_f(row[lane + 32 * e]);
+                    ss += x[e] * x[e];
+                }
+#pragma unroll
+                for (int d = 16; d >= 1; d >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, d);
+                const float inv = inv_l2(ss);
+#pragma unroll
+                for (int e = 0; e < DK / 32; ++e) row[lane + 32 * e] = x[e] * inv;
+            }
+        }
+        __syncthreads();
+
+        // ---- key factors K * e^{G_e - G} (G_e: last token of the key's sub-block)
+        for (int idx = tid; idx < C * DK; idx += NT) {
+            const int i = idx / DK, j = idx % DK;
+            const int e = (i | (kSub - 1));
+            Kh[i * KP + j] = Ks[i * KP + j] * __expf(Gs[e * KP + j] - Gs[i * KP + j]);
+        }
+        // ---- scores, one key sub-block at a time
+        for (int J = 0; J < C / kSub; ++J) {
+            const int e = J * kSub + kSub - 1, r0 = J * kSub;
+            for (int idx = tid; idx < (C - r0) * DK; idx += NT) {
+                const int r = r0 + idx / DK, j = idx % DK;
+                Qh[r * KP + j] = Qs[r * KP + j] * __expf(fminf(Gs[r * KP + j] - Gs[e * KP + j], 80.f));
+            }
+            __syncthreads();
+            for (int idx = tid; idx < C * kSub; idx += NT) {
+                const int r = idx / kSub, i = r0 + idx % kSub;
+                float p = 0.f;
+                if (i <= r) {
+#pragma unroll 8
+                    for (int j = 0; j < DK; ++j) p += Qh[r * KP + j] * Kh[i * KP + j];
+                }
+                Ps[r * PP + i] = p;
+            }
+            __syncthreads();
+        }
+
+        // ---- Q * e^G and K * e^{G_last - G}
+        for (int idx = tid; idx < C * DK; idx += NT) {
+            const int r = idx / DK, j = idx % DK;
+            const float G = Gs[r * KP + j], Gl = Gs[(C - 1) * KP + j];
+            Qs[r * KP + j] *= __expf(G);
+            Ks[r * KP + j] *= __expf(Gl - G);
+        }
+        __syncthreads();
+
+        // ---- output O = (Q * e^G) S^T + P V  (S still the block's initial state)
+        for (int idx = tid; idx < C * DVS; idx += NT) {
+            const int r = idx / DVS, c = idx % DVS;
+            if (r >= n) continue;
+            float qs = 0.f;
+#pragma unroll 8
+            for (int j = 0; j < DK; ++j) qs += Qs[r * KP + j] * Ss[c * KP + j];
+            float pv = 0.f;
+            for (int i = 0; i <= r; ++i) pv += Ps[r * PP + i] * Vs[i * DVS + c];
+            o[(bh * T + t0 + r) * dv + c0 + c] = from_f<Tin>(qs + pv);
+        }
+        __syncthreads();
+
+        // ---- carry S <- S Diag(e^{G_last}) + V^T (K * e^{G_last - G})
+        for (int idx = tid; idx < DVS * DK; idx += NT) {
+            const int c = idx / DK, j = idx % DK;
+            float acc = 0.f;
+#pragma unroll 8
+            for (int i = 0; i < C; ++i) acc += Vs[i * DVS + c] * Ks[i * KP + j];
+            Ss[c * KP + j] = __expf(Gs[(C - 1) * KP + j]) * Ss[c * KP + j] + acc;
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < DVS * DK; idx += NT) {
+        const int c = idx / DK, j = idx % DK;
+        ST[(bh * dv + c0 + c) * DK + j] = Ss[c * KP + j];
+    }
+}
+
+template <int DK, typename Tin>
+cudaError_t launch_diag(const void *q, const void *k, const void *v, const float *alpha,
+                        const float *S0, void *o, float *S_T, int B, int H, int T, int dv,
+                        const Fuse &fz, cudaStream_t stream, int slot) {
+    auto fn = chunk_simt_diag_kernel<DK, Tin>;
+    const int bytes = DiagSmem<DK>::bytes;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(fn), bytes, slot);
+    if (e != cudaSuccess) return e;
+    fn<<<dim3(dv / DVS, H, B), NT, bytes, stream>>>(
+        static_cast<const Tin *>(q), static_cast<const Tin *>(k), static_cast<const Tin *>(v),
+        alpha, S0, static_cast<Tin *>(o), S_T, H, T, dv, fz);
+    return cudaGetLastError();
+}
+
 template <int DK, typename Tin, bool ALPHA, bool DELTA>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *alpha,
                          const float *beta, const float *S0, void *o, float *S_T, int B, int H,
@@ -271,6 +451,9 @@ cudaError_t launch_mode(const void *q, const void *k, const void *v, const float
     case LR_MODE_DELTA:
         return launch_typed<DK, Tin, false, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T,
                                                   dv, fz, stream, slot + 2);
+    case LR_MODE_DIAG_DECAY:
+        return launch_diag<DK, Tin>(q, k, v, alpha, S0, o, S_T, B, H, T, dv, fz, stream,
+                                    slot + 96);
     default:
         return launch_typed<DK, Tin, true, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv,
                                                  fz, stream, slot + 3);
@@ -297,7 +480,7 @@ cudaError_t launch_dk(const void *q, const void *k, const void *v, const float *
 
 }  // namespace
 
-// Attribute slots 0..23 belong to this file.
+// Attribute slots 0..23 and 96..119 (diagonal gate) belong to this file.
 cudaError_t launch_chunked_simt(const void *q, const void *k, const void *v, const float *alpha,
                                 const float *beta, const float *S0, void *o, float *S_T, int B,
                                 int H, int T, int dk, int dv, lr_dtype dt, lr_mode mode,

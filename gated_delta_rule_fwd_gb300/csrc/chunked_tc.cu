@@ -107,6 +107,7 @@ struct Rec {
 };
 // offsets (in floats) inside the gate vector of a record
 constexpr int kVgPrev = 0, kVkdPrev = 64, kVkd = 128, kVgCPrev = 192;
+constexpr int kVgCDiag = 128;  // diagonal gate: g_C' per key channel (128 floats)
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
@@ -404,7 +405,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     float la = ALPHA ? __logf(araw) : 0.f;
     if (MAPS) {
         const bool has_a = ALPHA && (tid < C ? tok < n : blk > 0);
-        la = has_a ? log_gate(fl, araw, (fl & LR_FUSE_ALPHA_SOFTPLUS) ? fz.ascale[blockIdx.y] : 0.f)
+        la = has_a ? log_gate(fl, araw, (fl & kScaledAlphaMaps) ? fz.ascale[blockIdx.y] : 0.f)
                    : 0.f;
     }
     if (warp == 0) {
@@ -693,6 +694,217 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
+// ============================================================ diagonal gate
+// The GLA row (page "Scrivere meglio nella memoria: gate e delta rule",
+// section "Dimenticare: i gate"): S_t = S_{t-1} Diag(alpha_t) + v_t k_t^T, one
+// gate per key channel.  With G_r[c] the cumulative log gate of the block,
+//   O = (Q * e^G) S^T + P V,   P_ri = sum_c q_r[c] k_i[c] e^{G_r[c] - G_i[c]} (i <= r),
+//   S <- S Diag(e^{G_last}) + V^T (K * e^{G_last - G}).
+// So the scan is the one without delta, reading Q * e^G and K * e^{G_last - G}
+// (prepared here, to the workspace) in place of q and k, with unit g and kd and
+// a per-key-channel g_C for the state.  The scores use the second level of
+// blocks GLA needs for stability (summary of the same page): for key sub-block
+// J (16 tokens, last token e), P[:, J] = (Q * e^{G - G_e}) (K_J * e^{G_e - G_J})^T,
+// four tcgen05 products of M = 64, N = 16, one per J, into one 64-column
+// accumulator.  The key factors are <= 1; the query factors are <= 1 after J
+// and at most e^80 (clamped) inside J.  All factors are products of the gates
+// (prefix products along the tokens), one thread per key channel.
+template <int DK>
+struct DiagPrepLayout {
+    static constexpr int KB = (DK + 63) / 64;
+    static constexpr int TILE = KB * 8192;          // [64 rows][DK] bf16, K-major, 128-byte swizzle
+    static constexpr int QT = 0;                     // q, then q * e^G (to the workspace)
+    static constexpr int KT = QT + TILE;             // k, then k * e^{G_last - G} (to the workspace)
+    static constexpr int QH = KT + TILE;             // query factors of one key sub-block
+    static constexpr int KH = QH + TILE;             // k * e^{G_e - G}
+    static constexpr int NRM = KH + TILE;            // fp32 1/|q| [64], 1/|k| [64] (SiLU + L2)
+    static constexpr int BAR = NRM + 512;            // 2 barriers, TMEM slot
+    static constexpr int BYTES = BAR + 64;
+    static constexpr int ALLOC = BYTES + 1024;
+};
+
+template <int DK, bool QKN>
+__global__ void __launch_bounds__(NT)
+chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws, int H, int T,
+                       int nblk, const __grid_constant__ CUtensorMap tmq,
+                       const __grid_constant__ CUtensorMap tmk, const Fuse fz,
+                       const __grid_constant__ CUtensorMap tmqn,
+                       const __grid_constant__ CUtensorMap tmkn) {
+    using L = DiagPrepLayout<DK>;
+    using R = Rec<DK>;
+    constexpr int NS = C / 16;  // key sub-blocks
+    extern __shared__ uint8_t sm_raw[];
+    uint8_t *sm = align1024(sm_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int blk = blockIdx.x;
+    const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
+    const int t0 = blk * C;
+    const int n = min(C, T - t0);
+    uint8_t *rec = ws + (bh * (nblk + 1) + blk) * (size_t)R::BYTES;
+    uint8_t *rec_next = rec + R::BYTES;
+    uint8_t *QT = sm + L::QT, *KT = sm + L::KT, *QH = sm + L::QH, *KH = sm + L::KH;
+    float *inq = reinterpret_cast<float *>(sm + L::NRM), *ink = inq + 64;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);  // q/k tiles, products
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 16);
+    const unsigned fl = fz.flags;
+    const int c = tid;  // key channel of this thread (threads >= DK have none)
+
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+        mbar_expect_tx(&bar[0], 2u * (uint32_t)L::KB * 8192u);
+#pragma unroll
+        for (int kb = 0; kb < L::KB; ++kb) {
+            tma_load_3d(QT + kb * 8192, &tmq, kb * 64, t0, (int)bh, &bar[0]);
+            tma_load_3d(KT + kb * 8192, &tmk, kb * 64, t0, (int)bh, &bar[0]);
+        }
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 64);
+        tmem_relinquish();
+    }
+    // this channel's gates of the block (1 past the end of the sequence)
+    float a[C];
+    if (c < DK) {
+        const float ac = (fl & kScaledAlphaMaps) ? fz.ascale[blockIdx.y] : 0.f;
+#pragma unroll
+        for (int r = 0; r < C; ++r) {
+            float x = 1.f;
+            if (r < n) {
+                x = alpha[(bh * T + t0 + r) * DK + c];
+                if (fl & kAlphaMaps) x = gate(fl, x, ac);
+            }
+            a[r] = x;
+        }
+    }
+    bool ok = mbar_wait(&bar[0], 0);
+    if (QKN && ok) {  // SiLU of the q and k rows in place; their inverse norms
+        const float in = inv_l2(silu_cols<DK>(tid < C ? QT : KT, tid & 63, 64, 0));
+        if (tid < C) inq[tid] = in;
+        else ink[tid - C] = in;
+    }
+    tc_fence_before();
+    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto ld = [&](const uint8_t *t, int r) {
+        return __bfloat162float(*reinterpret_cast<const bf16 *>(t + sw128_offset(r, c, 64)));
+    };
+    auto st = [&](uint8_t *t, int r, float x) {
+        *reinterpret_cast<bf16 *>(t + sw128_offset(r, c, 64)) = __float2bfloat16_rn(x);
+    };
+
+    // ---- keys: K * e^{G_e - G} (sub-block suffix products) and K * e^{G_last - G}
+    float gC = 1.f;
+    if (ok && c < DK) {
+        float s_sub = 1.f;
+#pragma unroll
+        for (int r = C - 1; r >= 0; --r) {
+            if ((r & 15) == 15) s_sub = 1.f;
+            float kv = ld(KT, r);
+            if (QKN) kv *= ink[r];
+            st(KH, r, kv * s_sub);
+            st(KT, r, kv * gC);
+            s_sub *= a[r];
+            gC *= a[r];
+        }
+    }
+    // ---- scores, one key sub-block per product (unrolled: a[] stays in registers)
+#pragma unroll
+    for (int J = 0; J < NS; ++J) {
+        if (!ok) break;
+        const int e = 16 * J + 15;
+        if (c < DK) {
+            float s = 1.f;  // rows inside J: e^{G_r - G_e} = 1 / prod_{r < j <= e} alpha_j
+#pragma unroll
+            for (int r = 15; r >= 0; --r) {
+                const int rr = 16 * J + r;
+                float qv = ld(QT, rr);
+                if (QKN) qv *= inq[rr];
+                st(QH, rr, qv * fminf(__frcp_rn(s), 5.5e34f));
+                s *= a[rr];
+            }
+            float p = 1.f;  // rows after J: prod_{e < j <= r} alpha_j
+#pragma unroll
+            for (int rr = e + 1; rr < C; ++rr) {
+                p *= a[rr];
+                float qv = ld(QT, rr);
+                if (QKN) qv *= inq[rr];
+                st(QH, rr, qv * p);
+            }
+            if (J == NS - 1) {  // q * e^G in place (the raw rows are no longer needed)
+                float g = 1.f;
+#pragma unroll
+                for (int r = 0; r < C; ++r) {
+                    g *= a[r];
+                    float qv = ld(QT, r);
+                    if (QKN) qv *= inq[r];
+                    st(QT, r, qv * g);
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            const uint32_t id = idesc_bf16_f32(64, 16);
+#pragma unroll
+            for (int ks = 0; ks < DK / 16; ++ks)
+                mma_bf16(tmem + 16 * J, tile_desc(smem_u32(QH), 64, 0, ks),
+                         tile_desc(smem_u32(KH), 64, 16 * J, ks), id, ks > 0);
+            mma_commit(&bar[1]);
+        }
+        ok = __syncthreads_and(mbar_wait(&bar[1], J & 1) ? 1 : 0) != 0;  // QH may be rewritten
+        tc_fence_after();
+    }
+    // ---- the transformed q and k rows -> workspace (rows past T are not written)
+    if (tid == 0 && ok) {
+#pragma unroll
+        for (int kb = 0; kb < L::KB; ++kb) {
+            tma_store_3d(&tmqn, QT + kb * 8192, kb * 64, t0, (int)bh);
+            tma_store_3d(&tmkn, KT + kb * 8192, kb * 64, t0, (int)bh);
+        }
+        bulk_commit();
+    }
+    // ---- P rows (M = 64: rows 16w..16w+15 in lanes 32w..32w+15) -> record j+1
+    if (ok) {
+        const int r = 16 * warp + lane;
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float x[32];
+            tmem_ld32(tmem + lane_base + 32 * half, x);
+            tmem_ld_wait();
+            if (lane < 16) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (half * 32 + e > r) x[e] = 0.f;
+#pragma unroll
+                for (int i8 = 0; i8 < 4; ++i8)
+                    *reinterpret_cast<uint4 *>(rec_next + R::TZP +
+                                               sw128_offset(128 + r, half * 32 + i8 * 8, 192)) =
+                        pack8(x + i8 * 8);
+            }
+        }
+    }
+    // ---- gate vectors: unit g' and kd' (folded above), per-channel g_C
+    float *vn = reinterpret_cast<float *>(rec_next + R::VEC);
+    if (tid < 2 * C) vn[tid] = 1.f;
+    if (c < DK) vn[128 + c] = gC;
+    if (blk == 0) {  // stage 0 has no previous block
+        float *v0 = reinterpret_cast<float *>(rec + R::VEC);
+        if (tid < 2 * C) v0[tid] = 1.f;
+        if (c < DK) v0[128 + c] = 1.f;
+    }
+    if (!ok && lane == 0) atomicExch(&g_tc_error, 1);
+    if (tid == 0) bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
 // ===================================================================== scan
 
 template <int DK>
@@ -792,7 +1004,7 @@ struct ScanBars {
 static_assert(sizeof(ScanBars) <= 256, "the barriers must fit their shared-memory slot");
 constexpr uint32_t kEmptyLCount = 2 + 4 + 4 + 8;  // both issuers' commits, U, output and state warps
 
-template <int DK, bool ALPHA, bool DELTA>
+template <int DK, bool ALPHA, bool DELTA, bool DIAG = false>
 __global__ void __launch_bounds__(kScanThreads, 1)
 chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                   bf16 *__restrict__ o, float *__restrict__ ST, int H, int T, int dv, int nblk,
@@ -1146,7 +1358,8 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
             ok = __all_sync(0xffffffffu, mbar_wait(&bars->fullL[p], ph));
             if (!ok) break;
-            const float gC = vec_of(p)[kVgCPrev];  // the only late-group value read here
+            // the only late-group value read here: g_C', per key channel with the diagonal gate
+            const float gC = DIAG ? vec_of(p)[kVgCDiag + (kc & 127)] : vec_of(p)[kVgCPrev];
             if (DELTA) warp_arrive(&bars->emptyL[p]);
             ok = __all_sync(0xffffffffu, mbar_wait(&bars->dsf[p], ph));
             if (!ok) break;
@@ -1225,6 +1438,39 @@ size_t records_bytes(int B, int H, int T, int dk) {
     return (size_t)B * H * (nblk + 1) * rec;
 }
 
+// The diagonal gate: the GLA prep, then the scan without delta reading the
+// transformed q and k from the workspace.
+template <int DK>
+cudaError_t launch_diag(const void *q, const void *k, const void *v, const float *alpha,
+                        const float *S0, void *o, float *S_T, int B, int H, int T, int dv,
+                        const Fuse &fz, void *ws, cudaStream_t stream, int slot) {
+    const int nblk = (T + C - 1) / C;
+    const bool qk = (fz.flags & LR_FUSE_QK_SILU_L2) != 0;
+    auto prep = qk ? chunk_prep_diag_kernel<DK, true> : chunk_prep_diag_kernel<DK, false>;
+    auto scan = chunk_scan_kernel<DK, true, false, true>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(prep),
+                                     DiagPrepLayout<DK>::ALLOC, slot + (qk ? 1 : 0));
+    if (e != cudaSuccess) return e;
+    e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC, slot + 2);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tmq, tmk, tmv, tmqn, tmkn;
+    bf16 *qn = reinterpret_cast<bf16 *>(static_cast<uint8_t *>(ws) + records_bytes(B, H, T, DK));
+    bf16 *kn = qn + (size_t)B * H * T * DK;
+    if ((e = make_rows_map(&tmq, q, DK, T, B * H)) != cudaSuccess) return e;
+    if ((e = make_rows_map(&tmk, k, DK, T, B * H)) != cudaSuccess) return e;
+    if ((e = make_rows_map(&tmv, v, dv, T, B * H)) != cudaSuccess) return e;
+    if ((e = make_rows_map(&tmqn, qn, DK, T, B * H)) != cudaSuccess) return e;
+    if ((e = make_rows_map(&tmkn, kn, DK, T, B * H)) != cudaSuccess) return e;
+    prep<<<dim3(nblk, H, B), NT, DiagPrepLayout<DK>::ALLOC, stream>>>(
+        alpha, static_cast<uint8_t *>(ws), H, T, nblk, tmq, tmk, fz, tmqn, tmkn);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    scan<<<dim3(dv / DVS, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
+        static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qn, kn,
+        static_cast<const bf16 *>(v), tmqn, tmkn, tmv);
+    return cudaGetLastError();
+}
+
 template <int DK, bool ALPHA, bool DELTA>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *alpha,
                          const float *beta, const float *S0, void *o, float *S_T, int B, int H,
@@ -1290,6 +1536,9 @@ cudaError_t launch_mode(const void *q, const void *k, const void *v, const float
     case LR_MODE_DELTA:
         return launch_typed<DK, false, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, fz,
                                              ws, stream, slot + 2);
+    case LR_MODE_DIAG_DECAY:
+        return launch_diag<DK>(q, k, v, alpha, S0, o, S_T, B, H, T, dv, fz, ws, stream,
+                               120 + (slot - 32));
     default:
         return launch_typed<DK, true, true>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, fz,
                                             ws, stream, slot + 3);
@@ -1298,12 +1547,12 @@ cudaError_t launch_mode(const void *q, const void *k, const void *v, const float
 
 }  // namespace
 
-size_t chunked_tc_workspace_bytes(int B, int H, int T, int dk, unsigned flags) {
-    const size_t qk = (flags & LR_FUSE_QK_SILU_L2) ? 2 * (size_t)B * H * T * dk * 2 : 0;
-    return records_bytes(B, H, T, dk) + qk;
+size_t chunked_tc_workspace_bytes(int B, int H, int T, int dk, lr_mode mode, unsigned flags) {
+    const bool qk = (flags & LR_FUSE_QK_SILU_L2) || mode == LR_MODE_DIAG_DECAY;
+    return records_bytes(B, H, T, dk) + (qk ? 2 * (size_t)B * H * T * dk * 2 : 0);
 }
 
-// Attribute slots 32..91 belong to this file.
+// Attribute slots 32..91 and 120..131 (diagonal gate) belong to this file.
 cudaError_t launch_chunked_tc(const void *q, const void *k, const void *v, const float *alpha,
                               const float *beta, const float *S0, void *o, float *S_T, int B,
                               int H, int T, int dk, int dv, lr_mode mode, const Fuse &fz,

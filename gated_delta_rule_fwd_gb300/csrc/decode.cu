@@ -21,6 +21,10 @@
 // row hold a whole vector, so the norm is one more 8-lane sum), the gates are
 // mapped on load, and with the output RMSNorm the d_v outputs of the head are
 // kept in shared memory, normalised together and stored once.
+//
+// Diagonal gate (GLA row, same page, gates section): alpha is a vector over the
+// key channels, so each lane loads the gates of its own columns and the row
+// update is S[r,:] <- alpha * S[r,:] + v_r k (element-wise), o_r = S_new[r,:] . q.
 #include "lr_internal.cuh"
 
 namespace lr {
@@ -54,7 +58,7 @@ __device__ __forceinline__ float4 scale4(float4 a, float s) {
     return make_float4(a.x * s, a.y * s, a.z * s, a.w * s);
 }
 
-template <int DK, typename Tin, bool ALPHA, bool DELTA, int UNROLL>
+template <int DK, typename Tin, bool ALPHA, bool DELTA, bool DIAG, int UNROLL>
 __global__ void __launch_bounds__(kStepThreads)
 step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
             const float *__restrict__ alpha, const float *__restrict__ beta,
@@ -104,9 +108,20 @@ step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__r
 #pragma unroll
     for (int m = 0; m < NV; ++m) kq += dot4(kr[m], qr[m]);
     kq = sum8(kq);
-    const float a = ALPHA ? gate(fl, alpha[head],
-                                 (fl & LR_FUSE_ALPHA_SOFTPLUS) ? fz.ascale[head % H] : 0.f)
-                          : 1.f;
+    const float ac = (fl & kScaledAlphaMaps) ? fz.ascale[head % H] : 0.f;
+    const float a = (ALPHA && !DIAG) ? gate(fl, alpha[head], ac) : 1.f;
+    float4 ar[NV];  // the diagonal gate of this lane's columns
+    if (DIAG) {
+#pragma unroll
+        for (int m = 0; m < NV; ++m) {
+            float4 g = *reinterpret_cast<const float4 *>(alpha + (size_t)head * DK +
+                                                        4 * (kLanesPerRow * m + sub));
+            if (fl & kAlphaMaps)
+                g = make_float4(gate(fl, g.x, ac), gate(fl, g.y, ac), gate(fl, g.z, ac),
+                                gate(fl, g.w, ac));
+            ar[m] = g;
+        }
+    }
     const float b = DELTA ? write_strength(fl, beta[head]) : 1.f;
     const bool norm = (fl & LR_FUSE_O_RMSNORM) != 0;
     float oss = 0.f;  // sum of squares of the outputs this lane produced
@@ -120,6 +135,14 @@ step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__r
 #pragma unroll
             for (int m = 0; m < NV; ++m)
                 s[u][m] = ld_stream(Sh + (size_t)r * DK + 4 * (kLanesPerRow * m + sub));
+        }
+        if (DIAG) {  // decay first: the row update and read-out use alpha * s
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u)
+#pragma unroll
+                for (int m = 0; m < NV; ++m)
+                    s[u][m] = make_float4(s[u][m].x * ar[m].x, s[u][m].y * ar[m].y,
+                                          s[u][m].z * ar[m].z, s[u][m].w * ar[m].w);
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
@@ -170,12 +193,12 @@ step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__r
     }
 }
 
-template <int DK, typename Tin, bool ALPHA, bool DELTA>
+template <int DK, typename Tin, bool ALPHA, bool DELTA, bool DIAG = false>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *alpha,
                          const float *beta, float *S, void *o, int NH, int H, int dv,
                          const Fuse &fz, cudaStream_t stream) {
     // dv in {32, 64, 128}: 2, 4 or 8 passes of 16 rows; UNROLL 2 divides all.
-    step_kernel<DK, Tin, ALPHA, DELTA, 2><<<NH, kStepThreads, 0, stream>>>(
+    step_kernel<DK, Tin, ALPHA, DELTA, DIAG, 2><<<NH, kStepThreads, 0, stream>>>(
         static_cast<const Tin *>(q), static_cast<const Tin *>(k), static_cast<const Tin *>(v),
         alpha, beta, S, static_cast<Tin *>(o), H, dv, fz);
     return cudaGetLastError();
@@ -192,6 +215,9 @@ cudaError_t launch_mode(const void *q, const void *k, const void *v, const float
         return launch_typed<DK, Tin, true, false>(q, k, v, alpha, beta, S, o, NH, H, dv, fz, stream);
     case LR_MODE_DELTA:
         return launch_typed<DK, Tin, false, true>(q, k, v, alpha, beta, S, o, NH, H, dv, fz, stream);
+    case LR_MODE_DIAG_DECAY:
+        return launch_typed<DK, Tin, true, false, true>(q, k, v, alpha, beta, S, o, NH, H, dv, fz,
+                                                        stream);
     default:
         return launch_typed<DK, Tin, true, true>(q, k, v, alpha, beta, S, o, NH, H, dv, fz, stream);
     }

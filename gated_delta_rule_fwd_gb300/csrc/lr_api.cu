@@ -10,7 +10,7 @@ namespace lr {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxSlots = 128;
+constexpr int kMaxSlots = 160;
 std::atomic<int> g_smem_bytes[kMaxDevices][kMaxSlots];
 
 bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }
@@ -30,11 +30,22 @@ Span span(const void *p, size_t bytes) {
 }
 bool overlap(Span a, Span b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
 
-bool uses_alpha(lr_mode m) { return m == LR_MODE_DECAY || m == LR_MODE_GATED_DELTA; }
+bool uses_alpha(lr_mode m) {
+    return m == LR_MODE_DECAY || m == LR_MODE_GATED_DELTA || m == LR_MODE_DIAG_DECAY;
+}
+// fp32 values of alpha per token: one, or one per key channel for the diagonal gate
+size_t alpha_per_token(lr_mode m, int dk) { return m == LR_MODE_DIAG_DECAY ? (size_t)dk : 1; }
 bool uses_beta(lr_mode m) { return m == LR_MODE_DELTA || m == LR_MODE_GATED_DELTA; }
 
 constexpr unsigned kFuseAll = LR_FUSE_QK_SILU_L2 | LR_FUSE_BETA_SIGMOID | LR_FUSE_ALPHA_SIGMOID |
-                              LR_FUSE_ALPHA_SOFTPLUS | LR_FUSE_O_RMSNORM;
+                              LR_FUSE_ALPHA_SOFTPLUS | LR_FUSE_O_RMSNORM |
+                              LR_FUSE_ALPHA_SIGMOID_POW;
+
+// at most one alpha map
+bool alpha_maps_ok(unsigned fl) {
+    const unsigned a = fl & kAlphaMaps;
+    return (a & (a - 1)) == 0;
+}
 
 // The kernels' view of lr_fuse: flags validated, the gate maps dropped where
 // the mode has no such gate.
@@ -43,13 +54,13 @@ lr_status to_fuse(const lr_fuse *f, lr_mode mode, Fuse *out) {
     if (!f) return LR_OK;
     unsigned fl = f->flags;
     if (fl & ~kFuseAll) return LR_ERR_FUSE;
-    if ((fl & LR_FUSE_ALPHA_SIGMOID) && (fl & LR_FUSE_ALPHA_SOFTPLUS)) return LR_ERR_FUSE;
+    if (!alpha_maps_ok(fl)) return LR_ERR_FUSE;
     if ((fl & LR_FUSE_O_RMSNORM) && !(f->norm_eps >= 0.f && f->norm_eps <= 3.4e38f))
         return LR_ERR_FUSE;
-    if (!uses_alpha(mode)) fl &= ~(LR_FUSE_ALPHA_SIGMOID | LR_FUSE_ALPHA_SOFTPLUS);
+    if (!uses_alpha(mode)) fl &= ~kAlphaMaps;
     if (!uses_beta(mode)) fl &= ~LR_FUSE_BETA_SIGMOID;
     out->flags = fl;
-    out->ascale = (fl & LR_FUSE_ALPHA_SOFTPLUS) ? f->alpha_scale : nullptr;
+    out->ascale = (fl & kScaledAlphaMaps) ? f->alpha_scale : nullptr;
     out->norm_w = (fl & LR_FUSE_O_RMSNORM) ? f->norm_weight : nullptr;
     out->norm_eps = f->norm_eps;
     return LR_OK;
@@ -117,7 +128,7 @@ const char *lr_status_string(lr_status s) {
 
 static lr_status check_chunked_shape(int B, int H, int T, int dk, int dv, int chunk, lr_dtype dt,
                                      lr_mode mode) {
-    if (mode < LR_MODE_LINEAR || mode > LR_MODE_GATED_DELTA) return LR_ERR_MODE;
+    if (mode < LR_MODE_LINEAR || mode > LR_MODE_DIAG_DECAY) return LR_ERR_MODE;
     if (dt != LR_DT_F32 && dt != LR_DT_BF16) return LR_ERR_DTYPE;
     if (B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1 || chunk < 1) return LR_ERR_SHAPE;
     if (!count_ok(B, H, T, dk > dv ? dk : dv) || !count_ok(B, H, dv, dk)) return LR_ERR_SHAPE;
@@ -128,10 +139,10 @@ static lr_status check_chunked_shape(int B, int H, int T, int dk, int dv, int ch
 size_t lr_fwd_chunked_fused_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
                                            lr_dtype dt, lr_mode mode, unsigned flags) {
     if (check_chunked_shape(B, H, T, dk, dv, chunk, dt, mode) != LR_OK) return 0;
-    if ((flags & ~kFuseAll) || ((flags & LR_FUSE_ALPHA_SIGMOID) && (flags & LR_FUSE_ALPHA_SOFTPLUS)))
+    if ((flags & ~kFuseAll) || !alpha_maps_ok(flags))
         return 0;
     if (dt != LR_DT_BF16 || T == 0) return 0;
-    return chunked_tc_workspace_bytes(B, H, T, dk, flags);
+    return chunked_tc_workspace_bytes(B, H, T, dk, mode, flags);
 }
 
 size_t lr_fwd_chunked_workspace_size(int B, int H, int T, int dk, int dv, int chunk, lr_dtype dt,
@@ -153,7 +164,7 @@ lr_status lr_fwd_chunked_fused(const void *q, const void *k, const void *v, cons
     if (T > 0 && (!q || !k || !v || !o)) return LR_ERR_NULL;
     if (T > 0 && uses_alpha(mode) && !alpha) return LR_ERR_NULL;
     if (T > 0 && uses_beta(mode) && !beta) return LR_ERR_NULL;
-    if (T > 0 && (fz.flags & LR_FUSE_ALPHA_SOFTPLUS) && !fz.ascale) return LR_ERR_NULL;
+    if (T > 0 && (fz.flags & kScaledAlphaMaps) && !fz.ascale) return LR_ERR_NULL;
     const size_t need =
         lr_fwd_chunked_fused_workspace_size(B, H, T, dk, dv, chunk, dt, mode, fz.flags);
     if (need > 0 && (!workspace || workspace_bytes < need)) return LR_ERR_WORKSPACE;
@@ -167,7 +178,7 @@ lr_status lr_fwd_chunked_fused(const void *q, const void *k, const void *v, cons
     const size_t state_bytes = (size_t)B * H * dv * dk * 4;
     const Span sq = span(q, bht * dk * es), sk = span(k, bht * dk * es),
                sv = span(v, bht * dv * es);
-    const Span sa = span(uses_alpha(mode) ? alpha : nullptr, bht * 4);
+    const Span sa = span(uses_alpha(mode) ? alpha : nullptr, bht * alpha_per_token(mode, dk) * 4);
     const Span sb = span(uses_beta(mode) ? beta : nullptr, bht * 4);
     const Span s0 = span(S0, state_bytes), so = span(o, bht * dv * es),
                st = span(S_T, state_bytes);
@@ -220,7 +231,7 @@ lr_status lr_device_status(void) {
 lr_status lr_step_fused(const void *q, const void *k, const void *v, const float *alpha,
                         const float *beta, float *S, void *o, int N, int H, int dk, int dv,
                         lr_dtype dt, lr_mode mode, const lr_fuse *fuse, cudaStream_t stream) {
-    if (mode < LR_MODE_LINEAR || mode > LR_MODE_GATED_DELTA) return LR_ERR_MODE;
+    if (mode < LR_MODE_LINEAR || mode > LR_MODE_DIAG_DECAY) return LR_ERR_MODE;
     if (dt != LR_DT_F32 && dt != LR_DT_BF16) return LR_ERR_DTYPE;
     if (N < 1 || H < 1 || dk < 1 || dv < 1) return LR_ERR_SHAPE;
     if (!count_ok(N, H, dv, dk) || (long long)N * H > 0x7fffffffll) return LR_ERR_SHAPE;
@@ -231,7 +242,7 @@ lr_status lr_step_fused(const void *q, const void *k, const void *v, const float
     if (!q || !k || !v || !S || !o) return LR_ERR_NULL;
     if (uses_alpha(mode) && !alpha) return LR_ERR_NULL;
     if (uses_beta(mode) && !beta) return LR_ERR_NULL;
-    if ((fz.flags & LR_FUSE_ALPHA_SOFTPLUS) && !fz.ascale) return LR_ERR_NULL;
+    if ((fz.flags & kScaledAlphaMaps) && !fz.ascale) return LR_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) ||
         !aligned16(beta) || !aligned16(S) || !aligned16(o) || !aligned16(fz.ascale) ||
         !aligned16(fz.norm_w))
@@ -240,7 +251,7 @@ lr_status lr_step_fused(const void *q, const void *k, const void *v, const float
     const size_t es = dt == LR_DT_F32 ? 4 : 2;
     const size_t nh = (size_t)N * H;
     const Span sq = span(q, nh * dk * es), sk = span(k, nh * dk * es), sv = span(v, nh * dv * es);
-    const Span sa = span(uses_alpha(mode) ? alpha : nullptr, nh * 4);
+    const Span sa = span(uses_alpha(mode) ? alpha : nullptr, nh * alpha_per_token(mode, dk) * 4);
     const Span sb = span(uses_beta(mode) ? beta : nullptr, nh * 4);
     const Span ss = span(S, nh * dv * dk * 4), so = span(o, nh * dv * es);
     for (Span in : {sq, sk, sv, sa, sb, ss})

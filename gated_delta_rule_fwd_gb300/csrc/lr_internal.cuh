@@ -44,7 +44,8 @@ struct ModeBits {
     bool delta;  // the write is the corrected (delta-rule) pseudo-value
 };
 __host__ __device__ constexpr ModeBits mode_bits(int mode) {
-    return ModeBits{mode == LR_MODE_DECAY || mode == LR_MODE_GATED_DELTA,
+    return ModeBits{mode == LR_MODE_DECAY || mode == LR_MODE_GATED_DELTA ||
+                        mode == LR_MODE_DIAG_DECAY,
                     mode == LR_MODE_DELTA || mode == LR_MODE_GATED_DELTA};
 }
 
@@ -68,18 +69,23 @@ __device__ __forceinline__ float silu_f(float x) { return x / (1.f + __expf(-x))
 __device__ __forceinline__ float inv_l2(float ss) { return rsqrtf(fmaxf(ss, 1e-24f)); }
 
 // ln alpha from the value read from memory: ln a without a gate map,
-// ln sigmoid(a) = -softplus(-a), or -c softplus(a).
+// ln sigmoid(a) = -softplus(-a), -c softplus(a), or c ln sigmoid(a).
 __device__ __forceinline__ float log_gate(unsigned fl, float a, float c) {
     if (fl & LR_FUSE_ALPHA_SIGMOID) return -softplus_f(-a);
     if (fl & LR_FUSE_ALPHA_SOFTPLUS) return -c * softplus_f(a);
+    if (fl & LR_FUSE_ALPHA_SIGMOID_POW) return -c * softplus_f(-a);
     return __logf(a);
 }
-// alpha itself (decode)
+// alpha itself (decode, and the products of the diagonal gate)
 __device__ __forceinline__ float gate(unsigned fl, float a, float c) {
     if (fl & LR_FUSE_ALPHA_SIGMOID) return sigmoid_f(a);
     if (fl & LR_FUSE_ALPHA_SOFTPLUS) return __expf(-c * softplus_f(a));
+    if (fl & LR_FUSE_ALPHA_SIGMOID_POW) return __expf(-c * softplus_f(-a));
     return a;
 }
+// the alpha maps that take c_h from alpha_scale
+constexpr unsigned kScaledAlphaMaps = LR_FUSE_ALPHA_SOFTPLUS | LR_FUSE_ALPHA_SIGMOID_POW;
+constexpr unsigned kAlphaMaps = LR_FUSE_ALPHA_SIGMOID | kScaledAlphaMaps;
 __device__ __forceinline__ float write_strength(unsigned fl, float b) {
     return (fl & LR_FUSE_BETA_SIGMOID) ? sigmoid_f(b) : b;
 }
@@ -104,9 +110,9 @@ cudaError_t launch_chunked_tc(const void *q, const void *k, const void *v, const
                               const float *beta, const float *S0, void *o, float *S_T, int B,
                               int H, int T, int dk, int dv, lr_mode mode, const Fuse &fz,
                               void *ws, cudaStream_t stream);
-// Workspace bytes the tensor-core path needs (with the normalised q and k
-// when the flags ask for them).
-size_t chunked_tc_workspace_bytes(int B, int H, int T, int dk, unsigned flags);
+// Workspace bytes the tensor-core path needs (with the transformed q and k
+// for the diagonal gate or when the flags ask for SiLU + L2).
+size_t chunked_tc_workspace_bytes(int B, int H, int T, int dk, lr_mode mode, unsigned flags);
 
 // In-place RMSNorm of `rows` rows of dv channels (norm.cu).
 cudaError_t launch_rmsnorm(void *o, const float *w, float eps, size_t rows, int dv, lr_dtype dt,

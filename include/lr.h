@@ -58,7 +58,7 @@ typedef enum {
     LR_ERR_WORKSPACE = 10,  /* workspace NULL or smaller than lr_fwd_chunked_workspace_size */
     LR_ERR_TOO_LARGE = 11,  /* lr_fwd_chunked_noalloc: the problem needs more scratch
                                than LR_STATIC_WORKSPACE_BYTES */
-    LR_ERR_FUSE = 12        /* lr_fuse: unknown flag bits, both alpha maps at once,
+    LR_ERR_FUSE = 12        /* lr_fuse: unknown flag bits, two alpha maps at once,
                                or norm_eps negative or not finite */
 } lr_status;
 
@@ -76,7 +76,18 @@ typedef enum {
     LR_MODE_DELTA = 2,
     /* S_t = S_{t-1} [alpha_t (I - beta_t k_t k_t^T)] + beta_t v_t k_t^T
        (Gated DeltaNet).  Both alpha and beta are required. */
-    LR_MODE_GATED_DELTA = 3
+    LR_MODE_GATED_DELTA = 3,
+    /* S_t = S_{t-1} Diag(alpha_t) + v_t k_t^T  (the diagonal gate of GLA,
+       section "Dimenticare: i gate": one gate per key channel, multiplying
+       from the right, so column c of S decays by alpha_t[c]).  alpha has one
+       value per key channel: [B, H, T, dk] for lr_fwd_chunked, [N, H, dk] for
+       lr_step.  beta is ignored, may be NULL.  The chunked form computes the
+       scores of a 64-token block in 16-token sub-blocks (the second level of
+       blocks GLA needs for numerical stability, summary of the same page):
+       the per-channel decay across any 16 consecutive tokens of a block must
+       stay above e^-80 (an average gate above 0.007), else those scores are
+       inexact. */
+    LR_MODE_DIAG_DECAY = 4
 } lr_mode;
 
 /* Element type of q, k, v and o. */
@@ -103,7 +114,8 @@ typedef enum {
  *   q      [B, H, T, dk]   dtype dt
  *   k      [B, H, T, dk]   dtype dt
  *   v      [B, H, T, dv]   dtype dt
- *   alpha  [B, H, T]       fp32; required for DECAY and GATED_DELTA
+ *   alpha  [B, H, T]       fp32; required for DECAY and GATED_DELTA;
+ *                          [B, H, T, dk] for DIAG_DECAY
  *   beta   [B, H, T]       fp32; required for DELTA and GATED_DELTA
  *   S0     [B, H, dv, dk]  fp32 initial state, or NULL for zeros
  *   o      [B, H, T, dv]   dtype dt, written; must not overlap any input
@@ -157,7 +169,9 @@ size_t lr_fwd_chunked_workspace_size(int B, int H, int T, int dk, int dv, int ch
  *
  *   q, k   [N, H, dk]       dtype dt
  *   v      [N, H, dv]       dtype dt
- *   alpha  [N, H]           fp32 (required for DECAY, GATED_DELTA)
+ *   alpha  [N, H]           fp32 (required for DECAY, GATED_DELTA);
+ *                           [N, H, dk] for DIAG_DECAY (then a is the vector
+ *                           alpha and S[r, :] <- a * s + v_r k, o_r = S[r,:] . q)
  *   beta   [N, H]           fp32 (required for DELTA, GATED_DELTA)
  *   S      [N, H, dv, dk]   fp32, read and updated IN PLACE
  *   o      [N, H, dv]       dtype dt, written; must not overlap S or inputs
@@ -229,6 +243,9 @@ lr_status lr_fwd_chunked_noalloc(const void *q, const void *k, const void *v,
  *                           a decay computed from the input; the page leaves
  *                           the parametrisation open, these are the two in
  *                           common use)
+ *   LR_FUSE_ALPHA_SIGMOID_POW  alpha_t <- sigmoid(alpha_t)^c_h, c_h =
+ *                           alpha_scale[h]  (the same section: GLA's gate, a
+ *                           sigmoid raised to 1/tau, tau = 16, per key channel)
  *   LR_FUSE_O_RMSNORM       o_t <- o_t / sqrt(mean_r o_t[r]^2 + norm_eps) *
  *                           norm_weight, per token over the d_v channels of a
  *                           head (same page, the read-out of DeltaNet is
@@ -244,11 +261,13 @@ lr_status lr_fwd_chunked_noalloc(const void *q, const void *k, const void *v,
 #define LR_FUSE_ALPHA_SIGMOID 0x4u
 #define LR_FUSE_ALPHA_SOFTPLUS 0x8u
 #define LR_FUSE_O_RMSNORM 0x10u
+#define LR_FUSE_ALPHA_SIGMOID_POW 0x20u
 
 typedef struct {
     unsigned flags;            /* OR of LR_FUSE_* (0: the plain call)                */
-    const float *alpha_scale;  /* [H] fp32 device, c_h of LR_FUSE_ALPHA_SOFTPLUS;
-                                  required with that flag in modes using alpha     */
+    const float *alpha_scale;  /* [H] fp32 device, c_h of LR_FUSE_ALPHA_SOFTPLUS and
+                                  LR_FUSE_ALPHA_SIGMOID_POW; required with them in
+                                  modes using alpha                                 */
     const float *norm_weight;  /* [d_v] fp32 device, shared by all heads, or NULL
                                   for ones (LR_FUSE_O_RMSNORM)                      */
     float norm_eps;            /* >= 0, finite (LR_FUSE_O_RMSNORM)                  */

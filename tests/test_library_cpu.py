@@ -88,7 +88,7 @@ def step(**kw):
     return L.lr_step(a['q'], a['k'], a['v'], a['al'], a['be'], a['s'], a['o'], a['N'], a['H'],
                      a['dk'], a['dv'], a['dt'], a['mode'], None)
 cases = [
-    ("mode", chunk(mode=4), 5), ("mode-neg", chunk(mode=-1), 5), ("dtype", chunk(dt=2), 3),
+    ("mode", chunk(mode=6), 5), ("mode-neg", chunk(mode=-1), 5), ("dtype", chunk(dt=2), 3),
     ("B0", chunk(B=0), 2), ("Hneg", chunk(H=-1), 2), ("Tneg", chunk(T=-1), 2),
     ("huge", chunk(B=1 << 20, H=1 << 10, T=1 << 20), 2),
     ("dk48", chunk(dk=48), 6), ("dv256", chunk(dv=256), 6), ("chunk32", chunk(chunk=32), 6),
@@ -151,6 +151,15 @@ cases += [
     ("step-fused-null-scale", fstep(flags=0x8, ascale=None), 1),
     ("step-fused-alias-S-weight", fstep(flags=0x10, w=A[5]), 8),
     ("step-fused-misaligned-weight", fstep(flags=0x10, w=A[6] + 0x200004), 4),
+    ("fused-two-alpha-maps-pow", fchunk(flags=0x20 | 0x8), 12),
+    ("fused-pow-null-scale", fchunk(flags=0x20, ascale=None), 1),
+    # the diagonal gate: alpha [B, H, T, dk] (here 8 x 32 floats = 1 KB)
+    ("diag-null-alpha", chunk(mode=4, al=None), 1),
+    ("diag-mode-range", chunk(mode=5), 5),
+    ("diag-alias-o-alpha", chunk(mode=4, o=P(A[3] + 512)), 8),
+    ("scalar-alpha-span-is-short", chunk(mode=1, o=P(A[3] + 512)), 7),  # passes validation
+    ("diag-step-alias-o-alpha", step(mode=4, o=P(A[3] + 64)), 8),
+    ("diag-ws-larger", int(L.lr_fwd_chunked_workspace_size(1, 1, 8, 32, 32, 64, 1, 4) - need), 2 * 8 * 32 * 2),
 ]
 bad = [(n, got, want) for n, got, want in cases if got != want]
 print("BAD", bad)

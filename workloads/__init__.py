@@ -16,6 +16,13 @@ there -- and beta comes from a sigmoid):
   head h = 0..H-1, the same at every token.
 * ``mamba2``: q, k ~ N(0,1)/sqrt(dk); v ~ N(0,1);
   alpha = exp(-0.1 softplus(N(0,1))).
+* ``gla`` (diagonal gate, alpha [B,H,T,dk]): q, k ~ N(0,1)/sqrt(dk); v ~ N(0,1);
+  alpha = sigmoid(N(0,1))^(1/16) per key channel (GLA's gate with tau = 16,
+  first page, gates section).
+* ``gla_strong``: as ``gla`` with alpha = sigmoid(N(-2,1)): decays near e^-136
+  over a 64-token block (beyond fp32's range for one reference point per
+  block) and near e^-34 over 16 tokens, which the kernels' 16-token
+  sub-blocks must absorb.
 
 Draw order with one ``torch.Generator('cpu')``: q, k, v, beta, alpha, S0.
 Values are drawn in fp32 and, for bf16 workloads, rounded to bf16 once; the
@@ -28,7 +35,7 @@ import math
 
 import torch
 
-LINEAR, DECAY, DELTA, GATED_DELTA = 0, 1, 2, 3
+LINEAR, DECAY, DELTA, GATED_DELTA, DIAG_DECAY = 0, 1, 2, 3, 4
 
 
 @dataclasses.dataclass(frozen=True)
@@ -69,6 +76,8 @@ WORKLOADS = {
                                  64, 4, "gdn", 0.1),
     "gdn_decode_bf16": Workload("gdn_decode_bf16", GATED_DELTA, "bf16", 512, 32, 1, 128, 128, 64,
                                 5, "gdn", 0.1, steps=1000),
+    # the diagonal gate (GLA row), at the Mamba-2-style workload's size
+    "gla_bf16": Workload("gla_bf16", DIAG_DECAY, "bf16", 8, 16, 4096, 128, 128, 64, 6, "gla", 0.0),
 }
 
 
@@ -85,8 +94,8 @@ def retnet_gamma(H: int) -> torch.Tensor:
 def draw(gen: str, B, H, T, dk, dv, seed, dtype=torch.float32, s0_std=0.0, device="cpu"):
     """Draw one input set.  Returns dict q, k, v, alpha, beta, S0 (S0 may be None).
 
-    Shapes: q, k [B,H,T,dk]; v [B,H,T,dv]; alpha, beta [B,H,T] fp32;
-    S0 [B,H,dv,dk] fp32.  q, k, v are rounded once to ``dtype``.  Drawn on
+    Shapes: q, k [B,H,T,dk]; v [B,H,T,dv]; alpha, beta [B,H,T] fp32 (alpha
+    [B,H,T,dk] for the diagonal-gate generators); S0 [B,H,dv,dk] fp32.  q, k, v are rounded once to ``dtype``.  Drawn on
     the CPU generator and then moved to ``device``.
     """
     g = torch.Generator("cpu")
@@ -112,6 +121,16 @@ def draw(gen: str, B, H, T, dk, dv, seed, dtype=torch.float32, s0_std=0.0, devic
         v = torch.randn(shp_v, generator=g)
         beta = torch.zeros(shp_t)
         alpha = torch.exp(-0.1 * torch.nn.functional.softplus(torch.randn(shp_t, generator=g)))
+    elif gen in ("gla", "gla_strong"):
+        s = 1.0 / math.sqrt(dk)
+        q = torch.randn(shp_k, generator=g) * s
+        k = torch.randn(shp_k, generator=g) * s
+        v = torch.randn(shp_v, generator=g)
+        beta = torch.zeros(shp_t)
+        if gen == "gla":
+            alpha = torch.sigmoid(torch.randn(shp_k, generator=g)) ** (1.0 / 16.0)
+        else:
+            alpha = torch.sigmoid(torch.randn(shp_k, generator=g) - 2.0)
     elif gen == "uniform":
         # generic small-case inputs: keys of norm <= 1, gates in (0.5, 1)
         q = torch.randn(shp_k, generator=g) / math.sqrt(dk)
@@ -134,11 +153,14 @@ def draw(gen: str, B, H, T, dk, dv, seed, dtype=torch.float32, s0_std=0.0, devic
 # normalises o; the Mamba-2-style layer maps alpha by the softplus gate.
 FUSE_QK_SILU_L2, FUSE_BETA_SIGMOID, FUSE_ALPHA_SIGMOID, FUSE_ALPHA_SOFTPLUS, FUSE_O_RMSNORM = (
     0x1, 0x2, 0x4, 0x8, 0x10)
+FUSE_ALPHA_SIGMOID_POW = 0x20
 FUSED_FLAGS = {
     "gdn": FUSE_QK_SILU_L2 | FUSE_BETA_SIGMOID | FUSE_ALPHA_SIGMOID | FUSE_O_RMSNORM,
     "mamba2": FUSE_ALPHA_SOFTPLUS | FUSE_O_RMSNORM,
+    "gla": FUSE_ALPHA_SIGMOID_POW | FUSE_O_RMSNORM,
 }
 MAMBA2_ALPHA_SCALE = 0.1
+GLA_ALPHA_POWER = 1.0 / 16.0   # GLA's gate sigmoid(.)^(1/tau), tau = 16
 
 
 def draw_pre(gen: str, B, H, T, dk, dv, seed, dtype=torch.float32, s0_std=0.0, device="cpu"):
@@ -146,7 +168,9 @@ def draw_pre(gen: str, B, H, T, dk, dv, seed, dtype=torch.float32, s0_std=0.0, d
     as :func:`draw` before its maps): q, k, v ~ N(0,1) rounded once to
     ``dtype``; for "gdn" beta ~ N(0,1) and alpha ~ N(3,1) (sigmoid gates), for
     "mamba2" alpha ~ N(0,1) (softplus gate, alpha_scale 0.1 for every head)
-    and beta = 0; norm_weight ~ U(0.5, 1.5) [dv]; S0 ~ N(0, s0_std^2) or None.
+    and beta = 0, for "gla" alpha ~ N(0,1) per key channel [B,H,T,dk]
+    (sigmoid gate raised to alpha_scale = 1/16) and beta = 0;
+    norm_weight ~ U(0.5, 1.5) [dv]; S0 ~ N(0, s0_std^2) or None.
 
     Returns dict q, k, v, alpha, beta, S0, alpha_scale [H], norm_weight [dv].
     Draw order: q, k, v, beta, alpha, S0, norm_weight.
@@ -163,13 +187,17 @@ def draw_pre(gen: str, B, H, T, dk, dv, seed, dtype=torch.float32, s0_std=0.0, d
     elif gen == "mamba2":
         beta = torch.zeros(shp_t)
         alpha = torch.randn(shp_t, generator=g)
+    elif gen == "gla":
+        beta = torch.zeros(shp_t)
+        alpha = torch.randn(shp_k, generator=g)
     else:
         raise ValueError(gen)
     S0 = torch.randn((B, H, dv, dk), generator=g) * s0_std if s0_std > 0 else None
     w = 0.5 + torch.rand((dv,), generator=g)
+    scale = GLA_ALPHA_POWER if gen == "gla" else MAMBA2_ALPHA_SCALE
     out = dict(q=q.to(dtype), k=k.to(dtype), v=v.to(dtype), alpha=alpha.float().contiguous(),
                beta=beta.float().contiguous(), S0=S0,
-               alpha_scale=torch.full((H,), MAMBA2_ALPHA_SCALE), norm_weight=w.float())
+               alpha_scale=torch.full((H,), scale), norm_weight=w.float())
     if device != "cpu":
         out = {n: (t.to(device) if t is not None else None) for n, t in out.items()}
     return out
