@@ -35,6 +35,7 @@ import workloads  # noqa: E402
 
 DEFAULT_WORKLOAD = "gdn_prefill_bf16"
 DECODE_WORKLOAD = "gdn_decode_bf16"
+DIAG_WORKLOAD = "gla_bf16"
 METRIC = "chunked fwd tokens/s"
 UNIT = "tokens/s"
 
@@ -77,6 +78,8 @@ def head_token_bytes(w):
     b = es * (2 * w.dk + 2 * w.dv)
     if w.mode in (workloads.DECAY, workloads.GATED_DELTA):
         b += 4
+    if w.mode == workloads.DIAG_DECAY:   # one gate per key channel
+        b += 4 * w.dk
     if w.mode in (workloads.DELTA, workloads.GATED_DELTA):
         b += 4
     return b
@@ -93,7 +96,8 @@ def chunk_bytes(w):
 def chunk_flops(w):
     """Chunk-form tensor flops (dense C x C tiles counted in full, UT inverse
     excluded): 2C(3dk+2dv)+6dk*dv per head-token with delta,
-    2C(dk+dv)+4dk*dv without."""
+    2C(dk+dv)+4dk*dv without (the diagonal gate's four 64 x 16 sub-block
+    score products add up to one C x C product)."""
     C = w.chunk
     if w.mode in (workloads.DELTA, workloads.GATED_DELTA):
         per = 2 * C * (3 * w.dk + 2 * w.dv) + 6 * w.dk * w.dv
@@ -302,7 +306,8 @@ def run_ours(args, dist, rank, world, local):
     hx = {n: (t.pin_memory() if t is not None else None) for n, t in x.items()}
     used = {n for n, t in hx.items()
             if t is not None and not (n == "alpha" and w.mode in (workloads.LINEAR, workloads.DELTA))
-            and not (n == "beta" and w.mode in (workloads.LINEAR, workloads.DECAY))}
+            and not (n == "beta" and w.mode in (workloads.LINEAR, workloads.DECAY,
+                                                 workloads.DIAG_DECAY))}
     ho = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
     hs = [torch.empty(st.shape, dtype=st.dtype).pin_memory() for _ in range(2)]
     h2d = sum(hx[n].numel() * hx[n].element_size() for n in used)
@@ -363,6 +368,9 @@ def run_ours(args, dist, rank, world, local):
     fused_decode = None
     if not args.no_fused and not args.no_decode:
         fused_decode = run_decode(lr, dev, dist, peaks, args, fused=True)
+    diag = None
+    if not args.no_diag and w.name != DIAG_WORKLOAD:
+        diag = run_diag(lr, dev, dist, args, peaks)
 
     out = None
     if rank == 0:
@@ -374,7 +382,8 @@ def run_ours(args, dist, rank, world, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic (seeded; shapes and distributions of the workload)",
-            "config": {"workload": w.name, "mode": "gated_delta" if w.mode == 3 else w.mode,
+            "config": {"workload": w.name,
+                       "mode": ["linear", "decay", "delta", "gated_delta", "diag_decay"][w.mode],
                        "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
                        "state": "fp32", "global_batch": w.B * world, "seq_len": w.T,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -402,7 +411,48 @@ def run_ours(args, dist, rank, world, local):
             out["fused"] = fused
         if fused_decode is not None:
             out["fused_decode"] = fused_decode
+        if diag is not None:
+            out["diag"] = diag
     return out
+
+
+def run_diag(lr, dev, dist, args, peaks):
+    """The diagonal-gate (GLA) workload through lr_fwd_chunked, timed like the
+    headline, with its HBM roofline (algorithmic bytes include alpha, one fp32
+    gate per key channel and token)."""
+    w = workloads.WORKLOADS[DIAG_WORKLOAD]
+    x = workloads.draw_workload(w)
+    xd = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.torch_dtype, device=dev)
+    st = torch.empty((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, lr.workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.torch_dtype, w.mode,
+                                              w.chunk)), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    steps = max(3, min(args.steps, 100))
+
+    def step():
+        lr.lr_fwd_chunked(xd["q"], xd["k"], xd["v"], xd["alpha"], None, xd["S0"], mode=w.mode,
+                          chunk=w.chunk, o=o, S_T=st, workspace=ws, stream=stream)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(dist, e0.elapsed_time(e1), dev) / steps
+    world = dist.get_world_size() if dist else 1
+    gbs = chunk_bytes(w) / (ms / 1e3) / 1e9
+    return {"workload": w.name, "mode": "diag_decay", "entry_point": "lr_fwd_chunked",
+            "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
+            "value": w.B * w.T * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+            "steps": steps, "algorithmic_bytes_per_launch": chunk_bytes(w),
+            "achieved_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+            "achieved_tflops": chunk_flops(w) / (ms / 1e3) / 1e12,
+            "gpu_launches": steps * 2}
 
 
 def run_fused(lr, dev, dist, args, w, plain_ms):
@@ -559,6 +609,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fused", action="store_true",
                     help="skip the fused entry points' timings (prefill and decode)")
+    ap.add_argument("--no-diag", action="store_true",
+                    help="skip the diagonal-gate (GLA) workload's timing")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of single-core oracle work in the cpu_baseline sample")
     ap.add_argument("--ref-tokens", type=int, default=2048,

@@ -764,6 +764,10 @@ chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws
         tmem_alloc(tmem_slot, 64);
         tmem_relinquish();
     }
+    // the barriers are initialised before any thread waits on them
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
     // this channel's gates of the block (1 past the end of the sequence)
     float a[C];
     if (c < DK) {
