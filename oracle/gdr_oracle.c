@@ -47,6 +47,7 @@
  * Every (b, h) pair is an independent sequence; OpenMP runs them in
  * parallel.  Within a sequence the loop over t is strictly sequential.
  */
+#include <math.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -157,6 +158,95 @@ int gdr_oracle_recurrent(int mode, int B, int H, int T, int dk, int dv,
         memcpy(ST + (size_t)bh * sz, S, sz * sizeof(double));
         free(S);
         free(w);
+    }
+    (void)num_threads;
+    return failed ? 2 : 0;
+}
+
+/*
+ * mLSTM (page "Le architetture lineari: RetNet, RWKV, xLSTM", section on
+ * xLSTM, the matrix-memory cell): the scalar-gate row with a write factor
+ * i_t = exp(igate_t) and a normaliser,
+ *
+ *     C_t = f_t C_{t-1} + i_t v_t k_t^T,   n_t = f_t n_{t-1} + i_t k_t,
+ *     h_t = C_t q_t / max(|n_t^T q_t|, 1),
+ *
+ * evaluated in the stabilised form the page takes from the authors' appendix:
+ * a log-space state m_t = max(log f_t + m_{t-1}, igate_t) is subtracted
+ * before exponentiating, so the stored memory is C~ = e^{-m} C, n~ = e^{-m} n,
+ * and the threshold carries the same factor: h_t = C~_t q_t /
+ * max(|n~_t^T q_t|, e^{-m_t}).  (The plain form lives in oracle/mlstm.py; the
+ * tests pin the two against each other.)
+ *
+ * Layouts: q, k [B][H][T][dk]; v, h [B][H][T][dv]; logf, igate [B][H][T]
+ * (log of the forget gate, <= 0, and the input-gate pre-activation);
+ * C0, CT [B][H][dv][dk]; n0, nT [B][H][dk]; m0, mT [B][H].  C0, n0, m0 may
+ * all be NULL for the empty memory (C = 0, n = 0, m = -inf, so that the first
+ * step gives m = igate).  Returns 0, 1 on a bad argument, 2 on allocation
+ * failure.
+ */
+int gdr_oracle_mlstm(int B, int H, int T, int dk, int dv,
+                     const double *q, const double *k, const double *v,
+                     const double *logf, const double *igate,
+                     const double *C0, const double *n0, const double *m0,
+                     double *h, double *CT, double *nT, double *mT, int num_threads)
+{
+    if (B <= 0 || H <= 0 || T < 0 || dk <= 0 || dv <= 0) return 1;
+    if (!q || !k || !v || !logf || !igate || !h || !CT || !nT || !mT) return 1;
+    if ((C0 || n0 || m0) && !(C0 && n0 && m0)) return 1;
+    const int BH = B * H;
+    const size_t sz = (size_t)dv * dk;
+    int failed = 0;
+#ifdef _OPENMP
+    if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads) reduction(| : failed)
+#endif
+    for (int bh = 0; bh < BH; ++bh) {
+        double *C = (double *)malloc(sz * sizeof(double));
+        double *n = (double *)malloc((size_t)dk * sizeof(double));
+        if (!C || !n) {
+            free(C);
+            free(n);
+            failed |= 1;
+            continue;
+        }
+        double m;
+        if (C0) {
+            memcpy(C, C0 + (size_t)bh * sz, sz * sizeof(double));
+            memcpy(n, n0 + (size_t)bh * dk, (size_t)dk * sizeof(double));
+            m = m0[bh];
+        } else {
+            memset(C, 0, sz * sizeof(double));
+            memset(n, 0, (size_t)dk * sizeof(double));
+            m = -1.0 / 0.0;
+        }
+        for (int t = 0; t < T; ++t) {
+            const size_t it = (size_t)bh * T + t;
+            const double *qt = q + it * dk, *kt = k + it * dk, *vt = v + it * dv;
+            const double lf = logf[it], ig = igate[it];
+            const double m_new = (lf + m > ig) ? lf + m : ig;
+            const double a = exp(lf + m - m_new), b = exp(ig - m_new);
+            for (int r = 0; r < dv; ++r)
+                for (int c = 0; c < dk; ++c)
+                    C[(size_t)r * dk + c] = a * C[(size_t)r * dk + c] + b * vt[r] * kt[c];
+            double nq = 0.0;
+            for (int c = 0; c < dk; ++c) {
+                n[c] = a * n[c] + b * kt[c];
+                nq += n[c] * qt[c];
+            }
+            const double den = fabs(nq) > exp(-m_new) ? fabs(nq) : exp(-m_new);
+            for (int r = 0; r < dv; ++r) {
+                double acc = 0.0;
+                for (int c = 0; c < dk; ++c) acc += C[(size_t)r * dk + c] * qt[c];
+                h[it * dv + r] = acc / den;
+            }
+            m = m_new;
+        }
+        memcpy(CT + (size_t)bh * sz, C, sz * sizeof(double));
+        memcpy(nT + (size_t)bh * dk, n, (size_t)dk * sizeof(double));
+        mT[bh] = m;
+        free(C);
+        free(n);
     }
     (void)num_threads;
     return failed ? 2 : 0;
