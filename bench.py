@@ -36,6 +36,7 @@ import workloads  # noqa: E402
 DEFAULT_WORKLOAD = "gdn_prefill_bf16"
 DECODE_WORKLOAD = "gdn_decode_bf16"
 DIAG_WORKLOAD = "gla_bf16"
+MLSTM_WORKLOAD = "mlstm_bf16"
 METRIC = "chunked fwd tokens/s"
 UNIT = "tokens/s"
 
@@ -371,6 +372,9 @@ def run_ours(args, dist, rank, world, local):
     diag = None
     if not args.no_diag and w.name != DIAG_WORKLOAD:
         diag = run_diag(lr, dev, dist, args, peaks)
+    mlstm = None
+    if not args.no_diag:
+        mlstm = run_mlstm(lr, dev, dist, args, peaks)
 
     out = None
     if rank == 0:
@@ -413,7 +417,52 @@ def run_ours(args, dist, rank, world, local):
             out["fused_decode"] = fused_decode
         if diag is not None:
             out["diag"] = diag
+        if mlstm is not None:
+            out["mlstm"] = mlstm
     return out
+
+
+def run_mlstm(lr, dev, dist, args, peaks):
+    """The mLSTM workload through lr_fwd_chunked_mlstm (five launches: the
+    stabiliser, the per-block pass, the scan, the normaliser, the division),
+    timed like the headline.  Algorithmic bytes: q, k, v, h at bf16 and the two
+    gates per head-token, plus the final state."""
+    w = workloads.WORKLOADS[MLSTM_WORKLOAD]
+    x = workloads.draw_mlstm(w.B, w.H, w.T, w.dk, w.dv, seed=w.seed, dtype=w.torch_dtype)
+    xd = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    ws = torch.empty(max(1, lr.mlstm_workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.torch_dtype)),
+                     dtype=torch.uint8, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    h = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.torch_dtype, device=dev)
+    CT = torch.empty((w.B, w.H, w.dv, w.dk), **f32)
+    nT = torch.empty((w.B, w.H, w.dk), **f32)
+    mT = torch.empty((w.B, w.H), **f32)
+    stream = torch.cuda.current_stream(dev)
+    steps = max(3, min(args.steps, 100))
+
+    def step():
+        lr.lr_fwd_chunked_mlstm(xd["q"], xd["k"], xd["v"], xd["fgate"], xd["igate"], h=h, C_T=CT,
+                                n_T=nT, m_T=mT, workspace=ws, stream=stream)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(dist, e0.elapsed_time(e1), dev) / steps
+    world = dist.get_world_size() if dist else 1
+    heads = w.B * w.H
+    nbytes = heads * w.T * (2 * (2 * w.dk + 2 * w.dv) + 8) + heads * (w.dv * w.dk + w.dk + 1) * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"workload": w.name, "entry_point": "lr_fwd_chunked_mlstm", "B": w.B, "H": w.H,
+            "T": w.T, "dk": w.dk, "dv": w.dv, "value": w.B * w.T * world / (ms / 1e3),
+            "unit": UNIT, "ms_per_step": ms, "steps": steps,
+            "algorithmic_bytes_per_launch": nbytes, "achieved_gbs": gbs,
+            "frac_hbm": gbs / peaks["hbm_gbs"], "gpu_launches": steps * 5}
 
 
 def run_diag(lr, dev, dist, args, peaks):
@@ -610,7 +659,7 @@ def main():
     ap.add_argument("--no-fused", action="store_true",
                     help="skip the fused entry points' timings (prefill and decode)")
     ap.add_argument("--no-diag", action="store_true",
-                    help="skip the diagonal-gate (GLA) workload's timing")
+                    help="skip the diagonal-gate (GLA) and mLSTM workloads' timings")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of single-core oracle work in the cpu_baseline sample")
     ap.add_argument("--ref-tokens", type=int, default=2048,

@@ -10,6 +10,8 @@ missing or cannot be loaded, every call raises.
         chunkwise prefill over whole sequences (q, k: [B,H,T,dk], v: [B,H,T,dv])
     lr_step(q, k, v, alpha, beta, S, mode=...) -> o
         one decode step for N sequences, S: [N,H,dv,dk] updated in place
+    lr_fwd_chunked_mlstm / lr_step_mlstm(q, k, v, fgate, igate, ...)
+        the mLSTM memory (exponential write gate, normaliser, stabiliser)
     lr_fwd_chunked_fused / lr_step_fused(..., flags=..., ...)
         the same with the maps around the recurrence (SiLU + L2 of q and k,
         sigmoid beta, sigmoid or softplus alpha, output RMSNorm) applied inside
@@ -28,6 +30,7 @@ MODES = {"linear": LINEAR, "decay": DECAY, "delta": DELTA, "gated_delta": GATED_
 F32, BF16 = 0, 1
 SYMBOLS = ("lr_fwd_chunked", "lr_fwd_chunked_workspace_size", "lr_fwd_chunked_noalloc", "lr_step",
            "lr_fwd_chunked_fused", "lr_fwd_chunked_fused_workspace_size", "lr_step_fused",
+           "lr_fwd_chunked_mlstm", "lr_fwd_chunked_mlstm_workspace_size", "lr_step_mlstm",
            "lr_device_status", "lr_status_string", "lr_abi_version")
 # lr_fuse flags (include/lr.h)
 FUSE_QK_SILU_L2 = 0x1
@@ -94,6 +97,12 @@ def lib() -> ctypes.CDLL:
         L.lr_fwd_chunked_fused_workspace_size.argtypes = [i] * 8 + [ctypes.c_uint]
         L.lr_step_fused.restype = i
         L.lr_step_fused.argtypes = [vp, vp, vp, fp, fp, fp, vp] + [i] * 4 + [i, i, fz, vp]
+        L.lr_fwd_chunked_mlstm.restype = i
+        L.lr_fwd_chunked_mlstm.argtypes = ([vp] * 12 + [i] * 6 + [i, vp, ctypes.c_size_t, vp])
+        L.lr_fwd_chunked_mlstm_workspace_size.restype = ctypes.c_size_t
+        L.lr_fwd_chunked_mlstm_workspace_size.argtypes = [i] * 7
+        L.lr_step_mlstm.restype = i
+        L.lr_step_mlstm.argtypes = [vp] * 9 + [i] * 4 + [i, vp]
         L.lr_status_string.restype = ctypes.c_char_p
         L.lr_status_string.argtypes = [i]
         L.lr_abi_version.restype = i
@@ -388,3 +397,77 @@ def lr_step_fused(q, k, v, alpha, beta, S, *, mode=GATED_DELTA, flags=0, alpha_s
     if st != 0:
         raise LrError(st, "lr_step_fused")
     return o
+
+
+def mlstm_workspace_size(B, H, T, dk, dv, dtype, chunk=64) -> int:
+    """lr_fwd_chunked_mlstm_workspace_size for these sizes."""
+    import torch
+    dt = F32 if dtype == torch.float32 else BF16
+    return int(lib().lr_fwd_chunked_mlstm_workspace_size(B, H, T, dk, dv, int(chunk), dt))
+
+
+def lr_fwd_chunked_mlstm(q, k, v, fgate, igate, C0=None, n0=None, m0=None, *, chunk=64, h=None,
+                         C_T=None, n_T=None, m_T=None, workspace=None, stream=None):
+    """mLSTM memory over whole sequences (``lr_fwd_chunked_mlstm`` in include/lr.h).
+
+    q, k: [B,H,T,dk]; v: [B,H,T,dv] (float32 or bfloat16); fgate, igate:
+    [B,H,T] float32 (forget gate in (0,1], input-gate pre-activation); the
+    stabilised state (C0 [B,H,dv,dk], n0 [B,H,dk], m0 [B,H]) float32 or all
+    None for the empty memory.  Returns (h, C_T, n_T, m_T).
+    """
+    import torch
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _check(q, "q", (B, H, T, dk), q.dtype, dev)
+    _check(k, "k", (B, H, T, dk), q.dtype, dev)
+    _check(v, "v", (B, H, T, dv), q.dtype, dev)
+    _check(fgate, "fgate", (B, H, T), torch.float32, dev)
+    _check(igate, "igate", (B, H, T), torch.float32, dev)
+    if C0 is not None:
+        _check(C0, "C0", (B, H, dv, dk), torch.float32, dev)
+        _check(n0, "n0", (B, H, dk), torch.float32, dev)
+        _check(m0, "m0", (B, H), torch.float32, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    h = torch.empty((B, H, T, dv), dtype=q.dtype, device=dev) if h is None else h
+    C_T = torch.empty((B, H, dv, dk), **f32) if C_T is None else C_T
+    n_T = torch.empty((B, H, dk), **f32) if n_T is None else n_T
+    m_T = torch.empty((B, H), **f32) if m_T is None else m_T
+    need = int(lib().lr_fwd_chunked_mlstm_workspace_size(B, H, T, dk, dv, int(chunk), dt))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().lr_fwd_chunked_mlstm(_ptr(q), _ptr(k), _ptr(v), _ptr(fgate), _ptr(igate), _ptr(C0),
+                                    _ptr(n0), _ptr(m0), _ptr(h), _ptr(C_T), _ptr(n_T), _ptr(m_T),
+                                    B, H, T, dk, dv, int(chunk), dt, _ptr(workspace), ws_bytes,
+                                    _stream_handle(stream, dev))
+    if st != 0:
+        raise LrError(st, "lr_fwd_chunked_mlstm")
+    return h, C_T, n_T, m_T
+
+
+def lr_step_mlstm(q, k, v, fgate, igate, C, n, m, *, h=None, stream=None):
+    """One mLSTM step (``lr_step_mlstm``); (C, n, m) updated in place.
+    q, k: [N,H,dk]; v: [N,H,dv]; fgate, igate: [N,H]; C [N,H,dv,dk], n [N,H,dk],
+    m [N,H] float32.  Returns h: [N,H,dv]."""
+    import torch
+    dev = q.device
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _check(k, "k", (N, H, dk), q.dtype, dev)
+    _check(v, "v", (N, H, dv), q.dtype, dev)
+    _check(fgate, "fgate", (N, H), torch.float32, dev)
+    _check(igate, "igate", (N, H), torch.float32, dev)
+    _check(C, "C", (N, H, dv, dk), torch.float32, dev)
+    _check(n, "n", (N, H, dk), torch.float32, dev)
+    _check(m, "m", (N, H), torch.float32, dev)
+    h = torch.empty((N, H, dv), dtype=q.dtype, device=dev) if h is None else h
+    st = lib().lr_step_mlstm(_ptr(q), _ptr(k), _ptr(v), _ptr(fgate), _ptr(igate), _ptr(C), _ptr(n),
+                             _ptr(m), _ptr(h), N, H, dk, dv, dt, _stream_handle(stream, dev))
+    if st != 0:
+        raise LrError(st, "lr_step_mlstm")
+    return h

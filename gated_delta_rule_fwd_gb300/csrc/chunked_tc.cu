@@ -909,6 +909,189 @@ chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws
     if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
+// ==================================================================== mLSTM
+// The mLSTM memory (page "Le architetture lineari: RetNet, RWKV, xLSTM", xLSTM
+// section) in its stabilised form: with F_t the cumulative log forget gate of
+// block j, m_prev the stabiliser at the block start (given) and
+// m_t = max(F_t + m_prev, max_{s<=t} (F_t - F_s + igate_s)),
+//   numerator  g'_t (Q C~^T)_t + sum_s P_ts v_s,   g'_t = e^{F_t + m_prev - m_t},
+//              P_ts = (q_t . k_s) e^{F_t - F_s + igate_s - m_t}   (s <= t)
+//   normaliser g'_t (n~ . q_t) + sum_s P_ts
+//   carry      C~ <- g_C C~ + V^T diag(kd) K,  n~ <- g_C n~ + K^T kd,
+//              g_C = e^{F_C + m_prev - m_C},  kd_s = e^{F_C - F_s + igate_s - m_C}.
+// Every exponent is <= 0.  The numerator is the scan without delta with these
+// factors in the records (g' for the output rows, kd for Delta C, g_C for the
+// state); this pass also writes, per block, the row sums of P, m_t and
+// Delta n = K^T kd for the normaliser pass.  A final short block is padded
+// with log f = 0 and igate = -inf, which changes nothing.
+// floats per block of the aux record: row sums [64] at 0, m_t [64] at 64, g'_t [64] at 128,
+// g_C at 192, Delta n [<= 128] at 256 (the same constants are in mlstm.cu)
+constexpr int kMlstmAux = 384, kAuxRs = 0, kAuxM = 64, kAuxG = 128, kAuxGC = 192, kAuxDn = 256;
+
+template <int DK>
+__global__ void __launch_bounds__(NT)
+chunk_prep_mlstm_kernel(const float *__restrict__ fgate, const float *__restrict__ igate,
+                        const float *__restrict__ m_prev_all, uint8_t *__restrict__ ws,
+                        float *__restrict__ aux_all, int H, int T, int nblk,
+                        const __grid_constant__ CUtensorMap tmq,
+                        const __grid_constant__ CUtensorMap tmk) {
+    using L = PrepLayout<DK>;
+    using R = Rec<DK>;
+    extern __shared__ uint8_t sm_raw[];
+    uint8_t *sm = align1024(sm_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int blk = blockIdx.x;
+    const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
+    const int t0 = blk * C;
+    const int n = min(C, T - t0);
+    uint8_t *rec = ws + (bh * (nblk + 1) + blk) * (size_t)R::BYTES;
+    uint8_t *rec_next = rec + R::BYTES;
+    float *vn = reinterpret_cast<float *>(rec_next + R::VEC);
+    float *aux = aux_all + (bh * nblk + blk) * kMlstmAux;
+    uint8_t *QK = sm + L::QK;
+    float *Sv = reinterpret_cast<float *>(sm + L::AT);  // scratch vectors (the A region is unused)
+    float *At = Sv, *Bs = Sv + 64, *kdv = Sv + 128, *red = Sv + 192;  // F_t - m_t, igate_s - F_s, kd_s
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 32);
+    const float m_prev = m_prev_all[bh * nblk + blk];
+
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+        mbar_expect_tx(&bar[1], 2u * (uint32_t)L::KB * 8192u);
+#pragma unroll
+        for (int kb = 0; kb < L::KB; ++kb) {
+            tma_load_3d(QK + kb * 16384, &tmq, kb * 64, t0, (int)bh, &bar[1]);
+            tma_load_3d(QK + kb * 16384 + 8192, &tmk, kb * 64, t0, (int)bh, &bar[1]);
+        }
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 128);
+        tmem_relinquish();
+    }
+    // ---- gates (warps 0-1, token = tid): F_t by a scan of log f, the prefix
+    //      max of igate_s - F_s, then m_t and the factors
+    float F = 0.f, X = -INFINITY;
+    if (tid < C) {
+        const float lf = tid < n ? __logf(fgate[bh * T + t0 + tid]) : 0.f;
+        const float ig = tid < n ? igate[bh * T + t0 + tid] : -INFINITY;
+        F = lf;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, F, d);
+            if (lane >= d) F += y;
+        }
+        X = ig - F;  // with the warp-local F; corrected below for warp 1
+        if (warp == 0) red[lane] = F;  // warp 0's inclusive sums
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid < C) {
+        if (warp == 1) {
+            F += red[31];
+            X -= red[31];
+        }
+        float mx = X;  // inclusive prefix max within the warp
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, mx, d);
+            if (lane >= d) mx = fmaxf(mx, y);
+        }
+        if (warp == 0 && lane == 31) red[32] = mx;
+        Bs[tid] = X;
+        red[64 + tid] = F;
+        red[128 + tid] = mx;  // before warp 1 combines with warp 0's maximum
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const float FC = red[64 + 63];
+    float mC;
+    {
+        const float mx63 = fmaxf(red[128 + 63], red[32]);
+        mC = fmaxf(FC + m_prev, FC + mx63);
+    }
+    if (tid < C) {
+        const float mx = warp == 1 ? fmaxf(red[128 + tid], red[32]) : red[128 + tid];
+        const float mt = fmaxf(F + m_prev, F + mx);
+        At[tid] = F - mt;
+        const float gp = __expf(F + m_prev - mt);  // 0 when the memory is empty
+        vn[kVgPrev + tid] = gp;
+        const float kd = __expf(FC - mC + Bs[tid]);
+        kdv[tid] = kd;
+        vn[kVkdPrev + tid] = kd;
+        aux[kAuxM + tid] = mt;
+        aux[kAuxG + tid] = gp;
+        if (tid == 0) {
+            const float gc = __expf(FC + m_prev - mC);
+            vn[kVgCPrev] = gc;
+            aux[kAuxGC] = gc;
+        }
+    }
+    if (blk == 0) {  // stage 0 has no previous block
+        float *v0 = reinterpret_cast<float *>(rec + R::VEC);
+        if (tid < 2 * C) v0[tid] = 1.f;
+        if (tid == 0) v0[kVgCPrev] = 1.f;
+    }
+    bool ok = mbar_wait(&bar[1], 0);
+    tc_fence_before();
+    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+
+    // ---- Delta n = K^T kd (thread = key channel)
+    if (ok && tid < DK) {
+        float acc = 0.f;
+#pragma unroll 8
+        for (int s2 = 0; s2 < C; ++s2)
+            acc += kdv[s2] * __bfloat162float(*reinterpret_cast<const bf16 *>(
+                                 QK + sw128_offset(64 + s2, tid, 128)));
+        aux[kAuxDn + tid] = acc;
+    }
+    // ---- E1: [Q; K] K^T -> TMEM cols [0, 64) (only the Q rows are used)
+    if (tid == 0 && ok) {
+        const uint32_t id = idesc_bf16_f32(128, 64);
+#pragma unroll
+        for (int ks = 0; ks < DK / 16; ++ks)
+            mma_bf16(tmem, tile_desc(smem_u32(QK), 128, 0, ks), tile_desc(smem_u32(QK), 128, 64, ks),
+                     id, ks > 0);
+        mma_commit(&bar[0]);
+    }
+    ok = __syncthreads_and((ok && mbar_wait(&bar[0], 0)) ? 1 : 0) != 0;
+    tc_fence_after();
+    // ---- P rows (bf16, to the next stage's record) and their fp32 sums
+    if (ok && warp < 2) {
+        const int r = 32 * warp + lane;
+        const float ar = At[r];
+        float rs = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float a[32];
+            tmem_ld32(tmem + lane_base + 32 * half, a);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int i = half * 32 + e;
+                a[e] = i <= r ? a[e] * __expf(ar + Bs[i]) : 0.f;
+                rs += a[e];
+            }
+#pragma unroll
+            for (int i8 = 0; i8 < 4; ++i8)
+                *reinterpret_cast<uint4 *>(rec_next + R::TZP +
+                                           sw128_offset(128 + r, half * 32 + i8 * 8, 192)) =
+                    pack8(a + i8 * 8);
+        }
+        aux[kAuxRs + r] = rs;
+    }
+    if (!ok && lane == 0) atomicExch(&g_tc_error, 1);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
 // ===================================================================== scan
 
 template <int DK>
@@ -1475,6 +1658,35 @@ cudaError_t launch_diag(const void *q, const void *k, const void *v, const float
     return cudaGetLastError();
 }
 
+// mLSTM: the per-block pass, then the scan without delta (the numerator).
+template <int DK>
+cudaError_t launch_mlstm_dk(const void *q, const void *k, const void *v, const float *fgate,
+                            const float *igate, const float *m_prev, const float *C0, void *h,
+                            float *C_T, float *aux, int B, int H, int T, int dv, void *ws,
+                            cudaStream_t stream, int slot) {
+    const int nblk = (T + C - 1) / C;
+    auto prep = chunk_prep_mlstm_kernel<DK>;
+    auto scan = chunk_scan_kernel<DK, true, false>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(prep), PrepLayout<DK>::ALLOC,
+                                     slot);
+    if (e != cudaSuccess) return e;
+    e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC, slot + 1);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tmq, tmk, tmv;
+    if ((e = make_rows_map(&tmq, q, DK, T, B * H)) != cudaSuccess) return e;
+    if ((e = make_rows_map(&tmk, k, DK, T, B * H)) != cudaSuccess) return e;
+    if ((e = make_rows_map(&tmv, v, dv, T, B * H)) != cudaSuccess) return e;
+    prep<<<dim3(nblk, H, B), NT, PrepLayout<DK>::ALLOC, stream>>>(
+        fgate, igate, m_prev, static_cast<uint8_t *>(ws), aux, H, T, nblk, tmq, tmk);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    scan<<<dim3(dv / DVS, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
+        static_cast<const uint8_t *>(ws), C0, static_cast<bf16 *>(h), C_T, H, T, dv, nblk,
+        static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), static_cast<const bf16 *>(v),
+        tmq, tmk, tmv);
+    return cudaGetLastError();
+}
+
 template <int DK, bool ALPHA, bool DELTA>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *alpha,
                          const float *beta, const float *S0, void *o, float *S_T, int B, int H,
@@ -1571,6 +1783,26 @@ cudaError_t launch_chunked_tc(const void *q, const void *k, const void *v, const
     default:
         return launch_mode<128>(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dv, mode, fz, ws,
                                 stream, 40);
+    }
+}
+
+size_t records_bytes_tc(int B, int H, int T, int dk) { return records_bytes(B, H, T, dk); }
+
+// Attribute slots 136..141 belong to the mLSTM launch.
+cudaError_t launch_mlstm_tc(const void *q, const void *k, const void *v, const float *fgate,
+                            const float *igate, const float *m_prev, const float *C0, void *h,
+                            float *C_T, float *aux, int B, int H, int T, int dk, int dv, void *ws,
+                            cudaStream_t stream) {
+    switch (dk) {
+    case 32:
+        return launch_mlstm_dk<32>(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, B, H, T, dv, ws,
+                                   stream, 136);
+    case 64:
+        return launch_mlstm_dk<64>(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, B, H, T, dv, ws,
+                                   stream, 138);
+    default:
+        return launch_mlstm_dk<128>(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, B, H, T, dv, ws,
+                                    stream, 140);
     }
 }
 

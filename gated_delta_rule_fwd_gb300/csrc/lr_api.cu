@@ -79,10 +79,18 @@ bool count_ok(long long a, long long b, long long c, long long d) {
 }
 
 __global__ void copy_state_kernel(const float *__restrict__ src, float *__restrict__ dst,
-                                  size_t n) {
+                                  size_t n, float fill = 0.f) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
          i += (size_t)gridDim.x * blockDim.x)
-        dst[i] = src ? src[i] : 0.f;
+        dst[i] = src ? src[i] : fill;
+}
+
+cudaError_t copy_state(const float *src, float *dst, size_t n, cudaStream_t stream,
+                       float fill = 0.f) {
+    if (src == dst || n == 0) return cudaSuccess;
+    const size_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    copy_state_kernel<<<(unsigned)blocks, 256, 0, stream>>>(src, dst, n, fill);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -219,6 +227,96 @@ lr_status lr_fwd_chunked(const void *q, const void *k, const void *v, const floa
                          void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     return lr_fwd_chunked_fused(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, chunk, dt, mode,
                                 nullptr, workspace, workspace_bytes, stream);
+}
+
+size_t lr_fwd_chunked_mlstm_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
+                                           lr_dtype dt) {
+    if (check_chunked_shape(B, H, T, dk, dv, chunk, dt, LR_MODE_DECAY) != LR_OK) return 0;
+    if (dt != LR_DT_BF16 || T == 0) return 0;
+    return mlstm_workspace_bytes(B, H, T, dk);
+}
+
+lr_status lr_fwd_chunked_mlstm(const void *q, const void *k, const void *v, const float *fgate,
+                               const float *igate, const float *C0, const float *n0,
+                               const float *m0, void *h, float *C_T, float *n_T, float *m_T,
+                               int B, int H, int T, int dk, int dv, int chunk, lr_dtype dt,
+                               void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    const lr_status shape = check_chunked_shape(B, H, T, dk, dv, chunk, dt, LR_MODE_DECAY);
+    if (shape != LR_OK) return shape;
+    if (!C_T || !n_T || !m_T) return LR_ERR_NULL;
+    if ((C0 || n0 || m0) && !(C0 && n0 && m0)) return LR_ERR_NULL;
+    if (T > 0 && (!q || !k || !v || !h || !fgate || !igate)) return LR_ERR_NULL;
+    const size_t need = lr_fwd_chunked_mlstm_workspace_size(B, H, T, dk, dv, chunk, dt);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return LR_ERR_WORKSPACE;
+    for (const void *p : {q, k, v, (const void *)fgate, (const void *)igate, (const void *)C0,
+                          (const void *)n0, (const void *)m0, (const void *)h, (const void *)C_T,
+                          (const void *)n_T, (const void *)m_T})
+        if (!aligned16(p)) return LR_ERR_ALIGN;
+    if (need > 0 && !aligned16(workspace)) return LR_ERR_ALIGN;
+
+    const size_t es = dt == LR_DT_F32 ? 4 : 2;
+    const size_t bh = (size_t)B * H, bht = bh * T;
+    const Span sq = span(q, bht * dk * es), sk = span(k, bht * dk * es), sv = span(v, bht * dv * es);
+    const Span sf = span(fgate, bht * 4), si = span(igate, bht * 4);
+    const Span c0 = span(C0, bh * dv * dk * 4), n0s = span(n0, bh * dk * 4), m0s = span(m0, bh * 4);
+    const Span sh = span(h, bht * dv * es), ct = span(C_T, bh * dv * dk * 4),
+               nt = span(n_T, bh * dk * 4), mt = span(m_T, bh * 4);
+    const Span sw = span(need > 0 ? workspace : nullptr, need);
+    for (Span in : {sq, sk, sv, sf, si, c0, n0s, m0s, ct, nt, mt, sw})
+        if (overlap(sh, in)) return LR_ERR_ALIAS;
+    // each final state may be its own initial state, and overlaps nothing else
+    const Span outs[3] = {ct, nt, mt};
+    const void *own[3] = {C0, n0, m0};
+    const void *outp[3] = {C_T, n_T, m_T};
+    const Span ins[3] = {c0, n0s, m0s};
+    for (int a = 0; a < 3; ++a) {
+        for (Span in : {sq, sk, sv, sf, si, sw})
+            if (overlap(outs[a], in)) return LR_ERR_ALIAS;
+        for (int b = 0; b < 3; ++b) {
+            if (b != a && overlap(outs[a], outs[b])) return LR_ERR_ALIAS;
+            if (overlap(outs[a], ins[b]) && !(a == b && own[a] == outp[a])) return LR_ERR_ALIAS;
+        }
+    }
+    for (Span in : {sq, sk, sv, sf, si, c0, n0s, m0s})
+        if (overlap(sw, in)) return LR_ERR_ALIAS;
+
+    cudaError_t e;
+    if (T == 0) {
+        e = copy_state(C0, C_T, bh * dv * dk, stream);
+        if (e == cudaSuccess) e = copy_state(n0, n_T, bh * dk, stream);
+        if (e == cudaSuccess) e = copy_state(m0, m_T, bh, stream, -INFINITY);
+    } else {
+        e = launch_mlstm_chunked(q, k, v, fgate, igate, C0, n0, m0, h, C_T, n_T, m_T, B, H, T, dk,
+                                 dv, dt, workspace, stream);
+    }
+    return e == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+}
+
+lr_status lr_step_mlstm(const void *q, const void *k, const void *v, const float *fgate,
+                        const float *igate, float *C, float *n, float *m, void *h, int N, int H,
+                        int dk, int dv, lr_dtype dt, cudaStream_t stream) {
+    if (dt != LR_DT_F32 && dt != LR_DT_BF16) return LR_ERR_DTYPE;
+    if (N < 1 || H < 1 || dk < 1 || dv < 1) return LR_ERR_SHAPE;
+    if (!count_ok(N, H, dv, dk) || (long long)N * H > 0x7fffffffll) return LR_ERR_SHAPE;
+    if (!supported_dim(dk) || !supported_dim(dv)) return LR_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !fgate || !igate || !C || !n || !m || !h) return LR_ERR_NULL;
+    for (const void *p : {q, k, v, (const void *)fgate, (const void *)igate, (const void *)C,
+                          (const void *)n, (const void *)m, (const void *)h})
+        if (!aligned16(p)) return LR_ERR_ALIGN;
+    const size_t es = dt == LR_DT_F32 ? 4 : 2;
+    const size_t nh = (size_t)N * H;
+    const Span sq = span(q, nh * dk * es), sk = span(k, nh * dk * es), sv = span(v, nh * dv * es);
+    const Span sf = span(fgate, nh * 4), si = span(igate, nh * 4), sh = span(h, nh * dv * es);
+    const Span sc = span(C, nh * dv * dk * 4), sn = span(n, nh * dk * 4), sm = span(m, nh * 4);
+    for (Span in : {sq, sk, sv, sf, si, sc, sn, sm})
+        if (overlap(sh, in)) return LR_ERR_ALIAS;
+    for (Span st : {sc, sn, sm})
+        for (Span in : {sq, sk, sv, sf, si})
+            if (overlap(st, in)) return LR_ERR_ALIAS;
+    if (overlap(sc, sn) || overlap(sc, sm) || overlap(sn, sm)) return LR_ERR_ALIAS;
+    const cudaError_t e = launch_mlstm_step(q, k, v, fgate, igate, C, n, m, h, N, H, dk, dv, dt,
+                                            stream);
+    return e == cudaSuccess ? LR_OK : LR_ERR_CUDA;
 }
 
 lr_status lr_device_status(void) {

@@ -114,6 +114,27 @@ cudaError_t launch_chunked_tc(const void *q, const void *k, const void *v, const
 // for the diagonal gate or when the flags ask for SiLU + L2).
 size_t chunked_tc_workspace_bytes(int B, int H, int T, int dk, lr_mode mode, unsigned flags);
 
+// mLSTM (mlstm.cu).  Workspace of the bf16 path, and the launchers.
+size_t mlstm_workspace_bytes(int B, int H, int T, int dk);
+cudaError_t launch_mlstm_chunked(const void *q, const void *k, const void *v, const float *fgate,
+                                 const float *igate, const float *C0, const float *n0,
+                                 const float *m0, void *h, float *C_T, float *n_T, float *m_T,
+                                 int B, int H, int T, int dk, int dv, lr_dtype dt, void *ws,
+                                 cudaStream_t stream);
+cudaError_t launch_mlstm_step(const void *q, const void *k, const void *v, const float *fgate,
+                              const float *igate, float *C, float *n, float *m, void *h, int N,
+                              int H, int dk, int dv, lr_dtype dt, cudaStream_t stream);
+
+// The bf16 per-block pass of the mLSTM (chunked_tc.cu): records for the scan
+// without delta (stage layout of lr_fwd_chunked) plus, per block, the fp32
+// aux values [row sums 64][m_t 64][Delta n dk] at `aux`; m_prev [B*H][nblk]
+// the stabiliser at every block start.  Then the scan itself.
+cudaError_t launch_mlstm_tc(const void *q, const void *k, const void *v, const float *fgate,
+                            const float *igate, const float *m_prev, const float *C0, void *h,
+                            float *C_T, float *aux, int B, int H, int T, int dk, int dv, void *ws,
+                            cudaStream_t stream);
+size_t records_bytes_tc(int B, int H, int T, int dk);
+
 // In-place RMSNorm of `rows` rows of dv channels (norm.cu).
 cudaError_t launch_rmsnorm(void *o, const float *w, float eps, size_t rows, int dv, lr_dtype dt,
                            cudaStream_t stream);

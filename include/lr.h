@@ -320,11 +320,69 @@ lr_status lr_step_fused(const void *q, const void *k, const void *v,
                         int N, int H, int dk, int dv, lr_dtype dt, lr_mode mode,
                         const lr_fuse *fuse, cudaStream_t stream);
 
+/*
+ * mLSTM memory (page "Le architetture lineari: RetNet, RWKV, xLSTM", xLSTM
+ * section, the matrix-memory cell): the scalar-gate row with an exponential
+ * write factor and a normaliser,
+ *
+ *     C_t = f_t C_{t-1} + i_t v_t k_t^T,   n_t = f_t n_{t-1} + i_t k_t,   i_t = exp(igate_t),
+ *     h_t = C_t q_t / max(|n_t^T q_t|, 1),
+ *
+ * computed in the stabilised form the page gives: m_t = max(log f_t +
+ * m_{t-1}, igate_t), the memory kept as C~ = e^{-m} C and n~ = e^{-m} n, and
+ * h_t = C~_t q_t / max(|n~_t^T q_t|, e^{-m_t}) (the same output).  The state
+ * the caller passes in and gets back is that stabilised triple.
+ *
+ *   q, k   [B, H, T, dk]   dtype dt
+ *   v      [B, H, T, dv]   dtype dt
+ *   fgate  [B, H, T]       fp32 forget gate f_t in (0, 1]
+ *   igate  [B, H, T]       fp32 input-gate pre-activation (any real)
+ *   C0, n0, m0             [B, H, dv, dk], [B, H, dk], [B, H] fp32: the initial
+ *                          (C~, n~, m), or all three NULL for the empty memory
+ *                          (C = 0, n = 0, m = -inf: the first token's m is its igate)
+ *   h      [B, H, T, dv]   dtype dt, written; must not overlap any input
+ *   C_T, n_T, m_T          the final (C~, n~, m), written; each may be the same
+ *                          pointer as its initial counterpart (in place)
+ *   workspace              lr_fwd_chunked_mlstm_workspace_size(...) bytes (0 for fp32)
+ *
+ * Sizes and conventions as for lr_fwd_chunked (dk, dv in {32, 64, 128},
+ * chunk == 64, T >= 0).  The bf16 path runs five kernels: the stabiliser at
+ * every block start (it depends on the gates only, so one pass over f and
+ * igate gives it), the per-block pass (scores weighted by
+ * e^{F_t - F_s + igate_s - m_t}, F the cumulative log forget gate of the
+ * block), the sequential pass of lr_fwd_chunked without delta (the numerator),
+ * the normaliser n~ at every block start, and the division of every token's
+ * numerator by its threshold.  The fp32 path is one kernel.
+ */
+lr_status lr_fwd_chunked_mlstm(const void *q, const void *k, const void *v,
+                               const float *fgate, const float *igate,
+                               const float *C0, const float *n0, const float *m0,
+                               void *h, float *C_T, float *n_T, float *m_T,
+                               int B, int H, int T, int dk, int dv, int chunk, lr_dtype dt,
+                               void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes lr_fwd_chunked_mlstm needs (0 for fp32, T == 0, or
+ * arguments it would reject). */
+size_t lr_fwd_chunked_mlstm_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
+                                           lr_dtype dt);
+
+/*
+ * One mLSTM step for N sequences (decode), the state (C, n, m) [N, H, dv, dk],
+ * [N, H, dk], [N, H] updated in place: m' = max(log f + m, igate),
+ * C <- e^{log f + m - m'} C + e^{igate - m'} v k^T (n likewise with k),
+ * h = C q / max(|n^T q|, e^{-m'}).  q, k [N, H, dk]; v, h [N, H, dv] (dtype dt);
+ * fgate, igate [N, H] fp32.  An empty memory is C = 0, n = 0, m = -inf.
+ */
+lr_status lr_step_mlstm(const void *q, const void *k, const void *v, const float *fgate,
+                        const float *igate, float *C, float *n, float *m, void *h, int N,
+                        int H, int dk, int dv, lr_dtype dt, cudaStream_t stream);
+
 /* Static English text for a status code (never NULL). */
 const char *lr_status_string(lr_status s);
 
-/* ABI version of this header: 2 (2 added the fused entry points and
- * LR_ERR_FUSE; every entry point of 1 is unchanged). */
+/* ABI version of this header: 2 (2 added the fused entry points, the
+ * diagonal gate, the mLSTM entry points and LR_ERR_FUSE; every entry point of
+ * 1 is unchanged). */
 int lr_abi_version(void);
 
 #ifdef __cplusplus

@@ -35,6 +35,8 @@ def test_header_declares_expected_entry_points():
                                           "lr_fwd_chunked_noalloc", "lr_step", "lr_device_status",
                                           "lr_fwd_chunked_fused",
                                           "lr_fwd_chunked_fused_workspace_size", "lr_step_fused",
+                                          "lr_fwd_chunked_mlstm",
+                                          "lr_fwd_chunked_mlstm_workspace_size", "lr_step_mlstm",
                                           "lr_status_string", "lr_abi_version"}
 
 
@@ -160,6 +162,35 @@ cases += [
     ("scalar-alpha-span-is-short", chunk(mode=1, o=P(A[3] + 512)), 7),  # passes validation
     ("diag-step-alias-o-alpha", step(mode=4, o=P(A[3] + 64)), 8),
     ("diag-ws-larger", int(L.lr_fwd_chunked_workspace_size(1, 1, 8, 32, 32, 64, 1, 4) - need), 2 * 8 * 32 * 2),
+]
+# mLSTM: q k v fgate igate C0 n0 m0 h C_T n_T m_T
+M = [P(0x10000000 + i * 0x10000000) for i in range(12)]
+def ml(**kw):
+    a = dict(zip("q k v f i C0 n0 m0 h CT nT mT".split(), M))
+    a.update(dict(B=1, H=1, T=8, dk=32, dv=32, chunk=64, dt=0, ws=None, wsb=0))
+    a.update(kw)
+    return L.lr_fwd_chunked_mlstm(a["q"], a["k"], a["v"], a["f"], a["i"], a["C0"], a["n0"],
+                                  a["m0"], a["h"], a["CT"], a["nT"], a["mT"], a["B"], a["H"],
+                                  a["T"], a["dk"], a["dv"], a["chunk"], a["dt"], a["ws"],
+                                  a["wsb"], None)
+def mls(**kw):
+    a = dict(zip("q k v f i C n m h".split(), M))
+    a.update(dict(N=1, H=1, dk=32, dv=32, dt=1))
+    a.update(kw)
+    return L.lr_step_mlstm(a["q"], a["k"], a["v"], a["f"], a["i"], a["C"], a["n"], a["m"], a["h"],
+                           a["N"], a["H"], a["dk"], a["dv"], a["dt"], None)
+mneed = L.lr_fwd_chunked_mlstm_workspace_size(1, 1, 8, 32, 32, 64, 1)
+cases += [
+    ("mlstm-null-fgate", ml(f=None), 1), ("mlstm-null-mT", ml(mT=None), 1),
+    ("mlstm-partial-state", ml(n0=None), 1), ("mlstm-dtype", ml(dt=2), 3),
+    ("mlstm-dk48", ml(dk=48), 6), ("mlstm-misaligned", ml(v=P(0x30000008)), 4),
+    ("mlstm-alias-h-q", ml(h=M[0]), 8), ("mlstm-alias-CT-n0", ml(CT=M[6]), 8),
+    ("mlstm-ws-null-bf16", ml(dt=1), 10),
+    ("mlstm-in-place-ok", ml(CT=M[5], nT=M[6], mT=M[7]), 7),   # passes validation, no GPU
+    ("mlstm-ws-positive", int(mneed > 0), 1),
+    ("mlstm-ws-f32", L.lr_fwd_chunked_mlstm_workspace_size(1, 1, 8, 32, 32, 64, 0), 0),
+    ("mlstm-step-null", mls(n=None), 1), ("mlstm-step-alias-h-C", mls(h=M[5]), 8),
+    ("mlstm-step-dk16", mls(dk=16), 6),
 ]
 bad = [(n, got, want) for n, got, want in cases if got != want]
 print("BAD", bad)

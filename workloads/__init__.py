@@ -78,6 +78,8 @@ WORKLOADS = {
                                 5, "gdn", 0.1, steps=1000),
     # the diagonal gate (GLA row), at the Mamba-2-style workload's size
     "gla_bf16": Workload("gla_bf16", DIAG_DECAY, "bf16", 8, 16, 4096, 128, 128, 64, 6, "gla", 0.0),
+    # the mLSTM memory, same size (mode: the scalar-gate engine; inputs from draw_mlstm)
+    "mlstm_bf16": Workload("mlstm_bf16", DECAY, "bf16", 8, 16, 4096, 128, 128, 64, 7, "mlstm", 0.0),
 }
 
 
@@ -217,6 +219,36 @@ def draw_decode_step_pre(w: Workload, step: int, device, generator=None):
     alpha = 3.0 + torch.randn((N, H), generator=g, device=device)
     dt = w.torch_dtype
     return dict(q=q.to(dt), k=k.to(dt), v=v.to(dt), alpha=alpha.float(), beta=beta.float())
+
+
+def draw_mlstm(B, H, T, dk, dv, seed, dtype=torch.float32, state=False, igate_std=2.0,
+               device="cpu"):
+    """mLSTM inputs (page "Le architetture lineari", xLSTM section): q, k ~
+    N(0,1)/sqrt(dk), v ~ N(0,1) rounded once to ``dtype``; forget gate
+    f = sigmoid(N(3,1)); input-gate pre-activation igate ~ N(0, igate_std^2)
+    (the exponential gate e^igate spans several orders of magnitude); with
+    ``state`` a stabilised initial state C0 ~ N(0, 0.1^2), n0 ~ N(0, 0.1^2),
+    m0 ~ N(0, 1).  Draw order: q, k, v, f, igate, C0, n0, m0.
+    Returns dict q, k, v, fgate, igate, C0, n0, m0 (the last three may be None).
+    """
+    g = torch.Generator("cpu")
+    g.manual_seed(int(seed))
+    s = 1.0 / math.sqrt(dk)
+    q = torch.randn((B, H, T, dk), generator=g) * s
+    k = torch.randn((B, H, T, dk), generator=g) * s
+    v = torch.randn((B, H, T, dv), generator=g)
+    f = torch.sigmoid(3.0 + torch.randn((B, H, T), generator=g))
+    ig = torch.randn((B, H, T), generator=g) * igate_std
+    C0 = n0 = m0 = None
+    if state:
+        C0 = torch.randn((B, H, dv, dk), generator=g) * 0.1
+        n0 = torch.randn((B, H, dk), generator=g) * 0.1
+        m0 = torch.randn((B, H), generator=g)
+    out = dict(q=q.to(dtype), k=k.to(dtype), v=v.to(dtype), fgate=f.float().contiguous(),
+               igate=ig.float().contiguous(), C0=C0, n0=n0, m0=m0)
+    if device != "cpu":
+        out = {n: (t.to(device) if t is not None else None) for n, t in out.items()}
+    return out
 
 
 def draw_workload(w: Workload, device="cpu"):
