@@ -252,6 +252,69 @@ int gdr_oracle_mlstm(int B, int H, int T, int dk, int dv,
     return failed ? 2 : 0;
 }
 
+/*
+ * Generalised delta rule of RWKV-7 (page "Le architetture lineari: RetNet,
+ * RWKV, xLSTM", RWKV section).  The extracted page lost the update equation;
+ * its prose fixes a per-channel decay w_t multiplying the state (near 1 keeps,
+ * near 0 forgets), a normalised removal key kappa_t decoupled from the write
+ * key kw_t, a per-channel in-context learning rate a_t, a transition that is
+ * a diagonal decay plus a rank-one correction with eigenvalues in [-1, 1], and
+ * the chapter's convention (S is d_v x d_k, transitions multiply from the
+ * right).  Read as
+ *
+ *     S_t = S_{t-1} (Diag(w_t) - kappa_t (a_t * kappa_t)^T) + v_t kw_t^T,   o_t = S_t q_t,
+ *
+ * evaluated per value row r with s = S[r,:]:  u = s . kappa_t,
+ * s <- s * w_t - u (a_t * kappa_t) + v_t[r] kw_t.
+ *
+ * Layouts: q, kw, w, kappa, a [B][H][T][dk]; v, o [B][H][T][dv];
+ * S0, ST [B][H][dv][dk] (S0 NULL = zeros).  Returns 0, 1, or 2.
+ */
+int gdr_oracle_gen_delta(int B, int H, int T, int dk, int dv,
+                         const double *q, const double *kw, const double *v,
+                         const double *w, const double *kappa, const double *a,
+                         const double *S0, double *o, double *ST, int num_threads)
+{
+    if (B <= 0 || H <= 0 || T < 0 || dk <= 0 || dv <= 0) return 1;
+    if (!q || !kw || !v || !w || !kappa || !a || !o || !ST) return 1;
+    const int BH = B * H;
+    const size_t sz = (size_t)dv * dk;
+    int failed = 0;
+#ifdef _OPENMP
+    if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads) reduction(| : failed)
+#endif
+    for (int bh = 0; bh < BH; ++bh) {
+        double *S = (double *)malloc(sz * sizeof(double));
+        if (!S) {
+            failed |= 1;
+            continue;
+        }
+        if (S0) memcpy(S, S0 + (size_t)bh * sz, sz * sizeof(double));
+        else memset(S, 0, sz * sizeof(double));
+        for (int t = 0; t < T; ++t) {
+            const size_t it = (size_t)bh * T + t;
+            const double *qt = q + it * dk, *kt = kw + it * dk, *wt = w + it * dk;
+            const double *ct = kappa + it * dk, *at = a + it * dk, *vt = v + it * dv;
+            for (int r = 0; r < dv; ++r) {
+                double *row = S + (size_t)r * dk;
+                double u = 0.0;
+                for (int c = 0; c < dk; ++c) u += row[c] * ct[c];
+                double acc = 0.0;
+                for (int c = 0; c < dk; ++c) {
+                    row[c] = row[c] * wt[c] - u * at[c] * ct[c] + vt[r] * kt[c];
+                    acc += row[c] * qt[c];
+                }
+                o[it * dv + r] = acc;
+            }
+        }
+        memcpy(ST + (size_t)bh * sz, S, sz * sizeof(double));
+        free(S);
+    }
+    (void)num_threads;
+    return failed ? 2 : 0;
+}
+
 /* Number of threads an OpenMP region would use (1 without OpenMP). */
 int gdr_oracle_max_threads(void)
 {
