@@ -37,6 +37,7 @@ DEFAULT_WORKLOAD = "gdn_prefill_bf16"
 DECODE_WORKLOAD = "gdn_decode_bf16"
 DIAG_WORKLOAD = "gla_bf16"
 MLSTM_WORKLOAD = "mlstm_bf16"
+GEN_DELTA_WORKLOAD = "rwkv7_bf16"
 METRIC = "chunked fwd tokens/s"
 UNIT = "tokens/s"
 
@@ -372,9 +373,10 @@ def run_ours(args, dist, rank, world, local):
     diag = None
     if not args.no_diag and w.name != DIAG_WORKLOAD:
         diag = run_diag(lr, dev, dist, args, peaks)
-    mlstm = None
+    mlstm = gen_delta = None
     if not args.no_diag:
         mlstm = run_mlstm(lr, dev, dist, args, peaks)
+        gen_delta = run_gen_delta(lr, dev, dist, args, peaks)
 
     out = None
     if rank == 0:
@@ -419,7 +421,48 @@ def run_ours(args, dist, rank, world, local):
             out["diag"] = diag
         if mlstm is not None:
             out["mlstm"] = mlstm
+        if gen_delta is not None:
+            out["gen_delta"] = gen_delta
     return out
+
+
+def run_gen_delta(lr, dev, dist, args, peaks):
+    """The generalised delta rule (RWKV-7 reading) through
+    lr_fwd_chunked_gen_delta (one CUDA-core launch; no tensor-core path yet).
+    Algorithmic bytes: q, kw, v, o at bf16, w, kappa, a at fp32 per
+    head-token, the state read and written."""
+    w = workloads.WORKLOADS[GEN_DELTA_WORKLOAD]
+    x = workloads.draw_gen_delta(w.B, w.H, w.T, w.dk, w.dv, seed=w.seed, dtype=w.torch_dtype,
+                                 state=True)
+    xd = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.torch_dtype, device=dev)
+    st = torch.empty((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    steps = max(3, min(args.steps, 20))
+
+    def step():
+        lr.lr_fwd_chunked_gen_delta(xd["q"], xd["kw"], xd["v"], xd["w"], xd["kappa"], xd["a"],
+                                    xd["S0"], o=o, S_T=st, stream=stream)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(dist, e0.elapsed_time(e1), dev) / steps
+    world = dist.get_world_size() if dist else 1
+    heads = w.B * w.H
+    nbytes = heads * w.T * (2 * (2 * w.dk + 2 * w.dv) + 12 * w.dk) + 2 * heads * w.dv * w.dk * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"workload": w.name, "entry_point": "lr_fwd_chunked_gen_delta", "B": w.B, "H": w.H,
+            "T": w.T, "dk": w.dk, "dv": w.dv, "value": w.B * w.T * world / (ms / 1e3),
+            "unit": UNIT, "ms_per_step": ms, "steps": steps, "algorithmic_bytes_per_launch": nbytes,
+            "achieved_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "gpu_launches": steps,
+            "path": "CUDA cores, fp32 arithmetic (no tensor-core path yet)"}
 
 
 def run_mlstm(lr, dev, dist, args, peaks):

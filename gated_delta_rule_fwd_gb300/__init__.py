@@ -12,6 +12,9 @@ missing or cannot be loaded, every call raises.
         one decode step for N sequences, S: [N,H,dv,dk] updated in place
     lr_fwd_chunked_mlstm / lr_step_mlstm(q, k, v, fgate, igate, ...)
         the mLSTM memory (exponential write gate, normaliser, stabiliser)
+    lr_fwd_chunked_gen_delta / lr_step_gen_delta(q, kw, v, w, kappa, a, ...)
+        the generalised delta rule of RWKV-7 (per-channel decay plus a rank-one
+        correction)
     lr_fwd_chunked_fused / lr_step_fused(..., flags=..., ...)
         the same with the maps around the recurrence (SiLU + L2 of q and k,
         sigmoid beta, sigmoid or softplus alpha, output RMSNorm) applied inside
@@ -31,6 +34,7 @@ F32, BF16 = 0, 1
 SYMBOLS = ("lr_fwd_chunked", "lr_fwd_chunked_workspace_size", "lr_fwd_chunked_noalloc", "lr_step",
            "lr_fwd_chunked_fused", "lr_fwd_chunked_fused_workspace_size", "lr_step_fused",
            "lr_fwd_chunked_mlstm", "lr_fwd_chunked_mlstm_workspace_size", "lr_step_mlstm",
+           "lr_fwd_chunked_gen_delta", "lr_step_gen_delta",
            "lr_device_status", "lr_status_string", "lr_abi_version")
 # lr_fuse flags (include/lr.h)
 FUSE_QK_SILU_L2 = 0x1
@@ -103,6 +107,10 @@ def lib() -> ctypes.CDLL:
         L.lr_fwd_chunked_mlstm_workspace_size.argtypes = [i] * 7
         L.lr_step_mlstm.restype = i
         L.lr_step_mlstm.argtypes = [vp] * 9 + [i] * 4 + [i, vp]
+        L.lr_fwd_chunked_gen_delta.restype = i
+        L.lr_fwd_chunked_gen_delta.argtypes = [vp] * 9 + [i] * 6 + [i, vp]
+        L.lr_step_gen_delta.restype = i
+        L.lr_step_gen_delta.argtypes = [vp] * 8 + [i] * 4 + [i, vp]
         L.lr_status_string.restype = ctypes.c_char_p
         L.lr_status_string.argtypes = [i]
         L.lr_abi_version.restype = i
@@ -471,3 +479,49 @@ def lr_step_mlstm(q, k, v, fgate, igate, C, n, m, *, h=None, stream=None):
     if st != 0:
         raise LrError(st, "lr_step_mlstm")
     return h
+
+
+def lr_fwd_chunked_gen_delta(q, kw, v, w, kappa, a, S0=None, *, chunk=64, o=None, S_T=None,
+                             stream=None):
+    """Generalised delta rule over whole sequences (``lr_fwd_chunked_gen_delta``).
+    q, kw: [B,H,T,dk]; v: [B,H,T,dv] (float32 or bfloat16); w, kappa, a:
+    [B,H,T,dk] float32; S0: [B,H,dv,dk] float32 or None.  Returns (o, S_T)."""
+    import torch
+    dev = q.device
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _check(kw, "kw", (B, H, T, dk), q.dtype, dev)
+    _check(v, "v", (B, H, T, dv), q.dtype, dev)
+    for t, nm in ((w, "w"), (kappa, "kappa"), (a, "a")):
+        _check(t, nm, (B, H, T, dk), torch.float32, dev)
+    if S0 is not None:
+        _check(S0, "S0", (B, H, dv, dk), torch.float32, dev)
+    o = torch.empty((B, H, T, dv), dtype=q.dtype, device=dev) if o is None else o
+    S_T = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev) if S_T is None else S_T
+    st = lib().lr_fwd_chunked_gen_delta(_ptr(q), _ptr(kw), _ptr(v), _ptr(w), _ptr(kappa), _ptr(a),
+                                        _ptr(S0), _ptr(o), _ptr(S_T), B, H, T, dk, dv, int(chunk),
+                                        dt, _stream_handle(stream, dev))
+    if st != 0:
+        raise LrError(st, "lr_fwd_chunked_gen_delta")
+    return o, S_T
+
+
+def lr_step_gen_delta(q, kw, v, w, kappa, a, S, *, o=None, stream=None):
+    """One generalised-delta step (``lr_step_gen_delta``); S updated in place."""
+    import torch
+    dev = q.device
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _check(kw, "kw", (N, H, dk), q.dtype, dev)
+    _check(v, "v", (N, H, dv), q.dtype, dev)
+    for t, nm in ((w, "w"), (kappa, "kappa"), (a, "a")):
+        _check(t, nm, (N, H, dk), torch.float32, dev)
+    _check(S, "S", (N, H, dv, dk), torch.float32, dev)
+    o = torch.empty((N, H, dv), dtype=q.dtype, device=dev) if o is None else o
+    st = lib().lr_step_gen_delta(_ptr(q), _ptr(kw), _ptr(v), _ptr(w), _ptr(kappa), _ptr(a), _ptr(S),
+                                 _ptr(o), N, H, dk, dv, dt, _stream_handle(stream, dev))
+    if st != 0:
+        raise LrError(st, "lr_step_gen_delta")
+    return o

@@ -319,6 +319,59 @@ lr_status lr_step_mlstm(const void *q, const void *k, const void *v, const float
     return e == cudaSuccess ? LR_OK : LR_ERR_CUDA;
 }
 
+lr_status lr_fwd_chunked_gen_delta(const void *q, const void *kw, const void *v, const float *w,
+                                   const float *kappa, const float *a, const float *S0, void *o,
+                                   float *S_T, int B, int H, int T, int dk, int dv, int chunk,
+                                   lr_dtype dt, cudaStream_t stream) {
+    const lr_status shape = check_chunked_shape(B, H, T, dk, dv, chunk, dt, LR_MODE_DELTA);
+    if (shape != LR_OK) return shape;
+    if (!S_T) return LR_ERR_NULL;
+    if (T > 0 && (!q || !kw || !v || !w || !kappa || !a || !o)) return LR_ERR_NULL;
+    for (const void *p : {q, kw, v, (const void *)w, (const void *)kappa, (const void *)a,
+                          (const void *)S0, (const void *)o, (const void *)S_T})
+        if (!aligned16(p)) return LR_ERR_ALIGN;
+    const size_t es = dt == LR_DT_F32 ? 4 : 2;
+    const size_t bht = (size_t)B * H * T, state = (size_t)B * H * dv * dk * 4;
+    const Span sq = span(q, bht * dk * es), sk = span(kw, bht * dk * es), sv = span(v, bht * dv * es);
+    const Span sw = span(w, bht * dk * 4), sc = span(kappa, bht * dk * 4), sa = span(a, bht * dk * 4);
+    const Span s0 = span(S0, state), so = span(o, bht * dv * es), st = span(S_T, state);
+    for (Span in : {sq, sk, sv, sw, sc, sa, s0, st})
+        if (overlap(so, in)) return LR_ERR_ALIAS;
+    for (Span in : {sq, sk, sv, sw, sc, sa})
+        if (overlap(st, in)) return LR_ERR_ALIAS;
+    if (S0 && S0 != S_T && overlap(s0, st)) return LR_ERR_ALIAS;
+    const cudaError_t e =
+        T == 0 ? copy_state(S0, S_T, (size_t)B * H * dv * dk, stream)
+               : launch_gen_delta_chunked(q, kw, v, w, kappa, a, S0, o, S_T, B, H, T, dk, dv, dt,
+                                          stream);
+    return e == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+}
+
+lr_status lr_step_gen_delta(const void *q, const void *kw, const void *v, const float *w,
+                            const float *kappa, const float *a, float *S, void *o, int N, int H,
+                            int dk, int dv, lr_dtype dt, cudaStream_t stream) {
+    if (dt != LR_DT_F32 && dt != LR_DT_BF16) return LR_ERR_DTYPE;
+    if (N < 1 || H < 1 || dk < 1 || dv < 1) return LR_ERR_SHAPE;
+    if (!count_ok(N, H, dv, dk) || (long long)N * H > 0x7fffffffll) return LR_ERR_SHAPE;
+    if (!supported_dim(dk) || !supported_dim(dv)) return LR_ERR_UNSUPPORTED;
+    if (!q || !kw || !v || !w || !kappa || !a || !S || !o) return LR_ERR_NULL;
+    for (const void *p : {q, kw, v, (const void *)w, (const void *)kappa, (const void *)a,
+                          (const void *)S, (const void *)o})
+        if (!aligned16(p)) return LR_ERR_ALIGN;
+    const size_t es = dt == LR_DT_F32 ? 4 : 2;
+    const size_t nh = (size_t)N * H;
+    const Span sq = span(q, nh * dk * es), sk = span(kw, nh * dk * es), sv = span(v, nh * dv * es);
+    const Span sw = span(w, nh * dk * 4), sc = span(kappa, nh * dk * 4), sa = span(a, nh * dk * 4);
+    const Span ss = span(S, nh * dv * dk * 4), so = span(o, nh * dv * es);
+    for (Span in : {sq, sk, sv, sw, sc, sa, ss})
+        if (overlap(so, in)) return LR_ERR_ALIAS;
+    for (Span in : {sq, sk, sv, sw, sc, sa})
+        if (overlap(ss, in)) return LR_ERR_ALIAS;
+    const cudaError_t e = launch_gen_delta_step(q, kw, v, w, kappa, a, S, o, N, H, dk, dv, dt,
+                                                stream);
+    return e == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+}
+
 lr_status lr_device_status(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return LR_ERR_CUDA;
     const int e = read_and_clear_tc_error();

@@ -135,6 +135,15 @@ cudaError_t launch_mlstm_tc(const void *q, const void *k, const void *v, const f
                             cudaStream_t stream);
 size_t records_bytes_tc(int B, int H, int T, int dk);
 
+// Generalised delta rule of RWKV-7 (gen_delta.cu).
+cudaError_t launch_gen_delta_chunked(const void *q, const void *kw, const void *v, const float *w,
+                                     const float *kappa, const float *a, const float *S0, void *o,
+                                     float *S_T, int B, int H, int T, int dk, int dv, lr_dtype dt,
+                                     cudaStream_t stream);
+cudaError_t launch_gen_delta_step(const void *q, const void *kw, const void *v, const float *w,
+                                  const float *kappa, const float *a, float *S, void *o, int N,
+                                  int H, int dk, int dv, lr_dtype dt, cudaStream_t stream);
+
 // In-place RMSNorm of `rows` rows of dv channels (norm.cu).
 cudaError_t launch_rmsnorm(void *o, const float *w, float eps, size_t rows, int dv, lr_dtype dt,
                            cudaStream_t stream);

@@ -377,6 +377,42 @@ lr_status lr_step_mlstm(const void *q, const void *k, const void *v, const float
                         const float *igate, float *C, float *n, float *m, void *h, int N,
                         int H, int dk, int dv, lr_dtype dt, cudaStream_t stream);
 
+/*
+ * Generalised delta rule of RWKV-7 (page "Le architetture lineari: RetNet,
+ * RWKV, xLSTM", RWKV section: a per-channel decay plus a rank-one correction
+ * with a normalised removal key decoupled from the write key and a
+ * per-channel in-context learning rate; eigenvalues anywhere in [-1, 1]).
+ * The extracted page lost the equation; this library reads it, in the
+ * convention of lr_mode (S is d_v x d_k, transitions multiply from the
+ * right), as
+ *
+ *     S_t = S_{t-1} (Diag(w_t) - kappa_t (a_t * kappa_t)^T) + v_t kw_t^T,   o_t = S_t q_t.
+ *
+ *   q, kw       [B, H, T, dk]   dtype dt (query and write key)
+ *   v, o        [B, H, T, dv]   dtype dt
+ *   w, kappa, a [B, H, T, dk]   fp32 (decay in (0, 1], removal key, rate)
+ *   S0, S_T     [B, H, dv, dk]  fp32 (S0 NULL = zeros; S_T may be S0)
+ *
+ * Sizes and conventions as for lr_fwd_chunked; no workspace.  Computed on
+ * the CUDA cores in fp32 (bf16 inputs are widened) in 32-token blocks: a
+ * unit-lower-triangular system for the pseudo-values u_t = S_{t-1} kappa_t
+ * per block, every decay factor e^{L_t - L_s} (t >= s) at most 1.  No
+ * tensor-core path for this row yet.
+ */
+lr_status lr_fwd_chunked_gen_delta(const void *q, const void *kw, const void *v,
+                                   const float *w, const float *kappa, const float *a,
+                                   const float *S0, void *o, float *S_T,
+                                   int B, int H, int T, int dk, int dv, int chunk, lr_dtype dt,
+                                   cudaStream_t stream);
+
+/* One step of the same rule for N sequences (decode): per value row r with
+ * s = S[r, :], u = s . kappa, S[r, :] <- s * w - u (a * kappa) + v_r kw,
+ * o_r = S[r, :] . q.  q, kw, w, kappa, a [N, H, dk] (q, kw in dtype dt, the
+ * rest fp32); v, o [N, H, dv]; S [N, H, dv, dk] fp32 updated in place. */
+lr_status lr_step_gen_delta(const void *q, const void *kw, const void *v, const float *w,
+                            const float *kappa, const float *a, float *S, void *o, int N, int H,
+                            int dk, int dv, lr_dtype dt, cudaStream_t stream);
+
 /* Static English text for a status code (never NULL). */
 const char *lr_status_string(lr_status s);
 

@@ -37,6 +37,7 @@ def test_header_declares_expected_entry_points():
                                           "lr_fwd_chunked_fused_workspace_size", "lr_step_fused",
                                           "lr_fwd_chunked_mlstm",
                                           "lr_fwd_chunked_mlstm_workspace_size", "lr_step_mlstm",
+                                          "lr_fwd_chunked_gen_delta", "lr_step_gen_delta",
                                           "lr_status_string", "lr_abi_version"}
 
 
@@ -191,6 +192,20 @@ cases += [
     ("mlstm-ws-f32", L.lr_fwd_chunked_mlstm_workspace_size(1, 1, 8, 32, 32, 64, 0), 0),
     ("mlstm-step-null", mls(n=None), 1), ("mlstm-step-alias-h-C", mls(h=M[5]), 8),
     ("mlstm-step-dk16", mls(dk=16), 6),
+]
+def gd(**kw):
+    a = dict(zip("q kw v w kap a S0 o ST".split(), M[:9]))
+    a.update(dict(B=1, H=1, T=8, dk=32, dv=32, chunk=64, dt=0))
+    a.update(kw)
+    return L.lr_fwd_chunked_gen_delta(a["q"], a["kw"], a["v"], a["w"], a["kap"], a["a"], a["S0"],
+                                      a["o"], a["ST"], a["B"], a["H"], a["T"], a["dk"], a["dv"],
+                                      a["chunk"], a["dt"], None)
+cases += [
+    ("gd-null-kappa", gd(kap=None), 1), ("gd-dk48", gd(dk=48), 6), ("gd-chunk32", gd(chunk=32), 6),
+    ("gd-alias-o-w", gd(o=P(0x40000000 + 512)), 8), ("gd-misaligned", gd(a=P(0x60000004)), 4),
+    ("gd-valid", gd(), 7),   # passes validation, no GPU
+    ("gd-step-null", L.lr_step_gen_delta(M[0], M[1], M[2], M[3], M[4], None, M[6], M[7], 1, 1, 32,
+                                         32, 1, None), 1),
 ]
 bad = [(n, got, want) for n, got, want in cases if got != want]
 print("BAD", bad)

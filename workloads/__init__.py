@@ -80,6 +80,8 @@ WORKLOADS = {
     "gla_bf16": Workload("gla_bf16", DIAG_DECAY, "bf16", 8, 16, 4096, 128, 128, 64, 6, "gla", 0.0),
     # the mLSTM memory, same size (mode: the scalar-gate engine; inputs from draw_mlstm)
     "mlstm_bf16": Workload("mlstm_bf16", DECAY, "bf16", 8, 16, 4096, 128, 128, 64, 7, "mlstm", 0.0),
+    # the generalised delta rule of RWKV-7 (inputs from draw_gen_delta; CUDA-core path)
+    "rwkv7_bf16": Workload("rwkv7_bf16", DELTA, "bf16", 2, 16, 4096, 128, 128, 64, 8, "gd", 0.1),
 }
 
 
@@ -246,6 +248,31 @@ def draw_mlstm(B, H, T, dk, dv, seed, dtype=torch.float32, state=False, igate_st
         m0 = torch.randn((B, H), generator=g)
     out = dict(q=q.to(dtype), k=k.to(dtype), v=v.to(dtype), fgate=f.float().contiguous(),
                igate=ig.float().contiguous(), C0=C0, n0=n0, m0=m0)
+    if device != "cpu":
+        out = {n: (t.to(device) if t is not None else None) for n, t in out.items()}
+    return out
+
+
+def draw_gen_delta(B, H, T, dk, dv, seed, dtype=torch.float32, state=False, device="cpu"):
+    """Generalised-delta (RWKV-7) inputs: q, kw ~ N(0,1)/sqrt(dk), v ~ N(0,1)
+    rounded once to ``dtype``; decay w = exp(-e^{-1/2} sigmoid(N(0,1))) in
+    (0.54, 1); removal key kappa = N(0,1) normalised per token; rate
+    a = sigmoid(N(0,1)) per channel; with ``state`` S0 ~ N(0, 0.1^2).
+    Draw order: q, kw, v, w, kappa, a, S0."""
+    g = torch.Generator("cpu")
+    g.manual_seed(int(seed))
+    s = 1.0 / math.sqrt(dk)
+    shp = (B, H, T, dk)
+    q = torch.randn(shp, generator=g) * s
+    kw = torch.randn(shp, generator=g) * s
+    v = torch.randn((B, H, T, dv), generator=g)
+    w = torch.exp(-math.exp(-0.5) * torch.sigmoid(torch.randn(shp, generator=g)))
+    kap = torch.randn(shp, generator=g)
+    kap = kap / torch.linalg.vector_norm(kap, dim=-1, keepdim=True)
+    a = torch.sigmoid(torch.randn(shp, generator=g))
+    S0 = torch.randn((B, H, dv, dk), generator=g) * 0.1 if state else None
+    out = dict(q=q.to(dtype), kw=kw.to(dtype), v=v.to(dtype), w=w.float().contiguous(),
+               kappa=kap.float().contiguous(), a=a.float().contiguous(), S0=S0)
     if device != "cpu":
         out = {n: (t.to(device) if t is not None else None) for n, t in out.items()}
     return out
