@@ -45,13 +45,12 @@ UNIT = "tokens/s"
 # DRAM traffic per lr_fwd_chunked call (prep + scan launches) from one ncu
 # capture of each kernel (dram__bytes_read.sum + dram__bytes_write.sum), tied
 # to the kernel source it was taken on: reported only while that source is
-# unchanged (profiles/chunk_prep_gdn_prefill_b2h16t16384.md and
-# profiles/chunk_scan_gdn_prefill_b2h16t16384.md).
+# unchanged (profiles/traffic_gdn_prefill_b2h16t16384.md).
 TRAFFIC_SOURCES = ("gated_delta_rule_fwd_gb300/csrc/chunked_tc.cu",
                    "gated_delta_rule_fwd_gb300/csrc/tc_common.cuh")
 TRAFFIC = {
-    "gdn_prefill_bf16": {"bytes": 272.984064e6 + 289.703168e6 + 750.225152e6 + 122.367488e6,
-                         "sha256": "8879ae46b2b38daaabb472546913269b6a7683966ca5b06751cb702eef2acaf0"},
+    "gdn_prefill_bf16": {"bytes": 272.965120e6 + 288.576768e6 + 750.326272e6 + 119.162880e6,
+                         "sha256": "8ac8ca008dedfabe38494e613889b6eb28403d8269a496c5bff8b17fe43f41d2"},
 }
 
 
