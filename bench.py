@@ -47,6 +47,7 @@ UNIT = "tokens/s"
 # to the kernel source it was taken on: reported only while that source is
 # unchanged (profiles/traffic_gdn_prefill_b2h16t16384.md).
 TRAFFIC_SOURCES = ("gated_delta_rule_fwd_gb300/csrc/chunked_tc.cu",
+                   "gated_delta_rule_fwd_gb300/csrc/scan_tc.cuh",
                    "gated_delta_rule_fwd_gb300/csrc/tc_common.cuh")
 TRAFFIC = {
     "gdn_prefill_bf16": {"bytes": 272.965120e6 + 288.576768e6 + 750.326272e6 + 119.162880e6,
@@ -427,21 +428,24 @@ def run_ours(args, dist, rank, world, local):
 
 def run_gen_delta(lr, dev, dist, args, peaks):
     """The generalised delta rule (RWKV-7 reading) through
-    lr_fwd_chunked_gen_delta (one CUDA-core launch; no tensor-core path yet).
-    Algorithmic bytes: q, kw, v, o at bf16, w, kappa, a at fp32 per
-    head-token, the state read and written."""
+    lr_fwd_chunked_gen_delta: two launches, the per-block pass over 32-token
+    blocks (CUDA cores, fp32) and the tensor-core scan with values stacked on
+    pseudo-values.  Algorithmic bytes: q, kw, v, o at bf16, w, kappa, a at fp32
+    per head-token, the state read and written."""
     w = workloads.WORKLOADS[GEN_DELTA_WORKLOAD]
     x = workloads.draw_gen_delta(w.B, w.H, w.T, w.dk, w.dv, seed=w.seed, dtype=w.torch_dtype,
                                  state=True)
     xd = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
     o = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.torch_dtype, device=dev)
     st = torch.empty((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, lr.gen_delta_workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.torch_dtype)),
+                     dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    steps = max(3, min(args.steps, 20))
+    steps = max(3, min(args.steps, 100))
 
     def step():
         lr.lr_fwd_chunked_gen_delta(xd["q"], xd["kw"], xd["v"], xd["w"], xd["kappa"], xd["a"],
-                                    xd["S0"], o=o, S_T=st, stream=stream)
+                                    xd["S0"], o=o, S_T=st, workspace=ws, stream=stream)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -460,8 +464,10 @@ def run_gen_delta(lr, dev, dist, args, peaks):
     return {"workload": w.name, "entry_point": "lr_fwd_chunked_gen_delta", "B": w.B, "H": w.H,
             "T": w.T, "dk": w.dk, "dv": w.dv, "value": w.B * w.T * world / (ms / 1e3),
             "unit": UNIT, "ms_per_step": ms, "steps": steps, "algorithmic_bytes_per_launch": nbytes,
-            "achieved_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "gpu_launches": steps,
-            "path": "CUDA cores, fp32 arithmetic (no tensor-core path yet)"}
+            "achieved_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "gpu_launches": 2 * steps,
+            "workspace_bytes": ws.numel(),
+            "path": "per-block pass on the CUDA cores (fp32) + tcgen05 scan (bf16 operands, "
+                    "fp32 state)"}
 
 
 def run_mlstm(lr, dev, dist, args, peaks):

@@ -34,7 +34,8 @@ F32, BF16 = 0, 1
 SYMBOLS = ("lr_fwd_chunked", "lr_fwd_chunked_workspace_size", "lr_fwd_chunked_noalloc", "lr_step",
            "lr_fwd_chunked_fused", "lr_fwd_chunked_fused_workspace_size", "lr_step_fused",
            "lr_fwd_chunked_mlstm", "lr_fwd_chunked_mlstm_workspace_size", "lr_step_mlstm",
-           "lr_fwd_chunked_gen_delta", "lr_step_gen_delta",
+           "lr_fwd_chunked_gen_delta", "lr_fwd_chunked_gen_delta_workspace_size",
+           "lr_step_gen_delta",
            "lr_device_status", "lr_status_string", "lr_abi_version")
 # lr_fuse flags (include/lr.h)
 FUSE_QK_SILU_L2 = 0x1
@@ -108,7 +109,9 @@ def lib() -> ctypes.CDLL:
         L.lr_step_mlstm.restype = i
         L.lr_step_mlstm.argtypes = [vp] * 9 + [i] * 4 + [i, vp]
         L.lr_fwd_chunked_gen_delta.restype = i
-        L.lr_fwd_chunked_gen_delta.argtypes = [vp] * 9 + [i] * 6 + [i, vp]
+        L.lr_fwd_chunked_gen_delta.argtypes = [vp] * 9 + [i] * 6 + [i, vp, ctypes.c_size_t, vp]
+        L.lr_fwd_chunked_gen_delta_workspace_size.restype = ctypes.c_size_t
+        L.lr_fwd_chunked_gen_delta_workspace_size.argtypes = [i] * 7
         L.lr_step_gen_delta.restype = i
         L.lr_step_gen_delta.argtypes = [vp] * 8 + [i] * 4 + [i, vp]
         L.lr_status_string.restype = ctypes.c_char_p
@@ -481,11 +484,19 @@ def lr_step_mlstm(q, k, v, fgate, igate, C, n, m, *, h=None, stream=None):
     return h
 
 
+def gen_delta_workspace_size(B, H, T, dk, dv, dtype, chunk=64) -> int:
+    """lr_fwd_chunked_gen_delta_workspace_size for these sizes."""
+    import torch
+    dt = F32 if dtype == torch.float32 else BF16
+    return int(lib().lr_fwd_chunked_gen_delta_workspace_size(B, H, T, dk, dv, int(chunk), dt))
+
+
 def lr_fwd_chunked_gen_delta(q, kw, v, w, kappa, a, S0=None, *, chunk=64, o=None, S_T=None,
-                             stream=None):
+                             workspace=None, stream=None):
     """Generalised delta rule over whole sequences (``lr_fwd_chunked_gen_delta``).
     q, kw: [B,H,T,dk]; v: [B,H,T,dv] (float32 or bfloat16); w, kappa, a:
-    [B,H,T,dk] float32; S0: [B,H,dv,dk] float32 or None.  Returns (o, S_T)."""
+    [B,H,T,dk] float32; S0: [B,H,dv,dk] float32 or None.  The bfloat16 path
+    needs a workspace (allocated here when none is given).  Returns (o, S_T)."""
     import torch
     dev = q.device
     B, H, T, dk = q.shape
@@ -499,9 +510,13 @@ def lr_fwd_chunked_gen_delta(q, kw, v, w, kappa, a, S0=None, *, chunk=64, o=None
         _check(S0, "S0", (B, H, dv, dk), torch.float32, dev)
     o = torch.empty((B, H, T, dv), dtype=q.dtype, device=dev) if o is None else o
     S_T = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev) if S_T is None else S_T
+    need = int(lib().lr_fwd_chunked_gen_delta_workspace_size(B, H, T, dk, dv, int(chunk), dt))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().lr_fwd_chunked_gen_delta(_ptr(q), _ptr(kw), _ptr(v), _ptr(w), _ptr(kappa), _ptr(a),
                                         _ptr(S0), _ptr(o), _ptr(S_T), B, H, T, dk, dv, int(chunk),
-                                        dt, _stream_handle(stream, dev))
+                                        dt, _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
     if st != 0:
         raise LrError(st, "lr_fwd_chunked_gen_delta")
     return o, S_T

@@ -79,54 +79,14 @@
 #include <mutex>
 
 #include "lr_internal.cuh"
-#include "tc_common.cuh"
+#include "scan_tc.cuh"
 
 namespace lr {
 namespace {
 
-using bf16 = __nv_bfloat16;
-using namespace tc;
-
-constexpr int C = 64;      // tokens per block
-constexpr int DVS = 32;    // value channels per scan CTA
 constexpr int NT = 128;    // threads per prep CTA
 constexpr int AP = C + 4;  // fp32 row of A and T: 16-byte rows, 8-row groups on distinct banks
 constexpr int XS = 40;     // fp32 row of the solve scratch
-
-__device__ int g_tc_error = 0;  // set to 1 when a bounded wait gives up
-
-// Workspace record of stage j of one head (stages 0..nblk), written by the
-// prep CTAs of blocks j and j-1 and read by the scan.
-template <int DK>
-struct Rec {
-    static constexpr int KB = (DK + 63) / 64;
-    static constexpr int WT = 0;                // W_j: KB blocks of [64 rows][128 B]
-    static constexpr int TZP = WT + KB * 8192;  // [192 rows][64] bf16: T_j diag(beta), -Z_{j-1}, P_{j-1}
-    static constexpr int VEC = TZP + 24576;     // fp32: g' [64], kd' [64], kd [64], g_C'
-    static constexpr int BYTES = VEC + 1024;
-};
-// offsets (in floats) inside the gate vector of a record
-constexpr int kVgPrev = 0, kVkdPrev = 64, kVkd = 128, kVgCPrev = 192;
-constexpr int kVgCDiag = 128;  // diagonal gate: g_C' per key channel (128 floats)
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
-    return lo | (hi << 16);
-}
-__device__ __forceinline__ uint4 pack8(const float *x) {
-    uint4 r;
-    r.x = pack_bf16(x[0], x[1]);
-    r.y = pack_bf16(x[2], x[3]);
-    r.z = pack_bf16(x[4], x[5]);
-    r.w = pack_bf16(x[6], x[7]);
-    return r;
-}
-
-__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
-    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) &
-                                       ~static_cast<uintptr_t>(1023));
-}
 
 // ===================================================================== prep
 
@@ -1092,529 +1052,8 @@ chunk_prep_mlstm_kernel(const float *__restrict__ fgate, const float *__restrict
     if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
-// ===================================================================== scan
-
-template <int DK>
-struct ScanLayout {
-    static constexpr int KB = (DK + 63) / 64;
-    static constexpr int AW_BYTES = 128 * 128 * KB;  // [128][DK] K-major: W rows, Q' rows
-    static constexpr int AW = 0;                      // x2
-    static constexpr int TZP = AW + 2 * AW_BYTES;     // x2 [192][64] K-major: T diag(beta), -Z', P'
-    static constexpr int KR = TZP + 2 * 24576;        // x2 [64 tokens][128] MN-major: K'
-    static constexpr int VR = KR + 2 * 16384;         // x2 [64 tokens][64] MN-major: v box (this CTA: 32 channels)
-    static constexpr int VEC = VR + 2 * 8192;         // x2 gate vectors of the stage
-    static constexpr int UB = VEC + 2 * 1024;         // [64 tokens][64] MN-major: U
-    static constexpr int UBK = UB + 8192;             // x2 [64 tokens][64] MN-major: kd U (kd' V')
-    static constexpr int SB_BYTES = 128 * DK;         // [DK][64] MN-major: bf16 S^T slice (32 used)
-    static constexpr int SB = UBK + 2 * 8192;         // x2
-    static constexpr int BAR = SB + 2 * SB_BYTES;
-    static constexpr int BYTES = BAR + 256;
-    static constexpr int ALLOC = BYTES + 1024;
-};
-
-// TMEM columns of the scan kernel: per stage parity p, at p * kParCols, four
-// fp32 accumulators of 32 columns (M = 128 lanes).
-constexpr uint32_t kDa = 0, kDb = 32, kDc = 64, kDS = 96, kParCols = 128;
-constexpr uint32_t kScanCols = 256;
-
-// L2 prefetch of what stage `st` will fetch (one thread).
-template <int DK, bool DELTA>
-__device__ __forceinline__ void scan_prefetch_l2(const bf16 *q, const bf16 *k, const bf16 *v,
-                                                 const uint8_t *rec, size_t bh, int T, int st,
-                                                 int nblk, int dv) {
-    prefetch_l2(rec, Rec<DK>::BYTES);
-    const int pb = st - 1;
-    if (pb >= 0 && pb < nblk) {
-        const int t0 = pb * C, n = min(C, T - t0);
-        prefetch_l2(q + (bh * T + t0) * DK, (uint32_t)n * DK * 2);
-        prefetch_l2(k + (bh * T + t0) * DK, (uint32_t)n * DK * 2);
-    }
-    const int vb = DELTA ? st : st - 1;
-    if (vb >= 0 && vb < nblk) {
-        const int t0 = vb * C, n = min(C, T - t0);
-        prefetch_l2(v + (bh * T + t0) * dv, (uint32_t)n * dv * 2);
-    }
-}
-
-// Scan kernel roles (384 threads), stage j = 0..nblk (parity p = j & 1):
-//   warp 0, lane 0   issues b_j = [W_j; Q_{j-1}] S_{j-1}^T (the U rows take -g_C') and
-//                    c_j = [-Z_{j-1}; P_{j-1}] U_{j-1}   (P_{j-1} V_{j-1} without delta)
-//   warp 1, lane 0   issues a_j = [T_j diag(beta); *] V_j and
-//                    ds = K_{j-1}^T (kd U_{j-1})          (K^T (kd V) without delta)
-//   warp 2, lane 0   loads the early group of stage j into buffer p: what b_j
-//                    reads (W_j, Q_{j-1})
-//   warp 3, lane 0   loads the late group: what a_j, c_j, ds and the epilogues
-//                    read (T_j diag(beta), -Z_{j-1}, P_{j-1}, K_{j-1}, the gates,
-//                    V_j; V_{j-1} without delta)
-//   warps 4, 5, 8, 9 U rows (TMEM lanes 0..63): U_j = Da + Db + Dc -> bf16 U,
-//                    kd U; without delta they form kd' V' for ds instead
-//   warps 6, 7, 10, 11  output rows (lanes 64..127): O_{j-1} = g' Db + Dc
-//   warps 12..19     state (lanes 0..127 = key channels): S_j = g_C' S_{j-1} + ds,
-//                    fp32 in registers, bf16 copy for b_{j+1}
-// Each epilogue role is split over two warps per TMEM lane quarter, one per
-// half of the 32 value channels, to keep the per-warp instruction chains short.
-// All loads are TMA or bulk copies completing on the group's `full` barrier,
-// which the consumers wait on directly.  The early group is released as soon
-// as b_j is done, so the next fill of that part of the buffer starts about
-// half a stage earlier than the late one; it is kept small (32 KB at
-// d_k = 128) because b_j sits on the state chain.
-// The state before the first block plays S_{-1} (with g_C = 1 and U_{-1} = 0).
-// Hand-offs are mbarriers, every wait bounded.  Each barrier is waited on by
-// all of its consumers before it can complete again: barriers that complete
-// once per stage and could run ahead are kept per parity, and every consumer
-// arrives on a group's `empty` barrier only after its waits of that stage.
-constexpr int kScanThreads = 640;
-
-// Arrive once per warp on `bar`: every lane has finished its part (and its own
-// fences) before lane 0 arrives.
-__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-}
-
-struct ScanBars {
-    uint64_t fullE[2];   // early group landed                           (1 + tx bytes)
-    uint64_t emptyE[2];  // early group read                             (1 commit)
-    uint64_t fullL[2];   // late group landed                            (1 + tx bytes)
-    uint64_t emptyL[2];  // late group read                              (2 commits + 16 warps)
-    uint64_t vkr[2];     // kd' V' written (no delta)                    (4 warps)
-    uint64_t dA[2];      // b and c products of the stage done           (commit)
-    uint64_t dB[2];      // a product of the stage done                  (commit)
-    uint64_t dsf[2];     // ds product of the stage done                 (commit)
-    uint64_t tfree[2];   // output rows of the stage read                (4 warps)
-    uint64_t uk[2];      // kd U rows of this parity written             (4 warps)
-    uint64_t s[2];       // bf16 state copy of this parity written       (8 warps)
-    uint64_t u;          // U rows written                               (4 warps)
-    uint64_t fin[2];     // every product an issuer issued has completed (commit)
-    uint32_t tmem;
-};
-static_assert(sizeof(ScanBars) <= 256, "the barriers must fit their shared-memory slot");
-constexpr uint32_t kEmptyLCount = 2 + 4 + 4 + 8;  // both issuers' commits, U, output and state warps
-
-template <int DK, bool ALPHA, bool DELTA, bool DIAG = false>
-__global__ void __launch_bounds__(kScanThreads, 1)
-chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
-                  bf16 *__restrict__ o, float *__restrict__ ST, int H, int T, int dv, int nblk,
-                  const bf16 *__restrict__ q, const bf16 *__restrict__ k,
-                  const bf16 *__restrict__ v, const __grid_constant__ CUtensorMap tmq,
-                  const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
-    using L = ScanLayout<DK>;
-    using R = Rec<DK>;
-    extern __shared__ uint8_t sm_raw[];
-    uint8_t *sm = align1024(sm_raw);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c0 = blockIdx.x * DVS;
-    const int vx = c0 & ~63;                           // TMA box column of the v slice
-    const uint32_t voff = (uint32_t)(c0 & 63) * 2u;    // byte offset of the slice in a box row
-    const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
-    const uint8_t *recs = ws + bh * (nblk + 1) * (size_t)R::BYTES;
-    ScanBars *bars = reinterpret_cast<ScanBars *>(sm + L::BAR);
-    auto vec_of = [&](int p) { return reinterpret_cast<const float *>(sm + L::VEC + p * 1024); };
-
-    // zero everything once: padding rows and columns of the operands must read 0
-    for (int i = tid; i < L::BAR / 16; i += kScanThreads)
-        reinterpret_cast<uint4 *>(sm)[i] = make_uint4(0, 0, 0, 0);
-    if (tid == 0) {
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&bars->fullE[b], 1);
-            mbar_init(&bars->emptyE[b], 1);
-            mbar_init(&bars->fullL[b], 1);
-            mbar_init(&bars->emptyL[b], kEmptyLCount);
-            mbar_init(&bars->vkr[b], 4);
-            mbar_init(&bars->dA[b], 1);
-            mbar_init(&bars->dB[b], 1);
-            mbar_init(&bars->dsf[b], 1);
-            mbar_init(&bars->tfree[b], 4);
-            mbar_init(&bars->uk[b], 4);
-            mbar_init(&bars->s[b], 8);
-            mbar_init(&bars->fin[b], 1);
-        }
-        mbar_init(&bars->u, 4);
-        fence_mbar_init();
-    }
-    if (warp == 0) {
-        tmem_alloc(&bars->tmem, kScanCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = bars->tmem;
-    bool ok = true;
-
-    const uint32_t id_kn = idesc_bf16_f32_mn(128, DVS, false, true);
-    const uint32_t id_nn = idesc_bf16_f32_mn(128, DVS, true, true);
-    auto aw_desc = [&](int p) { return tile_desc(smem_u32(sm + L::AW + p * L::AW_BYTES), 128, 0, 0); };
-    auto tz_desc = [&](int p) { return tile_desc(smem_u32(sm + L::TZP + p * 24576), 192, 0, 0); };
-    auto zp_desc = [&](int p) { return tile_desc(smem_u32(sm + L::TZP + p * 24576), 192, 64, 0); };
-    auto kr_desc = [&](int p) { return tile_desc_mn(smem_u32(sm + L::KR + p * 16384), 64, 0); };
-    // the v box holds 64 channels; this CTA's 32 start `voff` bytes into each row
-    auto vr_desc = [&](int p) { return tile_desc_mn(smem_u32(sm + L::VR + p * 8192) + voff, 64, 0); };
-    auto ubk_desc = [&](int i) { return tile_desc_mn(smem_u32(sm + L::UBK + i * 8192), 64, 0); };
-    auto sb_desc = [&](int i) { return tile_desc_mn(smem_u32(sm + L::SB + i * L::SB_BYTES), DK, 0); };
-
-    if (warp == 0) {
-        // ======================================= b and c products (issuer A)
-        if (lane == 0) {
-            const uint64_t d_ub = tile_desc_mn(smem_u32(sm + L::UB), 64, 0);
-            for (int j = 0; j <= nblk && ok; ++j) {
-                const int p = j & 1;
-                const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
-                ok = mbar_wait(&bars->fullE[p], ph);
-                // output rows of stage j-2 (same accumulators) read
-                if (ok && j >= 2) ok = mbar_wait(&bars->tfree[p], ph ^ 1);
-                // S_{j-1} in state copy p
-                if (ok) ok = mbar_wait(&bars->s[p], ph);
-                if (!ok) break;
-                tc_fence_after();
-                const uint64_t d_aw = aw_desc(p), d_sb = sb_desc(p);
-#pragma unroll
-                for (int ks = 0; ks < DK / 16; ++ks)
-                    mma_bf16(tmem + base + kDb, kdesc_step(d_aw, 128, ks), mndesc_step(d_sb, ks),
-                             id_kn, ks > 0);
-                mma_commit(&bars->emptyE[p]);
-                if (j >= 1) {
-                    ok = mbar_wait(&bars->fullL[p], ph);
-                    if (ok && DELTA) ok = mbar_wait(&bars->u, (j - 1) & 1);  // U_{j-1}
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t d_zp = zp_desc(p), d_x = DELTA ? d_ub : vr_desc(p);
-#pragma unroll
-                    for (int ks = 0; ks < C / 16; ++ks)
-                        mma_bf16(tmem + base + kDc, kdesc_step(d_zp, 192, ks), mndesc_step(d_x, ks),
-                                 id_kn, ks > 0);
-                }
-                mma_commit(&bars->dA[p]);
-                mma_commit(&bars->emptyL[p]);
-            }
-            mma_commit(&bars->fin[0]);
-            if (!mbar_wait(&bars->fin[0], 0)) ok = false;
-        }
-    } else if (warp == 1) {
-        // ====================================== a and ds products (issuer B)
-        if (lane == 0) {
-            for (int j = 0; j <= nblk && ok; ++j) {
-                const int p = j & 1;
-                const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
-                ok = mbar_wait(&bars->fullL[p], ph);
-                if (!ok) break;
-                tc_fence_after();
-                if (DELTA && j < nblk) {
-                    const uint64_t d_tz = tz_desc(p), d_vr = vr_desc(p);
-#pragma unroll
-                    for (int ks = 0; ks < C / 16; ++ks)
-                        mma_bf16(tmem + base + kDa, kdesc_step(d_tz, 192, ks), mndesc_step(d_vr, ks),
-                                 id_kn, ks > 0);
-                }
-                mma_commit(&bars->dB[p]);
-                if (j >= 1) {
-                    if (ok) ok = DELTA ? mbar_wait(&bars->uk[(j - 1) & 1], ((j - 1) >> 1) & 1)  // kd U_{j-1}
-                                       : mbar_wait(&bars->vkr[p], ph);                          // kd' V'
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t d_kr = kr_desc(p), d_y = ubk_desc(DELTA ? (j - 1) & 1 : p);
-#pragma unroll
-                    for (int ks = 0; ks < C / 16; ++ks)
-                        mma_bf16(tmem + base + kDS, mndesc_step(d_kr, ks), mndesc_step(d_y, ks),
-                                 id_nn, ks > 0);
-                }
-                mma_commit(&bars->dsf[p]);
-                mma_commit(&bars->emptyL[p]);
-            }
-            mma_commit(&bars->fin[1]);
-            if (!mbar_wait(&bars->fin[1], 0)) ok = false;
-        }
-    } else if (warp == 2) {
-        // ============================================ early-group loads
-        if (lane == 0) {
-            int issued = -1;
-            for (int j = 0; j <= nblk && ok; ++j) {
-                const int p = j & 1;
-                if (j >= 2) ok = mbar_wait(&bars->emptyE[p], ((j >> 1) - 1) & 1);
-                if (!ok) break;
-                const uint8_t *rec = recs + (size_t)j * R::BYTES;
-                uint8_t *aw = sm + L::AW + p * L::AW_BYTES;
-                if (j + 2 <= nblk && blockIdx.x == 0)  // one CTA of the head suffices
-                    scan_prefetch_l2<DK, DELTA>(q, k, v, rec + 2 * (size_t)R::BYTES, bh, T, j + 2,
-                                                nblk, dv);
-                const bool cur = DELTA && j < nblk, prev = j >= 1;
-                const uint32_t bytes = (cur ? (uint32_t)R::KB * 8192u : 0u) +
-                                       (prev ? (uint32_t)R::KB * 8192u : 0u);
-                mbar_expect_tx(&bars->fullE[p], bytes);
-                if (cur) {
-#pragma unroll
-                    for (int kb = 0; kb < R::KB; ++kb)
-                        bulk_g2s(aw + kb * 16384, rec + R::WT + kb * 8192, 8192, &bars->fullE[p]);
-                }
-                if (prev) {
-#pragma unroll
-                    for (int kb = 0; kb < R::KB; ++kb)
-                        tma_load_3d(aw + kb * 16384 + 8192, &tmq, kb * 64, (j - 1) * C, (int)bh,
-                                    &bars->fullE[p]);
-                }
-                issued = j;
-            }
-            // never leave with copies into shared memory in flight
-            for (int j = issued > 0 ? issued - 1 : 0; j <= issued; ++j)
-                if (!mbar_wait(&bars->fullE[j & 1], (j >> 1) & 1)) ok = false;
-        }
-    } else if (warp == 3) {
-        // ============================================= late-group loads
-        int issued = -1;
-        for (int j = 0; j <= nblk && ok; ++j) {
-            const int p = j & 1;
-            const bool prev = j >= 1;
-            if (lane == 0) {
-                if (j >= 2) ok = mbar_wait(&bars->emptyL[p], ((j >> 1) - 1) & 1);
-                if (ok) {
-                    const uint8_t *rec = recs + (size_t)j * R::BYTES;
-                    const bool cur = DELTA && j < nblk;
-                    uint32_t bytes = 1024u + (DELTA ? 24576u : 0u) + (cur ? 8192u : 0u);
-                    if (prev) bytes += (DELTA ? 0u : 8192u) + (uint32_t)R::KB * 8192u +
-                                       (DELTA ? 0u : 8192u);
-                    mbar_expect_tx(&bars->fullL[p], bytes);
-                    bulk_g2s(sm + L::VEC + p * 1024, rec + R::VEC, 1024, &bars->fullL[p]);
-                    if (DELTA)
-                        bulk_g2s(sm + L::TZP + p * 24576, rec + R::TZP, 24576, &bars->fullL[p]);
-                    if (cur)
-                        tma_load_3d(sm + L::VR + p * 8192, &tmv, vx, j * C, (int)bh, &bars->fullL[p]);
-                    if (prev) {
-                        if (!DELTA)
-                            bulk_g2s(sm + L::TZP + p * 24576 + 16384, rec + R::TZP + 16384, 8192,
-                                     &bars->fullL[p]);
-#pragma unroll
-                        for (int kb = 0; kb < R::KB; ++kb)
-                            tma_load_3d(sm + L::KR + p * 16384 + kb * 8192, &tmk, kb * 64,
-                                        (j - 1) * C, (int)bh, &bars->fullL[p]);
-                        if (!DELTA)
-                            tma_load_3d(sm + L::VR + p * 8192, &tmv, vx, (j - 1) * C, (int)bh,
-                                        &bars->fullL[p]);
-                    }
-                    issued = j;
-                }
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-        }
-        // never leave with copies into shared memory in flight
-        if (lane == 0)
-            for (int j = issued > 0 ? issued - 1 : 0; j <= issued; ++j)
-                if (!mbar_wait(&bars->fullL[j & 1], (j >> 1) & 1)) ok = false;
-    } else if (warp < 12 && (warp & 3) < 2) {
-        // ============================================ U rows (TMEM lanes 0..63)
-        const int r = 32 * (warp & 3) + lane;
-        const int ch = 16 * ((warp - 4) >> 2);  // first value channel of this warp's half
-        const uint32_t lb = ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)ch;
-        for (int j = 0; j <= nblk && ok; ++j) {
-            const int p = j & 1;
-            const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->fullL[p], ph));
-            if (!ok) break;
-            // with delta only the gates are read from the late group: take them
-            // and release it now
-            const float kdr = DELTA ? vec_of(p)[kVkd + r] : 0.f;
-            const float gn = DELTA ? -vec_of(p)[kVgCPrev] : 0.f;  // b's W rows carry -g_C'
-            if (DELTA) warp_arrive(&bars->emptyL[p]);
-            if (DELTA && j < nblk) {
-                ok = mbar_wait(&bars->dA[p], ph);
-                ok = ok && mbar_wait(&bars->dB[p], ph);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                tc_fence_after();
-                float x[16], y[16], z[16];
-                tmem_ld16(tmem + lb + base + kDa, x);
-                tmem_ld16(tmem + lb + base + kDb, y);
-                if (j > 0) {
-                    tmem_ld16(tmem + lb + base + kDc, z);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) x[c] += gn * y[c] + z[c];
-                } else {
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) x[c] += gn * y[c];
-                }
-                // kd U (for ds, on the state chain) and U (for c, on the U chain)
-                float xk[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) xk[c] = x[c] * kdr;
-#pragma unroll
-                for (int c8 = 0; c8 < 2; ++c8) {
-                    *reinterpret_cast<uint4 *>(sm + L::UBK + p * 8192 +
-                                               sw128_offset(r, ch + c8 * 8, 64)) = pack8(xk + c8 * 8);
-                    *reinterpret_cast<uint4 *>(sm + L::UB + sw128_offset(r, ch + c8 * 8, 64)) =
-                        pack8(x + c8 * 8);
-                }
-                fence_async_smem();
-                tc_fence_before();
-                warp_arrive(&bars->uk[p]);
-                warp_arrive(&bars->u);
-            } else {
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                if (!DELTA && j >= 1) {
-                    // kd' V' (B operand of Delta S = K'^T diag(kd') V'): this warp's
-                    // 16 token rows
-                    const float *vec = vec_of(p);
-                    const uint8_t *vr = sm + L::VR + p * 8192;
-                    uint8_t *vk = sm + L::UBK + p * 8192;
-                    const int rw = 16 * (((warp & 3) << 1) | ((warp - 4) >> 2));
-                    for (int idx = lane; idx < 16 * (DVS / 8); idx += 32) {
-                        const int rr = rw + idx / (DVS / 8), c8 = idx % (DVS / 8);
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(
-                            vr + sw128_offset(rr, (c0 & 63) + c8 * 8, 64));
-                        const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
-                        const float f = vec[kVkdPrev + rr];
-                        float xv[8];
-#pragma unroll
-                        for (int t = 0; t < 8; ++t) xv[t] = f * __bfloat162float(e[t]);
-                        *reinterpret_cast<uint4 *>(vk + sw128_offset(rr, c8 * 8, 64)) = pack8(xv);
-                    }
-                    fence_async_smem();
-                }
-                // one completion per stage (also the first) keeps the parities aligned
-                if (!DELTA) warp_arrive(&bars->vkr[p]);
-            }
-            if (!DELTA) warp_arrive(&bars->emptyL[p]);
-        }
-    } else if (warp < 12) {
-        // ===================================== output rows (TMEM lanes 64..127)
-        const int r = 32 * (warp & 3) + lane - 64;
-        const int ch = 16 * ((warp - 4) >> 2);
-        const uint32_t lb = ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)ch;
-        for (int j = 0; j <= nblk && ok; ++j) {
-            const int p = j & 1;
-            const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->fullL[p], ph));
-            if (!ok) break;
-            const float gr = vec_of(p)[kVgPrev + r];  // the only late-group value read here
-            warp_arrive(&bars->emptyL[p]);
-            if (j >= 1) ok = __all_sync(0xffffffffu, mbar_wait(&bars->dA[p], ph));
-            if (!ok) break;
-            if (j >= 1) {
-                tc_fence_after();
-                float x[16], y[16];
-                tmem_ld16(tmem + lb + base + kDb, x);
-                tmem_ld16(tmem + lb + base + kDc, y);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 16; ++c) x[c] = gr * x[c] + y[c];  // g' Q' S'^T + P' U'
-                tc_fence_before();
-                warp_arrive(&bars->tfree[p]);
-                const int t = (j - 1) * C + r;
-                if (t < T) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(o + (bh * T + t) * dv + c0 + ch);
-#pragma unroll
-                    for (int i8 = 0; i8 < 2; ++i8) dst[i8] = pack8(x + i8 * 8);
-                }
-            } else {
-                warp_arrive(&bars->tfree[p]);
-            }
-        }
-    } else {
-        // ========================== state (TMEM lanes 0..127 = key channels)
-        constexpr int SC = DVS / 2;  // value channels per warp
-        const int kc = 32 * (warp & 3) + lane;
-        const int ch = SC * ((warp - 12) >> 2);
-        const uint32_t lb = ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)ch;
-        float Sr[SC];
-#pragma unroll
-        for (int c = 0; c < SC; ++c)
-            Sr[c] = (S0 && kc < DK) ? S0[(bh * dv + c0 + ch + c) * DK + kc] : 0.f;
-        auto write_sb = [&](int i) {
-            if (kc < DK) {
-#pragma unroll
-                for (int c8 = 0; c8 < SC / 8; ++c8)
-                    *reinterpret_cast<uint4 *>(sm + L::SB + i * L::SB_BYTES +
-                                               sw128_offset(kc, ch + c8 * 8, DK)) = pack8(Sr + c8 * 8);
-            }
-        };
-        // S_{-1} = S_0 in copy 0 (read by b_0), S_0 in copy 1 (read by b_1)
-        write_sb(0);
-        write_sb(1);
-        fence_async_smem();
-        warp_arrive(&bars->s[0]);
-        warp_arrive(&bars->s[1]);
-        // Without delta these warps also order two reuses that the U chain
-        // orders with delta: the late group (and with it the Delta S
-        // accumulator of this parity and its dsf barrier) is released only
-        // after Delta S is read, and a bf16 state copy is rewritten only after
-        // b_{j-1}, its last reader, is done (emptyE).
-        for (int j = 0; j <= nblk && ok; ++j) {
-            const int p = j & 1;
-            const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->fullL[p], ph));
-            if (!ok) break;
-            // the only late-group value read here: g_C', per key channel with the diagonal gate
-            const float gC = DIAG ? vec_of(p)[kVgCDiag + (kc & 127)] : vec_of(p)[kVgCPrev];
-            if (DELTA) warp_arrive(&bars->emptyL[p]);
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->dsf[p], ph));
-            if (!ok) break;
-            if (j >= 1) {
-                tc_fence_after();
-                float d[SC];
-                tmem_ld16(tmem + lb + base + kDS, d);
-                tmem_ld_wait();
-                tc_fence_before();
-                if (!DELTA) warp_arrive(&bars->emptyL[p]);
-#pragma unroll
-                for (int c = 0; c < SC; ++c) Sr[c] = gC * Sr[c] + d[c];
-                if (j < nblk) {  // S_j -> copy (j+1)&1, read by b_{j+1}
-                    if (!DELTA)
-                        ok = __all_sync(0xffffffffu,
-                                        mbar_wait(&bars->emptyE[(j - 1) & 1], ((j - 1) >> 1) & 1));
-                    if (!ok) break;
-                    write_sb((j + 1) & 1);
-                    fence_async_smem();
-                    warp_arrive(&bars->s[(j + 1) & 1]);
-                }
-            } else if (!DELTA) {
-                warp_arrive(&bars->emptyL[p]);
-            }
-        }
-        if (ok && kc < DK) {
-#pragma unroll
-            for (int c = 0; c < SC; ++c) ST[(bh * dv + c0 + ch + c) * DK + kc] = Sr[c];
-        }
-    }
-
-    if (!ok) atomicExch(&g_tc_error, 1);
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kScanCols);
-}
-
 // ================================================================== launch
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &qr) == cudaSuccess &&
-            qr == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// [B*H][T][d] bf16 tensor, boxes of 64 rows x 64 columns, 128-byte swizzle,
-// zero fill outside (also the columns of a box wider than d).
-cudaError_t make_rows_map(CUtensorMap *m, const void *base, int d, int T, int BH) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return cudaErrorNotSupported;
-    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
-    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * (cuuint64_t)T};
-    const cuuint32_t box[3] = {64, 64, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
 
 // One record per stage: a head of nblk blocks has nblk + 1 stages.  With
 // SiLU + L2 of q and k, the normalised q and k ([B, H, T, dk] bf16 each)

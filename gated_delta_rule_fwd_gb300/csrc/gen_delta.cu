@@ -19,8 +19,8 @@
 //                                    Qb_ts = (b_s e^{L_t - L_s}) . q_t           (s <= t)
 //   S <- S0 Diag(e^{L_last}) + V^T (kw e^{L_last - L}) - U^T (b e^{L_last - L}),
 // with b = a * kappa and Kdec_t = kappa_t e^{L_{t-1}}.  Every decay factor is
-// e^{L_t - L_s} with t >= s, at most 1, so no rescaling is needed.  There is
-// no tensor-core path for this row yet.
+// e^{L_t - L_s} with t >= s, at most 1, so no rescaling is needed.  This is
+// the fp32 path; bf16 runs on the tensor cores (gen_delta_tc.cu).
 #include "lr_internal.cuh"
 
 namespace lr {
@@ -264,16 +264,14 @@ cudaError_t chunked_typed(const void *q, const void *kw, const void *v, const fl
 
 }  // namespace
 
-// Attribute slots 148..153 belong to this file.
+// Attribute slots 148..150 belong to this file (the fp32 chunked kernel).
 cudaError_t launch_gen_delta_chunked(const void *q, const void *kw, const void *v, const float *w,
                                      const float *kappa, const float *a, const float *S0, void *o,
                                      float *S_T, int B, int H, int T, int dk, int dv, lr_dtype dt,
                                      cudaStream_t stream) {
-    const int s = 148 + (dk == 32 ? 0 : dk == 64 ? 1 : 2) + (dt == LR_DT_F32 ? 0 : 3);
-    if (dt == LR_DT_F32)
-        return chunked_typed<float>(q, kw, v, w, kappa, a, S0, o, S_T, B, H, T, dk, dv, stream, s);
-    return chunked_typed<__nv_bfloat16>(q, kw, v, w, kappa, a, S0, o, S_T, B, H, T, dk, dv, stream,
-                                        s);
+    if (dt != LR_DT_F32) return cudaErrorInvalidValue;  // bf16 runs on the tensor cores
+    const int s = 148 + (dk == 32 ? 0 : dk == 64 ? 1 : 2);
+    return chunked_typed<float>(q, kw, v, w, kappa, a, S0, o, S_T, B, H, T, dk, dv, stream, s);
 }
 
 cudaError_t launch_gen_delta_step(const void *q, const void *kw, const void *v, const float *w,

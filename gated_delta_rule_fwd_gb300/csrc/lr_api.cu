@@ -113,7 +113,7 @@ using namespace lr;
 
 extern "C" {
 
-int lr_abi_version(void) { return 2; }
+int lr_abi_version(void) { return 3; }
 
 const char *lr_status_string(lr_status s) {
     switch (s) {
@@ -319,31 +319,50 @@ lr_status lr_step_mlstm(const void *q, const void *k, const void *v, const float
     return e == cudaSuccess ? LR_OK : LR_ERR_CUDA;
 }
 
+size_t lr_fwd_chunked_gen_delta_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
+                                               lr_dtype dt) {
+    if (check_chunked_shape(B, H, T, dk, dv, chunk, dt, LR_MODE_DELTA) != LR_OK) return 0;
+    if (dt != LR_DT_BF16 || T == 0) return 0;
+    return gen_delta_tc_workspace_bytes(B, H, T, dk);
+}
+
 lr_status lr_fwd_chunked_gen_delta(const void *q, const void *kw, const void *v, const float *w,
                                    const float *kappa, const float *a, const float *S0, void *o,
                                    float *S_T, int B, int H, int T, int dk, int dv, int chunk,
-                                   lr_dtype dt, cudaStream_t stream) {
+                                   lr_dtype dt, void *workspace, size_t workspace_bytes,
+                                   cudaStream_t stream) {
     const lr_status shape = check_chunked_shape(B, H, T, dk, dv, chunk, dt, LR_MODE_DELTA);
     if (shape != LR_OK) return shape;
     if (!S_T) return LR_ERR_NULL;
     if (T > 0 && (!q || !kw || !v || !w || !kappa || !a || !o)) return LR_ERR_NULL;
+    const size_t need = lr_fwd_chunked_gen_delta_workspace_size(B, H, T, dk, dv, chunk, dt);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return LR_ERR_WORKSPACE;
     for (const void *p : {q, kw, v, (const void *)w, (const void *)kappa, (const void *)a,
                           (const void *)S0, (const void *)o, (const void *)S_T})
         if (!aligned16(p)) return LR_ERR_ALIGN;
+    if (need > 0 && !aligned16(workspace)) return LR_ERR_ALIGN;
     const size_t es = dt == LR_DT_F32 ? 4 : 2;
     const size_t bht = (size_t)B * H * T, state = (size_t)B * H * dv * dk * 4;
     const Span sq = span(q, bht * dk * es), sk = span(kw, bht * dk * es), sv = span(v, bht * dv * es);
     const Span sw = span(w, bht * dk * 4), sc = span(kappa, bht * dk * 4), sa = span(a, bht * dk * 4);
     const Span s0 = span(S0, state), so = span(o, bht * dv * es), st = span(S_T, state);
-    for (Span in : {sq, sk, sv, sw, sc, sa, s0, st})
+    const Span sws = span(need > 0 ? workspace : nullptr, need);
+    for (Span in : {sq, sk, sv, sw, sc, sa, s0, st, sws})
         if (overlap(so, in)) return LR_ERR_ALIAS;
-    for (Span in : {sq, sk, sv, sw, sc, sa})
+    for (Span in : {sq, sk, sv, sw, sc, sa, sws})
         if (overlap(st, in)) return LR_ERR_ALIAS;
+    for (Span in : {sq, sk, sv, sw, sc, sa, s0})
+        if (overlap(sws, in)) return LR_ERR_ALIAS;
     if (S0 && S0 != S_T && overlap(s0, st)) return LR_ERR_ALIAS;
-    const cudaError_t e =
-        T == 0 ? copy_state(S0, S_T, (size_t)B * H * dv * dk, stream)
-               : launch_gen_delta_chunked(q, kw, v, w, kappa, a, S0, o, S_T, B, H, T, dk, dv, dt,
-                                          stream);
+    cudaError_t e;
+    if (T == 0)
+        e = copy_state(S0, S_T, (size_t)B * H * dv * dk, stream);
+    else if (dt == LR_DT_BF16)
+        e = launch_gen_delta_tc(q, kw, v, w, kappa, a, S0, o, S_T, B, H, T, dk, dv, workspace,
+                                stream);
+    else
+        e = launch_gen_delta_chunked(q, kw, v, w, kappa, a, S0, o, S_T, B, H, T, dk, dv, dt,
+                                     stream);
     return e == cudaSuccess ? LR_OK : LR_ERR_CUDA;
 }
 
@@ -374,9 +393,9 @@ lr_status lr_step_gen_delta(const void *q, const void *kw, const void *v, const 
 
 lr_status lr_device_status(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return LR_ERR_CUDA;
-    const int e = read_and_clear_tc_error();
-    if (e < 0) return LR_ERR_CUDA;
-    return e ? LR_ERR_TIMEOUT : LR_OK;
+    const int e = read_and_clear_tc_error(), eg = read_and_clear_gd_tc_error();
+    if (e < 0 || eg < 0) return LR_ERR_CUDA;
+    return (e || eg) ? LR_ERR_TIMEOUT : LR_OK;
 }
 
 lr_status lr_step_fused(const void *q, const void *k, const void *v, const float *alpha,

@@ -135,7 +135,8 @@ cudaError_t launch_mlstm_tc(const void *q, const void *k, const void *v, const f
                             cudaStream_t stream);
 size_t records_bytes_tc(int B, int H, int T, int dk);
 
-// Generalised delta rule of RWKV-7 (gen_delta.cu).
+// Generalised delta rule of RWKV-7 (gen_delta.cu): the fp32 chunked kernel and
+// the decode step (fp32 or bf16).
 cudaError_t launch_gen_delta_chunked(const void *q, const void *kw, const void *v, const float *w,
                                      const float *kappa, const float *a, const float *S0, void *o,
                                      float *S_T, int B, int H, int T, int dk, int dv, lr_dtype dt,
@@ -143,14 +144,24 @@ cudaError_t launch_gen_delta_chunked(const void *q, const void *kw, const void *
 cudaError_t launch_gen_delta_step(const void *q, const void *kw, const void *v, const float *w,
                                   const float *kappa, const float *a, float *S, void *o, int N,
                                   int H, int dk, int dv, lr_dtype dt, cudaStream_t stream);
+// The bf16 path on the tensor cores (gen_delta_tc.cu): the per-block pass over
+// 32-token blocks, then the scan of scan_tc.cuh; workspace of
+// gen_delta_tc_workspace_bytes(...) bytes.
+size_t gen_delta_tc_workspace_bytes(int B, int H, int T, int dk);
+cudaError_t launch_gen_delta_tc(const void *q, const void *kw, const void *v, const float *w,
+                                const float *kappa, const float *a, const float *S0, void *o,
+                                float *S_T, int B, int H, int T, int dk, int dv, void *ws,
+                                cudaStream_t stream);
 
 // In-place RMSNorm of `rows` rows of dv channels (norm.cu).
 cudaError_t launch_rmsnorm(void *o, const float *w, float eps, size_t rows, int dv, lr_dtype dt,
                            cudaStream_t stream);
 
-// Returns and clears the tensor-core kernel's bounded-wait error word
-// (1 if set, 0 if clear, -1 if the device could not be read).
+// Return and clear the bounded-wait error word of the tensor-core kernels of
+// chunked_tc.cu and of gen_delta_tc.cu (each has its own): 1 if set, 0 if
+// clear, -1 if the device could not be read.
 int read_and_clear_tc_error();
+int read_and_clear_gd_tc_error();
 
 // Set the dynamic shared-memory limit of `fn` once per device.
 cudaError_t ensure_smem_attr(const void *fn, int bytes, int slot);

@@ -393,17 +393,33 @@ lr_status lr_step_mlstm(const void *q, const void *k, const void *v, const float
  *   w, kappa, a [B, H, T, dk]   fp32 (decay in (0, 1], removal key, rate)
  *   S0, S_T     [B, H, dv, dk]  fp32 (S0 NULL = zeros; S_T may be S0)
  *
- * Sizes and conventions as for lr_fwd_chunked; no workspace.  Computed on
- * the CUDA cores in fp32 (bf16 inputs are widened) in 32-token blocks: a
- * unit-lower-triangular system for the pseudo-values u_t = S_{t-1} kappa_t
- * per block, every decay factor e^{L_t - L_s} (t >= s) at most 1.  No
- * tensor-core path for this row yet.
+ *   workspace   lr_fwd_chunked_gen_delta_workspace_size(...) bytes (0 for fp32),
+ *               16-byte aligned, owned by the caller, not overlapping any argument
+ *
+ * Sizes and conventions as for lr_fwd_chunked (dk, dv in {32, 64, 128},
+ * chunk == 64, T >= 0).  Both paths work in 32-token blocks with the
+ * pseudo-values u_t = S_{t-1} kappa_t of a unit-lower-triangular system per
+ * block, every decay factor e^{L_t - L_s} (t >= s, L the cumulative log decay)
+ * at most 1.  The bf16 path runs two kernels: a per-block pass over all blocks
+ * in parallel (the four decayed score matrices, the triangular solve, the
+ * coupling to the previous block), stored in the workspace, then the
+ * sequential pass of lr_fwd_chunked with values stacked on pseudo-values, on
+ * the tensor cores.  Its score matrices split each decay at the last token of
+ * the key's 16-token half: exact while the decay over any 16 consecutive
+ * tokens stays above e^-80 (w >= 0.007 per token always satisfies it).  The
+ * fp32 path is one kernel on the CUDA cores with every decay factor taken
+ * directly.
  */
 lr_status lr_fwd_chunked_gen_delta(const void *q, const void *kw, const void *v,
                                    const float *w, const float *kappa, const float *a,
                                    const float *S0, void *o, float *S_T,
                                    int B, int H, int T, int dk, int dv, int chunk, lr_dtype dt,
-                                   cudaStream_t stream);
+                                   void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes lr_fwd_chunked_gen_delta needs (0 for fp32, T == 0, or
+ * arguments it would reject). */
+size_t lr_fwd_chunked_gen_delta_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
+                                               lr_dtype dt);
 
 /* One step of the same rule for N sequences (decode): per value row r with
  * s = S[r, :], u = s . kappa, S[r, :] <- s * w - u (a * kappa) + v_r kw,
@@ -416,9 +432,10 @@ lr_status lr_step_gen_delta(const void *q, const void *kw, const void *v, const 
 /* Static English text for a status code (never NULL). */
 const char *lr_status_string(lr_status s);
 
-/* ABI version of this header: 2 (2 added the fused entry points, the
- * diagonal gate, the mLSTM entry points and LR_ERR_FUSE; every entry point of
- * 1 is unchanged). */
+/* ABI version of this header: 3 (2 added the fused entry points, the
+ * diagonal gate, the mLSTM entry points and LR_ERR_FUSE; 3 gave
+ * lr_fwd_chunked_gen_delta a workspace and added its size query; every entry
+ * point of 1 is unchanged). */
 int lr_abi_version(void);
 
 #ifdef __cplusplus

@@ -37,8 +37,10 @@ def test_header_declares_expected_entry_points():
                                           "lr_fwd_chunked_fused_workspace_size", "lr_step_fused",
                                           "lr_fwd_chunked_mlstm",
                                           "lr_fwd_chunked_mlstm_workspace_size", "lr_step_mlstm",
-                                          "lr_fwd_chunked_gen_delta", "lr_step_gen_delta",
-                                          "lr_status_string", "lr_abi_version"}
+                                          "lr_fwd_chunked_gen_delta",
+                                          "lr_fwd_chunked_gen_delta_workspace_size",
+                                          "lr_step_gen_delta", "lr_status_string",
+                                          "lr_abi_version"}
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -52,7 +54,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings_and_version(lib):
     import gated_delta_rule_fwd_gb300 as lr
-    assert lib.lr_abi_version() == 2
+    assert lib.lr_abi_version() == 3
     for code in range(13):
         s = lr.status_string(code)
         assert s and s != "unknown status"
@@ -195,15 +197,22 @@ cases += [
 ]
 def gd(**kw):
     a = dict(zip("q kw v w kap a S0 o ST".split(), M[:9]))
-    a.update(dict(B=1, H=1, T=8, dk=32, dv=32, chunk=64, dt=0))
+    a.update(dict(B=1, H=1, T=8, dk=32, dv=32, chunk=64, dt=0, ws=None, wsb=0))
     a.update(kw)
     return L.lr_fwd_chunked_gen_delta(a["q"], a["kw"], a["v"], a["w"], a["kap"], a["a"], a["S0"],
                                       a["o"], a["ST"], a["B"], a["H"], a["T"], a["dk"], a["dv"],
-                                      a["chunk"], a["dt"], None)
+                                      a["chunk"], a["dt"], a["ws"], a["wsb"], None)
+gneed = L.lr_fwd_chunked_gen_delta_workspace_size(1, 1, 8, 32, 32, 64, 1)
 cases += [
     ("gd-null-kappa", gd(kap=None), 1), ("gd-dk48", gd(dk=48), 6), ("gd-chunk32", gd(chunk=32), 6),
     ("gd-alias-o-w", gd(o=P(0x40000000 + 512)), 8), ("gd-misaligned", gd(a=P(0x60000004)), 4),
     ("gd-valid", gd(), 7),   # passes validation, no GPU
+    ("gd-ws-null-bf16", gd(dt=1), 10), ("gd-ws-short", gd(dt=1, ws=P(0xD0000000), wsb=gneed - 16), 10),
+    ("gd-ws-alias-q", gd(dt=1, ws=M[0], wsb=gneed), 8),
+    ("gd-ws-misaligned", gd(dt=1, ws=P(0xD0000008), wsb=gneed), 4),
+    ("gd-ws-valid-bf16", gd(dt=1, ws=P(0xD0000000), wsb=gneed), 7),
+    ("gd-ws-positive", int(gneed > 0), 1),
+    ("gd-ws-f32", L.lr_fwd_chunked_gen_delta_workspace_size(1, 1, 8, 32, 32, 64, 0), 0),
     ("gd-step-null", L.lr_step_gen_delta(M[0], M[1], M[2], M[3], M[4], None, M[6], M[7], 1, 1, 32,
                                          32, 1, None), 1),
 ]
