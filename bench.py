@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import dataclasses
 import io
 import json
 import os
@@ -371,11 +372,12 @@ def run_ours(args, dist, rank, world, local):
     if not args.no_fused and not args.no_decode:
         fused_decode = run_decode(lr, dev, dist, peaks, args, fused=True)
     diag = None
-    if not args.no_diag and w.name != DIAG_WORKLOAD:
+    if not args.no_diag and not args.only_gen_delta and w.name != DIAG_WORKLOAD:
         diag = run_diag(lr, dev, dist, args, peaks)
     mlstm = gen_delta = None
-    if not args.no_diag:
+    if not args.no_diag and not args.only_gen_delta:
         mlstm = run_mlstm(lr, dev, dist, args, peaks)
+    if not args.no_diag:
         gen_delta = run_gen_delta(lr, dev, dist, args, peaks)
 
     out = None
@@ -433,6 +435,8 @@ def run_gen_delta(lr, dev, dist, args, peaks):
     pseudo-values.  Algorithmic bytes: q, kw, v, o at bf16, w, kappa, a at fp32
     per head-token, the state read and written."""
     w = workloads.WORKLOADS[GEN_DELTA_WORKLOAD]
+    if args.gen_delta_batch:  # a smaller case of the same shape per sequence (profiling)
+        w = dataclasses.replace(w, B=args.gen_delta_batch)
     x = workloads.draw_gen_delta(w.B, w.H, w.T, w.dk, w.dv, seed=w.seed, dtype=w.torch_dtype,
                                  state=True)
     xd = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
@@ -708,6 +712,10 @@ def main():
                     help="skip the fused entry points' timings (prefill and decode)")
     ap.add_argument("--no-diag", action="store_true",
                     help="skip the diagonal-gate (GLA) and mLSTM workloads' timings")
+    ap.add_argument("--only-gen-delta", action="store_true",
+                    help="of the extra workloads time only the RWKV-7 one")
+    ap.add_argument("--gen-delta-batch", type=int, default=None,
+                    help="batch of the RWKV-7 workload (default: its own; for profiling)")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of single-core oracle work in the cpu_baseline sample")
     ap.add_argument("--ref-tokens", type=int, default=2048,

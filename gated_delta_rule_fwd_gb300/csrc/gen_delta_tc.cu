@@ -46,40 +46,38 @@ constexpr int GH = GC / 2;      // tokens per half (reference of the key factors
 constexpr int GNT = 256;        // threads of the per-block pass
 constexpr float kMaxUp = 80.f;  // largest exponent of a query factor
 
-// Shared memory of the per-block pass (fp32 rows padded to 16 bytes past a
-// multiple of 128 so that 8 consecutive rows read as float4 hit distinct banks).
+// Shared memory of the per-block pass: bf16 operand tiles in the 128-byte
+// swizzled K-major layout of the tensor cores (1024-byte aligned), then fp32
+// matrices for the solve, the barriers and the TMEM slot.
 template <int DK>
 struct GdPrep {
-    static constexpr int KP = DK + 4;            // row of a [32][DK] operand
-    static constexpr int SP = GC + 4;            // row of a 32 x 32 matrix
-    static constexpr int ZP = 2 * GC + 4;        // row of the 32 x 64 Z rows
-    static constexpr int kQS = 0;                // q_t e^{L_t - L_15}; then Kt_{j-1} rows 0..31
-    static constexpr int kKS = kQS + GC * KP;    // kappa_t e^{L_{t-1} - L_15}; then Kt_{j-1} rows 32..63
-    static constexpr int kKw = kKS + GC * KP;    // kw_s e^{L_r - L_s}; then the Z rows (over kBv too)
-    static constexpr int kBv = kKw + GC * KP;    // b_s e^{L_r - L_s}
-    static constexpr int kX = kBv + GC * KP;     // second-half query factors; then Wg
-    static constexpr int kA = kX + GC * KP;      // A
-    static constexpr int kBk = kA + GC * SP;     // Bk, solved in place into Tb
-    static constexpr int kQk = kBk + GC * SP;
-    static constexpr int kQb = kQk + GC * SP;
-    static constexpr int kD = kQb + GC * SP;     // D_{j-1} per key channel
-    static constexpr int floats = kD + DK;
-    static constexpr int bytes = floats * 4;
-    static_assert(GC * ZP <= 2 * GC * KP, "the Z rows must fit over the kw and b rows");
+    static constexpr int KB = (DK + 63) / 64;     // 64-column blocks of a tile row
+    static constexpr int SP = GC + 4;             // fp32 row of a 32 x 32 matrix
+    static constexpr int AT = 0;                  // [128][DK]: query / removal-key rows, then Wg
+    static constexpr int BT = AT + KB * 128 * 128;  // [64][DK]: the key rows [kw; b]
+    static constexpr int KT = BT + KB * 64 * 128;   // [64][DK]: the previous block's Kt
+    static constexpr int F32 = KT + KB * 64 * 128;  // fp32 A [32][SP], Bk -> Tb [32][SP], D_{j-1} [DK]
+    static constexpr int BAR = F32 + (2 * GC * SP + DK) * 4;
+    static constexpr int BYTES = BAR + 32;        // two mbarriers and the TMEM slot
+    static constexpr int ALLOC = BYTES + 1024;
 };
 
-__device__ __forceinline__ float4 lds4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
-
-__device__ __forceinline__ void fma4(float &acc, float4 x, float4 y) {
-    acc = fmaf(x.x, y.x, acc);
-    acc = fmaf(x.y, y.y, acc);
-    acc = fmaf(x.z, y.z, acc);
-    acc = fmaf(x.w, y.w, acc);
+__device__ __forceinline__ void st_tile(uint8_t *tile, int rows, int r, int c, float x) {
+    *reinterpret_cast<bf16 *>(tile + sw128_offset(r, c, rows)) = __float2bfloat16_rn(x);
 }
 
 // One CTA per (block, head, batch).  q, kw [B*H][T][DK] bf16; w, kappa, a
 // [B*H][T][DK] fp32; ws: the records (B*H x (nblk + 1)); qo, ko: the per-stage
 // q and k operands, [B*H][nblk * 64][DK] bf16 each.
+//
+// Threads 0..DK-1 take this block's key channels and threads 128..128+DK-1
+// the previous block's (for its Kt).  Then two M = 128 tcgen05 products:
+//   S  = [Q e^{L-L_15}; K e^{L_{t-1}-L_15}; Q e^{L-L_31}; K e^{L_{t-1}-L_31}] [kw e^{L_r-L}; b e^{L_r-L}]^T
+//        (rows 64..127 only for queries of the second half), TMEM cols 0..63: the
+//        four score matrices, keys 0..15 from the first reference and 16..31
+//        from the second;
+//   Z  = [Wg; *] Kt_{j-1}^T, TMEM cols 64..127 (rows 0..31 used);
+// with the solve (I + A)[Wg | Tb] = [Kdec | Bk] on the CUDA cores between them.
 template <int DK>
 __global__ void __launch_bounds__(GNT, 2)
 chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
@@ -88,12 +86,14 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
                      bf16 *__restrict__ ko, int H, int T, int nblk) {
     using G = GdPrep<DK>;
     using R = Rec<DK>;
-    constexpr int KP = G::KP, SP = G::SP, ZP = G::ZP;
-    extern __shared__ float4 gd_smem[];
-    float *sm = reinterpret_cast<float *>(gd_smem);
-    float *QS = sm + G::kQS, *KS = sm + G::kKS, *KwS = sm + G::kKw, *BvS = sm + G::kBv;
-    float *X = sm + G::kX, *Am = sm + G::kA, *Bk = sm + G::kBk, *Qk = sm + G::kQk, *Qb = sm + G::kQb;
-    float *Dp = sm + G::kD;
+    constexpr int SP = G::SP;
+    extern __shared__ uint8_t gd_raw[];
+    uint8_t *sm = align1024(gd_raw);
+    uint8_t *At = sm + G::AT, *Bt = sm + G::BT, *Kt = sm + G::KT;
+    float *Am = reinterpret_cast<float *>(sm + G::F32);
+    float *Bk = Am + GC * SP, *Dp = Am + 2 * GC * SP;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + G::BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + G::BAR + 16);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int j = blockIdx.x;
     const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
@@ -102,7 +102,16 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
     uint8_t *rec_next = rec + R::BYTES;
     bf16 *qrow = qo + (bh * nblk + j) * (size_t)(2 * GC) * DK;
     bf16 *krow = ko + (bh * nblk + j) * (size_t)(2 * GC) * DK;
-    const bf16 zero = __float2bfloat16_rn(0.f);
+
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 128);
+        tmem_relinquish();
+    }
 
     // ---- this block, one thread per key channel: decays, scaled operands,
     //      the stage's q and k rows; Kdec stays in registers for the solve
@@ -115,7 +124,7 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
         float acc = 0.f;
 #pragma unroll
         for (int t = 0; t < GC; ++t) {
-            acc += t < n ? logf(w[g0 + (size_t)t * DK]) : 0.f;
+            acc += t < n ? __logf(w[g0 + (size_t)t * DK]) : 0.f;
             L[t] = acc;
         }
         const float Lh = L[GH - 1], Ll = L[GC - 1];
@@ -132,82 +141,112 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
             const float bf = ok ? ar[g] * kp : 0.f;
             const float Lt = L[t];
             const float fk = __expf((t < GH ? Lh : Ll) - Lt);  // key factor, at most 1
-            KwS[t * KP + c] = kf * fk;
-            BvS[t * KP + c] = bf * fk;
+            st_tile(Bt, 64, t, c, kf * fk);
+            st_tile(Bt, 64, GC + t, c, bf * fk);
             const float q0 = __expf(fminf(Lt - Lh, kMaxUp));
-            QS[t * KP + c] = qf * q0;
-            KS[t * KP + c] = kp * ks0;
+            st_tile(At, 128, t, c, qf * q0);
+            st_tile(At, 128, GC + t, c, kp * ks0);
             ks0 = q0;
             if (t >= GH) {
                 if (t == GH) ks1 = __expf(fminf(Lh - Ll, kMaxUp));
                 const float q1 = __expf(fminf(Lt - Ll, kMaxUp));
-                X[(t - GH) * KP + c] = qf * q1;  // second-half query rows 0..15
-                X[t * KP + c] = kp * ks1;        // second-half removal-key rows 16..31
+                st_tile(At, 128, 2 * GC + t, c, qf * q1);
+                st_tile(At, 128, 3 * GC + t, c, kp * ks1);
                 ks1 = q1;
+            } else {
+                st_tile(At, 128, 2 * GC + t, c, 0.f);
+                st_tile(At, 128, 3 * GC + t, c, 0.f);
             }
             kdec[t] = kp * eprev;
             const float eL = __expf(Lt);
             eprev = eL;
             qrow[t * DK + c] = __float2bfloat16_rn(qf * eL);
-            qrow[(GC + t) * DK + c] = zero;
             const float fK = t < GH ? fk * fh : fk;  // e^{L_last - L_t}
             krow[t * DK + c] = __float2bfloat16_rn(kf * fK);
             krow[(GC + t) * DK + c] = __float2bfloat16_rn(-bf * fK);
         }
         Dj = __expf(Ll);
-    }
-    __syncthreads();
-
-    // ---- the four score matrices: warps 0..3 take queries 0..31 against keys
-    //      0..15 (reference 15), warps 4..5 queries 16..31 against keys 16..31
-    //      (reference 31); each lane a 2 x 2 tile of all four
-    if (warp < 6) {
-        const int rt = lane >> 3, ct = lane & 7;
-        const bool second = warp >= 4;
-        const int tb = second ? GH + 8 * (warp - 4) : 8 * warp, sb = second ? GH : 0;
-        const int tr[2] = {tb + rt, tb + rt + 4}, sc[2] = {sb + ct, sb + ct + 8};
-        const float *qp[2], *kp[2], *wp[2], *bp[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            qp[i] = second ? X + (tr[i] - GH) * KP : QS + tr[i] * KP;
-            kp[i] = second ? X + tr[i] * KP : KS + tr[i] * KP;
-            wp[i] = KwS + sc[i] * KP;
-            bp[i] = BvS + sc[i] * KP;
-        }
-        float qk[4] = {0.f, 0.f, 0.f, 0.f}, qb[4] = {0.f, 0.f, 0.f, 0.f};
-        float bk[4] = {0.f, 0.f, 0.f, 0.f}, aa[4] = {0.f, 0.f, 0.f, 0.f};
+    } else if (tid >= 128 && tid < 128 + DK) {
+        // ---- the previous block's Kt = [Kw'; -B'] and D (block j-1 is full)
+        const int c = tid - 128;
+        if (j == 0) {
 #pragma unroll 4
-        for (int c4 = 0; c4 < DK; c4 += 4) {
-            const float4 q0 = lds4(qp[0] + c4), q1 = lds4(qp[1] + c4);
-            const float4 k0 = lds4(kp[0] + c4), k1 = lds4(kp[1] + c4);
-            const float4 w0 = lds4(wp[0] + c4), w1 = lds4(wp[1] + c4);
-            const float4 b0 = lds4(bp[0] + c4), b1 = lds4(bp[1] + c4);
-            fma4(qk[0], q0, w0), fma4(qk[1], q0, w1), fma4(qk[2], q1, w0), fma4(qk[3], q1, w1);
-            fma4(qb[0], q0, b0), fma4(qb[1], q0, b1), fma4(qb[2], q1, b0), fma4(qb[3], q1, b1);
-            fma4(bk[0], k0, w0), fma4(bk[1], k0, w1), fma4(bk[2], k1, w0), fma4(bk[3], k1, w1);
-            fma4(aa[0], k0, b0), fma4(aa[1], k0, b1), fma4(aa[2], k1, b0), fma4(aa[3], k1, b1);
-        }
+            for (int s = 0; s < 2 * GC; ++s) st_tile(Kt, 64, s, c, 0.f);
+            Dp[c] = 1.f;
+        } else {
+            const size_t g0 = (bh * T + t0 - GC) * DK + c;
+            float Lp[GC];
+            float acc = 0.f;
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int l = 0; l < 2; ++l) {
-                const int t = tr[i], s = sc[l], e = 2 * i + l;
-                Qk[t * SP + s] = s <= t ? qk[e] : 0.f;
-                Qb[t * SP + s] = s <= t ? qb[e] : 0.f;
-                Bk[t * SP + s] = s < t ? bk[e] : 0.f;
-                Am[t * SP + s] = s < t ? aa[e] : 0.f;
+            for (int s = 0; s < GC; ++s) {
+                acc += __logf(w[g0 + (size_t)s * DK]);
+                Lp[s] = acc;
             }
-    } else {
-        // queries of the first half never see keys of the second
-        for (int i = tid - 6 * 32; i < GH * GH; i += 2 * 32) {
-            const int t = i / GH, s = GH + i % GH;
-            Qk[t * SP + s] = Qb[t * SP + s] = Bk[t * SP + s] = Am[t * SP + s] = 0.f;
+#pragma unroll
+            for (int s = 0; s < GC; ++s) {
+                const size_t g = g0 + (size_t)s * DK;
+                const float f = __expf(acc - Lp[s]);
+                st_tile(Kt, 64, s, c, __bfloat162float(kw[g]) * f);
+                st_tile(Kt, 64, GC + s, c, -ar[g] * kappa[g] * f);
+            }
+            Dp[c] = __expf(acc);
         }
     }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // ---- S: the four score matrices, TMEM cols 0..63
+    if (tid == 0) {
+        const uint32_t id = idesc_bf16_f32(128, 64);
+#pragma unroll
+        for (int ks = 0; ks < DK / 16; ++ks)
+            mma_bf16(tmem, tile_desc(smem_u32(At), 128, 0, ks), tile_desc(smem_u32(Bt), 64, 0, ks),
+                     id, ks > 0);
+        mma_commit(&bar[0]);
+    }
+    bool ok = __syncthreads_and(mbar_wait(&bar[0], 0) ? 1 : 0) != 0;
+    tc_fence_after();
+    if (ok) {
+        // warp w: row quarter w & 3 (queries / removal keys, first / second
+        // reference), columns of the kw (w < 4) or b (w >= 4) keys of that
+        // reference's half; lane = token t
+        const int qr = warp & 3, h = warp >> 2, t = lane;
+        const int s0 = qr >= 2 ? GH : 0;
+        float x[16];
+        tmem_ld16(tmem + ((uint32_t)(32 * qr) << 16) + (uint32_t)(32 * h + s0), x);
+        tmem_ld_wait();
+        const bool keyrow = qr & 1;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int s = s0 + e;
+            if (keyrow ? s >= t : s > t) x[e] = 0.f;
+        }
+        if (keyrow) {  // Bk (kw keys) or A (b keys), fp32 for the solve
+            float *M = h ? Am : Bk;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) M[t * SP + s0 + e] = x[e];
+        } else {       // stage j+1's P row t: [Qk | -Qb]
+            if (h) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) x[e] = -x[e];
+            }
+#pragma unroll
+            for (int i8 = 0; i8 < 2; ++i8)
+                *reinterpret_cast<uint4 *>(rec_next + R::TZP +
+                                           sw128_offset(128 + t, 32 * h + s0 + 8 * i8, 192)) =
+                    pack8(x + 8 * i8);
+        }
+    }
+    tc_fence_before();
     __syncthreads();
 
     // ---- (I + A) [Wg | Tb] = [Kdec | Bk] by forward substitution, one column
-    //      per thread (Kdec columns from registers, Bk columns in place)
+    //      per thread; Wg goes to the A tile (rows 0..31) for Z and, times
+    //      D_{j-1}, to the record's W rows 32..63.  The other threads write the
+    //      record's constant parts.
     if (tid < DK + GC) {
         const bool tcol = tid >= DK;
         float x[GC];
@@ -219,7 +258,7 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
             // whole float4 groups: A is stored zero on and above the diagonal
 #pragma unroll
             for (int s4 = 0; s4 < t; s4 += 4) {
-                const float4 a4 = lds4(Am + t * SP + s4);
+                const float4 a4 = *reinterpret_cast<const float4 *>(Am + t * SP + s4);
                 acc = fmaf(-a4.x, x[s4], acc);
                 acc = fmaf(-a4.y, x[s4 + 1], acc);
                 acc = fmaf(-a4.z, x[s4 + 2], acc);
@@ -231,111 +270,85 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
 #pragma unroll
             for (int t = 0; t < GC; ++t) Bk[t * SP + (tid - DK)] = x[t];
         } else {
+            const float d = Dp[tid];
 #pragma unroll
-            for (int t = 0; t < GC; ++t) X[t * KP + tid] = x[t];
-        }
-    }
-    // ---- the previous block's Kt = [Kw'; -B'] and D, recomputed (same threads
-    //      as the Kdec columns, disjoint shared memory)
-    if (tid < DK) {
-        const int c = tid;
-        float *Kt = QS;  // [64][KP] over the QS and KS rows
-        if (j == 0) {
-#pragma unroll 4
-            for (int s = 0; s < 2 * GC; ++s) Kt[s * KP + c] = 0.f;
-            Dp[c] = 1.f;
-        } else {
-            const size_t g0 = (bh * T + t0 - GC) * DK + c;  // block j-1 is full
-            float Lp[GC];
-            float acc = 0.f;
-#pragma unroll
-            for (int s = 0; s < GC; ++s) {
-                acc += logf(w[g0 + (size_t)s * DK]);
-                Lp[s] = acc;
-            }
-#pragma unroll
-            for (int s = 0; s < GC; ++s) {
-                const size_t g = g0 + (size_t)s * DK;
-                const float f = __expf(acc - Lp[s]);
-                const float kp = kappa[g];
-                Kt[s * KP + c] = __bfloat162float(kw[g]) * f;
-                Kt[(GC + s) * KP + c] = -ar[g] * kp * f;
-            }
-            Dp[c] = __expf(acc);
-        }
-    }
-    __syncthreads();
-
-    // ---- Z rows Wg Kt^T (32 x 64), each lane a 2 x 4 tile, staged over the kw and b rows
-    {
-        const int rt = lane >> 3, ct = lane & 7;
-        const int rb = 8 * (warp & 3), cb = 32 * (warp >> 2);
-        const float *xp0 = X + (rb + rt) * KP, *xp1 = X + (rb + rt + 4) * KP;
-        const float *kt = QS + (cb + ct) * KP;
-        float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-        for (int c4 = 0; c4 < DK; c4 += 4) {
-            const float4 x0 = lds4(xp0 + c4), x1 = lds4(xp1 + c4);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float4 k4 = lds4(kt + 8 * i * KP + c4);
-                fma4(z[i], x0, k4);
-                fma4(z[4 + i], x1, k4);
+            for (int t = 0; t < GC; ++t) {
+                st_tile(At, 128, t, tid, x[t]);
+                *reinterpret_cast<bf16 *>(rec + R::WT + sw128_offset(GC + t, tid, 64)) =
+                    __float2bfloat16_rn(x[t] * d);
             }
         }
-        float *Z = KwS;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            Z[(rb + rt) * ZP + cb + ct + 8 * i] = z[i];
-            Z[(rb + rt + 4) * ZP + cb + ct + 8 * i] = z[4 + i];
-        }
-    }
-    __syncthreads();
-
-    // ---- the records, as bf16 tiles in the scan's operand layout
-    {
-        const float *Z = KwS;
-        constexpr int WCH = DK / 8;  // 8-column chunks of a W row
-        for (int i = tid; i < 2 * GC * WCH; i += GNT) {  // W = [0; Wg_j D_{j-1}]
+    } else {
+        const int i0 = tid - (DK + GC), ni = GNT - (DK + GC);
+        constexpr int WCH = DK / 8;
+        const uint4 z4 = make_uint4(0, 0, 0, 0);
+        for (int i = i0; i < GC * WCH; i += ni) {  // W rows 0..31 (the value rows of Ut)
             const int r = i / WCH, c8 = (i % WCH) * 8;
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = r < GC ? 0.f : X[(r - GC) * KP + c8 + e] * Dp[c8 + e];
-            *reinterpret_cast<uint4 *>(rec + R::WT + sw128_offset(r, c8, 64)) = pack8(x);
+            *reinterpret_cast<uint4 *>(rec + R::WT + sw128_offset(r, c8, 64)) = z4;
+            reinterpret_cast<uint4 *>(qrow + (GC + r) * DK)[c8 / 8] = z4;  // q rows 32..63
         }
-        for (int i = tid; i < 128 * 8; i += GNT) {  // T rows [I | 0; Tb | 0], Z rows [0; Z]
-            const int r = i >> 3, c8 = (i & 7) * 8;
-            float x[8];
+        for (int i = i0; i < 3 * GC * 8; i += ni) {  // T rows 0..31 = [I | 0], rows 64..95 = 0,
+            const int r = i >> 3, c8 = (i & 7) * 8;   // stage j+1's P rows 160..191 = 0
+            if (r < GC) {
+                float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int col = c8 + e;
-                x[e] = r < GC          ? (col == r ? 1.f : 0.f)
-                       : r < 2 * GC    ? (col < GC ? Bk[(r - GC) * SP + col] : 0.f)
-                       : r < 3 * GC    ? 0.f
-                                       : Z[(r - 3 * GC) * ZP + col];
+                for (int e = 0; e < 8; ++e) x[e] = c8 + e == r ? 1.f : 0.f;
+                *reinterpret_cast<uint4 *>(rec + R::TZP + sw128_offset(r, c8, 192)) = pack8(x);
+            } else if (r < 2 * GC) {
+                *reinterpret_cast<uint4 *>(rec + R::TZP + sw128_offset(GC + r, c8, 192)) = z4;
+            } else {
+                *reinterpret_cast<uint4 *>(rec_next + R::TZP + sw128_offset(96 + r, c8, 192)) = z4;
             }
-            *reinterpret_cast<uint4 *>(rec + R::TZP + sw128_offset(r, c8, 192)) = pack8(x);
         }
-        for (int i = tid; i < 64 * 8; i += GNT) {  // stage j+1's P rows [Qk | -Qb; 0]
-            const int r = i >> 3, c8 = (i & 7) * 8;
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int col = c8 + e;
-                x[e] = r >= GC ? 0.f : col < GC ? Qk[r * SP + col] : -Qb[r * SP + col - GC];
-            }
-            *reinterpret_cast<uint4 *>(rec_next + R::TZP + sw128_offset(128 + r, c8, 192)) = pack8(x);
-        }
-        float *vec = reinterpret_cast<float *>(rec + R::VEC);
-        vec[tid] = tid < DK ? Dp[tid] : 0.f;  // g_C' per key channel (GNT = 256 floats)
         if (j == nblk - 1) {
-            // the closing stage reads its gate vector and (unused) T and Z rows
-            float *vn = reinterpret_cast<float *>(rec_next + R::VEC);
-            vn[tid] = tid < DK ? Dj : 0.f;
-            for (int i = tid; i < (R::TZP + 128 * 128) / 16; i += GNT)
-                reinterpret_cast<uint4 *>(rec_next)[i] = make_uint4(0, 0, 0, 0);
+            // the closing stage reads (unused) W, T and Z rows
+            for (int i = i0; i < (R::TZP + 128 * 128) / 16; i += ni)
+                reinterpret_cast<uint4 *>(rec_next)[i] = z4;
         }
     }
+    float *vec = reinterpret_cast<float *>(rec + R::VEC);
+    vec[tid] = tid < DK ? Dp[tid] : 0.f;  // g_C' per key channel (GNT = 256 floats)
+    if (j == nblk - 1) {
+        float *vn = reinterpret_cast<float *>(rec_next + R::VEC);
+        vn[tid] = tid < DK ? Dj : 0.f;
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- Z = Wg Kt_{j-1}^T, TMEM cols 64..127; meanwhile the T rows [Tb | 0]
+    if (tid == 0 && ok) {
+        const uint32_t id = idesc_bf16_f32(128, 64);
+#pragma unroll
+        for (int ks = 0; ks < DK / 16; ++ks)
+            mma_bf16(tmem + 64, tile_desc(smem_u32(At), 128, 0, ks),
+                     tile_desc(smem_u32(Kt), 64, 0, ks), id, ks > 0);
+        mma_commit(&bar[1]);
+    }
+    {
+        const int r = tid >> 3, c8 = (tid & 7) * 8;  // 32 rows x 8 chunks
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = c8 + e < GC ? Bk[r * SP + c8 + e] : 0.f;
+        *reinterpret_cast<uint4 *>(rec + R::TZP + sw128_offset(GC + r, c8, 192)) = pack8(x);
+    }
+    ok = __syncthreads_and((ok && mbar_wait(&bar[1], 0)) ? 1 : 0) != 0;
+    tc_fence_after();
+    if (ok && (warp & 3) == 0) {  // warps 0 and 4: Z rows t = lane, columns 32 h ..
+        const int h = warp >> 2, t = lane;
+        float z[32];
+        tmem_ld32(tmem + 64 + 32 * h, z);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i8 = 0; i8 < 4; ++i8)
+            *reinterpret_cast<uint4 *>(rec + R::TZP + sw128_offset(3 * GC + t, 32 * h + 8 * i8, 192)) =
+                pack8(z + 8 * i8);
+    }
+    if (!ok && tid == 0) atomicExch(&g_tc_error, 1);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 template <int DK>
@@ -346,7 +359,7 @@ cudaError_t launch_gd_dk(const void *q, const void *kw, const void *v, const flo
     const int nblk = (T + GC - 1) / GC;
     auto prep = chunk_prep_gd_kernel<DK>;
     auto scan = chunk_scan_kernel<DK, true, true, false, true>;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(prep), GdPrep<DK>::bytes, slot);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(prep), GdPrep<DK>::ALLOC, slot);
     if (e != cudaSuccess) return e;
     e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC, slot + 1);
     if (e != cudaSuccess) return e;
@@ -358,7 +371,7 @@ cudaError_t launch_gd_dk(const void *q, const void *kw, const void *v, const flo
     if ((e = make_rows_map(&tmq, qo, DK, nblk * 2 * GC, B * H)) != cudaSuccess) return e;
     if ((e = make_rows_map(&tmk, ko, DK, nblk * 2 * GC, B * H)) != cudaSuccess) return e;
     if ((e = make_rows_map(&tmv, v, dv, T, B * H)) != cudaSuccess) return e;
-    prep<<<dim3(nblk, H, B), GNT, GdPrep<DK>::bytes, stream>>>(
+    prep<<<dim3(nblk, H, B), GNT, GdPrep<DK>::ALLOC, stream>>>(
         static_cast<const bf16 *>(q), static_cast<const bf16 *>(kw), w, kappa, a, recs, qo, ko, H,
         T, nblk);
     e = cudaGetLastError();
