@@ -51,8 +51,8 @@ TRAFFIC_SOURCES = ("gated_delta_rule_fwd_gb300/csrc/chunked_tc.cu",
                    "gated_delta_rule_fwd_gb300/csrc/scan_tc.cuh",
                    "gated_delta_rule_fwd_gb300/csrc/tc_common.cuh")
 TRAFFIC = {
-    "gdn_prefill_bf16": {"bytes": 272.965120e6 + 288.576768e6 + 750.326272e6 + 119.162880e6,
-                         "sha256": "8ac8ca008dedfabe38494e613889b6eb28403d8269a496c5bff8b17fe43f41d2"},
+    "gdn_prefill_bf16": {"bytes": 272.948992e6 + 289.060352e6 + 750.235136e6 + 119.285504e6,
+                         "sha256": "b6597eb4f89364b344a3e65b7a51844782445dde9e2b0ec7c58321b18a603e6e"},
 }
 
 
@@ -430,8 +430,10 @@ def run_ours(args, dist, rank, world, local):
 
 def run_gen_delta(lr, dev, dist, args, peaks):
     """The generalised delta rule (RWKV-7 reading) through
-    lr_fwd_chunked_gen_delta: two launches, the per-block pass over 32-token
-    blocks (CUDA cores, fp32) and the tensor-core scan with values stacked on
+    lr_fwd_chunked_gen_delta: three launches, the per-block pass over 32-token
+    blocks (decays on the CUDA cores, the four score matrices by one tcgen05
+    product, the triangular solve), the coupling of consecutive blocks (one
+    tcgen05 product per block) and the tensor-core scan with values stacked on
     pseudo-values.  Algorithmic bytes: q, kw, v, o at bf16, w, kappa, a at fp32
     per head-token, the state read and written."""
     w = workloads.WORKLOADS[GEN_DELTA_WORKLOAD]
@@ -468,10 +470,10 @@ def run_gen_delta(lr, dev, dist, args, peaks):
     return {"workload": w.name, "entry_point": "lr_fwd_chunked_gen_delta", "B": w.B, "H": w.H,
             "T": w.T, "dk": w.dk, "dv": w.dv, "value": w.B * w.T * world / (ms / 1e3),
             "unit": UNIT, "ms_per_step": ms, "steps": steps, "algorithmic_bytes_per_launch": nbytes,
-            "achieved_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "gpu_launches": 2 * steps,
+            "achieved_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "gpu_launches": 3 * steps,
             "workspace_bytes": ws.numel(),
-            "path": "per-block pass on the CUDA cores (fp32) + tcgen05 scan (bf16 operands, "
-                    "fp32 state)"}
+            "path": "per-block pass (tcgen05 scores, fp32 solve) + tcgen05 coupling + tcgen05 "
+                    "scan (bf16 operands, fp32 state)"}
 
 
 def run_mlstm(lr, dev, dist, args, peaks):

@@ -47,19 +47,38 @@ constexpr int GNT = 256;        // threads of the per-block pass
 constexpr float kMaxUp = 80.f;  // largest exponent of a query factor
 
 // Shared memory of the per-block pass: bf16 operand tiles in the 128-byte
-// swizzled K-major layout of the tensor cores (1024-byte aligned), then fp32
-// matrices for the solve, the barriers and the TMEM slot.
+// swizzled K-major layout of the tensor cores (1024-byte aligned), Kdec and
+// the partial log-decay sums in fp32, the barrier and the TMEM slot.  After
+// the score product the query tile hosts the fp32 matrices of the solve.
 template <int DK>
 struct GdPrep {
-    static constexpr int KB = (DK + 63) / 64;     // 64-column blocks of a tile row
-    static constexpr int SP = GC + 4;             // fp32 row of a 32 x 32 matrix
-    static constexpr int AT = 0;                  // [128][DK]: query / removal-key rows, then Wg
+    static constexpr int KB = (DK + 63) / 64;       // 64-column blocks of a tile row
+    static constexpr int TPC = GNT / DK;            // threads per key channel
+    static constexpr int TPT = GC / TPC;            // tokens per thread
+    static constexpr int SP = GC + 4;               // fp32 row of a 32 x 32 matrix
+    static constexpr int AT = 0;                    // [128][DK]: query / removal-key rows
     static constexpr int BT = AT + KB * 128 * 128;  // [64][DK]: the key rows [kw; b]
-    static constexpr int KT = BT + KB * 64 * 128;   // [64][DK]: the previous block's Kt
-    static constexpr int F32 = KT + KB * 64 * 128;  // fp32 A [32][SP], Bk -> Tb [32][SP], D_{j-1} [DK]
-    static constexpr int BAR = F32 + (2 * GC * SP + DK) * 4;
-    static constexpr int BYTES = BAR + 32;        // two mbarriers and the TMEM slot
+    static constexpr int KD = BT + KB * 64 * 128;   // fp32 [32][DK]: Kdec
+    static constexpr int PS = KD + GC * DK * 4;     // fp32 [2][TPC][DK]: partial sums of log w
+    static constexpr int BAR = PS + 2 * GNT * 4;
+    static constexpr int BYTES = BAR + 16;          // one mbarrier and the TMEM slot
     static constexpr int ALLOC = BYTES + 1024;
+    static_assert(2 * GC * SP * 4 <= KB * 128 * 128, "A and Bk must fit over the query tile");
+    static_assert(TPT * TPC == GC && TPC * DK == GNT && (GH % TPT) == 0, "token split");
+};
+
+// Workspace layout of the bf16 path, per (batch, head): nblk + 1 records,
+// then for all heads the per-stage q and k operands ([nblk * 64][DK] bf16
+// each) and Wg ([nblk] tiles of 32 rows x DK, 128-byte swizzled like the rows
+// 0..31 of a 64-row operand tile).
+template <int DK>
+struct GdWs {
+    static constexpr size_t WG_TILE = (size_t)((DK + 63) / 64) * 32 * 128;
+    static size_t rec_bytes(size_t BH, int nblk) { return BH * (nblk + 1) * (size_t)Rec<DK>::BYTES; }
+    static size_t qk_elems(size_t BH, int nblk) { return BH * (size_t)nblk * 2 * GC * DK; }
+    static size_t bytes(size_t BH, int nblk) {
+        return rec_bytes(BH, nblk) + 2 * qk_elems(BH, nblk) * 2 + BH * nblk * WG_TILE;
+    }
 };
 
 __device__ __forceinline__ void st_tile(uint8_t *tile, int rows, int r, int c, float x) {
@@ -67,34 +86,36 @@ __device__ __forceinline__ void st_tile(uint8_t *tile, int rows, int r, int c, f
 }
 
 // One CTA per (block, head, batch).  q, kw [B*H][T][DK] bf16; w, kappa, a
-// [B*H][T][DK] fp32; ws: the records (B*H x (nblk + 1)); qo, ko: the per-stage
-// q and k operands, [B*H][nblk * 64][DK] bf16 each.
+// [B*H][T][DK] fp32.  Writes record j (all but its Z rows), stage j+1's P
+// rows, the stage's q and k operands and Wg_j.
 //
-// Threads 0..DK-1 take this block's key channels and threads 128..128+DK-1
-// the previous block's (for its Kt).  Then two M = 128 tcgen05 products:
-//   S  = [Q e^{L-L_15}; K e^{L_{t-1}-L_15}; Q e^{L-L_31}; K e^{L_{t-1}-L_31}] [kw e^{L_r-L}; b e^{L_r-L}]^T
-//        (rows 64..127 only for queries of the second half), TMEM cols 0..63: the
-//        four score matrices, keys 0..15 from the first reference and 16..31
-//        from the second;
-//   Z  = [Wg; *] Kt_{j-1}^T, TMEM cols 64..127 (rows 0..31 used);
-// with the solve (I + A)[Wg | Tb] = [Kdec | Bk] on the CUDA cores between them.
+// Thread (part, c) takes key channel c for tokens part*TPT .. part*TPT+TPT-1;
+// the log decays are summed per part and combined through shared memory.
+// One M = 128, N = 64 tcgen05 product gives the four score matrices for both
+// references:
+//   [Q e^{L-L_15}; K e^{L_{t-1}-L_15}; Q e^{L-L_31}; K e^{L_{t-1}-L_31}] [kw e^{L_r-L}; b e^{L_r-L}]^T
+// (rows 64..127 only for queries of the second half; keys 0..15 from the
+// first reference, 16..31 from the second), then the solve
+// (I + A)[Wg | Tb] = [Kdec | Bk] runs on the CUDA cores, one column per thread.
 template <int DK>
-__global__ void __launch_bounds__(GNT, 2)
+__global__ void __launch_bounds__(GNT, 3)  // 3 CTAs per SM: 80 registers, 67 KB of shared memory
 chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
                      const float *__restrict__ w, const float *__restrict__ kappa,
                      const float *__restrict__ ar, uint8_t *__restrict__ ws, bf16 *__restrict__ qo,
-                     bf16 *__restrict__ ko, int H, int T, int nblk) {
+                     bf16 *__restrict__ ko, uint8_t *__restrict__ wgo, int H, int T, int nblk) {
     using G = GdPrep<DK>;
     using R = Rec<DK>;
-    constexpr int SP = G::SP;
+    constexpr int SP = G::SP, TPC = G::TPC, TPT = G::TPT;
     extern __shared__ uint8_t gd_raw[];
     uint8_t *sm = align1024(gd_raw);
-    uint8_t *At = sm + G::AT, *Bt = sm + G::BT, *Kt = sm + G::KT;
-    float *Am = reinterpret_cast<float *>(sm + G::F32);
-    float *Bk = Am + GC * SP, *Dp = Am + 2 * GC * SP;
+    uint8_t *At = sm + G::AT, *Bt = sm + G::BT;
+    float *Kd = reinterpret_cast<float *>(sm + G::KD);
+    float *Ps = reinterpret_cast<float *>(sm + G::PS);  // [0]: this block, [1]: the previous one
+    float *Am = reinterpret_cast<float *>(sm + G::AT), *Bk = Am + GC * SP;  // after the product
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + G::BAR);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + G::BAR + 16);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + G::BAR + 8);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = tid % DK, part = tid / DK, tb = part * TPT;
     const int j = blockIdx.x;
     const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
     const int t0 = j * GC, n = min(GC, T - t0);
@@ -102,94 +123,73 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
     uint8_t *rec_next = rec + R::BYTES;
     bf16 *qrow = qo + (bh * nblk + j) * (size_t)(2 * GC) * DK;
     bf16 *krow = ko + (bh * nblk + j) * (size_t)(2 * GC) * DK;
+    uint8_t *wg = wgo + (bh * nblk + j) * GdWs<DK>::WG_TILE;
 
     if (tid == 0) {
         mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, 128);
+        tmem_alloc(tmem_slot, 64);
         tmem_relinquish();
     }
-
-    // ---- this block, one thread per key channel: decays, scaled operands,
-    //      the stage's q and k rows; Kdec stays in registers for the solve
-    float kdec[GC];
-    float Dj = 1.f;  // e^{L_last} of this block
-    if (tid < DK) {
-        const int c = tid;
-        const size_t g0 = (bh * T + t0) * DK + c;
-        float L[GC];
-        float acc = 0.f;
+    // ---- log decays: this block's prefix within the part, the previous
+    //      block's total (its D)
+    const size_t g0 = (bh * T + t0 + tb) * DK + c;
+    float lw[TPT];
+    {
+        float acc = 0.f, pacc = 0.f;
 #pragma unroll
-        for (int t = 0; t < GC; ++t) {
-            acc += t < n ? __logf(w[g0 + (size_t)t * DK]) : 0.f;
-            L[t] = acc;
+        for (int i = 0; i < TPT; ++i) {
+            acc += tb + i < n ? __logf(w[g0 + (size_t)i * DK]) : 0.f;
+            lw[i] = acc;
         }
-        const float Lh = L[GH - 1], Ll = L[GC - 1];
-        const float fh = __expf(Ll - Lh);               // first half's reference to the block end
-        float ks0 = __expf(fminf(-Lh, kMaxUp));         // e^{L_{t-1} - L_15} at t = 0 (L_{-1} = 0)
-        float ks1 = 0.f, eprev = 1.f;
+        if (j > 0) {
 #pragma unroll
-        for (int t = 0; t < GC; ++t) {
+            for (int i = 0; i < TPT; ++i) pacc += __logf(w[g0 - (size_t)GC * DK + (size_t)i * DK]);
+        }
+        Ps[part * DK + c] = acc;
+        Ps[GNT + part * DK + c] = pacc;
+    }
+    __syncthreads();
+    float off = 0.f, Lh = 0.f, Ll = 0.f, Lp = 0.f;
+#pragma unroll
+    for (int p = 0; p < TPC; ++p) {
+        const float x = Ps[p * DK + c];
+        off += p < part ? x : 0.f;
+        Lh += p < TPC / 2 ? x : 0.f;
+        Ll += x;
+        Lp += Ps[GNT + p * DK + c];
+    }
+    const float Dp = __expf(Lp);  // D_{j-1} (1 for the first block)
+
+    // ---- this thread's tokens: scaled operands, Kdec, the stage's q and k rows
+    {
+        float Lm = off;  // L_{t-1}
+#pragma unroll
+        for (int i = 0; i < TPT; ++i) {
+            const int t = tb + i;
             const bool ok = t < n;
-            const size_t g = g0 + (size_t)t * DK;
+            const size_t g = g0 + (size_t)i * DK;
             const float qf = ok ? __bfloat162float(q[g]) : 0.f;
             const float kf = ok ? __bfloat162float(kw[g]) : 0.f;
             const float kp = ok ? kappa[g] : 0.f;
             const float bf = ok ? ar[g] * kp : 0.f;
-            const float Lt = L[t];
+            const float Lt = off + lw[i];
             const float fk = __expf((t < GH ? Lh : Ll) - Lt);  // key factor, at most 1
             st_tile(Bt, 64, t, c, kf * fk);
             st_tile(Bt, 64, GC + t, c, bf * fk);
-            const float q0 = __expf(fminf(Lt - Lh, kMaxUp));
-            st_tile(At, 128, t, c, qf * q0);
-            st_tile(At, 128, GC + t, c, kp * ks0);
-            ks0 = q0;
-            if (t >= GH) {
-                if (t == GH) ks1 = __expf(fminf(Lh - Ll, kMaxUp));
-                const float q1 = __expf(fminf(Lt - Ll, kMaxUp));
-                st_tile(At, 128, 2 * GC + t, c, qf * q1);
-                st_tile(At, 128, 3 * GC + t, c, kp * ks1);
-                ks1 = q1;
-            } else {
-                st_tile(At, 128, 2 * GC + t, c, 0.f);
-                st_tile(At, 128, 3 * GC + t, c, 0.f);
-            }
-            kdec[t] = kp * eprev;
-            const float eL = __expf(Lt);
-            eprev = eL;
-            qrow[t * DK + c] = __float2bfloat16_rn(qf * eL);
-            const float fK = t < GH ? fk * fh : fk;  // e^{L_last - L_t}
+            st_tile(At, 128, t, c, qf * __expf(fminf(Lt - Lh, kMaxUp)));
+            st_tile(At, 128, GC + t, c, kp * __expf(fminf(Lm - Lh, kMaxUp)));
+            const bool second = t >= GH;
+            st_tile(At, 128, 2 * GC + t, c, second ? qf * __expf(fminf(Lt - Ll, kMaxUp)) : 0.f);
+            st_tile(At, 128, 3 * GC + t, c, second ? kp * __expf(fminf(Lm - Ll, kMaxUp)) : 0.f);
+            Kd[t * DK + c] = kp * __expf(Lm);
+            qrow[t * DK + c] = __float2bfloat16_rn(qf * __expf(Lt));
+            const float fK = __expf(Ll - Lt);  // e^{L_last - L_t}
             krow[t * DK + c] = __float2bfloat16_rn(kf * fK);
             krow[(GC + t) * DK + c] = __float2bfloat16_rn(-bf * fK);
-        }
-        Dj = __expf(Ll);
-    } else if (tid >= 128 && tid < 128 + DK) {
-        // ---- the previous block's Kt = [Kw'; -B'] and D (block j-1 is full)
-        const int c = tid - 128;
-        if (j == 0) {
-#pragma unroll 4
-            for (int s = 0; s < 2 * GC; ++s) st_tile(Kt, 64, s, c, 0.f);
-            Dp[c] = 1.f;
-        } else {
-            const size_t g0 = (bh * T + t0 - GC) * DK + c;
-            float Lp[GC];
-            float acc = 0.f;
-#pragma unroll
-            for (int s = 0; s < GC; ++s) {
-                acc += __logf(w[g0 + (size_t)s * DK]);
-                Lp[s] = acc;
-            }
-#pragma unroll
-            for (int s = 0; s < GC; ++s) {
-                const size_t g = g0 + (size_t)s * DK;
-                const float f = __expf(acc - Lp[s]);
-                st_tile(Kt, 64, s, c, __bfloat162float(kw[g]) * f);
-                st_tile(Kt, 64, GC + s, c, -ar[g] * kappa[g] * f);
-            }
-            Dp[c] = __expf(acc);
+            Lm = Lt;
         }
     }
     fence_async_smem();
@@ -198,7 +198,7 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // ---- S: the four score matrices, TMEM cols 0..63
+    // ---- the four score matrices, TMEM cols 0..63
     if (tid == 0) {
         const uint32_t id = idesc_bf16_f32(128, 64);
 #pragma unroll
@@ -207,7 +207,7 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
                      id, ks > 0);
         mma_commit(&bar[0]);
     }
-    bool ok = __syncthreads_and(mbar_wait(&bar[0], 0) ? 1 : 0) != 0;
+    const bool ok = __syncthreads_and(mbar_wait(&bar[0], 0) ? 1 : 0) != 0;
     tc_fence_after();
     if (ok) {
         // warp w: row quarter w & 3 (queries / removal keys, first / second
@@ -244,14 +244,14 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
     __syncthreads();
 
     // ---- (I + A) [Wg | Tb] = [Kdec | Bk] by forward substitution, one column
-    //      per thread; Wg goes to the A tile (rows 0..31) for Z and, times
-    //      D_{j-1}, to the record's W rows 32..63.  The other threads write the
+    //      per thread: Wg to the workspace (for the Z rows) and, times D_{j-1},
+    //      to the record's W rows 32..63.  The other threads write the
     //      record's constant parts.
     if (tid < DK + GC) {
         const bool tcol = tid >= DK;
         float x[GC];
 #pragma unroll
-        for (int t = 0; t < GC; ++t) x[t] = tcol ? Bk[t * SP + (tid - DK)] : kdec[t];
+        for (int t = 0; t < GC; ++t) x[t] = tcol ? Bk[t * SP + (tid - DK)] : Kd[t * DK + tid];
 #pragma unroll
         for (int t = 1; t < GC; ++t) {
             float acc = x[t];
@@ -270,12 +270,12 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
 #pragma unroll
             for (int t = 0; t < GC; ++t) Bk[t * SP + (tid - DK)] = x[t];
         } else {
-            const float d = Dp[tid];
+            // D_{j-1} of this column: its own thread's Dp (tid < DK: part 0, c = tid)
 #pragma unroll
             for (int t = 0; t < GC; ++t) {
-                st_tile(At, 128, t, tid, x[t]);
+                *reinterpret_cast<bf16 *>(wg + sw128_offset(t, tid, 32)) = __float2bfloat16_rn(x[t]);
                 *reinterpret_cast<bf16 *>(rec + R::WT + sw128_offset(GC + t, tid, 64)) =
-                    __float2bfloat16_rn(x[t] * d);
+                    __float2bfloat16_rn(x[t] * Dp);
             }
         }
     } else {
@@ -300,6 +300,10 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
                 *reinterpret_cast<uint4 *>(rec_next + R::TZP + sw128_offset(96 + r, c8, 192)) = z4;
             }
         }
+        if (j == 0) {  // stage 0 has no Z rows (no previous block)
+            for (int i = i0; i < GC * 8; i += ni)
+                *reinterpret_cast<uint4 *>(rec + R::TZP + sw128_offset(3 * GC + (i >> 3), (i & 7) * 8, 192)) = z4;
+        }
         if (j == nblk - 1) {
             // the closing stage reads (unused) W, T and Z rows
             for (int i = i0; i < (R::TZP + 128 * 128) / 16; i += ni)
@@ -307,48 +311,117 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
         }
     }
     float *vec = reinterpret_cast<float *>(rec + R::VEC);
-    vec[tid] = tid < DK ? Dp[tid] : 0.f;  // g_C' per key channel (GNT = 256 floats)
+    if (part == 0) vec[c] = Dp;  // g_C' per key channel
+    if (tid >= DK) vec[tid] = 0.f;
     if (j == nblk - 1) {
         float *vn = reinterpret_cast<float *>(rec_next + R::VEC);
-        vn[tid] = tid < DK ? Dj : 0.f;
+        if (part == 0) vn[c] = __expf(Ll);
+        if (tid >= DK) vn[tid] = 0.f;
     }
-    fence_async_smem();
-    tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-
-    // ---- Z = Wg Kt_{j-1}^T, TMEM cols 64..127; meanwhile the T rows [Tb | 0]
-    if (tid == 0 && ok) {
-        const uint32_t id = idesc_bf16_f32(128, 64);
-#pragma unroll
-        for (int ks = 0; ks < DK / 16; ++ks)
-            mma_bf16(tmem + 64, tile_desc(smem_u32(At), 128, 0, ks),
-                     tile_desc(smem_u32(Kt), 64, 0, ks), id, ks > 0);
-        mma_commit(&bar[1]);
-    }
-    {
+    {   // T rows 32..63 = [Tb | 0]
         const int r = tid >> 3, c8 = (tid & 7) * 8;  // 32 rows x 8 chunks
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = c8 + e < GC ? Bk[r * SP + c8 + e] : 0.f;
         *reinterpret_cast<uint4 *>(rec + R::TZP + sw128_offset(GC + r, c8, 192)) = pack8(x);
     }
+    if (!ok && tid == 0) atomicExch(&g_tc_error, 1);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
+// The Z rows of stage j >= 1: Wg_j Kt_{j-1}^T (32 x 64, K = DK) -> record j's
+// T/Z tile rows 96..127.  Wg_j comes from the workspace by bulk copy, Kt_{j-1}
+// (the previous stage's k operand) by TMA; one M = 64 tcgen05 product.
+template <int DK>
+struct GdZ {
+    static constexpr int KB = (DK + 63) / 64;
+    static constexpr int AT = 0;                  // [64][DK]: Wg rows 0..31, zero rows 32..63
+    static constexpr int BT = AT + KB * 64 * 128; // [64][DK]: Kt_{j-1}
+    static constexpr int BAR = BT + KB * 64 * 128;
+    static constexpr int BYTES = BAR + 32;
+    static constexpr int ALLOC = BYTES + 1024;
+};
+constexpr int kZThreads = 128;
+
+template <int DK>
+__global__ void __launch_bounds__(kZThreads)
+chunk_prep_gd_z_kernel(uint8_t *__restrict__ ws, const uint8_t *__restrict__ wgo, int H, int nblk,
+                       const __grid_constant__ CUtensorMap tmk) {
+    using G = GdZ<DK>;
+    using R = Rec<DK>;
+    extern __shared__ uint8_t gz_raw[];
+    uint8_t *sm = align1024(gz_raw);
+    uint8_t *At = sm + G::AT, *Bt = sm + G::BT;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + G::BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + G::BAR + 16);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int j = blockIdx.x + 1;
+    const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
+    uint8_t *rec = ws + (bh * (nblk + 1) + j) * (size_t)R::BYTES;
+    const uint8_t *wg = wgo + (bh * nblk + j) * GdWs<DK>::WG_TILE;
+
+    for (int i = tid; i < G::KB * 256; i += kZThreads) {  // rows 32..63 of each A block
+        const int kb = i >> 8, o = (i & 255) * 16;
+        *reinterpret_cast<uint4 *>(At + kb * 8192 + 4096 + o) = make_uint4(0, 0, 0, 0);
+    }
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 64);
+        tmem_relinquish();
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (tid == 0) {
+        mbar_expect_tx(&bar[0], (uint32_t)G::KB * (4096u + 8192u));
+#pragma unroll
+        for (int kb = 0; kb < G::KB; ++kb) {
+            bulk_g2s(At + kb * 8192, wg + kb * 4096, 4096, &bar[0]);
+            tma_load_3d(Bt + kb * 8192, &tmk, kb * 64, (j - 1) * 2 * GC, (int)bh, &bar[0]);
+        }
+    }
+    bool ok = mbar_wait(&bar[0], 0);
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16_f32(64, 64);
+#pragma unroll
+        for (int ks = 0; ks < DK / 16; ++ks)
+            mma_bf16(tmem, tile_desc(smem_u32(At), 64, 0, ks), tile_desc(smem_u32(Bt), 64, 0, ks), id,
+                     ks > 0);
+        mma_commit(&bar[1]);
+    }
     ok = __syncthreads_and((ok && mbar_wait(&bar[1], 0)) ? 1 : 0) != 0;
     tc_fence_after();
-    if (ok && (warp & 3) == 0) {  // warps 0 and 4: Z rows t = lane, columns 32 h ..
-        const int h = warp >> 2, t = lane;
-        float z[32];
-        tmem_ld32(tmem + 64 + 32 * h, z);
-        tmem_ld_wait();
+    // M = 64: rows 16w .. 16w + 15 in lanes 32w .. 32w + 15; rows 0..31 are warps 0 and 1
+    if (ok && warp < 2) {
+        const int r = 16 * warp + lane;
 #pragma unroll
-        for (int i8 = 0; i8 < 4; ++i8)
-            *reinterpret_cast<uint4 *>(rec + R::TZP + sw128_offset(3 * GC + t, 32 * h + 8 * i8, 192)) =
-                pack8(z + 8 * i8);
+        for (int half = 0; half < 2; ++half) {
+            float z[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * half), z);
+            tmem_ld_wait();
+            if (lane < 16) {
+#pragma unroll
+                for (int i8 = 0; i8 < 4; ++i8)
+                    *reinterpret_cast<uint4 *>(rec + R::TZP +
+                                               sw128_offset(3 * GC + r, 32 * half + 8 * i8, 192)) =
+                        pack8(z + 8 * i8);
+            }
+        }
     }
     if (!ok && tid == 0) atomicExch(&g_tc_error, 1);
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
 template <int DK>
@@ -356,26 +429,34 @@ cudaError_t launch_gd_dk(const void *q, const void *kw, const void *v, const flo
                          const float *kappa, const float *a, const float *S0, void *o,
                          float *S_T, int B, int H, int T, int dv, void *ws, cudaStream_t stream,
                          int slot) {
+    using W = GdWs<DK>;
     const int nblk = (T + GC - 1) / GC;
+    const size_t BH = (size_t)B * H;
     auto prep = chunk_prep_gd_kernel<DK>;
+    auto zk = chunk_prep_gd_z_kernel<DK>;
     auto scan = chunk_scan_kernel<DK, true, true, false, true>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(prep), GdPrep<DK>::ALLOC, slot);
     if (e != cudaSuccess) return e;
     e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC, slot + 1);
     if (e != cudaSuccess) return e;
     uint8_t *recs = static_cast<uint8_t *>(ws);
-    const size_t rec_bytes = (size_t)B * H * (nblk + 1) * Rec<DK>::BYTES;
-    bf16 *qo = reinterpret_cast<bf16 *>(recs + rec_bytes);
-    bf16 *ko = qo + (size_t)B * H * nblk * 2 * GC * DK;
+    bf16 *qo = reinterpret_cast<bf16 *>(recs + W::rec_bytes(BH, nblk));
+    bf16 *ko = qo + W::qk_elems(BH, nblk);
+    uint8_t *wgo = reinterpret_cast<uint8_t *>(ko + W::qk_elems(BH, nblk));
     CUtensorMap tmq, tmk, tmv;
     if ((e = make_rows_map(&tmq, qo, DK, nblk * 2 * GC, B * H)) != cudaSuccess) return e;
     if ((e = make_rows_map(&tmk, ko, DK, nblk * 2 * GC, B * H)) != cudaSuccess) return e;
     if ((e = make_rows_map(&tmv, v, dv, T, B * H)) != cudaSuccess) return e;
     prep<<<dim3(nblk, H, B), GNT, GdPrep<DK>::ALLOC, stream>>>(
-        static_cast<const bf16 *>(q), static_cast<const bf16 *>(kw), w, kappa, a, recs, qo, ko, H,
-        T, nblk);
+        static_cast<const bf16 *>(q), static_cast<const bf16 *>(kw), w, kappa, a, recs, qo, ko, wgo,
+        H, T, nblk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (nblk > 1) {
+        zk<<<dim3(nblk - 1, H, B), kZThreads, GdZ<DK>::ALLOC, stream>>>(recs, wgo, H, nblk, tmk);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     scan<<<dim3(dv / DVS, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
         recs, S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qo, ko,
         static_cast<const bf16 *>(v), tmq, tmk, tmv);
@@ -385,9 +466,11 @@ cudaError_t launch_gd_dk(const void *q, const void *kw, const void *v, const flo
 }  // namespace
 
 size_t gen_delta_tc_workspace_bytes(int B, int H, int T, int dk) {
-    const size_t nblk = (size_t)((T + GC - 1) / GC);
-    const size_t rec = dk == 32 ? Rec<32>::BYTES : dk == 64 ? Rec<64>::BYTES : Rec<128>::BYTES;
-    return (size_t)B * H * ((nblk + 1) * rec + 2 * nblk * 2 * GC * (size_t)dk * 2);
+    const int nblk = (T + GC - 1) / GC;
+    const size_t BH = (size_t)B * H;
+    return dk == 32 ? GdWs<32>::bytes(BH, nblk)
+           : dk == 64 ? GdWs<64>::bytes(BH, nblk)
+                      : GdWs<128>::bytes(BH, nblk);
 }
 
 // Attribute slots 154..159 belong to this file.
