@@ -128,6 +128,12 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         fence_mbar_init();
+        // the block's rows of q, kw, kappa and a, read after the decays: to L2 now
+        const size_t r0 = (bh * T + t0) * DK;
+        prefetch_l2(q + r0, (uint32_t)(n * DK * 2));
+        prefetch_l2(kw + r0, (uint32_t)(n * DK * 2));
+        prefetch_l2(kappa + r0, (uint32_t)(n * DK * 4));
+        prefetch_l2(ar + r0, (uint32_t)(n * DK * 4));
     }
     if (warp == 0) {
         tmem_alloc(tmem_slot, 64);
