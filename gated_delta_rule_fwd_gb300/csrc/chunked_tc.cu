@@ -113,6 +113,17 @@ static_assert(32 * XS * 4 <= 8192, "solve scratch must fit inside the T tile");
 static_assert(128 * 64 * 2 <= C * AP * 4, "the W tile must fit over the A matrix");
 static_assert(PrepLayout<128>::AT % 1024 == 0, "the W tile must be 1024-byte aligned");
 
+// Thread 0 waits on `bar` (when `ok`) while the rest of the CTA is parked
+// at the barrier, which issues nothing; returns the CTA-wide outcome.
+// Reads of what the barrier guarded are ordered after it by the CTA
+// barrier (callers add tcgen05.fence::after_thread_sync before TMEM reads).
+__device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, bool ok) {
+    bool w = ok;
+    if (threadIdx.x == 0 && ok) w = mbar_wait(bar, parity);
+    tc_fence_before();
+    return __syncthreads_and(w ? 1 : 0) != 0;
+}
+
 // Element (r, c) of a 64 x 64 fp32 matrix in shared memory, rows padded to
 // AP floats.
 __device__ __forceinline__ int sw64(int r, int c) { return r * AP + c; }
@@ -668,7 +679,12 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
 // four tcgen05 products of M = 64, N = 16, one per J, into one 64-column
 // accumulator.  The key factors are <= 1; the query factors are <= 1 after J
 // and at most e^80 (clamped) inside J.  All factors are products of the gates
-// (prefix products along the tokens), one thread per key channel.
+// (prefix products along the tokens).  Two threads per key channel, one per
+// half of the block (32 tokens): each keeps its half's gates in registers,
+// and the products that cross the halves are formed from the gate products
+// of the four 16-token sub-blocks, exchanged through shared memory.
+constexpr int NTD = 256;  // threads per CTA of the diagonal-gate pass
+
 template <int DK>
 struct DiagPrepLayout {
     static constexpr int KB = (DK + 63) / 64;
@@ -678,13 +694,16 @@ struct DiagPrepLayout {
     static constexpr int QH = KT + TILE;             // query factors of one key sub-block
     static constexpr int KH = QH + TILE;             // k * e^{G_e - G}
     static constexpr int NRM = KH + TILE;            // fp32 1/|q| [64], 1/|k| [64] (SiLU + L2)
-    static constexpr int BAR = NRM + 512;            // 2 barriers, TMEM slot
+    static constexpr int PRD = NRM + 512;            // fp32 gate product per sub-block [4][128]
+    static constexpr int BAR = PRD + 2048;           // 2 barriers, TMEM slot
     static constexpr int BYTES = BAR + 64;
     static constexpr int ALLOC = BYTES + 1024;
+    static_assert(C * DK * 4 <= 2 * TILE, "the block's gates must fit over the QH and KH tiles");
+    static_assert(KH == QH + TILE, "QH and KH must be contiguous");
 };
 
 template <int DK, bool QKN>
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(NTD, 3)
 chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws, int H, int T,
                        int nblk, const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk, const Fuse fz,
@@ -693,6 +712,7 @@ chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws
     using L = DiagPrepLayout<DK>;
     using R = Rec<DK>;
     constexpr int NS = C / 16;  // key sub-blocks
+    constexpr int CH = C / 2;   // tokens per thread
     extern __shared__ uint8_t sm_raw[];
     uint8_t *sm = align1024(sm_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -704,21 +724,28 @@ chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws
     uint8_t *rec_next = rec + R::BYTES;
     uint8_t *QT = sm + L::QT, *KT = sm + L::KT, *QH = sm + L::QH, *KH = sm + L::KH;
     float *inq = reinterpret_cast<float *>(sm + L::NRM), *ink = inq + 64;
+    float *prd = reinterpret_cast<float *>(sm + L::PRD);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);  // q/k tiles, products
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 16);
     const unsigned fl = fz.flags;
-    const int c = tid;  // key channel of this thread (threads >= DK have none)
+    const int c = tid & 127;  // key channel of this thread (threads with c >= DK have none)
+    const int hf = tid >> 7;  // half of the block: tokens CH hf .. CH hf + CH - 1
+    const int r0 = hf * CH;
 
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
         fence_mbar_init();
-        mbar_expect_tx(&bar[0], 2u * (uint32_t)L::KB * 8192u);
+        const uint32_t abytes = (uint32_t)n * DK * 4u;
+        mbar_expect_tx(&bar[0], 2u * (uint32_t)L::KB * 8192u + abytes);
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb) {
             tma_load_3d(QT + kb * 8192, &tmq, kb * 64, t0, (int)bh, &bar[0]);
             tma_load_3d(KT + kb * 8192, &tmk, kb * 64, t0, (int)bh, &bar[0]);
         }
+        // the block's gates ([n][DK] fp32, contiguous) by one bulk copy into
+        // the QH and KH tiles, which are not written before the keys pass
+        bulk_g2s(QH, alpha + (bh * T + t0) * DK, abytes, &bar[0]);
     }
     if (warp == 0) {
         tmem_alloc(tmem_slot, 64);
@@ -728,22 +755,32 @@ chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // this channel's gates of the block (1 past the end of the sequence)
-    float a[C];
+    bool ok = cta_wait(&bar[0], 0, true);
+    // this channel's gates of this half (1 past the end of the sequence), and
+    // the product over each of its two sub-blocks
+    float a[CH];
     if (c < DK) {
         const float ac = (fl & kScaledAlphaMaps) ? fz.ascale[blockIdx.y] : 0.f;
+        const float *sa = reinterpret_cast<const float *>(QH) + r0 * DK + c;
 #pragma unroll
-        for (int r = 0; r < C; ++r) {
+        for (int rl = 0; rl < CH; ++rl) {
             float x = 1.f;
-            if (r < n) {
-                x = alpha[(bh * T + t0 + r) * DK + c];
+            if (ok && r0 + rl < n) {
+                x = sa[rl * DK];
                 if (fl & kAlphaMaps) x = gate(fl, x, ac);
             }
-            a[r] = x;
+            a[rl] = x;
         }
+        float p0 = 1.f, p1 = 1.f;
+#pragma unroll
+        for (int rl = 0; rl < 16; ++rl) {
+            p0 *= a[rl];
+            p1 *= a[16 + rl];
+        }
+        prd[(2 * hf) * 128 + c] = p0;
+        prd[(2 * hf + 1) * 128 + c] = p1;
     }
-    bool ok = mbar_wait(&bar[0], 0);
-    if (QKN && ok) {  // SiLU of the q and k rows in place; their inverse norms
+    if (QKN && ok && tid < 2 * C) {  // SiLU of the q and k rows in place; their inverse norms
         const float in = inv_l2(silu_cols<DK>(tid < C ? QT : KT, tid & 63, 64, 0));
         if (tid < C) inq[tid] = in;
         else ink[tid - C] = in;
@@ -752,59 +789,96 @@ chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws
     ok = __syncthreads_and(ok ? 1 : 0) != 0;
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    auto ld = [&](const uint8_t *t, int r) {
-        return __bfloat162float(*reinterpret_cast<const bf16 *>(t + sw128_offset(r, c, 64)));
+    // Element (r0 + il, c) of a [64][DK] tile (sw128_offset layout).  Every
+    // row a thread touches is r0 + il with il < CH, and r0 is a multiple of 8,
+    // so the swizzle term depends on il alone: the offsets are a per-thread
+    // base, a constant XOR and an immediate.
+    const uint32_t cofs = (uint32_t)((c >> 6) * 64 * 128 + (c & 7) * 2 + r0 * 128);
+    const uint32_t cx = (uint32_t)((c & 63) >> 3) << 4;
+    auto eo = [&](int il) { return cofs + (uint32_t)il * 128u + (cx ^ ((uint32_t)(il & 7) << 4)); };
+    auto ld = [&](const uint8_t *t, int il) {
+        return __bfloat162float(*reinterpret_cast<const bf16 *>(t + eo(il)));
     };
-    auto st = [&](uint8_t *t, int r, float x) {
-        *reinterpret_cast<bf16 *>(t + sw128_offset(r, c, 64)) = __float2bfloat16_rn(x);
+    auto st = [&](uint8_t *t, int il, float x) {
+        *reinterpret_cast<bf16 *>(t + eo(il)) = __float2bfloat16_rn(x);
     };
+    const float *inqh = inq + r0, *inkh = ink + r0;
+    auto qrow = [&](int il) {
+        float qv = ld(QT, il);
+        if (QKN) qv *= inqh[il];
+        return qv;
+    };
+    // gate products of the first half and of its second sub-block
+    const float plo = c < DK ? prd[c] * prd[128 + c] : 1.f;
+    const float psb1 = c < DK ? prd[128 + c] : 1.f;
 
-    // ---- keys: K * e^{G_e - G} (sub-block suffix products) and K * e^{G_last - G}
+    // ---- keys: K * e^{G_e - G} (sub-block suffix products) and K * e^{G_last - G};
+    // the first half starts from the product of the second half's gates, so
+    // its gC ends as the product over the whole block
     float gC = 1.f;
     if (ok && c < DK) {
+        if (hf == 0) gC = prd[2 * 128 + c] * prd[3 * 128 + c];
         float s_sub = 1.f;
 #pragma unroll
-        for (int r = C - 1; r >= 0; --r) {
-            if ((r & 15) == 15) s_sub = 1.f;
-            float kv = ld(KT, r);
-            if (QKN) kv *= ink[r];
-            st(KH, r, kv * s_sub);
-            st(KT, r, kv * gC);
-            s_sub *= a[r];
-            gC *= a[r];
+        for (int rl = CH - 1; rl >= 0; --rl) {
+            if ((rl & 15) == 15) s_sub = 1.f;
+            float kv = ld(KT, rl);
+            if (QKN) kv *= inkh[rl];
+            st(KH, rl, kv * s_sub);
+            st(KT, rl, kv * gC);
+            s_sub *= a[rl];
+            gC *= a[rl];
         }
     }
-    // ---- scores, one key sub-block per product (unrolled: a[] stays in registers)
+    // ---- scores, one key sub-block per product (unrolled: a[] stays in
+    // registers).  Rows of sub-block J get e^{G_r - G_e} (inside J: the
+    // inverse of the gates r < j <= e; after J: the gates e < j <= r); each
+    // half writes its own rows.  q * e^G replaces the raw q rows of a half
+    // once that half's last sub-block has been formed: the first half at
+    // J = 2, the second at J = 3.
 #pragma unroll
     for (int J = 0; J < NS; ++J) {
         if (!ok) break;
-        const int e = 16 * J + 15;
         if (c < DK) {
-            float s = 1.f;  // rows inside J: e^{G_r - G_e} = 1 / prod_{r < j <= e} alpha_j
+            if (hf == (J >> 1)) {  // rows inside J
+                float s = 1.f;
 #pragma unroll
-            for (int r = 15; r >= 0; --r) {
-                const int rr = 16 * J + r;
-                float qv = ld(QT, rr);
-                if (QKN) qv *= inq[rr];
-                st(QH, rr, qv * fminf(__frcp_rn(s), 5.5e34f));
-                s *= a[rr];
+                for (int rl = 15; rl >= 0; --rl) {
+                    const int il = 16 * (J & 1) + rl;
+                    st(QH, il, qrow(il) * fminf(__frcp_rn(s), 5.5e34f));
+                    s *= a[il];
+                }
             }
-            float p = 1.f;  // rows after J: prod_{e < j <= r} alpha_j
+            if (hf == 0 && J == 0) {  // rows 16..31 after J = 0
+                float p = 1.f;
 #pragma unroll
-            for (int rr = e + 1; rr < C; ++rr) {
-                p *= a[rr];
-                float qv = ld(QT, rr);
-                if (QKN) qv *= inq[rr];
-                st(QH, rr, qv * p);
+                for (int il = 16; il < CH; ++il) {
+                    p *= a[il];
+                    st(QH, il, qrow(il) * p);
+                }
             }
-            if (J == NS - 1) {  // q * e^G in place (the raw rows are no longer needed)
-                float g = 1.f;
+            if (hf == 1 && J < 2) {  // rows 32..63 after J = 0 or 1
+                float p = J == 0 ? psb1 : 1.f;
 #pragma unroll
-                for (int r = 0; r < C; ++r) {
-                    g *= a[r];
-                    float qv = ld(QT, r);
-                    if (QKN) qv *= inq[r];
-                    st(QT, r, qv * g);
+                for (int il = 0; il < CH; ++il) {
+                    p *= a[il];
+                    st(QH, il, qrow(il) * p);
+                }
+            }
+            if (hf == 1 && J == 2) {  // rows 48..63 after J = 2
+                float p = 1.f;
+#pragma unroll
+                for (int il = 16; il < CH; ++il) {
+                    p *= a[il];
+                    st(QH, il, qrow(il) * p);
+                }
+            }
+            if (J >= 2 && hf == J - 2) {  // q * e^G in place over this half's raw rows
+                float g = hf == 0 ? 1.f : plo;
+#pragma unroll
+                for (int il = 0; il < CH; ++il) {
+                    g *= a[il];
+                    st(QT, il, qrow(il) * g);
                 }
             }
         }
@@ -820,7 +894,7 @@ chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws
                          tile_desc(smem_u32(KH), 64, 16 * J, ks), id, ks > 0);
             mma_commit(&bar[1]);
         }
-        ok = __syncthreads_and(mbar_wait(&bar[1], J & 1) ? 1 : 0) != 0;  // QH may be rewritten
+        ok = cta_wait(&bar[1], J & 1, true);  // QH may be rewritten after the product
         tc_fence_after();
     }
     // ---- the transformed q and k rows -> workspace (rows past T are not written)
@@ -832,35 +906,33 @@ chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws
         }
         bulk_commit();
     }
-    // ---- P rows (M = 64: rows 16w..16w+15 in lanes 32w..32w+15) -> record j+1
+    // ---- P rows (M = 64: rows 16w..16w+15 in lanes 32w..32w+15) -> record j+1;
+    // warp w takes lane quarter w & 3 and column half w >> 2
     if (ok) {
-        const int r = 16 * warp + lane;
-        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        const int wq = warp & 3, half = warp >> 2;
+        const int r = 16 * wq + lane;
+        float x[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * wq) << 16) + 32 * half, x);
+        tmem_ld_wait();
+        if (lane < 16) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float x[32];
-            tmem_ld32(tmem + lane_base + 32 * half, x);
-            tmem_ld_wait();
-            if (lane < 16) {
+            for (int e = 0; e < 32; ++e)
+                if (half * 32 + e > r) x[e] = 0.f;
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    if (half * 32 + e > r) x[e] = 0.f;
-#pragma unroll
-                for (int i8 = 0; i8 < 4; ++i8)
-                    *reinterpret_cast<uint4 *>(rec_next + R::TZP +
-                                               sw128_offset(128 + r, half * 32 + i8 * 8, 192)) =
-                        pack8(x + i8 * 8);
-            }
+            for (int i8 = 0; i8 < 4; ++i8)
+                *reinterpret_cast<uint4 *>(rec_next + R::TZP +
+                                           sw128_offset(128 + r, half * 32 + i8 * 8, 192)) =
+                    pack8(x + i8 * 8);
         }
     }
     // ---- gate vectors: unit g' and kd' (folded above), per-channel g_C
     float *vn = reinterpret_cast<float *>(rec_next + R::VEC);
     if (tid < 2 * C) vn[tid] = 1.f;
-    if (c < DK) vn[128 + c] = gC;
+    if (hf == 0 && c < DK) vn[128 + c] = gC;
     if (blk == 0) {  // stage 0 has no previous block
         float *v0 = reinterpret_cast<float *>(rec + R::VEC);
         if (tid < 2 * C) v0[tid] = 1.f;
-        if (c < DK) v0[128 + c] = 1.f;
+        if (hf == 0 && c < DK) v0[128 + c] = 1.f;
     }
     if (!ok && lane == 0) atomicExch(&g_tc_error, 1);
     if (tid == 0) bulk_wait_all();
@@ -1087,7 +1159,7 @@ cudaError_t launch_diag(const void *q, const void *k, const void *v, const float
     if ((e = make_rows_map(&tmv, v, dv, T, B * H)) != cudaSuccess) return e;
     if ((e = make_rows_map(&tmqn, qn, DK, T, B * H)) != cudaSuccess) return e;
     if ((e = make_rows_map(&tmkn, kn, DK, T, B * H)) != cudaSuccess) return e;
-    prep<<<dim3(nblk, H, B), NT, DiagPrepLayout<DK>::ALLOC, stream>>>(
+    prep<<<dim3(nblk, H, B), NTD, DiagPrepLayout<DK>::ALLOC, stream>>>(
         alpha, static_cast<uint8_t *>(ws), H, T, nblk, tmq, tmk, fz, tmqn, tmkn);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
