@@ -35,8 +35,9 @@ def dev():
 
 
 def test_noalloc_matches_workspace_entry_point_twice(dev):
-    """Two calls in a row (different inputs, one of them with the state
-    updated in place) agree with lr_fwd_chunked given a workspace."""
+    """Two calls in a row (different modes, sizes and inputs, the second
+    reusing the scratch the first left behind) agree with lr_fwd_chunked
+    given a workspace."""
     cases = [(lr.GATED_DELTA, "gdn", 2, 4, 1000, 0.1, 11), (lr.DECAY, "mamba2", 2, 3, 333, 0.0, 12)]
     for mode, gen, B, H, T, s0, seed in cases:
         x = workloads.draw(gen, B, H, T, 128, 128, seed=seed, dtype=torch.bfloat16, s0_std=s0)
