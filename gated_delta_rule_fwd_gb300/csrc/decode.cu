@@ -17,10 +17,10 @@
 // three xor shuffles.
 //
 // With the lr_fuse maps (page "Scrivere meglio nella memoria: gate e delta
-// rule"): q and k are SiLU'd and L2-normalised in registers (the 8 lanes of a
-// row hold a whole vector, so the norm is one more 8-lane sum), the gates are
-// mapped on load, and with the output RMSNorm the d_v outputs of the head are
-// kept in shared memory, normalised together and stored once.
+// rule"): SiLU of q and k is taken once per element for the CTA, shared
+// through shared memory, and the two L2 norms are one CTA-wide sum; the gates
+// are mapped on load, and with the output RMSNorm the d_v outputs of the head
+// are kept in shared memory, normalised together and stored once.
 //
 // Diagonal gate (GLA row, same page, gates section): alpha is a vector over the
 // key channels, so each lane loads the gates of its own columns and the row
@@ -48,9 +48,6 @@ __device__ __forceinline__ float sum8(float x) {
     return x;
 }
 
-__device__ __forceinline__ float4 silu4(float4 x) {
-    return make_float4(silu_f(x.x), silu_f(x.y), silu_f(x.z), silu_f(x.w));
-}
 __device__ __forceinline__ float dot4(float4 a, float4 b) {
     return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
 }
@@ -89,19 +86,42 @@ step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__r
         qr[m] = load4(qh + col);
     }
     if (fl & LR_FUSE_QK_SILU_L2) {
+        // Every row group holds the same columns, so SiLU is taken once per
+        // element for the CTA (thread i: element i of k and of q) and shared;
+        // the two squared norms are one CTA-wide sum.
+        __shared__ __align__(16) float qk_sh[2 * DK];
+        __shared__ float nn_sh[2][kStepThreads / 32];
         float kk = 0.f, qq = 0.f;
-#pragma unroll
-        for (int m = 0; m < NV; ++m) {
-            kr[m] = silu4(kr[m]);
-            qr[m] = silu4(qr[m]);
-            kk += dot4(kr[m], kr[m]);
-            qq += dot4(qr[m], qr[m]);
+        for (int i = threadIdx.x; i < DK; i += kStepThreads) {
+            const float ks = silu_f(to_f(kh[i])), qs = silu_f(to_f(qh[i]));
+            qk_sh[i] = ks;
+            qk_sh[DK + i] = qs;
+            kk += ks * ks;
+            qq += qs * qs;
         }
-        const float ik = inv_l2(sum8(kk)), iq = inv_l2(sum8(qq));
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) {
+            kk += __shfl_xor_sync(0xffffffffu, kk, d);
+            qq += __shfl_xor_sync(0xffffffffu, qq, d);
+        }
+        if (lane == 0) {
+            nn_sh[0][warp] = kk;
+            nn_sh[1][warp] = qq;
+        }
+        __syncthreads();
+        kk = 0.f;
+        qq = 0.f;
+#pragma unroll
+        for (int w = 0; w < kStepThreads / 32; ++w) {
+            kk += nn_sh[0][w];
+            qq += nn_sh[1][w];
+        }
+        const float ik = inv_l2(kk), iq = inv_l2(qq);
 #pragma unroll
         for (int m = 0; m < NV; ++m) {
-            kr[m] = scale4(kr[m], ik);
-            qr[m] = scale4(qr[m], iq);
+            const int col = 4 * (kLanesPerRow * m + sub);
+            kr[m] = scale4(*reinterpret_cast<const float4 *>(qk_sh + col), ik);
+            qr[m] = scale4(*reinterpret_cast<const float4 *>(qk_sh + DK + col), iq);
         }
     }
     float kq = 0.f;
