@@ -61,9 +61,10 @@ struct GdPrep {
     static constexpr int KD = BT + KB * 64 * 128;   // fp32 [32][DK]: Kdec
     static constexpr int PS = KD + GC * DK * 4;     // fp32 [2][TPC][DK]: partial sums of log w
     static constexpr int BAR = PS + 2 * GNT * 4;
-    static constexpr int BYTES = BAR + 16;          // one mbarrier and the TMEM slot
+    static constexpr int BYTES = BAR + 24;          // two mbarriers and the TMEM slot
     static constexpr int ALLOC = BYTES + 1024;
     static_assert(2 * GC * SP * 4 <= KB * 128 * 128, "A and Bk must fit over the query tile");
+    static_assert(2 * GC * DK * 4 <= KB * 128 * 128, "two blocks of decays must fit over the query tile");
     static_assert(TPT * TPC == GC && TPC * DK == GNT && (GH % TPT) == 0, "token split");
 };
 
@@ -112,8 +113,11 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
     float *Kd = reinterpret_cast<float *>(sm + G::KD);
     float *Ps = reinterpret_cast<float *>(sm + G::PS);  // [0]: this block, [1]: the previous one
     float *Am = reinterpret_cast<float *>(sm + G::AT), *Bk = Am + GC * SP;  // after the product
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + G::BAR);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + G::BAR + 8);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + G::BAR);  // score product, decays
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + G::BAR + 16);
+    // decays of the previous block (rows 0..GC-1) and of this one (rows GC..),
+    // fp32 [2 GC][DK], in the query tile until the tokens' operands replace them
+    const float *Ws = reinterpret_cast<const float *>(sm + G::AT);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = tid % DK, part = tid / DK, tb = part * TPT;
     const int j = blockIdx.x;
@@ -127,7 +131,14 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
 
     if (tid == 0) {
         mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
         fence_mbar_init();
+        // the decays of this block and the previous one by one bulk copy
+        const int prow = j > 0 ? GC : 0;  // previous-block rows copied
+        const uint32_t wbytes = (uint32_t)((prow + n) * DK * 4);
+        mbar_expect_tx(&bar[1], wbytes);
+        bulk_g2s(sm + G::AT + (size_t)(GC - prow) * DK * 4, w + (bh * T + t0 - prow) * DK, wbytes,
+                 &bar[1]);
         // the block's rows of q, kw, kappa and a, read after the decays: to L2 now
         const size_t r0 = (bh * T + t0) * DK;
         prefetch_l2(q + r0, (uint32_t)(n * DK * 2));
@@ -139,20 +150,24 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
         tmem_alloc(tmem_slot, 64);
         tmem_relinquish();
     }
+    // the barriers are initialised before any thread waits on them
+    __syncthreads();
+    const bool wok = mbar_wait(&bar[1], 0);
     // ---- log decays: this block's prefix within the part, the previous
     //      block's total (its D)
     const size_t g0 = (bh * T + t0 + tb) * DK + c;
     float lw[TPT];
     {
         float acc = 0.f, pacc = 0.f;
+        const float *wc = Ws + (GC + tb) * DK + c, *wp = Ws + tb * DK + c;
 #pragma unroll
         for (int i = 0; i < TPT; ++i) {
-            acc += tb + i < n ? __logf(w[g0 + (size_t)i * DK]) : 0.f;
+            acc += (wok && tb + i < n) ? __logf(wc[i * DK]) : 0.f;
             lw[i] = acc;
         }
-        if (j > 0) {
+        if (j > 0 && wok) {
 #pragma unroll
-            for (int i = 0; i < TPT; ++i) pacc += __logf(w[g0 - (size_t)GC * DK + (size_t)i * DK]);
+            for (int i = 0; i < TPT; ++i) pacc += __logf(wp[i * DK]);
         }
         Ps[part * DK + c] = acc;
         Ps[GNT + part * DK + c] = pacc;
@@ -332,7 +347,9 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
         for (int e = 0; e < 8; ++e) x[e] = c8 + e < GC ? Bk[r * SP + c8 + e] : 0.f;
         *reinterpret_cast<uint4 *>(rec + R::TZP + sw128_offset(GC + r, c8, 192)) = pack8(x);
     }
-    if (!ok && tid == 0) atomicExch(&g_tc_error, 1);
+    if (!(ok && wok) && tid == 0) atomicExch(&g_tc_error, 1);
+    // never leave with the decay copy in flight
+    if (!wok && tid == 0) mbar_wait(&bar[1], 0);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 64);
