@@ -51,8 +51,8 @@ TRAFFIC_SOURCES = ("gated_delta_rule_fwd_gb300/csrc/chunked_tc.cu",
                    "gated_delta_rule_fwd_gb300/csrc/scan_tc.cuh",
                    "gated_delta_rule_fwd_gb300/csrc/tc_common.cuh")
 TRAFFIC = {
-    "gdn_prefill_bf16": {"bytes": 272.948992e6 + 289.060352e6 + 750.235136e6 + 119.285504e6,
-                         "sha256": "b6597eb4f89364b344a3e65b7a51844782445dde9e2b0ec7c58321b18a603e6e"},
+    "gdn_prefill_bf16": {"bytes": 272.992256e6 + 289.033472e6 + 750.329600e6 + 119.154944e6,
+                         "sha256": "d7fa48e9437fdc4f762c609d18cdc8e97518837284bc0bce3d2dc262d6a8f898"},
 }
 
 
