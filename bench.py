@@ -5,9 +5,12 @@ One step = one chunked prefill of the whole workload through the C ABI
 scores, delta couplings, UT/WY pseudo-values, output, state carry).  The
 default workload is the long gated-delta prefill: B=2, H=16, T=16384,
 dk=dv=128, bf16 q/k/v/o, fp32 state, chunk 64.  Its inputs (545 MB) are larger
-than L2, so no flush is needed between steps.  A second measurement, reported
-under "decode", times 1000 consecutive decode steps (lr_step) over 512
-sequences x 32 heads.
+than L2, so no flush is needed between steps.  The other prefill workloads --
+RetNet retention (B=4, H=8, T=2048; its inputs fit in L2, so L2 is flushed
+before every timed call) and the Mamba-2-style gate (B=8, H=16, T=4096) --
+are measured the same way under their own keys, each with its roofline,
+tensor, end-to-end and oracle lines.  "decode" times 1000 consecutive decode
+steps (lr_step) over 512 sequences x 32 heads.
 
     python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 
@@ -39,6 +42,8 @@ DECODE_WORKLOAD = "gdn_decode_bf16"
 DIAG_WORKLOAD = "gla_bf16"
 MLSTM_WORKLOAD = "mlstm_bf16"
 GEN_DELTA_WORKLOAD = "rwkv7_bf16"
+# the other prefill workloads measured beside the headline, each with its own lines
+CONFIG_WORKLOADS = ("retnet_bf16", "mamba2_gate_bf16")
 METRIC = "chunked fwd tokens/s"
 UNIT = "tokens/s"
 
@@ -46,7 +51,7 @@ UNIT = "tokens/s"
 # DRAM traffic per lr_fwd_chunked call (prep + scan launches) from one ncu
 # capture of each kernel (dram__bytes_read.sum + dram__bytes_write.sum), tied
 # to the kernel source it was taken on: reported only while that source is
-# unchanged (profiles/traffic_gdn_prefill_b2h16t16384.md).
+# unchanged.
 TRAFFIC_SOURCES = ("gated_delta_rule_fwd_gb300/csrc/chunked_tc.cu",
                    "gated_delta_rule_fwd_gb300/csrc/scan_tc.cuh",
                    "gated_delta_rule_fwd_gb300/csrc/tc_common.cuh")
@@ -222,13 +227,17 @@ def max_over_ranks(dist, x, device):
 
 # ------------------------------------------------------------ oracle timing
 
+def host_cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
 def time_oracle(w, budget_s=15.0, max_heads=None):
     """The fp64 oracle, as it stands, on a bounded sample of the workload:
-    whole sequences of the first n heads, n sized for about ``budget_s`` of
-    CPU work.  Returns (tokens/s scaled to the workload, info)."""
+    whole sequences of the first n heads of batch 0, n sized for about
+    ``budget_s`` of CPU work.  Returns (tokens/s scaled to the workload, info)."""
     import oracle
     x = workloads.draw(w.gen, 1, w.H, w.T, w.dk, w.dv, w.seed, w.torch_dtype, w.s0_std)
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    cores = host_cores()
 
     def run(nh, threads):
         sl = lambda t: None if t is None else t[:, :nh].contiguous()
@@ -238,87 +247,96 @@ def time_oracle(w, budget_s=15.0, max_heads=None):
         return time.perf_counter() - t0
 
     one = run(1, 1)                                    # one head, one thread
+    # about budget_s seconds of single-core work, spread over the host cores
     n = max(1, min(w.H if max_heads is None else max_heads, int(budget_s / max(one, 1e-6))))
     threads = min(n, cores)
     wall = run(n, threads)
     head_tokens_per_s = n * w.T / wall
     tokens_per_s = head_tokens_per_s / w.H             # a token carries H heads
-    info = {"value": tokens_per_s, "unit": UNIT, "cores": threads, "kind": "oracle",
+    info = {"value": tokens_per_s, "unit": UNIT, "cores": threads, "host_cores": cores,
+            "kind": "oracle",
             "sample": f"{n} of {w.B * w.H} (batch, head) sequences, all T={w.T} tokens each, "
-                      f"fp64 C recurrence; {n * w.T} head-tokens in {wall:.2f} s wall "
+                      f"fp64 C recurrence on {threads} threads ({cores} host cores); "
+                      f"{n * w.T} head-tokens in {wall:.2f} s wall "
                       f"({one:.2f} s for one sequence on one core)"}
     return tokens_per_s, info
 
 
-# ------------------------------------------------------------------- arms
+def l2_note(w, dev, flush):
+    """Input bytes of one call against the device's L2, and what the timing did."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    es = 2 if w.dtype == "bf16" else 4
+    heads = w.B * w.H
+    inputs = heads * w.T * es * (2 * w.dk + w.dv) + heads * w.T * 4 * 2
+    if w.s0_std > 0:
+        inputs += heads * w.dv * w.dk * 4
+    how = (f"L2 flushed before every timed call (a {2 * l2 >> 20} MB write outside the timed "
+           "events)" if flush else "no flush between calls")
+    rel = "<" if inputs < l2 else ">"
+    return f"inputs {inputs / 1e6:.1f} MB {rel} {l2 / 1e6:.1f} MB L2; {how}", inputs
 
-def run_ours(args, dist, rank, world, local):
-    import gated_delta_rule_fwd_gb300 as lr
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    w = workloads.WORKLOADS[args.workload]
-    peaks = load_peaks()
 
-    x = workloads.draw_workload(w)
-    xd = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
-    o = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.torch_dtype, device=dev)
-    st = torch.empty((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    ws = torch.empty(max(1, lr.workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.torch_dtype, w.mode,
-                                              w.chunk)), dtype=torch.uint8, device=dev)
+class Flusher:
+    """Writes a buffer of twice the L2 size, evicting whatever L2 held."""
 
-    def step():
-        lr.lr_fwd_chunked(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], xd["S0"],
-                          mode=w.mode, chunk=w.chunk, o=o, S_T=st, workspace=ws, stream=stream)
+    def __init__(self, dev):
+        n = 2 * torch.cuda.get_device_properties(dev).L2_cache_size
+        self.buf = torch.empty(n // 4, dtype=torch.int32, device=dev)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
+    def __call__(self):
+        self.buf.fill_(1)
 
-    clocks = ClockSampler(dev.index)
-    clocks.start()
-    time.sleep(0.3)
+
+def time_calls(step, stream, steps, dist, dev, flush=None):
+    """Mean ms per call over ``steps`` calls, CUDA events on ``stream``, max
+    over ranks.  With ``flush``: L2 is flushed before every call, outside the
+    timed events, and each call is timed on its own."""
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    wall0 = time.time()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    wall1 = time.time()
-    barrier(dist, dev)
-    clocks.stop()
-    ms = ev0.elapsed_time(ev1)
-    ms_max = max_over_ranks(dist, ms, dev)
-    ms_per_step = ms_max / args.steps
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1)
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for a, b in evs:
+            with torch.cuda.stream(stream):
+                flush()
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = sum(a.elapsed_time(b) for a, b in evs)
+    return max_over_ranks(dist, ms, dev) / steps
 
-    tokens = w.B * w.T * world
-    value = tokens * args.steps / (ms_max / 1e3)
-    kernel_s = ms / args.steps / 1e3                   # one call (prep + scan) per step
-    nbytes, nflops = chunk_bytes(w), chunk_flops(w)
-    achieved_gbs = nbytes / kernel_s / 1e9
-    achieved_tf = nflops / kernel_s / 1e12
 
-    # end to end through the public API: every step copies its inputs from
-    # pinned host memory to the device, calls lr_fwd_chunked and copies o and
-    # S_T back to pinned host memory.  Steps are pipelined over streams
-    # (uploads, calls, downloads) with two device buffer sets, so the uploads
-    # of step i+1 and the downloads of step i-1 overlap the call of step i.
+def e2e_chunked(lr, w, x, dev, dist, stream, ws, steps):
+    """End to end through the public API: every step copies its inputs from
+    pinned host memory to the device, calls lr_fwd_chunked and copies o and
+    S_T back to pinned host memory.  Steps are pipelined over streams
+    (uploads, calls, downloads) with two device buffer sets, so the uploads of
+    step i+1 and the downloads of step i-1 overlap the call of step i.
+    Returns (tokens/s over all ranks, h2d bytes, d2h bytes)."""
+    world = dist.get_world_size() if dist else 1
     hx = {n: (t.pin_memory() if t is not None else None) for n, t in x.items()}
     used = {n for n, t in hx.items()
             if t is not None and not (n == "alpha" and w.mode in (workloads.LINEAR, workloads.DELTA))
             and not (n == "beta" and w.mode in (workloads.LINEAR, workloads.DECAY,
                                                  workloads.DIAG_DECAY))}
-    ho = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
-    hs = [torch.empty(st.shape, dtype=st.dtype).pin_memory() for _ in range(2)]
+    oshape, sshape = (w.B, w.H, w.T, w.dv), (w.B, w.H, w.dv, w.dk)
+    ho = [torch.empty(oshape, dtype=w.torch_dtype).pin_memory() for _ in range(2)]
+    hs = [torch.empty(sshape, dtype=torch.float32).pin_memory() for _ in range(2)]
     h2d = sum(hx[n].numel() * hx[n].element_size() for n in used)
     d2h = ho[0].numel() * ho[0].element_size() + hs[0].numel() * hs[0].element_size()
     dx = [{n: (torch.empty_like(hx[n], device=dev) if n in used else None) for n in hx}
           for _ in range(2)]
-    do_ = [torch.empty_like(o) for _ in range(2)]
-    ds_ = [torch.empty_like(st) for _ in range(2)]
+    do_ = [torch.empty(oshape, dtype=w.torch_dtype, device=dev) for _ in range(2)]
+    ds_ = [torch.empty(sshape, dtype=torch.float32, device=dev) for _ in range(2)]
     s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     up_done = [torch.cuda.Event() for _ in range(2)]
     call_done = [torch.cuda.Event() for _ in range(2)]
@@ -347,84 +365,188 @@ def run_ours(args, dist, rank, world, local):
             down_done[b].record(s_down)
         started[b] = True
 
-    e2e_steps = max(3, min(args.steps, 20))
     for i in range(2):
         e2e_step(i)
     torch.cuda.synchronize(dev)
     barrier(dist, dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s_up)
-    for i in range(e2e_steps):
+    for i in range(steps):
         e2e_step(i)
     s_down.wait_stream(s_up)
     s_down.wait_stream(stream)
     e1.record(s_down)
     torch.cuda.synchronize(dev)
     e_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
-    e2e_value = tokens * e2e_steps / (e_ms / 1e3)
-    del hx, ho, hs, dx, do_, ds_
+    return w.B * w.T * world * steps / (e_ms / 1e3), h2d, d2h
 
-    decode = None if args.no_decode else run_decode(lr, dev, dist, peaks, args)
-    fused = None
+
+def work_lines(w, ms_per_call, peaks, traffic=None):
+    """roofline (HBM, algorithmic bytes) and tensor (chunk-form flops) objects
+    for one lr_fwd_chunked call of ``w`` taking ``ms_per_call``."""
+    s = ms_per_call / 1e3
+    nbytes, nflops = chunk_bytes(w), chunk_flops(w)
+    gbs, tf = nbytes / s / 1e9, nflops / s / 1e12
+    roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm_gbs"], "traffic": traffic,
+            "peak_source": peaks["source"] + " burst copy", "algorithmic_bytes_per_launch": nbytes}
+    tensor = {"achieved_tflops": tf, "peak_tflops": peaks["bf16_tflops"],
+              "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "flops_per_launch": nflops,
+              "count": "chunk-form MMA flops", "recurrent_flops_per_launch": recurrent_flops(w),
+              "achieved_tflops_recurrent_count": recurrent_flops(w) / s / 1e12}
+    return roof, tensor
+
+
+def mode_name(w):
+    return ["linear", "decay", "delta", "gated_delta", "diag_decay"][w.mode]
+
+
+def bench_config(lr, w, args, dist, dev, peaks, rank, world):
+    """One of the other prefill workloads (RetNet retention, Mamba-2-style
+    gate), measured like the headline: device-resident calls (with an L2
+    flush before every call when the inputs fit in L2, and back to back),
+    its roofline and tensor lines, the end-to-end number and the oracle on
+    the host cores."""
+    x = workloads.draw_workload(w)
+    xd = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.torch_dtype, device=dev)
+    st = torch.empty((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, lr.workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.torch_dtype, w.mode,
+                                              w.chunk)), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        lr.lr_fwd_chunked(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], xd["S0"],
+                          mode=w.mode, chunk=w.chunk, o=o, S_T=st, workspace=ws, stream=stream)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    steps = max(3, min(args.steps, 100))
+    note, inputs = l2_note(w, dev, flush=False)
+    fits = inputs < torch.cuda.get_device_properties(dev).L2_cache_size
+    ms_b2b = time_calls(step, stream, steps, dist, dev)
+    ms_fl = time_calls(step, stream, steps, dist, dev, flush=Flusher(dev)) if fits else None
+    ms = ms_fl if fits else ms_b2b
+    roof, tensor = work_lines(w, ms, peaks)
+    e2e_v, h2d, d2h = e2e_chunked(lr, w, x, dev, dist, stream, ws, max(3, min(args.steps, 20)))
+    out = {"workload": w.name, "entry_point": "lr_fwd_chunked", "metric": METRIC,
+           "value": w.B * w.T * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+           "steps": steps, "higher_is_better": True, "dtype": w.dtype,
+           "config": {"workload": w.name, "mode": mode_name(w), "B": w.B, "H": w.H, "T": w.T,
+                      "dk": w.dk, "dv": w.dv, "chunk": w.chunk, "state": "fp32",
+                      "l2": l2_note(w, dev, flush=fits)[0]},
+           "ms_per_step_back_to_back": ms_b2b, "roofline": roof, "tensor": tensor,
+           "e2e": {"value": e2e_v, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h},
+           "gpu_launches": steps * 2}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = time_oracle(w, budget_s=min(args.cpu_budget, 8.0))[1]
+    return out
+
+
+def run_ours(args, dist, rank, world, local):
+    import gated_delta_rule_fwd_gb300 as lr
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.WORKLOADS[args.workload]
+    peaks = load_peaks()
+
+    x = workloads.draw_workload(w)
+    xd = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.torch_dtype, device=dev)
+    st = torch.empty((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ws = torch.empty(max(1, lr.workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.torch_dtype, w.mode,
+                                              w.chunk)), dtype=torch.uint8, device=dev)
+
+    def step():
+        lr.lr_fwd_chunked(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], xd["S0"],
+                          mode=w.mode, chunk=w.chunk, o=o, S_T=st, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    note, inputs = l2_note(w, dev, flush=False)
+    fits = inputs < torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = Flusher(dev) if fits else None
+
+    # the timed region: exactly K steps (with an L2 flush before each when the
+    # inputs would fit in L2); then the same steps repeated for at least a
+    # second, so the clock sampler sees the GPU under this load
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.time()
+    ms_per_step = time_calls(step, stream, args.steps, dist, dev, flush=flush)
+    sustained_steps, t_end = 0, time.time() + 1.0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    while time.time() < t_end or sustained_steps < args.steps:
+        for _ in range(args.steps):
+            step()
+        sustained_steps += args.steps
+        torch.cuda.synchronize(dev)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    barrier(dist, dev)
+    clocks.stop()
+    sustained_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev) / sustained_steps
+
+    tokens = w.B * w.T * world
+    value = tokens / (ms_per_step / 1e3)
+    roof, tensor = work_lines(w, ms_per_step, peaks,
+                              args.traffic if args.traffic is not None else measured_traffic(w))
+    e2e_value, h2d, d2h = e2e_chunked(lr, w, x, dev, dist, stream, ws, max(3, min(args.steps, 20)))
+
+    extra = {}
+    if not args.no_configs:
+        for name in CONFIG_WORKLOADS:
+            if name != w.name:
+                extra[name] = bench_config(lr, workloads.WORKLOADS[name], args, dist, dev, peaks,
+                                           rank, world)
+    if not args.no_decode:
+        extra["decode"] = run_decode(lr, dev, dist, peaks, args)
     if not args.no_fused and w.gen in workloads.FUSED_FLAGS:
-        fused = run_fused(lr, dev, dist, args, w, ms_per_step)
-    fused_decode = None
+        extra["fused"] = run_fused(lr, dev, dist, args, w, ms_per_step)
     if not args.no_fused and not args.no_decode:
-        fused_decode = run_decode(lr, dev, dist, peaks, args, fused=True)
-    diag = None
+        extra["fused_decode"] = run_decode(lr, dev, dist, peaks, args, fused=True)
     if not args.no_diag and not args.only_gen_delta and w.name != DIAG_WORKLOAD:
-        diag = run_diag(lr, dev, dist, args, peaks)
-    mlstm = gen_delta = None
+        extra["diag"] = run_diag(lr, dev, dist, args, peaks)
     if not args.no_diag and not args.only_gen_delta:
-        mlstm = run_mlstm(lr, dev, dist, args, peaks)
+        extra["mlstm"] = run_mlstm(lr, dev, dist, args, peaks)
     if not args.no_diag:
-        gen_delta = run_gen_delta(lr, dev, dist, args, peaks)
+        extra["gen_delta"] = run_gen_delta(lr, dev, dist, args, peaks)
 
-    out = None
-    if rank == 0:
-        cpu = None
-        if world == 1 and not args.no_cpu_baseline:
-            _, cpu = time_oracle(w, budget_s=args.cpu_budget)
-        out = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": w.dtype, "data": "synthetic (seeded; shapes and distributions of the workload)",
-            "config": {"workload": w.name,
-                       "mode": ["linear", "decay", "delta", "gated_delta", "diag_decay"][w.mode],
-                       "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
-                       "state": "fp32", "global_batch": w.B * world, "seq_len": w.T,
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "inputs 545 MB > 129 MB L2, no flush between steps"},
-            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
-                         "traffic": args.traffic if args.traffic is not None else measured_traffic(w), "peak_source": peaks["source"] + " burst copy",
-                         "algorithmic_bytes_per_launch": nbytes},
-            "tensor": {"achieved_tflops": achieved_tf, "peak_tflops": peaks["bf16_tflops"],
-                       "frac_of_bf16_peak": achieved_tf / peaks["bf16_tflops"],
-                       "flops_per_launch": nflops, "count": "chunk-form MMA flops",
-                       "recurrent_flops_per_launch": recurrent_flops(w),
-                       "achieved_tflops_recurrent_count": recurrent_flops(w) / kernel_s / 1e12},
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "pipelined": "uploads, calls and downloads on three streams, two buffer sets"},
-            # lr_fwd_chunked launches chunk_prep + chunk_scan for bf16, one kernel for fp32
-            "gpu_launches": args.steps * (2 if w.dtype == "bf16" else 1),
-            "clocks": clocks.summary(wall0, wall1),
-            "cpu_baseline": cpu,
-        }
-        if decode is not None:
-            out["decode"] = decode
-        if fused is not None:
-            out["fused"] = fused
-        if fused_decode is not None:
-            out["fused_decode"] = fused_decode
-        if diag is not None:
-            out["diag"] = diag
-        if mlstm is not None:
-            out["mlstm"] = mlstm
-        if gen_delta is not None:
-            out["gen_delta"] = gen_delta
+    if rank != 0:
+        return None
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        _, cpu = time_oracle(w, budget_s=args.cpu_budget)
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": w.name, "mode": mode_name(w),
+                   "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
+                   "state": "fp32", "global_batch": w.B * world, "seq_len": w.T,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": l2_note(w, dev, flush=fits)[0]},
+        "roofline": roof,
+        "tensor": tensor,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": max(3, min(args.steps, 20)),
+                "pipelined": "uploads, calls and downloads on three streams, two buffer sets"},
+        # lr_fwd_chunked launches its per-block pass and its scan for bf16, one kernel for fp32
+        "gpu_launches": args.steps * (2 if w.dtype == "bf16" else 1),
+        "clocks": clocks.summary(wall0, wall1),
+        "sustained": {"ms_per_step": sustained_ms, "steps": sustained_steps,
+                      "note": "the timed steps repeated back to back for at least 1 s after the "
+                              "timed region; clocks are sampled over both"},
+        "cpu_baseline": cpu,
+    }
+    out.update(extra)
     return out
 
 
@@ -662,7 +784,7 @@ def run_reference(args, rank):
     w = workloads.WORKLOADS[args.workload]
     import oracle
     x = workloads.draw(w.gen, 1, w.H, w.T, w.dk, w.dv, w.seed, w.torch_dtype, w.s0_std)
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    cores = host_cores()
     nh = min(w.H, cores)
     T = min(w.T, args.ref_tokens)
     def sl(name, t):
@@ -693,8 +815,8 @@ def run_reference(args, rank):
             "data": "synthetic (seeded; shapes and distributions of the workload)",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
                        "chunk": w.chunk},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nh, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nh, "host_cores": cores,
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -707,6 +829,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=[k for k in workloads.WORKLOADS if k != DECODE_WORKLOAD])
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the RetNet and Mamba-2-style prefill workloads")
     ap.add_argument("--decode-steps", type=int, default=None,
                     help="decode steps to time (default: the workload's 1000)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

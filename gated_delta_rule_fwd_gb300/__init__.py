@@ -36,7 +36,8 @@ SYMBOLS = ("lr_fwd_chunked", "lr_fwd_chunked_workspace_size", "lr_fwd_chunked_no
            "lr_fwd_chunked_mlstm", "lr_fwd_chunked_mlstm_workspace_size", "lr_step_mlstm",
            "lr_fwd_chunked_gen_delta", "lr_fwd_chunked_gen_delta_workspace_size",
            "lr_step_gen_delta",
-           "lr_device_status", "lr_status_string", "lr_abi_version")
+           "lr_device_status", "lr_debug_inject_scan_timeout", "lr_status_string",
+           "lr_abi_version")
 # lr_fuse flags (include/lr.h)
 FUSE_QK_SILU_L2 = 0x1
 FUSE_BETA_SIGMOID = 0x2
@@ -120,6 +121,8 @@ def lib() -> ctypes.CDLL:
         L.lr_abi_version.argtypes = []
         L.lr_device_status.restype = i
         L.lr_device_status.argtypes = []
+        L.lr_debug_inject_scan_timeout.restype = i
+        L.lr_debug_inject_scan_timeout.argtypes = [i]
         _lib = L
     return _lib
 
@@ -132,6 +135,21 @@ def device_status() -> int:
     """lr_device_status(): synchronises the current device and returns (and
     clears) the library's bounded-wait error word as a status code."""
     return int(lib().lr_device_status())
+
+
+def debug_inject_scan_timeout(on: bool) -> None:
+    """lr_debug_inject_scan_timeout: the failure-detection test hook.  While
+    on, the chunked forward's bf16 sequential pass gives up a bounded wait on
+    purpose (short poll limit, stage 1 never loaded) and takes its exit path;
+    ``device_status()`` then reports LR_ERR_TIMEOUT.  Synchronises the device."""
+    st = lib().lr_debug_inject_scan_timeout(1 if on else 0)
+    if st != 0:
+        raise LrError(st, "lr_debug_inject_scan_timeout")
+
+
+def _require_cuda(device):
+    if device.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
 
 
 def _dtype_code(t):
@@ -187,8 +205,7 @@ def lr_fwd_chunked(q, k, v, alpha=None, beta=None, S0=None, *, mode=GATED_DELTA,
     import torch
     mode = MODES.get(mode, mode)
     dev = q.device
-    if dev.type != "cuda":
-        raise ValueError("inputs must be CUDA tensors")
+    _require_cuda(dev)
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     dt = _dtype_code(q)
@@ -238,8 +255,7 @@ def lr_fwd_chunked_noalloc(q, k, v, alpha=None, beta=None, S0=None, *, mode=GATE
     import torch
     mode = MODES.get(mode, mode)
     dev = q.device
-    if dev.type != "cuda":
-        raise ValueError("inputs must be CUDA tensors")
+    _require_cuda(dev)
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     dt = _dtype_code(q)
@@ -256,8 +272,12 @@ def lr_fwd_chunked_noalloc(q, k, v, alpha=None, beta=None, S0=None, *, mode=GATE
         _check(S0, "S0", (B, H, dv, dk), torch.float32, dev)
     if o is None:
         o = torch.empty((B, H, T, dv), dtype=q.dtype, device=dev)
+    else:
+        _check(o, "o", (B, H, T, dv), q.dtype, dev)
     if S_T is None:
         S_T = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+    else:
+        _check(S_T, "S_T", (B, H, dv, dk), torch.float32, dev)
     st = lib().lr_fwd_chunked_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
                                       _ptr(S0), _ptr(o), _ptr(S_T), B, H, T, dk, dv, int(chunk),
                                       dt, int(mode), _stream_handle(stream, dev))
@@ -275,8 +295,7 @@ def lr_step(q, k, v, alpha, beta, S, *, mode=GATED_DELTA, o=None, stream=None):
     import torch
     mode = MODES.get(mode, mode)
     dev = q.device
-    if dev.type != "cuda":
-        raise ValueError("inputs must be CUDA tensors")
+    _require_cuda(dev)
     N, H, dk = q.shape
     dv = v.shape[-1]
     dt = _dtype_code(q)
@@ -335,8 +354,7 @@ def lr_fwd_chunked_fused(q, k, v, alpha=None, beta=None, S0=None, *, mode=GATED_
     import torch
     mode = MODES.get(mode, mode)
     dev = q.device
-    if dev.type != "cuda":
-        raise ValueError("inputs must be CUDA tensors")
+    _require_cuda(dev)
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     dt = _dtype_code(q)
@@ -382,8 +400,7 @@ def lr_step_fused(q, k, v, alpha, beta, S, *, mode=GATED_DELTA, flags=0, alpha_s
     import torch
     mode = MODES.get(mode, mode)
     dev = q.device
-    if dev.type != "cuda":
-        raise ValueError("inputs must be CUDA tensors")
+    _require_cuda(dev)
     N, H, dk = q.shape
     dv = v.shape[-1]
     dt = _dtype_code(q)
@@ -428,8 +445,7 @@ def lr_fwd_chunked_mlstm(q, k, v, fgate, igate, C0=None, n0=None, m0=None, *, ch
     """
     import torch
     dev = q.device
-    if dev.type != "cuda":
-        raise ValueError("inputs must be CUDA tensors")
+    _require_cuda(dev)
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     dt = _dtype_code(q)

@@ -1317,6 +1317,10 @@ cudaError_t launch_mlstm_tc(const void *q, const void *k, const void *v, const f
     }
 }
 
+cudaError_t set_scan_fault_tc(unsigned on) {
+    return cudaMemcpyToSymbol(g_scan_fault, &on, sizeof(on));
+}
+
 int read_and_clear_tc_error() {
     int h = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&h, g_tc_error, sizeof(int)) != cudaSuccess) return -1;

@@ -398,6 +398,11 @@ lr_status lr_device_status(void) {
     return (e || eg) ? LR_ERR_TIMEOUT : LR_OK;
 }
 
+lr_status lr_debug_inject_scan_timeout(int on) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return LR_ERR_CUDA;
+    return set_scan_fault_tc(on ? 1u : 0u) == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+}
+
 lr_status lr_step_fused(const void *q, const void *k, const void *v, const float *alpha,
                         const float *beta, float *S, void *o, int N, int H, int dk, int dv,
                         lr_dtype dt, lr_mode mode, const lr_fuse *fuse, cudaStream_t stream) {

@@ -161,6 +161,8 @@ cudaError_t launch_rmsnorm(void *o, const float *w, float eps, size_t rows, int 
 // chunked_tc.cu and of gen_delta_tc.cu (each has its own): 1 if set, 0 if
 // clear, -1 if the device could not be read.
 int read_and_clear_tc_error();
+// The failure-detection test hook of the chunked forward's scan (0 = off).
+cudaError_t set_scan_fault_tc(unsigned on);
 int read_and_clear_gd_tc_error();
 
 // Set the dynamic shared-memory limit of `fn` once per device.

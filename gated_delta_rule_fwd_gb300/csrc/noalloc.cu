@@ -14,8 +14,9 @@
 // exits.  In host code the array's name only stands in for it (it is not a
 // device address), so its device address is looked up once per device with
 // cudaGetSymbolAddress, with that device current, the first time the entry
-// point runs there.  That first call should therefore come before any stream
-// capture.  All calls share the one array: calls whose kernels may overlap on
+// point runs there, and kept for the life of the process (the device must not
+// be reset while the library is loaded).  That first call should therefore
+// come before any stream capture.  All calls share the one array: calls whose kernels may overlap on
 // the GPU (different streams, or several host threads) race on it and must be
 // serialised by the caller.  Each call rewrites every byte of scratch it
 // reads, so nothing has to be cleared between calls.
@@ -40,7 +41,10 @@ void *static_workspace() {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (!g_workspace_ptr[dev]) {
         void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess) return nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess) {
+            cudaGetLastError();  // consume the error, so later launches do not report it
+            return nullptr;
+        }
         g_workspace_ptr[dev] = ptr;
     }
     return g_workspace_ptr[dev];

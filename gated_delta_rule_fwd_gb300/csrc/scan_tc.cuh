@@ -26,6 +26,11 @@ constexpr int C = 64;      // tokens per block
 constexpr int DVS = 32;    // value channels per scan CTA
 
 __device__ int g_tc_error = 0;  // set to 1 when a bounded wait gives up
+// Failure-detection test hook, set from the host (0 = off): a scan launched
+// while it is set polls each barrier at most kFaultSpinLimit times and its
+// late-group load thread skips the loads of stage 1, so the waits for that
+// stage run out and the kernel takes its exit path.
+__device__ unsigned g_scan_fault = 0;
 
 // Workspace record of stage j of one head (stages 0..nblk), written by the
 // prep CTAs of blocks j and j-1 and read by the scan.
@@ -221,6 +226,9 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
     tc_fence_after();
     const uint32_t tmem = bars->tmem;
     bool ok = true;
+    const bool fault = g_scan_fault != 0;
+    const uint32_t limit = fault ? kFaultSpinLimit : kSpinLimit;
+    auto wait = [limit](uint64_t *bar, uint32_t parity) { return mbar_wait(bar, parity, limit); };
 
     const uint32_t id_kn = idesc_bf16_f32_mn(128, DVS, false, true);
     const uint32_t id_nn = idesc_bf16_f32_mn(128, DVS, true, true);
@@ -240,11 +248,11 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             for (int j = 0; j <= nblk && ok; ++j) {
                 const int p = j & 1;
                 const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
-                ok = mbar_wait(&bars->fullE[p], ph);
+                ok = wait(&bars->fullE[p], ph);
                 // output rows of stage j-2 (same accumulators) read
-                if (ok && j >= 2) ok = mbar_wait(&bars->tfree[p], ph ^ 1);
+                if (ok && j >= 2) ok = wait(&bars->tfree[p], ph ^ 1);
                 // S_{j-1} in state copy p
-                if (ok) ok = mbar_wait(&bars->s[p], ph);
+                if (ok) ok = wait(&bars->s[p], ph);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t d_aw = aw_desc(p), d_sb = sb_desc(p);
@@ -254,8 +262,8 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                              id_kn, ks > 0);
                 mma_commit(&bars->emptyE[p]);
                 if (j >= 1) {
-                    ok = mbar_wait(&bars->fullL[p], ph);
-                    if (ok && DELTA) ok = mbar_wait(&bars->u, (j - 1) & 1);  // U_{j-1}
+                    ok = wait(&bars->fullL[p], ph);
+                    if (ok && DELTA) ok = wait(&bars->u, (j - 1) & 1);  // U_{j-1}
                     if (!ok) break;
                     tc_fence_after();
                     const uint64_t d_zp = zp_desc(p), d_x = DELTA ? d_ub : vr_desc(p);
@@ -268,7 +276,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                 mma_commit(&bars->emptyL[p]);
             }
             mma_commit(&bars->fin[0]);
-            if (!mbar_wait(&bars->fin[0], 0)) ok = false;
+            if (!wait(&bars->fin[0], 0)) ok = false;
         }
     } else if (warp == 1) {
         // ====================================== a and ds products (issuer B)
@@ -276,7 +284,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             for (int j = 0; j <= nblk && ok; ++j) {
                 const int p = j & 1;
                 const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
-                ok = mbar_wait(&bars->fullL[p], ph);
+                ok = wait(&bars->fullL[p], ph);
                 if (!ok) break;
                 tc_fence_after();
                 if (DELTA && j < nblk) {
@@ -288,8 +296,8 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                 }
                 mma_commit(&bars->dB[p]);
                 if (j >= 1) {
-                    if (ok) ok = DELTA ? mbar_wait(&bars->uk[(j - 1) & 1], ((j - 1) >> 1) & 1)  // kd U_{j-1}
-                                       : mbar_wait(&bars->vkr[p], ph);                          // kd' V'
+                    if (ok) ok = DELTA ? wait(&bars->uk[(j - 1) & 1], ((j - 1) >> 1) & 1)  // kd U_{j-1}
+                                       : wait(&bars->vkr[p], ph);                          // kd' V'
                     if (!ok) break;
                     tc_fence_after();
                     const uint64_t d_kr = kr_desc(p), d_y = ubk_desc(DELTA ? (j - 1) & 1 : p);
@@ -302,7 +310,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                 mma_commit(&bars->emptyL[p]);
             }
             mma_commit(&bars->fin[1]);
-            if (!mbar_wait(&bars->fin[1], 0)) ok = false;
+            if (!wait(&bars->fin[1], 0)) ok = false;
         }
     } else if (warp == 2) {
         // ============================================ early-group loads
@@ -310,7 +318,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             int issued = -1;
             for (int j = 0; j <= nblk && ok; ++j) {
                 const int p = j & 1;
-                if (j >= 2) ok = mbar_wait(&bars->emptyE[p], ((j >> 1) - 1) & 1);
+                if (j >= 2) ok = wait(&bars->emptyE[p], ((j >> 1) - 1) & 1);
                 if (!ok) break;
                 const uint8_t *rec = recs + (size_t)j * R::BYTES;
                 uint8_t *aw = sm + L::AW + p * L::AW_BYTES;
@@ -336,7 +344,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             }
             // never leave with copies into shared memory in flight
             for (int j = issued > 0 ? issued - 1 : 0; j <= issued; ++j)
-                if (!mbar_wait(&bars->fullE[j & 1], (j >> 1) & 1)) ok = false;
+                if (!wait(&bars->fullE[j & 1], (j >> 1) & 1)) ok = false;
         }
     } else if (warp == 3) {
         // ============================================= late-group loads
@@ -345,8 +353,10 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             const int p = j & 1;
             const bool prev = j >= 1;
             if (lane == 0) {
-                if (j >= 2) ok = mbar_wait(&bars->emptyL[p], ((j >> 1) - 1) & 1);
-                if (ok) {
+                if (j >= 2) ok = wait(&bars->emptyL[p], ((j >> 1) - 1) & 1);
+                if (ok && fault && j == 1) {
+                    issued = j;  // the test hook: stage 1 is never loaded
+                } else if (ok) {
                     const uint8_t *rec = recs + (size_t)j * R::BYTES;
                     const bool cur = DELTA && j < nblk;
                     uint32_t bytes = 1024u + (DELTA ? 24576u : 0u) + (cur ? 8192u : 0u);
@@ -379,7 +389,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
         // never leave with copies into shared memory in flight
         if (lane == 0)
             for (int j = issued > 0 ? issued - 1 : 0; j <= issued; ++j)
-                if (!mbar_wait(&bars->fullL[j & 1], (j >> 1) & 1)) ok = false;
+                if (!wait(&bars->fullL[j & 1], (j >> 1) & 1)) ok = false;
     } else if (warp < 12 && (warp & 3) < 2) {
         // ============================================ U rows (TMEM lanes 0..63)
         const int r = 32 * (warp & 3) + lane;
@@ -388,7 +398,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
         for (int j = 0; j <= nblk && ok; ++j) {
             const int p = j & 1;
             const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->fullL[p], ph));
+            ok = __all_sync(0xffffffffu, wait(&bars->fullL[p], ph));
             if (!ok) break;
             // with delta only the gates are read from the late group: take them
             // and release it now
@@ -397,8 +407,8 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             const float gn = GEN ? 1.f : DELTA ? -vec_of(p)[kVgCPrev] : 0.f;
             if (DELTA) warp_arrive(&bars->emptyL[p]);
             if (DELTA && j < nblk) {
-                ok = mbar_wait(&bars->dA[p], ph);
-                ok = ok && mbar_wait(&bars->dB[p], ph);
+                ok = wait(&bars->dA[p], ph);
+                ok = ok && wait(&bars->dB[p], ph);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -466,11 +476,11 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
         for (int j = 0; j <= nblk && ok; ++j) {
             const int p = j & 1;
             const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->fullL[p], ph));
+            ok = __all_sync(0xffffffffu, wait(&bars->fullL[p], ph));
             if (!ok) break;
             const float gr = GEN ? 1.f : vec_of(p)[kVgPrev + r];  // the only late-group value read here
             warp_arrive(&bars->emptyL[p]);
-            if (j >= 1) ok = __all_sync(0xffffffffu, mbar_wait(&bars->dA[p], ph));
+            if (j >= 1) ok = __all_sync(0xffffffffu, wait(&bars->dA[p], ph));
             if (!ok) break;
             if (j >= 1) {
                 tc_fence_after();
@@ -524,14 +534,14 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
         for (int j = 0; j <= nblk && ok; ++j) {
             const int p = j & 1;
             const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->fullL[p], ph));
+            ok = __all_sync(0xffffffffu, wait(&bars->fullL[p], ph));
             if (!ok) break;
             // the only late-group value read here: g_C', per key channel with the diagonal gate
             const float gC = GEN    ? vec_of(p)[kVgCGen + (kc & 127)]
                              : DIAG ? vec_of(p)[kVgCDiag + (kc & 127)]
                                     : vec_of(p)[kVgCPrev];
             if (DELTA) warp_arrive(&bars->emptyL[p]);
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->dsf[p], ph));
+            ok = __all_sync(0xffffffffu, wait(&bars->dsf[p], ph));
             if (!ok) break;
             if (j >= 1) {
                 tc_fence_after();
@@ -545,7 +555,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                 if (j < nblk) {  // S_j -> copy (j+1)&1, read by b_{j+1}
                     if (!DELTA)
                         ok = __all_sync(0xffffffffu,
-                                        mbar_wait(&bars->emptyE[(j - 1) & 1], ((j - 1) >> 1) & 1));
+                                        wait(&bars->emptyE[(j - 1) & 1], ((j - 1) >> 1) & 1));
                     if (!ok) break;
                     write_sb((j + 1) & 1);
                     fence_async_smem();

@@ -11,6 +11,8 @@ namespace lr {
 namespace tc {
 
 constexpr uint32_t kSpinLimit = 1u << 26;
+// Poll limit of a kernel run under the failure-detection test hook.
+constexpr uint32_t kFaultSpinLimit = 1u << 12;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -28,10 +30,11 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 // Wait until the phase with the given parity has completed.  Returns false
-// if the bounded spin ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// if the bounded spin ran out (after `limit` polls).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          uint32_t limit = kSpinLimit) {
     const uint32_t addr = smem_u32(bar);
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    for (uint32_t i = 0; i < limit; ++i) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"

@@ -193,6 +193,21 @@ lr_status lr_step(const void *q, const void *k, const void *v,
 lr_status lr_device_status(void);
 
 /*
+ * Failure-detection test hook (no counterpart on the pages).  While it is on
+ * (on != 0), every launch of the chunked forward's bf16 sequential pass on
+ * the current device polls each of its barriers at most a few thousand times
+ * and its late-group load thread skips the tile loads of stage 1, so every
+ * role's wait for that stage gives up: the kernel stops, waits for its own
+ * copies and tensor-core products in flight, frees its tensor memory, sets
+ * the error word and returns (lr_device_status then reports
+ * LR_ERR_TIMEOUT).  Outputs of such a call are undefined.  Nothing faults and
+ * nothing waits without a limit.  Synchronises the device; call with 0 to
+ * restore normal operation.  Returns LR_OK, or LR_ERR_CUDA if the hook could
+ * not be set.
+ */
+lr_status lr_debug_inject_scan_timeout(int on);
+
+/*
  * Chunked forward without any allocation by the caller.  No counterpart on
  * the pages: this is a deployment variant of lr_fwd_chunked.
  *
@@ -205,12 +220,16 @@ lr_status lr_device_status(void);
  * which every GPU that loads the library holds until the process exits.
  *
  *   - Returns LR_ERR_TOO_LARGE, launching nothing, when
- *     lr_fwd_chunked_workspace_size(...) exceeds LR_STATIC_WORKSPACE_BYTES
- *     (at dk = 128, 41 KB per (batch, head) for every 64-token block plus
- *     one, so B * H * (ceil(T / 64) + 1) <= 1598).
+ *     lr_fwd_chunked_workspace_size(...) for the same arguments exceeds
+ *     LR_STATIC_WORKSPACE_BYTES; that function is the rule for every mode.
+ *     (For the modes with a scalar gate or none at dk = 128 the scratch is
+ *     41 KB per (batch, head) for every 64-token block plus one, so
+ *     B * H * (ceil(T / 64) + 1) <= 1598; LR_MODE_DIAG_DECAY also keeps
+ *     its transformed q and k there, 2 * B * H * T * dk * 2 bytes more.)
  *   - The first call on a device looks up the array's device address (with
- *     cudaGetSymbolAddress, that device current); make that first call before
- *     any stream capture.
+ *     cudaGetSymbolAddress, that device current) and keeps it for the rest
+ *     of the process: make that first call before any stream capture, and do
+ *     not reset the device (cudaDeviceReset) while the library is loaded.
  *   - Every call uses the same array: calls that may run at the same time on
  *     the GPU (other streams, other host threads) race and must be ordered by
  *     the caller.  No clearing is needed between calls.

@@ -189,6 +189,40 @@ def test_fused_gdn_prefill_full_size(dev):
     assert eo <= 2e-2 and es <= 2e-2
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("case", ["strong_decay", "full_dose", "zero_dose", "alpha_one"])
+def test_fused_gates_at_domain_ends(dev, dtype, case):
+    """The maps driven to the ends of the gates' ranges (page "Scrivere meglio
+    nella memoria": sigmoid write strength, sigmoid or softplus forget gate):
+    sigmoid(-3 + N(0,1)) forgets a 64-token block far below e^-80; beta
+    pre-activations of +40 and -40 give a full dose (1.0 in fp32) and a dose of
+    about 4e-18; a softplus gate of -100 gives alpha = 1 to fp32 precision."""
+    flags = ALL
+    x = inputs("gdn", 2, 3, 200, 128, 128, seed=4600, dtype=dtype, s0_std=0.3, flags=flags)
+    if case == "strong_decay":
+        x["alpha"] = (x["alpha"] - 6.0).contiguous()          # N(-3, 1) before the sigmoid
+        # without the output norm: once the state is forgotten within a few
+        # tokens some read-out rows are 2000x smaller than others, and the
+        # per-row norm lifts their rounding to the scale of the largest row
+        # (the bf16 rounding of the normalised q and k alone gives 3.4e-2
+        # after the norm and 1.7e-3 before it, in the fp64 oracle)
+        flags = ALL & ~lr.FUSE_O_RMSNORM
+    elif case == "full_dose":
+        x["beta"] = torch.full_like(x["beta"], 40.0)
+    elif case == "zero_dose":
+        x["beta"] = torch.full_like(x["beta"], -40.0)
+        flags = ALL & ~lr.FUSE_O_RMSNORM
+    else:
+        flags = (ALL & ~lr.FUSE_ALPHA_SIGMOID) | lr.FUSE_ALPHA_SOFTPLUS
+        x["alpha"] = torch.full_like(x["alpha"], -100.0)
+        x["alpha_scale"] = torch.ones(3)
+    o, st = run_fused(x, lr.GATED_DELTA, flags, dev)
+    o_ref, s_ref = ref_fused(x, lr.GATED_DELTA, flags)
+    eo, es = rel_err(o, o_ref), rel_err(st, s_ref)
+    print(f"{case}: rel err o={eo:.3e} S_T={es:.3e}")
+    assert eo <= TOL[dtype] and es <= TOL[dtype]
+
+
 # ------------------------------------------------------------------ decode
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])

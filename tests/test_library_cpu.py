@@ -40,7 +40,7 @@ def test_header_declares_expected_entry_points():
                                           "lr_fwd_chunked_gen_delta",
                                           "lr_fwd_chunked_gen_delta_workspace_size",
                                           "lr_step_gen_delta", "lr_status_string",
-                                          "lr_abi_version"}
+                                          "lr_debug_inject_scan_timeout", "lr_abi_version"}
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -235,3 +235,42 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(lr, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="not built"):
         lr.lib()
+
+
+class _NoLaunch:
+    """Stands in for the loaded library: any attribute access (a call into the
+    C ABI) fails the test."""
+
+    def __getattr__(self, name):
+        raise AssertionError(f"the binding reached the library ({name}) with invalid arguments")
+
+
+@pytest.mark.parametrize("which", ["o", "S_T"])
+@pytest.mark.parametrize("bad", ["shape", "dtype", "strided"])
+def test_noalloc_binding_checks_outputs_before_any_call(monkeypatch, which, bad):
+    """lr_fwd_chunked_noalloc's binding checks a caller-given o or S_T the way
+    lr_fwd_chunked's does: a wrong shape, dtype or layout raises before the
+    library is reached (the C ABI cannot see a buffer's size, so a short
+    buffer would be written past its end)."""
+    import torch
+    import gated_delta_rule_fwd_gb300 as lr
+    monkeypatch.setattr(lr, "_require_cuda", lambda dev: None)   # CPU tensors stand in
+    monkeypatch.setattr(lr, "lib", lambda: _NoLaunch())
+    B, H, T, dk, dv = 1, 2, 10, 32, 32
+    q = torch.zeros(B, H, T, dk, dtype=torch.bfloat16)
+    v = torch.zeros(B, H, T, dv, dtype=torch.bfloat16)
+    a = torch.ones(B, H, T)
+    o = torch.zeros(B, H, T, dv, dtype=torch.bfloat16)
+    st = torch.zeros(B, H, dv, dk)
+    good = {"o": o, "S_T": st}
+    t = good[which]
+    if bad == "shape":
+        t = t[..., :-1].contiguous()
+    elif bad == "dtype":
+        t = t.to(torch.float16)
+    else:
+        t = t.transpose(-1, -2).contiguous().transpose(-1, -2)
+    kw = dict(good)
+    kw[which] = t
+    with pytest.raises((ValueError, TypeError)):
+        lr.lr_fwd_chunked_noalloc(q, q.clone(), v, a, a.clone(), None, **kw)

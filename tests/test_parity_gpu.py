@@ -254,3 +254,105 @@ def test_repeated_calls_bit_identical(dev, mode):
         bad += int(not (torch.equal(o, o0) and torch.equal(st, s0)))
     torch.cuda.synchronize()
     assert bad == 0, f"{bad} of 100 calls differ from the first"
+
+
+# ------------------------------------------------------- gates at the domain's ends
+
+def _strong(B, H, T, dk, dv, seed, dtype):
+    """gdn inputs with alpha = sigmoid(N(-3,1)): every 64-token block decays far
+    below e^-80, so the per-block pass takes the decay mask as direct
+    differences e^{G_r - G_i} instead of the factorised g_r / g_i."""
+    x = workloads.draw("gdn_strong", B, H, T, dk, dv, seed=seed, dtype=dtype, s0_std=0.1)
+    G = np.log(x["alpha"].double().numpy())
+    nblk = (T + 63) // 64
+    per_block = [G[..., 64 * j:64 * (j + 1)].sum(-1).max() for j in range(nblk)]
+    assert max(per_block[:-1] or per_block) < -80.0   # every full block is in that range
+    return x
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("mode", [lr.DECAY, lr.GATED_DELTA], ids=["decay", "gated_delta"])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 128)])
+def test_chunked_strong_decay(dev, dtype, mode, dk, dv):
+    """Page "Scrivere meglio nella memoria", section "Dimenticare: i gate": the
+    state forgets by the product of the gates; with gates near 0.05 a block's
+    product leaves fp32's range and only the exponent differences stay finite."""
+    x = _strong(2, 3, 200, dk, dv, seed=4100 + dk + dv + mode, dtype=dtype)
+    o, st = run_chunked(x, mode, dev)
+    o_ref, s_ref = ref_chunked(x, mode)
+    assert rel_err(o, o_ref) <= TOL[dtype] and rel_err(st, s_ref) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("mode", [lr.DECAY, lr.GATED_DELTA], ids=["decay", "gated_delta"])
+def test_chunked_mixed_decay_heads(dev, dtype, mode):
+    """One call, two regimes: head 0 forgets fast (alpha below 0.2), the other
+    heads barely forget (alpha within 1e-3 of 1), so per-block pass CTAs of the
+    same launch take both forms of the decay mask."""
+    x = workloads.draw("gdn", 2, 4, 333, 128, 128, seed=4200 + mode, dtype=dtype, s0_std=0.1)
+    g = torch.Generator().manual_seed(4201)
+    a = 1.0 - 1e-3 * torch.rand(x["alpha"].shape, generator=g)
+    a[:, 0] = 0.19 * torch.sigmoid(torch.randn(a[:, 0].shape, generator=g))
+    assert float(a[:, 0].max()) < 0.2
+    x["alpha"] = a.float().contiguous()
+    o, st = run_chunked(x, mode, dev)
+    o_ref, s_ref = ref_chunked(x, mode)
+    assert rel_err(o, o_ref) <= TOL[dtype] and rel_err(st, s_ref) <= TOL[dtype]
+    # per head, too: the fast-forgetting head is small next to the others
+    for h in range(4):
+        assert rel_err(o[:, h], o_ref[:, h]) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("mode,plain", [(lr.DECAY, lr.LINEAR), (lr.GATED_DELTA, lr.DELTA)],
+                         ids=["decay=linear", "gated_delta=delta"])
+def test_chunked_alpha_one(dev, dtype, mode, plain):
+    """alpha == 1 exactly: the gated rows reduce to their ungated rows (the
+    summary table of the first page), on the gated instantiation's kernels."""
+    x = workloads.draw("gdn", 2, 3, 200, 128, 128, seed=4300 + mode, dtype=dtype, s0_std=0.1)
+    x["alpha"] = torch.ones_like(x["alpha"])
+    o, st = run_chunked(x, mode, dev)
+    o_ref, s_ref = ref_chunked(x, plain)
+    assert rel_err(o, o_ref) <= TOL[dtype] and rel_err(st, s_ref) <= TOL[dtype]
+    o_p, st_p = run_chunked(x, plain, dev)
+    assert rel_err(o, o_p.float().cpu().numpy()) <= TOL[dtype]
+    assert rel_err(st, st_p.cpu().numpy()) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("mode", [lr.DELTA, lr.GATED_DELTA], ids=["delta", "gated_delta"])
+def test_chunked_full_dose_overwrites(dev, dtype, mode):
+    """Page "Scrivere meglio nella memoria", section "Correggere: la delta
+    rule": with beta = 1 and a unit key the write replaces what the memory
+    held for that key, so the final state read with the last key returns the
+    last value, S_T k_T = v_T (up to the rounding of k to the input dtype)."""
+    x = workloads.draw("gdn", 2, 3, 130, 128, 128, seed=4400 + mode, dtype=dtype, s0_std=0.1)
+    x["beta"] = torch.ones_like(x["beta"])
+    o, st = run_chunked(x, mode, dev)
+    o_ref, s_ref = ref_chunked(x, mode)
+    assert rel_err(o, o_ref) <= TOL[dtype] and rel_err(st, s_ref) <= TOL[dtype]
+    kT = x["k"][:, :, -1].double()                      # [B, H, dk]
+    vT = x["v"][:, :, -1].double()                      # [B, H, dv]
+    read = torch.einsum("bhvk,bhk->bhv", st.cpu().double(), kT)
+    # |k_T|^2 = 1 + e after rounding; the read then misses v_T by about e (|v| + |S k|)
+    e = float((kT.square().sum(-1) - 1.0).abs().max())
+    bound = TOL[dtype] + 4 * e
+    assert float((read - vT).abs().max()) <= bound * float(vT.abs().max())
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_chunked_zero_dose_is_pure_decay(dev, dtype):
+    """Page "Scrivere meglio nella memoria", section "Unire oblio e correzione:
+    Gated DeltaNet": with beta = 0 the gated delta rule writes nothing, so
+    S_T = (prod alpha) S0 and o_t = (prod_{s<=t} alpha_s) S0 q_t."""
+    x = workloads.draw("gdn", 2, 3, 200, 128, 128, seed=4500, dtype=dtype, s0_std=0.1)
+    x["beta"] = torch.zeros_like(x["beta"])
+    o, st = run_chunked(x, lr.GATED_DELTA, dev)
+    G = torch.cumsum(torch.log(x["alpha"].double()), dim=-1)     # [B, H, T]
+    S0 = x["S0"].double()
+    s_ref = torch.exp(G[..., -1])[..., None, None] * S0
+    o_ref = torch.exp(G)[..., None] * torch.einsum("bhvk,bhtk->bhtv", S0, x["q"].double())
+    assert rel_err(st, s_ref.numpy()) <= TOL[dtype]
+    assert rel_err(o, o_ref.numpy()) <= TOL[dtype]
+    o_or, s_or = ref_chunked(x, lr.GATED_DELTA)
+    assert rel_err(o, o_or) <= TOL[dtype] and rel_err(st, s_or) <= TOL[dtype]

@@ -36,21 +36,48 @@ def dev():
 
 def test_noalloc_matches_workspace_entry_point_twice(dev):
     """Two calls in a row (different modes, sizes and inputs, the second
-    reusing the scratch the first left behind) agree with lr_fwd_chunked
-    given a workspace."""
-    cases = [(lr.GATED_DELTA, "gdn", 2, 4, 1000, 0.1, 11), (lr.DECAY, "mamba2", 2, 3, 333, 0.0, 12)]
+    reusing the scratch the first left behind) give the same bits as
+    lr_fwd_chunked with a workspace: the same kernels run on the same inputs,
+    and the kernels are deterministic.  The diagonal gate also keeps its
+    transformed q and k in the scratch, after the records."""
+    cases = [(lr.GATED_DELTA, "gdn", 2, 4, 1000, 0.1, 11), (lr.DECAY, "mamba2", 2, 3, 333, 0.0, 12),
+             (lr.DIAG_DECAY, "gla", 1, 3, 700, 0.1, 13)]
     for mode, gen, B, H, T, s0, seed in cases:
         x = workloads.draw(gen, B, H, T, 128, 128, seed=seed, dtype=torch.bfloat16, s0_std=s0)
         d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
-        ws = torch.empty(lr.workspace_size(B, H, T, 128, 128, torch.bfloat16, mode),
-                         dtype=torch.uint8, device=dev)
+        need = lr.workspace_size(B, H, T, 128, 128, torch.bfloat16, mode)
+        assert need <= lr.STATIC_WORKSPACE_BYTES
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
         o_ref, s_ref = lr.lr_fwd_chunked(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["S0"],
                                          mode=mode, workspace=ws)
         o_na, s_na = lr.lr_fwd_chunked_noalloc(d["q"], d["k"], d["v"], d["alpha"], d["beta"],
                                                d["S0"], mode=mode)
         torch.cuda.synchronize()
-        assert _rel(o_na, o_ref) <= TOL and _rel(s_na, s_ref) <= TOL
+        assert torch.equal(o_na, o_ref) and torch.equal(s_na, s_ref)
+        assert _rel(o_na, o_ref) <= TOL   # (implied by the above; the parity tests' bar)
     assert lr.device_status() == 0
+
+
+def test_noalloc_allocates_no_device_memory(dev):
+    """With o and S_T given, a call takes no device memory: neither the
+    caching allocator's count nor the device's free memory changes."""
+    B, H, T = 2, 4, 1000
+    x = workloads.draw("gdn", B, H, T, 128, 128, seed=14, dtype=torch.bfloat16, s0_std=0.1)
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o = torch.empty((B, H, T, 128), dtype=torch.bfloat16, device=dev)
+    st = torch.empty((B, H, 128, 128), dtype=torch.float32, device=dev)
+
+    def call():
+        lr.lr_fwd_chunked_noalloc(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["S0"],
+                                  mode=lr.GATED_DELTA, o=o, S_T=st)
+    call()                      # first call: the scratch address is looked up
+    torch.cuda.synchronize()
+    used0 = torch.cuda.memory_allocated(dev)
+    free0 = torch.cuda.mem_get_info(dev)[0]
+    call()
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated(dev) == used0
+    assert torch.cuda.mem_get_info(dev)[0] == free0
 
 
 def test_noalloc_rejects_problems_beyond_static_scratch(dev):

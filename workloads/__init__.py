@@ -12,6 +12,10 @@ there -- and beta comes from a sigmoid):
 
 * ``gdn`` inputs: q, k = L2norm(SiLU(N(0,1))) per token; v ~ N(0,1);
   beta = sigmoid(N(0,1)); alpha = sigmoid(N(3,1)); S0 = 0 or N(0, 0.1^2).
+* ``gdn_strong``: as ``gdn`` with alpha = sigmoid(N(-3,1)) (about 0.05 per
+  token): a 64-token block decays near e^-190, far beyond fp32's range for
+  one reference point per block, so the kernels' direct-difference form of
+  the decay mask is the one that runs.
 * ``retnet``: q, k, v ~ N(0,1)/sqrt(dk); alpha = gamma_h = 1 - 2^(-5-h) for
   head h = 0..H-1, the same at every token.
 * ``mamba2``: q, k ~ N(0,1)/sqrt(dk); v ~ N(0,1);
@@ -105,12 +109,13 @@ def draw(gen: str, B, H, T, dk, dv, seed, dtype=torch.float32, s0_std=0.0, devic
     g = torch.Generator("cpu")
     g.manual_seed(int(seed))
     shp_k, shp_v, shp_t = (B, H, T, dk), (B, H, T, dv), (B, H, T)
-    if gen == "gdn":
+    if gen in ("gdn", "gdn_strong"):
         q = _silu_l2(torch.randn(shp_k, generator=g))
         k = _silu_l2(torch.randn(shp_k, generator=g))
         v = torch.randn(shp_v, generator=g)
         beta = torch.sigmoid(torch.randn(shp_t, generator=g))
-        alpha = torch.sigmoid(3.0 + torch.randn(shp_t, generator=g))
+        mu = 3.0 if gen == "gdn" else -3.0
+        alpha = torch.sigmoid(mu + torch.randn(shp_t, generator=g))
     elif gen == "retnet":
         s = 1.0 / math.sqrt(dk)
         q = torch.randn(shp_k, generator=g) * s
