@@ -135,8 +135,8 @@ __device__ __forceinline__ void unpack(uint2 w, float (&x)[4]) {
     x[3] = __uint_as_float(w.y & 0xffff0000u);
 }
 __device__ __forceinline__ uint32_t bf2(float a, float b) {
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
-           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // a low, b high
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
 __device__ __forceinline__ unsigned short pack(const float (&x)[1]) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x[0]));

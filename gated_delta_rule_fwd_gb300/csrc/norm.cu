@@ -43,8 +43,8 @@ template <> struct Vec16<__nv_bfloat16> {
         uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(x[2 * i]));
-            const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(x[2 * i + 1]));
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+            const uint32_t lo = __bfloat16_as_ushort(h2.x), hi = __bfloat16_as_ushort(h2.y);
             w[i] = lo | (hi << 16);
         }
         *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);

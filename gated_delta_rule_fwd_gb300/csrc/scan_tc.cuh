@@ -47,10 +47,11 @@ constexpr int kVgPrev = 0, kVkdPrev = 64, kVkd = 128, kVgCPrev = 192;
 constexpr int kVgCDiag = 128;  // diagonal gate: g_C' per key channel (128 floats)
 constexpr int kVgCGen = 0;     // generalised delta rule: g_C' per key channel (128 floats)
 
+// a in the low half, b in the high half, both rounded to nearest even by one
+// paired conversion (two single conversions run at a fraction of its rate)
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
-    return lo | (hi << 16);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
 __device__ __forceinline__ uint4 pack8(const float *x) {
     uint4 r;

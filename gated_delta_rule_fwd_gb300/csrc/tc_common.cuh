@@ -10,7 +10,10 @@
 namespace lr {
 namespace tc {
 
-constexpr uint32_t kSpinLimit = 1u << 26;
+#ifndef LR_SPIN_LIMIT_LOG2
+#define LR_SPIN_LIMIT_LOG2 26  // polls of a bounded wait: 2^26 by default
+#endif
+constexpr uint32_t kSpinLimit = 1u << LR_SPIN_LIMIT_LOG2;
 // Poll limit of a kernel run under the failure-detection test hook.
 constexpr uint32_t kFaultSpinLimit = 1u << 12;
 
