@@ -812,90 +812,153 @@ chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws
     const float plo = c < DK ? prd[c] * prd[128 + c] : 1.f;
     const float psb1 = c < DK ? prd[128 + c] : 1.f;
 
-    // ---- keys: K * e^{G_e - G} (sub-block suffix products) and K * e^{G_last - G};
-    // the first half starts from the product of the second half's gates, so
-    // its gC ends as the product over the whole block
+    // One reference point for the whole block (token 31) when every channel's
+    // decay over the block stays above e^-60: each score factor
+    // e^{G_r - G_i} = e^{G_r - G_31} e^{G_31 - G_i} then splits into a query
+    // factor and a key factor within [e^-60, e^60], and one product (N = 64
+    // keys) gives all of P.  Otherwise the 16-token key sub-blocks below.
+    const bool single =
+        __syncthreads_and((!ok || c >= DK || hf == 1 ||
+                           prd[c] * prd[128 + c] * prd[256 + c] * prd[384 + c] > 8.75e-27f)
+                              ? 1 : 0) != 0;
     float gC = 1.f;
-    if (ok && c < DK) {
-        if (hf == 0) gC = prd[2 * 128 + c] * prd[3 * 128 + c];
-        float s_sub = 1.f;
-#pragma unroll
-        for (int rl = CH - 1; rl >= 0; --rl) {
-            if ((rl & 15) == 15) s_sub = 1.f;
-            float kv = ld(KT, rl);
-            if (QKN) kv *= inkh[rl];
-            st(KH, rl, kv * s_sub);
-            st(KT, rl, kv * gC);
-            s_sub *= a[rl];
-            gC *= a[rl];
-        }
-    }
-    // ---- scores, one key sub-block per product (unrolled: a[] stays in
-    // registers).  Rows of sub-block J get e^{G_r - G_e} (inside J: the
-    // inverse of the gates r < j <= e; after J: the gates e < j <= r); each
-    // half writes its own rows.  q * e^G replaces the raw q rows of a half
-    // once that half's last sub-block has been formed: the first half at
-    // J = 2, the second at J = 3.
-#pragma unroll
-    for (int J = 0; J < NS; ++J) {
-        if (!ok) break;
-        if (c < DK) {
-            if (hf == (J >> 1)) {  // rows inside J
-                float s = 1.f;
-#pragma unroll
-                for (int rl = 15; rl >= 0; --rl) {
-                    const int il = 16 * (J & 1) + rl;
-                    st(QH, il, qrow(il) * fminf(__frcp_rn(s), 5.5e34f));
-                    s *= a[il];
-                }
-            }
-            if (hf == 0 && J == 0) {  // rows 16..31 after J = 0
-                float p = 1.f;
-#pragma unroll
-                for (int il = 16; il < CH; ++il) {
-                    p *= a[il];
-                    st(QH, il, qrow(il) * p);
-                }
-            }
-            if (hf == 1 && J < 2) {  // rows 32..63 after J = 0 or 1
-                float p = J == 0 ? psb1 : 1.f;
+    if (single) {
+        if (ok && c < DK) {
+            if (hf == 1) {
+                // tokens 32 + il: query factor = the gates 32..32+il, key factor its inverse
+                float pfx = 1.f;
 #pragma unroll
                 for (int il = 0; il < CH; ++il) {
-                    p *= a[il];
-                    st(QH, il, qrow(il) * p);
+                    pfx *= a[il];
+                    float kv = ld(KT, il);
+                    if (QKN) kv *= inkh[il];
+                    st(KH, il, kv * fminf(__frcp_rn(pfx), 5.5e34f));
+                    st(QH, il, qrow(il) * pfx);
                 }
             }
-            if (hf == 1 && J == 2) {  // rows 48..63 after J = 2
-                float p = 1.f;
+            // K * e^{G_last - G} (descending), and for the first half the key
+            // factor = the gates il+1..31, the query factor its inverse
+            float sfx = 1.f;
+            gC = hf == 0 ? prd[2 * 128 + c] * prd[3 * 128 + c] : 1.f;
 #pragma unroll
-                for (int il = 16; il < CH; ++il) {
-                    p *= a[il];
-                    st(QH, il, qrow(il) * p);
+            for (int rl = CH - 1; rl >= 0; --rl) {
+                float kv = ld(KT, rl);
+                if (QKN) kv *= inkh[rl];
+                if (hf == 0) {
+                    st(KH, rl, kv * sfx);
+                    st(QH, rl, qrow(rl) * fminf(__frcp_rn(sfx), 5.5e34f));
                 }
+                st(KT, rl, kv * gC);
+                sfx *= a[rl];
+                gC *= a[rl];
             }
-            if (J >= 2 && hf == J - 2) {  // q * e^G in place over this half's raw rows
-                float g = hf == 0 ? 1.f : plo;
+            // q * e^G in place over the raw rows (after the query factors read them)
+            float g = hf == 0 ? 1.f : plo;
 #pragma unroll
-                for (int il = 0; il < CH; ++il) {
-                    g *= a[il];
-                    st(QT, il, qrow(il) * g);
-                }
+            for (int il = 0; il < CH; ++il) {
+                g *= a[il];
+                st(QT, il, qrow(il) * g);
             }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (tid == 0) {
-            const uint32_t id = idesc_bf16_f32(64, 16);
+        if (tid == 0 && ok) {
+            const uint32_t id = idesc_bf16_f32(64, 64);
 #pragma unroll
             for (int ks = 0; ks < DK / 16; ++ks)
-                mma_bf16(tmem + 16 * J, tile_desc(smem_u32(QH), 64, 0, ks),
-                         tile_desc(smem_u32(KH), 64, 16 * J, ks), id, ks > 0);
+                mma_bf16(tmem, tile_desc(smem_u32(QH), 64, 0, ks), tile_desc(smem_u32(KH), 64, 0, ks),
+                         id, ks > 0);
             mma_commit(&bar[1]);
         }
-        ok = cta_wait(&bar[1], J & 1, true);  // QH may be rewritten after the product
+        ok = cta_wait(&bar[1], 0, ok);
         tc_fence_after();
+    } else {
+        // ---- keys: K * e^{G_e - G} (sub-block suffix products) and K * e^{G_last - G};
+        // the first half starts from the product of the second half's gates, so
+        // its gC ends as the product over the whole block
+        if (ok && c < DK) {
+            if (hf == 0) gC = prd[2 * 128 + c] * prd[3 * 128 + c];
+            float s_sub = 1.f;
+    #pragma unroll
+            for (int rl = CH - 1; rl >= 0; --rl) {
+                if ((rl & 15) == 15) s_sub = 1.f;
+                float kv = ld(KT, rl);
+                if (QKN) kv *= inkh[rl];
+                st(KH, rl, kv * s_sub);
+                st(KT, rl, kv * gC);
+                s_sub *= a[rl];
+                gC *= a[rl];
+            }
+        }
+        // ---- scores, one key sub-block per product (unrolled: a[] stays in
+        // registers).  Rows of sub-block J get e^{G_r - G_e} (inside J: the
+        // inverse of the gates r < j <= e; after J: the gates e < j <= r); each
+        // half writes its own rows.  q * e^G replaces the raw q rows of a half
+        // once that half's last sub-block has been formed: the first half at
+        // J = 2, the second at J = 3.
+    #pragma unroll
+        for (int J = 0; J < NS; ++J) {
+            if (!ok) break;
+            if (c < DK) {
+                if (hf == (J >> 1)) {  // rows inside J
+                    float s = 1.f;
+    #pragma unroll
+                    for (int rl = 15; rl >= 0; --rl) {
+                        const int il = 16 * (J & 1) + rl;
+                        st(QH, il, qrow(il) * fminf(__frcp_rn(s), 5.5e34f));
+                        s *= a[il];
+                    }
+                }
+                if (hf == 0 && J == 0) {  // rows 16..31 after J = 0
+                    float p = 1.f;
+    #pragma unroll
+                    for (int il = 16; il < CH; ++il) {
+                        p *= a[il];
+                        st(QH, il, qrow(il) * p);
+                    }
+                }
+                if (hf == 1 && J < 2) {  // rows 32..63 after J = 0 or 1
+                    float p = J == 0 ? psb1 : 1.f;
+    #pragma unroll
+                    for (int il = 0; il < CH; ++il) {
+                        p *= a[il];
+                        st(QH, il, qrow(il) * p);
+                    }
+                }
+                if (hf == 1 && J == 2) {  // rows 48..63 after J = 2
+                    float p = 1.f;
+    #pragma unroll
+                    for (int il = 16; il < CH; ++il) {
+                        p *= a[il];
+                        st(QH, il, qrow(il) * p);
+                    }
+                }
+                if (J >= 2 && hf == J - 2) {  // q * e^G in place over this half's raw rows
+                    float g = hf == 0 ? 1.f : plo;
+    #pragma unroll
+                    for (int il = 0; il < CH; ++il) {
+                        g *= a[il];
+                        st(QT, il, qrow(il) * g);
+                    }
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (tid == 0) {
+                const uint32_t id = idesc_bf16_f32(64, 16);
+    #pragma unroll
+                for (int ks = 0; ks < DK / 16; ++ks)
+                    mma_bf16(tmem + 16 * J, tile_desc(smem_u32(QH), 64, 0, ks),
+                             tile_desc(smem_u32(KH), 64, 16 * J, ks), id, ks > 0);
+                mma_commit(&bar[1]);
+            }
+            ok = cta_wait(&bar[1], J & 1, true);  // QH may be rewritten after the product
+            tc_fence_after();
+        }
     }
     // ---- the transformed q and k rows -> workspace (rows past T are not written)
     if (tid == 0 && ok) {
