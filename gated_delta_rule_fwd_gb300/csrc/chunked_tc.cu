@@ -1190,6 +1190,28 @@ chunk_prep_mlstm_kernel(const float *__restrict__ fgate, const float *__restrict
 // ================================================================== launch
 
 
+// Value channels per scan CTA.  Each (batch, head) takes dv / NV scan CTAs of
+// one SM each.  The scan's stage time is set by the issue and hand-off latency
+// of its products, which N = 64 costs barely more than N = 32, so 64-channel
+// CTAs pay off when 32-channel ones would need more waves over the SMs than
+// 64-channel ones (many heads); otherwise 32 keeps more SMs busy and each
+// SM's epilogues short.
+int scan_width(int B, int H, int dv) {
+    if (dv < 64) return 32;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return 32;
+    const long long n32 = (long long)B * H * (dv / 32), n64 = n32 / 2;
+    return (n64 + sms - 1) / sms < (n32 + sms - 1) / sms ? 64 : 32;
+}
+
+// Attribute slot of a 64-channel scan instantiation (the 32-channel ones use
+// the slots their launchers pass): 160 + 4 log2(DK / 32) + mode for the lr
+// modes, 172 + log2(DK / 32) for the diagonal gate, 175 + log2(DK / 32) for
+// mLSTM.
+constexpr int wide_slot_base(int dk) { return dk == 32 ? 0 : dk == 64 ? 1 : 2; }
+
 // One record per stage: a head of nblk blocks has nblk + 1 stages.  With
 // SiLU + L2 of q and k, the normalised q and k ([B, H, T, dk] bf16 each)
 // follow the records.
@@ -1208,11 +1230,14 @@ cudaError_t launch_diag(const void *q, const void *k, const void *v, const float
     const int nblk = (T + C - 1) / C;
     const bool qk = (fz.flags & LR_FUSE_QK_SILU_L2) != 0;
     auto prep = qk ? chunk_prep_diag_kernel<DK, true> : chunk_prep_diag_kernel<DK, false>;
-    auto scan = chunk_scan_kernel<DK, true, false, true>;
+    const int nv = scan_width(B, H, dv);
+    auto scan = nv == 64 ? chunk_scan_kernel<DK, true, false, true, false, 64>
+                         : chunk_scan_kernel<DK, true, false, true>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(prep),
                                      DiagPrepLayout<DK>::ALLOC, slot + (qk ? 1 : 0));
     if (e != cudaSuccess) return e;
-    e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC, slot + 2);
+    e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC,
+                         nv == 64 ? 172 + wide_slot_base(DK) : slot + 2);
     if (e != cudaSuccess) return e;
     CUtensorMap tmq, tmk, tmv, tmqn, tmkn;
     bf16 *qn = reinterpret_cast<bf16 *>(static_cast<uint8_t *>(ws) + records_bytes(B, H, T, DK));
@@ -1226,7 +1251,7 @@ cudaError_t launch_diag(const void *q, const void *k, const void *v, const float
         alpha, static_cast<uint8_t *>(ws), H, T, nblk, tmq, tmk, fz, tmqn, tmkn);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    scan<<<dim3(dv / DVS, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
+    scan<<<dim3(dv / nv, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
         static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qn, kn,
         static_cast<const bf16 *>(v), tmqn, tmkn, tmv);
     return cudaGetLastError();
@@ -1240,11 +1265,14 @@ cudaError_t launch_mlstm_dk(const void *q, const void *k, const void *v, const f
                             cudaStream_t stream, int slot) {
     const int nblk = (T + C - 1) / C;
     auto prep = chunk_prep_mlstm_kernel<DK>;
-    auto scan = chunk_scan_kernel<DK, true, false>;
+    const int nv = scan_width(B, H, dv);
+    auto scan = nv == 64 ? chunk_scan_kernel<DK, true, false, false, false, 64>
+                         : chunk_scan_kernel<DK, true, false>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(prep), PrepLayout<DK>::ALLOC,
                                      slot);
     if (e != cudaSuccess) return e;
-    e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC, slot + 1);
+    e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC,
+                         nv == 64 ? 175 + wide_slot_base(DK) : slot + 1);
     if (e != cudaSuccess) return e;
     CUtensorMap tmq, tmk, tmv;
     if ((e = make_rows_map(&tmq, q, DK, T, B * H)) != cudaSuccess) return e;
@@ -1254,7 +1282,7 @@ cudaError_t launch_mlstm_dk(const void *q, const void *k, const void *v, const f
         fgate, igate, m_prev, static_cast<uint8_t *>(ws), aux, H, T, nblk, tmq, tmk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    scan<<<dim3(dv / DVS, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
+    scan<<<dim3(dv / nv, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
         static_cast<const uint8_t *>(ws), C0, static_cast<bf16 *>(h), C_T, H, T, dv, nblk,
         static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), static_cast<const bf16 *>(v),
         tmq, tmk, tmv);
@@ -1271,11 +1299,15 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
     auto prep = maps == 2 ? chunk_prep_kernel<DK, ALPHA, DELTA, 2>
                 : maps == 1 ? chunk_prep_kernel<DK, ALPHA, DELTA, 1>
                             : chunk_prep_kernel<DK, ALPHA, DELTA, 0>;
-    auto scan = chunk_scan_kernel<DK, ALPHA, DELTA>;
+    const int nv = scan_width(B, H, dv);
+    auto scan = nv == 64 ? chunk_scan_kernel<DK, ALPHA, DELTA, false, false, 64>
+                         : chunk_scan_kernel<DK, ALPHA, DELTA>;
+    constexpr int mode_ix = (ALPHA ? 1 : 0) + (DELTA ? 2 : 0);  // LINEAR, DECAY, DELTA, GATED_DELTA
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(prep), PrepLayout<DK>::ALLOC,
                                      slot + 24 * maps);
     if (e != cudaSuccess) return e;
-    e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC, slot + 12);
+    e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC,
+                         nv == 64 ? 160 + 4 * wide_slot_base(DK) + mode_ix : slot + 12);
     if (e != cudaSuccess) return e;
     // q, k and v as [B*H][T][d] with 64 x 64 boxes (for d = 32 the box is
     // wider than a row; its outer half reads zeros)
@@ -1305,7 +1337,7 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
         DELTA ? beta : nullptr, static_cast<uint8_t *>(ws), H, T, nblk, tmq, tmk, fz, tmqn, tmkn);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    scan<<<dim3(dv / DVS, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
+    scan<<<dim3(dv / nv, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
         static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qs, ks,
         static_cast<const bf16 *>(v), qk ? tmqn : tmq, qk ? tmkn : tmk, tmv);
     return cudaGetLastError();

@@ -10,7 +10,7 @@ namespace lr {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxSlots = 160;
+constexpr int kMaxSlots = 192;
 std::atomic<int> g_smem_bytes[kMaxDevices][kMaxSlots];
 
 bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }

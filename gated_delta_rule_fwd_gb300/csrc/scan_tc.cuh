@@ -23,7 +23,8 @@ using bf16 = __nv_bfloat16;
 using namespace tc;
 
 constexpr int C = 64;      // tokens per block
-constexpr int DVS = 32;    // value channels per scan CTA
+constexpr int DVS = 32;    // value channels per scan CTA (the default width; 64 when that
+                           // halves the waves of CTAs, see scan_width)
 
 __device__ int g_tc_error = 0;  // set to 1 when a bounded wait gives up
 // Failure-detection test hook, set from the host (0 = off): a scan launched
@@ -87,10 +88,13 @@ struct ScanLayout {
     static constexpr int ALLOC = BYTES + 1024;
 };
 
-// TMEM columns of the scan kernel: per stage parity p, at p * kParCols, four
-// fp32 accumulators of 32 columns (M = 128 lanes).
-constexpr uint32_t kDa = 0, kDb = 32, kDc = 64, kDS = 96, kParCols = 128;
-constexpr uint32_t kScanCols = 256;
+// TMEM columns of the scan kernel with NV value channels per CTA: per stage
+// parity p, at p * 4 NV, four fp32 accumulators of NV columns (M = 128 lanes):
+// a at 0, b at NV, c at 2 NV, ds at 3 NV; 8 NV columns in all.
+template <int NV>
+struct ScanCols {
+    static constexpr uint32_t Da = 0, Db = NV, Dc = 2 * NV, DS = 3 * NV, PAR = 4 * NV, ALL = 8 * NV;
+};
 
 // L2 prefetch of what stage `st` will fetch (one thread).
 template <int DK, bool DELTA, bool GEN>
@@ -175,7 +179,7 @@ struct ScanBars {
 static_assert(sizeof(ScanBars) <= 256, "the barriers must fit their shared-memory slot");
 constexpr uint32_t kEmptyLCount = 2 + 4 + 4 + 8;  // both issuers' commits, U, output and state warps
 
-template <int DK, bool ALPHA, bool DELTA, bool DIAG = false, bool GEN = false>
+template <int DK, bool ALPHA, bool DELTA, bool DIAG = false, bool GEN = false, int NV = DVS>
 __global__ void __launch_bounds__(kScanThreads, 1)
 chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                   bf16 *__restrict__ o, float *__restrict__ ST, int H, int T, int dv, int nblk,
@@ -185,11 +189,15 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
     using L = ScanLayout<DK>;
     using R = Rec<DK>;
     static_assert(!GEN || (DELTA && !DIAG), "the generalised delta rule runs the delta protocol");
+    static_assert(NV == 32 || (NV == 64 && !GEN), "32 or 64 value channels per CTA");
+    using TC = ScanCols<NV>;
+    constexpr uint32_t kDa = TC::Da, kDb = TC::Db, kDc = TC::Dc, kDS = TC::DS, kParCols = TC::PAR;
+    constexpr uint32_t kScanCols = TC::ALL;
     constexpr int TS = GEN ? C / 2 : C;  // tokens per stage
     extern __shared__ uint8_t sm_raw[];
     uint8_t *sm = align1024(sm_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c0 = blockIdx.x * DVS;
+    const int c0 = blockIdx.x * NV;
     const int vx = c0 & ~63;                           // TMA box column of the v slice
     const uint32_t voff = (uint32_t)(c0 & 63) * 2u;    // byte offset of the slice in a box row
     const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
@@ -231,8 +239,8 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
     const uint32_t limit = fault ? kFaultSpinLimit : kSpinLimit;
     auto wait = [limit](uint64_t *bar, uint32_t parity) { return mbar_wait(bar, parity, limit); };
 
-    const uint32_t id_kn = idesc_bf16_f32_mn(128, DVS, false, true);
-    const uint32_t id_nn = idesc_bf16_f32_mn(128, DVS, true, true);
+    const uint32_t id_kn = idesc_bf16_f32_mn(128, NV, false, true);
+    const uint32_t id_nn = idesc_bf16_f32_mn(128, NV, true, true);
     auto aw_desc = [&](int p) { return tile_desc(smem_u32(sm + L::AW + p * L::AW_BYTES), 128, 0, 0); };
     auto tz_desc = [&](int p) { return tile_desc(smem_u32(sm + L::TZP + p * 24576), 192, 0, 0); };
     auto zp_desc = [&](int p) { return tile_desc(smem_u32(sm + L::TZP + p * 24576), 192, 64, 0); };
@@ -394,8 +402,8 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
     } else if (warp < 12 && (warp & 3) < 2) {
         // ============================================ U rows (TMEM lanes 0..63)
         const int r = 32 * (warp & 3) + lane;
-        const int ch = 16 * ((warp - 4) >> 2);  // first value channel of this warp's half
-        const uint32_t lb = ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)ch;
+        const int ch0 = (NV / 2) * ((warp - 4) >> 2);  // first value channel of this warp's half
+        const uint32_t lb0 = (uint32_t)(32 * (warp & 3)) << 16;
         for (int j = 0; j <= nblk && ok; ++j) {
             const int p = j & 1;
             const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
@@ -413,29 +421,34 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                float x[16], y[16], z[16];
-                tmem_ld16(tmem + lb + base + kDa, x);
-                tmem_ld16(tmem + lb + base + kDb, y);
-                if (j > 0) {
-                    tmem_ld16(tmem + lb + base + kDc, z);
-                    tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) x[c] += gn * y[c] + z[c];
-                } else {
-                    tmem_ld_wait();
+                for (int sub = 0; sub < NV / 32; ++sub) {  // 16 value channels at a time
+                    const int ch = ch0 + 16 * sub;
+                    const uint32_t lb = lb0 + (uint32_t)ch;
+                    float x[16], y[16], z[16];
+                    tmem_ld16(tmem + lb + base + kDa, x);
+                    tmem_ld16(tmem + lb + base + kDb, y);
+                    if (j > 0) {
+                        tmem_ld16(tmem + lb + base + kDc, z);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) x[c] += gn * y[c];
-                }
-                // kd U (for ds, on the state chain) and U (for c, on the U chain)
-                float xk[16];
+                        for (int c = 0; c < 16; ++c) x[c] += gn * y[c] + z[c];
+                    } else {
+                        tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 16; ++c) xk[c] = x[c] * kdr;
+                        for (int c = 0; c < 16; ++c) x[c] += gn * y[c];
+                    }
+                    // kd U (for ds, on the state chain) and U (for c, on the U chain)
+                    float xk[16];
 #pragma unroll
-                for (int c8 = 0; c8 < 2; ++c8) {
-                    *reinterpret_cast<uint4 *>(sm + L::UBK + p * 8192 +
-                                               sw128_offset(r, ch + c8 * 8, 64)) = pack8(xk + c8 * 8);
-                    *reinterpret_cast<uint4 *>(sm + L::UB + sw128_offset(r, ch + c8 * 8, 64)) =
-                        pack8(x + c8 * 8);
+                    for (int c = 0; c < 16; ++c) xk[c] = x[c] * kdr;
+#pragma unroll
+                    for (int c8 = 0; c8 < 2; ++c8) {
+                        *reinterpret_cast<uint4 *>(sm + L::UBK + p * 8192 +
+                                                   sw128_offset(r, ch + c8 * 8, 64)) = pack8(xk + c8 * 8);
+                        *reinterpret_cast<uint4 *>(sm + L::UB + sw128_offset(r, ch + c8 * 8, 64)) =
+                            pack8(x + c8 * 8);
+                    }
                 }
                 fence_async_smem();
                 tc_fence_before();
@@ -451,8 +464,8 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                     const uint8_t *vr = sm + L::VR + p * 8192;
                     uint8_t *vk = sm + L::UBK + p * 8192;
                     const int rw = 16 * (((warp & 3) << 1) | ((warp - 4) >> 2));
-                    for (int idx = lane; idx < 16 * (DVS / 8); idx += 32) {
-                        const int rr = rw + idx / (DVS / 8), c8 = idx % (DVS / 8);
+                    for (int idx = lane; idx < 16 * (NV / 8); idx += 32) {
+                        const int rr = rw + idx / (NV / 8), c8 = idx % (NV / 8);
                         const uint4 raw = *reinterpret_cast<const uint4 *>(
                             vr + sw128_offset(rr, (c0 & 63) + c8 * 8, 64));
                         const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
@@ -472,7 +485,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
     } else if (warp < 12) {
         // ===================================== output rows (TMEM lanes 64..127)
         const int r = 32 * (warp & 3) + lane - 64;
-        const int ch = 16 * ((warp - 4) >> 2);
+        const int ch = (NV / 2) * ((warp - 4) >> 2);  // this warp's NV / 2 value channels
         const uint32_t lb = ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)ch;
         for (int j = 0; j <= nblk && ok; ++j) {
             const int p = j & 1;
@@ -485,19 +498,23 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             if (!ok) break;
             if (j >= 1) {
                 tc_fence_after();
-                float x[16], y[16];
-                tmem_ld16(tmem + lb + base + kDb, x);
-                tmem_ld16(tmem + lb + base + kDc, y);
-                tmem_ld_wait();
+                float out[NV / 2];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) x[c] = gr * x[c] + y[c];  // g' Q' S'^T + P' U'
+                for (int sub = 0; sub < NV / 32; ++sub) {
+                    float x[16], y[16];
+                    tmem_ld16(tmem + lb + base + kDb + 16 * sub, x);
+                    tmem_ld16(tmem + lb + base + kDc + 16 * sub, y);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) out[16 * sub + c] = gr * x[c] + y[c];  // g' Q' S'^T + P' U'
+                }
                 tc_fence_before();
                 warp_arrive(&bars->tfree[p]);
                 const int t = (j - 1) * TS + r;
                 if (r < TS && t < T) {
                     uint4 *dst = reinterpret_cast<uint4 *>(o + (bh * T + t) * dv + c0 + ch);
 #pragma unroll
-                    for (int i8 = 0; i8 < 2; ++i8) dst[i8] = pack8(x + i8 * 8);
+                    for (int i8 = 0; i8 < NV / 16; ++i8) dst[i8] = pack8(out + i8 * 8);
                 }
             } else {
                 warp_arrive(&bars->tfree[p]);
@@ -505,7 +522,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
         }
     } else {
         // ========================== state (TMEM lanes 0..127 = key channels)
-        constexpr int SC = DVS / 2;  // value channels per warp
+        constexpr int SC = NV / 2;  // value channels per warp
         const int kc = 32 * (warp & 3) + lane;
         const int ch = SC * ((warp - 12) >> 2);
         const uint32_t lb = ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)ch;
@@ -547,7 +564,9 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             if (j >= 1) {
                 tc_fence_after();
                 float d[SC];
-                tmem_ld16(tmem + lb + base + kDS, d);
+#pragma unroll
+                for (int h = 0; h < SC / 16; ++h)
+                    tmem_ld16(tmem + lb + base + kDS + 16 * h, *reinterpret_cast<float(*)[16]>(d + 16 * h));
                 tmem_ld_wait();
                 tc_fence_before();
                 if (!DELTA) warp_arrive(&bars->emptyL[p]);
