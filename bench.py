@@ -56,10 +56,9 @@ TRAFFIC_SOURCES = ("gated_delta_rule_fwd_gb300/csrc/chunked_tc.cu",
                    "gated_delta_rule_fwd_gb300/csrc/scan_tc.cuh",
                    "gated_delta_rule_fwd_gb300/csrc/tc_common.cuh")
 TRAFFIC = {
-    "gdn_prefill_bf16": {"bytes": 272.992256e6 + 289.033472e6 + 750.329600e6 + 119.154944e6,
-                         "sha256": "d7fa48e9437fdc4f762c609d18cdc8e97518837284bc0bce3d2dc262d6a8f898"},
+    "gdn_prefill_bf16": {"bytes": 272.945408e6 + 289.673728e6 + 750.079744e6 + 118.984704e6,
+                         "sha256": "807fcc266fd2fb053558d4aea90175688ac541a668ac7e33e95cbe5dd64f1971"},
 }
-
 
 def kernel_source_sha256():
     import hashlib
