@@ -722,7 +722,9 @@ def run_fused(lr, dev, dist, args, w, plain_ms):
             "value": w.B * w.T * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
             "ms_per_step_without_norm": res["maps"], "ms_per_step_plain": plain_ms,
             "steps": steps,
-            "gpu_launches": steps * ((2 if w.dtype == "bf16" else 1) + 1)}
+            # bf16: per-block pass + scan (which applies the norm); fp32: the
+            # chunked kernel + the norm pass
+            "gpu_launches": steps * 2}
 
 
 def run_decode(lr, dev, dist, peaks, args, fused=False):

@@ -1209,7 +1209,8 @@ int scan_width(int B, int H, int dv) {
 // Attribute slot of a 64-channel scan instantiation (the 32-channel ones use
 // the slots their launchers pass): 160 + 4 log2(DK / 32) + mode for the lr
 // modes, 172 + log2(DK / 32) for the diagonal gate, 175 + log2(DK / 32) for
-// mLSTM.
+// mLSTM.  The scans with the folded output norm take 180 + 2 (4 log2(DK / 32) +
+// mode) + (NV == 64).
 constexpr int wide_slot_base(int dk) { return dk == 32 ? 0 : dk == 64 ? 1 : 2; }
 
 // One record per stage: a head of nblk blocks has nblk + 1 stages.  With
@@ -1253,7 +1254,7 @@ cudaError_t launch_diag(const void *q, const void *k, const void *v, const float
     if (e != cudaSuccess) return e;
     scan<<<dim3(dv / nv, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
         static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qn, kn,
-        static_cast<const bf16 *>(v), tmqn, tmkn, tmv);
+        static_cast<const bf16 *>(v), tmqn, tmkn, tmv, nullptr, 0.f);
     return cudaGetLastError();
 }
 
@@ -1285,7 +1286,7 @@ cudaError_t launch_mlstm_dk(const void *q, const void *k, const void *v, const f
     scan<<<dim3(dv / nv, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
         static_cast<const uint8_t *>(ws), C0, static_cast<bf16 *>(h), C_T, H, T, dv, nblk,
         static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), static_cast<const bf16 *>(v),
-        tmq, tmk, tmv);
+        tmq, tmk, tmv, nullptr, 0.f);
     return cudaGetLastError();
 }
 
@@ -1300,14 +1301,19 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
                 : maps == 1 ? chunk_prep_kernel<DK, ALPHA, DELTA, 1>
                             : chunk_prep_kernel<DK, ALPHA, DELTA, 0>;
     const int nv = scan_width(B, H, dv);
-    auto scan = nv == 64 ? chunk_scan_kernel<DK, ALPHA, DELTA, false, false, 64>
-                         : chunk_scan_kernel<DK, ALPHA, DELTA>;
+    // the output norm is applied by the scan (a cluster of the head's dv / nv CTAs)
+    const bool norm = (fz.flags & LR_FUSE_O_RMSNORM) != 0;
+    auto scan = norm ? (nv == 64 ? chunk_scan_kernel<DK, ALPHA, DELTA, false, false, 64, true>
+                                 : chunk_scan_kernel<DK, ALPHA, DELTA, false, false, 32, true>)
+                     : (nv == 64 ? chunk_scan_kernel<DK, ALPHA, DELTA, false, false, 64>
+                                 : chunk_scan_kernel<DK, ALPHA, DELTA>);
     constexpr int mode_ix = (ALPHA ? 1 : 0) + (DELTA ? 2 : 0);  // LINEAR, DECAY, DELTA, GATED_DELTA
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(prep), PrepLayout<DK>::ALLOC,
                                      slot + 24 * maps);
     if (e != cudaSuccess) return e;
     e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC,
-                         nv == 64 ? 160 + 4 * wide_slot_base(DK) + mode_ix : slot + 12);
+                         norm ? 180 + 2 * (4 * wide_slot_base(DK) + mode_ix) + (nv == 64 ? 1 : 0)
+                         : nv == 64 ? 160 + 4 * wide_slot_base(DK) + mode_ix : slot + 12);
     if (e != cudaSuccess) return e;
     // q, k and v as [B*H][T][d] with 64 x 64 boxes (for d = 32 the box is
     // wider than a row; its outer half reads zeros)
@@ -1337,10 +1343,28 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
         DELTA ? beta : nullptr, static_cast<uint8_t *>(ws), H, T, nblk, tmq, tmk, fz, tmqn, tmkn);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    scan<<<dim3(dv / nv, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
-        static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qs, ks,
-        static_cast<const bf16 *>(v), qk ? tmqn : tmq, qk ? tmkn : tmk, tmv);
-    return cudaGetLastError();
+    if (!norm) {
+        scan<<<dim3(dv / nv, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
+            static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qs,
+            ks, static_cast<const bf16 *>(v), qk ? tmqn : tmq, qk ? tmkn : tmk, tmv, nullptr, 0.f);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(dv / nv, H, B);
+    cfg.blockDim = dim3(kScanThreads);
+    cfg.dynamicSmemBytes = ScanLayout<DK>::ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)(dv / nv);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, scan, static_cast<const uint8_t *>(ws), S0,
+                              static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qs, ks,
+                              static_cast<const bf16 *>(v), qk ? tmqn : tmq, qk ? tmkn : tmk, tmv,
+                              fz.norm_w, fz.norm_eps);
 }
 
 template <int DK>
@@ -1393,6 +1417,8 @@ cudaError_t launch_chunked_tc(const void *q, const void *k, const void *v, const
 }
 
 size_t records_bytes_tc(int B, int H, int T, int dk) { return records_bytes(B, H, T, dk); }
+
+bool chunked_tc_applies_norm(lr_mode mode) { return mode != LR_MODE_DIAG_DECAY; }
 
 // Attribute slots 136..141 belong to the mLSTM launch.
 cudaError_t launch_mlstm_tc(const void *q, const void *k, const void *v, const float *fgate,

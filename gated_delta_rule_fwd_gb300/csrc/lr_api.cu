@@ -10,7 +10,7 @@ namespace lr {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxSlots = 192;
+constexpr int kMaxSlots = 208;
 std::atomic<int> g_smem_bytes[kMaxDevices][kMaxSlots];
 
 bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }
@@ -215,7 +215,8 @@ lr_status lr_fwd_chunked_fused(const void *q, const void *k, const void *v, cons
                                     workspace, stream)
                 : launch_chunked_simt(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, dt, mode,
                                       fz, stream);
-        if (e == cudaSuccess && (fz.flags & LR_FUSE_O_RMSNORM))
+        const bool folded = dt == LR_DT_BF16 && chunked_tc_applies_norm(mode);
+        if (e == cudaSuccess && (fz.flags & LR_FUSE_O_RMSNORM) && !folded)
             e = launch_rmsnorm(o, fz.norm_w, fz.norm_eps, (size_t)B * H * T, dv, dt, stream);
     }
     return e == cudaSuccess ? LR_OK : LR_ERR_CUDA;

@@ -83,7 +83,10 @@ struct ScanLayout {
     static constexpr int UBK = UB + 8192;             // x2 [64 tokens][64] MN-major: kd U (kd' V')
     static constexpr int SB_BYTES = 128 * DK;         // [DK][64] MN-major: bf16 S^T slice (32 used)
     static constexpr int SB = UBK + 2 * 8192;         // x2
-    static constexpr int BAR = SB + 2 * SB_BYTES;
+    // output norm folded into the scan: per slot (parity of the output block),
+    // per (cluster rank, warp half) and per token row, a partial sum of squares
+    static constexpr int PS = SB + 2 * SB_BYTES;      // fp32 [2][8][64]
+    static constexpr int BAR = PS + 2 * 8 * 64 * 4;
     static constexpr int BYTES = BAR + 256;
     static constexpr int ALLOC = BYTES + 1024;
 };
@@ -174,22 +177,41 @@ struct ScanBars {
     uint64_t s[2];       // bf16 state copy of this parity written       (8 warps)
     uint64_t u;          // U rows written                               (4 warps)
     uint64_t fin[2];     // every product an issuer issued has completed (commit)
+    uint64_t psfull[2];  // folded norm: every CTA's partial sums of slot s in   (1 + 512 bytes per CTA)
     uint32_t tmem;
 };
 static_assert(sizeof(ScanBars) <= 256, "the barriers must fit their shared-memory slot");
 constexpr uint32_t kEmptyLCount = 2 + 4 + 4 + 8;  // both issuers' commits, U, output and state warps
+constexpr uint32_t kPsBytes = 4 * 32 * 4;         // partial sums one CTA sends a CTA per block
 
-template <int DK, bool ALPHA, bool DELTA, bool DIAG = false, bool GEN = false, int NV = DVS>
+// NORM: the output RMSNorm folded into the output rows (o_t / sqrt(mean over the
+// d_v channels of o_t^2 + eps) * weight).  The dv / NV CTAs of a head run as one
+// cluster.  Per output block each output warp sends its 32 rows' partial sums
+// of squares to every CTA of the cluster with st.async (16 bytes per 4 rows),
+// into slot blk & 1 of the receiver, counted as transaction bytes on the
+// receiver's psfull[blk & 1]; the rows are then normalised with the total and
+// stored.  Two slots suffice: a CTA sends block m only after it has read block
+// m - 1, so once every CTA's sums of block m - 1 are in, every CTA is done with
+// block m - 2.  Each receiver arms a slot's next use (expect_tx) after its wait;
+// bytes that arrive first leave the transaction count negative until then.
+// Cluster barriers at the start (barriers initialised and armed) and at the
+// exit (no CTA leaves while another may still send to it) bracket the
+// exchange; a CTA whose wait gave up still meets the others there, and every
+// store it was sent was issued before its sender reached that barrier.
+template <int DK, bool ALPHA, bool DELTA, bool DIAG = false, bool GEN = false, int NV = DVS,
+          bool NORM = false>
 __global__ void __launch_bounds__(kScanThreads, 1)
 chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                   bf16 *__restrict__ o, float *__restrict__ ST, int H, int T, int dv, int nblk,
                   const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                   const bf16 *__restrict__ v, const __grid_constant__ CUtensorMap tmq,
-                  const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+                  const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  const float *__restrict__ norm_w, float norm_eps) {
     using L = ScanLayout<DK>;
     using R = Rec<DK>;
     static_assert(!GEN || (DELTA && !DIAG), "the generalised delta rule runs the delta protocol");
     static_assert(NV == 32 || (NV == 64 && !GEN), "32 or 64 value channels per CTA");
+    static_assert(!NORM || (!GEN && !DIAG), "the folded norm serves the lr modes");
     using TC = ScanCols<NV>;
     constexpr uint32_t kDa = TC::Da, kDb = TC::Db, kDc = TC::Dc, kDS = TC::DS, kParCols = TC::PAR;
     constexpr uint32_t kScanCols = TC::ALL;
@@ -224,7 +246,12 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             mbar_init(&bars->fin[b], 1);
         }
         mbar_init(&bars->u, 4);
+        if (NORM) {
+            for (int b = 0; b < 2; ++b) mbar_init(&bars->psfull[b], 1);
+        }
         fence_mbar_init();
+        if (NORM)  // each slot's first use: blocks 0 and 1
+            for (int b = 0; b < 2; ++b) mbar_expect_tx(&bars->psfull[b], kPsBytes * gridDim.x);
     }
     if (warp == 0) {
         tmem_alloc(&bars->tmem, kScanCols);
@@ -233,6 +260,8 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the peers' barriers are initialised before any CTA arrives on them
+    if (NORM) cluster_sync_all();
     const uint32_t tmem = bars->tmem;
     bool ok = true;
     const bool fault = g_scan_fault != 0;
@@ -485,8 +514,18 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
     } else if (warp < 12) {
         // ===================================== output rows (TMEM lanes 64..127)
         const int r = 32 * (warp & 3) + lane - 64;
-        const int ch = (NV / 2) * ((warp - 4) >> 2);  // this warp's NV / 2 value channels
+        const int half = (warp - 4) >> 2;
+        const int ch = (NV / 2) * half;  // this warp's NV / 2 value channels
         const uint32_t lb = ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)ch;
+        auto store_rows = [&](const float *rows, int blk) {
+            const int t = blk * TS + r;
+            if (r < TS && t < T) {
+                uint4 *dst = reinterpret_cast<uint4 *>(o + (bh * T + t) * dv + c0 + ch);
+#pragma unroll
+                for (int i8 = 0; i8 < NV / 16; ++i8) dst[i8] = pack8(rows + i8 * 8);
+            }
+        };
+        float *const ps = reinterpret_cast<float *>(sm + L::PS);
         for (int j = 0; j <= nblk && ok; ++j) {
             const int p = j & 1;
             const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
@@ -510,12 +549,37 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                 }
                 tc_fence_before();
                 warp_arrive(&bars->tfree[p]);
-                const int t = (j - 1) * TS + r;
-                if (r < TS && t < T) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(o + (bh * T + t) * dv + c0 + ch);
+                if (NORM) {
+                    const int m = j - 1, sl = m & 1;  // this output block and its slot
+                    float ss = 0.f;
 #pragma unroll
-                    for (int i8 = 0; i8 < NV / 16; ++i8) dst[i8] = pack8(out + i8 * 8);
+                    for (int c = 0; c < NV / 2; ++c) ss = fmaf(out[c], out[c], ss);
+                    // lanes 0..7 send the sums of rows 4 lane .. 4 lane + 3 of the warp
+                    float g[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) g[i] = __shfl_sync(0xffffffffu, ss, 4 * (lane & 7) + i);
+                    if (lane < 8) {
+                        const uint32_t dst = smem_u32(ps + (sl * 8 + 2 * cluster_rank() + half) * 64 +
+                                                      (r - lane) + 4 * lane);
+                        const uint32_t bar = smem_u32(&bars->psfull[sl]);
+                        for (uint32_t t = 0; t < gridDim.x; ++t)
+                            st_async_v4(map_to_rank(dst, t), g[0], g[1], g[2], g[3],
+                                        map_to_rank(bar, t));
+                    }
+                    if (!__all_sync(0xffffffffu, wait(&bars->psfull[sl], (m >> 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    // the slot's next use is block m + 2 (whose sums may already be arriving)
+                    if (warp == 6 && lane == 0) mbar_expect_tx(&bars->psfull[sl], kPsBytes * gridDim.x);
+                    float tot = 0.f;
+                    for (uint32_t i = 0; i < 2 * gridDim.x; ++i) tot += ps[(sl * 8 + i) * 64 + r];
+                    const float inv = rsqrtf(tot / (float)dv + norm_eps);
+#pragma unroll
+                    for (int c = 0; c < NV / 2; ++c)
+                        out[c] *= inv * (norm_w ? __ldg(norm_w + c0 + ch + c) : 1.f);
                 }
+                store_rows(out, j - 1);
             } else {
                 warp_arrive(&bars->tfree[p]);
             }
@@ -595,6 +659,9 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kScanCols);
+    // no CTA leaves while another may still write its partial-sum slots or
+    // arrive on its barriers
+    if (NORM) cluster_sync_all();
 }
 
 // ============================================================ tensor maps

@@ -51,6 +51,40 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     return false;
 }
 
+// ------------------------------------------------------------- clusters
+// Rank of this CTA in its cluster.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address, in the shared memory of CTA `rank` of this cluster, of the object
+// at shared-memory address `local` of this CTA.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+// Store 16 bytes at cluster address `addr` (possibly in another CTA) and count
+// them as transaction bytes on the mbarrier at cluster address `bar`, in the
+// same CTA as `addr`.  As with a TMA copy, the bytes are in that CTA's shared
+// memory once the barrier's phase completes, and a plain (CTA-scope) wait on
+// the barrier orders the waiter's reads after them.  (An acquire at cluster
+// scope would also do, but even one per warp and block costs the scan about
+// 7 %: it stalls the SM's memory pipeline.)
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d,
+                                            uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+        ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
+        : "memory");
+}
+// Every thread of every CTA of the cluster (all threads must execute it).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                     "memory");
+}
+
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -78,3 +78,35 @@ def test_scan_timeout_hook_without_delta(dev):
     o_ref, s_ref = oracle.recurrent(lr.DECAY, x["q"], x["k"], x["v"], x["alpha"], x["beta"], None)
     assert _rel(o, o_ref) <= 2e-2 and _rel(st, s_ref) <= 2e-2
     assert lr.device_status() == 0
+
+
+def test_scan_timeout_hook_with_folded_norm(dev):
+    """The same exit path in the scan that applies the output RMSNorm, where the
+    dv / NV CTAs of a head run as one cluster and exchange the rows' partial
+    sums through each other's shared memory: the CTAs that gave up still meet
+    at the cluster barrier before any of them leaves."""
+    from oracle import prologue as P
+    flags = lr.FUSE_QK_SILU_L2 | lr.FUSE_BETA_SIGMOID | lr.FUSE_ALPHA_SIGMOID | lr.FUSE_O_RMSNORM
+    x = workloads.draw_pre("gdn", 1, 2, 200, 128, 128, seed=23, dtype=torch.bfloat16, s0_std=0.3)
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+
+    def call():
+        return lr.lr_fwd_chunked_fused(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["S0"],
+                                       mode=lr.GATED_DELTA, flags=flags,
+                                       alpha_scale=d["alpha_scale"], norm_weight=d["norm_weight"])
+
+    lr.debug_inject_scan_timeout(True)
+    try:
+        call()
+        torch.cuda.synchronize()
+        assert lr.device_status() == LR_ERR_TIMEOUT
+    finally:
+        lr.debug_inject_scan_timeout(False)
+    o, st = call()
+    torch.cuda.synchronize()
+    f64 = lambda t: t.double().numpy()
+    o_ref, s_ref = P.fused(lr.GATED_DELTA, flags, f64(x["q"]), f64(x["k"]), f64(x["v"]),
+                           f64(x["alpha"]), f64(x["beta"]), f64(x["S0"]),
+                           alpha_scale=f64(x["alpha_scale"]), norm_weight=f64(x["norm_weight"]))
+    assert _rel(o, o_ref) <= 2e-2 and _rel(st, s_ref) <= 2e-2
+    assert lr.device_status() == 0
