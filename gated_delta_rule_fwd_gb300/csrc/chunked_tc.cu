@@ -800,7 +800,7 @@ chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws
         return __bfloat162float(*reinterpret_cast<const bf16 *>(t + eo(il)));
     };
     auto st = [&](uint8_t *t, int il, float x) {
-        *reinterpret_cast<bf16 *>(t + eo(il)) = __float2bfloat16_rn(x);
+        *reinterpret_cast<bf16 *>(t + eo(il)) = bf16_rn(x);
     };
     const float *inqh = inq + r0, *inkh = ink + r0;
     auto qrow = [&](int il) {
@@ -832,7 +832,7 @@ chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws
                     pfx *= a[il];
                     float kv = ld(KT, il);
                     if (QKN) kv *= inkh[il];
-                    st(KH, il, kv * fminf(__frcp_rn(pfx), 5.5e34f));
+                    st(KH, il, kv * fminf(__fdividef(1.f, pfx), 5.5e34f));
                     st(QH, il, qrow(il) * pfx);
                 }
             }
@@ -846,7 +846,7 @@ chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws
                 if (QKN) kv *= inkh[rl];
                 if (hf == 0) {
                     st(KH, rl, kv * sfx);
-                    st(QH, rl, qrow(rl) * fminf(__frcp_rn(sfx), 5.5e34f));
+                    st(QH, rl, qrow(rl) * fminf(__fdividef(1.f, sfx), 5.5e34f));
                 }
                 st(KT, rl, kv * gC);
                 sfx *= a[rl];
@@ -907,7 +907,7 @@ chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws
     #pragma unroll
                     for (int rl = 15; rl >= 0; --rl) {
                         const int il = 16 * (J & 1) + rl;
-                        st(QH, il, qrow(il) * fminf(__frcp_rn(s), 5.5e34f));
+                        st(QH, il, qrow(il) * fminf(__fdividef(1.f, s), 5.5e34f));
                         s *= a[il];
                     }
                 }

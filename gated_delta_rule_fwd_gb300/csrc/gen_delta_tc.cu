@@ -83,7 +83,7 @@ struct GdWs {
 };
 
 __device__ __forceinline__ void st_tile(uint8_t *tile, int rows, int r, int c, float x) {
-    *reinterpret_cast<bf16 *>(tile + sw128_offset(r, c, rows)) = __float2bfloat16_rn(x);
+    *reinterpret_cast<bf16 *>(tile + sw128_offset(r, c, rows)) = bf16_rn(x);
 }
 
 // One CTA per (block, head, batch).  q, kw [B*H][T][DK] bf16; w, kappa, a
@@ -206,10 +206,10 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
             st_tile(At, 128, 2 * GC + t, c, second ? qf * __expf(fminf(Lt - Ll, kMaxUp)) : 0.f);
             st_tile(At, 128, 3 * GC + t, c, second ? kp * __expf(fminf(Lm - Ll, kMaxUp)) : 0.f);
             Kd[t * DK + c] = kp * __expf(Lm);
-            qrow[t * DK + c] = __float2bfloat16_rn(qf * __expf(Lt));
+            qrow[t * DK + c] = bf16_rn(qf * __expf(Lt));
             const float fK = __expf(Ll - Lt);  // e^{L_last - L_t}
-            krow[t * DK + c] = __float2bfloat16_rn(kf * fK);
-            krow[(GC + t) * DK + c] = __float2bfloat16_rn(-bf * fK);
+            krow[t * DK + c] = bf16_rn(kf * fK);
+            krow[(GC + t) * DK + c] = bf16_rn(-bf * fK);
             Lm = Lt;
         }
     }
@@ -294,9 +294,9 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
             // D_{j-1} of this column: its own thread's Dp (tid < DK: part 0, c = tid)
 #pragma unroll
             for (int t = 0; t < GC; ++t) {
-                *reinterpret_cast<bf16 *>(wg + sw128_offset(t, tid, 32)) = __float2bfloat16_rn(x[t]);
+                *reinterpret_cast<bf16 *>(wg + sw128_offset(t, tid, 32)) = bf16_rn(x[t]);
                 *reinterpret_cast<bf16 *>(rec + R::WT + sw128_offset(GC + t, tid, 64)) =
-                    __float2bfloat16_rn(x[t] * Dp);
+                    bf16_rn(x[t] * Dp);
             }
         }
     } else {

@@ -17,10 +17,19 @@ template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x
     return __bfloat162float(x);
 }
 
+// fp32 -> bf16, rounded to nearest even, through the paired conversion
+// instruction (same bits as the single-value conversion, which is slower on
+// this target).
+__device__ __forceinline__ __nv_bfloat16 bf16_rn(float x) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(0.f), "f"(x));
+    return __ushort_as_bfloat16((unsigned short)(r & 0xffffu));
+}
+
 template <typename T> __device__ __forceinline__ T from_f(float x);
 template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
-    return __float2bfloat16_rn(x);
+    return bf16_rn(x);
 }
 
 // Four consecutive elements widened to fp32 (16-byte aligned for float,

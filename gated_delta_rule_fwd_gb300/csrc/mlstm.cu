@@ -139,7 +139,7 @@ __device__ __forceinline__ uint32_t bf2(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 __device__ __forceinline__ unsigned short pack(const float (&x)[1]) {
-    return __bfloat16_as_ushort(__float2bfloat16_rn(x[0]));
+    return __bfloat16_as_ushort(bf16_rn(x[0]));
 }
 __device__ __forceinline__ unsigned int pack(const float (&x)[2]) { return bf2(x[0], x[1]); }
 __device__ __forceinline__ uint2 pack(const float (&x)[4]) {
