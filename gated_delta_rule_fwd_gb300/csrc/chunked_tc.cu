@@ -1254,7 +1254,7 @@ cudaError_t launch_diag(const void *q, const void *k, const void *v, const float
     if (e != cudaSuccess) return e;
     scan<<<dim3(dv / nv, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
         static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qn, kn,
-        static_cast<const bf16 *>(v), tmqn, tmkn, tmv, nullptr, 0.f);
+        static_cast<const bf16 *>(v), tmqn, tmkn, tmv, nullptr, 0.f, nullptr);
     return cudaGetLastError();
 }
 
@@ -1262,8 +1262,8 @@ cudaError_t launch_diag(const void *q, const void *k, const void *v, const float
 template <int DK>
 cudaError_t launch_mlstm_dk(const void *q, const void *k, const void *v, const float *fgate,
                             const float *igate, const float *m_prev, const float *C0, void *h,
-                            float *C_T, float *aux, int B, int H, int T, int dv, void *ws,
-                            cudaStream_t stream, int slot) {
+                            float *C_T, float *aux, const float *row_scale, int phase, int B,
+                            int H, int T, int dv, void *ws, cudaStream_t stream, int slot) {
     const int nblk = (T + C - 1) / C;
     auto prep = chunk_prep_mlstm_kernel<DK>;
     const int nv = scan_width(B, H, dv);
@@ -1279,14 +1279,15 @@ cudaError_t launch_mlstm_dk(const void *q, const void *k, const void *v, const f
     if ((e = make_rows_map(&tmq, q, DK, T, B * H)) != cudaSuccess) return e;
     if ((e = make_rows_map(&tmk, k, DK, T, B * H)) != cudaSuccess) return e;
     if ((e = make_rows_map(&tmv, v, dv, T, B * H)) != cudaSuccess) return e;
-    prep<<<dim3(nblk, H, B), NT, PrepLayout<DK>::ALLOC, stream>>>(
-        fgate, igate, m_prev, static_cast<uint8_t *>(ws), aux, H, T, nblk, tmq, tmk);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (phase == 0) {
+        prep<<<dim3(nblk, H, B), NT, PrepLayout<DK>::ALLOC, stream>>>(
+            fgate, igate, m_prev, static_cast<uint8_t *>(ws), aux, H, T, nblk, tmq, tmk);
+        return cudaGetLastError();
+    }
     scan<<<dim3(dv / nv, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
         static_cast<const uint8_t *>(ws), C0, static_cast<bf16 *>(h), C_T, H, T, dv, nblk,
         static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), static_cast<const bf16 *>(v),
-        tmq, tmk, tmv, nullptr, 0.f);
+        tmq, tmk, tmv, nullptr, 0.f, row_scale);
     return cudaGetLastError();
 }
 
@@ -1346,7 +1347,7 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
     if (!norm) {
         scan<<<dim3(dv / nv, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
             static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qs,
-            ks, static_cast<const bf16 *>(v), qk ? tmqn : tmq, qk ? tmkn : tmk, tmv, nullptr, 0.f);
+            ks, static_cast<const bf16 *>(v), qk ? tmqn : tmq, qk ? tmkn : tmk, tmv, nullptr, 0.f, nullptr);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -1364,7 +1365,7 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
     return cudaLaunchKernelEx(&cfg, scan, static_cast<const uint8_t *>(ws), S0,
                               static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qs, ks,
                               static_cast<const bf16 *>(v), qk ? tmqn : tmq, qk ? tmkn : tmk, tmv,
-                              fz.norm_w, fz.norm_eps);
+                              fz.norm_w, fz.norm_eps, static_cast<const float *>(nullptr));
 }
 
 template <int DK>
@@ -1423,18 +1424,18 @@ bool chunked_tc_applies_norm(lr_mode mode) { return mode != LR_MODE_DIAG_DECAY; 
 // Attribute slots 136..141 belong to the mLSTM launch.
 cudaError_t launch_mlstm_tc(const void *q, const void *k, const void *v, const float *fgate,
                             const float *igate, const float *m_prev, const float *C0, void *h,
-                            float *C_T, float *aux, int B, int H, int T, int dk, int dv, void *ws,
-                            cudaStream_t stream) {
+                            float *C_T, float *aux, const float *row_scale, int phase, int B,
+                            int H, int T, int dk, int dv, void *ws, cudaStream_t stream) {
     switch (dk) {
     case 32:
-        return launch_mlstm_dk<32>(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, B, H, T, dv, ws,
-                                   stream, 136);
+        return launch_mlstm_dk<32>(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, row_scale,
+                                   phase, B, H, T, dv, ws, stream, 136);
     case 64:
-        return launch_mlstm_dk<64>(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, B, H, T, dv, ws,
-                                   stream, 138);
+        return launch_mlstm_dk<64>(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, row_scale,
+                                   phase, B, H, T, dv, ws, stream, 138);
     default:
-        return launch_mlstm_dk<128>(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, B, H, T, dv, ws,
-                                    stream, 140);
+        return launch_mlstm_dk<128>(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, row_scale,
+                                    phase, B, H, T, dv, ws, stream, 140);
     }
 }
 

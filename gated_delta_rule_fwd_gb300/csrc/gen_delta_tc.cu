@@ -482,7 +482,7 @@ cudaError_t launch_gd_dk(const void *q, const void *kw, const void *v, const flo
     }
     scan<<<dim3(dv / DVS, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
         recs, S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qo, ko,
-        static_cast<const bf16 *>(v), tmq, tmk, tmv, nullptr, 0.f);
+        static_cast<const bf16 *>(v), tmq, tmk, tmv, nullptr, 0.f, nullptr);
     return cudaGetLastError();
 }
 

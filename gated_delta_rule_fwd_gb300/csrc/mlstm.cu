@@ -7,11 +7,11 @@
 //
 // The stabiliser depends on the gates only, so the bf16 path computes it for
 // every block start first (mlstm_stab_kernel), then runs the per-block pass
-// and the scan without delta for the numerator (chunked_tc.cu), then the
-// normaliser n~ at every block start (mlstm_nscan_kernel) and the division
-// of every token's numerator by max(|denominator|, e^{-m_t})
-// (mlstm_div_kernel).  The fp32 path and the decode step do it all in one
-// kernel each.
+// (chunked_tc.cu), the normaliser n~ at every block start
+// (mlstm_nscan_kernel) and every token's factor 1 / max(|denominator|,
+// e^{-m_t}) (mlstm_den_kernel), and last the scan without delta, which
+// multiplies each token's numerator by its factor before the one rounding to
+// bf16.  The fp32 path and the decode step do it all in one kernel each.
 #include <math.h>
 
 #include <type_traits>
@@ -30,7 +30,7 @@ constexpr int kMlstmAux = 384, kAuxRs = 0, kAuxM = 64, kAuxG = 128, kAuxGC = 192
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct MlstmWs {
-    size_t recs, mprev, aux, nst, total;
+    size_t recs, mprev, aux, nst, rs, total;
 };
 MlstmWs mlstm_ws(int B, int H, int T, int dk) {
     const size_t nblk = (size_t)((T + C - 1) / C), bh = (size_t)B * H;
@@ -39,7 +39,8 @@ MlstmWs mlstm_ws(int B, int H, int T, int dk) {
     w.mprev = align256(records_bytes_tc(B, H, T, dk));
     w.aux = align256(w.mprev + bh * nblk * 4);
     w.nst = align256(w.aux + bh * nblk * kMlstmAux * 4);
-    w.total = w.nst + bh * nblk * (size_t)dk * 4;
+    w.rs = align256(w.nst + bh * nblk * (size_t)dk * 4);
+    w.total = w.rs + bh * (size_t)T * 4;
     return w;
 }
 
@@ -113,9 +114,10 @@ mlstm_nscan_kernel(const float *__restrict__ aux, const float *__restrict__ n0,
 }
 
 // One CTA of 4 warps per (block, b, h); a warp takes four tokens at a time:
-// den = g'_t (n~ . q_t) + row sum, h_t = numerator / max(|den|, e^{-m_t}) in
-// place.  Each lane holds d_k / 32 consecutive channels (one 2-, 4- or 8-byte
-// access per row), the four tokens' loads are independent.
+// den = g'_t (n~ . q_t) + row sum, and the token's factor
+// rs_t = 1 / max(|den|, e^{-m_t}).  Each lane holds d_k / 32 consecutive
+// channels of q (one 2-, 4- or 8-byte access per row); the four tokens' loads
+// are independent.
 template <int N> struct Lanes;
 template <> struct Lanes<1> { using T = unsigned short; };
 template <> struct Lanes<2> { using T = unsigned int; };
@@ -134,26 +136,13 @@ __device__ __forceinline__ void unpack(uint2 w, float (&x)[4]) {
     x[2] = __uint_as_float(w.y << 16);
     x[3] = __uint_as_float(w.y & 0xffff0000u);
 }
-__device__ __forceinline__ uint32_t bf2(float a, float b) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // a low, b high
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
-__device__ __forceinline__ unsigned short pack(const float (&x)[1]) {
-    return __bfloat16_as_ushort(bf16_rn(x[0]));
-}
-__device__ __forceinline__ unsigned int pack(const float (&x)[2]) { return bf2(x[0], x[1]); }
-__device__ __forceinline__ uint2 pack(const float (&x)[4]) {
-    return make_uint2(bf2(x[0], x[1]), bf2(x[2], x[3]));
-}
 
-template <int DK, int DV>
+template <int DK>
 __global__ void __launch_bounds__(128)
-mlstm_div_kernel(const __nv_bfloat16 *__restrict__ q, const float *__restrict__ aux,
-                 const float *__restrict__ nst, __nv_bfloat16 *__restrict__ h, int H, int T,
-                 int nblk) {
-    constexpr int EK = DK / 32, EV = DV / 32, U = 4;
+mlstm_den_kernel(const __nv_bfloat16 *__restrict__ q, const float *__restrict__ aux,
+                 const float *__restrict__ nst, float *__restrict__ rs, int H, int T, int nblk) {
+    constexpr int EK = DK / 32, U = 4;
     using LK = typename Lanes<EK>::T;
-    using LV = typename Lanes<EV>::T;
     const int blk = blockIdx.x;
     const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -163,33 +152,23 @@ mlstm_div_kernel(const __nv_bfloat16 *__restrict__ q, const float *__restrict__ 
     for (int e = 0; e < EK; ++e) nv[e] = nst[(bh * nblk + blk) * DK + EK * lane + e];
     const int t0 = blk * C, n = min(C, T - t0);
     const LK *qr = reinterpret_cast<const LK *>(q);
-    LV *hr = reinterpret_cast<LV *>(h);
     for (int r0 = warp * U; r0 < n; r0 += 4 * U) {
         LK qw[U];
-        LV hw[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const size_t t = bh * T + t0 + min(r0 + u, n - 1);
-            qw[u] = qr[t * 32 + lane];
-            hw[u] = hr[t * 32 + lane];
-        }
+        for (int u = 0; u < U; ++u) qw[u] = qr[(bh * T + t0 + min(r0 + u, n - 1)) * 32 + lane];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int r = r0 + u;
-            float qf[EK], hf[EV];
+            float qf[EK];
             unpack(qw[u], qf);
-            unpack(hw[u], hf);
             float d = 0.f;
 #pragma unroll
             for (int e = 0; e < EK; ++e) d += nv[e] * qf[e];
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-            if (r < n) {
+            if (r < n && lane == 0) {
                 const float den = a[kAuxG + r] * d + a[kAuxRs + r];
-                const float inv = 1.f / fmaxf(fabsf(den), __expf(-a[kAuxM + r]));
-#pragma unroll
-                for (int e = 0; e < EV; ++e) hf[e] *= inv;
-                hr[(bh * T + t0 + r) * 32 + lane] = pack(hf);
+                rs[bh * T + t0 + r] = 1.f / fmaxf(fabsf(den), __expf(-a[kAuxM + r]));
             }
         }
     }
@@ -446,7 +425,9 @@ cudaError_t launch_mlstm_chunked(const void *q, const void *k, const void *v, co
     mlstm_stab_kernel<<<BH, kStabThreads, 0, stream>>>(fgate, igate, m0, m_prev, m_T, T, nblk);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = launch_mlstm_tc(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, B, H, T, dk, dv, ws, stream);
+    float *rs = reinterpret_cast<float *>(base + w.rs);
+    e = launch_mlstm_tc(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, nullptr, 0, B, H, T, dk,
+                        dv, ws, stream);
     if (e != cudaSuccess) return e;
     switch (dk) {
     case 32: mlstm_nscan_kernel<32><<<BH, 32, 0, stream>>>(aux, n0, nst, n_T, nblk); break;
@@ -455,24 +436,15 @@ cudaError_t launch_mlstm_chunked(const void *q, const void *k, const void *v, co
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const dim3 grid(nblk, H, B);
-    using bf = __nv_bfloat16;
-    const bf *qb = static_cast<const bf *>(q);
-    bf *hb = static_cast<bf *>(h);
-    auto div = [&](auto kern) { kern<<<grid, 128, 0, stream>>>(qb, aux, nst, hb, H, T, nblk); };
-    auto div_dk = [&](auto dkc) {
-        constexpr int DKc = decltype(dkc)::value;
-        switch (dv) {
-        case 32: div(mlstm_div_kernel<DKc, 32>); break;
-        case 64: div(mlstm_div_kernel<DKc, 64>); break;
-        default: div(mlstm_div_kernel<DKc, 128>); break;
-        }
-    };
+    const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(q);
     switch (dk) {
-    case 32: div_dk(std::integral_constant<int, 32>{}); break;
-    case 64: div_dk(std::integral_constant<int, 64>{}); break;
-    default: div_dk(std::integral_constant<int, 128>{}); break;
+    case 32: mlstm_den_kernel<32><<<grid, 128, 0, stream>>>(qb, aux, nst, rs, H, T, nblk); break;
+    case 64: mlstm_den_kernel<64><<<grid, 128, 0, stream>>>(qb, aux, nst, rs, H, T, nblk); break;
+    default: mlstm_den_kernel<128><<<grid, 128, 0, stream>>>(qb, aux, nst, rs, H, T, nblk); break;
     }
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_mlstm_tc(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, rs, 1, B, H, T, dk, dv,
+                           ws, stream);
 }
 
 cudaError_t launch_mlstm_step(const void *q, const void *k, const void *v, const float *fgate,

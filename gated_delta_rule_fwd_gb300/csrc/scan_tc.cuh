@@ -206,7 +206,8 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                   const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                   const bf16 *__restrict__ v, const __grid_constant__ CUtensorMap tmq,
                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                  const float *__restrict__ norm_w, float norm_eps) {
+                  const float *__restrict__ norm_w, float norm_eps,
+                  const float *__restrict__ row_scale) {
     using L = ScanLayout<DK>;
     using R = Rec<DK>;
     static_assert(!GEN || (DELTA && !DIAG), "the generalised delta rule runs the delta protocol");
@@ -533,6 +534,13 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             if (!ok) break;
             const float gr = GEN ? 1.f : vec_of(p)[kVgPrev + r];  // the only late-group value read here
             warp_arrive(&bars->emptyL[p]);
+            // a factor per token (mLSTM: 1 / max(|denominator|, e^-m)), fetched
+            // before the wait for the products
+            float rsc = 1.f;
+            if (row_scale != nullptr && j >= 1) {
+                const int t = (j - 1) * TS + r;
+                if (r < TS && t < T) rsc = __ldg(row_scale + bh * T + t);
+            }
             if (j >= 1) ok = __all_sync(0xffffffffu, wait(&bars->dA[p], ph));
             if (!ok) break;
             if (j >= 1) {
@@ -545,7 +553,8 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                     tmem_ld16(tmem + lb + base + kDc + 16 * sub, y);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) out[16 * sub + c] = gr * x[c] + y[c];  // g' Q' S'^T + P' U'
+                    for (int c = 0; c < 16; ++c)  // (g' Q' S'^T + P' U') times the token's factor
+                        out[16 * sub + c] = (gr * x[c] + y[c]) * rsc;
                 }
                 tc_fence_before();
                 warp_arrive(&bars->tfree[p]);

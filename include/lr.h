@@ -372,9 +372,10 @@ lr_status lr_step_fused(const void *q, const void *k, const void *v,
  * every block start (it depends on the gates only, so one pass over f and
  * igate gives it), the per-block pass (scores weighted by
  * e^{F_t - F_s + igate_s - m_t}, F the cumulative log forget gate of the
- * block), the sequential pass of lr_fwd_chunked without delta (the numerator),
- * the normaliser n~ at every block start, and the division of every token's
- * numerator by its threshold.  The fp32 path is one kernel.
+ * block), the normaliser n~ at every block start, every token's factor
+ * 1 / max(|n~_t^T q_t|, e^{-m_t}), and the sequential pass of lr_fwd_chunked
+ * without delta, which scales each token's numerator by its factor in fp32
+ * before the one rounding of h.  The fp32 path is one kernel.
  */
 lr_status lr_fwd_chunked_mlstm(const void *q, const void *k, const void *v,
                                const float *fgate, const float *igate,
