@@ -1303,7 +1303,8 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
                             : chunk_prep_kernel<DK, ALPHA, DELTA, 0>;
     const int nv = scan_width(B, H, dv);
     // the output norm is applied by the scan (a cluster of the head's dv / nv CTAs)
-    const bool norm = (fz.flags & LR_FUSE_O_RMSNORM) != 0;
+    const bool norm =
+        (fz.flags & LR_FUSE_O_RMSNORM) != 0 && chunked_tc_applies_norm(LR_MODE_DECAY, B, H, dv);
     auto scan = norm ? (nv == 64 ? chunk_scan_kernel<DK, ALPHA, DELTA, false, false, 64, true>
                                  : chunk_scan_kernel<DK, ALPHA, DELTA, false, false, 32, true>)
                      : (nv == 64 ? chunk_scan_kernel<DK, ALPHA, DELTA, false, false, 64>
@@ -1419,7 +1420,14 @@ cudaError_t launch_chunked_tc(const void *q, const void *k, const void *v, const
 
 size_t records_bytes_tc(int B, int H, int T, int dk) { return records_bytes(B, H, T, dk); }
 
-bool chunked_tc_applies_norm(lr_mode mode) { return mode != LR_MODE_DIAG_DECAY; }
+// The scan folds the output norm when a head's value channels span at most
+// two CTAs.  With four (d_v = 128 on 32-channel CTAs) the exchange cost as
+// much as the separate pass saved, or more, depending on the device: 0.495
+// against 0.499 ms on one GB300 and 0.507 against 0.500 ms on another for the
+// gated-delta prefill B=2 H=16 T=16384; with two it saved 3 to 8 %.
+bool chunked_tc_applies_norm(lr_mode mode, int B, int H, int dv) {
+    return mode != LR_MODE_DIAG_DECAY && dv / scan_width(B, H, dv) <= 2;
+}
 
 // Attribute slots 136..141 belong to the mLSTM launch.
 cudaError_t launch_mlstm_tc(const void *q, const void *k, const void *v, const float *fgate,

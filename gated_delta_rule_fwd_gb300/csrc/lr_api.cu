@@ -215,7 +215,7 @@ lr_status lr_fwd_chunked_fused(const void *q, const void *k, const void *v, cons
                                     workspace, stream)
                 : launch_chunked_simt(q, k, v, alpha, beta, S0, o, S_T, B, H, T, dk, dv, dt, mode,
                                       fz, stream);
-        const bool folded = dt == LR_DT_BF16 && chunked_tc_applies_norm(mode);
+        const bool folded = dt == LR_DT_BF16 && chunked_tc_applies_norm(mode, B, H, dv);
         if (e == cudaSuccess && (fz.flags & LR_FUSE_O_RMSNORM) && !folded)
             e = launch_rmsnorm(o, fz.norm_w, fz.norm_eps, (size_t)B * H * T, dv, dt, stream);
     }

@@ -146,8 +146,8 @@ cudaError_t launch_mlstm_tc(const void *q, const void *k, const void *v, const f
                             int H, int T, int dk, int dv, void *ws, cudaStream_t stream);
 size_t records_bytes_tc(int B, int H, int T, int dk);
 // Whether launch_chunked_tc applies LR_FUSE_O_RMSNORM itself (in the scan) for
-// this mode; otherwise the caller runs the norm pass after it.
-bool chunked_tc_applies_norm(lr_mode mode);
+// this mode and these sizes; otherwise the caller runs the norm pass after it.
+bool chunked_tc_applies_norm(lr_mode mode, int B, int H, int dv);
 
 // Generalised delta rule of RWKV-7 (gen_delta.cu): the fp32 chunked kernel and
 // the decode step (fp32 or bf16).

@@ -310,12 +310,14 @@ typedef struct {
  * bytes of workspace).  fp32: the single kernel applies the maps to what it
  * stages, in fp32.  Rows whose sum of squares overflows fp32 (entries beyond
  * about 1e19) normalise to zero.
- * With LR_FUSE_O_RMSNORM, bf16 in the lr modes: the sequential pass launches
- * the d_v / NV CTAs that share a head's value channels as one thread-block
- * cluster; they exchange each token's partial sums of squares through
- * distributed shared memory and store o normalised (fp32 sums and scaling,
- * one rounding to bf16).  fp32, and bf16 with LR_MODE_DIAG_DECAY: one more
- * kernel normalises o in place after the chunked kernel.
+ * With LR_FUSE_O_RMSNORM, bf16 in the lr modes, when a head's value channels
+ * span at most two CTAs of the sequential pass (d_v <= 64, or d_v = 128 where
+ * B * H is large enough for 64-channel CTAs): the pass launches those CTAs
+ * as one thread-block cluster; they exchange each token's partial sums of
+ * squares through distributed shared memory and store o normalised (fp32
+ * sums and scaling, one rounding to bf16).  Otherwise (four CTAs per head,
+ * fp32, or LR_MODE_DIAG_DECAY) one more kernel normalises o in place after
+ * the chunked kernel.
  */
 lr_status lr_fwd_chunked_fused(const void *q, const void *k, const void *v,
                                const float *alpha, const float *beta,

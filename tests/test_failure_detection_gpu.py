@@ -87,7 +87,8 @@ def test_scan_timeout_hook_with_folded_norm(dev):
     at the cluster barrier before any of them leaves."""
     from oracle import prologue as P
     flags = lr.FUSE_QK_SILU_L2 | lr.FUSE_BETA_SIGMOID | lr.FUSE_ALPHA_SIGMOID | lr.FUSE_O_RMSNORM
-    x = workloads.draw_pre("gdn", 1, 2, 200, 128, 128, seed=23, dtype=torch.bfloat16, s0_std=0.3)
+    # d_v = 64: two 32-channel CTAs per head, the scan applies the norm
+    x = workloads.draw_pre("gdn", 1, 2, 200, 128, 64, seed=23, dtype=torch.bfloat16, s0_std=0.3)
     d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
 
     def call():
