@@ -265,8 +265,11 @@ __device__ __forceinline__ void ut_inverse(float *AT, float *Xt, int tid) {
 }
 
 // SiLU(x) = x sigmoid(x) = h + h tanh(h), h = x / 2, with the hardware tanh
-// approximation (one special-function operation per element; its relative
-// error, about 2^-11, is below a bf16 rounding of the result).
+// approximation (one special-function operation per element).  Its error,
+// about 2^-11 relative to tanh, makes an absolute error of about 2^-12 |x| in
+// SiLU: below a bf16 rounding of the result for x > -1, larger relative to
+// the small values SiLU takes far below 0 (about 1.4 % at x = -4), which
+// carry little weight after the L2 normalisation.
 __device__ __forceinline__ float silu_fast(float x) {
     const float h = 0.5f * x;
     float t;

@@ -302,7 +302,7 @@ typedef struct {
  *
  * bf16: the per-block pass applies the gate maps to the gates it reads, and
  * SiLU to the q and k tiles it stages (fp32 through the hardware tanh
- * approximation, relative error about 2^-11, then one rounding to bf16); the
+ * approximation: absolute error about 2^-12 |x|, then one rounding to bf16); the
  * rows' L2 norms are kept in fp32 and folded into the factors the products
  * are scaled by, so the result is that of the normalised vectors.  It writes
  * SiLU(q) and SiLU(k) (bf16, [B, H, T, dk] each) to the workspace, where the
