@@ -56,8 +56,8 @@ TRAFFIC_SOURCES = ("gated_delta_rule_fwd_gb300/csrc/chunked_tc.cu",
                    "gated_delta_rule_fwd_gb300/csrc/scan_tc.cuh",
                    "gated_delta_rule_fwd_gb300/csrc/tc_common.cuh")
 TRAFFIC = {
-    "gdn_prefill_bf16": {"bytes": 272.945408e6 + 289.673728e6 + 750.079744e6 + 118.984704e6,
-                         "sha256": "807fcc266fd2fb053558d4aea90175688ac541a668ac7e33e95cbe5dd64f1971"},
+    "gdn_prefill_bf16": {"bytes": 272.943104e6 + 289.676800e6 + 750.076416e6 + 118.955008e6,
+                         "sha256": "96f6ec319e3c8a46b2020143078cb79df508438c1d837ddd6138d023653c2379"},
 }
 
 def kernel_source_sha256():
