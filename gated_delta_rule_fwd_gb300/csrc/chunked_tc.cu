@@ -481,7 +481,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         for (int half = 0; half < 2; ++half) {
             float a[32];
             tmem_ld32(tmem + lane_base + 32 * half, a);
-            tmem_ld_wait();
+            tmem_ld_wait(a);
             float gi[32];  // 1 / g of the key tokens of this half
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
@@ -592,7 +592,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
             for (int cb = 0; cb < DK / 32; ++cb) {
                 float w[32];
                 tmem_ld32(tmem + lane_base + 32 * cb, w);
-                tmem_ld_wait();
+                tmem_ld_wait(w);
                 if (lane < 16) {
 #pragma unroll
                     for (int i8 = 0; i8 < 4; ++i8)
@@ -637,7 +637,7 @@ chunk_prep_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                 for (int half = 0; half < 2; ++half) {
                     float z[32];
                     tmem_ld32(tmem + lane_base + 32 * half, z);
-                    tmem_ld_wait();
+                    tmem_ld_wait(z);
                     if (lane < 16) {
 #pragma unroll
                         for (int e4 = 0; e4 < 8; ++e4) {  // -Z' diag(kd') (/ |k'|)
@@ -979,7 +979,7 @@ chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws
         const int r = 16 * wq + lane;
         float x[32];
         tmem_ld32(tmem + ((uint32_t)(32 * wq) << 16) + 32 * half, x);
-        tmem_ld_wait();
+        tmem_ld_wait(x);
         if (lane < 16) {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
@@ -1169,7 +1169,7 @@ chunk_prep_mlstm_kernel(const float *__restrict__ fgate, const float *__restrict
         for (int half = 0; half < 2; ++half) {
             float a[32];
             tmem_ld32(tmem + lane_base + 32 * half, a);
-            tmem_ld_wait();
+            tmem_ld_wait(a);
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
                 const int i = half * 32 + e;
@@ -1257,7 +1257,7 @@ cudaError_t launch_diag(const void *q, const void *k, const void *v, const float
     if (e != cudaSuccess) return e;
     scan<<<dim3(dv / nv, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
         static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qn, kn,
-        static_cast<const bf16 *>(v), tmqn, tmkn, tmv, nullptr, 0.f, nullptr);
+        static_cast<const bf16 *>(v), tmqn, tmkn, tmv, nullptr, 0.f, 0);
     return cudaGetLastError();
 }
 
@@ -1265,8 +1265,8 @@ cudaError_t launch_diag(const void *q, const void *k, const void *v, const float
 template <int DK>
 cudaError_t launch_mlstm_dk(const void *q, const void *k, const void *v, const float *fgate,
                             const float *igate, const float *m_prev, const float *C0, void *h,
-                            float *C_T, float *aux, const float *row_scale, int phase, int B,
-                            int H, int T, int dv, void *ws, cudaStream_t stream, int slot) {
+                            float *C_T, float *aux, int phase, int B, int H, int T, int dv,
+                            void *ws, cudaStream_t stream, int slot) {
     const int nblk = (T + C - 1) / C;
     auto prep = chunk_prep_mlstm_kernel<DK>;
     const int nv = scan_width(B, H, dv);
@@ -1290,7 +1290,7 @@ cudaError_t launch_mlstm_dk(const void *q, const void *k, const void *v, const f
     scan<<<dim3(dv / nv, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
         static_cast<const uint8_t *>(ws), C0, static_cast<bf16 *>(h), C_T, H, T, dv, nblk,
         static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), static_cast<const bf16 *>(v),
-        tmq, tmk, tmv, nullptr, 0.f, row_scale);
+        tmq, tmk, tmv, nullptr, 0.f, 1);
     return cudaGetLastError();
 }
 
@@ -1351,7 +1351,7 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
     if (!norm) {
         scan<<<dim3(dv / nv, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
             static_cast<const uint8_t *>(ws), S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qs,
-            ks, static_cast<const bf16 *>(v), qk ? tmqn : tmq, qk ? tmkn : tmk, tmv, nullptr, 0.f, nullptr);
+            ks, static_cast<const bf16 *>(v), qk ? tmqn : tmq, qk ? tmkn : tmk, tmv, nullptr, 0.f, 0);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -1369,7 +1369,7 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
     return cudaLaunchKernelEx(&cfg, scan, static_cast<const uint8_t *>(ws), S0,
                               static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qs, ks,
                               static_cast<const bf16 *>(v), qk ? tmqn : tmq, qk ? tmkn : tmk, tmv,
-                              fz.norm_w, fz.norm_eps, static_cast<const float *>(nullptr));
+                              fz.norm_w, fz.norm_eps, 0);
 }
 
 template <int DK>
@@ -1435,19 +1435,29 @@ bool chunked_tc_applies_norm(lr_mode mode, int B, int H, int dv) {
 // Attribute slots 136..141 belong to the mLSTM launch.
 cudaError_t launch_mlstm_tc(const void *q, const void *k, const void *v, const float *fgate,
                             const float *igate, const float *m_prev, const float *C0, void *h,
-                            float *C_T, float *aux, const float *row_scale, int phase, int B,
-                            int H, int T, int dk, int dv, void *ws, cudaStream_t stream) {
+                            float *C_T, float *aux, int phase, int B, int H, int T, int dk,
+                            int dv, void *ws, cudaStream_t stream) {
     switch (dk) {
     case 32:
-        return launch_mlstm_dk<32>(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, row_scale,
-                                   phase, B, H, T, dv, ws, stream, 136);
+        return launch_mlstm_dk<32>(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, phase, B, H, T,
+                                   dv, ws, stream, 136);
     case 64:
-        return launch_mlstm_dk<64>(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, row_scale,
-                                   phase, B, H, T, dv, ws, stream, 138);
+        return launch_mlstm_dk<64>(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, phase, B, H, T,
+                                   dv, ws, stream, 138);
     default:
-        return launch_mlstm_dk<128>(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, row_scale,
-                                    phase, B, H, T, dv, ws, stream, 140);
+        return launch_mlstm_dk<128>(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, phase, B, H, T,
+                                    dv, ws, stream, 140);
     }
+}
+
+// Where the per-token factor of block j's output rows goes: the record of
+// stage j + 1, at this byte offset within it (vector slot kVrs), records of
+// this many bytes, nblk + 1 per (batch, head) from the start of the workspace.
+void mlstm_factor_slot(int dk, size_t *rec_bytes, size_t *offset) {
+    const int rb = dk == 32 ? Rec<32>::BYTES : dk == 64 ? Rec<64>::BYTES : Rec<128>::BYTES;
+    const int vo = dk == 32 ? Rec<32>::VEC : dk == 64 ? Rec<64>::VEC : Rec<128>::VEC;
+    *rec_bytes = (size_t)rb;
+    *offset = (size_t)vo + (size_t)kVrs * 4;
 }
 
 cudaError_t set_scan_fault_tc(unsigned on) {

@@ -238,7 +238,7 @@ chunk_prep_gd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ kw,
         const int s0 = qr >= 2 ? GH : 0;
         float x[16];
         tmem_ld16(tmem + ((uint32_t)(32 * qr) << 16) + (uint32_t)(32 * h + s0), x);
-        tmem_ld_wait();
+        tmem_ld_wait(x);
         const bool keyrow = qr & 1;
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -431,7 +431,7 @@ chunk_prep_gd_z_kernel(uint8_t *__restrict__ ws, const uint8_t *__restrict__ wgo
         for (int half = 0; half < 2; ++half) {
             float z[32];
             tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * half), z);
-            tmem_ld_wait();
+            tmem_ld_wait(z);
             if (lane < 16) {
 #pragma unroll
                 for (int i8 = 0; i8 < 4; ++i8)
@@ -482,7 +482,7 @@ cudaError_t launch_gd_dk(const void *q, const void *kw, const void *v, const flo
     }
     scan<<<dim3(dv / DVS, H, B), kScanThreads, ScanLayout<DK>::ALLOC, stream>>>(
         recs, S0, static_cast<bf16 *>(o), S_T, H, T, dv, nblk, qo, ko,
-        static_cast<const bf16 *>(v), tmq, tmk, tmv, nullptr, 0.f, nullptr);
+        static_cast<const bf16 *>(v), tmq, tmk, tmv, nullptr, 0.f, 0);
     return cudaGetLastError();
 }
 

@@ -138,12 +138,14 @@ cudaError_t launch_mlstm_step(const void *q, const void *k, const void *v, const
 // pass, records for the scan without delta (stage layout of lr_fwd_chunked)
 // plus, per block, the fp32 aux values [row sums 64][m_t 64][g'_t 64][g_C]
 // [Delta n dk] at `aux`; m_prev [B*H][nblk] is the stabiliser at every block
-// start.  phase 1: the scan, h = numerator times row_scale[b, h, t] (fp32,
-// [B*H][T]), C_T.
+// start.  phase 1: the scan, h = numerator times the token's factor, which the
+// caller has written into the records (mlstm_factor_slot), and C_T.
 cudaError_t launch_mlstm_tc(const void *q, const void *k, const void *v, const float *fgate,
                             const float *igate, const float *m_prev, const float *C0, void *h,
-                            float *C_T, float *aux, const float *row_scale, int phase, int B,
-                            int H, int T, int dk, int dv, void *ws, cudaStream_t stream);
+                            float *C_T, float *aux, int phase, int B, int H, int T, int dk, int dv,
+                            void *ws, cudaStream_t stream);
+// The record slot of the mLSTM's per-token factors (see launch_mlstm_tc).
+void mlstm_factor_slot(int dk, size_t *rec_bytes, size_t *offset);
 size_t records_bytes_tc(int B, int H, int T, int dk);
 // Whether launch_chunked_tc applies LR_FUSE_O_RMSNORM itself (in the scan) for
 // this mode and these sizes; otherwise the caller runs the norm pass after it.

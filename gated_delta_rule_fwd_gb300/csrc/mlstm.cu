@@ -30,7 +30,7 @@ constexpr int kMlstmAux = 384, kAuxRs = 0, kAuxM = 64, kAuxG = 128, kAuxGC = 192
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct MlstmWs {
-    size_t recs, mprev, aux, nst, rs, total;
+    size_t recs, mprev, aux, nst, total;
 };
 MlstmWs mlstm_ws(int B, int H, int T, int dk) {
     const size_t nblk = (size_t)((T + C - 1) / C), bh = (size_t)B * H;
@@ -39,8 +39,7 @@ MlstmWs mlstm_ws(int B, int H, int T, int dk) {
     w.mprev = align256(records_bytes_tc(B, H, T, dk));
     w.aux = align256(w.mprev + bh * nblk * 4);
     w.nst = align256(w.aux + bh * nblk * kMlstmAux * 4);
-    w.rs = align256(w.nst + bh * nblk * (size_t)dk * 4);
-    w.total = w.rs + bh * (size_t)T * 4;
+    w.total = w.nst + bh * nblk * (size_t)dk * 4;
     return w;
 }
 
@@ -115,7 +114,9 @@ mlstm_nscan_kernel(const float *__restrict__ aux, const float *__restrict__ n0,
 
 // One CTA of 4 warps per (block, b, h); a warp takes four tokens at a time:
 // den = g'_t (n~ . q_t) + row sum, and the token's factor
-// rs_t = 1 / max(|den|, e^{-m_t}).  Each lane holds d_k / 32 consecutive
+// 1 / max(|den|, e^{-m_t}), written into the vector of the stage record that
+// the scan reads with the block's output rows (record blk + 1, float slot
+// `slot` bytes in, records `rec_bytes` apart).  Each lane holds d_k / 32 consecutive
 // channels of q (one 2-, 4- or 8-byte access per row); the four tokens' loads
 // are independent.
 template <int N> struct Lanes;
@@ -140,7 +141,8 @@ __device__ __forceinline__ void unpack(uint2 w, float (&x)[4]) {
 template <int DK>
 __global__ void __launch_bounds__(128)
 mlstm_den_kernel(const __nv_bfloat16 *__restrict__ q, const float *__restrict__ aux,
-                 const float *__restrict__ nst, float *__restrict__ rs, int H, int T, int nblk) {
+                 const float *__restrict__ nst, uint8_t *__restrict__ recs, size_t rec_bytes,
+                 size_t slot, int H, int T, int nblk) {
     constexpr int EK = DK / 32, U = 4;
     using LK = typename Lanes<EK>::T;
     const int blk = blockIdx.x;
@@ -151,6 +153,7 @@ mlstm_den_kernel(const __nv_bfloat16 *__restrict__ q, const float *__restrict__ 
 #pragma unroll
     for (int e = 0; e < EK; ++e) nv[e] = nst[(bh * nblk + blk) * DK + EK * lane + e];
     const int t0 = blk * C, n = min(C, T - t0);
+    float *fac = reinterpret_cast<float *>(recs + (bh * (nblk + 1) + blk + 1) * rec_bytes + slot);
     const LK *qr = reinterpret_cast<const LK *>(q);
     for (int r0 = warp * U; r0 < n; r0 += 4 * U) {
         LK qw[U];
@@ -168,7 +171,7 @@ mlstm_den_kernel(const __nv_bfloat16 *__restrict__ q, const float *__restrict__ 
             for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
             if (r < n && lane == 0) {
                 const float den = a[kAuxG + r] * d + a[kAuxRs + r];
-                rs[bh * T + t0 + r] = 1.f / fmaxf(fabsf(den), __expf(-a[kAuxM + r]));
+                fac[r] = 1.f / fmaxf(fabsf(den), __expf(-a[kAuxM + r]));
             }
         }
     }
@@ -425,9 +428,8 @@ cudaError_t launch_mlstm_chunked(const void *q, const void *k, const void *v, co
     mlstm_stab_kernel<<<BH, kStabThreads, 0, stream>>>(fgate, igate, m0, m_prev, m_T, T, nblk);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    float *rs = reinterpret_cast<float *>(base + w.rs);
-    e = launch_mlstm_tc(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, nullptr, 0, B, H, T, dk,
-                        dv, ws, stream);
+    e = launch_mlstm_tc(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, 0, B, H, T, dk, dv, ws,
+                        stream);
     if (e != cudaSuccess) return e;
     switch (dk) {
     case 32: mlstm_nscan_kernel<32><<<BH, 32, 0, stream>>>(aux, n0, nst, n_T, nblk); break;
@@ -437,14 +439,16 @@ cudaError_t launch_mlstm_chunked(const void *q, const void *k, const void *v, co
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const dim3 grid(nblk, H, B);
     const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(q);
+    size_t rb = 0, slot = 0;
+    mlstm_factor_slot(dk, &rb, &slot);
     switch (dk) {
-    case 32: mlstm_den_kernel<32><<<grid, 128, 0, stream>>>(qb, aux, nst, rs, H, T, nblk); break;
-    case 64: mlstm_den_kernel<64><<<grid, 128, 0, stream>>>(qb, aux, nst, rs, H, T, nblk); break;
-    default: mlstm_den_kernel<128><<<grid, 128, 0, stream>>>(qb, aux, nst, rs, H, T, nblk); break;
+    case 32: mlstm_den_kernel<32><<<grid, 128, 0, stream>>>(qb, aux, nst, base, rb, slot, H, T, nblk); break;
+    case 64: mlstm_den_kernel<64><<<grid, 128, 0, stream>>>(qb, aux, nst, base, rb, slot, H, T, nblk); break;
+    default: mlstm_den_kernel<128><<<grid, 128, 0, stream>>>(qb, aux, nst, base, rb, slot, H, T, nblk); break;
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    return launch_mlstm_tc(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, rs, 1, B, H, T, dk, dv,
-                           ws, stream);
+    return launch_mlstm_tc(q, k, v, fgate, igate, m_prev, C0, h, C_T, aux, 1, B, H, T, dk, dv, ws,
+                           stream);
 }
 
 cudaError_t launch_mlstm_step(const void *q, const void *k, const void *v, const float *fgate,

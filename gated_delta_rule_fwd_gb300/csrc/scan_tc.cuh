@@ -45,6 +45,7 @@ struct Rec {
 };
 // offsets (in floats) inside the gate vector of a record
 constexpr int kVgPrev = 0, kVkdPrev = 64, kVkd = 128, kVgCPrev = 192;
+constexpr int kVrs = 128;  // without delta (kd unused): a factor per output row (mLSTM)
 constexpr int kVgCDiag = 128;  // diagonal gate: g_C' per key channel (128 floats)
 constexpr int kVgCGen = 0;     // generalised delta rule: g_C' per key channel (128 floats)
 
@@ -206,8 +207,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                   const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                   const bf16 *__restrict__ v, const __grid_constant__ CUtensorMap tmq,
                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                  const float *__restrict__ norm_w, float norm_eps,
-                  const float *__restrict__ row_scale) {
+                  const float *__restrict__ norm_w, float norm_eps, int row_scale) {
     using L = ScanLayout<DK>;
     using R = Rec<DK>;
     static_assert(!GEN || (DELTA && !DIAG), "the generalised delta rule runs the delta protocol");
@@ -460,11 +460,11 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                     tmem_ld16(tmem + lb + base + kDb, y);
                     if (j > 0) {
                         tmem_ld16(tmem + lb + base + kDc, z);
-                        tmem_ld_wait();
+                        tmem_ld_wait(x, y, z);
 #pragma unroll
                         for (int c = 0; c < 16; ++c) x[c] += gn * y[c] + z[c];
                     } else {
-                        tmem_ld_wait();
+                        tmem_ld_wait(x, y);
 #pragma unroll
                         for (int c = 0; c < 16; ++c) x[c] += gn * y[c];
                     }
@@ -532,15 +532,11 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
             const uint32_t ph = (j >> 1) & 1, base = p * kParCols;
             ok = __all_sync(0xffffffffu, wait(&bars->fullL[p], ph));
             if (!ok) break;
-            const float gr = GEN ? 1.f : vec_of(p)[kVgPrev + r];  // the only late-group value read here
+            // the late-group values read here: g' and, with row_scale, a factor
+            // per token (mLSTM: 1 / max(|denominator|, e^-m))
+            const float gr = GEN ? 1.f : vec_of(p)[kVgPrev + r];
+            const float rsc = (!DELTA && row_scale) ? vec_of(p)[kVrs + r] : 1.f;
             warp_arrive(&bars->emptyL[p]);
-            // a factor per token (mLSTM: 1 / max(|denominator|, e^-m)), fetched
-            // before the wait for the products
-            float rsc = 1.f;
-            if (row_scale != nullptr && j >= 1) {
-                const int t = (j - 1) * TS + r;
-                if (r < TS && t < T) rsc = __ldg(row_scale + bh * T + t);
-            }
             if (j >= 1) ok = __all_sync(0xffffffffu, wait(&bars->dA[p], ph));
             if (!ok) break;
             if (j >= 1) {
@@ -551,7 +547,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
                     float x[16], y[16];
                     tmem_ld16(tmem + lb + base + kDb + 16 * sub, x);
                     tmem_ld16(tmem + lb + base + kDc + 16 * sub, y);
-                    tmem_ld_wait();
+                    tmem_ld_wait(x, y);
 #pragma unroll
                     for (int c = 0; c < 16; ++c)  // (g' Q' S'^T + P' U') times the token's factor
                         out[16 * sub + c] = (gr * x[c] + y[c]) * rsc;
@@ -640,7 +636,7 @@ chunk_scan_kernel(const uint8_t *__restrict__ ws, const float *__restrict__ S0,
 #pragma unroll
                 for (int h = 0; h < SC / 16; ++h)
                     tmem_ld16(tmem + lb + base + kDS + 16 * h, *reinterpret_cast<float(*)[16]>(d + 16 * h));
-                tmem_ld_wait();
+                tmem_ld_wait(d);
                 tc_fence_before();
                 if (!DELTA) warp_arrive(&bars->emptyL[p]);
 #pragma unroll

@@ -145,8 +145,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
-__device__ __forceinline__ void tmem_ld_wait() {
+// Wait for this thread's tensor-memory loads, then pin every register they
+// wrote (the arrays passed) behind the wait: tcgen05.ld's outputs hold their
+// values only after tcgen05.wait::ld, but nothing in the load's own asm tells
+// the compiler so, and it may otherwise schedule a use of them above the
+// wait (seen as rows of the mLSTM output that changed from call to call).
+// Each array gets an empty asm with the values as in-out operands, ordered
+// after the wait like every volatile asm.
+template <int N>
+__device__ __forceinline__ void tmem_pin(float (&v)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]));
+}
+template <typename A, typename... R>
+__device__ __forceinline__ void tmem_ld_wait(A &a, R &...rest) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    tmem_pin(a);
+    (tmem_pin(rest), ...);
 }
 
 // ---------------------------------------------------- matrix descriptors
