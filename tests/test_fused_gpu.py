@@ -290,3 +290,26 @@ def test_step_fused_decode_workload_sampled(dev):
     es = rel_err(S[pn, ph].unsqueeze(1), s_ref)
     print(f"fused decode 20 steps, 64 sampled heads: rel err o={eo:.3e} S={es:.3e}")
     assert eo <= 2e-2 and es <= 2e-2
+
+
+def test_fused_folded_norm_repeated_calls_bit_identical(dev):
+    """The scan that applies the output norm (2-CTA clusters exchanging row sums
+    through distributed shared memory, on the Mamba-2 workload's 64-channel
+    CTAs): 30 calls on the same inputs give the same bits."""
+    w = workloads.WORKLOADS["mamba2_gate_bf16"]
+    flags = workloads.FUSED_FLAGS["mamba2"]
+    x = workloads.draw_pre("mamba2", w.B, w.H, w.T, w.dk, w.dv, w.seed, torch.bfloat16, w.s0_std)
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+
+    def call():
+        return lr.lr_fwd_chunked_fused(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["S0"],
+                                       mode=w.mode, flags=flags, alpha_scale=d["alpha_scale"],
+                                       norm_weight=d["norm_weight"])
+
+    o0, s0 = [t.clone() for t in call()]
+    bad = 0
+    for _ in range(30):
+        o, s = call()
+        bad += int(not (torch.equal(o, o0) and torch.equal(s, s0)))
+    torch.cuda.synchronize()
+    assert bad == 0, f"{bad} of 30 calls differ from the first"

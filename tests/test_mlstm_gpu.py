@@ -130,6 +130,24 @@ def test_mlstm_repeated_calls_bit_identical(dev):
     assert bad == 0, f"{bad} of 30 calls differ from the first"
 
 
+def test_mlstm_workload_repeated_calls_bit_identical(dev):
+    """The bench workload (B=8 H=16 T=4096, a given state, 64-channel scan CTAs):
+    40 calls on the same inputs give the same bits.  A form of the scan that
+    read the per-token factor from a global array inside its output loop
+    failed this in about one call in five."""
+    w = workloads.WORKLOADS["mlstm_bf16"]
+    x = to_dev(workloads.draw_mlstm(w.B, w.H, w.T, w.dk, w.dv, seed=w.seed, dtype=torch.bfloat16,
+                                    state=True), dev)
+    args = (x["q"], x["k"], x["v"], x["fgate"], x["igate"], x["C0"], x["n0"], x["m0"])
+    outs0 = [t.clone() for t in lr.lr_fwd_chunked_mlstm(*args)]
+    bad = 0
+    for _ in range(40):
+        outs = lr.lr_fwd_chunked_mlstm(*args)
+        bad += int(not all(torch.equal(a, b) for a, b in zip(outs, outs0)))
+    torch.cuda.synchronize()
+    assert bad == 0, f"{bad} of 40 calls differ from the first"
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 @pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 128)])
 @pytest.mark.parametrize("state", [True, False], ids=["state", "empty"])
