@@ -56,8 +56,8 @@ TRAFFIC_SOURCES = ("gated_delta_rule_fwd_gb300/csrc/chunked_tc.cu",
                    "gated_delta_rule_fwd_gb300/csrc/scan_tc.cuh",
                    "gated_delta_rule_fwd_gb300/csrc/tc_common.cuh")
 TRAFFIC = {
-    "gdn_prefill_bf16": {"bytes": 272.943104e6 + 289.676800e6 + 750.076416e6 + 118.955008e6,
-                         "sha256": "96f6ec319e3c8a46b2020143078cb79df508438c1d837ddd6138d023653c2379"},
+    "gdn_prefill_bf16": {"bytes": 272.943872e6 + 289.699840e6 + 750.234112e6 + 118.994944e6,
+                         "sha256": "a456f76a0985f07f94fc54c01f26c4b54327983fc53570317453cf7195160a6a"},
 }
 
 def kernel_source_sha256():
