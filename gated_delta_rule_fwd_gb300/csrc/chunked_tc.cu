@@ -1026,6 +1026,19 @@ chunk_prep_diag_kernel(const float *__restrict__ alpha, uint8_t *__restrict__ ws
 // g_C at 192, Delta n [<= 128] at 256 (the same constants are in mlstm.cu)
 constexpr int kMlstmAux = 384, kAuxRs = 0, kAuxM = 64, kAuxG = 128, kAuxGC = 192, kAuxDn = 256;
 
+// Shared memory of the mLSTM per-block pass: the [Q; K] tile, 384 floats of
+// scratch vectors, the barriers (35 KB at d_k = 128: six CTAs per SM; with
+// the 51 KB layout of the delta pass it ran four, and the call took 3 % longer).
+template <int DK>
+struct MlstmPrepLayout {
+    static constexpr int KB = (DK + 63) / 64;
+    static constexpr int QK = 0;
+    static constexpr int SV = QK + 128 * 128 * KB;
+    static constexpr int BAR = SV + 2048;
+    static constexpr int BYTES = BAR + 64;
+    static constexpr int ALLOC = BYTES + 1024;
+};
+
 template <int DK>
 __global__ void __launch_bounds__(NT)
 chunk_prep_mlstm_kernel(const float *__restrict__ fgate, const float *__restrict__ igate,
@@ -1033,7 +1046,7 @@ chunk_prep_mlstm_kernel(const float *__restrict__ fgate, const float *__restrict
                         float *__restrict__ aux_all, int H, int T, int nblk,
                         const __grid_constant__ CUtensorMap tmq,
                         const __grid_constant__ CUtensorMap tmk) {
-    using L = PrepLayout<DK>;
+    using L = MlstmPrepLayout<DK>;
     using R = Rec<DK>;
     extern __shared__ uint8_t sm_raw[];
     uint8_t *sm = align1024(sm_raw);
@@ -1047,7 +1060,7 @@ chunk_prep_mlstm_kernel(const float *__restrict__ fgate, const float *__restrict
     float *vn = reinterpret_cast<float *>(rec_next + R::VEC);
     float *aux = aux_all + (bh * nblk + blk) * kMlstmAux;
     uint8_t *QK = sm + L::QK;
-    float *Sv = reinterpret_cast<float *>(sm + L::AT);  // scratch vectors (the A region is unused)
+    float *Sv = reinterpret_cast<float *>(sm + L::SV);  // scratch vectors
     float *At = Sv, *Bs = Sv + 64, *kdv = Sv + 128, *red = Sv + 192;  // F_t - m_t, igate_s - F_s, kd_s
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 32);
@@ -1272,7 +1285,7 @@ cudaError_t launch_mlstm_dk(const void *q, const void *k, const void *v, const f
     const int nv = scan_width(B, H, dv);
     auto scan = nv == 64 ? chunk_scan_kernel<DK, true, false, false, false, 64>
                          : chunk_scan_kernel<DK, true, false>;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(prep), PrepLayout<DK>::ALLOC,
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(prep), MlstmPrepLayout<DK>::ALLOC,
                                      slot);
     if (e != cudaSuccess) return e;
     e = ensure_smem_attr(reinterpret_cast<const void *>(scan), ScanLayout<DK>::ALLOC,
@@ -1283,7 +1296,7 @@ cudaError_t launch_mlstm_dk(const void *q, const void *k, const void *v, const f
     if ((e = make_rows_map(&tmk, k, DK, T, B * H)) != cudaSuccess) return e;
     if ((e = make_rows_map(&tmv, v, dv, T, B * H)) != cudaSuccess) return e;
     if (phase == 0) {
-        prep<<<dim3(nblk, H, B), NT, PrepLayout<DK>::ALLOC, stream>>>(
+        prep<<<dim3(nblk, H, B), NT, MlstmPrepLayout<DK>::ALLOC, stream>>>(
             fgate, igate, m_prev, static_cast<uint8_t *>(ws), aux, H, T, nblk, tmq, tmk);
         return cudaGetLastError();
     }
